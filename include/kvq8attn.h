@@ -1,0 +1,137 @@
+/*
+ * kvq8attn.h -- C ABI of the Q8_0 GQA verify / prompt attention library (GB300, sm_103a).
+ *
+ * The operation: multi-row causal attention of fp32 (verify) or fp16 (prompt) query rows
+ * over a grouped-query KV cache stored in the Q8_0 format -- int8 codes plus one fp16
+ * scale per 32-value block.  Sources (titles and sections of the pages):
+ *   - "perf(gfx1100): share Q8 KV scans across verifier rows", Summary: one wave owns
+ *     four or eight Q8 attention query rows and shares each K/V scan across them; the
+ *     partials layout and reducer stay as they are; the route is limited to Q8 KV,
+ *     head_dim 128 or 256 and sequential (non-tree) windows of 4-32 rows.
+ *   - "gfx12 WMMA kernel for the int8-KV QSA prompt attention", How: int8-KV prompt
+ *     attention with online softmax and the V scale folded into p; the heads that
+ *     share one KV head fill the rows of the tensor-core tile.
+ *   - "Engine perf(hip): MTP draft, shared expert, verify/sampler head", Summary
+ *     item 4: the warp-per-block Q8_0 quantiser, bitwise equal to its CPU reference.
+ *
+ * Layout of the cache (all device memory, owned by the caller):
+ *   codes  int8   [n_kv_heads][capacity][head_dim]        one row of head_dim codes per token
+ *   scales uint16 [n_kv_heads][capacity][head_dim / 32]   fp16 bit patterns, one per 32-code block
+ * The dequantised value of element j of token n is codes[h][n][j] * fp16(scales[h][n][j/32]).
+ *
+ * Conventions shared by every entry point:
+ *   - Query head h reads KV head h / (n_q_heads / n_kv_heads).
+ *   - Query row i of a call sees keys n with n <= q_pos0 + i and n < kv_len.  A verify
+ *     window of T rows after ctx cached tokens uses q_pos0 = ctx, kv_len = ctx + T; a
+ *     prompt chunk of n_q rows ending the context uses q_pos0 = kv_len - n_q.
+ *   - All pointers are device pointers (cudaMalloc / torch), 16-byte aligned, caller-owned.
+ *     The library never allocates, frees or synchronises and keeps no state between
+ *     calls; work is enqueued on `stream` (NULL = the legacy default stream).
+ *   - Every call validates its arguments on the host first and, on any error, returns a
+ *     nonzero status and launches nothing ("fail closed": there is no fallback route).
+ *     A CUDA launch error is returned as KVQ8_ERR_CUDA.
+ */
+#ifndef KVQ8ATTN_H
+#define KVQ8ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st* kvq8_stream_t;
+
+enum kvq8_status {
+    KVQ8_OK = 0,
+    KVQ8_ERR_INVALID_ARG = 1,   /* null pointer, negative or inconsistent size          */
+    KVQ8_ERR_UNSUPPORTED = 2,   /* head_dim, group or row count outside what is built   */
+    KVQ8_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned                     */
+    KVQ8_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required           */
+    KVQ8_ERR_CUDA = 5           /* a CUDA call or kernel launch failed                  */
+};
+
+/* The caller's cache planes.  head_dim is 128 or 256; capacity >= kv_len of any call. */
+typedef struct {
+    const int8_t* k_codes;
+    const uint16_t* k_scales;
+    const int8_t* v_codes;
+    const uint16_t* v_scales;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int32_t capacity;
+} kvq8_cache;
+
+/*
+ * kvq8_quantize -- append n_tok tokens of K (or V) values to one plane pair.
+ *   x      : fp32 [n_tok][n_kv_heads][head_dim]
+ *   codes  : int8 plane [n_kv_heads][capacity][head_dim]; tokens land at [pos0, pos0 + n_tok)
+ *   scales : uint16 plane [n_kv_heads][capacity][head_dim / 32]
+ * Per 32-value block: amax = max |x|; d32 = amax / 127 (IEEE fp32 division); the stored
+ * scale is fp16(d32) rounded to nearest even; code = clamp(round-half-away-from-zero(x / d32),
+ * -127, 127) with an IEEE fp32 division; a block with d32 == 0 stores scale 0 and zero codes.
+ * Results are bit-exact with that definition.  Inputs must be finite; for amax > 65504 * 127
+ * the stored scale is +inf.  head_dim must be a multiple of 32.
+ * Source: "Engine perf(hip): ...", Summary item 4 (warp-per-block Q8_0 quantiser).
+ */
+int kvq8_quantize(const float* x, int n_tok, int n_kv_heads, int head_dim,
+                  int8_t* codes, uint16_t* scales, int capacity, int pos0, kvq8_stream_t stream);
+
+/* Bytes of workspace attn_verify_q8 needs for this shape (n_split 0 = the automatic choice). */
+size_t attn_verify_q8_workspace_bytes(int n_rows, int n_q_heads, int head_dim, int kv_len,
+                                      int n_kv_heads, int n_split);
+
+/*
+ * attn_verify_q8 -- speculative-decode verify attention over a Q8_0 cache.
+ *   q        : fp32 [n_rows][n_q_heads][head_dim], 1 <= n_rows <= 32
+ *   kv       : the cache (head_dim 128 or 256; n_q_heads / n_kv_heads integral, <= 16)
+ *   kv_len   : tokens of the cache to attend over; q_pos0: position of row 0 (see above)
+ *   out      : fp32 [n_rows][n_q_heads][head_dim], normalised attention output
+ *   workspace: device scratch of at least attn_verify_q8_workspace_bytes(...) bytes,
+ *              caller-owned; holds the split-context partials between the two kernels
+ *   n_split  : context slices per KV head (0 = automatic; otherwise 1..1024)
+ * One thread block per (KV head, context slice) reads each K/V block of its slice from
+ * HBM once for all n_rows x group query rows; the per-slice (o, m, l) partials are then
+ * merged by log-sum-exp.  fp32 result; q and p enter the tensor cores as fp16 hi + lo
+ * pairs, so the result stays within 1e-4 of the fp64 oracle (max |err| / max |out|).
+ * Source: "perf(gfx1100): share Q8 KV scans across verifier rows", Summary.
+ */
+int attn_verify_q8(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv, int kv_len,
+                   int q_pos0, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                   int n_split, kvq8_stream_t stream);
+
+/*
+ * attn_combine -- merge split-context partials (log-sum-exp reducer).
+ *   part_o  : fp32 [n_split][rows][head_dim]  unnormalised o_s = sum_n exp(s_n - m_s) v_n
+ *   part_ml : fp32 [n_split][rows][2]         (m_s, l_s): m_s = max s_n over the slice in natural-log
+ *             units (-inf for an empty slice), l_s = sum_n exp(s_n - m_s)
+ *   out     : fp32 [rows][head_dim] = sum_s o_s e^(m_s - m*) / sum_s l_s e^(m_s - m*), m* = max_s m_s;
+ *             a row whose every slice is empty is written as zeros
+ * head_dim is a multiple of 4, <= 1024; 1 <= n_split <= 4096.
+ * Source: "perf(gfx1100): share Q8 KV scans across verifier rows", Summary (partials + reducer).
+ */
+int attn_combine(const float* part_o, const float* part_ml, int n_split, int rows, int head_dim,
+                 float* out, kvq8_stream_t stream);
+
+/*
+ * attn_prompt_q8 -- prompt-chunk attention: many query rows over a long Q8_0 context.
+ *   q   : fp16 bits [n_q][n_q_heads][head_dim], head_dim 256
+ *   out : fp32 [n_q][n_q_heads][head_dim]
+ * K and V are dequantised to fp16 on chip and contracted on the tcgen05 tensor cores
+ * with fp32 accumulation (S and O in tensor memory); tiles above the causal diagonal are
+ * skipped.  Within 2e-3 of the fp64 oracle (max |err| / max |out|).
+ * Source: "gfx12 WMMA kernel for the int8-KV QSA prompt attention", How and Measurements.
+ */
+int attn_prompt_q8(const uint16_t* q, int n_q, int n_q_heads, const kvq8_cache* kv, int kv_len,
+                   int q_pos0, float softmax_scale, float* out, kvq8_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* kvq8_status_str(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ8ATTN_H */

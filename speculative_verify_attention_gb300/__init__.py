@@ -1,0 +1,13 @@
+"""GB300-native multi-row attention over a Q8_0 GQA KV cache.
+
+The compute lives in libkvq8attn.so (hand-written CUDA for sm_103a, C ABI in
+include/kvq8attn.h); this package is its thin Python binding plus the seeded workload
+generators used by the tests and the benchmark.
+"""
+from .binding import (EXPORTED, KVCacheQ8, KVQ8Error, attn_combine, attn_prompt_q8, attn_verify_q8,
+                      attn_verify_q8_workspace_bytes, kvq8_cache, kvq8_quantize, kvq8_status_str, library_path,
+                      load_library)
+
+__all__ = ["EXPORTED", "KVCacheQ8", "KVQ8Error", "attn_combine", "attn_prompt_q8", "attn_verify_q8",
+           "attn_verify_q8_workspace_bytes", "kvq8_cache", "kvq8_quantize", "kvq8_status_str", "library_path",
+           "load_library"]

@@ -1,0 +1,193 @@
+"""ctypes binding of libkvq8attn.so -- argument marshalling only.
+
+Every entry point mirrors the C ABI in include/kvq8attn.h under the same name.  Tensors
+are torch CUDA tensors; their data pointers and the current CUDA stream are passed
+through unchanged, and every step of the computation runs in the library's kernels.
+There is no fallback: a missing library raises, and a nonzero status raises
+KVQ8Error with the library's own message.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+KVQ8_OK = 0
+KVQ8_ERR_INVALID_ARG = 1
+KVQ8_ERR_UNSUPPORTED = 2
+KVQ8_ERR_MISALIGNED = 3
+KVQ8_ERR_WORKSPACE = 4
+KVQ8_ERR_CUDA = 5
+
+# Entry points declared in include/kvq8attn.h.
+EXPORTED = ("kvq8_quantize", "attn_verify_q8_workspace_bytes", "attn_verify_q8", "attn_combine",
+            "attn_prompt_q8", "kvq8_status_str")
+
+
+class KVQ8Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed with status {status}: {kvq8_status_str(status)}")
+
+
+class kvq8_cache(ctypes.Structure):
+    _fields_ = [("k_codes", ctypes.c_void_p), ("k_scales", ctypes.c_void_p),
+                ("v_codes", ctypes.c_void_p), ("v_scales", ctypes.c_void_p),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("capacity", ctypes.c_int32)]
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library():
+    """Load the in-tree library (built by ``build.build()``); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(path)
+        vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        cp = ctypes.POINTER(kvq8_cache)
+        lib.kvq8_quantize.argtypes = [vp, i32, i32, i32, vp, vp, i32, i32, vp]
+        lib.kvq8_quantize.restype = i32
+        lib.attn_verify_q8_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.attn_verify_q8_workspace_bytes.restype = sz
+        lib.attn_verify_q8.argtypes = [vp, i32, i32, cp, i32, i32, f32, vp, vp, sz, i32, vp]
+        lib.attn_verify_q8.restype = i32
+        lib.attn_combine.argtypes = [vp, vp, i32, i32, i32, vp, vp]
+        lib.attn_combine.restype = i32
+        lib.attn_prompt_q8.argtypes = [vp, i32, i32, cp, i32, i32, f32, vp, vp]
+        lib.attn_prompt_q8.restype = i32
+        lib.kvq8_status_str.argtypes = [i32]
+        lib.kvq8_status_str.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def kvq8_status_str(status: int) -> str:
+    return load_library().kvq8_status_str(int(status)).decode()
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _check(fn: str, status: int) -> None:
+    if status != KVQ8_OK:
+        raise KVQ8Error(fn, status)
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype) -> None:
+    if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor (got {t.dtype}, {t.device})")
+
+
+class KVCacheQ8:
+    """Caller-owned Q8_0 K/V planes on one device (the layout of include/kvq8attn.h):
+    codes int8 [n_kv_heads][capacity][head_dim], scales fp16 [n_kv_heads][capacity][head_dim/32]."""
+
+    def __init__(self, n_kv_heads: int, head_dim: int, capacity: int, device="cuda"):
+        self.n_kv_heads, self.head_dim, self.capacity = n_kv_heads, head_dim, capacity
+        nb = head_dim // 32
+        self.k_codes = torch.zeros((n_kv_heads, capacity, head_dim), dtype=torch.int8, device=device)
+        self.v_codes = torch.zeros((n_kv_heads, capacity, head_dim), dtype=torch.int8, device=device)
+        self.k_scales = torch.zeros((n_kv_heads, capacity, nb), dtype=torch.float16, device=device)
+        self.v_scales = torch.zeros((n_kv_heads, capacity, nb), dtype=torch.float16, device=device)
+
+    @classmethod
+    def from_planes(cls, k_codes, k_scales, v_codes, v_scales):
+        c = cls.__new__(cls)
+        c.n_kv_heads, c.capacity, c.head_dim = k_codes.shape
+        c.k_codes, c.k_scales, c.v_codes, c.v_scales = k_codes, k_scales, v_codes, v_scales
+        return c
+
+    def struct(self) -> kvq8_cache:
+        return kvq8_cache(self.k_codes.data_ptr(), self.k_scales.data_ptr(), self.v_codes.data_ptr(),
+                          self.v_scales.data_ptr(), self.n_kv_heads, self.head_dim, self.capacity)
+
+    def append(self, k: torch.Tensor, v: torch.Tensor, pos0: int, stream=None) -> None:
+        """Quantise K and V values [n_tok][n_kv_heads][head_dim] (fp32) into positions pos0.."""
+        kvq8_quantize(k, self.k_codes, self.k_scales, pos0, stream)
+        kvq8_quantize(v, self.v_codes, self.v_scales, pos0, stream)
+
+
+def kvq8_quantize(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, pos0: int, stream=None) -> None:
+    _need(x, "x", torch.float32)
+    _need(codes, "codes", torch.int8)
+    _need(scales, "scales", torch.float16)
+    n_tok, n_kv_heads, head_dim = x.shape
+    capacity = codes.shape[1]
+    st = load_library().kvq8_quantize(_ptr(x), n_tok, n_kv_heads, head_dim, _ptr(codes), _ptr(scales),
+                                      capacity, int(pos0), _stream(stream))
+    _check("kvq8_quantize", st)
+
+
+def attn_verify_q8_workspace_bytes(n_rows: int, n_q_heads: int, head_dim: int, kv_len: int, n_kv_heads: int,
+                                   n_split: int = 0) -> int:
+    return int(load_library().attn_verify_q8_workspace_bytes(n_rows, n_q_heads, head_dim, kv_len, n_kv_heads,
+                                                             n_split))
+
+
+def attn_verify_q8(q: torch.Tensor, cache: KVCacheQ8, kv_len: int, q_pos0: int, softmax_scale: float,
+                   out: torch.Tensor | None = None, workspace: torch.Tensor | None = None, n_split: int = 0,
+                   stream=None) -> torch.Tensor:
+    """Verify attention of fp32 q [T][Hq][hd] over the cache; returns fp32 [T][Hq][hd]."""
+    _need(q, "q", torch.float32)
+    n_rows, n_q_heads, head_dim = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.float32)
+    if workspace is None:
+        nbytes = attn_verify_q8_workspace_bytes(n_rows, n_q_heads, head_dim, kv_len, cache.n_kv_heads, n_split)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    st = load_library().attn_verify_q8(_ptr(q), n_rows, n_q_heads, ctypes.byref(cache.struct()), int(kv_len),
+                                       int(q_pos0), float(softmax_scale), _ptr(out), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), int(n_split), _stream(stream))
+    _check("attn_verify_q8", st)
+    return out
+
+
+def attn_combine(part_o: torch.Tensor, part_ml: torch.Tensor, out: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+    """Merge partials part_o [n_split][rows][hd], part_ml [n_split][rows][2] -> out [rows][hd] (fp32)."""
+    _need(part_o, "part_o", torch.float32)
+    _need(part_ml, "part_ml", torch.float32)
+    n_split, rows, head_dim = part_o.shape
+    if out is None:
+        out = torch.empty((rows, head_dim), dtype=torch.float32, device=part_o.device)
+    _need(out, "out", torch.float32)
+    st = load_library().attn_combine(_ptr(part_o), _ptr(part_ml), n_split, rows, head_dim, _ptr(out),
+                                     _stream(stream))
+    _check("attn_combine", st)
+    return out
+
+
+def attn_prompt_q8(q: torch.Tensor, cache: KVCacheQ8, kv_len: int, q_pos0: int, softmax_scale: float,
+                   out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Prompt-chunk attention of fp16 q [n_q][Hq][hd] over the cache; returns fp32 [n_q][Hq][hd]."""
+    _need(q, "q", torch.float16)
+    n_q, n_q_heads, head_dim = q.shape
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32)
+    st = load_library().attn_prompt_q8(_ptr(q), n_q, n_q_heads, ctypes.byref(cache.struct()), int(kv_len),
+                                       int(q_pos0), float(softmax_scale), _ptr(out), _stream(stream))
+    _check("attn_prompt_q8", st)
+    return out

@@ -1,0 +1,73 @@
+// common.cuh -- helpers shared by the kvq8attn kernels (sm_103a).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvq8attn.h"
+
+namespace kvq8 {
+
+constexpr int kQBlock = 32;          // values per Q8_0 block
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int launch_status() {
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? KVQ8_OK : KVQ8_ERR_CUDA;
+}
+
+// Two int8 codes -> two fp16 values, exactly.  The input word x holds the codes already
+// offset by +128 (sign bit flipped), so each is an unsigned byte u in [1, 255].  Placing u
+// in the low mantissa byte of the fp16 pattern 0x64uu gives 1024 + u exactly; subtracting
+// 1152 = 1024 + 128 leaves the signed code.  `sel` picks which two bytes of x are used.
+template <unsigned kSel>
+__device__ __forceinline__ uint32_t biased_bytes_to_half2(uint32_t x) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(0x64646464u), "n"(kSel));
+    const __half2 h = *reinterpret_cast<const __half2*>(&r);
+    const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480u));  // 1152.0
+    const __half2 v = __hsub2(h, bias);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Byte interleave of two words: result bytes = {a.b[i], b.b[i], a.b[j], b.b[j]}.
+template <unsigned kSel>
+__device__ __forceinline__ uint32_t prmt2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "n"(kSel));
+    return r;
+}
+
+// D += A * B, m16n8k16, fp16 inputs, fp32 accumulate (register fragments).
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte global -> shared copy; bytes past src_bytes (0 or 16) are zero-filled.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes));
+}
+// 8-byte global -> shared copy (L1-allocating form); bytes past src_bytes are zero-filled.
+__device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src, int src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+
+__device__ __forceinline__ float half_bits_to_float(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+
+}  // namespace kvq8

@@ -1,0 +1,86 @@
+// quantize.cu -- Q8_0 quantiser for KV-cache appends (kvq8_quantize).
+//
+// Source: "Engine perf(hip): MTP draft, shared expert, verify/sampler head", Summary item 4:
+// a warp-per-block quantiser that reduces max|x| over the 32-value block with shuffles
+// and writes the fp16 scale and 32 int8 codes, bitwise equal to its CPU reference.
+//
+// Here a warp covers four blocks: eight lanes per block, four values per lane (one
+// 16-byte load), a 3-step shuffle max, then per value an IEEE fp32 division and round
+// half away from zero.  Bandwidth-bound: 4 bytes read, 1 + 1/16 bytes written per value.
+#include "common.cuh"
+
+namespace kvq8 {
+namespace {
+
+__global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4* __restrict__ x, int64_t n_blocks,
+                                                            int n_kv_heads, int nb_per_head_row,
+                                                            int8_t* __restrict__ codes,
+                                                            uint16_t* __restrict__ scales, int capacity,
+                                                            int pos0) {
+    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t blk = gid >> 3;  // Q8_0 block handled by this lane's group of 8
+    const int sub = threadIdx.x & 7;
+    const bool live = blk < n_blocks;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (live) v = __ldg(x + blk * 8 + sub);
+    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (!live) return;
+
+    const float d32 = __fdiv_rn(amax, 127.0f);
+    int8_t q[4];
+    const float xs[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        float r = 0.0f;
+        if (d32 != 0.0f) r = fminf(fmaxf(roundf(__fdiv_rn(xs[e], d32)), -127.0f), 127.0f);
+        q[e] = (int8_t)(int)r;
+    }
+    // block index -> (token, kv head, block within the head row)
+    const int64_t row_blocks = (int64_t)n_kv_heads * nb_per_head_row;
+    const int64_t tok = blk / row_blocks;
+    const int64_t rem = blk - tok * row_blocks;
+    const int h = (int)(rem / nb_per_head_row);
+    const int b = (int)(rem - (int64_t)h * nb_per_head_row);
+    const int64_t row = (int64_t)h * capacity + pos0 + tok;
+    uint32_t packed = (uint32_t)(uint8_t)q[0] | ((uint32_t)(uint8_t)q[1] << 8) | ((uint32_t)(uint8_t)q[2] << 16) |
+                      ((uint32_t)(uint8_t)q[3] << 24);
+    int8_t* dst = codes + row * (int64_t)nb_per_head_row * kQBlock + b * kQBlock + sub * 4;
+    *reinterpret_cast<uint32_t*>(dst) = packed;
+    if (sub == 0) scales[row * nb_per_head_row + b] = __half_as_ushort(__float2half_rn(d32));
+}
+
+}  // namespace
+}  // namespace kvq8
+
+extern "C" int kvq8_quantize(const float* x, int n_tok, int n_kv_heads, int head_dim, int8_t* codes,
+                             uint16_t* scales, int capacity, int pos0, kvq8_stream_t stream) {
+    using namespace kvq8;
+    if (n_tok < 0 || n_kv_heads <= 0 || head_dim <= 0 || capacity <= 0 || pos0 < 0) return KVQ8_ERR_INVALID_ARG;
+    if (head_dim % kQBlock) return KVQ8_ERR_UNSUPPORTED;
+    if ((int64_t)pos0 + n_tok > capacity) return KVQ8_ERR_INVALID_ARG;
+    if (n_tok == 0) return KVQ8_OK;
+    if (!x || !codes || !scales) return KVQ8_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(codes) || !aligned16(scales)) return KVQ8_ERR_MISALIGNED;
+    const int nb = head_dim / kQBlock;
+    const int64_t n_blocks = (int64_t)n_tok * n_kv_heads * nb;
+    const int64_t threads = n_blocks * 8;
+    const int64_t grid = (threads + 255) / 256;
+    if (grid > 0x7fffffffLL) return KVQ8_ERR_UNSUPPORTED;
+    quantize_q8_0_kernel<<<(unsigned)grid, 256, 0, (cudaStream_t)stream>>>(
+        reinterpret_cast<const float4*>(x), n_blocks, n_kv_heads, nb, codes, scales, capacity, pos0);
+    return launch_status();
+}
+
+extern "C" const char* kvq8_status_str(int status) {
+    switch (status) {
+        case KVQ8_OK: return "ok";
+        case KVQ8_ERR_INVALID_ARG: return "invalid argument";
+        case KVQ8_ERR_UNSUPPORTED: return "unsupported shape";
+        case KVQ8_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case KVQ8_ERR_WORKSPACE: return "workspace missing or too small";
+        case KVQ8_ERR_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}

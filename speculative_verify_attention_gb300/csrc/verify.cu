@@ -1,0 +1,615 @@
+// verify.cu -- split-context multi-row verify attention over a Q8_0 GQA cache (attn_verify_q8).
+//
+// Source: "perf(gfx1100): share Q8 KV scans across verifier rows", Summary: one worker owns
+// all the query rows of a verify window and shares each K/V scan across them; the context
+// is split into slices whose partials are merged by a reducer.  "gfx12 WMMA kernel for the
+// int8-KV QSA prompt attention", How: fp16 hi + lo split of q and p with fp32 accumulation,
+// online softmax, V scale folded into p.
+//
+// GB300 design (one thread block of 4 warps per (row chunk, context slice, KV head)):
+//   * K/V codes and scales of a 128-key tile are staged in shared memory with 16-byte
+//     cp.async copies into an XOR-swizzled layout (conflict-free fragment reads).  K of the
+//     next tile streams in while the softmax and PV of this tile run, and V while QK runs,
+//     so every K/V byte of the slice crosses HBM once for all T x group rows.
+//   * QK runs transposed on the tensor cores (m16n8k16, fp32 accumulate): keys are the M
+//     dimension (16 per fragment) and query rows the N dimension (8 per fragment), so a
+//     window of 4 rows x group 6 = 24 rows needs no padding.  int8 codes become fp16
+//     exactly in registers (byte permute + magic-bias subtract); q enters as fp16 hi + lo,
+//     both accumulated into the same fragment; the K scale, which varies along the
+//     contraction in 32-value blocks, is applied after each 32-deep step: s += dK * (q.k)_b.
+//   * Online softmax in base 2 (q pre-scaled by softmax_scale * log2 e), one cross-warp
+//     max per tile.
+//   * PV runs transposed too (M = 16 output dims, N = 8 rows, K = 16 keys).  Each warp owns
+//     32-dim output blocks; its B fragments are w = p * dV[n][block] * 2^E split into fp16
+//     hi + lo, with E a per-warp power of two that keeps w inside the fp16 normal range
+//     (the accumulator is rescaled when E changes, and divided by 2^E at the end).
+//   * Each slice writes an unnormalised partial (o, m, l); attn_combine merges them.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace kvq8 {
+
+int launch_combine(const float* part_o, const float* part_ml, int n_split, int rows, int head_dim, float* out,
+                   cudaStream_t stream);
+
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kKT = 128;  // keys per tile
+constexpr int kMaxNT = 4;  // n8 row tiles per chunk (<= 32 rows per thread block)
+
+struct VerifyParams {
+    const float* q;
+    const int8_t* k_codes;
+    const uint16_t* k_scales;
+    const int8_t* v_codes;
+    const uint16_t* v_scales;
+    float* part_o;     // [n_split][rows_total][HD]
+    float2* part_ml;   // [n_split][rows_total]
+    int n_rows;        // T
+    int n_q_heads;
+    int group;
+    int capacity;
+    int kv_len;
+    int q_pos0;
+    int keys_per_split;
+    int rows_per_chunk;  // real rows per chunk (<= 8 * NT)
+    float qscale;        // softmax_scale * log2(e)
+};
+
+template <int HD, int NT>
+struct Smem {
+    static constexpr int NB = HD / 32;      // scale blocks per token
+    static constexpr int RP = 8 * NT;       // padded rows per chunk
+    static constexpr int kK = 0;
+    static constexpr int kKs = kK + kKT * HD;
+    static constexpr int kV = kKs + kKT * NB * 2;
+    static constexpr int kVs = kV + kKT * HD;
+    static constexpr int kQ = kVs + kKT * NB * 2;
+    static constexpr int kP = kQ + NB * NT * 1024;
+    static constexpr int kRedMax = kP + kKT * RP * 4;
+    static constexpr int kRedSum = kRedMax + kWarps * RP * 4;
+    static constexpr int kAlpha = kRedSum + kWarps * RP * 4;
+    static constexpr int kBytes = kAlpha + RP * 4;
+};
+
+// Byte offset of code byte c of tile row n in the swizzled layout (16-byte chunks XOR row%8).
+template <int HD>
+__device__ __forceinline__ int swz(int n, int c) {
+    return n * HD + ((((c >> 4) ^ (n & 7)) << 4) | (c & 15));
+}
+
+template <int HD>
+__device__ __forceinline__ void load_codes(uint8_t* smem, const int8_t* plane, int64_t head_row0, int tile_key0,
+                                           int key_end) {
+    constexpr int CPR = HD / 16;  // 16-byte chunks per row
+    const uint32_t base = smem_u32(smem);
+#pragma unroll 4
+    for (int ci = threadIdx.x; ci < kKT * CPR; ci += kThreads) {
+        const int n = ci / CPR, c16 = ci % CPR;
+        const int key = tile_key0 + n;
+        const bool ok = key < key_end;
+        const int8_t* src = plane + (head_row0 + (ok ? key : tile_key0)) * HD + c16 * 16;
+        cp_async_16(base + n * HD + ((c16 ^ (n & 7)) << 4), src, ok ? 16 : 0);
+    }
+}
+
+// Scales of one tile: HD/16 bytes per token (16 at hd256, 8 at hd128), copied in
+// per-token pieces so that no alignment beyond the token's own is assumed.
+template <int HD>
+__device__ __forceinline__ void load_scales(uint8_t* smem, const uint16_t* plane, int64_t head_row0, int tile_key0,
+                                            int key_end) {
+    constexpr int SB = HD / 16;
+    const uint32_t base = smem_u32(smem);
+    const uint16_t* src0 = plane + (head_row0 + tile_key0) * (HD / 32);
+    for (int n = threadIdx.x; n < kKT; n += kThreads) {
+        const bool ok = tile_key0 + n < key_end;
+        const uint16_t* src = ok ? src0 + n * (HD / 32) : src0;
+        if constexpr (SB == 16)
+            cp_async_16(base + n * SB, src, ok ? 16 : 0);
+        else
+            cp_async_8(base + n * SB, src, ok ? 8 : 0);
+    }
+}
+
+template <int HD, int NT>
+__global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyParams p) {
+    using L = Smem<HD, NT>;
+    constexpr int NB = L::NB, RP = L::RP;
+    constexpr int BPW = NB / kWarps;  // 32-dim output blocks per warp in PV
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t* sK = smem + L::kK;
+    const uint16_t* sKs = reinterpret_cast<const uint16_t*>(smem + L::kKs);
+    uint8_t* sV = smem + L::kV;
+    const uint16_t* sVs = reinterpret_cast<const uint16_t*>(smem + L::kVs);
+    __half* sQ = reinterpret_cast<__half*>(smem + L::kQ);
+    float* sP = reinterpret_cast<float*>(smem + L::kP);
+    float* sRedMax = reinterpret_cast<float*>(smem + L::kRedMax);
+    float* sRedSum = reinterpret_cast<float*>(smem + L::kRedSum);
+    float* sAlpha = reinterpret_cast<float*>(smem + L::kAlpha);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int chunk = blockIdx.x, split = blockIdx.y, kvh = blockIdx.z;
+    const int R = p.n_rows * p.group;
+    const int rows_total = p.n_rows * p.n_q_heads;
+    const int row0 = chunk * p.rows_per_chunk;
+    const int rows_here = min(p.rows_per_chunk, R - row0);
+    const int key_begin = split * p.keys_per_split;
+    const int key_end = min(key_begin + p.keys_per_split, p.kv_len);
+    const int64_t head_row0 = (int64_t)kvh * p.capacity;
+
+    // Stage q rows of this chunk as fp16 hi/lo in mma B-fragment order:
+    // entry (block b, n-tile nt, hi|lo, lane g*4+t) holds row 8nt+g, dims 32b+8t .. +7.
+    for (int idx = threadIdx.x; idx < RP * HD; idx += kThreads) {
+        const int r = idx / HD, j = idx - r * HD;
+        float v = 0.0f;
+        if (r < rows_here) {
+            const int rr = row0 + r;
+            const int i = rr / p.group, hh = rr - i * p.group;
+            v = __ldg(p.q + ((int64_t)i * p.n_q_heads + kvh * p.group + hh) * HD + j) * p.qscale;
+        }
+        const __half hi = __float2half_rn(v);
+        const __half lo = __float2half_rn(v - __half2float(hi));
+        const int b = j >> 5, tt = (j >> 3) & 3, e = j & 7, nt = r >> 3, gg = r & 7;
+        const int base = ((b * NT + nt) * 2) * 256 + (gg * 4 + tt) * 8 + e;
+        sQ[base] = hi;
+        sQ[base + 256] = lo;
+    }
+
+    // Visibility bound per owned row: row rr sees keys < vis_end.
+    int vis_end[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int r = 8 * nt + 2 * t + c;
+            if (r < rows_here) {
+                const int i = (row0 + r) / p.group;
+                vis_end[nt][c] = min(min(p.q_pos0 + i + 1, p.kv_len), key_end);
+            } else {
+                vis_end[nt][c] = 0;
+            }
+        }
+
+    float m_run[NT][2], l_run[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            m_run[nt][c] = -INFINITY;
+            l_run[nt][c] = 0.0f;
+        }
+    float O[BPW][2][NT][4];
+#pragma unroll
+    for (int i = 0; i < BPW; ++i)
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) O[i][mt][nt][c] = 0.0f;
+    int E[BPW];
+#pragma unroll
+    for (int i = 0; i < BPW; ++i) E[i] = INT32_MIN;  // unset
+
+    if (key_begin < key_end) {
+        load_codes<HD>(sK, p.k_codes, head_row0, key_begin, key_end);
+        load_scales<HD>(smem + L::kKs, p.k_scales, head_row0, key_begin, key_end);
+        cp_async_commit();
+        load_codes<HD>(sV, p.v_codes, head_row0, key_begin, key_end);
+        load_scales<HD>(smem + L::kVs, p.v_scales, head_row0, key_begin, key_end);
+        cp_async_commit();
+    }
+
+    for (int tile0 = key_begin; tile0 < key_end; tile0 += kKT) {
+        cp_async_wait<1>();  // K of this tile landed (V may still be in flight)
+        __syncthreads();
+
+        // ---------------- QK^T: S^T[key][row] for this warp's 32 keys ----------------
+        float S[2][NT][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) S[mt][nt][c] = 0.0f;
+
+#pragma unroll 2
+        for (int b = 0; b < NB; ++b) {
+            uint4 qh[NT], ql[NT];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const uint4* qp = reinterpret_cast<const uint4*>(sQ + ((b * NT + nt) * 2) * 256) + lane;
+                qh[nt] = qp[0];
+                ql[nt] = qp[32];
+            }
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                const int n0 = warp * 32 + mt * 16 + g;
+                const uint2 k0 = *reinterpret_cast<const uint2*>(sK + swz<HD>(n0, 32 * b + 8 * t));
+                const uint2 k1 = *reinterpret_cast<const uint2*>(sK + swz<HD>(n0 + 8, 32 * b + 8 * t));
+                const uint32_t x0 = k0.x ^ 0x80808080u, x1 = k1.x ^ 0x80808080u;
+                const uint32_t y0 = k0.y ^ 0x80808080u, y1 = k1.y ^ 0x80808080u;
+                const uint32_t a00 = biased_bytes_to_half2<0x4140>(x0), a01 = biased_bytes_to_half2<0x4140>(x1);
+                const uint32_t a02 = biased_bytes_to_half2<0x4342>(x0), a03 = biased_bytes_to_half2<0x4342>(x1);
+                const uint32_t a10 = biased_bytes_to_half2<0x4140>(y0), a11 = biased_bytes_to_half2<0x4140>(y1);
+                const uint32_t a12 = biased_bytes_to_half2<0x4342>(y0), a13 = biased_bytes_to_half2<0x4342>(y1);
+                float tmp[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    tmp[nt][0] = tmp[nt][1] = tmp[nt][2] = tmp[nt][3] = 0.0f;
+                    mma_f16_16816(tmp[nt], a00, a01, a02, a03, qh[nt].x, qh[nt].y);
+                    mma_f16_16816(tmp[nt], a10, a11, a12, a13, qh[nt].z, qh[nt].w);
+                    mma_f16_16816(tmp[nt], a00, a01, a02, a03, ql[nt].x, ql[nt].y);
+                    mma_f16_16816(tmp[nt], a10, a11, a12, a13, ql[nt].z, ql[nt].w);
+                }
+                const float dk0 = half_bits_to_float(sKs[n0 * NB + b]);
+                const float dk1 = half_bits_to_float(sKs[(n0 + 8) * NB + b]);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    S[mt][nt][0] = fmaf(dk0, tmp[nt][0], S[mt][nt][0]);
+                    S[mt][nt][1] = fmaf(dk0, tmp[nt][1], S[mt][nt][1]);
+                    S[mt][nt][2] = fmaf(dk1, tmp[nt][2], S[mt][nt][2]);
+                    S[mt][nt][3] = fmaf(dk1, tmp[nt][3], S[mt][nt][3]);
+                }
+            }
+        }
+
+        // ---------------- mask + per-warp row max ----------------
+        float mx[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float m = -INFINITY;
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int key = tile0 + warp * 32 + mt * 16 + g + 8 * h;
+                        float& s = S[mt][nt][2 * h + c];
+                        if (key >= vis_end[nt][c]) s = -INFINITY;
+                        m = fmaxf(m, s);
+                    }
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                mx[nt][c] = m;
+                if (g == 0) sRedMax[warp * RP + 8 * nt + 2 * t + c] = m;
+            }
+        __syncthreads();  // all warps done reading sK; row maxima visible
+
+        {  // stream the next tile's K while softmax and PV run
+            const int next0 = tile0 + kKT;
+            if (next0 < key_end) {
+                load_codes<HD>(sK, p.k_codes, head_row0, next0, key_end);
+                load_scales<HD>(smem + L::kKs, p.k_scales, head_row0, next0, key_end);
+            }
+            cp_async_commit();
+        }
+
+        // ---------------- softmax: p = 2^(s - m_new) ----------------
+        float alpha[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int r = 8 * nt + 2 * t + c;
+                float mt_ = sRedMax[r];
+#pragma unroll
+                for (int w = 1; w < kWarps; ++w) mt_ = fmaxf(mt_, sRedMax[w * RP + r]);
+                const float m_new = fmaxf(m_run[nt][c], mt_);
+                float a = 1.0f, sum = 0.0f;
+                if (m_new != -INFINITY) {
+                    a = exp2f(m_run[nt][c] - m_new);
+#pragma unroll
+                    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            float& s = S[mt][nt][2 * h + c];
+                            s = exp2f(s - m_new);
+                            sum += s;
+                        }
+                } else {
+#pragma unroll
+                    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) S[mt][nt][2 * h + c] = 0.0f;
+                }
+                m_run[nt][c] = m_new;
+                alpha[nt][c] = a;
+                sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+                if (g == 0) {
+                    sRedSum[warp * RP + r] = sum;
+                    if (warp == 0) sAlpha[r] = a;
+                }
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int kl = warp * 32 + mt * 16 + g + 8 * h;
+                        sP[((kl >> 1) * RP + r) * 2 + (kl & 1)] = S[mt][nt][2 * h + c];
+                    }
+            }
+        (void)mx;
+
+        cp_async_wait<1>();  // V of this tile landed (next K may still be in flight)
+        __syncthreads();
+
+        if (warp == 0) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int r = 8 * nt + 2 * t + c;
+                    float s = 0.0f;
+#pragma unroll
+                    for (int w = 0; w < kWarps; ++w) s += sRedSum[w * RP + r];
+                    l_run[nt][c] = l_run[nt][c] * alpha[nt][c] + s;
+                }
+        }
+
+        // ---------------- PV: O^T[dim][row] += V^T * (p dV 2^E) ----------------
+#pragma unroll
+        for (int i = 0; i < BPW; ++i) {
+            const int b = warp + kWarps * i;
+            // per-warp exponent keeping w = p dV 2^E below 2^14
+            float dmax = 0.0f;
+#pragma unroll
+            for (int k = 0; k < kKT / 32; ++k) dmax = fmaxf(dmax, half_bits_to_float(sVs[(lane + 32 * k) * NB + b]));
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, o));
+            if (dmax > 0.0f) {
+                int e2;
+                (void)frexpf(dmax, &e2);
+                const int et = 14 - e2;
+                if (E[i] == INT32_MIN) {
+                    E[i] = et;
+                } else if (et < E[i]) {
+                    const float f = ldexpf(1.0f, et - E[i]);
+#pragma unroll
+                    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) O[i][mt][nt][c] *= f;
+                    E[i] = et;
+                }
+            }
+            const float esc = (E[i] == INT32_MIN) ? 0.0f : ldexpf(1.0f, E[i]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const float a0 = sAlpha[8 * nt + 2 * t], a1 = sAlpha[8 * nt + 2 * t + 1];
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    O[i][mt][nt][0] *= a0;
+                    O[i][mt][nt][1] *= a1;
+                    O[i][mt][nt][2] *= a0;
+                    O[i][mt][nt][3] *= a1;
+                }
+            }
+#pragma unroll 2
+            for (int ks = 0; ks < kKT / 16; ++ks) {
+                const int kb = ks * 16;
+                const int cb = 32 * b + 4 * g;
+                const uint32_t w0 = *reinterpret_cast<const uint32_t*>(sV + swz<HD>(kb + 2 * t, cb)) ^ 0x80808080u;
+                const uint32_t w1 = *reinterpret_cast<const uint32_t*>(sV + swz<HD>(kb + 2 * t + 1, cb)) ^ 0x80808080u;
+                const uint32_t w8 = *reinterpret_cast<const uint32_t*>(sV + swz<HD>(kb + 2 * t + 8, cb)) ^ 0x80808080u;
+                const uint32_t w9 = *reinterpret_cast<const uint32_t*>(sV + swz<HD>(kb + 2 * t + 9, cb)) ^ 0x80808080u;
+                const uint32_t y01lo = prmt2<0x5140>(w0, w1), y01hi = prmt2<0x7362>(w0, w1);
+                const uint32_t y89lo = prmt2<0x5140>(w8, w9), y89hi = prmt2<0x7362>(w8, w9);
+                uint32_t A[2][4];
+                A[0][0] = biased_bytes_to_half2<0x4140>(y01lo);
+                A[0][1] = biased_bytes_to_half2<0x4342>(y01lo);
+                A[0][2] = biased_bytes_to_half2<0x4140>(y89lo);
+                A[0][3] = biased_bytes_to_half2<0x4342>(y89lo);
+                A[1][0] = biased_bytes_to_half2<0x4140>(y01hi);
+                A[1][1] = biased_bytes_to_half2<0x4342>(y01hi);
+                A[1][2] = biased_bytes_to_half2<0x4140>(y89hi);
+                A[1][3] = biased_bytes_to_half2<0x4342>(y89hi);
+                const float ds0 = half_bits_to_float(sVs[(kb + 2 * t) * NB + b]) * esc;
+                const float ds1 = half_bits_to_float(sVs[(kb + 2 * t + 1) * NB + b]) * esc;
+                const float ds8 = half_bits_to_float(sVs[(kb + 2 * t + 8) * NB + b]) * esc;
+                const float ds9 = half_bits_to_float(sVs[(kb + 2 * t + 9) * NB + b]) * esc;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float2 p01 = *reinterpret_cast<const float2*>(sP + (((kb >> 1) + t) * RP + 8 * nt + g) * 2);
+                    const float2 p89 =
+                        *reinterpret_cast<const float2*>(sP + (((kb >> 1) + t + 4) * RP + 8 * nt + g) * 2);
+                    const float w00 = p01.x * ds0, w01 = p01.y * ds1, w10 = p89.x * ds8, w11 = p89.y * ds9;
+                    const __half2 h0 = __floats2half2_rn(w00, w01);
+                    const __half2 h1 = __floats2half2_rn(w10, w11);
+                    const __half2 l0 = __floats2half2_rn(w00 - __low2float(h0), w01 - __high2float(h0));
+                    const __half2 l1 = __floats2half2_rn(w10 - __low2float(h1), w11 - __high2float(h1));
+                    const uint32_t bh0 = *reinterpret_cast<const uint32_t*>(&h0);
+                    const uint32_t bh1 = *reinterpret_cast<const uint32_t*>(&h1);
+                    const uint32_t bl0 = *reinterpret_cast<const uint32_t*>(&l0);
+                    const uint32_t bl1 = *reinterpret_cast<const uint32_t*>(&l1);
+#pragma unroll
+                    for (int mt = 0; mt < 2; ++mt) {
+                        mma_f16_16816(O[i][mt][nt], A[mt][0], A[mt][1], A[mt][2], A[mt][3], bh0, bh1);
+                        mma_f16_16816(O[i][mt][nt], A[mt][0], A[mt][1], A[mt][2], A[mt][3], bl0, bl1);
+                    }
+                }
+            }
+        }
+        __syncthreads();  // all warps done with sV and sP
+
+        {  // stream the next tile's V while the next QK runs
+            const int next0 = tile0 + kKT;
+            if (next0 < key_end) {
+                load_codes<HD>(sV, p.v_codes, head_row0, next0, key_end);
+                load_scales<HD>(smem + L::kVs, p.v_scales, head_row0, next0, key_end);
+            }
+            cp_async_commit();
+        }
+    }
+    cp_async_wait<0>();
+
+    // ---------------- write the slice partial ----------------
+    float* po = p.part_o + (int64_t)split * rows_total * HD;
+#pragma unroll
+    for (int i = 0; i < BPW; ++i) {
+        const int b = warp + kWarps * i;
+        const float inv = (E[i] == INT32_MIN) ? 1.0f : ldexpf(1.0f, -E[i]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int r = 8 * nt + 2 * t + c;
+                if (r >= rows_here) continue;
+                const int rr = row0 + r;
+                const int iq = rr / p.group, hh = rr - iq * p.group;
+                const int64_t grow = (int64_t)iq * p.n_q_heads + kvh * p.group + hh;
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    const int j0 = 32 * b + 4 * g + 2 * mt;
+                    float2 v;
+                    v.x = O[i][mt][nt][c] * inv;      // (dim j0, row r)
+                    v.y = O[i][mt][nt][2 + c] * inv;  // (dim j0 + 1, row r)
+                    *reinterpret_cast<float2*>(po + grow * HD + j0) = v;
+                }
+            }
+    }
+    if (warp == 0 && g == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int r = 8 * nt + 2 * t + c;
+                if (r >= rows_here) continue;
+                const int rr = row0 + r;
+                const int iq = rr / p.group, hh = rr - iq * p.group;
+                const int64_t grow = (int64_t)iq * p.n_q_heads + kvh * p.group + hh;
+                const float m = m_run[nt][c];
+                p.part_ml[(int64_t)split * rows_total + grow] =
+                    make_float2(m == -INFINITY ? -INFINITY : m * kLn2, l_run[nt][c]);
+            }
+    }
+}
+
+struct Plan {
+    int hd, nt, n_chunks, rows_per_chunk, n_split, keys_per_split;
+    size_t ws_bytes;
+};
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+int make_plan(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_kv_heads, int n_split_req, Plan* pl) {
+    if (n_rows < 1 || n_rows > 32 || n_q_heads < 1 || n_kv_heads < 1 || kv_len < 1) return KVQ8_ERR_INVALID_ARG;
+    if (n_q_heads % n_kv_heads) return KVQ8_ERR_UNSUPPORTED;
+    const int group = n_q_heads / n_kv_heads;
+    if (group > 64) return KVQ8_ERR_UNSUPPORTED;
+    if (head_dim != 128 && head_dim != 256) return KVQ8_ERR_UNSUPPORTED;
+    if (n_split_req < 0 || n_split_req > 1024) return KVQ8_ERR_INVALID_ARG;
+    const int R = n_rows * group;
+    pl->hd = head_dim;
+    pl->n_chunks = (R + 8 * kMaxNT - 1) / (8 * kMaxNT);
+    pl->rows_per_chunk = (R + pl->n_chunks - 1) / pl->n_chunks;
+    pl->nt = (pl->rows_per_chunk + 7) / 8;
+    const int n_tiles = (kv_len + kKT - 1) / kKT;
+    int ns = n_split_req;
+    if (ns == 0) {
+        int sms = sm_count();
+        if (sms <= 0) sms = 152;
+        ns = std::max(1, (2 * sms) / (n_kv_heads * pl->n_chunks));
+    }
+    ns = std::min(ns, n_tiles);
+    const int tiles_per_split = (n_tiles + ns - 1) / ns;
+    pl->keys_per_split = tiles_per_split * kKT;
+    pl->n_split = (kv_len + pl->keys_per_split - 1) / pl->keys_per_split;
+    const size_t rows_total = (size_t)n_rows * n_q_heads;
+    const size_t o_bytes = (size_t)pl->n_split * rows_total * head_dim * sizeof(float);
+    pl->ws_bytes = ((o_bytes + 255) / 256) * 256 + (size_t)pl->n_split * rows_total * 2 * sizeof(float);
+    return KVQ8_OK;
+}
+
+template <int HD, int NT>
+int launch_verify(const VerifyParams& vp, const Plan& pl, int n_kv_heads, cudaStream_t stream) {
+    constexpr int bytes = Smem<HD, NT>::kBytes;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(verify_split_kernel<HD, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+            cudaSuccess)
+            return KVQ8_ERR_CUDA;
+        attr_set = true;
+    }
+    dim3 grid(pl.n_chunks, pl.n_split, n_kv_heads);
+    verify_split_kernel<HD, NT><<<grid, kThreads, bytes, stream>>>(vp);
+    return launch_status();
+}
+
+template <int HD>
+int dispatch_nt(const VerifyParams& vp, const Plan& pl, int n_kv_heads, cudaStream_t s) {
+    switch (pl.nt) {
+        case 1: return launch_verify<HD, 1>(vp, pl, n_kv_heads, s);
+        case 2: return launch_verify<HD, 2>(vp, pl, n_kv_heads, s);
+        case 3: return launch_verify<HD, 3>(vp, pl, n_kv_heads, s);
+        case 4: return launch_verify<HD, 4>(vp, pl, n_kv_heads, s);
+        default: return KVQ8_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace
+}  // namespace kvq8
+
+extern "C" size_t attn_verify_q8_workspace_bytes(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_kv_heads,
+                                                 int n_split) {
+    kvq8::Plan pl;
+    if (kvq8::make_plan(n_rows, n_q_heads, head_dim, kv_len, n_kv_heads, n_split, &pl) != KVQ8_OK) return 0;
+    return pl.ws_bytes;
+}
+
+extern "C" int attn_verify_q8(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv, int kv_len,
+                              int q_pos0, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                              int n_split, kvq8_stream_t stream) {
+    using namespace kvq8;
+    if (!kv || !q || !out) return KVQ8_ERR_INVALID_ARG;
+    if (!kv->k_codes || !kv->k_scales || !kv->v_codes || !kv->v_scales) return KVQ8_ERR_INVALID_ARG;
+    if (kv->n_kv_heads < 1 || kv->capacity < 1 || q_pos0 < 0) return KVQ8_ERR_INVALID_ARG;
+    if (kv_len > kv->capacity) return KVQ8_ERR_INVALID_ARG;
+    if (!(softmax_scale == softmax_scale) || softmax_scale == INFINITY || softmax_scale == -INFINITY)
+        return KVQ8_ERR_INVALID_ARG;
+    Plan pl;
+    const int rc = make_plan(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, n_split, &pl);
+    if (rc != KVQ8_OK) return rc;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(kv->k_codes) || !aligned16(kv->k_scales) ||
+        !aligned16(kv->v_codes) || !aligned16(kv->v_scales))
+        return KVQ8_ERR_MISALIGNED;
+    if (!workspace || workspace_bytes < pl.ws_bytes) return KVQ8_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return KVQ8_ERR_MISALIGNED;
+
+    VerifyParams vp;
+    vp.q = q;
+    vp.k_codes = kv->k_codes;
+    vp.k_scales = kv->k_scales;
+    vp.v_codes = kv->v_codes;
+    vp.v_scales = kv->v_scales;
+    const size_t rows_total = (size_t)n_rows * n_q_heads;
+    const size_t o_bytes = (size_t)pl.n_split * rows_total * kv->head_dim * sizeof(float);
+    vp.part_o = static_cast<float*>(workspace);
+    vp.part_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + ((o_bytes + 255) / 256) * 256);
+    vp.n_rows = n_rows;
+    vp.n_q_heads = n_q_heads;
+    vp.group = n_q_heads / kv->n_kv_heads;
+    vp.capacity = kv->capacity;
+    vp.kv_len = kv_len;
+    vp.q_pos0 = q_pos0;
+    vp.keys_per_split = pl.keys_per_split;
+    vp.rows_per_chunk = pl.rows_per_chunk;
+    vp.qscale = softmax_scale * kLog2e;
+    cudaStream_t s = (cudaStream_t)stream;
+    const int r1 = pl.hd == 128 ? dispatch_nt<128>(vp, pl, kv->n_kv_heads, s) : dispatch_nt<256>(vp, pl, kv->n_kv_heads, s);
+    if (r1 != KVQ8_OK) return r1;
+    return launch_combine(vp.part_o, reinterpret_cast<const float*>(vp.part_ml), pl.n_split, (int)rows_total,
+                          kv->head_dim, out, s);
+}

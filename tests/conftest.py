@@ -25,3 +25,12 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def lib():
+    """Build (if needed) and load the CUDA library once per test session."""
+    from speculative_verify_attention_gb300 import build, load_library
+
+    build.build()
+    return load_library()

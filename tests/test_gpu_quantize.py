@@ -1,0 +1,108 @@
+"""kvq8_quantize on the GPU: bit-exact against the oracle's Q8_0 quantiser."""
+import numpy as np
+import pytest
+
+import oracle
+from speculative_verify_attention_gb300 import workloads
+
+from ._util import build_caches, planes_equal
+from .test_oracle_pins import _read_hand_cases
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_quant(x):
+    import torch
+
+    from speculative_verify_attention_gb300 import kvq8_quantize
+    n_tok, h, hd = x.shape
+    codes = torch.zeros((h, n_tok, hd), dtype=torch.int8, device="cuda")
+    scales = torch.zeros((h, n_tok, hd // 32), dtype=torch.float16, device="cuda")
+    kvq8_quantize(torch.from_numpy(np.ascontiguousarray(x, np.float32)).cuda(), codes, scales, 0)
+    torch.cuda.synchronize()
+    return codes.cpu().numpy(), scales.cpu().numpy().view(np.uint16)
+
+
+def test_hand_cases_bit_exact(lib):
+    cases = _read_hand_cases()
+    x = np.zeros((len(cases), 1, 32), np.float32)
+    for i, c in enumerate(cases):
+        x[i, 0, : len(c["x"])] = c["x"]
+    codes, scales = _gpu_quant(x)
+    for i, c in enumerate(cases):
+        exp_q = np.zeros(32, np.int8)
+        exp_q[: len(c["q"])] = c["q"]
+        assert int(scales[0, i, 0]) == c["scale"], c["name"]
+        assert np.array_equal(codes[0, i], exp_q), c["name"]
+
+
+def test_random_wide_range_bit_exact(lib):
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((4096, 2, 256)).astype(np.float32)
+    x *= np.exp2(rng.integers(-30, 14, (4096, 2, 8)).repeat(32, axis=2)).astype(np.float32)
+    x[5, 1, :32] = 0.0
+    x[6, 0, :32] = -0.0
+    x[7, 0, 0] = np.float32(1e-45)
+    x[8, 1, 3] = np.float32(1e7)
+    codes, scales = _gpu_quant(x)
+    q, d = oracle.quantize_q8_0(x)          # [n_tok][h][hd], [n_tok][h][nb]
+    assert np.array_equal(codes, q.transpose(1, 0, 2))
+    assert np.array_equal(scales, d.transpose(1, 0, 2))
+
+
+def test_exact_ties_bit_exact(lib):
+    # d = 1 blocks (amax 127) whose other values are k + 0.5: every quotient is an exact tie
+    rng = np.random.default_rng(22)
+    x = (rng.integers(-127, 127, (512, 1, 128)) + 0.5).astype(np.float32)
+    x[:, :, ::32] = 127.0
+    codes, scales = _gpu_quant(x)
+    q, d = oracle.quantize_q8_0(x)
+    assert np.array_equal(codes, q.transpose(1, 0, 2)) and np.array_equal(scales, d.transpose(1, 0, 2))
+
+
+def test_append_at_offset_and_capacity(lib):
+    import torch
+
+    inp = workloads.random_small(23, 4, 2, 128, 37, 1)
+    gpu, orc = build_caches(inp, capacity=64, pos0=11)
+    assert planes_equal(gpu, orc)
+    # n_tok = 0 is a no-op
+    from speculative_verify_attention_gb300 import kvq8_quantize
+    before = gpu.k_codes.clone()
+    kvq8_quantize(torch.zeros((0, 2, 128), device="cuda"), gpu.k_codes, gpu.k_scales, 5)
+    torch.cuda.synchronize()
+    assert torch.equal(before, gpu.k_codes)
+
+
+def test_full_long_context_planes_bit_exact(lib):
+    w = workloads.long_verify(32768, 32)
+    inp = workloads.make_inputs(w)
+    gpu, orc = build_caches(inp, garbage_tail=False)
+    assert planes_equal(gpu, orc)
+
+
+def test_outlier_workload_planes_bit_exact(lib):
+    w = workloads.verify_27b(8)
+    inp = workloads.make_inputs(w)
+    assert inp.outlier_channels.shape == (4, 4)
+    gpu, orc = build_caches(inp, garbage_tail=False)
+    assert planes_equal(gpu, orc)
+
+
+def test_quantize_rejects_bad_arguments(lib):
+    import torch
+
+    from speculative_verify_attention_gb300 import KVQ8Error, kvq8_quantize
+    codes = torch.zeros((1, 8, 64), dtype=torch.int8, device="cuda")
+    scales = torch.zeros((1, 8, 2), dtype=torch.float16, device="cuda")
+    with pytest.raises(KVQ8Error) as e:   # does not fit the capacity
+        kvq8_quantize(torch.zeros((4, 1, 64), device="cuda"), codes, scales, 6)
+    assert e.value.status == 1
+    with pytest.raises(KVQ8Error) as e:   # head_dim not a multiple of 32
+        kvq8_quantize(torch.zeros((1, 1, 48), device="cuda"), torch.zeros((1, 8, 48), dtype=torch.int8,
+                      device="cuda"), scales, 0)
+    assert e.value.status == 2
+    buf = torch.zeros(4 * 64 + 1, device="cuda")
+    with pytest.raises(KVQ8Error) as e:   # misaligned input pointer
+        kvq8_quantize(buf[1:].view(4, 1, 64), codes, scales, 0)
+    assert e.value.status == 3
