@@ -1,0 +1,505 @@
+#!/usr/bin/env python
+"""Benchmark of the Q8_0 GQA verify / prompt attention path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+One JSON line on rank 0.  A step is one speculative-verify step on the 27B-class
+workload (24 q heads / 4 kv heads, head_dim 256, context 4096): for each window length
+T in {4, 8}, append the T new K/V tokens to the Q8_0 cache (kvq8_quantize, K and V) and
+run attn_verify_q8 (split-context kernel + log-sum-exp combine) over ctx + T keys.
+`value` is the KV-scan bandwidth of the whole job (Q8_0 K/V bytes read by the verify
+calls / time), in GB/s; `us_per_call` gives the per-call latency.  The prompt-chunk
+kernel (12 q heads / 1 kv head, hd256, 2048 queries over a 32768-token int8 context) is
+timed in the same run and reported under "prompt" in TFLOP/s.
+
+Timing: steps are captured once in a CUDA graph and replayed, so the device time is not
+hidden behind Python launch overhead; every step reads a different cache of a ring whose
+total size is above 4x the L2, so K/V bytes come from HBM.  The `e2e` figure instead goes
+through the Python API with pinned host buffers: each step copies q and the new K/V
+tokens host->device and reads the outputs back, eagerly, with no graph.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify-attn us/call and KV-scan GB/s (% HBM peak); prompt-attn TFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+VERIFY_T = (4, 8)
+GRAPH_STEPS = 64
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+def oracle_verify_sample(n_pairs_per_step: int, steps: int, warmup: int, threads: int | None = None):
+    """Time the fp64 oracle on (row, head) pairs of the 27B-class T=4 verify call.
+    Returns (GB/s-equivalent, seconds per step, threads, description)."""
+    import oracle
+    from speculative_verify_attention_gb300 import workloads
+
+    w = workloads.verify_27b(4)
+    inp = workloads.make_inputs(w)
+    c = oracle.Cache(w.n_kv_heads, w.head_dim, w.kv_len)
+    c.append(inp.k, inp.v, 0)
+    if threads:
+        oracle.set_threads(threads)
+    n_thr = oracle.get_threads()
+    pairs = [(i, h) for i in range(w.n_q) for h in range(w.n_q_heads)]
+    rng = np.random.default_rng(0)
+
+    def one():
+        sel = [pairs[k] for k in rng.integers(0, len(pairs), n_pairs_per_step)]
+        oracle.attention(c, inp.q, w.kv_len, w.q_pos0, w.softmax_scale, sel=sel)
+
+    for _ in range(warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    dt = time.perf_counter() - t0
+    calls = steps * n_pairs_per_step / len(pairs)
+    gbs = calls * w.kv_bytes() / dt / 1e9
+    desc = (f"{n_pairs_per_step} (row, q-head) pairs per step of the T=4 call (kv_len {w.kv_len}); "
+            f"GB/s counts each pair as 1/{len(pairs)} of the call's {w.kv_bytes() / 1e6:.2f} MB of K/V")
+    return gbs, dt / steps, n_thr, desc
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    n_pairs = 8 if args.steps > 200 else 96
+    gbs, sec, thr, desc = oracle_verify_sample(n_pairs, args.steps, min(args.warmup, 3))
+    from speculative_verify_attention_gb300 import workloads
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workloads.verify_27b(4).name + " (CPU oracle sample)"},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": thr, "kind": "oracle", "sample": desc},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- native arm
+
+def run_native(args, world, rank, local):
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from speculative_verify_attention_gb300 import (KVCacheQ8, KVQ8Error, attn_prompt_q8, attn_verify_q8,
+                                                    attn_verify_q8_workspace_bytes, kvq8_quantize, workloads)
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hbm_peak, bf16_peak, peak_src = _peaks()
+    fp16_peak = bf16_peak * 0.951   # cuBLAS fp16 / bf16 measured on this part: 1815.6 / 1908.7
+
+    ws_ = {T: workloads.verify_27b(T) for T in VERIFY_T}
+    w0 = ws_[VERIFY_T[0]]
+    ctx = w0.ctx
+    cap = ctx + max(VERIFY_T)
+    inp = workloads.make_inputs(workloads.verify_27b(max(VERIFY_T)))   # K/V for ctx + 8 tokens, seeded
+    base = KVCacheQ8(w0.n_kv_heads, w0.head_dim, cap, device=dev)
+    base.append(torch.from_numpy(inp.k).to(dev), torch.from_numpy(inp.v).to(dev), 0)
+    cache_bytes = sum(t.numel() * t.element_size() for t in (base.k_codes, base.v_codes, base.k_scales, base.v_scales))
+    n_ring = max(2, int(np.ceil(args.ring_l2 * L2_BYTES / cache_bytes)))
+    ring = [base]
+    for _ in range(n_ring - 1):
+        c = KVCacheQ8(w0.n_kv_heads, w0.head_dim, cap, device=dev)
+        for a, b in ((c.k_codes, base.k_codes), (c.v_codes, base.v_codes), (c.k_scales, base.k_scales),
+                     (c.v_scales, base.v_scales)):
+            a.copy_(b)
+        ring.append(c)
+    q = {T: torch.from_numpy(workloads.make_inputs(ws_[T], kv_len=1).q).to(dev) for T in VERIFY_T}
+    knew = {T: torch.from_numpy(inp.k[ctx:ctx + T].copy()).to(dev) for T in VERIFY_T}
+    vnew = {T: torch.from_numpy(inp.v[ctx:ctx + T].copy()).to(dev) for T in VERIFY_T}
+    out = {T: torch.empty_like(q[T]) for T in VERIFY_T}
+    wsb = {T: torch.empty(attn_verify_q8_workspace_bytes(T, w0.n_q_heads, w0.head_dim, ctx + T, w0.n_kv_heads),
+                          dtype=torch.uint8, device=dev) for T in VERIFY_T}
+    kv_bytes_step = sum(ws_[T].kv_bytes() for T in VERIFY_T)
+
+    def step(s, do_append=True, do_verify=True):
+        c = ring[s % n_ring]
+        for T in VERIFY_T:
+            if do_append:
+                kvq8_quantize(knew[T], c.k_codes, c.k_scales, ctx)
+                kvq8_quantize(vnew[T], c.v_codes, c.v_scales, ctx)
+            if do_verify:
+                attn_verify_q8(q[T], c, ctx + T, ctx, w0.softmax_scale, out=out[T], workspace=wsb[T])
+
+    launches_per_step = len(VERIFY_T) * 4   # 2 quantise + verify split + combine per T
+
+    def capture(**kw):
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for i in range(3):
+                step(i, **kw)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(GRAPH_STEPS):
+                step(i, **kw)
+        return g
+
+    g_step = capture()
+    g_verify = capture(do_append=False)
+    reps = max(1, int(np.ceil(args.steps / GRAPH_STEPS)))
+    steps = reps * GRAPH_STEPS
+    wreps = max(1, int(np.ceil(args.warmup / GRAPH_STEPS)))
+
+    for _ in range(wreps):
+        g_step.replay()
+    torch.cuda.synchronize()
+    _barrier(world)
+    torch.cuda.synchronize()
+    clk = ClockSampler(local)
+    clk.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g_step.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    _barrier(world)
+    ms = e0.elapsed_time(e1)
+    # the verify calls alone (same ring walk), for the roofline of the dominant kernel
+    v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    v0.record()
+    for _ in range(reps):
+        g_verify.replay()
+    v1.record()
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    ms_verify = v0.elapsed_time(v1)
+    ms = _max_over_ranks(ms, world)
+
+    ms_per_step = ms / steps
+    gbs = world * kv_bytes_step * steps / (ms * 1e-3) / 1e9
+    us_per_call_verify = ms_verify * 1e3 / (steps * len(VERIFY_T))
+    verify_gbs = kv_bytes_step * steps / (ms_verify * 1e-3) / 1e9
+
+    # per-T latency (graph of a single T)
+    per_t = {}
+    for T in VERIFY_T:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(GRAPH_STEPS):
+                attn_verify_q8(q[T], ring[i % n_ring], ctx + T, ctx, w0.softmax_scale, out=out[T], workspace=wsb[T])
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(max(1, reps // 2)):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / (max(1, reps // 2) * GRAPH_STEPS)
+        per_t[f"T{T}"] = {"us_per_call": us, "kv_gbs": ws_[T].kv_bytes() / (us * 1e-6) / 1e9,
+                          "hbm_frac": ws_[T].kv_bytes() / (us * 1e-6) / 1e9 / hbm_peak}
+
+    # e2e through the Python API with pinned host buffers, eager
+    h_q = {T: q[T].cpu().pin_memory() for T in VERIFY_T}
+    h_k = {T: knew[T].cpu().pin_memory() for T in VERIFY_T}
+    h_v = {T: vnew[T].cpu().pin_memory() for T in VERIFY_T}
+    h_out = {T: torch.empty(out[T].shape, dtype=torch.float32).pin_memory() for T in VERIFY_T}
+    d_q = {T: torch.empty_like(q[T]) for T in VERIFY_T}
+    d_k = {T: torch.empty_like(knew[T]) for T in VERIFY_T}
+    d_v = {T: torch.empty_like(vnew[T]) for T in VERIFY_T}
+    h2d = sum(h_q[T].numel() * 4 + h_k[T].numel() * 4 + h_v[T].numel() * 4 for T in VERIFY_T)
+    d2h = sum(h_out[T].numel() * 4 for T in VERIFY_T)
+
+    def e2e_step(s):
+        c = ring[s % n_ring]
+        for T in VERIFY_T:
+            d_q[T].copy_(h_q[T], non_blocking=True)
+            d_k[T].copy_(h_k[T], non_blocking=True)
+            d_v[T].copy_(h_v[T], non_blocking=True)
+            c.append(d_k[T], d_v[T], ctx)
+            attn_verify_q8(d_q[T], c, ctx + T, ctx, w0.softmax_scale, out=out[T], workspace=wsb[T])
+            h_out[T].copy_(out[T], non_blocking=True)
+
+    e2e_steps = min(steps, 2000)
+    for s in range(min(args.warmup, 20)):
+        e2e_step(s)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for s in range(e2e_steps):
+        e2e_step(s)
+    torch.cuda.synchronize()
+    e2e_sec = _max_over_ranks(time.perf_counter() - t0, world)
+    e2e_gbs = world * kv_bytes_step * e2e_steps / e2e_sec / 1e9
+
+    # prompt chunk (tensor-core kernel), L2 flushed between timed calls
+    prompt = prompt_bench(args, dev, fp16_peak) if not args.no_prompt else None
+
+    result = None
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            n_pairs = 24
+            cpu_steps = 6
+            g_, sec_, thr_, desc_ = oracle_verify_sample(n_pairs, cpu_steps, 1)
+            cpu = {"value": g_, "unit": "GB/s", "cores": thr_, "kind": "oracle",
+                   "sample": desc_ + f"; {cpu_steps} steps timed"}
+        bytes_per_launch = kv_bytes_step / len(VERIFY_T)
+        achieved = bytes_per_launch / (us_per_call_verify * 1e-6) / 1e9
+        result = {
+            "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int8-kv, f16 hi+lo tensor-core, f32 accumulate", "data": "synthetic",
+            "config": {"workload": "verify-24q4kv-hd256-ctx4096-T4+T8-outliers", "model": None,
+                       "global_batch": world, "seq_len": ctx, "verify_rows": list(VERIFY_T),
+                       "parallelism": f"replicas x{world}", "l2": f"ring of {n_ring} caches, "
+                       f"{n_ring * cache_bytes / 2**20:.0f} MiB > 4x L2 (every step reads a different cache)",
+                       "step": "per T in {4,8}: kvq8_quantize K and V of T new tokens + attn_verify_q8 over ctx+T",
+                       "graph": f"{GRAPH_STEPS} steps per CUDA graph replay"},
+            "us_per_call": us_per_call_verify, "verify_only_gbs": verify_gbs,
+            "hbm_frac": verify_gbs / hbm_peak, "per_T": per_t,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": None, "peak_source": peak_src,
+                         "kernel": "attn_verify_q8 (verify_split_kernel + combine_kernel)",
+                         "algorithmic_bytes_per_launch": bytes_per_launch},
+            "prompt": prompt,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "us_per_step": e2e_sec / e2e_steps * 1e6, "path": "python API, eager, pinned host buffers"},
+            "clocks": clocks,
+            "gpu_launches": launches_per_step * steps,
+        }
+    return result
+
+
+def prompt_bench(args, dev, fp16_peak):
+    import torch
+
+    from speculative_verify_attention_gb300 import KVCacheQ8, KVQ8Error, attn_prompt_q8, workloads
+    w = workloads.PROMPT
+    inp = workloads.make_inputs(w)
+    c = KVCacheQ8(w.n_kv_heads, w.head_dim, w.kv_len, device=dev)
+    c.append(torch.from_numpy(inp.k).to(dev), torch.from_numpy(inp.v).to(dev), 0)
+    q = torch.from_numpy(inp.q).to(dev)
+    out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    try:
+        attn_prompt_q8(q, c, w.kv_len, w.q_pos0, w.softmax_scale, out=out)
+    except KVQ8Error as e:
+        return {"unavailable": str(e)}
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    times = []
+    n = max(3, min(args.prompt_steps, 20))
+    for i in range(n + 2):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        attn_prompt_q8(q, c, w.kv_len, w.q_pos0, w.softmax_scale, out=out)
+        b.record()
+        torch.cuda.synchronize()
+        if i >= 2:
+            times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    tf = w.causal_flops() / (ms * 1e-3) / 1e12
+    return {"workload": w.name, "ms_per_call": ms, "tflops": tf, "peak_tflops": fp16_peak,
+            "frac": tf / fp16_peak, "peak_source": "fp16 = measured bf16 x 0.951 (cuBLAS fp16/bf16 on GB300)",
+            "flops": w.causal_flops(), "calls_timed": n, "l2": "flushed (256 MiB write) before every call"}
+
+
+def sweep(args):
+    """Verify latency and KV-scan bandwidth per (context, T) cell of the long-context and
+    hd128 workload families (one JSON line per cell; not the headline line)."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from speculative_verify_attention_gb300 import (KVCacheQ8, attn_verify_q8, attn_verify_q8_workspace_bytes,
+                                                    workloads)
+    hbm_peak, _, _ = _peaks()
+    dev = torch.device("cuda", 0)
+    cells = [workloads.long_verify(c, t) for c in workloads.LONG_CTX for t in workloads.LONG_T]
+    cells += [workloads.hd128_verify(t) for t in workloads.HD128_T]
+    cells = [w for w in cells if not args.sweep_filter or args.sweep_filter in w.name]
+    built = {}
+    for w in cells:
+        key = (w.n_kv_heads, w.head_dim, w.kv_len)
+        if key not in built:
+            built.clear()
+            torch.cuda.empty_cache()
+            inp = workloads.make_inputs(w)
+            base = KVCacheQ8(w.n_kv_heads, w.head_dim, w.kv_len, device=dev)
+            base.append(torch.from_numpy(inp.k).to(dev), torch.from_numpy(inp.v).to(dev), 0)
+            nbytes = sum(t.numel() * t.element_size() for t in (base.k_codes, base.v_codes, base.k_scales,
+                                                                base.v_scales))
+            n_ring = max(2, int(np.ceil(args.ring_l2 * L2_BYTES / nbytes)))
+            ring = [base]
+            for _ in range(n_ring - 1):
+                c = KVCacheQ8(w.n_kv_heads, w.head_dim, w.kv_len, device=dev)
+                for a, b in ((c.k_codes, base.k_codes), (c.v_codes, base.v_codes), (c.k_scales, base.k_scales),
+                             (c.v_scales, base.v_scales)):
+                    a.copy_(b)
+                ring.append(c)
+            built[key] = ring
+        ring = built[key]
+        q = torch.from_numpy(workloads.make_inputs(w, kv_len=1).q).to(dev)
+        out = torch.empty_like(q)
+        ws = torch.empty(attn_verify_q8_workspace_bytes(w.n_q, w.n_q_heads, w.head_dim, w.kv_len, w.n_kv_heads),
+                         dtype=torch.uint8, device=dev)
+        for i in range(3):
+            attn_verify_q8(q, ring[i % len(ring)], w.kv_len, w.q_pos0, w.softmax_scale, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        n_calls = max(len(ring), 32)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n_calls):
+                attn_verify_q8(q, ring[i % len(ring)], w.kv_len, w.q_pos0, w.softmax_scale, out=out, workspace=ws)
+        g.replay()
+        torch.cuda.synchronize()
+        reps = 10
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / (reps * n_calls)
+        gbs = w.kv_bytes() / (us * 1e-6) / 1e9
+        print(json.dumps({"workload": w.name, "us_per_call": us, "kv_mb": w.kv_bytes() / 1e6, "kv_gbs": gbs,
+                          "hbm_frac": gbs / hbm_peak, "tflops_alg": w.causal_flops() / (us * 1e-6) / 1e12,
+                          "ring": len(ring)}), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2048)
+    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--ring-l2", type=float, default=4.2, help="ring size in multiples of the L2")
+    ap.add_argument("--prompt-steps", type=int, default=10)
+    ap.add_argument("--no-prompt", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="per-cell verify sweep instead of the headline line")
+    ap.add_argument("--sweep-filter", default="")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = _dist()
+    if args.sweep:
+        sweep(args)
+        return 0
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    res = run_native(args, world, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -142,20 +142,47 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
 
     // Stage q rows of this chunk as fp16 hi/lo in mma B-fragment order:
     // entry (block b, n-tile nt, hi|lo, lane g*4+t) holds row 8nt+g, dims 32b+8t .. +7.
-    for (int idx = threadIdx.x; idx < RP * HD; idx += kThreads) {
-        const int r = idx / HD, j = idx - r * HD;
-        float v = 0.0f;
-        if (r < rows_here) {
-            const int rr = row0 + r;
-            const int i = rr / p.group, hh = rr - i * p.group;
-            v = __ldg(p.q + ((int64_t)i * p.n_q_heads + kvh * p.group + hh) * HD + j) * p.qscale;
+    // One entry = 8 consecutive dims of one row: two float4 loads, one 16-byte store each
+    // for hi and lo; all loads of a thread are issued before any is used.
+    {
+        constexpr int GPR = HD / 8;                       // 8-dim groups per row
+        constexpr int PER = (RP * GPR + kThreads - 1) / kThreads;
+        float4 v[PER][2];
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int idx = threadIdx.x + k * kThreads;
+            const int r = idx / GPR, j8 = idx - r * GPR;
+            v[k][0] = v[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (idx < RP * GPR && r < rows_here) {
+                const int rr = row0 + r;
+                const int i = rr / p.group, hh = rr - i * p.group;
+                const float4* src =
+                    reinterpret_cast<const float4*>(p.q + ((int64_t)i * p.n_q_heads + kvh * p.group + hh) * HD) + 2 * j8;
+                v[k][0] = __ldg(src);
+                v[k][1] = __ldg(src + 1);
+            }
         }
-        const __half hi = __float2half_rn(v);
-        const __half lo = __float2half_rn(v - __half2float(hi));
-        const int b = j >> 5, tt = (j >> 3) & 3, e = j & 7, nt = r >> 3, gg = r & 7;
-        const int base = ((b * NT + nt) * 2) * 256 + (gg * 4 + tt) * 8 + e;
-        sQ[base] = hi;
-        sQ[base + 256] = lo;
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int idx = threadIdx.x + k * kThreads;
+            if (idx >= RP * GPR) continue;
+            const int r = idx / GPR, j8 = idx - r * GPR;
+            const float x[8] = {v[k][0].x, v[k][0].y, v[k][0].z, v[k][0].w,
+                                v[k][1].x, v[k][1].y, v[k][1].z, v[k][1].w};
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float a = x[2 * e] * p.qscale, b = x[2 * e + 1] * p.qscale;
+                const __half2 h = __floats2half2_rn(a, b);
+                const __half2 l = __floats2half2_rn(a - __low2float(h), b - __high2float(h));
+                hi[e] = *reinterpret_cast<const uint32_t*>(&h);
+                lo[e] = *reinterpret_cast<const uint32_t*>(&l);
+            }
+            const int b = j8 >> 2, tt = j8 & 3, nt = r >> 3, gg = r & 7;
+            uint4* dst = reinterpret_cast<uint4*>(sQ + ((b * NT + nt) * 2) * 256 + (gg * 4 + tt) * 8);
+            dst[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            dst[32] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
     }
 
     // Visibility bound per owned row: row rr sees keys < vis_end.
