@@ -86,7 +86,7 @@ size_t attn_verify_q8_workspace_bytes(int n_rows, int n_q_heads, int head_dim, i
 /*
  * attn_verify_q8 -- speculative-decode verify attention over a Q8_0 cache.
  *   q        : fp32 [n_rows][n_q_heads][head_dim], 1 <= n_rows <= 32
- *   kv       : the cache (head_dim 128 or 256; n_q_heads / n_kv_heads integral, <= 16)
+ *   kv       : the cache (head_dim 128 or 256; n_q_heads / n_kv_heads integral, <= 64)
  *   kv_len   : tokens of the cache to attend over; q_pos0: position of row 0 (see above)
  *   out      : fp32 [n_rows][n_q_heads][head_dim], normalised attention output
  *   workspace: device scratch of at least attn_verify_q8_workspace_bytes(...) bytes,
@@ -126,6 +126,31 @@ int attn_combine(const float* part_o, const float* part_ml, int n_split, int row
  */
 int attn_prompt_q8(const uint16_t* q, int n_q, int n_q_heads, const kvq8_cache* kv, int kv_len,
                    int q_pos0, float softmax_scale, float* out, kvq8_stream_t stream);
+
+/*
+ * attn_verify_q8_noalloc -- attn_verify_q8 for callers that cannot allocate device memory.
+ *
+ * No counterpart on the pages: this is a library convenience.  Some callers cannot call
+ * cudaMalloc at the point where they run attention: a runtime that hands all device memory
+ * out of its own fixed arena and forbids other allocations, code running inside a custom
+ * allocator's callback (where allocating again would re-enter the allocator), or a plug-in
+ * that is not allowed to touch the process allocator at all.  This entry point takes the same
+ * arguments as attn_verify_q8 minus the workspace: the split-context partials live in one
+ * static device array of KVQ8_NOALLOC_SCRATCH_BYTES bytes built into the library, which
+ * every GPU that loads the library holds until the process exits.
+ *   - It never calls cudaMalloc, cudaFree or any allocating library routine.
+ *   - The first call on each device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (different streams, or
+ *     several host threads) race on it and must be serialised by the caller.
+ *   - With n_split = 0 the split count is lowered, if needed, until the partials fit; a
+ *     shape whose partials do not fit even with one slice (n_rows * n_q_heads * (head_dim
+ *     + 2) * 4 bytes above the array), or an explicit n_split that does not fit, returns
+ *     KVQ8_ERR_WORKSPACE and launches nothing.
+ */
+#define KVQ8_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+int attn_verify_q8_noalloc(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv, int kv_len,
+                           int q_pos0, float softmax_scale, float* out, int n_split, kvq8_stream_t stream);
 
 /* Human-readable name of a status code (static string). */
 const char* kvq8_status_str(int status);

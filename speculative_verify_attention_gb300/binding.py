@@ -28,7 +28,8 @@ KVQ8_ERR_CUDA = 5
 
 # Entry points declared in include/kvq8attn.h.
 EXPORTED = ("kvq8_quantize", "attn_verify_q8_workspace_bytes", "attn_verify_q8", "attn_combine",
-            "attn_prompt_q8", "kvq8_status_str")
+            "attn_prompt_q8", "attn_verify_q8_noalloc", "kvq8_status_str")
+NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 
 class KVQ8Error(RuntimeError):
@@ -69,6 +70,8 @@ def load_library():
         lib.attn_combine.restype = i32
         lib.attn_prompt_q8.argtypes = [vp, i32, i32, cp, i32, i32, f32, vp, vp]
         lib.attn_prompt_q8.restype = i32
+        lib.attn_verify_q8_noalloc.argtypes = [vp, i32, i32, cp, i32, i32, f32, vp, i32, vp]
+        lib.attn_verify_q8_noalloc.restype = i32
         lib.kvq8_status_str.argtypes = [i32]
         lib.kvq8_status_str.restype = ctypes.c_char_p
         _lib = lib
@@ -190,4 +193,23 @@ def attn_prompt_q8(q: torch.Tensor, cache: KVCacheQ8, kv_len: int, q_pos0: int, 
     st = load_library().attn_prompt_q8(_ptr(q), n_q, n_q_heads, ctypes.byref(cache.struct()), int(kv_len),
                                        int(q_pos0), float(softmax_scale), _ptr(out), _stream(stream))
     _check("attn_prompt_q8", st)
+    return out
+
+
+def attn_verify_q8_noalloc(q: torch.Tensor, cache: KVCacheQ8, kv_len: int, q_pos0: int, softmax_scale: float,
+                           out: torch.Tensor | None = None, n_split: int = 0, stream=None) -> torch.Tensor:
+    """attn_verify_q8 without a workspace, for callers that cannot allocate device memory at
+    call time: the library keeps the split partials in its own static device array.  The
+    first call on a device must come before any stream capture; calls that overlap on the
+    GPU share that array and must be serialised by the caller.  `out` must be given by such
+    callers (it is only allocated here when omitted, as a convenience)."""
+    _need(q, "q", torch.float32)
+    n_rows, n_q_heads, _ = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.float32)
+    st = load_library().attn_verify_q8_noalloc(_ptr(q), n_rows, n_q_heads, ctypes.byref(cache.struct()),
+                                               int(kv_len), int(q_pos0), float(softmax_scale), _ptr(out),
+                                               int(n_split), _stream(stream))
+    _check("attn_verify_q8_noalloc", st)
     return out

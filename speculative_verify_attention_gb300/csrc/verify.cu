@@ -640,3 +640,65 @@ extern "C" int attn_verify_q8(const float* q, int n_rows, int n_q_heads, const k
     return launch_combine(vp.part_o, reinterpret_cast<const float*>(vp.part_ml), pl.n_split, (int)rows_total,
                           kv->head_dim, out, s);
 }
+
+// ---------------------------------------------------------------------------------------
+// attn_verify_q8_noalloc: the same computation for callers that cannot allocate device
+// memory.  The split partials live in one file-scope device array that every GPU loading
+// this library holds until the process exits; the entry point looks up that array's device
+// address once per device and never calls cudaMalloc / cudaFree.
+// ---------------------------------------------------------------------------------------
+#include <mutex>
+
+static __device__ __align__(256) unsigned char g_verify_noalloc_scratch[KVQ8_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  The first call on a device
+// performs the lookup (cudaGetSymbolAddress) with that device current; later calls reuse it.
+int noalloc_scratch(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVQ8_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_verify_noalloc_scratch) != cudaSuccess || !p) return KVQ8_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return KVQ8_OK;
+}
+
+}  // namespace
+
+extern "C" int attn_verify_q8_noalloc(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv, int kv_len,
+                                      int q_pos0, float softmax_scale, float* out, int n_split,
+                                      kvq8_stream_t stream) {
+    using namespace kvq8;
+    if (!kv) return KVQ8_ERR_INVALID_ARG;
+    Plan pl;
+    int rc = make_plan(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, n_split, &pl);
+    if (rc != KVQ8_OK) return rc;
+    if (pl.ws_bytes > (size_t)KVQ8_NOALLOC_SCRATCH_BYTES) {
+        if (n_split != 0) return KVQ8_ERR_WORKSPACE;  // the caller's split count does not fit
+        // automatic split count: take the largest one whose partials fit the array
+        const size_t rows_total = (size_t)n_rows * n_q_heads;
+        const size_t per_split = rows_total * (size_t)kv->head_dim * sizeof(float) + rows_total * 2 * sizeof(float);
+        int ns = (int)((KVQ8_NOALLOC_SCRATCH_BYTES - 256) / per_split);
+        for (; ns >= 1; --ns) {
+            rc = make_plan(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, ns, &pl);
+            if (rc != KVQ8_OK) return rc;
+            if (pl.ws_bytes <= (size_t)KVQ8_NOALLOC_SCRATCH_BYTES) break;
+        }
+        if (ns < 1) return KVQ8_ERR_WORKSPACE;  // even one slice exceeds the array
+        n_split = ns;
+    }
+    void* scratch = nullptr;
+    rc = noalloc_scratch(&scratch);
+    if (rc != KVQ8_OK) return rc;
+    return attn_verify_q8(q, n_rows, n_q_heads, kv, kv_len, q_pos0, softmax_scale, out, scratch,
+                          (size_t)KVQ8_NOALLOC_SCRATCH_BYTES, n_split, stream);
+}
