@@ -118,10 +118,15 @@ int attn_combine(const float* part_o, const float* part_ml, int n_split, int row
 /*
  * attn_prompt_q8 -- prompt-chunk attention: many query rows over a long Q8_0 context.
  *   q   : fp16 bits [n_q][n_q_heads][head_dim], head_dim 256
+ *   kv  : the cache (head_dim 256, any n_kv_heads dividing n_q_heads)
  *   out : fp32 [n_q][n_q_heads][head_dim]
- * K and V are dequantised to fp16 on chip and contracted on the tcgen05 tensor cores
- * with fp32 accumulation (S and O in tensor memory); tiles above the causal diagonal are
- * skipped.  Within 2e-3 of the fp64 oracle (max |err| / max |out|).
+ * Row i sees keys n <= q_pos0 + i, n < kv_len.  K and V are dequantised on chip to fp16
+ * (code * scale, one rounding) and contracted on the tcgen05 tensor cores with fp32
+ * accumulation in tensor memory; p enters the PV product as fp16.  Tiles past the last
+ * row's causal bound are skipped.  Within 2e-3 of the fp64 oracle (max |err| / max |out|)
+ * for values inside the fp16 range.  One 128-row tile of (query, head) pairs of one KV head
+ * per thread block; every internal wait is bounded, and a timeout sets the flag that
+ * kvq8_device_error reports (the output is then undefined).
  * Source: "gfx12 WMMA kernel for the int8-KV QSA prompt attention", How and Measurements.
  */
 int attn_prompt_q8(const uint16_t* q, int n_q, int n_q_heads, const kvq8_cache* kv, int kv_len,
@@ -151,6 +156,14 @@ int attn_prompt_q8(const uint16_t* q, int n_q, int n_q_heads, const kvq8_cache* 
 #define KVQ8_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
 int attn_verify_q8_noalloc(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv, int kv_len,
                            int q_pos0, float softmax_scale, float* out, int n_split, kvq8_stream_t stream);
+
+/*
+ * kvq8_device_error -- read (and with reset != 0, clear) the library's device error flag.
+ * Nonzero means a kernel gave up on an internal wait after its bounded poll count and
+ * returned early.  Returns the flag, or -1 if it could not be read.  Unlike every other
+ * entry point this one synchronises: it copies the flag from the current device.
+ */
+int kvq8_device_error(int reset);
 
 /* Human-readable name of a status code (static string). */
 const char* kvq8_status_str(int status);

@@ -28,7 +28,7 @@ KVQ8_ERR_CUDA = 5
 
 # Entry points declared in include/kvq8attn.h.
 EXPORTED = ("kvq8_quantize", "attn_verify_q8_workspace_bytes", "attn_verify_q8", "attn_combine",
-            "attn_prompt_q8", "attn_verify_q8_noalloc", "kvq8_status_str")
+            "attn_prompt_q8", "attn_verify_q8_noalloc", "kvq8_device_error", "kvq8_status_str")
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 
@@ -72,6 +72,8 @@ def load_library():
         lib.attn_prompt_q8.restype = i32
         lib.attn_verify_q8_noalloc.argtypes = [vp, i32, i32, cp, i32, i32, f32, vp, i32, vp]
         lib.attn_verify_q8_noalloc.restype = i32
+        lib.kvq8_device_error.argtypes = [i32]
+        lib.kvq8_device_error.restype = i32
         lib.kvq8_status_str.argtypes = [i32]
         lib.kvq8_status_str.restype = ctypes.c_char_p
         _lib = lib
@@ -80,6 +82,12 @@ def load_library():
 
 def kvq8_status_str(status: int) -> str:
     return load_library().kvq8_status_str(int(status)).decode()
+
+
+def kvq8_device_error(reset: bool = False) -> int:
+    """The library's device error flag (nonzero: a kernel timed out on an internal wait).
+    Synchronises the current device."""
+    return int(load_library().kvq8_device_error(1 if reset else 0))
 
 
 def _stream(stream) -> ctypes.c_void_p:

@@ -1,5 +1,419 @@
-// prompt.cu -- placeholder, replaced by the tcgen05 prompt kernel.
+// prompt.cu -- prompt-chunk attention over a Q8_0 GQA cache on the tcgen05 tensor cores
+// (attn_prompt_q8).
+//
+// Source: "gfx12 WMMA kernel for the int8-KV QSA prompt attention", How: int8-KV prompt
+// attention on the tensor cores with fp32 accumulation, online softmax, the V scale folded
+// into the operands, and the heads that share one KV head stacked as the rows of the
+// tile; Measurements: a 32K-token int8 context with a 2,048-query chunk.
+//
+// GB300 design: one CTA per (128-row tile of (query, head) pairs, KV head); rows r = i*g + hh
+// of one KV head, so the 12 heads of a query and ~11 consecutive queries share every K/V
+// tile.  Ten warps, each with one role:
+//   warp 0      producer: 1-D bulk async copies of the int8 codes and fp16 scales of a
+//               64-key tile into a 2-stage staging ring (mbarrier transaction counts);
+//   warp 1      MMA issuer (one thread) and tensor-memory owner;
+//   warps 2-5   softmax, one thread per row (each warp reads its 32-lane quarter of TMEM);
+//   warps 6-9   dequantisers: int8 -> fp16 exactly (byte permute + magic-bias subtract), then
+//               times the block scale (one fp16 rounding), written to double-buffered
+//               128-byte-swizzled K^ and V^ tiles in shared memory.
+// Tensor memory (512 columns): Q as fp16 pairs (128), O fp32 (256), two S buffers (64 each)
+// whose first 32 columns take P as fp16 pairs after the softmax has read S.
+//   S = Q K^T : tcgen05.mma kind::f16, A = Q from TMEM, B = K^ (K-major), M=128 N=64 K=256
+//   O += P V^ : A = P from TMEM, B = V^ (MN-major), M=128 N=256 K=64
+// The softmax keeps a per-row reference maximum and rescales the O row in TMEM only when a
+// new maximum exceeds it by more than 2^8, so p stays <= 256 in fp16.  Tiles past the
+// causal bound of the last row are never loaded; only the diagonal tile is masked.
+// Every mbarrier wait is bounded: on timeout the kernel records an error flag (read with
+// kvq8_device_error) and returns after releasing its tensor memory.
 #include "common.cuh"
-extern "C" int attn_prompt_q8(const uint16_t*, int, int, const kvq8_cache*, int, int, float, float*, kvq8_stream_t) {
-    return KVQ8_ERR_UNSUPPORTED;
+#include "tc.cuh"
+
+__device__ unsigned int g_kvq8_device_error = 0;
+
+namespace kvq8 {
+namespace {
+
+constexpr int HD = 256;
+constexpr int BM = 128;
+constexpr int BN = 64;
+constexpr int kThreads = 320;
+constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+// tensor memory columns
+constexpr uint32_t TM_Q = 0, TM_O = 128, TM_S0 = 384, TM_NCOLS = 512;
+
+// shared memory layout (bytes, 1024-aligned tiles)
+constexpr int SM_KHAT = 0;                   // 2 x 32 KB, K-major 128B-swizzled [4 atoms][64 keys][128 B]
+constexpr int SM_VHAT = 65536;               // 2 x 32 KB, same physical layout, read as MN-major
+constexpr int HAT_BYTES = 32768;
+constexpr int SM_STAGE = 131072;             // 2 x 34 KB: K codes 16K | V codes 16K | K scales 1K | V scales 1K
+constexpr int STAGE_BYTES = 34816;
+constexpr int ST_KC = 0, ST_VC = 16384, ST_KS = 32768, ST_VS = 33792;
+constexpr int SM_BAR = SM_STAGE + 2 * STAGE_BYTES;
+enum { B_ST_FULL = 0, B_ST_EMPTY = 2, B_KH_FULL = 4, B_VH_FULL = 6, B_KV_EMPTY = 8, B_S_FULL = 10, B_P_FULL = 12,
+       B_PV_DONE = 14, B_Q_READY = 16, B_COUNT = 17 };
+constexpr int SM_TMEM_SLOT = SM_BAR + B_COUNT * 8;
+constexpr int SMEM_BYTES = SM_TMEM_SLOT + 16;
+
+constexpr uint32_t IDESC_QK = tc::idesc_f16_f32(BM, BN, false);
+constexpr uint32_t IDESC_PV = tc::idesc_f16_f32(BM, HD, true);
+
+struct PromptParams {
+    const uint16_t* q;
+    const int8_t* kc;
+    const uint16_t* ks;
+    const int8_t* vc;
+    const uint16_t* vs;
+    float* out;
+    int n_q, n_q_heads, group, capacity, kv_len, q_pos0, rows;
+    float scale_log2;
+};
+
+__device__ __forceinline__ void flag_timeout() { atomicOr(&g_kvq8_device_error, 1u); }
+
+// Convert one 64-key plane tile (codes + scales in staging) into the swizzled fp16 tile:
+// element (key n, dim j) -> atom j/64, row n, 16-byte chunk ((j%64)/8) ^ (n%8).
+__device__ __forceinline__ void dequant_tile(const uint8_t* codes, const uint16_t* scales, uint8_t* hat, int nk,
+                                             int d) {
+#pragma unroll 2
+    for (int k = 0; k < 8; ++k) {
+        const int c = d + 128 * k;  // 1024 chunks of 16 codes
+        const int n = c >> 4, j16 = c & 15;
+        uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
+        if (n < nk) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(codes + n * HD + j16 * 16);
+            const __half2 sc = __half2half2(__ushort_as_half(scales[n * (HD / 32) + (j16 >> 1)]));
+            const uint32_t w[4] = {raw.x ^ 0x80808080u, raw.y ^ 0x80808080u, raw.z ^ 0x80808080u,
+                                   raw.w ^ 0x80808080u};
+            uint32_t h[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                uint32_t lo = biased_bytes_to_half2<0x4140>(w[e]);
+                uint32_t hi = biased_bytes_to_half2<0x4342>(w[e]);
+                const __half2 a = __hmul2(*reinterpret_cast<const __half2*>(&lo), sc);
+                const __half2 b = __hmul2(*reinterpret_cast<const __half2*>(&hi), sc);
+                h[2 * e] = *reinterpret_cast<const uint32_t*>(&a);
+                h[2 * e + 1] = *reinterpret_cast<const uint32_t*>(&b);
+            }
+            o0 = make_uint4(h[0], h[1], h[2], h[3]);
+            o1 = make_uint4(h[4], h[5], h[6], h[7]);
+        }
+        const int base = (j16 >> 2) * (BN * 128) + (n >> 3) * 1024 + (n & 7) * 128;
+        const int c0 = 2 * (j16 & 3);
+        *reinterpret_cast<uint4*>(hat + base + ((c0 ^ (n & 7)) << 4)) = o0;
+        *reinterpret_cast<uint4*>(hat + base + (((c0 + 1) ^ (n & 7)) << 4)) = o1;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptParams p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kvh = blockIdx.y;
+    const int r0 = blockIdx.x * BM;
+    const int rows_here = min(BM, p.rows - r0);
+    const int key_hi = min(p.kv_len, p.q_pos0 + (r0 + rows_here - 1) / p.group + 1);
+    const int key_lo = min(p.kv_len, p.q_pos0 + r0 / p.group + 1);
+    const int n_tiles = (key_hi + BN - 1) / BN;
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar = sbase + SM_BAR;
+    auto B = [&](int id) { return bar + 8u * (uint32_t)id; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM_TMEM_SLOT);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(B(B_ST_FULL + s), 1);
+            tc::mbar_init(B(B_ST_EMPTY + s), 128);
+            tc::mbar_init(B(B_KH_FULL + s), 128);
+            tc::mbar_init(B(B_VH_FULL + s), 128);
+            tc::mbar_init(B(B_KV_EMPTY + s), 1);
+            tc::mbar_init(B(B_S_FULL + s), 1);
+            tc::mbar_init(B(B_P_FULL + s), 128);
+            tc::mbar_init(B(B_PV_DONE + s), 1);
+        }
+        tc::mbar_init(B(B_Q_READY), 128);
+        tc::mbar_init_fence();
+    }
+    if (warp == 1) tc::tmem_alloc(smem_u32(tmem_slot), TM_NCOLS);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int j = 0; j < n_tiles; ++j) {
+                const int s = j & 1, use = j >> 1;
+                if (j >= 2 && !tc::mbar_wait(B(B_ST_EMPTY + s), (use - 1) & 1, kWaitLimit)) {
+                    flag_timeout();
+                    break;
+                }
+                const int key0 = j * BN;
+                const int nk = min(BN, key_hi - key0);
+                const int64_t row0 = (int64_t)kvh * p.capacity + key0;
+                const uint32_t st = sbase + SM_STAGE + s * STAGE_BYTES;
+                tc::mbar_arrive_expect_tx(B(B_ST_FULL + s), (uint32_t)(nk * (2 * HD + 2 * (HD / 16))));
+                tc::bulk_g2s(st + ST_KC, p.kc + row0 * HD, nk * HD, B(B_ST_FULL + s));
+                tc::bulk_g2s(st + ST_VC, p.vc + row0 * HD, nk * HD, B(B_ST_FULL + s));
+                tc::bulk_g2s(st + ST_KS, p.ks + row0 * (HD / 32), nk * (HD / 16), B(B_ST_FULL + s));
+                tc::bulk_g2s(st + ST_VS, p.vs + row0 * (HD / 32), nk * (HD / 16), B(B_ST_FULL + s));
+                issued = j + 1;
+            }
+            // never leave the block while a copy into its shared memory is in flight
+            for (int j = max(0, issued - 2); j < issued; ++j)
+                if (!tc::mbar_wait(B(B_ST_FULL + (j & 1)), (j >> 1) & 1, kWaitLimit)) flag_timeout();
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            bool ok = tc::mbar_wait(B(B_Q_READY), 0, kWaitLimit);
+            int pv_issued = 0;
+            auto issue_pv = [&](int jj) -> bool {
+                const int bb = jj & 1, u = jj >> 1;
+                if (!tc::mbar_wait(B(B_P_FULL + bb), u & 1, kWaitLimit)) return false;
+                if (!tc::mbar_wait(B(B_VH_FULL + bb), u & 1, kWaitLimit)) return false;
+                tc::fence_after_sync();
+                const uint32_t vhat = sbase + SM_VHAT + bb * HAT_BYTES;
+                const uint32_t pcol = tmem + TM_S0 + bb * BN;
+#pragma unroll
+                for (int ks = 0; ks < BN / 16; ++ks)
+                    tc::mma_ts(tmem + TM_O, pcol + ks * 8, tc::smem_desc_sw128(vhat + ks * 2048, BN * 128, 1024),
+                               IDESC_PV, (jj > 0 || ks > 0) ? 1u : 0u);
+                tc::mma_commit(B(B_PV_DONE + bb));
+                tc::mma_commit(B(B_KV_EMPTY + bb));
+                pv_issued = jj + 1;
+                return true;
+            };
+            if (ok) tc::fence_after_sync();
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                const int b = j & 1, use = j >> 1;
+                if (!tc::mbar_wait(B(B_KH_FULL + b), use & 1, kWaitLimit)) { ok = false; break; }
+                if (j >= 2 && !tc::mbar_wait(B(B_PV_DONE + b), (use - 1) & 1, kWaitLimit)) { ok = false; break; }
+                tc::fence_after_sync();
+                const uint32_t khat = sbase + SM_KHAT + b * HAT_BYTES;
+#pragma unroll
+                for (int ks = 0; ks < HD / 16; ++ks)
+                    tc::mma_ts(tmem + TM_S0 + b * BN, tmem + TM_Q + ks * 8,
+                               tc::smem_desc_sw128(khat + (ks >> 2) * (BN * 128) + (ks & 3) * 32, 16, 1024),
+                               IDESC_QK, ks > 0 ? 1u : 0u);
+                tc::mma_commit(B(B_S_FULL + b));
+                if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+            }
+            if (ok && n_tiles > 0 && !issue_pv(n_tiles - 1)) ok = false;
+            if (!ok) flag_timeout();
+            // the tensor memory is released only after the last committed MMA has completed
+            if (pv_issued > 0 &&
+                !tc::mbar_wait(B(B_PV_DONE + ((pv_issued - 1) & 1)), ((pv_issued - 1) >> 1) & 1, kWaitLimit))
+                flag_timeout();
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        // ---------------------------------------------------------------- softmax (one row per thread)
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const bool valid = r < rows_here;
+        const int rr = r0 + r;
+        const int iq = valid ? rr / p.group : 0;
+        const int qh = kvh * p.group + (valid ? rr - iq * p.group : 0);
+        const int vis_end = valid ? min(p.kv_len, p.q_pos0 + iq + 1) : 0;
+        // Q row -> TMEM (fp16 pairs, A operand of S = Q K^T)
+        {
+            const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)iq * p.n_q_heads + qh) * HD);
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t w[32];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (valid) v = __ldg(src + c * 8 + k);
+                    w[4 * k] = v.x;
+                    w[4 * k + 1] = v.y;
+                    w[4 * k + 2] = v.z;
+                    w[4 * k + 3] = v.w;
+                }
+                tc::tmem_st32(tmem + lane_base + TM_Q + 32 * c, w);
+            }
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
+            tc::mbar_arrive(B(B_Q_READY));
+        }
+        float m_ref = -INFINITY, l = 0.0f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int b = j & 1, use = j >> 1;
+            const bool ready = tc::mbar_wait(B(B_S_FULL + b), use & 1, kWaitLimit);
+            if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }
+            tc::fence_after_sync();
+            uint32_t s0[32], s1[32];
+            const uint32_t scol = tmem + lane_base + TM_S0 + b * BN;
+            tc::tmem_ld32(scol, s0);
+            tc::tmem_ld32(scol + 32, s1);
+            tc::tmem_wait_ld();
+            float x[64];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                x[c] = __uint_as_float(s0[c]) * p.scale_log2;
+                x[32 + c] = __uint_as_float(s1[c]) * p.scale_log2;
+            }
+            const int key0 = j * BN;
+            if (key0 + BN > key_lo) {  // the causal diagonal (or rows past kv_len) crosses this tile
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    if (key0 + c >= vis_end) x[c] = -INFINITY;
+            }
+            float mt = x[0];
+#pragma unroll
+            for (int c = 1; c < 64; ++c) mt = fmaxf(mt, x[c]);
+            const float m_new = fmaxf(m_ref, mt);
+            const bool need = m_new > m_ref + kRescaleThreshold || (m_ref == -INFINITY && m_new != -INFINITY);
+            if (__any_sync(0xffffffffu, need)) {
+                float alpha = 1.0f;
+                if (need) {
+                    alpha = (m_ref == -INFINITY) ? 0.0f : exp2f(m_ref - m_new);
+                    m_ref = m_new;
+                    l *= alpha;
+                }
+                if (j > 0) {  // rescale the O row once every earlier PV has landed
+                    const int pj = j - 1;
+                    const bool done = tc::mbar_wait(B(B_PV_DONE + (pj & 1)), (pj >> 1) & 1, kWaitLimit);
+                    if (!__all_sync(0xffffffffu, done)) { ok = false; break; }
+                    tc::fence_after_sync();
+#pragma unroll 1
+                    for (int c = 0; c < HD / 32; ++c) {
+                        uint32_t o[32];
+                        tc::tmem_ld32(tmem + lane_base + TM_O + 32 * c, o);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                        tc::tmem_st32(tmem + lane_base + TM_O + 32 * c, o);
+                    }
+                }
+            }
+            uint32_t pk[32];
+            float sum = 0.0f;
+            const bool live = m_ref != -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float a = live ? exp2f(x[2 * c] - m_ref) : 0.0f;
+                const float bq = live ? exp2f(x[2 * c + 1] - m_ref) : 0.0f;
+                const __half2 h = __floats2half2_rn(a, bq);
+                sum += __low2float(h) + __high2float(h);
+                pk[c] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            l += sum;
+            tc::tmem_st32(scol, pk);  // P overwrites the first 32 columns of this S buffer
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
+            tc::mbar_arrive(B(B_P_FULL + b));
+        }
+        if (!ok) flag_timeout();
+        // epilogue: O / l
+        if (ok && n_tiles > 0) {
+            const int pj = n_tiles - 1;
+            const bool done = tc::mbar_wait(B(B_PV_DONE + (pj & 1)), (pj >> 1) & 1, kWaitLimit);
+            if (__all_sync(0xffffffffu, done)) {
+                tc::fence_after_sync();
+                const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
+                float4* dst = reinterpret_cast<float4*>(p.out + ((int64_t)iq * p.n_q_heads + qh) * HD);
+#pragma unroll 1
+                for (int c = 0; c < HD / 32; ++c) {
+                    uint32_t o[32];
+                    tc::tmem_ld32(tmem + lane_base + TM_O + 32 * c, o);
+                    tc::tmem_wait_ld();
+                    if (valid) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            dst[c * 8 + k] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
+                                                         __uint_as_float(o[4 * k + 2]) * inv,
+                                                         __uint_as_float(o[4 * k + 3]) * inv);
+                    }
+                }
+            } else {
+                flag_timeout();
+            }
+        }
+    } else {
+        // ---------------------------------------------------------------- dequantisers
+        const int d = threadIdx.x - 192;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int s = j & 1, use = j >> 1;
+            if (!tc::mbar_wait(B(B_ST_FULL + s), use & 1, kWaitLimit)) { flag_timeout(); break; }
+            if (j >= 2 && !tc::mbar_wait(B(B_KV_EMPTY + s), (use - 1) & 1, kWaitLimit)) { flag_timeout(); break; }
+            const int nk = min(BN, key_hi - j * BN);
+            const uint8_t* st = smem + SM_STAGE + s * STAGE_BYTES;
+            dequant_tile(st + ST_KC, reinterpret_cast<const uint16_t*>(st + ST_KS), smem + SM_KHAT + s * HAT_BYTES,
+                         nk, d);
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive(B(B_KH_FULL + s));
+            dequant_tile(st + ST_VC, reinterpret_cast<const uint16_t*>(st + ST_VS), smem + SM_VHAT + s * HAT_BYTES,
+                         nk, d);
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive(B(B_VH_FULL + s));
+            tc::mbar_arrive(B(B_ST_EMPTY + s));
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 1) tc::tmem_dealloc(tmem, TM_NCOLS);
+}
+
+}  // namespace
+}  // namespace kvq8
+
+extern "C" int attn_prompt_q8(const uint16_t* q, int n_q, int n_q_heads, const kvq8_cache* kv, int kv_len, int q_pos0,
+                              float softmax_scale, float* out, kvq8_stream_t stream) {
+    using namespace kvq8;
+    if (!kv || !q || !out) return KVQ8_ERR_INVALID_ARG;
+    if (!kv->k_codes || !kv->k_scales || !kv->v_codes || !kv->v_scales) return KVQ8_ERR_INVALID_ARG;
+    if (n_q < 1 || n_q_heads < 1 || kv->n_kv_heads < 1 || kv_len < 1 || q_pos0 < 0) return KVQ8_ERR_INVALID_ARG;
+    if (kv_len > kv->capacity) return KVQ8_ERR_INVALID_ARG;
+    if (!(softmax_scale == softmax_scale) || softmax_scale == INFINITY || softmax_scale == -INFINITY)
+        return KVQ8_ERR_INVALID_ARG;
+    if (kv->head_dim != HD || n_q_heads % kv->n_kv_heads) return KVQ8_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(kv->k_codes) || !aligned16(kv->k_scales) ||
+        !aligned16(kv->v_codes) || !aligned16(kv->v_scales))
+        return KVQ8_ERR_MISALIGNED;
+    const int64_t rows = (int64_t)n_q * (n_q_heads / kv->n_kv_heads);
+    const int64_t tiles = (rows + BM - 1) / BM;
+    if (rows > 0x7fffffffLL || tiles > 0x7fffffffLL || kv->n_kv_heads > 65535) return KVQ8_ERR_UNSUPPORTED;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(prompt_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+            cudaSuccess)
+            return KVQ8_ERR_CUDA;
+        attr_set = true;
+    }
+    PromptParams pp;
+    pp.q = q;
+    pp.kc = kv->k_codes;
+    pp.ks = kv->k_scales;
+    pp.vc = kv->v_codes;
+    pp.vs = kv->v_scales;
+    pp.out = out;
+    pp.n_q = n_q;
+    pp.n_q_heads = n_q_heads;
+    pp.group = n_q_heads / kv->n_kv_heads;
+    pp.capacity = kv->capacity;
+    pp.kv_len = kv_len;
+    pp.q_pos0 = q_pos0;
+    pp.rows = (int)rows;
+    pp.scale_log2 = softmax_scale * kLog2e;
+    dim3 grid((unsigned)tiles, (unsigned)kv->n_kv_heads);
+    prompt_attn_kernel<<<grid, kThreads, SMEM_BYTES, (cudaStream_t)stream>>>(pp);
+    return launch_status();
+}
+
+extern "C" int kvq8_device_error(int reset) {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_kvq8_device_error, sizeof v) != cudaSuccess) return -1;
+    if (reset && v) {
+        const unsigned int z = 0;
+        if (cudaMemcpyToSymbol(g_kvq8_device_error, &z, sizeof z) != cudaSuccess) return -1;
+    }
+    return (int)v;
 }

@@ -1,0 +1,97 @@
+"""attn_prompt_q8 (tcgen05) against the fp64 oracle: max|gpu - oracle| / max|oracle| <= 2e-3."""
+import numpy as np
+import pytest
+
+import oracle
+from speculative_verify_attention_gb300 import workloads
+
+from ._util import PROMPT_TOL, build_caches, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(gpu_cache, q16, kv_len, q_pos0, scale):
+    import torch
+
+    from speculative_verify_attention_gb300 import attn_prompt_q8
+    q = torch.from_numpy(np.ascontiguousarray(q16)).cuda()
+    out = torch.full(q.shape, float("nan"), dtype=torch.float32, device="cuda")
+    attn_prompt_q8(q, gpu_cache, kv_len, q_pos0, scale, out=out)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def _check(hq, hkv, L, nq, pos0, seed, capacity=None, sel_every=None):
+    inp = workloads.random_small(seed, hq, hkv, 256, L, nq, q_dtype="f16")
+    gpu, orc = build_caches(inp, capacity=capacity)
+    scale = 1.0 / 16.0
+    got = _run(gpu, inp.q, L, pos0, scale)
+    if sel_every is None:
+        ref = oracle.attention(orc, inp.q, L, pos0, scale)
+        err = rel_err(got, ref)
+    else:
+        rng = np.random.default_rng(seed)
+        sel = [(i, int(rng.integers(hq))) for i in range(0, nq, sel_every)]
+        sel += [(nq - 1, h) for h in range(hq)]
+        ref = oracle.attention(orc, inp.q, L, pos0, scale, sel=sel)
+        err = rel_err(np.stack([got[i, h] for i, h in sel]), ref)
+    assert np.all(np.isfinite(got)), "non-finite output"
+    assert err <= PROMPT_TOL, f"rel err {err:.3e}"
+    return err
+
+
+@pytest.mark.parametrize("hq,hkv,L,nq,pos0", [
+    (12, 1, 64, 11, 53),       # one tile, 132 rows over two CTAs
+    (12, 1, 200, 50, 150),     # ragged last tile
+    (12, 1, 1, 1, 0),          # a single key
+    (4, 1, 333, 40, 290),      # group 4, rows crossing tiles
+    (2, 2, 130, 130, 0),       # MHA, pure causal from position 0
+    (24, 2, 512, 64, 448),     # two KV heads
+    (12, 1, 300, 60, 280),     # rows past kv_len see kv_len keys
+])
+def test_small_shapes(lib, hq, hkv, L, nq, pos0):
+    _check(hq, hkv, L, nq, pos0, seed=hq * 100 + L)
+
+
+def test_capacity_larger_than_kv_len(lib):
+    _check(12, 1, 700, 100, 600, seed=77, capacity=2048)
+
+
+def test_medium_chunk(lib):
+    _check(12, 1, 4096, 512, 3584, seed=78, sel_every=3)
+
+
+def test_full_prompt_workload_sampled(lib):
+    import torch
+
+    w = workloads.PROMPT
+    inp = workloads.make_inputs(w)
+    gpu, orc = build_caches(inp, garbage_tail=False)
+    got = _run(gpu, inp.q, w.kv_len, w.q_pos0, w.softmax_scale)
+    rng = np.random.default_rng(5)
+    sel = [(int(i), int(rng.integers(w.n_q_heads))) for i in rng.integers(0, w.n_q, 40)]
+    sel += [(0, h) for h in range(w.n_q_heads)] + [(w.n_q - 1, h) for h in range(w.n_q_heads)]
+    ref = oracle.attention(orc, inp.q, w.kv_len, w.q_pos0, w.softmax_scale, sel=sel)
+    err = rel_err(np.stack([got[i, h] for i, h in sel]), ref)
+    assert np.all(np.isfinite(got))
+    assert err <= PROMPT_TOL, f"rel err {err:.3e}"
+    from speculative_verify_attention_gb300 import kvq8_device_error
+    assert kvq8_device_error(reset=True) == 0
+    del torch
+
+
+def test_prompt_rejects_bad_arguments(lib):
+    import torch
+
+    from speculative_verify_attention_gb300 import KVCacheQ8, KVQ8Error, attn_prompt_q8
+    q = torch.zeros((4, 12, 256), dtype=torch.float16, device="cuda")
+    with pytest.raises(KVQ8Error) as e:       # head_dim 128 has no prompt kernel
+        attn_prompt_q8(torch.zeros((4, 4, 128), dtype=torch.float16, device="cuda"), KVCacheQ8(1, 128, 64), 64, 60,
+                       0.1)
+    assert e.value.status == 2
+    with pytest.raises(KVQ8Error) as e:       # kv_len beyond capacity
+        attn_prompt_q8(q, KVCacheQ8(1, 256, 64), 65, 61, 0.1)
+    assert e.value.status == 1
+    with pytest.raises(KVQ8Error) as e:       # 12 q heads over 5 kv heads
+        attn_prompt_q8(q, KVCacheQ8(5, 256, 64), 64, 60, 0.1)
+    assert e.value.status == 2
