@@ -477,6 +477,7 @@ def main():
     ap.add_argument("--no-prompt", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="per-cell verify sweep instead of the headline line")
+    ap.add_argument("--prompt-only", action="store_true", help="time only the prompt-chunk kernel")
     ap.add_argument("--sweep-filter", default="")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -484,6 +485,14 @@ def main():
     world, rank, local = _dist()
     if args.sweep:
         sweep(args)
+        return 0
+    if args.prompt_only:
+        import torch
+
+        import __graft_entry__
+        __graft_entry__.build()
+        hbm_peak, bf16_peak, _ = _peaks()
+        print(json.dumps(prompt_bench(args, torch.device("cuda", 0), bf16_peak * 0.951)), flush=True)
         return 0
     if args.impl == "reference":
         return run_reference(args, world, rank)
