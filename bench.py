@@ -373,15 +373,18 @@ def run_native(args, world, rank, local):
 def prompt_bench(args, dev, fp16_peak):
     import torch
 
-    from speculative_verify_attention_gb300 import KVCacheQ8, KVQ8Error, attn_prompt_q8, workloads
+    from speculative_verify_attention_gb300 import (KVCacheQ8, KVQ8Error, attn_prompt_q8,
+                                                    attn_prompt_q8_workspace_bytes, workloads)
     w = workloads.PROMPT
     inp = workloads.make_inputs(w)
     c = KVCacheQ8(w.n_kv_heads, w.head_dim, w.kv_len, device=dev)
     c.append(torch.from_numpy(inp.k).to(dev), torch.from_numpy(inp.v).to(dev), 0)
     q = torch.from_numpy(inp.q).to(dev)
     out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    ws = torch.empty(attn_prompt_q8_workspace_bytes(w.n_q, w.n_q_heads, w.head_dim, w.kv_len, w.q_pos0,
+                                                    w.n_kv_heads), dtype=torch.uint8, device=dev)
     try:
-        attn_prompt_q8(q, c, w.kv_len, w.q_pos0, w.softmax_scale, out=out)
+        attn_prompt_q8(q, c, w.kv_len, w.q_pos0, w.softmax_scale, out=out, workspace=ws)
     except KVQ8Error as e:
         return {"unavailable": str(e)}
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
@@ -391,7 +394,7 @@ def prompt_bench(args, dev, fp16_peak):
         flush.fill_(float(i))
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        attn_prompt_q8(q, c, w.kv_len, w.q_pos0, w.softmax_scale, out=out)
+        attn_prompt_q8(q, c, w.kv_len, w.q_pos0, w.softmax_scale, out=out, workspace=ws)
         b.record()
         torch.cuda.synchronize()
         if i >= 2:

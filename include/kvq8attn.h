@@ -115,22 +115,32 @@ int attn_verify_q8(const float* q, int n_rows, int n_q_heads, const kvq8_cache* 
 int attn_combine(const float* part_o, const float* part_ml, int n_split, int rows, int head_dim,
                  float* out, kvq8_stream_t stream);
 
+/* Bytes of workspace attn_prompt_q8 needs for this shape (on the current device). */
+size_t attn_prompt_q8_workspace_bytes(int n_q, int n_q_heads, int head_dim, int kv_len, int q_pos0,
+                                      int n_kv_heads);
+
 /*
  * attn_prompt_q8 -- prompt-chunk attention: many query rows over a long Q8_0 context.
- *   q   : fp16 bits [n_q][n_q_heads][head_dim], head_dim 256
- *   kv  : the cache (head_dim 256, any n_kv_heads dividing n_q_heads)
- *   out : fp32 [n_q][n_q_heads][head_dim]
+ *   q        : fp16 bits [n_q][n_q_heads][head_dim], head_dim 256
+ *   kv       : the cache (head_dim 256, any n_kv_heads dividing n_q_heads)
+ *   out      : fp32 [n_q][n_q_heads][head_dim]
+ *   workspace: device scratch of at least attn_prompt_q8_workspace_bytes(...) bytes,
+ *              caller-owned; holds the per-slice partials merged by the second kernel
+ *   softmax_scale must be > 0.
  * Row i sees keys n <= q_pos0 + i, n < kv_len.  K and V are dequantised on chip to fp16
  * (code * scale, one rounding) and contracted on the tcgen05 tensor cores with fp32
- * accumulation in tensor memory; p enters the PV product as fp16.  Tiles past the last
- * row's causal bound are skipped.  Within 2e-3 of the fp64 oracle (max |err| / max |out|)
- * for values inside the fp16 range.  One 128-row tile of (query, head) pairs of one KV head
- * per thread block; every internal wait is bounded, and a timeout sets the flag that
+ * accumulation in tensor memory; p enters the PV product as fp16.  The work -- 64-key
+ * tiles of 128-row tiles of (query, head) pairs of every KV head -- is cut into one equal
+ * contiguous share per SM (a persistent grid); each share writes partials that the
+ * log-sum-exp combine merges into `out`.  Tiles past a row tile's causal bound are
+ * skipped.  Within 2e-3 of the fp64 oracle (max |err| / max |out|) for values inside the
+ * fp16 range.  Every internal wait is bounded; a timeout sets the flag that
  * kvq8_device_error reports (the output is then undefined).
  * Source: "gfx12 WMMA kernel for the int8-KV QSA prompt attention", How and Measurements.
  */
 int attn_prompt_q8(const uint16_t* q, int n_q, int n_q_heads, const kvq8_cache* kv, int kv_len,
-                   int q_pos0, float softmax_scale, float* out, kvq8_stream_t stream);
+                   int q_pos0, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                   kvq8_stream_t stream);
 
 /*
  * attn_verify_q8_noalloc -- attn_verify_q8 for callers that cannot allocate device memory.

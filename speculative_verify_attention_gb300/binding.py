@@ -28,7 +28,7 @@ KVQ8_ERR_CUDA = 5
 
 # Entry points declared in include/kvq8attn.h.
 EXPORTED = ("kvq8_quantize", "attn_verify_q8_workspace_bytes", "attn_verify_q8", "attn_combine",
-            "attn_prompt_q8", "attn_verify_q8_noalloc", "kvq8_device_error", "kvq8_status_str")
+            "attn_prompt_q8_workspace_bytes", "attn_prompt_q8", "attn_verify_q8_noalloc", "kvq8_device_error", "kvq8_status_str")
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 
@@ -68,7 +68,9 @@ def load_library():
         lib.attn_verify_q8.restype = i32
         lib.attn_combine.argtypes = [vp, vp, i32, i32, i32, vp, vp]
         lib.attn_combine.restype = i32
-        lib.attn_prompt_q8.argtypes = [vp, i32, i32, cp, i32, i32, f32, vp, vp]
+        lib.attn_prompt_q8_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.attn_prompt_q8_workspace_bytes.restype = sz
+        lib.attn_prompt_q8.argtypes = [vp, i32, i32, cp, i32, i32, f32, vp, vp, sz, vp]
         lib.attn_prompt_q8.restype = i32
         lib.attn_verify_q8_noalloc.argtypes = [vp, i32, i32, cp, i32, i32, f32, vp, i32, vp]
         lib.attn_verify_q8_noalloc.restype = i32
@@ -190,16 +192,26 @@ def attn_combine(part_o: torch.Tensor, part_ml: torch.Tensor, out: torch.Tensor 
     return out
 
 
+def attn_prompt_q8_workspace_bytes(n_q: int, n_q_heads: int, head_dim: int, kv_len: int, q_pos0: int,
+                                   n_kv_heads: int) -> int:
+    return int(load_library().attn_prompt_q8_workspace_bytes(n_q, n_q_heads, head_dim, kv_len, q_pos0, n_kv_heads))
+
+
 def attn_prompt_q8(q: torch.Tensor, cache: KVCacheQ8, kv_len: int, q_pos0: int, softmax_scale: float,
-                   out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                   out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
     """Prompt-chunk attention of fp16 q [n_q][Hq][hd] over the cache; returns fp32 [n_q][Hq][hd]."""
     _need(q, "q", torch.float16)
     n_q, n_q_heads, head_dim = q.shape
     if out is None:
         out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
     _need(out, "out", torch.float32)
+    if workspace is None:
+        nbytes = attn_prompt_q8_workspace_bytes(n_q, n_q_heads, head_dim, kv_len, q_pos0, cache.n_kv_heads)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
     st = load_library().attn_prompt_q8(_ptr(q), n_q, n_q_heads, ctypes.byref(cache.struct()), int(kv_len),
-                                       int(q_pos0), float(softmax_scale), _ptr(out), _stream(stream))
+                                       int(q_pos0), float(softmax_scale), _ptr(out), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream))
     _check("attn_prompt_q8", st)
     return out
 

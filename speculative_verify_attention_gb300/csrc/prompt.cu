@@ -31,14 +31,20 @@
 __device__ unsigned int g_kvq8_device_error = 0;
 
 namespace kvq8 {
+
+int launch_combine(const float* part_o, const float* part_ml, int n_split, int rows, int head_dim, float* out,
+                   cudaStream_t stream);
+
 namespace {
 
 constexpr int HD = 256;
 constexpr int BM = 128;
 constexpr int BN = 64;
-constexpr int kThreads = 320;
+constexpr int kSoftWarp0 = 2, kDeqWarp0 = 6, kDeqThreads = 256;
+constexpr int kThreads = (kDeqWarp0 + kDeqThreads / 32) * 32;   // 448
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kMaxSegments = 8;
 
 // tensor memory columns
 constexpr uint32_t TM_Q = 0, TM_O = 128, TM_S0 = 384, TM_NCOLS = 512;
@@ -51,10 +57,11 @@ constexpr int SM_STAGE = 131072;             // 2 x 34 KB: K codes 16K | V codes
 constexpr int STAGE_BYTES = 34816;
 constexpr int ST_KC = 0, ST_VC = 16384, ST_KS = 32768, ST_VS = 33792;
 constexpr int SM_BAR = SM_STAGE + 2 * STAGE_BYTES;
-enum { B_ST_FULL = 0, B_ST_EMPTY = 2, B_KH_FULL = 4, B_VH_FULL = 6, B_KV_EMPTY = 8, B_S_FULL = 10, B_P_FULL = 12,
-       B_PV_DONE = 14, B_Q_READY = 16, B_COUNT = 17 };
+enum { B_ST_FULL = 0, B_ST_EMPTY = 2, B_K_FULL = 4, B_V_FULL = 6, B_K_EMPTY = 8, B_V_EMPTY = 10, B_S_FULL = 12,
+       B_P_FULL = 14, B_PV_DONE = 16, B_Q_READY = 18, B_COUNT = 19 };
 constexpr int SM_TMEM_SLOT = SM_BAR + B_COUNT * 8;
-constexpr int SMEM_BYTES = SM_TMEM_SLOT + 16;
+constexpr int SM_SEG = SM_TMEM_SLOT + 16;    // this CTA's work segments (written by thread 0)
+constexpr int SMEM_BYTES = SM_SEG + 8 * 5 * 4 + 16;
 
 constexpr uint32_t IDESC_QK = tc::idesc_f16_f32(BM, BN, false);
 constexpr uint32_t IDESC_PV = tc::idesc_f16_f32(BM, HD, true);
@@ -65,20 +72,79 @@ struct PromptParams {
     const uint16_t* ks;
     const int8_t* vc;
     const uint16_t* vs;
-    float* out;
-    int n_q, n_q_heads, group, capacity, kv_len, q_pos0, rows;
+    float* part_o;     // [n_parts][n_q * n_q_heads][HD]
+    float2* part_ml;   // [n_parts][n_q * n_q_heads]
+    int n_q, n_q_heads, group, capacity, kv_len, q_pos0, rows, n_mtiles, n_items, n_parts;
+    long long units;   // total 64-key tiles over all (KV head, row tile) items
     float scale_log2;
 };
 
+// Geometry of one work item: rows [r0, r0 + rows_here) of KV head kvh see keys < key_hi;
+// every row sees at least the keys < key_lo.
+struct Item {
+    int kvh, r0, rows_here, key_lo, key_hi, n_tiles;
+};
+
+__host__ __device__ inline Item item_geometry(int it, int n_mtiles, int rows, int group, int kv_len, int q_pos0) {
+    Item g;
+    g.kvh = it / n_mtiles;
+    const int m = it - g.kvh * n_mtiles;
+    g.r0 = m * BM;
+    g.rows_here = rows - g.r0 < BM ? rows - g.r0 : BM;
+    const long long hi = (long long)q_pos0 + (g.r0 + g.rows_here - 1) / group + 1;
+    const long long lo = (long long)q_pos0 + g.r0 / group + 1;
+    g.key_hi = (int)(hi < kv_len ? hi : kv_len);
+    g.key_lo = (int)(lo < kv_len ? lo : kv_len);
+    g.n_tiles = (g.key_hi + BN - 1) / BN;
+    return g;
+}
+
+// Stream-K split: CTA c of G owns the units [floor(c U / G), floor((c+1) U / G)).
+__host__ __device__ inline long long unit_begin(long long c, long long U, long long G) { return c * U / G; }
+// First CTA whose range contains unit u.
+__host__ __device__ inline long long cta_of_unit(long long u, long long U, long long G) { return ((u + 1) * G - 1) / U; }
+
+struct Segment {
+    int item, t0, t1, part, last;  // tiles [t0, t1) of item; part index; last = owns the item's final tile
+};
+
+__device__ int cta_segments(const PromptParams& p, int c, int G, Segment* seg) {
+    const long long u0 = unit_begin(c, p.units, G), u1 = unit_begin(c + 1, p.units, G);
+    int n = 0;
+    long long s = 0;
+    for (int it = 0; it < p.n_items && s < u1 && n < kMaxSegments; ++it) {
+        const Item g = item_geometry(it, p.n_mtiles, p.rows, p.group, p.kv_len, p.q_pos0);
+        const long long e = s + g.n_tiles;
+        if (e > u0) {
+            const long long a = s > u0 ? s : u0, b = e < u1 ? e : u1;
+            seg[n].item = it;
+            seg[n].t0 = (int)(a - s);
+            seg[n].t1 = (int)(b - s);
+            seg[n].part = (int)(c - cta_of_unit(s, p.units, G));
+            seg[n].last = (b == e) ? 1 : 0;
+            ++n;
+        }
+        s = e;
+    }
+    return n;
+}
+
 __device__ __forceinline__ void flag_timeout() { atomicOr(&g_kvq8_device_error, 1u); }
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // Convert one 64-key plane tile (codes + scales in staging) into the swizzled fp16 tile:
 // element (key n, dim j) -> atom j/64, row n, 16-byte chunk ((j%64)/8) ^ (n%8).
+// 256 threads, 4 chunks of 16 codes each.
 __device__ __forceinline__ void dequant_tile(const uint8_t* codes, const uint16_t* scales, uint8_t* hat, int nk,
                                              int d) {
-#pragma unroll 2
-    for (int k = 0; k < 8; ++k) {
-        const int c = d + 128 * k;  // 1024 chunks of 16 codes
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int c = d + kDeqThreads * k;  // 1024 chunks of 16 codes
         const int n = c >> 4, j16 = c & 15;
         uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
         if (n < nk) {
@@ -109,24 +175,23 @@ __device__ __forceinline__ void dequant_tile(const uint8_t* codes, const uint16_
 __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kvh = blockIdx.y;
-    const int r0 = blockIdx.x * BM;
-    const int rows_here = min(BM, p.rows - r0);
-    const int key_hi = min(p.kv_len, p.q_pos0 + (r0 + rows_here - 1) / p.group + 1);
-    const int key_lo = min(p.kv_len, p.q_pos0 + r0 / p.group + 1);
-    const int n_tiles = (key_hi + BN - 1) / BN;
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar = sbase + SM_BAR;
     auto B = [&](int id) { return bar + 8u * (uint32_t)id; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM_TMEM_SLOT);
 
+    Segment* seg = reinterpret_cast<Segment*>(smem + SM_SEG);
+    int* n_seg_slot = reinterpret_cast<int*>(smem + SM_SEG + kMaxSegments * (int)sizeof(Segment));
+
     if (threadIdx.x == 0) {
+        *n_seg_slot = cta_segments(p, blockIdx.x, gridDim.x, seg);
         for (int s = 0; s < 2; ++s) {
             tc::mbar_init(B(B_ST_FULL + s), 1);
-            tc::mbar_init(B(B_ST_EMPTY + s), 128);
-            tc::mbar_init(B(B_KH_FULL + s), 128);
-            tc::mbar_init(B(B_VH_FULL + s), 128);
-            tc::mbar_init(B(B_KV_EMPTY + s), 1);
+            tc::mbar_init(B(B_ST_EMPTY + s), kDeqThreads);
+            tc::mbar_init(B(B_K_FULL + s), kDeqThreads);
+            tc::mbar_init(B(B_V_FULL + s), kDeqThreads);
+            tc::mbar_init(B(B_K_EMPTY + s), 1);
+            tc::mbar_init(B(B_V_EMPTY + s), 1);
             tc::mbar_init(B(B_S_FULL + s), 1);
             tc::mbar_init(B(B_P_FULL + s), 128);
             tc::mbar_init(B(B_PV_DONE + s), 1);
@@ -139,221 +204,245 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptPa
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    const int n_seg = *n_seg_slot;
 
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
-            int issued = 0;
-            for (int j = 0; j < n_tiles; ++j) {
-                const int s = j & 1, use = j >> 1;
-                if (j >= 2 && !tc::mbar_wait(B(B_ST_EMPTY + s), (use - 1) & 1, kWaitLimit)) {
-                    flag_timeout();
-                    break;
+            int j = 0;
+            bool ok = true;
+            for (int si = 0; ok && si < n_seg; ++si) {
+                const Item g = item_geometry(seg[si].item, p.n_mtiles, p.rows, p.group, p.kv_len, p.q_pos0);
+                for (int t = seg[si].t0; t < seg[si].t1; ++t, ++j) {
+                    const int s = j & 1, use = j >> 1;
+                    if (j >= 2 && !tc::mbar_wait(B(B_ST_EMPTY + s), (use - 1) & 1, kWaitLimit)) { ok = false; break; }
+                    const int key0 = t * BN;
+                    const int nk = min(BN, g.key_hi - key0);
+                    const int64_t row0 = (int64_t)g.kvh * p.capacity + key0;
+                    const uint32_t st = sbase + SM_STAGE + s * STAGE_BYTES;
+                    tc::mbar_arrive_expect_tx(B(B_ST_FULL + s), (uint32_t)(nk * (2 * HD + 2 * (HD / 16))));
+                    tc::bulk_g2s(st + ST_KC, p.kc + row0 * HD, nk * HD, B(B_ST_FULL + s));
+                    tc::bulk_g2s(st + ST_VC, p.vc + row0 * HD, nk * HD, B(B_ST_FULL + s));
+                    tc::bulk_g2s(st + ST_KS, p.ks + row0 * (HD / 32), nk * (HD / 16), B(B_ST_FULL + s));
+                    tc::bulk_g2s(st + ST_VS, p.vs + row0 * (HD / 32), nk * (HD / 16), B(B_ST_FULL + s));
                 }
-                const int key0 = j * BN;
-                const int nk = min(BN, key_hi - key0);
-                const int64_t row0 = (int64_t)kvh * p.capacity + key0;
-                const uint32_t st = sbase + SM_STAGE + s * STAGE_BYTES;
-                tc::mbar_arrive_expect_tx(B(B_ST_FULL + s), (uint32_t)(nk * (2 * HD + 2 * (HD / 16))));
-                tc::bulk_g2s(st + ST_KC, p.kc + row0 * HD, nk * HD, B(B_ST_FULL + s));
-                tc::bulk_g2s(st + ST_VC, p.vc + row0 * HD, nk * HD, B(B_ST_FULL + s));
-                tc::bulk_g2s(st + ST_KS, p.ks + row0 * (HD / 32), nk * (HD / 16), B(B_ST_FULL + s));
-                tc::bulk_g2s(st + ST_VS, p.vs + row0 * (HD / 32), nk * (HD / 16), B(B_ST_FULL + s));
-                issued = j + 1;
             }
+            if (!ok) flag_timeout();
             // never leave the block while a copy into its shared memory is in flight
-            for (int j = max(0, issued - 2); j < issued; ++j)
-                if (!tc::mbar_wait(B(B_ST_FULL + (j & 1)), (j >> 1) & 1, kWaitLimit)) flag_timeout();
+            for (int i = max(0, j - 2); i < j; ++i)
+                if (!tc::mbar_wait(B(B_ST_FULL + (i & 1)), (i >> 1) & 1, kWaitLimit)) flag_timeout();
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            bool ok = tc::mbar_wait(B(B_Q_READY), 0, kWaitLimit);
-            int pv_issued = 0;
-            auto issue_pv = [&](int jj) -> bool {
+            bool ok = true;
+            int j = 0, pv_issued = 0;
+            auto issue_pv = [&](int jj, bool first) -> bool {
                 const int bb = jj & 1, u = jj >> 1;
                 if (!tc::mbar_wait(B(B_P_FULL + bb), u & 1, kWaitLimit)) return false;
-                if (!tc::mbar_wait(B(B_VH_FULL + bb), u & 1, kWaitLimit)) return false;
+                if (!tc::mbar_wait(B(B_V_FULL + bb), u & 1, kWaitLimit)) return false;
                 tc::fence_after_sync();
                 const uint32_t vhat = sbase + SM_VHAT + bb * HAT_BYTES;
                 const uint32_t pcol = tmem + TM_S0 + bb * BN;
 #pragma unroll
                 for (int ks = 0; ks < BN / 16; ++ks)
                     tc::mma_ts(tmem + TM_O, pcol + ks * 8, tc::smem_desc_sw128(vhat + ks * 2048, BN * 128, 1024),
-                               IDESC_PV, (jj > 0 || ks > 0) ? 1u : 0u);
+                               IDESC_PV, (!first || ks > 0) ? 1u : 0u);
                 tc::mma_commit(B(B_PV_DONE + bb));
-                tc::mma_commit(B(B_KV_EMPTY + bb));
+                tc::mma_commit(B(B_V_EMPTY + bb));
                 pv_issued = jj + 1;
                 return true;
             };
-            if (ok) tc::fence_after_sync();
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                const int b = j & 1, use = j >> 1;
-                if (!tc::mbar_wait(B(B_KH_FULL + b), use & 1, kWaitLimit)) { ok = false; break; }
-                if (j >= 2 && !tc::mbar_wait(B(B_PV_DONE + b), (use - 1) & 1, kWaitLimit)) { ok = false; break; }
+            for (int si = 0; ok && si < n_seg; ++si) {
+                if (!tc::mbar_wait(B(B_Q_READY), si & 1, kWaitLimit)) { ok = false; break; }
                 tc::fence_after_sync();
-                const uint32_t khat = sbase + SM_KHAT + b * HAT_BYTES;
+                const int jfirst = j;
+                for (int t = seg[si].t0; t < seg[si].t1; ++t, ++j) {
+                    const int b = j & 1, use = j >> 1;
+                    if (!tc::mbar_wait(B(B_K_FULL + b), use & 1, kWaitLimit)) { ok = false; break; }
+                    if (j >= 2 && !tc::mbar_wait(B(B_PV_DONE + b), (use - 1) & 1, kWaitLimit)) { ok = false; break; }
+                    tc::fence_after_sync();
+                    const uint32_t khat = sbase + SM_KHAT + b * HAT_BYTES;
 #pragma unroll
-                for (int ks = 0; ks < HD / 16; ++ks)
-                    tc::mma_ts(tmem + TM_S0 + b * BN, tmem + TM_Q + ks * 8,
-                               tc::smem_desc_sw128(khat + (ks >> 2) * (BN * 128) + (ks & 3) * 32, 16, 1024),
-                               IDESC_QK, ks > 0 ? 1u : 0u);
-                tc::mma_commit(B(B_S_FULL + b));
-                if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+                    for (int ks = 0; ks < HD / 16; ++ks)
+                        tc::mma_ts(tmem + TM_S0 + b * BN, tmem + TM_Q + ks * 8,
+                                   tc::smem_desc_sw128(khat + (ks >> 2) * (BN * 128) + (ks & 3) * 32, 16, 1024),
+                                   IDESC_QK, ks > 0 ? 1u : 0u);
+                    tc::mma_commit(B(B_S_FULL + b));
+                    tc::mma_commit(B(B_K_EMPTY + b));
+                    if (j > jfirst && !issue_pv(j - 1, j - 1 == jfirst)) { ok = false; break; }
+                }
+                if (ok && j > jfirst && !issue_pv(j - 1, j - 1 == jfirst)) ok = false;
             }
-            if (ok && n_tiles > 0 && !issue_pv(n_tiles - 1)) ok = false;
             if (!ok) flag_timeout();
-            // the tensor memory is released only after the last committed MMA has completed
+            // tensor memory is released only after the last committed MMA has completed
             if (pv_issued > 0 &&
                 !tc::mbar_wait(B(B_PV_DONE + ((pv_issued - 1) & 1)), ((pv_issued - 1) >> 1) & 1, kWaitLimit))
                 flag_timeout();
         }
         __syncwarp();
-    } else if (warp < 6) {
+    } else if (warp < kDeqWarp0) {
         // ---------------------------------------------------------------- softmax (one row per thread)
         const int quad = warp & 3;
         const int r = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        const bool valid = r < rows_here;
-        const int rr = r0 + r;
-        const int iq = valid ? rr / p.group : 0;
-        const int qh = kvh * p.group + (valid ? rr - iq * p.group : 0);
-        const int vis_end = valid ? min(p.kv_len, p.q_pos0 + iq + 1) : 0;
-        // Q row -> TMEM (fp16 pairs, A operand of S = Q K^T)
-        {
-            const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)iq * p.n_q_heads + qh) * HD);
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t w[32];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                    if (valid) v = __ldg(src + c * 8 + k);
-                    w[4 * k] = v.x;
-                    w[4 * k + 1] = v.y;
-                    w[4 * k + 2] = v.z;
-                    w[4 * k + 3] = v.w;
-                }
-                tc::tmem_st32(tmem + lane_base + TM_Q + 32 * c, w);
-            }
-            tc::tmem_wait_st();
-            tc::fence_before_sync();
-            tc::mbar_arrive(B(B_Q_READY));
-        }
-        float m_ref = -INFINITY, l = 0.0f;
+        const float cs = p.scale_log2;
+        const int rows_out = p.n_q * p.n_q_heads;
         bool ok = true;
-        for (int j = 0; j < n_tiles; ++j) {
-            const int b = j & 1, use = j >> 1;
-            const bool ready = tc::mbar_wait(B(B_S_FULL + b), use & 1, kWaitLimit);
-            if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }
-            tc::fence_after_sync();
-            uint32_t s0[32], s1[32];
-            const uint32_t scol = tmem + lane_base + TM_S0 + b * BN;
-            tc::tmem_ld32(scol, s0);
-            tc::tmem_ld32(scol + 32, s1);
-            tc::tmem_wait_ld();
-            float x[64];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                x[c] = __uint_as_float(s0[c]) * p.scale_log2;
-                x[32 + c] = __uint_as_float(s1[c]) * p.scale_log2;
-            }
-            const int key0 = j * BN;
-            if (key0 + BN > key_lo) {  // the causal diagonal (or rows past kv_len) crosses this tile
-#pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (key0 + c >= vis_end) x[c] = -INFINITY;
-            }
-            float mt = x[0];
-#pragma unroll
-            for (int c = 1; c < 64; ++c) mt = fmaxf(mt, x[c]);
-            const float m_new = fmaxf(m_ref, mt);
-            const bool need = m_new > m_ref + kRescaleThreshold || (m_ref == -INFINITY && m_new != -INFINITY);
-            if (__any_sync(0xffffffffu, need)) {
-                float alpha = 1.0f;
-                if (need) {
-                    alpha = (m_ref == -INFINITY) ? 0.0f : exp2f(m_ref - m_new);
-                    m_ref = m_new;
-                    l *= alpha;
-                }
-                if (j > 0) {  // rescale the O row once every earlier PV has landed
-                    const int pj = j - 1;
-                    const bool done = tc::mbar_wait(B(B_PV_DONE + (pj & 1)), (pj >> 1) & 1, kWaitLimit);
-                    if (!__all_sync(0xffffffffu, done)) { ok = false; break; }
-                    tc::fence_after_sync();
+        int j = 0;
+        for (int si = 0; ok && si < n_seg; ++si) {
+            const Item g = item_geometry(seg[si].item, p.n_mtiles, p.rows, p.group, p.kv_len, p.q_pos0);
+            const bool valid = r < g.rows_here;
+            const int rr = g.r0 + r;
+            const int iq = valid ? rr / p.group : 0;
+            const int qh = g.kvh * p.group + (valid ? rr - iq * p.group : 0);
+            const int vis_end = valid ? min(p.kv_len, p.q_pos0 + iq + 1) : 0;
+            // Q row -> TMEM (fp16 pairs, A operand of S = Q K^T); the previous segment's
+            // epilogue has already waited for every MMA that read the old Q.
+            {
+                const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)iq * p.n_q_heads + qh) * HD);
 #pragma unroll 1
-                    for (int c = 0; c < HD / 32; ++c) {
-                        uint32_t o[32];
-                        tc::tmem_ld32(tmem + lane_base + TM_O + 32 * c, o);
-                        tc::tmem_wait_ld();
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t w[32];
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                        tc::tmem_st32(tmem + lane_base + TM_O + 32 * c, o);
+                    for (int k = 0; k < 8; ++k) {
+                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                        if (valid) v = __ldg(src + c * 8 + k);
+                        w[4 * k] = v.x;
+                        w[4 * k + 1] = v.y;
+                        w[4 * k + 2] = v.z;
+                        w[4 * k + 3] = v.w;
+                    }
+                    tc::tmem_st32(tmem + lane_base + TM_Q + 32 * c, w);
+                }
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                tc::mbar_arrive(B(B_Q_READY));
+            }
+            float m_ref = -INFINITY, l = 0.0f;
+            for (int t = seg[si].t0; t < seg[si].t1; ++t, ++j) {
+                const int b = j & 1, use = j >> 1;
+                const bool ready = tc::mbar_wait(B(B_S_FULL + b), use & 1, kWaitLimit);
+                if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }
+                tc::fence_after_sync();
+                uint32_t s0[32], s1[32];
+                const uint32_t scol = tmem + lane_base + TM_S0 + b * BN;
+                tc::tmem_ld32(scol, s0);
+                tc::tmem_ld32(scol + 32, s1);
+                tc::tmem_wait_ld();
+                float x[64];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    x[c] = __uint_as_float(s0[c]);
+                    x[32 + c] = __uint_as_float(s1[c]);
+                }
+                const int key0 = t * BN;
+                if (key0 + BN > g.key_lo) {  // the causal diagonal (or rows past kv_len) crosses this tile
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if (key0 + c >= vis_end) x[c] = -INFINITY;
+                }
+                float mt = x[0];
+#pragma unroll
+                for (int c = 1; c < 64; ++c) mt = fmaxf(mt, x[c]);
+                const float m_new = fmaxf(m_ref, mt * cs);
+                const bool need = m_new > m_ref + kRescaleThreshold || (m_ref == -INFINITY && m_new != -INFINITY);
+                if (__any_sync(0xffffffffu, need)) {
+                    float alpha = 1.0f;
+                    if (need) {
+                        alpha = (m_ref == -INFINITY) ? 0.0f : ex2_approx(m_ref - m_new);
+                        m_ref = m_new;
+                        l *= alpha;
+                    }
+                    if (t > seg[si].t0) {  // rescale the O row once every earlier PV has landed
+                        const int pj = j - 1;
+                        const bool done = tc::mbar_wait(B(B_PV_DONE + (pj & 1)), (pj >> 1) & 1, kWaitLimit);
+                        if (!__all_sync(0xffffffffu, done)) { ok = false; break; }
+                        tc::fence_after_sync();
+#pragma unroll 1
+                        for (int c = 0; c < HD / 32; ++c) {
+                            uint32_t o[32];
+                            tc::tmem_ld32(tmem + lane_base + TM_O + 32 * c, o);
+                            tc::tmem_wait_ld();
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                            tc::tmem_st32(tmem + lane_base + TM_O + 32 * c, o);
+                        }
                     }
                 }
-            }
-            uint32_t pk[32];
-            float sum = 0.0f;
-            const bool live = m_ref != -INFINITY;
+                uint32_t pk[32];
+                float sum = 0.0f;
+                const bool live = m_ref != -INFINITY;
+                const float neg = live ? -m_ref : 0.0f;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const float a = live ? exp2f(x[2 * c] - m_ref) : 0.0f;
-                const float bq = live ? exp2f(x[2 * c + 1] - m_ref) : 0.0f;
-                const __half2 h = __floats2half2_rn(a, bq);
-                sum += __low2float(h) + __high2float(h);
-                pk[c] = *reinterpret_cast<const uint32_t*>(&h);
+                for (int c = 0; c < 32; ++c) {
+                    const float a = live ? ex2_approx(fmaf(x[2 * c], cs, neg)) : 0.0f;
+                    const float bq = live ? ex2_approx(fmaf(x[2 * c + 1], cs, neg)) : 0.0f;
+                    sum += a + bq;
+                    const __half2 h = __floats2half2_rn(a, bq);
+                    pk[c] = *reinterpret_cast<const uint32_t*>(&h);
+                }
+                l += sum;
+                tc::tmem_st32(scol, pk);  // P overwrites the first 32 columns of this S buffer
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                tc::mbar_arrive(B(B_P_FULL + b));
             }
-            l += sum;
-            tc::tmem_st32(scol, pk);  // P overwrites the first 32 columns of this S buffer
-            tc::tmem_wait_st();
-            tc::fence_before_sync();
-            tc::mbar_arrive(B(B_P_FULL + b));
+            if (!ok) break;
+            // epilogue: the unnormalised partial (o, m, l) of this segment
+            const int pj = j - 1;
+            const bool done = tc::mbar_wait(B(B_PV_DONE + (pj & 1)), (pj >> 1) & 1, kWaitLimit);
+            if (!__all_sync(0xffffffffu, done)) { ok = false; break; }
+            tc::fence_after_sync();
+            const int64_t orow = (int64_t)iq * p.n_q_heads + qh;
+            float4* dst = reinterpret_cast<float4*>(p.part_o + ((int64_t)seg[si].part * rows_out + orow) * HD);
+#pragma unroll 1
+            for (int c = 0; c < HD / 32; ++c) {
+                uint32_t o[32];
+                tc::tmem_ld32(tmem + lane_base + TM_O + 32 * c, o);
+                tc::tmem_wait_ld();
+                if (valid) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        dst[c * 8 + k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                                     __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+                }
+            }
+            if (valid) {
+                p.part_ml[(int64_t)seg[si].part * rows_out + orow] =
+                    make_float2(m_ref == -INFINITY ? -INFINITY : m_ref * kLn2, l);
+                if (seg[si].last)  // the slots of parts this item does not have hold an empty partial
+                    for (int q2 = seg[si].part + 1; q2 < p.n_parts; ++q2)
+                        p.part_ml[(int64_t)q2 * rows_out + orow] = make_float2(-INFINITY, 0.0f);
+            }
         }
         if (!ok) flag_timeout();
-        // epilogue: O / l
-        if (ok && n_tiles > 0) {
-            const int pj = n_tiles - 1;
-            const bool done = tc::mbar_wait(B(B_PV_DONE + (pj & 1)), (pj >> 1) & 1, kWaitLimit);
-            if (__all_sync(0xffffffffu, done)) {
-                tc::fence_after_sync();
-                const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
-                float4* dst = reinterpret_cast<float4*>(p.out + ((int64_t)iq * p.n_q_heads + qh) * HD);
-#pragma unroll 1
-                for (int c = 0; c < HD / 32; ++c) {
-                    uint32_t o[32];
-                    tc::tmem_ld32(tmem + lane_base + TM_O + 32 * c, o);
-                    tc::tmem_wait_ld();
-                    if (valid) {
-#pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            dst[c * 8 + k] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
-                                                         __uint_as_float(o[4 * k + 2]) * inv,
-                                                         __uint_as_float(o[4 * k + 3]) * inv);
-                    }
-                }
-            } else {
-                flag_timeout();
-            }
-        }
     } else {
         // ---------------------------------------------------------------- dequantisers
-        const int d = threadIdx.x - 192;
-        for (int j = 0; j < n_tiles; ++j) {
-            const int s = j & 1, use = j >> 1;
-            if (!tc::mbar_wait(B(B_ST_FULL + s), use & 1, kWaitLimit)) { flag_timeout(); break; }
-            if (j >= 2 && !tc::mbar_wait(B(B_KV_EMPTY + s), (use - 1) & 1, kWaitLimit)) { flag_timeout(); break; }
-            const int nk = min(BN, key_hi - j * BN);
-            const uint8_t* st = smem + SM_STAGE + s * STAGE_BYTES;
-            dequant_tile(st + ST_KC, reinterpret_cast<const uint16_t*>(st + ST_KS), smem + SM_KHAT + s * HAT_BYTES,
-                         nk, d);
-            tc::fence_proxy_async_smem();
-            tc::mbar_arrive(B(B_KH_FULL + s));
-            dequant_tile(st + ST_VC, reinterpret_cast<const uint16_t*>(st + ST_VS), smem + SM_VHAT + s * HAT_BYTES,
-                         nk, d);
-            tc::fence_proxy_async_smem();
-            tc::mbar_arrive(B(B_VH_FULL + s));
-            tc::mbar_arrive(B(B_ST_EMPTY + s));
+        const int d = threadIdx.x - kDeqWarp0 * 32;
+        int j = 0;
+        bool ok = true;
+        for (int si = 0; ok && si < n_seg; ++si) {
+            const Item g = item_geometry(seg[si].item, p.n_mtiles, p.rows, p.group, p.kv_len, p.q_pos0);
+            for (int t = seg[si].t0; t < seg[si].t1; ++t, ++j) {
+                const int s = j & 1, use = j >> 1;
+                if (!tc::mbar_wait(B(B_ST_FULL + s), use & 1, kWaitLimit)) { ok = false; break; }
+                const int nk = min(BN, g.key_hi - t * BN);
+                const uint8_t* st = smem + SM_STAGE + s * STAGE_BYTES;
+                if (j >= 2 && !tc::mbar_wait(B(B_K_EMPTY + s), (use - 1) & 1, kWaitLimit)) { ok = false; break; }
+                dequant_tile(st + ST_KC, reinterpret_cast<const uint16_t*>(st + ST_KS), smem + SM_KHAT + s * HAT_BYTES,
+                             nk, d);
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(B(B_K_FULL + s));
+                if (j >= 2 && !tc::mbar_wait(B(B_V_EMPTY + s), (use - 1) & 1, kWaitLimit)) { ok = false; break; }
+                dequant_tile(st + ST_VC, reinterpret_cast<const uint16_t*>(st + ST_VS), smem + SM_VHAT + s * HAT_BYTES,
+                             nk, d);
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(B(B_V_FULL + s));
+                tc::mbar_arrive(B(B_ST_EMPTY + s));
+            }
         }
+        if (!ok) flag_timeout();
     }
 
     tc::fence_before_sync();
@@ -362,25 +451,80 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptPa
     if (warp == 1) tc::tmem_dealloc(tmem, TM_NCOLS);
 }
 
+struct PromptPlan {
+    int n_mtiles, n_items, n_parts, grid;
+    long long units;
+    size_t ws_bytes;
+};
+
+int prompt_plan(int n_q, int n_q_heads, int head_dim, int kv_len, int q_pos0, int n_kv_heads, PromptPlan* pl) {
+    if (n_q < 1 || n_q_heads < 1 || n_kv_heads < 1 || kv_len < 1 || q_pos0 < 0) return KVQ8_ERR_INVALID_ARG;
+    if (head_dim != HD || n_q_heads % n_kv_heads) return KVQ8_ERR_UNSUPPORTED;
+    const int group = n_q_heads / n_kv_heads;
+    const long long rows = (long long)n_q * group;
+    if (rows > 0x7fffffffLL || (long long)n_q * n_q_heads > 0x7fffffffLL) return KVQ8_ERR_UNSUPPORTED;
+    pl->n_mtiles = (int)((rows + BM - 1) / BM);
+    const long long items = (long long)pl->n_mtiles * n_kv_heads;
+    if (items > (1 << 24)) return KVQ8_ERR_UNSUPPORTED;
+    pl->n_items = (int)items;
+    long long U = 0;
+    for (int it = 0; it < pl->n_items; ++it)
+        U += item_geometry(it, pl->n_mtiles, (int)rows, group, kv_len, q_pos0).n_tiles;
+    pl->units = U;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess || sms <= 0)
+        sms = 152;
+    pl->grid = (int)(U < sms ? U : sms);
+    // parts per item: CTAs its units span; segments per CTA: items its units touch
+    int parts = 1;
+    long long s = 0;
+    int max_seg = 0, cur_cta = -1, cur_seg = 0;
+    for (int it = 0; it < pl->n_items; ++it) {
+        const int nt = item_geometry(it, pl->n_mtiles, (int)rows, group, kv_len, q_pos0).n_tiles;
+        const long long c0 = cta_of_unit(s, U, pl->grid), c1 = cta_of_unit(s + nt - 1, U, pl->grid);
+        parts = (int)(c1 - c0 + 1) > parts ? (int)(c1 - c0 + 1) : parts;
+        for (long long c = c0; c <= c1; ++c) {
+            if (c != cur_cta) { cur_cta = (int)c; cur_seg = 0; }
+            ++cur_seg;
+            max_seg = cur_seg > max_seg ? cur_seg : max_seg;
+        }
+        s += nt;
+    }
+    if (max_seg > kMaxSegments) return KVQ8_ERR_UNSUPPORTED;
+    pl->n_parts = parts;
+    const size_t rows_out = (size_t)n_q * n_q_heads;
+    const size_t o_bytes = (size_t)parts * rows_out * HD * sizeof(float);
+    pl->ws_bytes = ((o_bytes + 255) / 256) * 256 + (size_t)parts * rows_out * 2 * sizeof(float);
+    return KVQ8_OK;
+}
+
 }  // namespace
 }  // namespace kvq8
 
+extern "C" size_t attn_prompt_q8_workspace_bytes(int n_q, int n_q_heads, int head_dim, int kv_len, int q_pos0,
+                                                 int n_kv_heads) {
+    kvq8::PromptPlan pl;
+    if (kvq8::prompt_plan(n_q, n_q_heads, head_dim, kv_len, q_pos0, n_kv_heads, &pl) != KVQ8_OK) return 0;
+    return pl.ws_bytes;
+}
+
 extern "C" int attn_prompt_q8(const uint16_t* q, int n_q, int n_q_heads, const kvq8_cache* kv, int kv_len, int q_pos0,
-                              float softmax_scale, float* out, kvq8_stream_t stream) {
+                              float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                              kvq8_stream_t stream) {
     using namespace kvq8;
     if (!kv || !q || !out) return KVQ8_ERR_INVALID_ARG;
     if (!kv->k_codes || !kv->k_scales || !kv->v_codes || !kv->v_scales) return KVQ8_ERR_INVALID_ARG;
-    if (n_q < 1 || n_q_heads < 1 || kv->n_kv_heads < 1 || kv_len < 1 || q_pos0 < 0) return KVQ8_ERR_INVALID_ARG;
-    if (kv_len > kv->capacity) return KVQ8_ERR_INVALID_ARG;
-    if (!(softmax_scale == softmax_scale) || softmax_scale == INFINITY || softmax_scale == -INFINITY)
-        return KVQ8_ERR_INVALID_ARG;
-    if (kv->head_dim != HD || n_q_heads % kv->n_kv_heads) return KVQ8_ERR_UNSUPPORTED;
+    if (kv->n_kv_heads < 1 || kv_len > kv->capacity) return KVQ8_ERR_INVALID_ARG;
+    if (!(softmax_scale > 0.0f) || softmax_scale == INFINITY) return KVQ8_ERR_INVALID_ARG;
+    PromptPlan pl;
+    const int rc = prompt_plan(n_q, n_q_heads, kv->head_dim, kv_len, q_pos0, kv->n_kv_heads, &pl);
+    if (rc != KVQ8_OK) return rc;
     if (!aligned16(q) || !aligned16(out) || !aligned16(kv->k_codes) || !aligned16(kv->k_scales) ||
         !aligned16(kv->v_codes) || !aligned16(kv->v_scales))
         return KVQ8_ERR_MISALIGNED;
-    const int64_t rows = (int64_t)n_q * (n_q_heads / kv->n_kv_heads);
-    const int64_t tiles = (rows + BM - 1) / BM;
-    if (rows > 0x7fffffffLL || tiles > 0x7fffffffLL || kv->n_kv_heads > 65535) return KVQ8_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < pl.ws_bytes) return KVQ8_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return KVQ8_ERR_MISALIGNED;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(prompt_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
@@ -388,24 +532,33 @@ extern "C" int attn_prompt_q8(const uint16_t* q, int n_q, int n_q_heads, const k
             return KVQ8_ERR_CUDA;
         attr_set = true;
     }
+    const size_t rows_out = (size_t)n_q * n_q_heads;
+    const size_t o_bytes = (size_t)pl.n_parts * rows_out * HD * sizeof(float);
     PromptParams pp;
     pp.q = q;
     pp.kc = kv->k_codes;
     pp.ks = kv->k_scales;
     pp.vc = kv->v_codes;
     pp.vs = kv->v_scales;
-    pp.out = out;
+    pp.part_o = static_cast<float*>(workspace);
+    pp.part_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + ((o_bytes + 255) / 256) * 256);
     pp.n_q = n_q;
     pp.n_q_heads = n_q_heads;
     pp.group = n_q_heads / kv->n_kv_heads;
     pp.capacity = kv->capacity;
     pp.kv_len = kv_len;
     pp.q_pos0 = q_pos0;
-    pp.rows = (int)rows;
+    pp.rows = n_q * pp.group;
+    pp.n_mtiles = pl.n_mtiles;
+    pp.n_items = pl.n_items;
+    pp.n_parts = pl.n_parts;
+    pp.units = pl.units;
     pp.scale_log2 = softmax_scale * kLog2e;
-    dim3 grid((unsigned)tiles, (unsigned)kv->n_kv_heads);
-    prompt_attn_kernel<<<grid, kThreads, SMEM_BYTES, (cudaStream_t)stream>>>(pp);
-    return launch_status();
+    cudaStream_t s = (cudaStream_t)stream;
+    prompt_attn_kernel<<<pl.grid, kThreads, SMEM_BYTES, s>>>(pp);
+    const int r1 = launch_status();
+    if (r1 != KVQ8_OK) return r1;
+    return launch_combine(pp.part_o, reinterpret_cast<const float*>(pp.part_ml), pl.n_parts, (int)rows_out, HD, out, s);
 }
 
 extern "C" int kvq8_device_error(int reset) {
