@@ -131,12 +131,6 @@ __device__ int cta_segments(const PromptParams& p, int c, int G, Segment* seg) {
 
 __device__ __forceinline__ void flag_timeout() { atomicOr(&g_kvq8_device_error, 1u); }
 
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 // Convert one 64-key plane tile (codes + scales in staging) into the swizzled fp16 tile:
 // element (key n, dim j) -> atom j/64, row n, 16-byte chunk ((j%64)/8) ^ (n%8).
 // 256 threads, 4 chunks of 16 codes each.

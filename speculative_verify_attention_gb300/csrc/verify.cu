@@ -63,13 +63,14 @@ template <int HD, int NT>
 struct Smem {
     static constexpr int NB = HD / 32;      // scale blocks per token
     static constexpr int RP = 8 * NT;       // padded rows per chunk
+    static constexpr int PS = RP + 4;       // P-tile entries per key pair (padding spreads banks)
     static constexpr int kK = 0;
     static constexpr int kKs = kK + kKT * HD;
     static constexpr int kV = kKs + kKT * NB * 2;
     static constexpr int kVs = kV + kKT * HD;
     static constexpr int kQ = kVs + kKT * NB * 2;
     static constexpr int kP = kQ + NB * NT * 1024;
-    static constexpr int kRedMax = kP + kKT * RP * 4;
+    static constexpr int kRedMax = kP + (kKT / 2) * PS * 8;
     static constexpr int kRedSum = kRedMax + kWarps * RP * 4;
     static constexpr int kAlpha = kRedSum + kWarps * RP * 4;
     static constexpr int kBytes = kAlpha + RP * 4;
@@ -117,7 +118,7 @@ __device__ __forceinline__ void load_scales(uint8_t* smem, const uint16_t* plane
 template <int HD, int NT>
 __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyParams p) {
     using L = Smem<HD, NT>;
-    constexpr int NB = L::NB, RP = L::RP;
+    constexpr int NB = L::NB, RP = L::RP, PS = L::PS;
     constexpr int BPW = NB / kWarps;  // 32-dim output blocks per warp in PV
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* sK = smem + L::kK;
@@ -125,7 +126,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
     uint8_t* sV = smem + L::kV;
     const uint16_t* sVs = reinterpret_cast<const uint16_t*>(smem + L::kVs);
     __half* sQ = reinterpret_cast<__half*>(smem + L::kQ);
-    float* sP = reinterpret_cast<float*>(smem + L::kP);
+    // P tile: entry (key pair k, row r) = (hi, lo) fp16 pairs of (p[2k][r], p[2k+1][r]) * 2^12
+    uint2* sP = reinterpret_cast<uint2*>(smem + L::kP);
     float* sRedMax = reinterpret_cast<float*>(smem + L::kRedMax);
     float* sRedSum = reinterpret_cast<float*>(smem + L::kRedSum);
     float* sAlpha = reinterpret_cast<float*>(smem + L::kAlpha);
@@ -265,13 +267,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
                 const uint32_t a12 = biased_bytes_to_half2<0x4342>(y0), a13 = biased_bytes_to_half2<0x4342>(y1);
                 float tmp[NT][4];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    tmp[nt][0] = tmp[nt][1] = tmp[nt][2] = tmp[nt][3] = 0.0f;
-                    mma_f16_16816(tmp[nt], a00, a01, a02, a03, qh[nt].x, qh[nt].y);
-                    mma_f16_16816(tmp[nt], a10, a11, a12, a13, qh[nt].z, qh[nt].w);
-                    mma_f16_16816(tmp[nt], a00, a01, a02, a03, ql[nt].x, ql[nt].y);
-                    mma_f16_16816(tmp[nt], a10, a11, a12, a13, ql[nt].z, ql[nt].w);
-                }
+                for (int nt = 0; nt < NT; ++nt) mma_f16_16816_zc(tmp[nt], a00, a01, a02, a03, qh[nt].x, qh[nt].y);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_f16_16816(tmp[nt], a10, a11, a12, a13, qh[nt].z, qh[nt].w);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_f16_16816(tmp[nt], a00, a01, a02, a03, ql[nt].x, ql[nt].y);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_f16_16816(tmp[nt], a10, a11, a12, a13, ql[nt].z, ql[nt].w);
                 const float dk0 = half_bits_to_float(sKs[n0 * NB + b]);
                 const float dk1 = half_bits_to_float(sKs[(n0 + 8) * NB + b]);
 #pragma unroll
@@ -330,13 +332,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
                 const float m_new = fmaxf(m_run[nt][c], mt_);
                 float a = 1.0f, sum = 0.0f;
                 if (m_new != -INFINITY) {
-                    a = exp2f(m_run[nt][c] - m_new);
+                    a = ex2_approx(m_run[nt][c] - m_new);
 #pragma unroll
                     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             float& s = S[mt][nt][2 * h + c];
-                            s = exp2f(s - m_new);
+                            s = ex2_approx(s - m_new);
                             sum += s;
                         }
                 } else {
@@ -354,15 +356,26 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
                     sRedSum[warp * RP + r] = sum;
                     if (warp == 0) sAlpha[r] = a;
                 }
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int kl = warp * 32 + mt * 16 + g + 8 * h;
-                        sP[((kl >> 1) * RP + r) * 2 + (kl & 1)] = S[mt][nt][2 * h + c];
-                    }
             }
         (void)mx;
+        // P tile: a key and its pair partner sit in lanes 4 apart; each pair of lanes swaps one
+        // value so that the even-g lane writes row 2t and the odd-g lane row 2t+1.
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float v0 = S[mt][nt][2 * h], v1 = S[mt][nt][2 * h + 1];
+                    const bool ev = (g & 1) == 0;
+                    const float recv = __shfl_xor_sync(0xffffffffu, ev ? v1 : v0, 4);
+                    const float pe = (ev ? v0 : recv) * 4096.0f;  // even key
+                    const float po = (ev ? recv : v1) * 4096.0f;  // odd key
+                    const __half2 ph = __floats2half2_rn(pe, po);
+                    const __half2 pl = __floats2half2_rn(pe - __low2float(ph), po - __high2float(ph));
+                    const int kl = warp * 32 + mt * 16 + g + 8 * h;
+                    sP[(kl >> 1) * PS + 8 * nt + 2 * t + (ev ? 0 : 1)] = make_uint2(h2_as_u32(ph), h2_as_u32(pl));
+                }
 
         cp_async_wait<1>();  // V of this tile landed (next K may still be in flight)
         __syncthreads();
@@ -380,11 +393,14 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
                 }
         }
 
-        // ---------------- PV: O^T[dim][row] += V^T * (p dV 2^E) ----------------
+        // ---------------- PV: O^T[dim][row] += V^T * (p 2^12) (dV 2^E) ----------------
+        // Per output block, E keeps dV 2^E of the tile's largest scale in [2, 4), so that
+        // w = (p 2^12)(dV 2^E) < 2^14 stays in the fp16 range.  w = hi + lo exactly up to
+        // 2^-22: hi = fl(ph d), lo = fl((ph d - hi) + pl d), the first residual exact by FMA.
+        float esc[BPW];
 #pragma unroll
         for (int i = 0; i < BPW; ++i) {
             const int b = warp + kWarps * i;
-            // per-warp exponent keeping w = p dV 2^E below 2^14
             float dmax = 0.0f;
 #pragma unroll
             for (int k = 0; k < kKT / 32; ++k) dmax = fmaxf(dmax, half_bits_to_float(sVs[(lane + 32 * k) * NB + b]));
@@ -393,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
             if (dmax > 0.0f) {
                 int e2;
                 (void)frexpf(dmax, &e2);
-                const int et = 14 - e2;
+                const int et = 2 - e2;
                 if (E[i] == INT32_MIN) {
                     E[i] = et;
                 } else if (et < E[i]) {
@@ -407,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
                     E[i] = et;
                 }
             }
-            const float esc = (E[i] == INT32_MIN) ? 0.0f : ldexpf(1.0f, E[i]);
+            esc[i] = (E[i] == INT32_MIN) ? 0.0f : ldexpf(1.0f, E[i]);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const float a0 = sAlpha[8 * nt + 2 * t], a1 = sAlpha[8 * nt + 2 * t + 1];
@@ -419,9 +435,19 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
                     O[i][mt][nt][3] *= a1;
                 }
             }
+        }
 #pragma unroll 2
-            for (int ks = 0; ks < kKT / 16; ++ks) {
-                const int kb = ks * 16;
+        for (int ks = 0; ks < kKT / 16; ++ks) {
+            const int kb = ks * 16;
+            uint2 pp01[NT], pp89[NT];  // (hi, lo) pairs of keys (2t, 2t+1) and (2t+8, 2t+9), row g of n-tile
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                pp01[nt] = sP[((kb >> 1) + t) * PS + 8 * nt + g];
+                pp89[nt] = sP[((kb >> 1) + t + 4) * PS + 8 * nt + g];
+            }
+#pragma unroll
+            for (int i = 0; i < BPW; ++i) {
+                const int b = warp + kWarps * i;
                 const int cb = 32 * b + 4 * g;
                 const uint32_t w0 = *reinterpret_cast<const uint32_t*>(sV + swz<HD>(kb + 2 * t, cb)) ^ 0x80808080u;
                 const uint32_t w1 = *reinterpret_cast<const uint32_t*>(sV + swz<HD>(kb + 2 * t + 1, cb)) ^ 0x80808080u;
@@ -438,24 +464,20 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
                 A[1][1] = biased_bytes_to_half2<0x4342>(y01hi);
                 A[1][2] = biased_bytes_to_half2<0x4140>(y89hi);
                 A[1][3] = biased_bytes_to_half2<0x4342>(y89hi);
-                const float ds0 = half_bits_to_float(sVs[(kb + 2 * t) * NB + b]) * esc;
-                const float ds1 = half_bits_to_float(sVs[(kb + 2 * t + 1) * NB + b]) * esc;
-                const float ds8 = half_bits_to_float(sVs[(kb + 2 * t + 8) * NB + b]) * esc;
-                const float ds9 = half_bits_to_float(sVs[(kb + 2 * t + 9) * NB + b]) * esc;
+                const __half2 d01 = __floats2half2_rn(half_bits_to_float(sVs[(kb + 2 * t) * NB + b]) * esc[i],
+                                                      half_bits_to_float(sVs[(kb + 2 * t + 1) * NB + b]) * esc[i]);
+                const __half2 d89 = __floats2half2_rn(half_bits_to_float(sVs[(kb + 2 * t + 8) * NB + b]) * esc[i],
+                                                      half_bits_to_float(sVs[(kb + 2 * t + 9) * NB + b]) * esc[i]);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const float2 p01 = *reinterpret_cast<const float2*>(sP + (((kb >> 1) + t) * RP + 8 * nt + g) * 2);
-                    const float2 p89 =
-                        *reinterpret_cast<const float2*>(sP + (((kb >> 1) + t + 4) * RP + 8 * nt + g) * 2);
-                    const float w00 = p01.x * ds0, w01 = p01.y * ds1, w10 = p89.x * ds8, w11 = p89.y * ds9;
-                    const __half2 h0 = __floats2half2_rn(w00, w01);
-                    const __half2 h1 = __floats2half2_rn(w10, w11);
-                    const __half2 l0 = __floats2half2_rn(w00 - __low2float(h0), w01 - __high2float(h0));
-                    const __half2 l1 = __floats2half2_rn(w10 - __low2float(h1), w11 - __high2float(h1));
-                    const uint32_t bh0 = *reinterpret_cast<const uint32_t*>(&h0);
-                    const uint32_t bh1 = *reinterpret_cast<const uint32_t*>(&h1);
-                    const uint32_t bl0 = *reinterpret_cast<const uint32_t*>(&l0);
-                    const uint32_t bl1 = *reinterpret_cast<const uint32_t*>(&l1);
+                    const __half2 ph0 = u32_as_h2(pp01[nt].x), pl0 = u32_as_h2(pp01[nt].y);
+                    const __half2 ph1 = u32_as_h2(pp89[nt].x), pl1 = u32_as_h2(pp89[nt].y);
+                    const __half2 h0 = __hmul2(ph0, d01);
+                    const __half2 h1 = __hmul2(ph1, d89);
+                    const __half2 l0 = __hfma2(pl0, d01, __hfma2(ph0, d01, __hneg2(h0)));
+                    const __half2 l1 = __hfma2(pl1, d89, __hfma2(ph1, d89, __hneg2(h1)));
+                    const uint32_t bh0 = h2_as_u32(h0), bh1 = h2_as_u32(h1);
+                    const uint32_t bl0 = h2_as_u32(l0), bl1 = h2_as_u32(l1);
 #pragma unroll
                     for (int mt = 0; mt < 2; ++mt) {
                         mma_f16_16816(O[i][mt][nt], A[mt][0], A[mt][1], A[mt][2], A[mt][3], bh0, bh1);
@@ -482,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
 #pragma unroll
     for (int i = 0; i < BPW; ++i) {
         const int b = warp + kWarps * i;
-        const float inv = (E[i] == INT32_MIN) ? 1.0f : ldexpf(1.0f, -E[i]);
+        const float inv = (E[i] == INT32_MIN) ? 1.0f : ldexpf(1.0f, -E[i] - 12);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
