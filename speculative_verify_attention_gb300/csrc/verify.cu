@@ -82,18 +82,24 @@ __device__ __forceinline__ int swz(int n, int c) {
     return n * HD + ((((c >> 4) ^ (n & 7)) << 4) | (c & 15));
 }
 
+// A thread copies the chunks ci = tid + k * kThreads; since kThreads is a multiple of 8 rows'
+// worth of chunks, its row advances by a fixed step and its swizzled column never changes,
+// so every copy is a pointer increment.
 template <int HD>
 __device__ __forceinline__ void load_codes(uint8_t* smem, const int8_t* plane, int64_t head_row0, int tile_key0,
                                            int key_end) {
-    constexpr int CPR = HD / 16;  // 16-byte chunks per row
-    const uint32_t base = smem_u32(smem);
-#pragma unroll 4
-    for (int ci = threadIdx.x; ci < kKT * CPR; ci += kThreads) {
-        const int n = ci / CPR, c16 = ci % CPR;
-        const int key = tile_key0 + n;
-        const bool ok = key < key_end;
-        const int8_t* src = plane + (head_row0 + (ok ? key : tile_key0)) * HD + c16 * 16;
-        cp_async_16(base + n * HD + ((c16 ^ (n & 7)) << 4), src, ok ? 16 : 0);
+    constexpr int CPR = HD / 16;                 // 16-byte chunks per row
+    constexpr int ROWS_PER_PASS = kThreads / CPR;
+    static_assert(ROWS_PER_PASS % 8 == 0, "row step must keep the swizzle phase");
+    const int n0 = threadIdx.x / CPR, c16 = threadIdx.x % CPR;
+    const uint32_t dst0 = smem_u32(smem) + n0 * HD + ((c16 ^ (n0 & 7)) << 4);
+    const int8_t* src0 = plane + (head_row0 + tile_key0 + n0) * HD + c16 * 16;
+    const int valid = key_end - tile_key0 - n0;  // rows of this thread's column still inside the slice
+#pragma unroll
+    for (int k = 0; k < kKT / ROWS_PER_PASS; ++k) {
+        const bool ok = k * ROWS_PER_PASS < valid;
+        cp_async_16(dst0 + k * ROWS_PER_PASS * HD, ok ? src0 + (int64_t)k * ROWS_PER_PASS * HD : src0 - (int64_t)n0 * HD,
+                    ok ? 16 : 0);
     }
 }
 
@@ -141,6 +147,16 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
     const int key_begin = split * p.keys_per_split;
     const int key_end = min(key_begin + p.keys_per_split, p.kv_len);
     const int64_t head_row0 = (int64_t)kvh * p.capacity;
+
+    // First K/V tile in flight before anything else.
+    if (key_begin < key_end) {
+        load_codes<HD>(sK, p.k_codes, head_row0, key_begin, key_end);
+        load_scales<HD>(smem + L::kKs, p.k_scales, head_row0, key_begin, key_end);
+        cp_async_commit();
+        load_codes<HD>(sV, p.v_codes, head_row0, key_begin, key_end);
+        load_scales<HD>(smem + L::kVs, p.v_scales, head_row0, key_begin, key_end);
+        cp_async_commit();
+    }
 
     // Stage q rows of this chunk as fp16 hi/lo in mma B-fragment order:
     // entry (block b, n-tile nt, hi|lo, lane g*4+t) holds row 8nt+g, dims 32b+8t .. +7.
@@ -223,14 +239,6 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
 #pragma unroll
     for (int i = 0; i < BPW; ++i) E[i] = INT32_MIN;  // unset
 
-    if (key_begin < key_end) {
-        load_codes<HD>(sK, p.k_codes, head_row0, key_begin, key_end);
-        load_scales<HD>(smem + L::kKs, p.k_scales, head_row0, key_begin, key_end);
-        cp_async_commit();
-        load_codes<HD>(sV, p.v_codes, head_row0, key_begin, key_end);
-        load_scales<HD>(smem + L::kVs, p.v_scales, head_row0, key_begin, key_end);
-        cp_async_commit();
-    }
 
     for (int tile0 = key_begin; tile0 < key_end; tile0 += kKT) {
         cp_async_wait<1>();  // K of this tile landed (V may still be in flight)
@@ -500,7 +508,19 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
     cp_async_wait<0>();
 
     // ---------------- write the slice partial ----------------
+    // Each lane owns dims 32b + 4g .. +3 of rows 8nt + 2t + c: one 16-byte store per row, and
+    // the 8 lanes of a row cover 128 contiguous bytes, so every L2 sector is written whole.
     float* po = p.part_o + (int64_t)split * rows_total * HD;
+    int64_t grow[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int r = 8 * nt + 2 * t + c;
+            const int rr = row0 + r;
+            const int iq = rr / p.group, hh = rr - iq * p.group;
+            grow[nt][c] = (r < rows_here) ? (int64_t)iq * p.n_q_heads + kvh * p.group + hh : -1;
+        }
 #pragma unroll
     for (int i = 0; i < BPW; ++i) {
         const int b = warp + kWarps * i;
@@ -509,19 +529,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                const int r = 8 * nt + 2 * t + c;
-                if (r >= rows_here) continue;
-                const int rr = row0 + r;
-                const int iq = rr / p.group, hh = rr - iq * p.group;
-                const int64_t grow = (int64_t)iq * p.n_q_heads + kvh * p.group + hh;
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    const int j0 = 32 * b + 4 * g + 2 * mt;
-                    float2 v;
-                    v.x = O[i][mt][nt][c] * inv;      // (dim j0, row r)
-                    v.y = O[i][mt][nt][2 + c] * inv;  // (dim j0 + 1, row r)
-                    *reinterpret_cast<float2*>(po + grow * HD + j0) = v;
-                }
+                if (grow[nt][c] < 0) continue;
+                *reinterpret_cast<float4*>(po + grow[nt][c] * HD + 32 * b + 4 * g) =
+                    make_float4(O[i][0][nt][c] * inv, O[i][0][nt][2 + c] * inv, O[i][1][nt][c] * inv,
+                                O[i][1][nt][2 + c] * inv);
             }
     }
     if (warp == 0 && g == 0) {
