@@ -218,6 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
             }
         }
 
+    // every real row of this chunk sees all keys below vis_min; padding rows hold q = 0 and
+    // never reach the output, so tiles wholly below vis_min skip the mask
+    const int vis_min = min(min(p.q_pos0 + row0 / p.group + 1, p.kv_len), key_end);
     float m_run[NT][2], l_run[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -295,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
         }
 
         // ---------------- mask + per-warp row max ----------------
+        const bool tile_needs_mask = tile0 + kKT > vis_min;
         float mx[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -307,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
                     for (int h = 0; h < 2; ++h) {
                         const int key = tile0 + warp * 32 + mt * 16 + g + 8 * h;
                         float& s = S[mt][nt][2 * h + c];
-                        if (key >= vis_end[nt][c]) s = -INFINITY;
+                        if (tile_needs_mask && key >= vis_end[nt][c]) s = -INFINITY;
                         m = fmaxf(m, s);
                     }
                 m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
