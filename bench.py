@@ -105,26 +105,34 @@ class ClockSampler:
 
 
 def _dist():
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return world, rank, local
+    from speculative_verify_attention_gb300 import multigpu
+    return multigpu.env_world()
 
 
 def _barrier(world):
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
+    from speculative_verify_attention_gb300 import multigpu
+    multigpu.barrier()
 
 
 def _max_over_ranks(x: float, world: int) -> float:
-    if world == 1:
-        return x
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    from speculative_verify_attention_gb300 import multigpu
+    return multigpu.max_over_ranks(x, device="cuda" if world > 1 else None)
+
+
+def _kernel_traffic(kernel_files, workload: str):
+    """DRAM bytes per launch from the committed ncu capture of `workload`, if the kernel
+    sources are still the ones that capture measured (else None: the counters are stale)."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            entry = json.load(f)[workload]
+        h = hashlib.sha256()
+        for name in kernel_files:
+            with open(os.path.join(ROOT, "speculative_verify_attention_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        return float(entry["dram_bytes_per_launch"]) if entry.get("source_sha256") == h.hexdigest() else None
+    except Exception:
+        return None
 
 
 # ----------------------------------------------------------------------------- oracle arm
@@ -298,6 +306,19 @@ def run_native(args, world, rank, local):
         per_t[f"T{T}"] = {"us_per_call": us, "kv_gbs": ws_[T].kv_bytes() / (us * 1e-6) / 1e9,
                           "hbm_frac": ws_[T].kv_bytes() / (us * 1e-6) / 1e9 / hbm_peak}
 
+    # the long-context cells the pages' headline speedups are quoted at (ctx 20,676)
+    long_ctx = {}
+    if not args.no_long_context:
+        torch.cuda.empty_cache()
+        lw = {T: workloads.long_verify(20676, T) for T in VERIFY_T}
+        lring = _ring_for(lw[max(VERIFY_T)], dev, args.ring_l2)   # capacity covers every T
+        for T in VERIFY_T:
+            us = time_verify_cell(lw[T], lring, dev)
+            gbs_ = lw[T].kv_bytes() / (us * 1e-6) / 1e9
+            long_ctx[f"T{T}"] = {"workload": lw[T].name, "us_per_call": us, "kv_gbs": gbs_, "hbm_frac": gbs_ / hbm_peak}
+        del lring
+        torch.cuda.empty_cache()
+
     # e2e through the Python API with pinned host buffers, eager
     h_q = {T: q[T].cpu().pin_memory() for T in VERIFY_T}
     h_k = {T: knew[T].cpu().pin_memory() for T in VERIFY_T}
@@ -357,9 +378,12 @@ def run_native(args, world, rank, local):
             "us_per_call": us_per_call_verify, "verify_only_gbs": verify_gbs,
             "hbm_frac": verify_gbs / hbm_peak, "per_T": per_t,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": None, "peak_source": peak_src,
+                         "frac": achieved / hbm_peak,
+                         "traffic": _kernel_traffic(["verify.cu", "combine.cu"], "verify-24q4kv-hd256-ctx4096-T4+T8"),
+                         "peak_source": peak_src,
                          "kernel": "attn_verify_q8 (verify_split_kernel + combine_kernel)",
                          "algorithmic_bytes_per_launch": bytes_per_launch},
+            "long_context": long_ctx,
             "prompt": prompt,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -406,6 +430,54 @@ def prompt_bench(args, dev, fp16_peak):
             "flops": w.causal_flops(), "calls_timed": n, "l2": "flushed (256 MiB write) before every call"}
 
 
+def _ring_for(w, dev, ring_l2):
+    import torch
+
+    from speculative_verify_attention_gb300 import KVCacheQ8, workloads
+    inp = workloads.make_inputs(w)
+    base = KVCacheQ8(w.n_kv_heads, w.head_dim, w.kv_len, device=dev)
+    base.append(torch.from_numpy(inp.k).to(dev), torch.from_numpy(inp.v).to(dev), 0)
+    nbytes = sum(t.numel() * t.element_size() for t in (base.k_codes, base.v_codes, base.k_scales, base.v_scales))
+    n_ring = max(2, int(np.ceil(ring_l2 * L2_BYTES / nbytes)))
+    ring = [base]
+    for _ in range(n_ring - 1):
+        c = KVCacheQ8(w.n_kv_heads, w.head_dim, w.kv_len, device=dev)
+        for a, b in ((c.k_codes, base.k_codes), (c.v_codes, base.v_codes), (c.k_scales, base.k_scales),
+                     (c.v_scales, base.v_scales)):
+            a.copy_(b)
+        ring.append(c)
+    return ring
+
+
+def time_verify_cell(w, ring, dev, reps=10):
+    """Median-free device time per attn_verify_q8 call: a CUDA graph of calls walking the ring
+    (total size > 4x L2) replayed `reps` times; returns microseconds per call."""
+    import torch
+
+    from speculative_verify_attention_gb300 import attn_verify_q8, attn_verify_q8_workspace_bytes, workloads
+    q = torch.from_numpy(workloads.make_inputs(w, kv_len=1).q).to(dev)
+    out = torch.empty_like(q)
+    ws = torch.empty(attn_verify_q8_workspace_bytes(w.n_q, w.n_q_heads, w.head_dim, w.kv_len, w.n_kv_heads),
+                     dtype=torch.uint8, device=dev)
+    for i in range(3):
+        attn_verify_q8(q, ring[i % len(ring)], w.kv_len, w.q_pos0, w.softmax_scale, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    n_calls = max(len(ring), 32)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n_calls):
+            attn_verify_q8(q, ring[i % len(ring)], w.kv_len, w.q_pos0, w.softmax_scale, out=out, workspace=ws)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / (reps * n_calls)
+
+
 def sweep(args):
     """Verify latency and KV-scan bandwidth per (context, T) cell of the long-context and
     hd128 workload families (one JSON line per cell; not the headline line)."""
@@ -413,56 +485,21 @@ def sweep(args):
 
     import __graft_entry__
     __graft_entry__.build()
-    from speculative_verify_attention_gb300 import (KVCacheQ8, attn_verify_q8, attn_verify_q8_workspace_bytes,
-                                                    workloads)
+    from speculative_verify_attention_gb300 import workloads
     hbm_peak, _, _ = _peaks()
     dev = torch.device("cuda", 0)
-    cells = [workloads.long_verify(c, t) for c in workloads.LONG_CTX for t in workloads.LONG_T]
+    cells = [workloads.verify_27b(t) for t in workloads.VERIFY_27B_T]
+    cells += [workloads.long_verify(c, t) for c in workloads.LONG_CTX for t in workloads.LONG_T]
     cells += [workloads.hd128_verify(t) for t in workloads.HD128_T]
     cells = [w for w in cells if not args.sweep_filter or args.sweep_filter in w.name]
-    built = {}
+    key, ring = None, None
     for w in cells:
-        key = (w.n_kv_heads, w.head_dim, w.kv_len)
-        if key not in built:
-            built.clear()
+        if key != (w.n_kv_heads, w.head_dim, w.kv_len):
+            ring = None
             torch.cuda.empty_cache()
-            inp = workloads.make_inputs(w)
-            base = KVCacheQ8(w.n_kv_heads, w.head_dim, w.kv_len, device=dev)
-            base.append(torch.from_numpy(inp.k).to(dev), torch.from_numpy(inp.v).to(dev), 0)
-            nbytes = sum(t.numel() * t.element_size() for t in (base.k_codes, base.v_codes, base.k_scales,
-                                                                base.v_scales))
-            n_ring = max(2, int(np.ceil(args.ring_l2 * L2_BYTES / nbytes)))
-            ring = [base]
-            for _ in range(n_ring - 1):
-                c = KVCacheQ8(w.n_kv_heads, w.head_dim, w.kv_len, device=dev)
-                for a, b in ((c.k_codes, base.k_codes), (c.v_codes, base.v_codes), (c.k_scales, base.k_scales),
-                             (c.v_scales, base.v_scales)):
-                    a.copy_(b)
-                ring.append(c)
-            built[key] = ring
-        ring = built[key]
-        q = torch.from_numpy(workloads.make_inputs(w, kv_len=1).q).to(dev)
-        out = torch.empty_like(q)
-        ws = torch.empty(attn_verify_q8_workspace_bytes(w.n_q, w.n_q_heads, w.head_dim, w.kv_len, w.n_kv_heads),
-                         dtype=torch.uint8, device=dev)
-        for i in range(3):
-            attn_verify_q8(q, ring[i % len(ring)], w.kv_len, w.q_pos0, w.softmax_scale, out=out, workspace=ws)
-        torch.cuda.synchronize()
-        n_calls = max(len(ring), 32)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for i in range(n_calls):
-                attn_verify_q8(q, ring[i % len(ring)], w.kv_len, w.q_pos0, w.softmax_scale, out=out, workspace=ws)
-        g.replay()
-        torch.cuda.synchronize()
-        reps = 10
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(reps):
-            g.replay()
-        b.record()
-        torch.cuda.synchronize()
-        us = a.elapsed_time(b) * 1e3 / (reps * n_calls)
+            ring = _ring_for(w, dev, args.ring_l2)
+            key = (w.n_kv_heads, w.head_dim, w.kv_len)
+        us = time_verify_cell(w, ring, dev)
         gbs = w.kv_bytes() / (us * 1e-6) / 1e9
         print(json.dumps({"workload": w.name, "us_per_call": us, "kv_mb": w.kv_bytes() / 1e6, "kv_gbs": gbs,
                           "hbm_frac": gbs / hbm_peak, "tflops_alg": w.causal_flops() / (us * 1e-6) / 1e12,
@@ -479,6 +516,7 @@ def main():
     ap.add_argument("--prompt-steps", type=int, default=10)
     ap.add_argument("--no-prompt", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-long-context", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="per-cell verify sweep instead of the headline line")
     ap.add_argument("--prompt-only", action="store_true", help="time only the prompt-chunk kernel")
     ap.add_argument("--sweep-filter", default="")

@@ -1,0 +1,69 @@
+"""Host-side helpers for running the attention path on several GPUs of one node.
+
+Two ways to use N GPUs, both built from the single-GPU entry points:
+
+* replicas -- every rank runs its own independent verify / prompt problems (different
+  sequences); no data crosses ranks, only the benchmark's timing reduction does.
+* context slices -- one long context is cut into N contiguous key ranges, each rank
+  computes the unnormalised partials (o, m, l) of its range, the partials are all-gathered,
+  and the log-sum-exp merge (attn_combine) produces the output.  This is the one real
+  exchange step the path has ("perf(gfx1100): share Q8 KV scans across verifier rows",
+  Summary: split-context partials and their reducer).
+
+Everything here is plain torch.distributed (NCCL between GPUs, gloo on CPU); the tests run
+the context-slice exchange with two gloo ranks.
+"""
+from __future__ import annotations
+
+import os
+
+import torch
+import torch.distributed as dist
+
+
+def env_world() -> tuple[int, int, int]:
+    """(world_size, rank, local_rank) from the torchrun environment (1, 0, 0 without it)."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def barrier() -> None:
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Maximum of a scalar over all ranks (the value itself when not distributed)."""
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def context_slices(kv_len: int, world: int, align: int = 128) -> list[tuple[int, int]]:
+    """Cut keys [0, kv_len) into `world` contiguous ranges of whole `align`-key tiles
+    (the last ranges may be empty when there are fewer tiles than ranks)."""
+    if kv_len < 0 or world < 1 or align < 1:
+        raise ValueError("bad slice arguments")
+    tiles = (kv_len + align - 1) // align
+    per = (tiles + world - 1) // world
+    out = []
+    for r in range(world):
+        b = min(kv_len, r * per * align)
+        e = min(kv_len, (r + 1) * per * align)
+        out.append((b, e))
+    return out
+
+
+def allgather_partials(part_o: torch.Tensor, part_ml: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
+    """Gather every rank's partials: part_o [n][rows][hd], part_ml [n][rows][2] ->
+    ([world * n][rows][hd], [world * n][rows][2]) in rank order, ready for attn_combine."""
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return part_o, part_ml
+    w = dist.get_world_size()
+    os_ = [torch.empty_like(part_o) for _ in range(w)]
+    ms_ = [torch.empty_like(part_ml) for _ in range(w)]
+    dist.all_gather(os_, part_o.contiguous())
+    dist.all_gather(ms_, part_ml.contiguous())
+    return torch.cat(os_, dim=0), torch.cat(ms_, dim=0)

@@ -1,0 +1,85 @@
+"""The N > 1 host path on CPU: two gloo ranks.
+
+* max_over_ranks / barrier behave as the benchmark's timing reduction needs.
+* Context-slice sharding: each rank computes the partials of its key range (with the fp64
+  oracle standing in for the per-rank kernel), the partials are all-gathered, and the
+  log-sum-exp merge of the gathered partials equals unsharded attention."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+from speculative_verify_attention_gb300 import multigpu
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, results):
+    import torch.distributed as dist
+
+    import oracle
+    from speculative_verify_attention_gb300 import workloads
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # timing reduction
+        m = multigpu.max_over_ranks(float(rank + 1))
+        multigpu.barrier()
+        # context-slice sharding of one verify problem
+        inp = workloads.random_small(77, 6, 2, 128, 700, 4)
+        c = oracle.Cache(2, 128, 700)
+        c.append(inp.k, inp.v, 0)
+        b, e = multigpu.context_slices(700, world, align=128)[rank]
+        o, ml_m, ml_l = oracle.attention_partial(c, inp.q, 700, 696, 0.09, b, e)
+        part_o = torch.from_numpy(o.reshape(1, -1, 128))
+        part_ml = torch.from_numpy(np.stack([ml_m.reshape(1, -1), ml_l.reshape(1, -1)], axis=-1))
+        go, gml = multigpu.allgather_partials(part_o, part_ml)
+        out = oracle.combine(go.numpy(), gml[..., 0].numpy(), gml[..., 1].numpy())
+        ref = oracle.attention(c, inp.q, 700, 696, 0.09).reshape(-1, 128)
+        results[rank] = (m, float(np.max(np.abs(out - ref))), tuple(go.shape))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_reduce_and_merge_context_slices():
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        results = mgr.dict()
+        procs = [ctx.Process(target=_worker, args=(r, world, port, results)) for r in range(world)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(timeout=240)
+        assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+        for r in range(world):
+            m, err, shape = results[r]
+            assert m == 2.0
+            assert err < 1e-12
+            assert shape == (2, 24, 128)
+
+
+def test_context_slices_cover_the_context_in_whole_tiles():
+    for kv_len, world in ((700, 2), (4100, 8), (100, 4), (0, 3), (129, 2)):
+        sl = multigpu.context_slices(kv_len, world)
+        assert len(sl) == world and sl[0][0] == 0 and sl[-1][1] == kv_len
+        for (b0, e0), (b1, _) in zip(sl[:-1], sl[1:]):
+            assert e0 == b1 and b0 <= e0
+            assert b0 % 128 == 0 or b0 == kv_len
+    with pytest.raises(ValueError):
+        multigpu.context_slices(10, 0)
+
+
+def test_single_process_helpers_are_identities():
+    assert multigpu.max_over_ranks(3.5) == 3.5
+    o, m = torch.zeros(1, 2, 4), torch.zeros(1, 2, 2)
+    assert multigpu.allgather_partials(o, m)[0] is o
