@@ -5,19 +5,20 @@
 // o_s = sum exp(s_n - m_s) v_n, m_s = max s_n (natural-log units) and l_s = sum exp(s_n - m_s);
 // the merge is out = sum_s o_s e^(m_s - m*) / sum_s l_s e^(m_s - m*) with m* = max_s m_s.
 //
-// One 256-thread block per row.  The block loads all (m_s, l_s) of its row in parallel,
-// reduces m*, and keeps the weights w_s = e^(m_s - m*) in shared memory.  The o_s are then
-// read by 64 column threads x 4 split groups, each thread with four independent loads in
-// flight, and the four group sums are added in shared memory -- so a row costs a few
-// memory round trips, not one per split.
+// Launch shape: blocks of 256 threads = 32 column threads (one float4 of the row each) x 8
+// split groups (one warp each); a row of HD floats takes ceil(HD/128) blocks.  Every load a
+// block needs -- the (m, l) of all splits and each thread's first kPrefetch partial vectors --
+// is issued before any of them is used, so a row costs about one memory round trip plus two
+// block reductions.  The split groups' sums are added in shared memory at the end.
 #include "common.cuh"
 
 namespace kvq8 {
 namespace {
 
 constexpr int kCombineThreads = 256;
-constexpr int kColThreads = 64;
+constexpr int kColThreads = 32;
 constexpr int kSplitGroups = kCombineThreads / kColThreads;
+constexpr int kPrefetch = 12;      // partial vectors per thread loaded up front
 constexpr int kMaxSplits = 4096;
 
 __device__ __forceinline__ float block_reduce(float v, bool is_max, float* s_red) {
@@ -36,82 +37,86 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float* s_red
     return r;
 }
 
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* __restrict__ part_o,
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float4* __restrict__ part_o,
                                                                   const float2* __restrict__ part_ml, int n_split,
                                                                   int rows, int hd4, float* __restrict__ out) {
-    __shared__ float s_w[kMaxSplits];
+    extern __shared__ float2 s_wl[];  // [n_split]: (m, l), then (weight, l)
     __shared__ float s_red[kCombineThreads / 32];
     __shared__ float4 s_acc[kSplitGroups - 1][kColThreads];
     const int row = blockIdx.x, tid = threadIdx.x;
+    const int cl = tid % kColThreads, sg = tid / kColThreads;
+    const int c = blockIdx.y * kColThreads + cl;
+    const bool col_ok = c < hd4;
+    const int64_t stride = (int64_t)rows * hd4;  // float4s between consecutive splits
+    const float4* src = part_o + (int64_t)row * hd4 + c;
+    // launched as a programmatic dependent of the split kernel: wait until its partials are complete
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
+    float4 o[kPrefetch];
+#pragma unroll
+    for (int k = 0; k < kPrefetch; ++k) {
+        const int s = sg + k * kSplitGroups;
+        o[k] = (col_ok && s < n_split) ? __ldg(src + s * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     float mx = -INFINITY;
     for (int s = tid; s < n_split; s += kCombineThreads) {
-        const float m = __ldg(part_ml + (int64_t)s * rows + row).x;
-        s_w[s] = m;
-        mx = fmaxf(mx, m);
+        const float2 ml = __ldg(part_ml + (int64_t)s * rows + row);
+        s_wl[s] = ml;
+        mx = fmaxf(mx, ml.x);
     }
-    const float ms = block_reduce(mx, true, s_red);
-
+    const float ms = block_reduce(mx, true, s_red);  // its barriers also publish s_wl
     float lsum = 0.0f;
     for (int s = tid; s < n_split; s += kCombineThreads) {
-        const float m = s_w[s];
-        const float w = (ms == -INFINITY || m == -INFINITY) ? 0.0f : expf(m - ms);
-        s_w[s] = w;
-        if (w != 0.0f) lsum += w * __ldg(part_ml + (int64_t)s * rows + row).y;
+        const float2 ml = s_wl[s];
+        const float w = (ms == -INFINITY || ml.x == -INFINITY) ? 0.0f : expf(ml.x - ms);
+        s_wl[s].x = w;
+        lsum += w * ml.y;
     }
-    const float l = block_reduce(lsum, false, s_red);  // its barriers also publish s_w
+    const float l = block_reduce(lsum, false, s_red);  // its barriers also publish the weights
     const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
 
-    const int cl = tid % kColThreads, sg = tid / kColThreads;
-    const int64_t stride = (int64_t)rows * hd4;
-    for (int c0 = 0; c0 < hd4; c0 += kColThreads) {
-        const int c = c0 + cl;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (c < hd4) {
-            const float4* src = reinterpret_cast<const float4*>(part_o) + (int64_t)row * hd4 + c;
-            int s = sg;
-            for (; s + 3 * kSplitGroups < n_split; s += 4 * kSplitGroups) {
-                float w[4];
-                float4 o[4];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    w[k] = s_w[s + k * kSplitGroups];
-                    o[k] = w[k] != 0.0f ? __ldg(src + (s + k * kSplitGroups) * stride)
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+    for (int k = 0; k < kPrefetch; ++k) {
+        const int s = sg + k * kSplitGroups;
+        const float w = s < n_split ? s_wl[s].x : 0.0f;
+        acc.x = fmaf(w, o[k].x, acc.x);
+        acc.y = fmaf(w, o[k].y, acc.y);
+        acc.z = fmaf(w, o[k].z, acc.z);
+        acc.w = fmaf(w, o[k].w, acc.w);
+    }
+    if (col_ok) {  // splits past the prefetched ones: four loads in flight per step
+        for (int s0 = sg + kPrefetch * kSplitGroups; s0 < n_split; s0 += 4 * kSplitGroups) {
+            float w[4];
+            float4 v[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    acc.x = fmaf(w[k], o[k].x, acc.x);
-                    acc.y = fmaf(w[k], o[k].y, acc.y);
-                    acc.z = fmaf(w[k], o[k].z, acc.z);
-                    acc.w = fmaf(w[k], o[k].w, acc.w);
-                }
+            for (int k = 0; k < 4; ++k) {
+                const int s = s0 + k * kSplitGroups;
+                w[k] = s < n_split ? s_wl[s].x : 0.0f;
+                v[k] = w[k] != 0.0f ? __ldg(src + s * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            for (; s < n_split; s += kSplitGroups) {
-                const float w = s_w[s];
-                if (w == 0.0f) continue;
-                const float4 o = __ldg(src + s * stride);
-                acc.x = fmaf(w, o.x, acc.x);
-                acc.y = fmaf(w, o.y, acc.y);
-                acc.z = fmaf(w, o.z, acc.z);
-                acc.w = fmaf(w, o.w, acc.w);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                acc.x = fmaf(w[k], v[k].x, acc.x);
+                acc.y = fmaf(w[k], v[k].y, acc.y);
+                acc.z = fmaf(w[k], v[k].z, acc.z);
+                acc.w = fmaf(w[k], v[k].w, acc.w);
             }
         }
-        if (sg > 0) s_acc[sg - 1][cl] = acc;
-        __syncthreads();
-        if (sg == 0 && c < hd4) {
+    }
+    if (sg > 0) s_acc[sg - 1][cl] = acc;
+    __syncthreads();
+    if (sg == 0 && col_ok) {
 #pragma unroll
-            for (int k = 0; k < kSplitGroups - 1; ++k) {
-                const float4 a = s_acc[k][cl];
-                acc.x += a.x;
-                acc.y += a.y;
-                acc.z += a.z;
-                acc.w += a.w;
-            }
-            reinterpret_cast<float4*>(out + (int64_t)row * (hd4 * 4))[c] =
-                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        for (int k = 0; k < kSplitGroups - 1; ++k) {
+            const float4 a = s_acc[k][cl];
+            acc.x += a.x;
+            acc.y += a.y;
+            acc.z += a.z;
+            acc.w += a.w;
         }
-        __syncthreads();
+        reinterpret_cast<float4*>(out + (int64_t)row * (hd4 * 4))[c] =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     }
 }
 
@@ -120,9 +125,22 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* _
 int launch_combine(const float* part_o, const float* part_ml, int n_split, int rows, int head_dim, float* out,
                    cudaStream_t stream) {
     if (rows == 0) return KVQ8_OK;
-    combine_kernel<<<rows, kCombineThreads, 0, stream>>>(part_o, reinterpret_cast<const float2*>(part_ml), n_split,
-                                                         rows, head_dim / 4, out);
-    return launch_status();
+    const int hd4 = head_dim / 4;
+    // Programmatic dependent launch: the grid may be scheduled while the kernel before it in
+    // the stream is still running; griddepcontrol.wait in the kernel orders the reads.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(rows, (hd4 + kColThreads - 1) / kColThreads);
+    cfg.blockDim = dim3(kCombineThreads);
+    cfg.dynamicSmemBytes = (size_t)n_split * sizeof(float2);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, combine_kernel, reinterpret_cast<const float4*>(part_o),
+                                             reinterpret_cast<const float2*>(part_ml), n_split, rows, hd4, out);
+    return e == cudaSuccess ? KVQ8_OK : KVQ8_ERR_CUDA;
 }
 
 }  // namespace kvq8

@@ -35,10 +35,13 @@ int launch_combine(const float* part_o, const float* part_ml, int n_split, int r
 
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kKT = 128;  // keys per tile
-constexpr int kMaxNT = 4;  // n8 row tiles per chunk (<= 32 rows per thread block)
+constexpr int kKT = 128;       // keys per tile
+constexpr int kSplitUnit = 64; // context slices are whole multiples of this many keys
+constexpr int kMaxNT = 4;      // n8 row tiles per chunk (<= 32 rows per thread block)
+constexpr float kLazy = 8.0f;  // log2 units: a row's reference maximum moves only when a score exceeds it by this
+constexpr float kPShift = 4.0f;  // p is stored as p * 2^kPShift; with p <= 2^kLazy that stays <= 2^12
 
 struct VerifyParams {
     const float* q;
@@ -70,10 +73,9 @@ struct Smem {
     static constexpr int kVs = kV + kKT * HD;
     static constexpr int kQ = kVs + kKT * NB * 2;
     static constexpr int kP = kQ + NB * NT * 1024;
-    static constexpr int kRedMax = kP + (kKT / 2) * PS * 8;
-    static constexpr int kRedSum = kRedMax + kWarps * RP * 4;
-    static constexpr int kAlpha = kRedSum + kWarps * RP * 4;
-    static constexpr int kBytes = kAlpha + RP * 4;
+    static constexpr int kDv = kP + (kKT / 2) * PS * 8;   // per warp: its block's V scales * 2^E as fp16
+    static constexpr int kRed = kDv + kWarps * kKT * 2;   // [RP][kWarps] floats
+    static constexpr int kBytes = kRed + RP * kWarps * 4;
 };
 
 // Byte offset of code byte c of tile row n in the swizzled layout (16-byte chunks XOR row%8).
@@ -121,22 +123,26 @@ __device__ __forceinline__ void load_scales(uint8_t* smem, const uint16_t* plane
     }
 }
 
+// Work split inside a thread block (8 warps):
+//   QK  : warp w owns keys 16w .. 16w+15 of the tile (one m16 fragment), all row tiles;
+//   PV  : at hd256 warp w owns the 32-dim output block w (two m16 fragments); at hd128 warps
+//         2b and 2b+1 share block b, one m16 fragment each.
+// Row statistics live in the lanes that own the rows: lane (g, t) holds rows 8nt + 2t + c in
+// both the S^T and the O^T fragments, so the softmax factors never leave the thread.
 template <int HD, int NT>
-__global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyParams p) {
+__global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kernel(const VerifyParams p) {
     using L = Smem<HD, NT>;
     constexpr int NB = L::NB, RP = L::RP, PS = L::PS;
-    constexpr int BPW = NB / kWarps;  // 32-dim output blocks per warp in PV
+    constexpr int MTW = HD / 128;  // m16 fragments of V^T per warp in PV
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* sK = smem + L::kK;
     const uint16_t* sKs = reinterpret_cast<const uint16_t*>(smem + L::kKs);
     uint8_t* sV = smem + L::kV;
     const uint16_t* sVs = reinterpret_cast<const uint16_t*>(smem + L::kVs);
     __half* sQ = reinterpret_cast<__half*>(smem + L::kQ);
-    // P tile: entry (key pair k, row r) = (hi, lo) fp16 pairs of (p[2k][r], p[2k+1][r]) * 2^12
+    // P tile: entry (key pair k, row r) = (hi, lo) fp16 pairs of (p[2k][r], p[2k+1][r]) * 2^kPShift
     uint2* sP = reinterpret_cast<uint2*>(smem + L::kP);
-    float* sRedMax = reinterpret_cast<float*>(smem + L::kRedMax);
-    float* sRedSum = reinterpret_cast<float*>(smem + L::kRedSum);
-    float* sAlpha = reinterpret_cast<float*>(smem + L::kAlpha);
+    float* sRed = reinterpret_cast<float*>(smem + L::kRed);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int chunk = blockIdx.x, split = blockIdx.y, kvh = blockIdx.z;
@@ -147,21 +153,14 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
     const int key_begin = split * p.keys_per_split;
     const int key_end = min(key_begin + p.keys_per_split, p.kv_len);
     const int64_t head_row0 = (int64_t)kvh * p.capacity;
+    const int pvb = HD == 256 ? warp : (warp >> 1);  // PV output block of this warp
+    uint16_t* sDv = reinterpret_cast<uint16_t*>(smem + L::kDv) + warp * kKT;
 
-    // First K/V tile in flight before anything else.
-    if (key_begin < key_end) {
-        load_codes<HD>(sK, p.k_codes, head_row0, key_begin, key_end);
-        load_scales<HD>(smem + L::kKs, p.k_scales, head_row0, key_begin, key_end);
-        cp_async_commit();
-        load_codes<HD>(sV, p.v_codes, head_row0, key_begin, key_end);
-        load_scales<HD>(smem + L::kVs, p.v_scales, head_row0, key_begin, key_end);
-        cp_async_commit();
-    }
+    // The combine kernel may be launched now; it waits for this grid before reading.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // Stage q rows of this chunk as fp16 hi/lo in mma B-fragment order:
     // entry (block b, n-tile nt, hi|lo, lane g*4+t) holds row 8nt+g, dims 32b+8t .. +7.
-    // One entry = 8 consecutive dims of one row: two float4 loads, one 16-byte store each
-    // for hi and lo; all loads of a thread are issued before any is used.
     {
         constexpr int GPR = HD / 8;                       // 8-dim groups per row
         constexpr int PER = (RP * GPR + kThreads - 1) / kThreads;
@@ -180,6 +179,14 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
                 v[k][1] = __ldg(src + 1);
             }
         }
+        // The first K tile is requested after the q loads, so those are not queued behind
+        // every block's first tile; K alone lands in about half the time of K + V.  The V
+        // tile of each iteration is requested once its K has landed (top of the loop).
+        if (key_begin < key_end) {
+            load_codes<HD>(sK, p.k_codes, head_row0, key_begin, key_end);
+            load_scales<HD>(smem + L::kKs, p.k_scales, head_row0, key_begin, key_end);
+        }
+        cp_async_commit();
 #pragma unroll
         for (int k = 0; k < PER; ++k) {
             const int idx = threadIdx.x + k * kThreads;
@@ -193,8 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
                 const float a = x[2 * e] * p.qscale, b = x[2 * e + 1] * p.qscale;
                 const __half2 h = __floats2half2_rn(a, b);
                 const __half2 l = __floats2half2_rn(a - __low2float(h), b - __high2float(h));
-                hi[e] = *reinterpret_cast<const uint32_t*>(&h);
-                lo[e] = *reinterpret_cast<const uint32_t*>(&l);
+                hi[e] = h2_as_u32(h);
+                lo[e] = h2_as_u32(l);
             }
             const int b = j8 >> 2, tt = j8 & 3, nt = r >> 3, gg = r & 7;
             uint4* dst = reinterpret_cast<uint4*>(sQ + ((b * NT + nt) * 2) * 256 + (gg * 4 + tt) * 8);
@@ -203,71 +210,70 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
         }
     }
 
-    // Visibility bound per owned row: row rr sees keys < vis_end.
-    int vis_end[NT][2];
+    // Visibility bound per owned row (row rr sees keys < vis_end) and its output row
+    // (-1 for padding rows).
+    int vis_end[NT][2], grow[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
             const int r = 8 * nt + 2 * t + c;
             if (r < rows_here) {
-                const int i = (row0 + r) / p.group;
+                const int rr = row0 + r;
+                const int i = rr / p.group, hh = rr - i * p.group;
                 vis_end[nt][c] = min(min(p.q_pos0 + i + 1, p.kv_len), key_end);
+                grow[nt][c] = i * p.n_q_heads + kvh * p.group + hh;
             } else {
                 vis_end[nt][c] = 0;
+                grow[nt][c] = -1;
             }
         }
 
     // every real row of this chunk sees all keys below vis_min; padding rows hold q = 0 and
     // never reach the output, so tiles wholly below vis_min skip the mask
     const int vis_min = min(min(p.q_pos0 + row0 / p.group + 1, p.kv_len), key_end);
-    float m_run[NT][2], l_run[NT][2];
+    float m_ref[NT][2], l_w[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-            m_run[nt][c] = -INFINITY;
-            l_run[nt][c] = 0.0f;
+            m_ref[nt][c] = -INFINITY;
+            l_w[nt][c] = 0.0f;
         }
-    float O[BPW][2][NT][4];
+    float O[MTW][NT][4];
 #pragma unroll
-    for (int i = 0; i < BPW; ++i)
+    for (int mt = 0; mt < MTW; ++mt)
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) O[i][mt][nt][c] = 0.0f;
-    int E[BPW];
-#pragma unroll
-    for (int i = 0; i < BPW; ++i) E[i] = INT32_MIN;  // unset
-
+            for (int c = 0; c < 4; ++c) O[mt][nt][c] = 0.0f;
+    int E = INT32_MIN;  // unset
 
     for (int tile0 = key_begin; tile0 < key_end; tile0 += kKT) {
-        cp_async_wait<1>();  // K of this tile landed (V may still be in flight)
-        __syncthreads();
+        const int nk = min(kKT, key_end - tile0);  // keys of this tile inside the slice
+        cp_async_wait<0>();  // K of this tile landed (the only copy group in flight)
+        __syncthreads();     // ... for every thread; and every warp is done with the previous sV
+        load_codes<HD>(sV, p.v_codes, head_row0, tile0, key_end);
+        load_scales<HD>(smem + L::kVs, p.v_scales, head_row0, tile0, key_end);
+        cp_async_commit();
 
-        // ---------------- QK^T: S^T[key][row] for this warp's 32 keys ----------------
-        float S[2][NT][4];
+        // ---------------- QK^T: S^T[key][row] for this warp's 16 keys ----------------
+        float S[NT][4];
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) S[mt][nt][c] = 0.0f;
-
+            for (int c = 0; c < 4; ++c) S[nt][c] = 0.0f;
+        const int n0 = warp * 16 + g;
+        if (warp * 16 < nk) {
 #pragma unroll 2
-        for (int b = 0; b < NB; ++b) {
-            uint4 qh[NT], ql[NT];
+            for (int b = 0; b < NB; ++b) {
+                uint4 qh[NT], ql[NT];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const uint4* qp = reinterpret_cast<const uint4*>(sQ + ((b * NT + nt) * 2) * 256) + lane;
-                qh[nt] = qp[0];
-                ql[nt] = qp[32];
-            }
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                const int n0 = warp * 32 + mt * 16 + g;
+                for (int nt = 0; nt < NT; ++nt) {
+                    const uint4* qp = reinterpret_cast<const uint4*>(sQ + ((b * NT + nt) * 2) * 256) + lane;
+                    qh[nt] = qp[0];
+                    ql[nt] = qp[32];
+                }
                 const uint2 k0 = *reinterpret_cast<const uint2*>(sK + swz<HD>(n0, 32 * b + 8 * t));
                 const uint2 k1 = *reinterpret_cast<const uint2*>(sK + swz<HD>(n0 + 8, 32 * b + 8 * t));
                 const uint32_t x0 = k0.x ^ 0x80808080u, x1 = k1.x ^ 0x80808080u;
@@ -289,38 +295,61 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
                 const float dk1 = half_bits_to_float(sKs[(n0 + 8) * NB + b]);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    S[mt][nt][0] = fmaf(dk0, tmp[nt][0], S[mt][nt][0]);
-                    S[mt][nt][1] = fmaf(dk0, tmp[nt][1], S[mt][nt][1]);
-                    S[mt][nt][2] = fmaf(dk1, tmp[nt][2], S[mt][nt][2]);
-                    S[mt][nt][3] = fmaf(dk1, tmp[nt][3], S[mt][nt][3]);
+                    S[nt][0] = fmaf(dk0, tmp[nt][0], S[nt][0]);
+                    S[nt][1] = fmaf(dk0, tmp[nt][1], S[nt][1]);
+                    S[nt][2] = fmaf(dk1, tmp[nt][2], S[nt][2]);
+                    S[nt][3] = fmaf(dk1, tmp[nt][3], S[nt][3]);
                 }
             }
         }
 
-        // ---------------- mask + per-warp row max ----------------
+        // ---------------- mask; does any score pass its row's reference by more than kLazy? ----------------
         const bool tile_needs_mask = tile0 + kKT > vis_min;
-        float mx[NT][2];
+        bool need = false;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                float m = -INFINITY;
+            for (int c = 0; c < 2; ++c)
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt)
+                for (int h = 0; h < 2; ++h) {
+                    const int key = tile0 + n0 + 8 * h;
+                    float& s = S[nt][2 * h + c];
+                    if (tile_needs_mask && key >= vis_end[nt][c]) s = -INFINITY;
+                    need |= s > m_ref[nt][c] + kLazy;
+                }
+        // barrier: every warp is done with sK, and the vote is known to all
+        if (__syncthreads_or(need)) {
+            // exact tile maxima: per warp over its 16 keys, then over the 8 warps
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int key = tile0 + warp * 32 + mt * 16 + g + 8 * h;
-                        float& s = S[mt][nt][2 * h + c];
-                        if (tile_needs_mask && key >= vis_end[nt][c]) s = -INFINITY;
-                        m = fmaxf(m, s);
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    float m = fmaxf(S[nt][c], S[nt][2 + c]);
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                    if (g == 0) sRed[(8 * nt + 2 * t + c) * kWarps + warp] = m;
+                }
+            __syncthreads();
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const float4* rp = reinterpret_cast<const float4*>(sRed + (8 * nt + 2 * t + c) * kWarps);
+                    const float4 u = rp[0], w = rp[1];
+                    const float mt_ = fmaxf(fmaxf(fmaxf(u.x, u.y), fmaxf(u.z, u.w)), fmaxf(fmaxf(w.x, w.y), fmaxf(w.z, w.w)));
+                    const float m_old = m_ref[nt][c];
+                    const float m_new = fmaxf(m_old, mt_);
+                    const float a = (m_old == -INFINITY) ? 1.0f : ex2_approx(m_old - m_new);
+                    m_ref[nt][c] = m_new;
+                    l_w[nt][c] *= a;
+#pragma unroll
+                    for (int mt = 0; mt < MTW; ++mt) {
+                        O[mt][nt][c] *= a;
+                        O[mt][nt][2 + c] *= a;
                     }
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-                mx[nt][c] = m;
-                if (g == 0) sRedMax[warp * RP + 8 * nt + 2 * t + c] = m;
-            }
-        __syncthreads();  // all warps done reading sK; row maxima visible
+                }
+        }
 
         {  // stream the next tile's K while softmax and PV run
             const int next0 = tile0 + kKT;
@@ -331,125 +360,81 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
             cp_async_commit();
         }
 
-        // ---------------- softmax: p = 2^(s - m_new) ----------------
-        float alpha[NT][2];
+        // ---------------- softmax: p = 2^(s - m_ref), stored as p 2^kPShift ----------------
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                const int r = 8 * nt + 2 * t + c;
-                float mt_ = sRedMax[r];
+                const float mb = (m_ref[nt][c] == -INFINITY) ? 0.0f : m_ref[nt][c] - kPShift;
+                float sum = 0.0f;
 #pragma unroll
-                for (int w = 1; w < kWarps; ++w) mt_ = fmaxf(mt_, sRedMax[w * RP + r]);
-                const float m_new = fmaxf(m_run[nt][c], mt_);
-                float a = 1.0f, sum = 0.0f;
-                if (m_new != -INFINITY) {
-                    a = ex2_approx(m_run[nt][c] - m_new);
-#pragma unroll
-                    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            float& s = S[mt][nt][2 * h + c];
-                            s = ex2_approx(s - m_new);
-                            sum += s;
-                        }
-                } else {
-#pragma unroll
-                    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) S[mt][nt][2 * h + c] = 0.0f;
+                for (int h = 0; h < 2; ++h) {
+                    float& s = S[nt][2 * h + c];
+                    s = ex2_approx(s - mb);
+                    sum += s;
                 }
-                m_run[nt][c] = m_new;
-                alpha[nt][c] = a;
-                sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 8);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 16);
-                if (g == 0) {
-                    sRedSum[warp * RP + r] = sum;
-                    if (warp == 0) sAlpha[r] = a;
-                }
+                l_w[nt][c] += sum;
             }
-        (void)mx;
         // P tile: a key and its pair partner sit in lanes 4 apart; each pair of lanes swaps one
         // value so that the even-g lane writes row 2t and the odd-g lane row 2t+1.
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const float v0 = S[mt][nt][2 * h], v1 = S[mt][nt][2 * h + 1];
-                    const bool ev = (g & 1) == 0;
-                    const float recv = __shfl_xor_sync(0xffffffffu, ev ? v1 : v0, 4);
-                    const float pe = (ev ? v0 : recv) * 4096.0f;  // even key
-                    const float po = (ev ? recv : v1) * 4096.0f;  // odd key
-                    const __half2 ph = __floats2half2_rn(pe, po);
-                    const __half2 pl = __floats2half2_rn(pe - __low2float(ph), po - __high2float(ph));
-                    const int kl = warp * 32 + mt * 16 + g + 8 * h;
-                    sP[(kl >> 1) * PS + 8 * nt + 2 * t + (ev ? 0 : 1)] = make_uint2(h2_as_u32(ph), h2_as_u32(pl));
-                }
+            for (int nt = 0; nt < NT; ++nt) {
+                const float v0 = S[nt][2 * h], v1 = S[nt][2 * h + 1];
+                const bool ev = (g & 1) == 0;
+                const float recv = __shfl_xor_sync(0xffffffffu, ev ? v1 : v0, 4);
+                const float pe = ev ? v0 : recv;  // even key
+                const float po = ev ? recv : v1;  // odd key
+                const __half2 ph = __floats2half2_rn(pe, po);
+                const __half2 pl = __floats2half2_rn(pe - __low2float(ph), po - __high2float(ph));
+                const int kl = n0 + 8 * h;
+                sP[(kl >> 1) * PS + 8 * nt + 2 * t + (ev ? 0 : 1)] = make_uint2(h2_as_u32(ph), h2_as_u32(pl));
+            }
 
         cp_async_wait<1>();  // V of this tile landed (next K may still be in flight)
         __syncthreads();
 
-        if (warp == 0) {
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int r = 8 * nt + 2 * t + c;
-                    float s = 0.0f;
-#pragma unroll
-                    for (int w = 0; w < kWarps; ++w) s += sRedSum[w * RP + r];
-                    l_run[nt][c] = l_run[nt][c] * alpha[nt][c] + s;
-                }
-        }
-
-        // ---------------- PV: O^T[dim][row] += V^T * (p 2^12) (dV 2^E) ----------------
+        // ---------------- PV: O^T[dim][row] += V^T * (p 2^kPShift) (dV 2^E) ----------------
         // Per output block, E keeps dV 2^E of the tile's largest scale in [2, 4), so that
-        // w = (p 2^12)(dV 2^E) < 2^14 stays in the fp16 range.  w = hi + lo exactly up to
+        // w = (p 2^kPShift)(dV 2^E) < 2^14 stays in the fp16 range; w = hi + lo exactly up to
         // 2^-22: hi = fl(ph d), lo = fl((ph d - hi) + pl d), the first residual exact by FMA.
-        float esc[BPW];
-#pragma unroll
-        for (int i = 0; i < BPW; ++i) {
-            const int b = warp + kWarps * i;
+        // The warp's scaled block scales go to its own fp16 table, read as key pairs below.
+        {
+            float dv[kKT / 32];
             float dmax = 0.0f;
 #pragma unroll
-            for (int k = 0; k < kKT / 32; ++k) dmax = fmaxf(dmax, half_bits_to_float(sVs[(lane + 32 * k) * NB + b]));
+            for (int k = 0; k < kKT / 32; ++k) {
+                dv[k] = half_bits_to_float(sVs[(lane + 32 * k) * NB + pvb]);
+                dmax = fmaxf(dmax, dv[k]);
+            }
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, o));
             if (dmax > 0.0f) {
                 int e2;
                 (void)frexpf(dmax, &e2);
                 const int et = 2 - e2;
-                if (E[i] == INT32_MIN) {
-                    E[i] = et;
-                } else if (et < E[i]) {
-                    const float f = ldexpf(1.0f, et - E[i]);
+                if (E == INT32_MIN) {
+                    E = et;
+                } else if (et < E) {
+                    const float f = ldexpf(1.0f, et - E);
 #pragma unroll
-                    for (int mt = 0; mt < 2; ++mt)
+                    for (int mt = 0; mt < MTW; ++mt)
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                            for (int c = 0; c < 4; ++c) O[i][mt][nt][c] *= f;
-                    E[i] = et;
+                            for (int c = 0; c < 4; ++c) O[mt][nt][c] *= f;
+                    E = et;
                 }
             }
-            esc[i] = (E[i] == INT32_MIN) ? 0.0f : ldexpf(1.0f, E[i]);
+            const float esc = (E == INT32_MIN) ? 0.0f : ldexpf(1.0f, E);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const float a0 = sAlpha[8 * nt + 2 * t], a1 = sAlpha[8 * nt + 2 * t + 1];
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    O[i][mt][nt][0] *= a0;
-                    O[i][mt][nt][1] *= a1;
-                    O[i][mt][nt][2] *= a0;
-                    O[i][mt][nt][3] *= a1;
-                }
-            }
+            for (int k = 0; k < kKT / 32; ++k) sDv[lane + 32 * k] = __half_as_ushort(__float2half_rn(dv[k] * esc));
+            __syncwarp();
         }
+        const int n_ks = (nk + 15) >> 4;
 #pragma unroll 2
-        for (int ks = 0; ks < kKT / 16; ++ks) {
+        for (int ks = 0; ks < n_ks; ++ks) {
             const int kb = ks * 16;
             uint2 pp01[NT], pp89[NT];  // (hi, lo) pairs of keys (2t, 2t+1) and (2t+8, 2t+9), row g of n-tile
 #pragma unroll
@@ -457,101 +442,92 @@ __global__ void __launch_bounds__(kThreads, 1) verify_split_kernel(const VerifyP
                 pp01[nt] = sP[((kb >> 1) + t) * PS + 8 * nt + g];
                 pp89[nt] = sP[((kb >> 1) + t + 4) * PS + 8 * nt + g];
             }
+            const __half2 d01 = u32_as_h2(*reinterpret_cast<const uint32_t*>(sDv + kb + 2 * t));
+            const __half2 d89 = u32_as_h2(*reinterpret_cast<const uint32_t*>(sDv + kb + 2 * t + 8));
+            const int cb = 32 * pvb + 4 * g;
+            const uint32_t w0 = *reinterpret_cast<const uint32_t*>(sV + swz<HD>(kb + 2 * t, cb)) ^ 0x80808080u;
+            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(sV + swz<HD>(kb + 2 * t + 1, cb)) ^ 0x80808080u;
+            const uint32_t w8 = *reinterpret_cast<const uint32_t*>(sV + swz<HD>(kb + 2 * t + 8, cb)) ^ 0x80808080u;
+            const uint32_t w9 = *reinterpret_cast<const uint32_t*>(sV + swz<HD>(kb + 2 * t + 9, cb)) ^ 0x80808080u;
+            uint32_t A[MTW][4];
+            if (HD == 256 || (warp & 1) == 0) {  // dims 4g, 4g+1 (and 4g+2, 4g+3 at hd256)
+                const uint32_t y01 = prmt2<0x5140>(w0, w1), y89 = prmt2<0x5140>(w8, w9);
+                A[0][0] = biased_bytes_to_half2<0x4140>(y01);
+                A[0][1] = biased_bytes_to_half2<0x4342>(y01);
+                A[0][2] = biased_bytes_to_half2<0x4140>(y89);
+                A[0][3] = biased_bytes_to_half2<0x4342>(y89);
+            }
+            if (HD == 256 || (warp & 1) == 1) {  // dims 4g+2, 4g+3
+                const uint32_t y01 = prmt2<0x7362>(w0, w1), y89 = prmt2<0x7362>(w8, w9);
+                A[MTW - 1][0] = biased_bytes_to_half2<0x4140>(y01);
+                A[MTW - 1][1] = biased_bytes_to_half2<0x4342>(y01);
+                A[MTW - 1][2] = biased_bytes_to_half2<0x4140>(y89);
+                A[MTW - 1][3] = biased_bytes_to_half2<0x4342>(y89);
+            }
 #pragma unroll
-            for (int i = 0; i < BPW; ++i) {
-                const int b = warp + kWarps * i;
-                const int cb = 32 * b + 4 * g;
-                const uint32_t w0 = *reinterpret_cast<const uint32_t*>(sV + swz<HD>(kb + 2 * t, cb)) ^ 0x80808080u;
-                const uint32_t w1 = *reinterpret_cast<const uint32_t*>(sV + swz<HD>(kb + 2 * t + 1, cb)) ^ 0x80808080u;
-                const uint32_t w8 = *reinterpret_cast<const uint32_t*>(sV + swz<HD>(kb + 2 * t + 8, cb)) ^ 0x80808080u;
-                const uint32_t w9 = *reinterpret_cast<const uint32_t*>(sV + swz<HD>(kb + 2 * t + 9, cb)) ^ 0x80808080u;
-                const uint32_t y01lo = prmt2<0x5140>(w0, w1), y01hi = prmt2<0x7362>(w0, w1);
-                const uint32_t y89lo = prmt2<0x5140>(w8, w9), y89hi = prmt2<0x7362>(w8, w9);
-                uint32_t A[2][4];
-                A[0][0] = biased_bytes_to_half2<0x4140>(y01lo);
-                A[0][1] = biased_bytes_to_half2<0x4342>(y01lo);
-                A[0][2] = biased_bytes_to_half2<0x4140>(y89lo);
-                A[0][3] = biased_bytes_to_half2<0x4342>(y89lo);
-                A[1][0] = biased_bytes_to_half2<0x4140>(y01hi);
-                A[1][1] = biased_bytes_to_half2<0x4342>(y01hi);
-                A[1][2] = biased_bytes_to_half2<0x4140>(y89hi);
-                A[1][3] = biased_bytes_to_half2<0x4342>(y89hi);
-                const __half2 d01 = __floats2half2_rn(half_bits_to_float(sVs[(kb + 2 * t) * NB + b]) * esc[i],
-                                                      half_bits_to_float(sVs[(kb + 2 * t + 1) * NB + b]) * esc[i]);
-                const __half2 d89 = __floats2half2_rn(half_bits_to_float(sVs[(kb + 2 * t + 8) * NB + b]) * esc[i],
-                                                      half_bits_to_float(sVs[(kb + 2 * t + 9) * NB + b]) * esc[i]);
+            for (int nt = 0; nt < NT; ++nt) {
+                const __half2 ph0 = u32_as_h2(pp01[nt].x), pl0 = u32_as_h2(pp01[nt].y);
+                const __half2 ph1 = u32_as_h2(pp89[nt].x), pl1 = u32_as_h2(pp89[nt].y);
+                const __half2 h0 = __hmul2(ph0, d01);
+                const __half2 h1 = __hmul2(ph1, d89);
+                const __half2 l0 = __hfma2(pl0, d01, __hfma2(ph0, d01, __hneg2(h0)));
+                const __half2 l1 = __hfma2(pl1, d89, __hfma2(ph1, d89, __hneg2(h1)));
+                const uint32_t bh0 = h2_as_u32(h0), bh1 = h2_as_u32(h1);
+                const uint32_t bl0 = h2_as_u32(l0), bl1 = h2_as_u32(l1);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const __half2 ph0 = u32_as_h2(pp01[nt].x), pl0 = u32_as_h2(pp01[nt].y);
-                    const __half2 ph1 = u32_as_h2(pp89[nt].x), pl1 = u32_as_h2(pp89[nt].y);
-                    const __half2 h0 = __hmul2(ph0, d01);
-                    const __half2 h1 = __hmul2(ph1, d89);
-                    const __half2 l0 = __hfma2(pl0, d01, __hfma2(ph0, d01, __hneg2(h0)));
-                    const __half2 l1 = __hfma2(pl1, d89, __hfma2(ph1, d89, __hneg2(h1)));
-                    const uint32_t bh0 = h2_as_u32(h0), bh1 = h2_as_u32(h1);
-                    const uint32_t bl0 = h2_as_u32(l0), bl1 = h2_as_u32(l1);
-#pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) {
-                        mma_f16_16816(O[i][mt][nt], A[mt][0], A[mt][1], A[mt][2], A[mt][3], bh0, bh1);
-                        mma_f16_16816(O[i][mt][nt], A[mt][0], A[mt][1], A[mt][2], A[mt][3], bl0, bl1);
-                    }
+                for (int mt = 0; mt < MTW; ++mt) {
+                    mma_f16_16816(O[mt][nt], A[mt][0], A[mt][1], A[mt][2], A[mt][3], bh0, bh1);
+                    mma_f16_16816(O[mt][nt], A[mt][0], A[mt][1], A[mt][2], A[mt][3], bl0, bl1);
                 }
             }
         }
-        __syncthreads();  // all warps done with sV and sP
-
-        {  // stream the next tile's V while the next QK runs
-            const int next0 = tile0 + kKT;
-            if (next0 < key_end) {
-                load_codes<HD>(sV, p.v_codes, head_row0, next0, key_end);
-                load_scales<HD>(smem + L::kVs, p.v_scales, head_row0, next0, key_end);
-            }
-            cp_async_commit();
-        }
+        __syncthreads();  // all warps done with sV, sP and the scale tables
     }
     cp_async_wait<0>();
 
     // ---------------- write the slice partial ----------------
-    // Each lane owns dims 32b + 4g .. +3 of rows 8nt + 2t + c: one 16-byte store per row, and
-    // the 8 lanes of a row cover 128 contiguous bytes, so every L2 sector is written whole.
-    float* po = p.part_o + (int64_t)split * rows_total * HD;
-    int64_t grow[NT][2];
+    // row sums: over the lanes that share a row (g), then over the warps
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-            const int r = 8 * nt + 2 * t + c;
-            const int rr = row0 + r;
-            const int iq = rr / p.group, hh = rr - iq * p.group;
-            grow[nt][c] = (r < rows_here) ? (int64_t)iq * p.n_q_heads + kvh * p.group + hh : -1;
+            float l = l_w[nt][c];
+            l += __shfl_xor_sync(0xffffffffu, l, 4);
+            l += __shfl_xor_sync(0xffffffffu, l, 8);
+            l += __shfl_xor_sync(0xffffffffu, l, 16);
+            if (g == 0) sRed[(8 * nt + 2 * t + c) * kWarps + warp] = l;
         }
+    __syncthreads();
+    float* po = p.part_o + (int64_t)split * rows_total * HD;
+    // O is (p 2^kPShift)(v 2^E) summed; lane owns dims 32b + 4g .. +3 (hd256) or the pair at
+    // 32b + 4g + 2(w & 1) (hd128) of rows 8nt + 2t + c
+    const float inv = (E == INT32_MIN) ? 1.0f : ldexpf(1.0f, -E - (int)kPShift);
 #pragma unroll
-    for (int i = 0; i < BPW; ++i) {
-        const int b = warp + kWarps * i;
-        const float inv = (E[i] == INT32_MIN) ? 1.0f : ldexpf(1.0f, -E[i] - 12);
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            if (grow[nt][c] < 0) continue;
+            float* dst = po + (int64_t)grow[nt][c] * HD + 32 * pvb + 4 * g;
+            if constexpr (HD == 256) {
+                *reinterpret_cast<float4*>(dst) = make_float4(O[0][nt][c] * inv, O[0][nt][2 + c] * inv,
+                                                              O[1][nt][c] * inv, O[1][nt][2 + c] * inv);
+            } else {
+                *reinterpret_cast<float2*>(dst + 2 * (warp & 1)) = make_float2(O[0][nt][c] * inv, O[0][nt][2 + c] * inv);
+            }
+        }
+    if (warp == 0 && g == 0) {
+        const float lscale = ldexpf(1.0f, -(int)kPShift);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 if (grow[nt][c] < 0) continue;
-                *reinterpret_cast<float4*>(po + grow[nt][c] * HD + 32 * b + 4 * g) =
-                    make_float4(O[i][0][nt][c] * inv, O[i][0][nt][2 + c] * inv, O[i][1][nt][c] * inv,
-                                O[i][1][nt][2 + c] * inv);
-            }
-    }
-    if (warp == 0 && g == 0) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int r = 8 * nt + 2 * t + c;
-                if (r >= rows_here) continue;
-                const int rr = row0 + r;
-                const int iq = rr / p.group, hh = rr - iq * p.group;
-                const int64_t grow = (int64_t)iq * p.n_q_heads + kvh * p.group + hh;
-                const float m = m_run[nt][c];
-                p.part_ml[(int64_t)split * rows_total + grow] =
-                    make_float2(m == -INFINITY ? -INFINITY : m * kLn2, l_run[nt][c]);
+                const float4* rp = reinterpret_cast<const float4*>(sRed + (8 * nt + 2 * t + c) * kWarps);
+                const float4 u = rp[0], w = rp[1];
+                const float l = ((u.x + u.y) + (u.z + u.w)) + ((w.x + w.y) + (w.z + w.w));
+                const float m = m_ref[nt][c];
+                p.part_ml[(int64_t)split * rows_total + grow[nt][c]] =
+                    make_float2(m == -INFINITY ? -INFINITY : m * kLn2, l * lscale);
             }
     }
 }
@@ -580,16 +556,21 @@ int make_plan(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_kv_head
     pl->n_chunks = (R + 8 * kMaxNT - 1) / (8 * kMaxNT);
     pl->rows_per_chunk = (R + pl->n_chunks - 1) / pl->n_chunks;
     pl->nt = (pl->rows_per_chunk + 7) / 8;
-    const int n_tiles = (kv_len + kKT - 1) / kKT;
+    // slices are whole 64-key units; the automatic count fills every SM with as many thread
+    // blocks as fit at once (two for NT <= 3, one at NT = 4)
+    const int n_units = (kv_len + kSplitUnit - 1) / kSplitUnit;
     int ns = n_split_req;
     if (ns == 0) {
         int sms = sm_count();
         if (sms <= 0) sms = 152;
-        ns = std::max(1, (2 * sms) / (n_kv_heads * pl->n_chunks));
+        const int per_sm = pl->nt <= 3 ? 2 : 1;
+        ns = std::max(1, (per_sm * sms) / (n_kv_heads * pl->n_chunks));
     }
-    ns = std::min(ns, n_tiles);
-    const int tiles_per_split = (n_tiles + ns - 1) / ns;
-    pl->keys_per_split = tiles_per_split * kKT;
+    ns = std::min(ns, n_units);
+    // an automatic slice holds at least one whole 128-key tile
+    const int min_units = n_split_req > 0 ? 1 : kKT / kSplitUnit;
+    const int units_per_split = std::max(min_units, (n_units + ns - 1) / ns);
+    pl->keys_per_split = units_per_split * kSplitUnit;
     pl->n_split = (kv_len + pl->keys_per_split - 1) / pl->keys_per_split;
     const size_t rows_total = (size_t)n_rows * n_q_heads;
     const size_t o_bytes = (size_t)pl->n_split * rows_total * head_dim * sizeof(float);
