@@ -10,6 +10,8 @@
 // block needs -- the (m, l) of all splits and each thread's first kPrefetch partial vectors --
 // is issued before any of them is used, so a row costs about one memory round trip plus two
 // block reductions.  The split groups' sums are added in shared memory at the end.
+// With few splits and many rows (the prompt path) a flat kernel is used instead: one thread
+// per float4 of a row, looping over the splits.
 #include "common.cuh"
 
 namespace kvq8 {
@@ -120,6 +122,48 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float4* 
     }
 }
 
+// Few splits, many rows (the prompt path): one thread per float4 of a row, looping over the
+// splits itself; the (m, l) pairs of a row are shared by its hd/4 threads through L1.
+constexpr int kWideMaxSplits = 16;
+constexpr int kWideThreads = 256;
+
+__global__ void __launch_bounds__(kWideThreads) combine_wide_kernel(const float4* __restrict__ part_o,
+                                                                    const float2* __restrict__ part_ml,
+                                                                    int n_split, int rows, int hd4,
+                                                                    float* __restrict__ out) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int64_t idx = (int64_t)blockIdx.x * kWideThreads + threadIdx.x;
+    if (idx >= (int64_t)rows * hd4) return;
+    const int row = (int)(idx / hd4);
+    const int64_t stride = (int64_t)rows * hd4;
+    float2 ml[kWideMaxSplits];
+    float4 o[kWideMaxSplits];
+    float ms = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < kWideMaxSplits; ++s) {
+        if (s < n_split) {
+            ml[s] = __ldg(part_ml + (int64_t)s * rows + row);
+            o[s] = __ldg(part_o + idx + s * stride);
+            ms = fmaxf(ms, ml[s].x);
+        }
+    }
+    float l = 0.0f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < kWideMaxSplits; ++s) {
+        if (s < n_split) {
+            const float w = (ms == -INFINITY || ml[s].x == -INFINITY) ? 0.0f : expf(ml[s].x - ms);
+            l = fmaf(w, ml[s].y, l);
+            acc.x = fmaf(w, o[s].x, acc.x);
+            acc.y = fmaf(w, o[s].y, acc.y);
+            acc.z = fmaf(w, o[s].z, acc.z);
+            acc.w = fmaf(w, o[s].w, acc.w);
+        }
+    }
+    const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
+    reinterpret_cast<float4*>(out)[idx] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+}
+
 }  // namespace
 
 int launch_combine(const float* part_o, const float* part_ml, int n_split, int rows, int head_dim, float* out,
@@ -129,17 +173,27 @@ int launch_combine(const float* part_o, const float* part_ml, int n_split, int r
     // Programmatic dependent launch: the grid may be scheduled while the kernel before it in
     // the stream is still running; griddepcontrol.wait in the kernel orders the reads.
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(rows, (hd4 + kColThreads - 1) / kColThreads);
-    cfg.blockDim = dim3(kCombineThreads);
-    cfg.dynamicSmemBytes = (size_t)n_split * sizeof(float2);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, combine_kernel, reinterpret_cast<const float4*>(part_o),
-                                             reinterpret_cast<const float2*>(part_ml), n_split, rows, hd4, out);
+    cudaError_t e;
+    const int64_t threads = (int64_t)rows * hd4;
+    if (n_split <= kWideMaxSplits && threads >= (1 << 18)) {  // many rows: one thread per float4
+        cfg.gridDim = dim3((unsigned)((threads + kWideThreads - 1) / kWideThreads));
+        cfg.blockDim = dim3(kWideThreads);
+        cfg.dynamicSmemBytes = 0;
+        e = cudaLaunchKernelEx(&cfg, combine_wide_kernel, reinterpret_cast<const float4*>(part_o),
+                               reinterpret_cast<const float2*>(part_ml), n_split, rows, hd4, out);
+    } else {
+        cfg.gridDim = dim3(rows, (hd4 + kColThreads - 1) / kColThreads);
+        cfg.blockDim = dim3(kCombineThreads);
+        cfg.dynamicSmemBytes = (size_t)n_split * sizeof(float2);
+        e = cudaLaunchKernelEx(&cfg, combine_kernel, reinterpret_cast<const float4*>(part_o),
+                               reinterpret_cast<const float2*>(part_ml), n_split, rows, hd4, out);
+    }
     return e == cudaSuccess ? KVQ8_OK : KVQ8_ERR_CUDA;
 }
 

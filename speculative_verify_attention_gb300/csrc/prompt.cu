@@ -8,12 +8,12 @@
 //
 // GB300 design: one CTA per (128-row tile of (query, head) pairs, KV head); rows r = i*g + hh
 // of one KV head, so the 12 heads of a query and ~11 consecutive queries share every K/V
-// tile.  Ten warps, each with one role:
+// tile.  Fourteen warps, each with one role:
 //   warp 0      producer: 1-D bulk async copies of the int8 codes and fp16 scales of a
 //               64-key tile into a 2-stage staging ring (mbarrier transaction counts);
 //   warp 1      MMA issuer (one thread) and tensor-memory owner;
 //   warps 2-5   softmax, one thread per row (each warp reads its 32-lane quarter of TMEM);
-//   warps 6-9   dequantisers: int8 -> fp16 exactly (byte permute + magic-bias subtract), then
+//   warps 6-13  dequantisers: int8 -> fp16 exactly (byte permute + magic-bias subtract), then
 //               times the block scale (one fp16 rounding), written to double-buffered
 //               128-byte-swizzled K^ and V^ tiles in shared memory.
 // Tensor memory (512 columns): Q as fp16 pairs (128), O fp32 (256), two S buffers (64 each)
@@ -23,7 +23,8 @@
 // The softmax keeps a per-row reference maximum and rescales the O row in TMEM only when a
 // new maximum exceeds it by more than 2^8, so p stays <= 256 in fp16.  Tiles past the
 // causal bound of the last row are never loaded; only the diagonal tile is masked.
-// Every mbarrier wait is bounded: on timeout the kernel records an error flag (read with
+// Barriers that many threads signal take one arrival per warp (after __syncwarp), not one
+// per thread.  Every mbarrier wait is bounded: on timeout the kernel records an error flag (read with
 // kvq8_device_error) and returns after releasing its tensor memory.
 #include "common.cuh"
 #include "tc.cuh"
@@ -181,16 +182,16 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptPa
         *n_seg_slot = cta_segments(p, blockIdx.x, gridDim.x, seg);
         for (int s = 0; s < 2; ++s) {
             tc::mbar_init(B(B_ST_FULL + s), 1);
-            tc::mbar_init(B(B_ST_EMPTY + s), kDeqThreads);
-            tc::mbar_init(B(B_K_FULL + s), kDeqThreads);
-            tc::mbar_init(B(B_V_FULL + s), kDeqThreads);
+            tc::mbar_init(B(B_ST_EMPTY + s), kDeqThreads / 32);  // one arrival per warp
+            tc::mbar_init(B(B_K_FULL + s), kDeqThreads / 32);
+            tc::mbar_init(B(B_V_FULL + s), kDeqThreads / 32);
             tc::mbar_init(B(B_K_EMPTY + s), 1);
             tc::mbar_init(B(B_V_EMPTY + s), 1);
             tc::mbar_init(B(B_S_FULL + s), 1);
-            tc::mbar_init(B(B_P_FULL + s), 128);
+            tc::mbar_init(B(B_P_FULL + s), 4);
             tc::mbar_init(B(B_PV_DONE + s), 1);
         }
-        tc::mbar_init(B(B_Q_READY), 128);
+        tc::mbar_init(B(B_Q_READY), 4);
         tc::mbar_init_fence();
     }
     if (warp == 1) tc::tmem_alloc(smem_u32(tmem_slot), TM_NCOLS);
@@ -275,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptPa
                 flag_timeout();
         }
         __syncwarp();
-    } else if (warp < kDeqWarp0) {
+    } else if (warp >= kSoftWarp0 && warp < kDeqWarp0) {
         // ---------------------------------------------------------------- softmax (one row per thread)
         const int quad = warp & 3;
         const int r = quad * 32 + lane;
@@ -311,7 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptPa
                 }
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
-                tc::mbar_arrive(B(B_Q_READY));
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(B(B_Q_READY));
             }
             float m_ref = -INFINITY, l = 0.0f;
             for (int t = seg[si].t0; t < seg[si].t1; ++t, ++j) {
@@ -380,7 +382,8 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptPa
                 tc::tmem_st32(scol, pk);  // P overwrites the first 32 columns of this S buffer
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
-                tc::mbar_arrive(B(B_P_FULL + b));
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(B(B_P_FULL + b));
             }
             if (!ok) break;
             // epilogue: the unnormalised partial (o, m, l) of this segment
@@ -420,20 +423,31 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptPa
             const Item g = item_geometry(seg[si].item, p.n_mtiles, p.rows, p.group, p.kv_len, p.q_pos0);
             for (int t = seg[si].t0; t < seg[si].t1; ++t, ++j) {
                 const int s = j & 1, use = j >> 1;
-                if (!tc::mbar_wait(B(B_ST_FULL + s), use & 1, kWaitLimit)) { ok = false; break; }
+                // waits are decided per warp, so that a warp arrives (lane 0) only as a whole
+                if (!__all_sync(0xffffffffu, tc::mbar_wait(B(B_ST_FULL + s), use & 1, kWaitLimit))) { ok = false; break; }
                 const int nk = min(BN, g.key_hi - t * BN);
                 const uint8_t* st = smem + SM_STAGE + s * STAGE_BYTES;
-                if (j >= 2 && !tc::mbar_wait(B(B_K_EMPTY + s), (use - 1) & 1, kWaitLimit)) { ok = false; break; }
+                if (j >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait(B(B_K_EMPTY + s), (use - 1) & 1, kWaitLimit))) {
+                    ok = false;
+                    break;
+                }
                 dequant_tile(st + ST_KC, reinterpret_cast<const uint16_t*>(st + ST_KS), smem + SM_KHAT + s * HAT_BYTES,
                              nk, d);
                 tc::fence_proxy_async_smem();
-                tc::mbar_arrive(B(B_K_FULL + s));
-                if (j >= 2 && !tc::mbar_wait(B(B_V_EMPTY + s), (use - 1) & 1, kWaitLimit)) { ok = false; break; }
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(B(B_K_FULL + s));
+                if (j >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait(B(B_V_EMPTY + s), (use - 1) & 1, kWaitLimit))) {
+                    ok = false;
+                    break;
+                }
                 dequant_tile(st + ST_VC, reinterpret_cast<const uint16_t*>(st + ST_VS), smem + SM_VHAT + s * HAT_BYTES,
                              nk, d);
                 tc::fence_proxy_async_smem();
-                tc::mbar_arrive(B(B_V_FULL + s));
-                tc::mbar_arrive(B(B_ST_EMPTY + s));
+                __syncwarp();
+                if (lane == 0) {
+                    tc::mbar_arrive(B(B_V_FULL + s));
+                    tc::mbar_arrive(B(B_ST_EMPTY + s));
+                }
             }
         }
         if (!ok) flag_timeout();
