@@ -11,7 +11,7 @@
 // is issued before any of them is used, so a row costs about one memory round trip plus two
 // block reductions.  The split groups' sums are added in shared memory at the end.
 // With few splits and many rows (the prompt path) a flat kernel is used instead: one thread
-// per float4 of a row, looping over the splits.
+// per four float4s of a row, looping over the splits.
 #include "common.cuh"
 
 namespace kvq8 {
@@ -122,46 +122,58 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float4* 
     }
 }
 
-// Few splits, many rows (the prompt path): one thread per float4 of a row, looping over the
-// splits itself; the (m, l) pairs of a row are shared by its hd/4 threads through L1.
-constexpr int kWideMaxSplits = 16;
+// Few splits, many rows (the prompt path): a thread takes kWideVec consecutive float4s of one
+// row and loops over the splits itself, with every load of the row issued before use.
+constexpr int kWideMaxSplits = 4;
 constexpr int kWideThreads = 256;
+constexpr int kWideVec = 4;
 
 __global__ void __launch_bounds__(kWideThreads) combine_wide_kernel(const float4* __restrict__ part_o,
                                                                     const float2* __restrict__ part_ml,
                                                                     int n_split, int rows, int hd4,
                                                                     float* __restrict__ out) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int64_t idx = (int64_t)blockIdx.x * kWideThreads + threadIdx.x;
-    if (idx >= (int64_t)rows * hd4) return;
-    const int row = (int)(idx / hd4);
+    const int per_row = hd4 / kWideVec;
+    const int64_t item = (int64_t)blockIdx.x * kWideThreads + threadIdx.x;
+    if (item >= (int64_t)rows * per_row) return;
+    const int row = (int)(item / per_row);
+    const int64_t idx = (int64_t)row * hd4 + (int64_t)(item - (int64_t)row * per_row) * kWideVec;
     const int64_t stride = (int64_t)rows * hd4;
     float2 ml[kWideMaxSplits];
-    float4 o[kWideMaxSplits];
+    float4 o[kWideMaxSplits][kWideVec];
     float ms = -INFINITY;
 #pragma unroll
     for (int s = 0; s < kWideMaxSplits; ++s) {
         if (s < n_split) {
             ml[s] = __ldg(part_ml + (int64_t)s * rows + row);
-            o[s] = __ldg(part_o + idx + s * stride);
+#pragma unroll
+            for (int v = 0; v < kWideVec; ++v) o[s][v] = __ldg(part_o + idx + s * stride + v);
             ms = fmaxf(ms, ml[s].x);
         }
     }
     float l = 0.0f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc[kWideVec];
+#pragma unroll
+    for (int v = 0; v < kWideVec; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int s = 0; s < kWideMaxSplits; ++s) {
         if (s < n_split) {
             const float w = (ms == -INFINITY || ml[s].x == -INFINITY) ? 0.0f : expf(ml[s].x - ms);
             l = fmaf(w, ml[s].y, l);
-            acc.x = fmaf(w, o[s].x, acc.x);
-            acc.y = fmaf(w, o[s].y, acc.y);
-            acc.z = fmaf(w, o[s].z, acc.z);
-            acc.w = fmaf(w, o[s].w, acc.w);
+#pragma unroll
+            for (int v = 0; v < kWideVec; ++v) {
+                acc[v].x = fmaf(w, o[s][v].x, acc[v].x);
+                acc[v].y = fmaf(w, o[s][v].y, acc[v].y);
+                acc[v].z = fmaf(w, o[s][v].z, acc[v].z);
+                acc[v].w = fmaf(w, o[s][v].w, acc[v].w);
+            }
         }
     }
     const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
-    reinterpret_cast<float4*>(out)[idx] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    float4* dst = reinterpret_cast<float4*>(out) + idx;
+#pragma unroll
+    for (int v = 0; v < kWideVec; ++v)
+        dst[v] = make_float4(acc[v].x * inv, acc[v].y * inv, acc[v].z * inv, acc[v].w * inv);
 }
 
 }  // namespace
@@ -180,8 +192,8 @@ int launch_combine(const float* part_o, const float* part_ml, int n_split, int r
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e;
-    const int64_t threads = (int64_t)rows * hd4;
-    if (n_split <= kWideMaxSplits && threads >= (1 << 18)) {  // many rows: one thread per float4
+    const int64_t threads = (int64_t)rows * (hd4 / kWideVec);
+    if (n_split <= kWideMaxSplits && hd4 % kWideVec == 0 && threads >= (1 << 16)) {  // many rows
         cfg.gridDim = dim3((unsigned)((threads + kWideThreads - 1) / kWideThreads));
         cfg.blockDim = dim3(kWideThreads);
         cfg.dynamicSmemBytes = 0;

@@ -8,12 +8,12 @@
 //
 // GB300 design: one CTA per (128-row tile of (query, head) pairs, KV head); rows r = i*g + hh
 // of one KV head, so the 12 heads of a query and ~11 consecutive queries share every K/V
-// tile.  Fourteen warps, each with one role:
+// tile.  Sixteen warps, each with one role:
 //   warp 0      producer: 1-D bulk async copies of the int8 codes and fp16 scales of a
 //               64-key tile into a 2-stage staging ring (mbarrier transaction counts);
 //   warp 1      MMA issuer (one thread) and tensor-memory owner;
 //   warps 2-5   softmax, one thread per row (each warp reads its 32-lane quarter of TMEM);
-//   warps 6-13  dequantisers: int8 -> fp16 exactly (byte permute + magic-bias subtract), then
+//   warps 6-15  dequantisers: int8 -> fp16 exactly (byte permute + magic-bias subtract), then
 //               times the block scale (one fp16 rounding), written to double-buffered
 //               128-byte-swizzled K^ and V^ tiles in shared memory.
 // Tensor memory (512 columns): Q as fp16 pairs (128), O fp32 (256), two S buffers (64 each)
@@ -41,8 +41,9 @@ namespace {
 constexpr int HD = 256;
 constexpr int BM = 128;
 constexpr int BN = 64;
-constexpr int kSoftWarp0 = 2, kDeqWarp0 = 6, kDeqThreads = 256;
-constexpr int kThreads = (kDeqWarp0 + kDeqThreads / 32) * 32;   // 448
+constexpr int kSoftWarp0 = 2, kDeqWarp0 = 6, kDeqThreads = 320;
+constexpr int kThreads = (kDeqWarp0 + kDeqThreads / 32) * 32;   // 512: 128 registers per thread fill the SM
+constexpr int kChunks = BN * HD / 16;                            // 16-code chunks of one plane of a tile
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kMaxSegments = 8;
@@ -134,12 +135,13 @@ __device__ __forceinline__ void flag_timeout() { atomicOr(&g_kvq8_device_error, 
 
 // Convert one 64-key plane tile (codes + scales in staging) into the swizzled fp16 tile:
 // element (key n, dim j) -> atom j/64, row n, 16-byte chunk ((j%64)/8) ^ (n%8).
-// 256 threads, 4 chunks of 16 codes each.
+// kDeqThreads threads share the tile's kChunks chunks of 16 codes.
 __device__ __forceinline__ void dequant_tile(const uint8_t* codes, const uint16_t* scales, uint8_t* hat, int nk,
                                              int d) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int c = d + kDeqThreads * k;  // 1024 chunks of 16 codes
+    for (int k = 0; k < (kChunks + kDeqThreads - 1) / kDeqThreads; ++k) {
+        const int c = d + kDeqThreads * k;
+        if (c >= kChunks) break;
         const int n = c >> 4, j16 = c & 15;
         uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
         if (n < nk) {

@@ -42,3 +42,30 @@ def test_combine_all_empty_rows_are_zero(lib):
     exp = torch.zeros((4, 64), device="cuda")
     exp[2] = po[1, 2] / 2.0
     assert torch.allclose(out, exp, rtol=1e-6, atol=0)
+
+
+@pytest.mark.parametrize("n_split", [1, 2, 3, 4, 5])
+def test_combine_many_rows_matches_oracle(lib, n_split):
+    """Prompt-sized merges (thousands of rows, a few partials) take the flat one-thread-per-
+    four-float4s kernel up to 4 partials and the row-per-block kernel beyond; both must agree
+    with the oracle's reducer, including partials with no keys (m = -inf, l = 0)."""
+    import torch
+
+    from speculative_verify_attention_gb300 import attn_combine
+    rows, hd = 5000, 256
+    rng = np.random.default_rng(700 + n_split)
+    po = rng.standard_normal((n_split, rows, hd)).astype(np.float32)
+    pm = rng.normal(0.0, 3.0, (n_split, rows)).astype(np.float32)
+    pl = rng.uniform(0.5, 50.0, (n_split, rows)).astype(np.float32)
+    empty = rng.random((n_split, rows)) < 0.1
+    empty[:, :3] = True                         # rows 0-2: no partial has keys
+    pm[empty] = -np.inf
+    pl[empty] = 0.0
+    po[empty] = 0.0
+    ref = oracle.combine(po.astype(np.float64), pm.astype(np.float64), pl.astype(np.float64))
+    ml = np.stack([pm, pl], axis=-1)
+    out = attn_combine(torch.from_numpy(po).cuda(), torch.from_numpy(ml).cuda())
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    assert np.all(got[:3] == 0.0)
+    assert rel_err(got, ref) <= VERIFY_TOL
