@@ -77,11 +77,14 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float4* 
     const float l = block_reduce(lsum, false, s_red);  // its barriers also publish the weights
     const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
 
+    // a partial with weight 0 (no keys: m = -inf) is skipped, never multiplied: its o slot
+    // may hold anything
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < kPrefetch; ++k) {
         const int s = sg + k * kSplitGroups;
         const float w = s < n_split ? s_wl[s].x : 0.0f;
+        if (w == 0.0f) continue;
         acc.x = fmaf(w, o[k].x, acc.x);
         acc.y = fmaf(w, o[k].y, acc.y);
         acc.z = fmaf(w, o[k].z, acc.z);
@@ -159,6 +162,7 @@ __global__ void __launch_bounds__(kWideThreads) combine_wide_kernel(const float4
     for (int s = 0; s < kWideMaxSplits; ++s) {
         if (s < n_split) {
             const float w = (ms == -INFINITY || ml[s].x == -INFINITY) ? 0.0f : expf(ml[s].x - ms);
+            if (w == 0.0f) continue;  // an empty partial's o slot may hold anything
             l = fmaf(w, ml[s].y, l);
 #pragma unroll
             for (int v = 0; v < kWideVec; ++v) {

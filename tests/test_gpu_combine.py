@@ -48,7 +48,8 @@ def test_combine_all_empty_rows_are_zero(lib):
 def test_combine_many_rows_matches_oracle(lib, n_split):
     """Prompt-sized merges (thousands of rows, a few partials) take the flat one-thread-per-
     four-float4s kernel up to 4 partials and the row-per-block kernel beyond; both must agree
-    with the oracle's reducer, including partials with no keys (m = -inf, l = 0)."""
+    with the oracle's reducer, including partials with no keys (m = -inf, l = 0) whose o slots
+    hold NaN."""
     import torch
 
     from speculative_verify_attention_gb300 import attn_combine
@@ -63,6 +64,7 @@ def test_combine_many_rows_matches_oracle(lib, n_split):
     pl[empty] = 0.0
     po[empty] = 0.0
     ref = oracle.combine(po.astype(np.float64), pm.astype(np.float64), pl.astype(np.float64))
+    po[empty] = np.nan                          # an empty partial's o slot is never read
     ml = np.stack([pm, pl], axis=-1)
     out = attn_combine(torch.from_numpy(po).cuda(), torch.from_numpy(ml).cuda())
     torch.cuda.synchronize()
