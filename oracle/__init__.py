@@ -68,6 +68,9 @@ def _load():
             lib.oracle_attention.argtypes = [ctypes.POINTER(_Cache), vp, i32, i32, i32, i32, f64,
                                              vp, vp, i64, vp]
             lib.oracle_attention.restype = i32
+            lib.oracle_attention_tree.argtypes = [ctypes.POINTER(_Cache), vp, i32, i32, i32, i32, vp, f64,
+                                                  vp, vp, i64, vp]
+            lib.oracle_attention_tree.restype = i32
             lib.oracle_combine.argtypes = [vp, vp, vp, i32, i64, i32, vp]
             lib.oracle_combine.restype = i32
             lib.oracle_set_threads.argtypes = [i32]
@@ -183,6 +186,32 @@ def attention(cache: Cache, q, kv_len: int, q_pos0: int, scale: float, sel=None)
                                   None if heads is None else _ptr(heads), n_sel, _ptr(out))
     if rc:
         raise ValueError("oracle_attention rejected its arguments")
+    return out.reshape(n_q, n_q_heads, hd) if sel is None else out
+
+
+def chain_mask(n_rows: int) -> np.ndarray:
+    """Window mask of the sequential window: row i sees window keys 0..i."""
+    return np.array([(1 << (i + 1)) - 1 for i in range(n_rows)], dtype=np.uint32)
+
+
+def attention_tree(cache: Cache, q, kv_len: int, q_pos0: int, scale: float, mask, sel=None) -> np.ndarray:
+    """fp64 attention of a tree-shaped window: row i sees every key n < q_pos0 and the window
+    key q_pos0 + j when bit j of mask[i] (uint32) is set.  Shapes as in attention()."""
+    qa = np.ascontiguousarray(q, dtype=np.float64)
+    n_q, n_q_heads, hd = qa.shape
+    if hd != cache.head_dim:
+        raise ValueError("head_dim mismatch")
+    mk = np.ascontiguousarray(mask, dtype=np.uint32)
+    if mk.shape != (n_q,):
+        raise ValueError("mask must hold one uint32 per row")
+    rows, heads, n_sel = _sel(sel, n_q, n_q_heads)
+    out = np.empty((n_sel, hd), dtype=np.float64)
+    st = cache._struct()
+    rc = _load().oracle_attention_tree(ctypes.byref(st), _ptr(qa), n_q, n_q_heads, int(kv_len), int(q_pos0),
+                                       _ptr(mk), float(scale), None if rows is None else _ptr(rows),
+                                       None if heads is None else _ptr(heads), n_sel, _ptr(out))
+    if rc:
+        raise ValueError("oracle_attention_tree rejected its arguments")
     return out.reshape(n_q, n_q_heads, hd) if sel is None else out
 
 

@@ -28,6 +28,12 @@
  *      s_n = scale * sum_j q_j * kcode[n][j] * dK[n][j/32]
  *      p_n = exp(s_n - max s) / sum exp(s - max s);  out_j = sum_n p_n vcode[n][j] dV[n][j/32]
  *
+ *  - Tree-shaped verify windows (the variant the multi-row route does not admit, "share Q8
+ *    KV scans across verifier rows", Summary: sequential windows only).  Reading: the T
+ *    window tokens sit at positions q_pos0 .. q_pos0 + T - 1 in the order given; row i sees
+ *    every key n < q_pos0 and the window key q_pos0 + j exactly when bit j of mask[i] is
+ *    set (j < 32, n < kv_len).  The sequential window is mask[i] = 2^(i+1) - 1.
+ *
  *  - Split-context partials and their merge ("share Q8 KV scans across verifier
  *    rows", Summary: "The partials layout and reducer are unchanged"): a partial over
  *    keys [k0, k1) is (o, m, l) with m = max s over the visible keys of the range,
@@ -267,6 +273,64 @@ int oracle_attention(const oracle_cache* c, const double* q, int n_q, int n_q_he
     free(m);
     free(l);
     return rc;
+}
+
+/* One (query row, q head): softmax attention over an explicit ascending list of keys. */
+static void attend_list(const oracle_cache* c, const double* qrow, int kv_head, const int64_t* keys, int64_t n_keys,
+                        double scale, double* out, double* s_buf) {
+    const int hd = c->head_dim;
+    for (int j = 0; j < hd; ++j) out[j] = 0.0;
+    if (n_keys <= 0) return;
+    double m = -INFINITY;
+    for (int64_t t = 0; t < n_keys; ++t) {
+        double s = 0.0;
+        for (int j = 0; j < hd; ++j) s += qrow[j] * deq(c->k_codes, c->k_scales, c, kv_head, keys[t], j);
+        s *= scale;
+        s_buf[t] = s;
+        if (s > m) m = s;
+    }
+    double l = 0.0;
+    for (int64_t t = 0; t < n_keys; ++t) {
+        double p = exp(s_buf[t] - m);
+        l += p;
+        for (int j = 0; j < hd; ++j) out[j] += p * deq(c->v_codes, c->v_scales, c, kv_head, keys[t], j);
+    }
+    for (int j = 0; j < hd; ++j) out[j] /= l;
+}
+
+/* Normalised attention of a tree-shaped window for selected (row, head) pairs: row i sees
+ * the keys n < min(q_pos0, kv_len) and q_pos0 + j (< kv_len) for every bit j of mask[i].
+ * A row with no visible key gives zeros.  Returns 0 or -1. */
+int oracle_attention_tree(const oracle_cache* c, const double* q, int n_q, int n_q_heads, int kv_len,
+                          int q_pos0, const uint32_t* mask, double scale, const int32_t* sel_row,
+                          const int32_t* sel_head, int64_t n_sel, double* out) {
+    if (check_cache(c, n_q_heads, kv_len) || n_q < 0 || n_q > 32 || q_pos0 < 0 || !mask) return -1;
+    if (!sel_row && n_sel != (int64_t)n_q * n_q_heads) return -1;
+    const int g = n_q_heads / c->n_kv_heads;
+    const int hd = c->head_dim;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double* s_buf = (double*)malloc(sizeof(double) * (size_t)(kv_len > 0 ? kv_len : 1));
+        int64_t* keys = (int64_t*)malloc(sizeof(int64_t) * (size_t)(kv_len > 0 ? kv_len : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < n_sel; ++t) {
+            int i = sel_row ? sel_row[t] : (int)(t / n_q_heads);
+            int h = sel_row ? sel_head[t] : (int)(t % n_q_heads);
+            if (i < 0 || i >= n_q || h < 0 || h >= n_q_heads || !s_buf || !keys) {
+                bad = 1;
+                continue;
+            }
+            int64_t n_keys = 0;
+            for (int64_t n = 0; n < q_pos0 && n < kv_len; ++n) keys[n_keys++] = n;
+            for (int j = 0; j < 32; ++j)
+                if (((mask[i] >> j) & 1u) && (int64_t)q_pos0 + j < kv_len) keys[n_keys++] = (int64_t)q_pos0 + j;
+            attend_list(c, q + ((int64_t)i * n_q_heads + h) * hd, h / g, keys, n_keys, scale, out + t * hd, s_buf);
+        }
+        free(s_buf);
+        free(keys);
+    }
+    return bad ? -1 : 0;
 }
 
 /* Merge n_split partials: part_o [n_split][rows][hd], part_m / part_l [n_split][rows]

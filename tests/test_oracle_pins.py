@@ -302,3 +302,91 @@ def test_empty_partial_and_combine_hand_case():
     pl = np.array([[1.0], [3.0], [0.0]])
     out = oracle.combine(po, pm, pl)
     assert np.allclose(out, [[(2.0 * 0.5 + 3.0) / (0.5 + 3.0), (4.0 * 0.5 - 1.0) / (0.5 + 3.0)]], rtol=0, atol=1e-15)
+
+
+# --------------------------------------------------------------------------- tree-shaped windows
+
+def _dense_tree_reference(cache, q, kv_len, q_pos0, scale, mask):
+    """Brute force with an explicit boolean mask: key n is visible to row i when n < q_pos0,
+    or when n = q_pos0 + j < kv_len and bit j of mask[i] is set; a row that sees nothing is 0."""
+    n_q, hq, hd = q.shape
+    g = hq // cache.n_kv_heads
+    kd = cache.k_codes.astype(np.float64) * np.repeat(cache.k_scales.view(np.float16).astype(np.float64), 32, axis=-1)
+    vd = cache.v_codes.astype(np.float64) * np.repeat(cache.v_scales.view(np.float16).astype(np.float64), 32, axis=-1)
+    vis = np.zeros((n_q, kv_len), dtype=bool)
+    for i in range(n_q):
+        vis[i, : min(q_pos0, kv_len)] = True
+        for j in range(32):
+            if (int(mask[i]) >> j) & 1 and q_pos0 + j < kv_len:
+                vis[i, q_pos0 + j] = True
+    out = np.zeros((n_q, hq, hd))
+    for h in range(hq):
+        kh, vh = kd[h // g, :kv_len], vd[h // g, :kv_len]
+        s = np.where(vis, scale * (q[:, h, :].astype(np.float64) @ kh.T), -np.inf)
+        live = vis.any(axis=1)
+        out[live, h, :] = scipy.special.softmax(s[live], axis=1) @ vh
+    return out
+
+
+def _tree_masks(parents):
+    """Ancestor-or-self masks of a tree given each node's parent (-1 for a root)."""
+    masks = []
+    for i in range(len(parents)):
+        m, a = 0, i
+        while a >= 0:
+            m |= 1 << a
+            a = parents[a]
+        masks.append(m)
+    return np.array(masks, dtype=np.uint32)
+
+
+def test_tree_chain_mask_equals_causal_attention():
+    inp = workloads.random_small(401, 4, 2, 64, 40, 6)
+    c = _cache_from(inp)
+    got = oracle.attention_tree(c, inp.q, 40, 34, 0.3, oracle.chain_mask(6))
+    assert np.max(np.abs(got - oracle.attention(c, inp.q, 40, 34, 0.3))) <= 1e-15
+
+
+@pytest.mark.parametrize("parents,pos0,L", [([-1, 0, 0, 1, 1, 2, 5], 20, 27),     # a draft tree
+                                            ([-1, -1, 0, 1, 2, 3], 9, 15),        # two branches
+                                            ([-1, 0, 1, 2], 0, 4)])               # no context
+def test_tree_matches_dense_bruteforce(parents, pos0, L):
+    T = len(parents)
+    inp = workloads.random_small(500 + T + pos0, 6, 2, 32, L, T, k_gain=2.0)
+    c = _cache_from(inp)
+    mask = _tree_masks(parents)
+    got = oracle.attention_tree(c, inp.q, L, pos0, 0.41, mask)
+    ref = _dense_tree_reference(c, inp.q, L, pos0, 0.41, mask)
+    assert np.max(np.abs(got - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+
+
+def test_tree_arbitrary_masks_and_bits_past_kv_len():
+    inp = workloads.random_small(601, 3, 1, 64, 30, 8)
+    c = _cache_from(inp)
+    rng = np.random.default_rng(5)
+    mask = rng.integers(0, 1 << 32, 8, dtype=np.uint64).astype(np.uint32)
+    mask[0] = 0                                     # sees the context only
+    got = oracle.attention_tree(c, inp.q, 30, 24, 0.2, mask)
+    ref = _dense_tree_reference(c, inp.q, 30, 24, 0.2, mask)
+    assert np.max(np.abs(got - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+    clipped = mask & np.uint32((1 << 6) - 1)        # keys 24..29 exist, bits 6.. point past kv_len
+    assert np.array_equal(oracle.attention_tree(c, inp.q, 30, 24, 0.2, clipped), got)
+    zero = oracle.attention_tree(c, inp.q[:1], 30, 0, 0.2, np.zeros(1, np.uint32))
+    assert not zero.any()                           # nothing visible: zeros
+
+
+def test_tree_permuting_window_tokens_with_their_bits():
+    """Reordering the window tokens in the cache, and the mask bits with them, changes nothing."""
+    parents = [-1, 0, 0, 1, 2]
+    T, pos0, L = 5, 11, 16
+    inp = workloads.random_small(701, 4, 1, 64, L, T)
+    c = _cache_from(inp)
+    mask = _tree_masks(parents)
+    base = oracle.attention_tree(c, inp.q, L, pos0, 0.3, mask)
+    perm = np.array([3, 0, 4, 1, 2])                # slot s of the new window holds old token perm[s]
+    c2 = oracle.Cache.from_planes(c.k_codes.copy(), c.k_scales.copy(), c.v_codes.copy(), c.v_scales.copy())
+    for plane in (c2.k_codes, c2.k_scales, c2.v_codes, c2.v_scales):
+        plane[0, pos0:pos0 + T] = plane[0, pos0 + perm]
+    inv = np.argsort(perm)
+    mask2 = np.array([sum(1 << int(inv[j]) for j in range(T) if (int(m) >> j) & 1) for m in mask], np.uint32)
+    assert np.max(np.abs(oracle.attention_tree(c2, inp.q, L, pos0, 0.3, mask2) - base)) < 1e-13
