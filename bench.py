@@ -5,7 +5,7 @@
 
 One JSON line on rank 0.  A step is one speculative-verify step on the 27B-class
 workload (24 q heads / 4 kv heads, head_dim 256, context 4096): for each window length
-T in {4, 8}, append the T new K/V tokens to the Q8_0 cache (kvq8_quantize, K and V) and
+T in {4, 8}, append the T new K/V tokens to the Q8_0 cache (kvq8_append, one launch) and
 run attn_verify_q8 (split-context kernel + log-sum-exp combine) over ctx + T keys.
 `value` is the KV-scan bandwidth of the whole job (Q8_0 K/V bytes read by the verify
 calls / time), in GB/s; `us_per_call` gives the per-call latency.  The prompt-chunk
@@ -194,7 +194,7 @@ def run_native(args, world, rank, local):
     import __graft_entry__
     __graft_entry__.build()
     from speculative_verify_attention_gb300 import (KVCacheQ8, KVQ8Error, attn_prompt_q8, attn_verify_q8,
-                                                    attn_verify_q8_workspace_bytes, kvq8_quantize, workloads)
+                                                    attn_verify_q8_workspace_bytes, kvq8_append, workloads)
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -229,12 +229,11 @@ def run_native(args, world, rank, local):
         c = ring[s % n_ring]
         for T in VERIFY_T:
             if do_append:
-                kvq8_quantize(knew[T], c.k_codes, c.k_scales, ctx)
-                kvq8_quantize(vnew[T], c.v_codes, c.v_scales, ctx)
+                kvq8_append(knew[T], vnew[T], c, ctx)
             if do_verify:
                 attn_verify_q8(q[T], c, ctx + T, ctx, w0.softmax_scale, out=out[T], workspace=wsb[T])
 
-    launches_per_step = len(VERIFY_T) * 4   # 2 quantise + verify split + combine per T
+    launches_per_step = len(VERIFY_T) * 3   # K+V append + verify split + combine per T
 
     def capture(**kw):
         s = torch.cuda.Stream(device=dev)
@@ -373,7 +372,7 @@ def run_native(args, world, rank, local):
                        "global_batch": world, "seq_len": ctx, "verify_rows": list(VERIFY_T),
                        "parallelism": f"replicas x{world}", "l2": f"ring of {n_ring} caches, "
                        f"{n_ring * cache_bytes / 2**20:.0f} MiB > 4x L2 (every step reads a different cache)",
-                       "step": "per T in {4,8}: kvq8_quantize K and V of T new tokens + attn_verify_q8 over ctx+T",
+                       "step": "per T in {4,8}: kvq8_append (K and V) of T new tokens + attn_verify_q8 over ctx+T",
                        "graph": f"{GRAPH_STEPS} steps per CUDA graph replay"},
             "us_per_call": us_per_call_verify, "verify_only_gbs": verify_gbs,
             "hbm_frac": verify_gbs / hbm_peak, "per_T": per_t,
@@ -449,24 +448,47 @@ def _ring_for(w, dev, ring_l2):
     return ring
 
 
-def time_verify_cell(w, ring, dev, reps=10):
-    """Median-free device time per attn_verify_q8 call: a CUDA graph of calls walking the ring
-    (total size > 4x L2) replayed `reps` times; returns microseconds per call."""
+def binary_tree_mask(T: int) -> np.ndarray:
+    """Window mask of a binary draft tree of T tokens (node i's parent is (i - 1) // 2): each row
+    sees its ancestors and itself."""
+    masks = []
+    for i in range(T):
+        m, a = 0, i
+        while a >= 0:
+            m |= 1 << a
+            a = (a - 1) // 2 if a > 0 else -1
+        masks.append(m)
+    return np.array(masks, dtype=np.uint32)
+
+
+def time_verify_cell(w, ring, dev, reps=10, tree_mask=None):
+    """Median-free device time per attn_verify_q8 call (attn_verify_tree_q8 when a window mask
+    is given): a CUDA graph of calls walking the ring (total size > 4x L2) replayed `reps`
+    times; returns microseconds per call."""
     import torch
 
-    from speculative_verify_attention_gb300 import attn_verify_q8, attn_verify_q8_workspace_bytes, workloads
+    from speculative_verify_attention_gb300 import (attn_verify_q8, attn_verify_q8_workspace_bytes,
+                                                    attn_verify_tree_q8, workloads)
     q = torch.from_numpy(workloads.make_inputs(w, kv_len=1).q).to(dev)
     out = torch.empty_like(q)
     ws = torch.empty(attn_verify_q8_workspace_bytes(w.n_q, w.n_q_heads, w.head_dim, w.kv_len, w.n_kv_heads),
                      dtype=torch.uint8, device=dev)
+    if tree_mask is not None:
+        m = torch.from_numpy(np.ascontiguousarray(tree_mask, np.uint32).view(np.int32)).to(dev)
+
+        def call(c):
+            attn_verify_tree_q8(q, c, w.kv_len, w.q_pos0, m, w.softmax_scale, out=out, workspace=ws)
+    else:
+        def call(c):
+            attn_verify_q8(q, c, w.kv_len, w.q_pos0, w.softmax_scale, out=out, workspace=ws)
     for i in range(3):
-        attn_verify_q8(q, ring[i % len(ring)], w.kv_len, w.q_pos0, w.softmax_scale, out=out, workspace=ws)
+        call(ring[i % len(ring)])
     torch.cuda.synchronize()
     n_calls = max(len(ring), 32)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         for i in range(n_calls):
-            attn_verify_q8(q, ring[i % len(ring)], w.kv_len, w.q_pos0, w.softmax_scale, out=out, workspace=ws)
+            call(ring[i % len(ring)])
     g.replay()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -491,19 +513,23 @@ def sweep(args):
     cells = [workloads.verify_27b(t) for t in workloads.VERIFY_27B_T]
     cells += [workloads.long_verify(c, t) for c in workloads.LONG_CTX for t in workloads.LONG_T]
     cells += [workloads.hd128_verify(t) for t in workloads.HD128_T]
-    cells = [w for w in cells if not args.sweep_filter or args.sweep_filter in w.name]
+    # tree-shaped windows (binary draft trees) on the 27B-class shape
+    cells += [(workloads.verify_27b(t), "tree-binary") for t in (8, 16)]
+    cells = [c if isinstance(c, tuple) else (c, None) for c in cells]
+    cells = [(w, kind) for w, kind in cells
+             if not args.sweep_filter or args.sweep_filter in (f"{kind}-{w.name}" if kind else w.name)]
     key, ring = None, None
-    for w in cells:
+    for w, kind in cells:
         if key != (w.n_kv_heads, w.head_dim, w.kv_len):
             ring = None
             torch.cuda.empty_cache()
             ring = _ring_for(w, dev, args.ring_l2)
             key = (w.n_kv_heads, w.head_dim, w.kv_len)
-        us = time_verify_cell(w, ring, dev)
+        us = time_verify_cell(w, ring, dev, tree_mask=binary_tree_mask(w.n_q) if kind else None)
         gbs = w.kv_bytes() / (us * 1e-6) / 1e9
-        print(json.dumps({"workload": w.name, "us_per_call": us, "kv_mb": w.kv_bytes() / 1e6, "kv_gbs": gbs,
-                          "hbm_frac": gbs / hbm_peak, "tflops_alg": w.causal_flops() / (us * 1e-6) / 1e12,
-                          "ring": len(ring)}), flush=True)
+        print(json.dumps({"workload": f"{kind}-{w.name}" if kind else w.name, "us_per_call": us,
+                          "kv_mb": w.kv_bytes() / 1e6, "kv_gbs": gbs, "hbm_frac": gbs / hbm_peak,
+                          "tflops_alg": w.causal_flops() / (us * 1e-6) / 1e12, "ring": len(ring)}), flush=True)
 
 
 def main():

@@ -79,6 +79,20 @@ typedef struct {
 int kvq8_quantize(const float* x, int n_tok, int n_kv_heads, int head_dim,
                   int8_t* codes, uint16_t* scales, int capacity, int pos0, kvq8_stream_t stream);
 
+/*
+ * kvq8_append -- append n_tok tokens of K and V to both planes of a cache in one launch.
+ *   k, v : fp32 [n_tok][kv->n_kv_heads][kv->head_dim], device memory; tokens land at
+ *          positions [pos0, pos0 + n_tok) of every KV head.
+ * Each plane is quantised exactly as kvq8_quantize would (bit-exact with it); the cache's
+ * plane pointers are written through although the struct declares them const.
+ * Errors: INVALID_ARG for null pointers, negative n_tok or pos0, or pos0 + n_tok > capacity;
+ * UNSUPPORTED when head_dim is not a multiple of 32; MISALIGNED unless every pointer is
+ * 16-byte aligned.
+ * Source: "Engine perf(hip): ...", Summary item 4 (warp-per-block Q8_0 quantiser).
+ */
+int kvq8_append(const float* k, const float* v, int n_tok, const kvq8_cache* kv, int pos0,
+                kvq8_stream_t stream);
+
 /* Bytes of workspace attn_verify_q8 needs for this shape (n_split 0 = the automatic choice). */
 size_t attn_verify_q8_workspace_bytes(int n_rows, int n_q_heads, int head_dim, int kv_len,
                                       int n_kv_heads, int n_split);
@@ -101,6 +115,24 @@ size_t attn_verify_q8_workspace_bytes(int n_rows, int n_q_heads, int head_dim, i
 int attn_verify_q8(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv, int kv_len,
                    int q_pos0, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
                    int n_split, kvq8_stream_t stream);
+
+/*
+ * attn_verify_tree_q8 -- attn_verify_q8 for a tree-shaped verify window.
+ *   window_mask : device uint32 [n_rows], 4-byte aligned: row i sees every key n < q_pos0
+ *                 and the window key q_pos0 + j (j < 32, q_pos0 + j < kv_len) exactly when
+ *                 bit j of window_mask[i] is set.  The sequential window of attn_verify_q8
+ *                 is window_mask[i] = 2^(i+1) - 1; a tree of drafted tokens sets the bits
+ *                 of a row's ancestors and of itself.  A row that sees no key gets zeros.
+ * Everything else (shapes, workspace from attn_verify_q8_workspace_bytes, n_split,
+ * precision, errors) is as for attn_verify_q8; a null window_mask is INVALID_ARG and a
+ * misaligned one MISALIGNED.
+ * The pages admit only sequential windows on the multi-row route and send trees to the
+ * fallback ("perf(gfx1100): share Q8 KV scans across verifier rows", Summary: route
+ * conditions); here a tree costs the same K/V scan as a chain.
+ */
+int attn_verify_tree_q8(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv, int kv_len,
+                        int q_pos0, const uint32_t* window_mask, float softmax_scale, float* out,
+                        void* workspace, size_t workspace_bytes, int n_split, kvq8_stream_t stream);
 
 /*
  * attn_combine -- merge split-context partials (log-sum-exp reducer).

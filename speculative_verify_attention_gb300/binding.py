@@ -27,7 +27,7 @@ KVQ8_ERR_WORKSPACE = 4
 KVQ8_ERR_CUDA = 5
 
 # Entry points declared in include/kvq8attn.h.
-EXPORTED = ("kvq8_quantize", "attn_verify_q8_workspace_bytes", "attn_verify_q8", "attn_combine",
+EXPORTED = ("kvq8_quantize", "kvq8_append", "attn_verify_q8_workspace_bytes", "attn_verify_q8", "attn_verify_tree_q8", "attn_combine",
             "attn_prompt_q8_workspace_bytes", "attn_prompt_q8", "attn_verify_q8_noalloc", "kvq8_device_error", "kvq8_status_str")
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
@@ -62,10 +62,14 @@ def load_library():
         cp = ctypes.POINTER(kvq8_cache)
         lib.kvq8_quantize.argtypes = [vp, i32, i32, i32, vp, vp, i32, i32, vp]
         lib.kvq8_quantize.restype = i32
+        lib.kvq8_append.argtypes = [vp, vp, i32, cp, i32, vp]
+        lib.kvq8_append.restype = i32
         lib.attn_verify_q8_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.attn_verify_q8_workspace_bytes.restype = sz
         lib.attn_verify_q8.argtypes = [vp, i32, i32, cp, i32, i32, f32, vp, vp, sz, i32, vp]
         lib.attn_verify_q8.restype = i32
+        lib.attn_verify_tree_q8.argtypes = [vp, i32, i32, cp, i32, i32, vp, f32, vp, vp, sz, i32, vp]
+        lib.attn_verify_tree_q8.restype = i32
         lib.attn_combine.argtypes = [vp, vp, i32, i32, i32, vp, vp]
         lib.attn_combine.restype = i32
         lib.attn_prompt_q8_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
@@ -136,9 +140,9 @@ class KVCacheQ8:
                           self.v_scales.data_ptr(), self.n_kv_heads, self.head_dim, self.capacity)
 
     def append(self, k: torch.Tensor, v: torch.Tensor, pos0: int, stream=None) -> None:
-        """Quantise K and V values [n_tok][n_kv_heads][head_dim] (fp32) into positions pos0.."""
-        kvq8_quantize(k, self.k_codes, self.k_scales, pos0, stream)
-        kvq8_quantize(v, self.v_codes, self.v_scales, pos0, stream)
+        """Quantise K and V values [n_tok][n_kv_heads][head_dim] (fp32) into positions pos0..
+        (one kvq8_append launch for both planes)."""
+        kvq8_append(k, v, self, pos0, stream)
 
 
 def kvq8_quantize(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, pos0: int, stream=None) -> None:
@@ -150,6 +154,18 @@ def kvq8_quantize(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, po
     st = load_library().kvq8_quantize(_ptr(x), n_tok, n_kv_heads, head_dim, _ptr(codes), _ptr(scales),
                                       capacity, int(pos0), _stream(stream))
     _check("kvq8_quantize", st)
+
+
+def kvq8_append(k: torch.Tensor, v: torch.Tensor, cache: "KVCacheQ8", pos0: int, stream=None) -> None:
+    """Quantise K and V values [n_tok][n_kv_heads][head_dim] (fp32) into both planes of
+    `cache` at positions pos0.. in one launch."""
+    _need(k, "k", torch.float32)
+    _need(v, "v", torch.float32)
+    if k.shape != v.shape or k.dim() != 3 or k.shape[1:] != (cache.n_kv_heads, cache.head_dim):
+        raise ValueError(f"k and v must both be [n_tok][{cache.n_kv_heads}][{cache.head_dim}]")
+    st = load_library().kvq8_append(_ptr(k), _ptr(v), k.shape[0], ctypes.byref(cache.struct()), int(pos0),
+                                    _stream(stream))
+    _check("kvq8_append", st)
 
 
 def attn_verify_q8_workspace_bytes(n_rows: int, n_q_heads: int, head_dim: int, kv_len: int, n_kv_heads: int,
@@ -174,6 +190,31 @@ def attn_verify_q8(q: torch.Tensor, cache: KVCacheQ8, kv_len: int, q_pos0: int, 
                                        int(q_pos0), float(softmax_scale), _ptr(out), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), int(n_split), _stream(stream))
     _check("attn_verify_q8", st)
+    return out
+
+
+def attn_verify_tree_q8(q: torch.Tensor, cache: KVCacheQ8, kv_len: int, q_pos0: int, window_mask: torch.Tensor,
+                        softmax_scale: float, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                        n_split: int = 0, stream=None) -> torch.Tensor:
+    """Verify attention of a tree-shaped window: fp32 q [T][Hq][hd]; window_mask int32 [T] on
+    the device, bit j of row i's word = row i sees key q_pos0 + j (keys before q_pos0 are
+    always visible).  Returns fp32 [T][Hq][hd]."""
+    _need(q, "q", torch.float32)
+    _need(window_mask, "window_mask", torch.int32)
+    n_rows, n_q_heads, head_dim = q.shape
+    if window_mask.shape != (n_rows,):
+        raise ValueError(f"window_mask must hold one word per row ({n_rows})")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.float32)
+    if workspace is None:
+        nbytes = attn_verify_q8_workspace_bytes(n_rows, n_q_heads, head_dim, kv_len, cache.n_kv_heads, n_split)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    st = load_library().attn_verify_tree_q8(_ptr(q), n_rows, n_q_heads, ctypes.byref(cache.struct()), int(kv_len),
+                                            int(q_pos0), _ptr(window_mask), float(softmax_scale), _ptr(out),
+                                            _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                            int(n_split), _stream(stream))
+    _check("attn_verify_tree_q8", st)
     return out
 
 

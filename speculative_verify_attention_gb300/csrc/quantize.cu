@@ -7,20 +7,31 @@
 // Here a warp covers four blocks: eight lanes per block, four values per lane (one
 // 16-byte load), a 3-step shuffle max, then per value an IEEE fp32 division and round
 // half away from zero.  Bandwidth-bound: 4 bytes read, 1 + 1/16 bytes written per value.
+// kvq8_append writes both planes (K and V) of a cache in one launch.
 #include "common.cuh"
 
 namespace kvq8 {
 namespace {
 
-__global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4* __restrict__ x, int64_t n_blocks,
+// Plane 0 (x0 -> codes0/scales0) holds blocks [0, n_blocks); when x1 is given, plane 1
+// (x1 -> codes1/scales1) holds blocks [n_blocks, 2 n_blocks) of the same launch.
+__global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4* __restrict__ x0,
+                                                            const float4* __restrict__ x1, int64_t n_blocks,
                                                             int n_kv_heads, int nb_per_head_row,
-                                                            int8_t* __restrict__ codes,
-                                                            uint16_t* __restrict__ scales, int capacity,
+                                                            int8_t* __restrict__ codes0,
+                                                            uint16_t* __restrict__ scales0,
+                                                            int8_t* __restrict__ codes1,
+                                                            uint16_t* __restrict__ scales1, int capacity,
                                                             int pos0) {
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t blk = gid >> 3;  // Q8_0 block handled by this lane's group of 8
+    const int64_t blk_all = gid >> 3;  // Q8_0 block handled by this lane's group of 8
+    const bool second = blk_all >= n_blocks;
+    const int64_t blk = second ? blk_all - n_blocks : blk_all;
+    const float4* x = second ? x1 : x0;
+    int8_t* codes = second ? codes1 : codes0;
+    uint16_t* scales = second ? scales1 : scales0;
     const int sub = threadIdx.x & 7;
-    const bool live = blk < n_blocks;
+    const bool live = blk_all < (x1 ? 2 * n_blocks : n_blocks);
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (live) v = __ldg(x + blk * 8 + sub);
     float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
@@ -54,6 +65,27 @@ __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4* __rest
 }  // namespace
 }  // namespace kvq8
 
+namespace kvq8 {
+namespace {
+
+int launch_quantize(const float* x0, const float* x1, int n_tok, int n_kv_heads, int head_dim, int8_t* codes0,
+                    uint16_t* scales0, int8_t* codes1, uint16_t* scales1, int capacity, int pos0,
+                    cudaStream_t stream) {
+    const int nb = head_dim / kQBlock;
+    const int64_t n_blocks = (int64_t)n_tok * n_kv_heads * nb;
+    const int64_t threads = n_blocks * 8 * (x1 ? 2 : 1);
+    const int64_t grid = (threads + 255) / 256;
+    if (grid > 0x7fffffffLL) return KVQ8_ERR_UNSUPPORTED;
+    quantize_q8_0_kernel<<<(unsigned)grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(x0),
+                                                           reinterpret_cast<const float4*>(x1), n_blocks,
+                                                           n_kv_heads, nb, codes0, scales0, codes1, scales1,
+                                                           capacity, pos0);
+    return launch_status();
+}
+
+}  // namespace
+}  // namespace kvq8
+
 extern "C" int kvq8_quantize(const float* x, int n_tok, int n_kv_heads, int head_dim, int8_t* codes,
                              uint16_t* scales, int capacity, int pos0, kvq8_stream_t stream) {
     using namespace kvq8;
@@ -63,14 +95,25 @@ extern "C" int kvq8_quantize(const float* x, int n_tok, int n_kv_heads, int head
     if (n_tok == 0) return KVQ8_OK;
     if (!x || !codes || !scales) return KVQ8_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(codes) || !aligned16(scales)) return KVQ8_ERR_MISALIGNED;
-    const int nb = head_dim / kQBlock;
-    const int64_t n_blocks = (int64_t)n_tok * n_kv_heads * nb;
-    const int64_t threads = n_blocks * 8;
-    const int64_t grid = (threads + 255) / 256;
-    if (grid > 0x7fffffffLL) return KVQ8_ERR_UNSUPPORTED;
-    quantize_q8_0_kernel<<<(unsigned)grid, 256, 0, (cudaStream_t)stream>>>(
-        reinterpret_cast<const float4*>(x), n_blocks, n_kv_heads, nb, codes, scales, capacity, pos0);
-    return launch_status();
+    return launch_quantize(x, nullptr, n_tok, n_kv_heads, head_dim, codes, scales, nullptr, nullptr, capacity, pos0,
+                           (cudaStream_t)stream);
+}
+
+extern "C" int kvq8_append(const float* k, const float* v, int n_tok, const kvq8_cache* kv, int pos0,
+                           kvq8_stream_t stream) {
+    using namespace kvq8;
+    if (!kv || n_tok < 0 || pos0 < 0) return KVQ8_ERR_INVALID_ARG;
+    if (kv->n_kv_heads <= 0 || kv->head_dim <= 0 || kv->capacity <= 0) return KVQ8_ERR_INVALID_ARG;
+    if (kv->head_dim % kQBlock) return KVQ8_ERR_UNSUPPORTED;
+    if ((int64_t)pos0 + n_tok > kv->capacity) return KVQ8_ERR_INVALID_ARG;
+    if (n_tok == 0) return KVQ8_OK;
+    if (!k || !v || !kv->k_codes || !kv->k_scales || !kv->v_codes || !kv->v_scales) return KVQ8_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(kv->k_codes) || !aligned16(kv->k_scales) ||
+        !aligned16(kv->v_codes) || !aligned16(kv->v_scales))
+        return KVQ8_ERR_MISALIGNED;
+    return launch_quantize(k, v, n_tok, kv->n_kv_heads, kv->head_dim, const_cast<int8_t*>(kv->k_codes),
+                           const_cast<uint16_t*>(kv->k_scales), const_cast<int8_t*>(kv->v_codes),
+                           const_cast<uint16_t*>(kv->v_scales), kv->capacity, pos0, (cudaStream_t)stream);
 }
 
 extern "C" const char* kvq8_status_str(int status) {

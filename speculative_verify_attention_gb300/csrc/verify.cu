@@ -60,6 +60,7 @@ struct VerifyParams {
     int keys_per_split;
     int rows_per_chunk;  // real rows per chunk (<= 8 * NT)
     float qscale;        // softmax_scale * log2(e)
+    const uint32_t* wmask;  // tree windows: bit j of wmask[i] = row i sees key q_pos0 + j; null = causal
 };
 
 template <int HD, int NT>
@@ -75,7 +76,8 @@ struct Smem {
     static constexpr int kP = kQ + NB * NT * 1024;
     static constexpr int kDv = kP + (kKT / 2) * PS * 8;   // per warp: its block's V scales * 2^E as fp16
     static constexpr int kRed = kDv + kWarps * kKT * 2;   // [RP][kWarps] floats
-    static constexpr int kBytes = kRed + RP * kWarps * 4;
+    static constexpr int kWm = kRed + RP * kWarps * 4;    // [RP] window masks (tree windows)
+    static constexpr int kBytes = kWm + RP * 4;
 };
 
 // Byte offset of code byte c of tile row n in the swizzled layout (16-byte chunks XOR row%8).
@@ -129,7 +131,9 @@ __device__ __forceinline__ void load_scales(uint8_t* smem, const uint16_t* plane
 //         2b and 2b+1 share block b, one m16 fragment each.
 // Row statistics live in the lanes that own the rows: lane (g, t) holds rows 8nt + 2t + c in
 // both the S^T and the O^T fragments, so the softmax factors never leave the thread.
-template <int HD, int NT>
+// TREE: the window's rows see the window keys their mask selects (p.wmask); otherwise the
+// window is sequential (row i sees keys < q_pos0 + i + 1) and the mask code is compiled out.
+template <int HD, int NT, bool TREE>
 __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kernel(const VerifyParams p) {
     using L = Smem<HD, NT>;
     constexpr int NB = L::NB, RP = L::RP, PS = L::PS;
@@ -143,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
     // P tile: entry (key pair k, row r) = (hi, lo) fp16 pairs of (p[2k][r], p[2k+1][r]) * 2^kPShift
     uint2* sP = reinterpret_cast<uint2*>(smem + L::kP);
     float* sRed = reinterpret_cast<float*>(smem + L::kRed);
+    uint32_t* sWm = reinterpret_cast<uint32_t*>(smem + L::kWm);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int chunk = blockIdx.x, split = blockIdx.y, kvh = blockIdx.z;
@@ -210,8 +215,9 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
         }
     }
 
-    // Visibility bound per owned row (row rr sees keys < vis_end) and its output row
-    // (-1 for padding rows).
+    // Visibility bound per owned row (row rr sees keys < vis_end; for a tree window, keys at
+    // or past q_pos0 also need their mask bit) and its output row (-1 for padding rows).
+    constexpr bool tree = TREE;
     int vis_end[NT][2], grow[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -221,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
             if (r < rows_here) {
                 const int rr = row0 + r;
                 const int i = rr / p.group, hh = rr - i * p.group;
-                vis_end[nt][c] = min(min(p.q_pos0 + i + 1, p.kv_len), key_end);
+                vis_end[nt][c] = min(min(tree ? p.q_pos0 + 32 : p.q_pos0 + i + 1, p.kv_len), key_end);
                 grow[nt][c] = i * p.n_q_heads + kvh * p.group + hh;
             } else {
                 vis_end[nt][c] = 0;
@@ -229,9 +235,14 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
             }
         }
 
+    if (TREE && threadIdx.x < RP) {  // the window mask of each row of the chunk (read in masked tiles)
+        const int r = threadIdx.x;
+        sWm[r] = r < rows_here ? __ldg(p.wmask + (row0 + r) / p.group) : 0u;
+    }  // published by the barrier at the top of the first tile
+
     // every real row of this chunk sees all keys below vis_min; padding rows hold q = 0 and
     // never reach the output, so tiles wholly below vis_min skip the mask
-    const int vis_min = min(min(p.q_pos0 + row0 / p.group + 1, p.kv_len), key_end);
+    const int vis_min = min(min(tree ? p.q_pos0 : p.q_pos0 + row0 / p.group + 1, p.kv_len), key_end);
     float m_ref[NT][2], l_w[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -314,7 +325,12 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
                 for (int h = 0; h < 2; ++h) {
                     const int key = tile0 + n0 + 8 * h;
                     float& s = S[nt][2 * h + c];
-                    if (tile_needs_mask && key >= vis_end[nt][c]) s = -INFINITY;
+                    if (tile_needs_mask) {
+                        bool vis = key < vis_end[nt][c];
+                        if (tree && vis && key >= p.q_pos0)
+                            vis = (sWm[8 * nt + 2 * t + c] >> (key - p.q_pos0)) & 1u;
+                        if (!vis) s = -INFINITY;
+                    }
                     need |= s > m_ref[nt][c] + kLazy;
                 }
         // barrier: every warp is done with sK, and the vote is known to all
@@ -578,28 +594,28 @@ int make_plan(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_kv_head
     return KVQ8_OK;
 }
 
-template <int HD, int NT>
+template <int HD, int NT, bool TREE>
 int launch_verify(const VerifyParams& vp, const Plan& pl, int n_kv_heads, cudaStream_t stream) {
     constexpr int bytes = Smem<HD, NT>::kBytes;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(verify_split_kernel<HD, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(verify_split_kernel<HD, NT, TREE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 bytes) != cudaSuccess)
             return KVQ8_ERR_CUDA;
         attr_set = true;
     }
     dim3 grid(pl.n_chunks, pl.n_split, n_kv_heads);
-    verify_split_kernel<HD, NT><<<grid, kThreads, bytes, stream>>>(vp);
+    verify_split_kernel<HD, NT, TREE><<<grid, kThreads, bytes, stream>>>(vp);
     return launch_status();
 }
 
-template <int HD>
+template <int HD, bool TREE>
 int dispatch_nt(const VerifyParams& vp, const Plan& pl, int n_kv_heads, cudaStream_t s) {
     switch (pl.nt) {
-        case 1: return launch_verify<HD, 1>(vp, pl, n_kv_heads, s);
-        case 2: return launch_verify<HD, 2>(vp, pl, n_kv_heads, s);
-        case 3: return launch_verify<HD, 3>(vp, pl, n_kv_heads, s);
-        case 4: return launch_verify<HD, 4>(vp, pl, n_kv_heads, s);
+        case 1: return launch_verify<HD, 1, TREE>(vp, pl, n_kv_heads, s);
+        case 2: return launch_verify<HD, 2, TREE>(vp, pl, n_kv_heads, s);
+        case 3: return launch_verify<HD, 3, TREE>(vp, pl, n_kv_heads, s);
+        case 4: return launch_verify<HD, 4, TREE>(vp, pl, n_kv_heads, s);
         default: return KVQ8_ERR_UNSUPPORTED;
     }
 }
@@ -614,10 +630,12 @@ extern "C" size_t attn_verify_q8_workspace_bytes(int n_rows, int n_q_heads, int 
     return pl.ws_bytes;
 }
 
-extern "C" int attn_verify_q8(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv, int kv_len,
-                              int q_pos0, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
-                              int n_split, kvq8_stream_t stream) {
-    using namespace kvq8;
+namespace kvq8 {
+namespace {
+
+int verify_impl(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv, int kv_len, int q_pos0,
+                const uint32_t* wmask, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                int n_split, kvq8_stream_t stream) {
     if (!kv || !q || !out) return KVQ8_ERR_INVALID_ARG;
     if (!kv->k_codes || !kv->k_scales || !kv->v_codes || !kv->v_scales) return KVQ8_ERR_INVALID_ARG;
     if (kv->n_kv_heads < 1 || kv->capacity < 1 || q_pos0 < 0) return KVQ8_ERR_INVALID_ARG;
@@ -652,11 +670,37 @@ extern "C" int attn_verify_q8(const float* q, int n_rows, int n_q_heads, const k
     vp.keys_per_split = pl.keys_per_split;
     vp.rows_per_chunk = pl.rows_per_chunk;
     vp.qscale = softmax_scale * kLog2e;
+    vp.wmask = wmask;
     cudaStream_t s = (cudaStream_t)stream;
-    const int r1 = pl.hd == 128 ? dispatch_nt<128>(vp, pl, kv->n_kv_heads, s) : dispatch_nt<256>(vp, pl, kv->n_kv_heads, s);
+    int r1;
+    if (wmask)
+        r1 = pl.hd == 128 ? dispatch_nt<128, true>(vp, pl, kv->n_kv_heads, s)
+                          : dispatch_nt<256, true>(vp, pl, kv->n_kv_heads, s);
+    else
+        r1 = pl.hd == 128 ? dispatch_nt<128, false>(vp, pl, kv->n_kv_heads, s)
+                          : dispatch_nt<256, false>(vp, pl, kv->n_kv_heads, s);
     if (r1 != KVQ8_OK) return r1;
     return launch_combine(vp.part_o, reinterpret_cast<const float*>(vp.part_ml), pl.n_split, (int)rows_total,
                           kv->head_dim, out, s);
+}
+
+}  // namespace
+}  // namespace kvq8
+
+extern "C" int attn_verify_q8(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv, int kv_len,
+                              int q_pos0, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                              int n_split, kvq8_stream_t stream) {
+    return kvq8::verify_impl(q, n_rows, n_q_heads, kv, kv_len, q_pos0, nullptr, softmax_scale, out, workspace,
+                             workspace_bytes, n_split, stream);
+}
+
+extern "C" int attn_verify_tree_q8(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv, int kv_len,
+                                   int q_pos0, const uint32_t* window_mask, float softmax_scale, float* out,
+                                   void* workspace, size_t workspace_bytes, int n_split, kvq8_stream_t stream) {
+    if (!window_mask) return KVQ8_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(window_mask) & 3u) != 0) return KVQ8_ERR_MISALIGNED;
+    return kvq8::verify_impl(q, n_rows, n_q_heads, kv, kv_len, q_pos0, window_mask, softmax_scale, out, workspace,
+                             workspace_bytes, n_split, stream);
 }
 
 // ---------------------------------------------------------------------------------------

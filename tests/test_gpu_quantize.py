@@ -106,3 +106,39 @@ def test_quantize_rejects_bad_arguments(lib):
     with pytest.raises(KVQ8Error) as e:   # misaligned input pointer
         kvq8_quantize(buf[1:].view(4, 1, 64), codes, scales, 0)
     assert e.value.status == 3
+
+
+def test_append_both_planes_bit_exact_against_two_quantize_calls(lib):
+    """kvq8_append (one launch, K and V) writes the same bits as the oracle's quantiser and as
+    two kvq8_quantize calls, at an offset, and leaves the other positions untouched."""
+    import torch
+
+    from speculative_verify_attention_gb300 import KVCacheQ8, kvq8_append, kvq8_quantize
+    inp = workloads.random_small(91, 8, 2, 256, 37, 4)
+    k = torch.from_numpy(inp.k).cuda()
+    v = torch.from_numpy(inp.v).cuda()
+    a = KVCacheQ8(2, 256, 64, device="cuda")
+    b = KVCacheQ8(2, 256, 64, device="cuda")
+    kvq8_append(k, v, a, 20)
+    kvq8_quantize(k, b.k_codes, b.k_scales, 20)
+    kvq8_quantize(v, b.v_codes, b.v_scales, 20)
+    torch.cuda.synchronize()
+    for name in ("k_codes", "k_scales", "v_codes", "v_scales"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+    orc = oracle.Cache(2, 256, 64)
+    orc.append(inp.k, inp.v, 20)
+    assert planes_equal(a, orc)
+    assert not a.k_codes[:, :20].any() and not a.v_codes[:, 57:].any()
+
+
+def test_append_rejects_bad_arguments(lib):
+    import torch
+
+    from speculative_verify_attention_gb300 import KVCacheQ8, KVQ8Error, kvq8_append
+    c = KVCacheQ8(1, 128, 16, device="cuda")
+    k = torch.zeros((4, 1, 128), device="cuda")
+    with pytest.raises(KVQ8Error) as e:       # past capacity
+        kvq8_append(k, k, c, 13)
+    assert e.value.status == 1
+    with pytest.raises(ValueError):           # shape does not match the cache
+        kvq8_append(torch.zeros((4, 2, 128), device="cuda"), k, c, 0)
