@@ -242,3 +242,6 @@ def combine(part_o, part_m, part_l) -> np.ndarray:
     if rc:
         raise ValueError("oracle_combine rejected its arguments")
     return out
+
+
+from .head import argmax_rows_top_prob  # noqa: E402  (verify-head acceptance oracle)
