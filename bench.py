@@ -352,6 +352,7 @@ def run_native(args, world, rank, local):
 
     # prompt chunk (tensor-core kernel), L2 flushed between timed calls
     prompt = prompt_bench(args, dev, fp16_peak) if not args.no_prompt else None
+    head = head_bench(dev, hbm_peak, args.ring_l2) if not args.no_head else None
 
     result = None
     if rank == 0:
@@ -384,6 +385,7 @@ def run_native(args, world, rank, local):
                          "algorithmic_bytes_per_launch": bytes_per_launch},
             "long_context": long_ctx,
             "prompt": prompt,
+            "verify_head": head,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "us_per_step": e2e_sec / e2e_steps * 1e6, "path": "python API, eager, pinned host buffers"},
@@ -391,6 +393,49 @@ def run_native(args, world, rank, local):
             "gpu_launches": launches_per_step * steps,
         }
     return result
+
+
+def head_bench(dev, hbm_peak, ring_l2):
+    """argmax_rows_top_prob over T x 248,320 fp32 logits (T = 4, 8, 32): device time per call from
+    a CUDA graph walking a ring of logits buffers larger than 4x the L2."""
+    import torch
+
+    from speculative_verify_attention_gb300 import argmax_rows_top_prob, load_library
+    V = 248320
+    res = {}
+    for T in (4, 8, 32):
+        nbytes = T * V * 4
+        n_ring = max(2, int(np.ceil(ring_l2 * L2_BYTES / nbytes)))
+        gen = torch.Generator(device=dev).manual_seed(77 + T)
+        ring = [torch.randn((T, V), device=dev, generator=gen) * 3.0 for _ in range(n_ring)]
+        idx = torch.empty(T, dtype=torch.int32, device=dev)
+        top = torch.empty(T, dtype=torch.float32, device=dev)
+        ws = torch.empty(max(16, int(load_library().argmax_rows_top_prob_workspace_bytes(T, V))), dtype=torch.uint8,
+                         device=dev)
+        for i in range(3):
+            argmax_rows_top_prob(ring[i % n_ring], workspace=ws, argmax=idx, top_prob=top)
+        torch.cuda.synchronize()
+        n_calls = max(n_ring, 32)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n_calls):
+                argmax_rows_top_prob(ring[i % n_ring], workspace=ws, argmax=idx, top_prob=top)
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 10
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / (reps * n_calls)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        res[f"T{T}"] = {"vocab": V, "us_per_call": us, "logits_gbs": gbs, "hbm_frac": gbs / hbm_peak,
+                        "ring": n_ring}
+        del ring
+        torch.cuda.empty_cache()
+    return res
 
 
 def prompt_bench(args, dev, fp16_peak):
@@ -541,6 +586,7 @@ def main():
     ap.add_argument("--ring-l2", type=float, default=4.2, help="ring size in multiples of the L2")
     ap.add_argument("--prompt-steps", type=int, default=10)
     ap.add_argument("--no-prompt", action="store_true")
+    ap.add_argument("--no-head", action="store_true", help="skip the verify-head (argmax / top probability) timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-long-context", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="per-cell verify sweep instead of the headline line")

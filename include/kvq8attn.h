@@ -135,6 +135,24 @@ int attn_verify_tree_q8(const float* q, int n_rows, int n_q_heads, const kvq8_ca
                         void* workspace, size_t workspace_bytes, int n_split, kvq8_stream_t stream);
 
 /*
+ * argmax_rows_top_prob -- verify-head acceptance: per row of fp32 logits [n_rows][vocab]
+ * (device, 4-byte aligned), argmax[i] (int32) = the first index of the row's maximum and
+ * top_prob[i] (fp32) = softmax(row)[argmax[i]] = 1 / sum_j exp(x_j - max).
+ * Special values: a row holding NaN gives the index of its first NaN and probability NaN;
+ * +inf entries share the probability mass equally (argmax = the first +inf); a row of -inf
+ * only gives index 0 and probability 1 / vocab; otherwise -inf entries carry probability 0.
+ * argmax is exact; top_prob is within 1e-5 (relative) of its fp64 value.
+ * workspace: device scratch of argmax_rows_top_prob_workspace_bytes(n_rows, vocab) bytes,
+ * 16-byte aligned.  1 <= n_rows <= 65535, vocab >= 1.  Errors: INVALID_ARG, WORKSPACE,
+ * MISALIGNED.  Two kernel launches; asynchronous on `stream`.
+ * Source: "Engine perf(hip): MTP draft, shared expert, verify/sampler head", Summary item 1
+ * and "Verification & Parity Evidence" (argmax_rows, row_top_prob over T x 248,320 logits).
+ */
+size_t argmax_rows_top_prob_workspace_bytes(int n_rows, int vocab);
+int argmax_rows_top_prob(const float* logits, int n_rows, int vocab, int32_t* argmax, float* top_prob,
+                         void* workspace, size_t workspace_bytes, kvq8_stream_t stream);
+
+/*
  * attn_combine -- merge split-context partials (log-sum-exp reducer).
  *   part_o  : fp32 [n_split][rows][head_dim]  unnormalised o_s = sum_n exp(s_n - m_s) v_n
  *   part_ml : fp32 [n_split][rows][2]         (m_s, l_s): m_s = max s_n over the slice in natural-log

@@ -28,7 +28,8 @@ KVQ8_ERR_CUDA = 5
 
 # Entry points declared in include/kvq8attn.h.
 EXPORTED = ("kvq8_quantize", "kvq8_append", "attn_verify_q8_workspace_bytes", "attn_verify_q8", "attn_verify_tree_q8", "attn_combine",
-            "attn_prompt_q8_workspace_bytes", "attn_prompt_q8", "attn_verify_q8_noalloc", "kvq8_device_error", "kvq8_status_str")
+            "attn_prompt_q8_workspace_bytes", "attn_prompt_q8", "attn_verify_q8_noalloc", "kvq8_device_error", "kvq8_status_str",
+            "argmax_rows_top_prob_workspace_bytes", "argmax_rows_top_prob")
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 
@@ -70,6 +71,10 @@ def load_library():
         lib.attn_verify_q8.restype = i32
         lib.attn_verify_tree_q8.argtypes = [vp, i32, i32, cp, i32, i32, vp, f32, vp, vp, sz, i32, vp]
         lib.attn_verify_tree_q8.restype = i32
+        lib.argmax_rows_top_prob_workspace_bytes.argtypes = [i32, i32]
+        lib.argmax_rows_top_prob_workspace_bytes.restype = sz
+        lib.argmax_rows_top_prob.argtypes = [vp, i32, i32, vp, vp, vp, sz, vp]
+        lib.argmax_rows_top_prob.restype = i32
         lib.attn_combine.argtypes = [vp, vp, i32, i32, i32, vp, vp]
         lib.attn_combine.restype = i32
         lib.attn_prompt_q8_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
@@ -216,6 +221,30 @@ def attn_verify_tree_q8(q: torch.Tensor, cache: KVCacheQ8, kv_len: int, q_pos0: 
                                             int(n_split), _stream(stream))
     _check("attn_verify_tree_q8", st)
     return out
+
+
+def argmax_rows_top_prob(logits: torch.Tensor, workspace: torch.Tensor | None = None, argmax=None, top_prob=None,
+                         stream=None):
+    """Verify-head acceptance over fp32 logits [T][V] on the device: returns (argmax int32 [T],
+    top_prob fp32 [T]) -- the first index of each row's maximum and softmax(row) there."""
+    _need(logits, "logits", torch.float32)
+    if logits.dim() != 2:
+        raise ValueError("logits must be [T][V]")
+    n_rows, vocab = logits.shape
+    if argmax is None:
+        argmax = torch.empty(n_rows, dtype=torch.int32, device=logits.device)
+    if top_prob is None:
+        top_prob = torch.empty(n_rows, dtype=torch.float32, device=logits.device)
+    _need(argmax, "argmax", torch.int32)
+    _need(top_prob, "top_prob", torch.float32)
+    lib = load_library()
+    if workspace is None:
+        workspace = torch.empty(max(int(lib.argmax_rows_top_prob_workspace_bytes(n_rows, vocab)), 16),
+                                dtype=torch.uint8, device=logits.device)
+    st = lib.argmax_rows_top_prob(_ptr(logits), n_rows, vocab, _ptr(argmax), _ptr(top_prob), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("argmax_rows_top_prob", st)
+    return argmax, top_prob
 
 
 def attn_combine(part_o: torch.Tensor, part_ml: torch.Tensor, out: torch.Tensor | None = None,
