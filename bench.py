@@ -5,8 +5,9 @@
 
 One JSON line on rank 0.  A step is one speculative-verify step on the 27B-class
 workload (24 q heads / 4 kv heads, head_dim 256, context 4096): for each window length
-T in {4, 8}, append the T new K/V tokens to the Q8_0 cache (kvq8_append, one launch) and
-run attn_verify_q8 (split-context kernel + log-sum-exp combine) over ctx + T keys.
+T in {4, 8}, one attn_verify_append_q8 call appends the T new K/V tokens to the Q8_0 cache
+(one quantiser launch) and runs the verify scan over ctx + T keys (split-context kernel,
+launched as a programmatic dependent of the append, + log-sum-exp combine).
 `value` is the KV-scan bandwidth of the whole job (Q8_0 K/V bytes read by the verify
 calls / time), in GB/s; `us_per_call` gives the per-call latency.  The prompt-chunk
 kernel (12 q heads / 1 kv head, hd256, 2048 queries over a 32768-token int8 context) is
@@ -193,8 +194,9 @@ def run_native(args, world, rank, local):
 
     import __graft_entry__
     __graft_entry__.build()
-    from speculative_verify_attention_gb300 import (KVCacheQ8, KVQ8Error, attn_prompt_q8, attn_verify_q8,
-                                                    attn_verify_q8_workspace_bytes, kvq8_append, workloads)
+    from speculative_verify_attention_gb300 import (KVCacheQ8, KVQ8Error, attn_prompt_q8, attn_verify_append_q8,
+                                                    attn_verify_append_q8_workspace_bytes, attn_verify_q8,
+                                                    attn_verify_q8_workspace_bytes, workloads)
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -221,16 +223,19 @@ def run_native(args, world, rank, local):
     knew = {T: torch.from_numpy(inp.k[ctx:ctx + T].copy()).to(dev) for T in VERIFY_T}
     vnew = {T: torch.from_numpy(inp.v[ctx:ctx + T].copy()).to(dev) for T in VERIFY_T}
     out = {T: torch.empty_like(q[T]) for T in VERIFY_T}
-    wsb = {T: torch.empty(attn_verify_q8_workspace_bytes(T, w0.n_q_heads, w0.head_dim, ctx + T, w0.n_kv_heads),
+    wsb = {T: torch.empty(max(attn_verify_q8_workspace_bytes(T, w0.n_q_heads, w0.head_dim, ctx + T, w0.n_kv_heads),
+                              attn_verify_append_q8_workspace_bytes(T, w0.n_q_heads, w0.head_dim, ctx,
+                                                                    w0.n_kv_heads)),
                           dtype=torch.uint8, device=dev) for T in VERIFY_T}
     kv_bytes_step = sum(ws_[T].kv_bytes() for T in VERIFY_T)
 
-    def step(s, do_append=True, do_verify=True):
+    def step(s, do_append=True):
         c = ring[s % n_ring]
         for T in VERIFY_T:
-            if do_append:
-                kvq8_append(knew[T], vnew[T], c, ctx)
-            if do_verify:
+            if do_append:   # append of the window's K/V fused with the verify scan
+                attn_verify_append_q8(q[T], knew[T], vnew[T], c, ctx, w0.softmax_scale, out=out[T],
+                                      workspace=wsb[T])
+            else:
                 attn_verify_q8(q[T], c, ctx + T, ctx, w0.softmax_scale, out=out[T], workspace=wsb[T])
 
     launches_per_step = len(VERIFY_T) * 3   # K+V append + verify split + combine per T
@@ -335,8 +340,7 @@ def run_native(args, world, rank, local):
             d_q[T].copy_(h_q[T], non_blocking=True)
             d_k[T].copy_(h_k[T], non_blocking=True)
             d_v[T].copy_(h_v[T], non_blocking=True)
-            c.append(d_k[T], d_v[T], ctx)
-            attn_verify_q8(d_q[T], c, ctx + T, ctx, w0.softmax_scale, out=out[T], workspace=wsb[T])
+            attn_verify_append_q8(d_q[T], d_k[T], d_v[T], c, ctx, w0.softmax_scale, out=out[T], workspace=wsb[T])
             h_out[T].copy_(out[T], non_blocking=True)
 
     e2e_steps = min(steps, 2000)
@@ -373,7 +377,8 @@ def run_native(args, world, rank, local):
                        "global_batch": world, "seq_len": ctx, "verify_rows": list(VERIFY_T),
                        "parallelism": f"replicas x{world}", "l2": f"ring of {n_ring} caches, "
                        f"{n_ring * cache_bytes / 2**20:.0f} MiB > 4x L2 (every step reads a different cache)",
-                       "step": "per T in {4,8}: kvq8_append (K and V) of T new tokens + attn_verify_q8 over ctx+T",
+                       "step": "per T in {4,8}: attn_verify_append_q8 (K/V of T new tokens appended, then the "
+                               "verify scan over ctx+T, overlapped)",
                        "graph": f"{GRAPH_STEPS} steps per CUDA graph replay"},
             "us_per_call": us_per_call_verify, "verify_only_gbs": verify_gbs,
             "hbm_frac": verify_gbs / hbm_peak, "per_T": per_t,

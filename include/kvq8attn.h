@@ -116,6 +116,34 @@ int attn_verify_q8(const float* q, int n_rows, int n_q_heads, const kvq8_cache* 
                    int q_pos0, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
                    int n_split, kvq8_stream_t stream);
 
+/* Bytes of workspace attn_verify_append_q8 needs (kv_len = q_pos0 + n_rows; n_split as there). */
+size_t attn_verify_append_q8_workspace_bytes(int n_rows, int n_q_heads, int head_dim, int q_pos0,
+                                             int n_kv_heads, int n_split);
+
+/*
+ * attn_verify_append_q8 -- kvq8_append of the window's K and V, then attn_verify_q8 over
+ * kv_len = q_pos0 + n_rows, as one call.
+ *   k_new, v_new : fp32 [n_rows][kv->n_kv_heads][kv->head_dim], device, 16-byte aligned:
+ *                  the window tokens' keys and values, quantised into positions
+ *                  [q_pos0, q_pos0 + n_rows) of the cache (bit-exact with kvq8_append).
+ *   n_split      : context slices over the keys below q_pos0 (0 = automatic); the window
+ *                  keys get one more slice of their own.
+ * The verify grid is launched as a programmatic dependent of the append kernel: every block
+ * but the window slice's reads q and the old keys while the append is still running, and
+ * the window slice waits for the append before it reads the new keys.  The result equals
+ * kvq8_append followed by attn_verify_q8 up to rounding order (the slices differ).
+ * Errors: as for kvq8_append and attn_verify_q8; INVALID_ARG also when k_new or v_new is
+ * null or q_pos0 + n_rows > capacity.
+ * No counterpart on the pages: the verify rows of "perf(gfx1100): share Q8 KV scans across
+ * verifier rows" (Summary) attend to the window's own keys, so those keys must be in the
+ * cache first; this entry point fuses that write (the quantiser of "Engine perf(hip): ...",
+ * Summary item 4) with the scan so the two overlap.
+ */
+int attn_verify_append_q8(const float* q, const float* k_new, const float* v_new, int n_rows,
+                          int n_q_heads, const kvq8_cache* kv, int q_pos0, float softmax_scale,
+                          float* out, void* workspace, size_t workspace_bytes, int n_split,
+                          kvq8_stream_t stream);
+
 /*
  * attn_verify_tree_q8 -- attn_verify_q8 for a tree-shaped verify window.
  *   window_mask : device uint32 [n_rows], 4-byte aligned: row i sees every key n < q_pos0

@@ -27,7 +27,8 @@ KVQ8_ERR_WORKSPACE = 4
 KVQ8_ERR_CUDA = 5
 
 # Entry points declared in include/kvq8attn.h.
-EXPORTED = ("kvq8_quantize", "kvq8_append", "attn_verify_q8_workspace_bytes", "attn_verify_q8", "attn_verify_tree_q8", "attn_combine",
+EXPORTED = ("kvq8_quantize", "kvq8_append", "attn_verify_q8_workspace_bytes", "attn_verify_q8", "attn_verify_tree_q8",
+            "attn_verify_append_q8_workspace_bytes", "attn_verify_append_q8", "attn_combine",
             "attn_prompt_q8_workspace_bytes", "attn_prompt_q8", "attn_verify_q8_noalloc", "kvq8_device_error", "kvq8_status_str",
             "argmax_rows_top_prob_workspace_bytes", "argmax_rows_top_prob")
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
@@ -71,6 +72,10 @@ def load_library():
         lib.attn_verify_q8.restype = i32
         lib.attn_verify_tree_q8.argtypes = [vp, i32, i32, cp, i32, i32, vp, f32, vp, vp, sz, i32, vp]
         lib.attn_verify_tree_q8.restype = i32
+        lib.attn_verify_append_q8_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.attn_verify_append_q8_workspace_bytes.restype = sz
+        lib.attn_verify_append_q8.argtypes = [vp, vp, vp, i32, i32, cp, i32, f32, vp, vp, sz, i32, vp]
+        lib.attn_verify_append_q8.restype = i32
         lib.argmax_rows_top_prob_workspace_bytes.argtypes = [i32, i32]
         lib.argmax_rows_top_prob_workspace_bytes.restype = sz
         lib.argmax_rows_top_prob.argtypes = [vp, i32, i32, vp, vp, vp, sz, vp]
@@ -220,6 +225,39 @@ def attn_verify_tree_q8(q: torch.Tensor, cache: KVCacheQ8, kv_len: int, q_pos0: 
                                             _ptr(workspace), workspace.numel() * workspace.element_size(),
                                             int(n_split), _stream(stream))
     _check("attn_verify_tree_q8", st)
+    return out
+
+
+def attn_verify_append_q8_workspace_bytes(n_rows: int, n_q_heads: int, head_dim: int, q_pos0: int,
+                                          n_kv_heads: int, n_split: int = 0) -> int:
+    return int(load_library().attn_verify_append_q8_workspace_bytes(n_rows, n_q_heads, head_dim, q_pos0,
+                                                                    n_kv_heads, n_split))
+
+
+def attn_verify_append_q8(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, cache: KVCacheQ8, q_pos0: int,
+                          softmax_scale: float, out: torch.Tensor | None = None,
+                          workspace: torch.Tensor | None = None, n_split: int = 0, stream=None) -> torch.Tensor:
+    """Append the window's fp32 keys and values [T][Hkv][hd] to the cache at q_pos0.. and run
+    verify attention of fp32 q [T][Hq][hd] over q_pos0 + T keys, in one call; returns fp32
+    [T][Hq][hd]."""
+    _need(q, "q", torch.float32)
+    _need(k_new, "k_new", torch.float32)
+    _need(v_new, "v_new", torch.float32)
+    n_rows, n_q_heads, head_dim = q.shape
+    if k_new.shape != v_new.shape or k_new.shape != (n_rows, cache.n_kv_heads, cache.head_dim):
+        raise ValueError(f"k_new and v_new must both be [{n_rows}][{cache.n_kv_heads}][{cache.head_dim}]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.float32)
+    if workspace is None:
+        nbytes = attn_verify_append_q8_workspace_bytes(n_rows, n_q_heads, head_dim, q_pos0, cache.n_kv_heads,
+                                                       n_split)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    st = load_library().attn_verify_append_q8(_ptr(q), _ptr(k_new), _ptr(v_new), n_rows, n_q_heads,
+                                              ctypes.byref(cache.struct()), int(q_pos0), float(softmax_scale),
+                                              _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                              int(n_split), _stream(stream))
+    _check("attn_verify_append_q8", st)
     return out
 
 

@@ -23,6 +23,9 @@ __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4* __rest
                                                             int8_t* __restrict__ codes1,
                                                             uint16_t* __restrict__ scales1, int capacity,
                                                             int pos0) {
+    // a verify kernel launched as a programmatic dependent may start now; it orders its reads
+    // of the appended keys with griddepcontrol.wait
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t blk_all = gid >> 3;  // Q8_0 block handled by this lane's group of 8
     const bool second = blk_all >= n_blocks;
@@ -84,6 +87,15 @@ int launch_quantize(const float* x0, const float* x1, int n_tok, int n_kv_heads,
 }
 
 }  // namespace
+
+// Both planes of `kv` at positions [pos0, pos0 + n_tok); arguments already validated.
+int launch_append(const float* k, const float* v, int n_tok, const kvq8_cache* kv, int pos0, cudaStream_t stream) {
+    if ((int64_t)pos0 + n_tok > kv->capacity || kv->head_dim % kQBlock) return KVQ8_ERR_INVALID_ARG;
+    return launch_quantize(k, v, n_tok, kv->n_kv_heads, kv->head_dim, const_cast<int8_t*>(kv->k_codes),
+                           const_cast<uint16_t*>(kv->k_scales), const_cast<int8_t*>(kv->v_codes),
+                           const_cast<uint16_t*>(kv->v_scales), kv->capacity, pos0, stream);
+}
+
 }  // namespace kvq8
 
 extern "C" int kvq8_quantize(const float* x, int n_tok, int n_kv_heads, int head_dim, int8_t* codes,

@@ -32,6 +32,7 @@ namespace kvq8 {
 
 int launch_combine(const float* part_o, const float* part_ml, int n_split, int rows, int head_dim, float* out,
                    cudaStream_t stream);
+int launch_append(const float* k, const float* v, int n_tok, const kvq8_cache* kv, int pos0, cudaStream_t stream);
 
 namespace {
 
@@ -58,6 +59,8 @@ struct VerifyParams {
     int kv_len;
     int q_pos0;
     int keys_per_split;
+    int key_shift;       // slice s starts at key s * keys_per_split - key_shift (0 without a window slice)
+    int n_ctx_splits;    // slices >= n_ctx_splits: the window slice, which waits for the append
     int rows_per_chunk;  // real rows per chunk (<= 8 * NT)
     float qscale;        // softmax_scale * log2(e)
     const uint32_t* wmask;  // tree windows: bit j of wmask[i] = row i sees key q_pos0 + j; null = causal
@@ -155,8 +158,13 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
     const int rows_total = p.n_rows * p.n_q_heads;
     const int row0 = chunk * p.rows_per_chunk;
     const int rows_here = min(p.rows_per_chunk, R - row0);
-    const int key_begin = split * p.keys_per_split;
-    const int key_end = min(key_begin + p.keys_per_split, p.kv_len);
+    // Slice s covers keys [s * keys_per_split - key_shift, (s + 1) * keys_per_split - key_shift)
+    // clipped to [0, kv_len). key_shift is 0 unless a window slice follows the context slices
+    // (the append-and-verify path): then it puts the end of slice n_ctx_splits - 1 at the first
+    // window key, and slice n_ctx_splits holds the window keys alone.
+    const int key_base = split * p.keys_per_split - p.key_shift;
+    const int key_begin = split == 0 ? 0 : key_base;  // key_shift < keys_per_split
+    const int key_end = min(key_base + p.keys_per_split, p.kv_len);
     const int64_t head_row0 = (int64_t)kvh * p.capacity;
     const int pvb = HD == 256 ? warp : (warp >> 1);  // PV output block of this warp
     uint16_t* sDv = reinterpret_cast<uint16_t*>(smem + L::kDv) + warp * kKT;
@@ -187,6 +195,10 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
         // The first K tile is requested after the q loads, so those are not queued behind
         // every block's first tile; K alone lands in about half the time of K + V.  The V
         // tile of each iteration is requested once its K has landed (top of the loop).
+        // The window keys are written by the append kernel launched just before this grid,
+        // which may still be running: only the window slice waits for it (every other slice
+        // reads keys and q that earlier work in the stream wrote).
+        if (split >= p.n_ctx_splits) asm volatile("griddepcontrol.wait;" ::: "memory");
         if (key_begin < key_end) {
             load_codes<HD>(sK, p.k_codes, head_row0, key_begin, key_end);
             load_scales<HD>(smem + L::kKs, p.k_scales, head_row0, key_begin, key_end);
@@ -549,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
 }
 
 struct Plan {
-    int hd, nt, n_chunks, rows_per_chunk, n_split, keys_per_split;
+    int hd, nt, n_chunks, rows_per_chunk, n_split, keys_per_split, key_shift, n_ctx_splits;
     size_t ws_bytes;
 };
 
@@ -560,7 +572,10 @@ int sm_count() {
     return n;
 }
 
-int make_plan(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_kv_heads, int n_split_req, Plan* pl) {
+// window_keys > 0: the last window_keys keys get a slice of their own (the append-and-verify
+// path), the context slices cover the keys before them.
+int make_plan(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_kv_heads, int n_split_req, Plan* pl,
+              int window_keys = 0) {
     if (n_rows < 1 || n_rows > 32 || n_q_heads < 1 || n_kv_heads < 1 || kv_len < 1) return KVQ8_ERR_INVALID_ARG;
     if (n_q_heads % n_kv_heads) return KVQ8_ERR_UNSUPPORTED;
     const int group = n_q_heads / n_kv_heads;
@@ -574,7 +589,9 @@ int make_plan(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_kv_head
     pl->nt = (pl->rows_per_chunk + 7) / 8;
     // slices are whole 64-key units; the automatic count fills every SM with as many thread
     // blocks as fit at once (two for NT <= 3, one at NT = 4)
-    const int n_units = (kv_len + kSplitUnit - 1) / kSplitUnit;
+    const int ctx_end = kv_len - window_keys;
+    if (ctx_end < 0) return KVQ8_ERR_INVALID_ARG;
+    const int n_units = (ctx_end + kSplitUnit - 1) / kSplitUnit;
     int ns = n_split_req;
     if (ns == 0) {
         int sms = sm_count();
@@ -582,20 +599,26 @@ int make_plan(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_kv_head
         const int per_sm = pl->nt <= 3 ? 2 : 1;
         ns = std::max(1, (per_sm * sms) / (n_kv_heads * pl->n_chunks));
     }
-    ns = std::min(ns, n_units);
+    ns = std::max(1, std::min(ns, n_units));
     // an automatic slice holds at least one whole 128-key tile
     const int min_units = n_split_req > 0 ? 1 : kKT / kSplitUnit;
     const int units_per_split = std::max(min_units, (n_units + ns - 1) / ns);
     pl->keys_per_split = units_per_split * kSplitUnit;
-    pl->n_split = (kv_len + pl->keys_per_split - 1) / pl->keys_per_split;
+    pl->n_ctx_splits = (ctx_end + pl->keys_per_split - 1) / pl->keys_per_split;
+    // with a window slice (window_keys <= 32 < keys_per_split) the context slices are aligned
+    // to end at ctx_end, so the first one is the short one
+    pl->key_shift = window_keys > 0 ? pl->n_ctx_splits * pl->keys_per_split - ctx_end : 0;
+    pl->n_split = pl->n_ctx_splits + (window_keys > 0 ? 1 : 0);
     const size_t rows_total = (size_t)n_rows * n_q_heads;
     const size_t o_bytes = (size_t)pl->n_split * rows_total * head_dim * sizeof(float);
     pl->ws_bytes = ((o_bytes + 255) / 256) * 256 + (size_t)pl->n_split * rows_total * 2 * sizeof(float);
     return KVQ8_OK;
 }
 
+// pdl: launch as a programmatic dependent of the kernel before it in the stream (the append
+// kernel); the window slice orders its reads with griddepcontrol.wait.
 template <int HD, int NT, bool TREE>
-int launch_verify(const VerifyParams& vp, const Plan& pl, int n_kv_heads, cudaStream_t stream) {
+int launch_verify(const VerifyParams& vp, const Plan& pl, int n_kv_heads, cudaStream_t stream, bool pdl) {
     constexpr int bytes = Smem<HD, NT>::kBytes;
     static bool attr_set = false;
     if (!attr_set) {
@@ -604,18 +627,26 @@ int launch_verify(const VerifyParams& vp, const Plan& pl, int n_kv_heads, cudaSt
             return KVQ8_ERR_CUDA;
         attr_set = true;
     }
-    dim3 grid(pl.n_chunks, pl.n_split, n_kv_heads);
-    verify_split_kernel<HD, NT, TREE><<<grid, kThreads, bytes, stream>>>(vp);
-    return launch_status();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(pl.n_chunks, pl.n_split, n_kv_heads);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, verify_split_kernel<HD, NT, TREE>, vp) == cudaSuccess ? KVQ8_OK : KVQ8_ERR_CUDA;
 }
 
 template <int HD, bool TREE>
-int dispatch_nt(const VerifyParams& vp, const Plan& pl, int n_kv_heads, cudaStream_t s) {
+int dispatch_nt(const VerifyParams& vp, const Plan& pl, int n_kv_heads, cudaStream_t s, bool pdl) {
     switch (pl.nt) {
-        case 1: return launch_verify<HD, 1, TREE>(vp, pl, n_kv_heads, s);
-        case 2: return launch_verify<HD, 2, TREE>(vp, pl, n_kv_heads, s);
-        case 3: return launch_verify<HD, 3, TREE>(vp, pl, n_kv_heads, s);
-        case 4: return launch_verify<HD, 4, TREE>(vp, pl, n_kv_heads, s);
+        case 1: return launch_verify<HD, 1, TREE>(vp, pl, n_kv_heads, s, pdl);
+        case 2: return launch_verify<HD, 2, TREE>(vp, pl, n_kv_heads, s, pdl);
+        case 3: return launch_verify<HD, 3, TREE>(vp, pl, n_kv_heads, s, pdl);
+        case 4: return launch_verify<HD, 4, TREE>(vp, pl, n_kv_heads, s, pdl);
         default: return KVQ8_ERR_UNSUPPORTED;
     }
 }
@@ -633,21 +664,28 @@ extern "C" size_t attn_verify_q8_workspace_bytes(int n_rows, int n_q_heads, int 
 namespace kvq8 {
 namespace {
 
+// k_new / v_new (append-and-verify): quantise the n_rows window tokens into positions
+// [q_pos0, q_pos0 + n_rows) first (kv_len must be q_pos0 + n_rows); the window keys then get
+// a slice of their own.
 int verify_impl(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv, int kv_len, int q_pos0,
                 const uint32_t* wmask, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
-                int n_split, kvq8_stream_t stream) {
+                int n_split, kvq8_stream_t stream, const float* k_new = nullptr, const float* v_new = nullptr) {
+    const bool append = k_new != nullptr;
     if (!kv || !q || !out) return KVQ8_ERR_INVALID_ARG;
     if (!kv->k_codes || !kv->k_scales || !kv->v_codes || !kv->v_scales) return KVQ8_ERR_INVALID_ARG;
     if (kv->n_kv_heads < 1 || kv->capacity < 1 || q_pos0 < 0) return KVQ8_ERR_INVALID_ARG;
     if (kv_len > kv->capacity) return KVQ8_ERR_INVALID_ARG;
     if (!(softmax_scale == softmax_scale) || softmax_scale == INFINITY || softmax_scale == -INFINITY)
         return KVQ8_ERR_INVALID_ARG;
+    if (append && (!v_new || kv_len != q_pos0 + n_rows)) return KVQ8_ERR_INVALID_ARG;
     Plan pl;
-    const int rc = make_plan(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, n_split, &pl);
+    const int rc = make_plan(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, n_split, &pl,
+                             append ? n_rows : 0);
     if (rc != KVQ8_OK) return rc;
     if (!aligned16(q) || !aligned16(out) || !aligned16(kv->k_codes) || !aligned16(kv->k_scales) ||
         !aligned16(kv->v_codes) || !aligned16(kv->v_scales))
         return KVQ8_ERR_MISALIGNED;
+    if (append && (!aligned16(k_new) || !aligned16(v_new))) return KVQ8_ERR_MISALIGNED;
     if (!workspace || workspace_bytes < pl.ws_bytes) return KVQ8_ERR_WORKSPACE;
     if (!aligned16(workspace)) return KVQ8_ERR_MISALIGNED;
 
@@ -668,17 +706,23 @@ int verify_impl(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv,
     vp.kv_len = kv_len;
     vp.q_pos0 = q_pos0;
     vp.keys_per_split = pl.keys_per_split;
+    vp.key_shift = pl.key_shift;
+    vp.n_ctx_splits = pl.n_ctx_splits;
     vp.rows_per_chunk = pl.rows_per_chunk;
     vp.qscale = softmax_scale * kLog2e;
     vp.wmask = wmask;
     cudaStream_t s = (cudaStream_t)stream;
+    if (append) {
+        const int ra = launch_append(k_new, v_new, n_rows, kv, q_pos0, s);
+        if (ra != KVQ8_OK) return ra;
+    }
     int r1;
     if (wmask)
-        r1 = pl.hd == 128 ? dispatch_nt<128, true>(vp, pl, kv->n_kv_heads, s)
-                          : dispatch_nt<256, true>(vp, pl, kv->n_kv_heads, s);
+        r1 = pl.hd == 128 ? dispatch_nt<128, true>(vp, pl, kv->n_kv_heads, s, append)
+                          : dispatch_nt<256, true>(vp, pl, kv->n_kv_heads, s, append);
     else
-        r1 = pl.hd == 128 ? dispatch_nt<128, false>(vp, pl, kv->n_kv_heads, s)
-                          : dispatch_nt<256, false>(vp, pl, kv->n_kv_heads, s);
+        r1 = pl.hd == 128 ? dispatch_nt<128, false>(vp, pl, kv->n_kv_heads, s, append)
+                          : dispatch_nt<256, false>(vp, pl, kv->n_kv_heads, s, append);
     if (r1 != KVQ8_OK) return r1;
     return launch_combine(vp.part_o, reinterpret_cast<const float*>(vp.part_ml), pl.n_split, (int)rows_total,
                           kv->head_dim, out, s);
@@ -692,6 +736,24 @@ extern "C" int attn_verify_q8(const float* q, int n_rows, int n_q_heads, const k
                               int n_split, kvq8_stream_t stream) {
     return kvq8::verify_impl(q, n_rows, n_q_heads, kv, kv_len, q_pos0, nullptr, softmax_scale, out, workspace,
                              workspace_bytes, n_split, stream);
+}
+
+extern "C" size_t attn_verify_append_q8_workspace_bytes(int n_rows, int n_q_heads, int head_dim, int q_pos0,
+                                                        int n_kv_heads, int n_split) {
+    kvq8::Plan pl;
+    if (q_pos0 < 0 || kvq8::make_plan(n_rows, n_q_heads, head_dim, q_pos0 + n_rows, n_kv_heads, n_split, &pl,
+                                      n_rows) != KVQ8_OK)
+        return 0;
+    return pl.ws_bytes;
+}
+
+extern "C" int attn_verify_append_q8(const float* q, const float* k_new, const float* v_new, int n_rows,
+                                     int n_q_heads, const kvq8_cache* kv, int q_pos0, float softmax_scale,
+                                     float* out, void* workspace, size_t workspace_bytes, int n_split,
+                                     kvq8_stream_t stream) {
+    if (!k_new || !v_new || q_pos0 < 0) return KVQ8_ERR_INVALID_ARG;
+    return kvq8::verify_impl(q, n_rows, n_q_heads, kv, q_pos0 + n_rows, q_pos0, nullptr, softmax_scale, out,
+                             workspace, workspace_bytes, n_split, stream, k_new, v_new);
 }
 
 extern "C" int attn_verify_tree_q8(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv, int kv_len,
