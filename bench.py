@@ -6,8 +6,8 @@
 One JSON line on rank 0.  A step is one speculative-verify step on the 27B-class
 workload (24 q heads / 4 kv heads, head_dim 256, context 4096): for each window length
 T in {4, 8}, one attn_verify_append_q8 call appends the T new K/V tokens to the Q8_0 cache
-(one quantiser launch) and runs the verify scan over ctx + T keys (split-context kernel,
-launched as a programmatic dependent of the append, + log-sum-exp combine).
+and runs the verify scan over ctx + T keys: the split-context kernel, whose window slice
+quantises the new tokens itself, and the log-sum-exp combine.
 `value` is the KV-scan bandwidth of the whole job (Q8_0 K/V bytes read by the verify
 calls / time), in GB/s; `us_per_call` gives the per-call latency.  The prompt-chunk
 kernel (12 q heads / 1 kv head, hd256, 2048 queries over a 32768-token int8 context) is
@@ -238,7 +238,7 @@ def run_native(args, world, rank, local):
             else:
                 attn_verify_q8(q[T], c, ctx + T, ctx, w0.softmax_scale, out=out[T], workspace=wsb[T])
 
-    launches_per_step = len(VERIFY_T) * 3   # K+V append + verify split + combine per T
+    launches_per_step = len(VERIFY_T) * 2   # verify split (with the append) + combine per T
 
     def capture(**kw):
         s = torch.cuda.Stream(device=dev)
@@ -377,8 +377,8 @@ def run_native(args, world, rank, local):
                        "global_batch": world, "seq_len": ctx, "verify_rows": list(VERIFY_T),
                        "parallelism": f"replicas x{world}", "l2": f"ring of {n_ring} caches, "
                        f"{n_ring * cache_bytes / 2**20:.0f} MiB > 4x L2 (every step reads a different cache)",
-                       "step": "per T in {4,8}: attn_verify_append_q8 (K/V of T new tokens appended, then the "
-                               "verify scan over ctx+T, overlapped)",
+                       "step": "per T in {4,8}: attn_verify_append_q8 (K/V of T new tokens quantised into the "
+                               "cache by the verify kernel's window slice; scan over ctx+T)",
                        "graph": f"{GRAPH_STEPS} steps per CUDA graph replay"},
             "us_per_call": us_per_call_verify, "verify_only_gbs": verify_gbs,
             "hbm_frac": verify_gbs / hbm_peak, "per_T": per_t,

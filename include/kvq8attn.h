@@ -128,10 +128,11 @@ size_t attn_verify_append_q8_workspace_bytes(int n_rows, int n_q_heads, int head
  *                  [q_pos0, q_pos0 + n_rows) of the cache (bit-exact with kvq8_append).
  *   n_split      : context slices over the keys below q_pos0 (0 = automatic); the window
  *                  keys get one more slice of their own.
- * The verify grid is launched as a programmatic dependent of the append kernel: every block
- * but the window slice's reads q and the old keys while the append is still running, and
- * the window slice waits for the append before it reads the new keys.  The result equals
- * kvq8_append followed by attn_verify_q8 up to rounding order (the slices differ).
+ * Two launches, as attn_verify_q8: the verify grid gets one more slice per KV head holding
+ * the window keys alone, and that slice's blocks quantise k_new / v_new themselves (into
+ * their tiles and into the cache) while every other block scans the old keys.  The cache
+ * bytes equal kvq8_append's; the result equals kvq8_append followed by attn_verify_q8 up to
+ * rounding order (the slices differ).
  * Errors: as for kvq8_append and attn_verify_q8; INVALID_ARG also when k_new or v_new is
  * null or q_pos0 + n_rows > capacity.
  * No counterpart on the pages: the verify rows of "perf(gfx1100): share Q8 KV scans across

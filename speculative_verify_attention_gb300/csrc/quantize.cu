@@ -6,9 +6,11 @@
 //
 // Here a warp covers four blocks: eight lanes per block, four values per lane (one
 // 16-byte load), a 3-step shuffle max, then per value an IEEE fp32 division and round
-// half away from zero.  Bandwidth-bound: 4 bytes read, 1 + 1/16 bytes written per value.
+// half away from zero (q8_0_block).  Bandwidth-bound: 4 bytes read, 1 + 1/16 bytes
+// written per value.
 // kvq8_append writes both planes (K and V) of a cache in one launch.
 #include "common.cuh"
+#include "q8_0.cuh"
 
 namespace kvq8 {
 namespace {
@@ -23,9 +25,6 @@ __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4* __rest
                                                             int8_t* __restrict__ codes1,
                                                             uint16_t* __restrict__ scales1, int capacity,
                                                             int pos0) {
-    // a verify kernel launched as a programmatic dependent may start now; it orders its reads
-    // of the appended keys with griddepcontrol.wait
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t blk_all = gid >> 3;  // Q8_0 block handled by this lane's group of 8
     const bool second = blk_all >= n_blocks;
@@ -37,20 +36,10 @@ __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4* __rest
     const bool live = blk_all < (x1 ? 2 * n_blocks : n_blocks);
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (live) v = __ldg(x + blk * 8 + sub);
-    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    uint16_t scale_bits;
+    const uint32_t packed = q8_0_block(v, &scale_bits);
     if (!live) return;
 
-    const float d32 = __fdiv_rn(amax, 127.0f);
-    int8_t q[4];
-    const float xs[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        float r = 0.0f;
-        if (d32 != 0.0f) r = fminf(fmaxf(roundf(__fdiv_rn(xs[e], d32)), -127.0f), 127.0f);
-        q[e] = (int8_t)(int)r;
-    }
     // block index -> (token, kv head, block within the head row)
     const int64_t row_blocks = (int64_t)n_kv_heads * nb_per_head_row;
     const int64_t tok = blk / row_blocks;
@@ -58,11 +47,9 @@ __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4* __rest
     const int h = (int)(rem / nb_per_head_row);
     const int b = (int)(rem - (int64_t)h * nb_per_head_row);
     const int64_t row = (int64_t)h * capacity + pos0 + tok;
-    uint32_t packed = (uint32_t)(uint8_t)q[0] | ((uint32_t)(uint8_t)q[1] << 8) | ((uint32_t)(uint8_t)q[2] << 16) |
-                      ((uint32_t)(uint8_t)q[3] << 24);
     int8_t* dst = codes + row * (int64_t)nb_per_head_row * kQBlock + b * kQBlock + sub * 4;
     *reinterpret_cast<uint32_t*>(dst) = packed;
-    if (sub == 0) scales[row * nb_per_head_row + b] = __half_as_ushort(__float2half_rn(d32));
+    if (sub == 0) scales[row * nb_per_head_row + b] = scale_bits;
 }
 
 }  // namespace
@@ -87,15 +74,6 @@ int launch_quantize(const float* x0, const float* x1, int n_tok, int n_kv_heads,
 }
 
 }  // namespace
-
-// Both planes of `kv` at positions [pos0, pos0 + n_tok); arguments already validated.
-int launch_append(const float* k, const float* v, int n_tok, const kvq8_cache* kv, int pos0, cudaStream_t stream) {
-    if ((int64_t)pos0 + n_tok > kv->capacity || kv->head_dim % kQBlock) return KVQ8_ERR_INVALID_ARG;
-    return launch_quantize(k, v, n_tok, kv->n_kv_heads, kv->head_dim, const_cast<int8_t*>(kv->k_codes),
-                           const_cast<uint16_t*>(kv->k_scales), const_cast<int8_t*>(kv->v_codes),
-                           const_cast<uint16_t*>(kv->v_scales), kv->capacity, pos0, stream);
-}
-
 }  // namespace kvq8
 
 extern "C" int kvq8_quantize(const float* x, int n_tok, int n_kv_heads, int head_dim, int8_t* codes,

@@ -27,12 +27,12 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "q8_0.cuh"
 
 namespace kvq8 {
 
 int launch_combine(const float* part_o, const float* part_ml, int n_split, int rows, int head_dim, float* out,
                    cudaStream_t stream);
-int launch_append(const float* k, const float* v, int n_tok, const kvq8_cache* kv, int pos0, cudaStream_t stream);
 
 namespace {
 
@@ -60,7 +60,10 @@ struct VerifyParams {
     int q_pos0;
     int keys_per_split;
     int key_shift;       // slice s starts at key s * keys_per_split - key_shift (0 without a window slice)
-    int n_ctx_splits;    // slices >= n_ctx_splits: the window slice, which waits for the append
+    int n_ctx_splits;    // slices >= n_ctx_splits: the window slice (append-and-verify path)
+    int n_kv_heads;
+    const float* k_new;  // append-and-verify: fp32 [n_rows][n_kv_heads][HD] window keys and values,
+    const float* v_new;  // quantised by the window slice (into its tile and into the cache)
     int rows_per_chunk;  // real rows per chunk (<= 8 * NT)
     float qscale;        // softmax_scale * log2(e)
     const uint32_t* wmask;  // tree windows: bit j of wmask[i] = row i sees key q_pos0 + j; null = causal
@@ -128,6 +131,55 @@ __device__ __forceinline__ void load_scales(uint8_t* smem, const uint16_t* plane
     }
 }
 
+// Append-and-verify, window slice: quantises the nk (<= 32) window tokens' fp32 keys and
+// values to Q8_0 (bit-exact with the append kernel).  The keys go straight into this block's
+// K tile (the layout load_codes and load_scales produce, rows past nk zeroed as the
+// zero-filling copies would leave them) and, from the chunk-0 block, into the cache.  The
+// values go to the cache only: the tile loop then loads them like any V tile, after the
+// barrier at its top has made this block's stores visible.  With several row chunks every
+// chunk's window block stores the same value bytes.  8 lanes per 32-value block, both planes
+// in one pass over 2 nk HD/32 blocks.
+template <int HD>
+__device__ __forceinline__ void window_tile(const VerifyParams& p, uint8_t* smem, int kvh, bool chunk0, int pos0,
+                                            int nk) {
+    using L = Smem<HD, 1>;  // the tile offsets do not depend on NT
+    constexpr int NB = HD / 32;
+    uint8_t* sK = smem + L::kK;
+    uint16_t* sKs = reinterpret_cast<uint16_t*>(smem + L::kKs);
+    // zero code rows [nk, 32) (read by the 16-key steps) and scale rows [nk, kKT)
+    for (int i = nk * HD / 16 + threadIdx.x; i < 32 * HD / 16; i += kThreads)
+        reinterpret_cast<uint4*>(sK)[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = nk * NB / 2 + threadIdx.x; i < kKT * NB / 2; i += kThreads)
+        reinterpret_cast<uint32_t*>(sKs)[i] = 0u;
+    const int nblk = nk * NB;  // blocks per plane
+    const int sub = threadIdx.x & 7;
+    for (int base = 0; base < 2 * nblk; base += kThreads / 8) {  // uniform trip count
+        const int blk = base + (threadIdx.x >> 3);
+        const bool live = blk < 2 * nblk;
+        const bool vplane = blk >= nblk;
+        const int bb = vplane ? blk - nblk : blk;
+        const int j = bb / NB, b = bb - j * NB;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live)
+            x = __ldg(reinterpret_cast<const float4*>((vplane ? p.v_new : p.k_new) +
+                                                      ((int64_t)j * p.n_kv_heads + kvh) * HD + 32 * b) + sub);
+        uint16_t scale_bits;
+        const uint32_t packed = q8_0_block(x, &scale_bits);
+        if (!live) continue;
+        const int64_t row = (int64_t)kvh * p.capacity + pos0 + j;
+        if (!vplane) {
+            *reinterpret_cast<uint32_t*>(sK + swz<HD>(j, 32 * b + 4 * sub)) = packed;
+            if (sub == 0) sKs[j * NB + b] = scale_bits;
+        }
+        if (vplane || chunk0) {
+            int8_t* codes = const_cast<int8_t*>(vplane ? p.v_codes : p.k_codes);
+            uint16_t* scales = const_cast<uint16_t*>(vplane ? p.v_scales : p.k_scales);
+            *reinterpret_cast<uint32_t*>(codes + row * HD + 32 * b + 4 * sub) = packed;
+            if (sub == 0) scales[row * NB + b] = scale_bits;
+        }
+    }
+}
+
 // Work split inside a thread block (8 warps):
 //   QK  : warp w owns keys 16w .. 16w+15 of the tile (one m16 fragment), all row tiles;
 //   PV  : at hd256 warp w owns the 32-dim output block w (two m16 fragments); at hd128 warps
@@ -136,7 +188,7 @@ __device__ __forceinline__ void load_scales(uint8_t* smem, const uint16_t* plane
 // both the S^T and the O^T fragments, so the softmax factors never leave the thread.
 // TREE: the window's rows see the window keys their mask selects (p.wmask); otherwise the
 // window is sequential (row i sees keys < q_pos0 + i + 1) and the mask code is compiled out.
-template <int HD, int NT, bool TREE>
+template <int HD, int NT, bool TREE, bool APPEND>
 __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kernel(const VerifyParams p) {
     using L = Smem<HD, NT>;
     constexpr int NB = L::NB, RP = L::RP, PS = L::PS;
@@ -195,11 +247,8 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
         // The first K tile is requested after the q loads, so those are not queued behind
         // every block's first tile; K alone lands in about half the time of K + V.  The V
         // tile of each iteration is requested once its K has landed (top of the loop).
-        // The window keys are written by the append kernel launched just before this grid,
-        // which may still be running: only the window slice waits for it (every other slice
-        // reads keys and q that earlier work in the stream wrote).
-        if (split >= p.n_ctx_splits) asm volatile("griddepcontrol.wait;" ::: "memory");
-        if (key_begin < key_end) {
+        // (on the append-and-verify path the window slice quantises its tile itself, below)
+        if (key_begin < key_end && !(APPEND && split >= p.n_ctx_splits)) {
             load_codes<HD>(sK, p.k_codes, head_row0, key_begin, key_end);
             load_scales<HD>(smem + L::kKs, p.k_scales, head_row0, key_begin, key_end);
         }
@@ -225,6 +274,10 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
             dst[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             dst[32] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
+    }
+
+    if constexpr (APPEND) {
+        if (split >= p.n_ctx_splits) window_tile<HD>(p, smem, kvh, chunk == 0, key_begin, key_end - key_begin);
     }
 
     // Visibility bound per owned row (row rr sees keys < vis_end; for a tree window, keys at
@@ -615,38 +668,28 @@ int make_plan(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_kv_head
     return KVQ8_OK;
 }
 
-// pdl: launch as a programmatic dependent of the kernel before it in the stream (the append
-// kernel); the window slice orders its reads with griddepcontrol.wait.
-template <int HD, int NT, bool TREE>
-int launch_verify(const VerifyParams& vp, const Plan& pl, int n_kv_heads, cudaStream_t stream, bool pdl) {
+template <int HD, int NT, bool TREE, bool APPEND>
+int launch_verify(const VerifyParams& vp, const Plan& pl, int n_kv_heads, cudaStream_t stream) {
     constexpr int bytes = Smem<HD, NT>::kBytes;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(verify_split_kernel<HD, NT, TREE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 bytes) != cudaSuccess)
+        if (cudaFuncSetAttribute(verify_split_kernel<HD, NT, TREE, APPEND>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
             return KVQ8_ERR_CUDA;
         attr_set = true;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(pl.n_chunks, pl.n_split, n_kv_heads);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = bytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, verify_split_kernel<HD, NT, TREE>, vp) == cudaSuccess ? KVQ8_OK : KVQ8_ERR_CUDA;
+    dim3 grid(pl.n_chunks, pl.n_split, n_kv_heads);
+    verify_split_kernel<HD, NT, TREE, APPEND><<<grid, kThreads, bytes, stream>>>(vp);
+    return launch_status();
 }
 
-template <int HD, bool TREE>
-int dispatch_nt(const VerifyParams& vp, const Plan& pl, int n_kv_heads, cudaStream_t s, bool pdl) {
+template <int HD, bool TREE, bool APPEND>
+int dispatch_nt(const VerifyParams& vp, const Plan& pl, int n_kv_heads, cudaStream_t s) {
     switch (pl.nt) {
-        case 1: return launch_verify<HD, 1, TREE>(vp, pl, n_kv_heads, s, pdl);
-        case 2: return launch_verify<HD, 2, TREE>(vp, pl, n_kv_heads, s, pdl);
-        case 3: return launch_verify<HD, 3, TREE>(vp, pl, n_kv_heads, s, pdl);
-        case 4: return launch_verify<HD, 4, TREE>(vp, pl, n_kv_heads, s, pdl);
+        case 1: return launch_verify<HD, 1, TREE, APPEND>(vp, pl, n_kv_heads, s);
+        case 2: return launch_verify<HD, 2, TREE, APPEND>(vp, pl, n_kv_heads, s);
+        case 3: return launch_verify<HD, 3, TREE, APPEND>(vp, pl, n_kv_heads, s);
+        case 4: return launch_verify<HD, 4, TREE, APPEND>(vp, pl, n_kv_heads, s);
         default: return KVQ8_ERR_UNSUPPORTED;
     }
 }
@@ -664,9 +707,8 @@ extern "C" size_t attn_verify_q8_workspace_bytes(int n_rows, int n_q_heads, int 
 namespace kvq8 {
 namespace {
 
-// k_new / v_new (append-and-verify): quantise the n_rows window tokens into positions
-// [q_pos0, q_pos0 + n_rows) first (kv_len must be q_pos0 + n_rows); the window keys then get
-// a slice of their own.
+// k_new / v_new (append-and-verify): the n_rows window tokens (kv_len must be q_pos0 + n_rows)
+// get a slice of their own, whose blocks quantise them into their tiles and into the cache.
 int verify_impl(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv, int kv_len, int q_pos0,
                 const uint32_t* wmask, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
                 int n_split, kvq8_stream_t stream, const float* k_new = nullptr, const float* v_new = nullptr) {
@@ -711,18 +753,20 @@ int verify_impl(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv,
     vp.rows_per_chunk = pl.rows_per_chunk;
     vp.qscale = softmax_scale * kLog2e;
     vp.wmask = wmask;
+    vp.n_kv_heads = kv->n_kv_heads;
+    vp.k_new = k_new;
+    vp.v_new = v_new;
     cudaStream_t s = (cudaStream_t)stream;
-    if (append) {
-        const int ra = launch_append(k_new, v_new, n_rows, kv, q_pos0, s);
-        if (ra != KVQ8_OK) return ra;
-    }
     int r1;
-    if (wmask)
-        r1 = pl.hd == 128 ? dispatch_nt<128, true>(vp, pl, kv->n_kv_heads, s, append)
-                          : dispatch_nt<256, true>(vp, pl, kv->n_kv_heads, s, append);
+    if (wmask)  // tree windows have no append variant
+        r1 = pl.hd == 128 ? dispatch_nt<128, true, false>(vp, pl, kv->n_kv_heads, s)
+                          : dispatch_nt<256, true, false>(vp, pl, kv->n_kv_heads, s);
+    else if (append)
+        r1 = pl.hd == 128 ? dispatch_nt<128, false, true>(vp, pl, kv->n_kv_heads, s)
+                          : dispatch_nt<256, false, true>(vp, pl, kv->n_kv_heads, s);
     else
-        r1 = pl.hd == 128 ? dispatch_nt<128, false>(vp, pl, kv->n_kv_heads, s, append)
-                          : dispatch_nt<256, false>(vp, pl, kv->n_kv_heads, s, append);
+        r1 = pl.hd == 128 ? dispatch_nt<128, false, false>(vp, pl, kv->n_kv_heads, s)
+                          : dispatch_nt<256, false, false>(vp, pl, kv->n_kv_heads, s);
     if (r1 != KVQ8_OK) return r1;
     return launch_combine(vp.part_o, reinterpret_cast<const float*>(vp.part_ml), pl.n_split, (int)rows_total,
                           kv->head_dim, out, s);
