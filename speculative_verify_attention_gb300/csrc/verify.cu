@@ -55,6 +55,7 @@ struct VerifyParams {
     int n_rows;        // T
     int n_q_heads;
     int group;
+    int group_magic;     // ceil(2^20 / group): x / group == (x * group_magic) >> 20 for x * group < 2^20
     int capacity;
     int kv_len;
     int q_pos0;
@@ -130,6 +131,18 @@ __device__ __forceinline__ void load_scales(uint8_t* smem, const uint16_t* plane
             cp_async_8(base + n * SB, src, ok ? 8 : 0);
     }
 }
+
+// Row index / group by a multiply: (x * ceil(2^20 / g)) >> 20 equals x / g whenever x g < 2^20,
+// which holds for every row index here (x < 32 rows * 64 heads per group, g <= 64).
+__device__ __forceinline__ int div_group(int x, const VerifyParams& p) {
+    return (int)(((uint32_t)x * (uint32_t)p.group_magic) >> 20);
+}
+
+// frexp's exponent of a positive normal float (x = m 2^e, m in [0.5, 1)), and 2^n for a
+// normal result (-126 <= n <= 127), from the exponent bits.  The V scales reaching them are
+// fp16 values as fp32, so x is normal and n stays within [-60, 40].
+__device__ __forceinline__ int frexp_exponent(float x) { return (int)((__float_as_uint(x) >> 23) & 0xFFu) - 126; }
+__device__ __forceinline__ float exp2_int(int n) { return __uint_as_float((uint32_t)(n + 127) << 23); }
 
 // Append-and-verify, window slice: quantises the nk (<= 32) window tokens' fp32 keys and
 // values to Q8_0 (bit-exact with the append kernel).  The keys go straight into this block's
@@ -237,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
             v[k][0] = v[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (idx < RP * GPR && r < rows_here) {
                 const int rr = row0 + r;
-                const int i = rr / p.group, hh = rr - i * p.group;
+                const int i = div_group(rr, p), hh = rr - i * p.group;
                 const float4* src =
                     reinterpret_cast<const float4*>(p.q + ((int64_t)i * p.n_q_heads + kvh * p.group + hh) * HD) + 2 * j8;
                 v[k][0] = __ldg(src);
@@ -291,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
             const int r = 8 * nt + 2 * t + c;
             if (r < rows_here) {
                 const int rr = row0 + r;
-                const int i = rr / p.group, hh = rr - i * p.group;
+                const int i = div_group(rr, p), hh = rr - i * p.group;
                 vis_end[nt][c] = min(min(tree ? p.q_pos0 + 32 : p.q_pos0 + i + 1, p.kv_len), key_end);
                 grow[nt][c] = i * p.n_q_heads + kvh * p.group + hh;
             } else {
@@ -302,12 +315,12 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
 
     if (TREE && threadIdx.x < RP) {  // the window mask of each row of the chunk (read in masked tiles)
         const int r = threadIdx.x;
-        sWm[r] = r < rows_here ? __ldg(p.wmask + (row0 + r) / p.group) : 0u;
+        sWm[r] = r < rows_here ? __ldg(p.wmask + div_group(row0 + r, p)) : 0u;
     }  // published by the barrier at the top of the first tile
 
     // every real row of this chunk sees all keys below vis_min; padding rows hold q = 0 and
     // never reach the output, so tiles wholly below vis_min skip the mask
-    const int vis_min = min(min(tree ? p.q_pos0 : p.q_pos0 + row0 / p.group + 1, p.kv_len), key_end);
+    const int vis_min = min(min(tree ? p.q_pos0 : p.q_pos0 + div_group(row0, p) + 1, p.kv_len), key_end);
     float m_ref[NT][2], l_w[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -324,6 +337,19 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
 #pragma unroll
             for (int c = 0; c < 4; ++c) O[mt][nt][c] = 0.0f;
     int E = INT32_MIN;  // unset
+
+    // Per-lane shared-memory bases of the inner loops, fixed for the whole slice.
+    // QK: row n0 = 16 warp + g reads bytes 32b + 8t .. +7, i.e. chunk 2b + t/2 of 16 bytes at
+    // offset 8 (t & 1), stored at chunk (2b + t/2) ^ g = ((2b) ^ (g & 6)) + ((t/2) ^ (g & 1)).
+    const int k_gh = g & 6;
+    const uint8_t* const k_lane = sK + (warp * 16 + g) * HD + ((((t >> 1) ^ (g & 1))) << 4) + 8 * (t & 1);
+    const uint4* const q_lane = reinterpret_cast<const uint4*>(sQ) + lane;
+    // PV: rows 16 ks + 2t (+1, +8, +9) have swizzle phase 2t (2t + 1); the lane's 4 bytes sit at
+    // dims 32 pvb + 4g, chunk 2 pvb + g/4, offset 4 (g & 3).
+    const int v_cx = 2 * pvb + (g >> 2);
+    const int v_off0 = (2 * t) * HD + ((v_cx ^ (2 * t)) << 4) + 4 * (g & 3);
+    const int v_off1 = (2 * t + 1) * HD + ((v_cx ^ (2 * t + 1)) << 4) + 4 * (g & 3);
+    const uint2* const p_lane = sP + t * PS + g;
 
     for (int tile0 = key_begin; tile0 < key_end; tile0 += kKT) {
         const int nk = min(kKT, key_end - tile0);  // keys of this tile inside the slice
@@ -344,14 +370,16 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
 #pragma unroll 2
             for (int b = 0; b < NB; ++b) {
                 uint4 qh[NT], ql[NT];
+                const uint4* qp = q_lane + b * NT * 64;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const uint4* qp = reinterpret_cast<const uint4*>(sQ + ((b * NT + nt) * 2) * 256) + lane;
-                    qh[nt] = qp[0];
-                    ql[nt] = qp[32];
+                    qh[nt] = qp[nt * 64];
+                    ql[nt] = qp[nt * 64 + 32];
                 }
-                const uint2 k0 = *reinterpret_cast<const uint2*>(sK + swz<HD>(n0, 32 * b + 8 * t));
-                const uint2 k1 = *reinterpret_cast<const uint2*>(sK + swz<HD>(n0 + 8, 32 * b + 8 * t));
+                // rows n0 and n0 + 8 share the swizzle phase g: chunk (2b + t/2) ^ g
+                const uint8_t* kp = k_lane + (((2 * b) ^ k_gh) << 4);
+                const uint2 k0 = *reinterpret_cast<const uint2*>(kp);
+                const uint2 k1 = *reinterpret_cast<const uint2*>(kp + 8 * HD);
                 const uint32_t x0 = k0.x ^ 0x80808080u, x1 = k1.x ^ 0x80808080u;
                 const uint32_t y0 = k0.y ^ 0x80808080u, y1 = k1.y ^ 0x80808080u;
                 const uint32_t a00 = biased_bytes_to_half2<0x4140>(x0), a01 = biased_bytes_to_half2<0x4140>(x1);
@@ -492,13 +520,11 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, o));
             if (dmax > 0.0f) {
-                int e2;
-                (void)frexpf(dmax, &e2);
-                const int et = 2 - e2;
+                const int et = 2 - frexp_exponent(dmax);
                 if (E == INT32_MIN) {
                     E = et;
                 } else if (et < E) {
-                    const float f = ldexpf(1.0f, et - E);
+                    const float f = exp2_int(et - E);
 #pragma unroll
                     for (int mt = 0; mt < MTW; ++mt)
 #pragma unroll
@@ -508,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
                     E = et;
                 }
             }
-            const float esc = (E == INT32_MIN) ? 0.0f : ldexpf(1.0f, E);
+            const float esc = (E == INT32_MIN) ? 0.0f : exp2_int(E);
 #pragma unroll
             for (int k = 0; k < kKT / 32; ++k) sDv[lane + 32 * k] = __half_as_ushort(__float2half_rn(dv[k] * esc));
             __syncwarp();
@@ -518,18 +544,19 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
         for (int ks = 0; ks < n_ks; ++ks) {
             const int kb = ks * 16;
             uint2 pp01[NT], pp89[NT];  // (hi, lo) pairs of keys (2t, 2t+1) and (2t+8, 2t+9), row g of n-tile
+            const uint2* pp = p_lane + ks * 8 * PS;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                pp01[nt] = sP[((kb >> 1) + t) * PS + 8 * nt + g];
-                pp89[nt] = sP[((kb >> 1) + t + 4) * PS + 8 * nt + g];
+                pp01[nt] = pp[8 * nt];
+                pp89[nt] = pp[4 * PS + 8 * nt];
             }
             const __half2 d01 = u32_as_h2(*reinterpret_cast<const uint32_t*>(sDv + kb + 2 * t));
             const __half2 d89 = u32_as_h2(*reinterpret_cast<const uint32_t*>(sDv + kb + 2 * t + 8));
-            const int cb = 32 * pvb + 4 * g;
-            const uint32_t w0 = *reinterpret_cast<const uint32_t*>(sV + swz<HD>(kb + 2 * t, cb)) ^ 0x80808080u;
-            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(sV + swz<HD>(kb + 2 * t + 1, cb)) ^ 0x80808080u;
-            const uint32_t w8 = *reinterpret_cast<const uint32_t*>(sV + swz<HD>(kb + 2 * t + 8, cb)) ^ 0x80808080u;
-            const uint32_t w9 = *reinterpret_cast<const uint32_t*>(sV + swz<HD>(kb + 2 * t + 9, cb)) ^ 0x80808080u;
+            const uint8_t* vp = sV + ks * 16 * HD;
+            const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vp + v_off0) ^ 0x80808080u;
+            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vp + v_off1) ^ 0x80808080u;
+            const uint32_t w8 = *reinterpret_cast<const uint32_t*>(vp + v_off0 + 8 * HD) ^ 0x80808080u;
+            const uint32_t w9 = *reinterpret_cast<const uint32_t*>(vp + v_off1 + 8 * HD) ^ 0x80808080u;
             uint32_t A[MTW][4];
             if (HD == 256 || (warp & 1) == 0) {  // dims 4g, 4g+1 (and 4g+2, 4g+3 at hd256)
                 const uint32_t y01 = prmt2<0x5140>(w0, w1), y89 = prmt2<0x5140>(w8, w9);
@@ -582,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
     float* po = p.part_o + (int64_t)split * rows_total * HD;
     // O is (p 2^kPShift)(v 2^E) summed; lane owns dims 32b + 4g .. +3 (hd256) or the pair at
     // 32b + 4g + 2(w & 1) (hd128) of rows 8nt + 2t + c
-    const float inv = (E == INT32_MIN) ? 1.0f : ldexpf(1.0f, -E - (int)kPShift);
+    const float inv = (E == INT32_MIN) ? 1.0f : exp2_int(-E - (int)kPShift);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -597,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
             }
         }
     if (warp == 0 && g == 0) {
-        const float lscale = ldexpf(1.0f, -(int)kPShift);
+        const float lscale = exp2_int(-(int)kPShift);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -744,6 +771,7 @@ int verify_impl(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv,
     vp.n_rows = n_rows;
     vp.n_q_heads = n_q_heads;
     vp.group = n_q_heads / kv->n_kv_heads;
+    vp.group_magic = ((1 << 20) + vp.group - 1) / vp.group;  // exact: rows * group <= 32 * 64^2 < 2^20
     vp.capacity = kv->capacity;
     vp.kv_len = kv_len;
     vp.q_pos0 = q_pos0;
