@@ -116,6 +116,32 @@ int attn_verify_q8(const float* q, int n_rows, int n_q_heads, const kvq8_cache* 
                    int q_pos0, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
                    int n_split, kvq8_stream_t stream);
 
+/* Partials attn_verify_q8_partials writes for this shape (its resolved n_split; 0 = invalid). */
+int attn_verify_q8_partials_count(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_kv_heads,
+                                  int n_split);
+
+/*
+ * attn_verify_q8_partials -- the split-context scan of attn_verify_q8 without the merge: the
+ * per-slice partials of the window rows over cache positions [0, kv_len).
+ *   q_pos0   : position of row 0 in this cache's coordinates; row i sees positions <= q_pos0 + i.
+ *              It may be negative (down to -2^30): a rank holding a later context slice in a
+ *              cache of its own passes q_pos0 - (its slice's first key), and rows that see
+ *              none of its keys get empty partials.
+ *   part_o   : fp32 [n][n_rows * n_q_heads][head_dim], n = attn_verify_q8_partials_count(...)
+ *   part_ml  : fp32 [n][n_rows * n_q_heads][2]
+ *   The layout attn_combine takes: per slice and row, o = sum exp(s_n - m) v_n (unnormalised),
+ *   m = max s_n in natural-log units (-inf when the row sees no key of the slice, o = 0 and
+ *   l = 0 then) and l = sum exp(s_n - m).
+ * Concatenating the partials of several calls (other ranks' slices of one context, in any
+ * order) and passing them to attn_combine gives the attention over the union of the
+ * slices.  Other arguments and errors as for attn_verify_q8; no workspace is used.
+ * Source: "perf(gfx1100): share Q8 KV scans across verifier rows", Summary: the partials
+ * layout and the reducer are kept; here they are the exchange of a context-sharded verify.
+ */
+int attn_verify_q8_partials(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv, int kv_len,
+                            int q_pos0, float softmax_scale, float* part_o, float* part_ml, int n_split,
+                            kvq8_stream_t stream);
+
 /* Bytes of workspace attn_verify_append_q8 needs (kv_len = q_pos0 + n_rows; n_split as there). */
 size_t attn_verify_append_q8_workspace_bytes(int n_rows, int n_q_heads, int head_dim, int q_pos0,
                                              int n_kv_heads, int n_split);

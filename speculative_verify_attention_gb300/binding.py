@@ -28,7 +28,8 @@ KVQ8_ERR_CUDA = 5
 
 # Entry points declared in include/kvq8attn.h.
 EXPORTED = ("kvq8_quantize", "kvq8_append", "attn_verify_q8_workspace_bytes", "attn_verify_q8", "attn_verify_tree_q8",
-            "attn_verify_append_q8_workspace_bytes", "attn_verify_append_q8", "attn_combine",
+            "attn_verify_append_q8_workspace_bytes", "attn_verify_append_q8", "attn_verify_q8_partials_count",
+            "attn_verify_q8_partials", "attn_combine",
             "attn_prompt_q8_workspace_bytes", "attn_prompt_q8", "attn_verify_q8_noalloc", "kvq8_device_error", "kvq8_status_str",
             "argmax_rows_top_prob_workspace_bytes", "argmax_rows_top_prob")
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
@@ -72,6 +73,10 @@ def load_library():
         lib.attn_verify_q8.restype = i32
         lib.attn_verify_tree_q8.argtypes = [vp, i32, i32, cp, i32, i32, vp, f32, vp, vp, sz, i32, vp]
         lib.attn_verify_tree_q8.restype = i32
+        lib.attn_verify_q8_partials_count.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.attn_verify_q8_partials_count.restype = i32
+        lib.attn_verify_q8_partials.argtypes = [vp, i32, i32, cp, i32, i32, f32, vp, vp, i32, vp]
+        lib.attn_verify_q8_partials.restype = i32
         lib.attn_verify_append_q8_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.attn_verify_append_q8_workspace_bytes.restype = sz
         lib.attn_verify_append_q8.argtypes = [vp, vp, vp, i32, i32, cp, i32, f32, vp, vp, sz, i32, vp]
@@ -226,6 +231,39 @@ def attn_verify_tree_q8(q: torch.Tensor, cache: KVCacheQ8, kv_len: int, q_pos0: 
                                             int(n_split), _stream(stream))
     _check("attn_verify_tree_q8", st)
     return out
+
+
+def attn_verify_q8_partials_count(n_rows: int, n_q_heads: int, head_dim: int, kv_len: int, n_kv_heads: int,
+                                  n_split: int = 0) -> int:
+    return int(load_library().attn_verify_q8_partials_count(n_rows, n_q_heads, head_dim, kv_len, n_kv_heads,
+                                                            n_split))
+
+
+def attn_verify_q8_partials(q: torch.Tensor, cache: KVCacheQ8, kv_len: int, q_pos0: int, softmax_scale: float,
+                            n_split: int = 0, part_o: torch.Tensor | None = None,
+                            part_ml: torch.Tensor | None = None, stream=None):
+    """Per-slice partials of verify attention of fp32 q [T][Hq][hd] over cache positions
+    [0, kv_len), row i seeing positions <= q_pos0 + i (q_pos0 may be negative).  Returns
+    (part_o fp32 [n][T*Hq][hd], part_ml fp32 [n][T*Hq][2]) in attn_combine's layout."""
+    _need(q, "q", torch.float32)
+    n_rows, n_q_heads, head_dim = q.shape
+    n = attn_verify_q8_partials_count(n_rows, n_q_heads, head_dim, kv_len, cache.n_kv_heads, n_split)
+    if n <= 0:
+        raise KVQ8Error("attn_verify_q8_partials_count", KVQ8_ERR_INVALID_ARG)
+    rows = n_rows * n_q_heads
+    if part_o is None:
+        part_o = torch.empty((n, rows, head_dim), dtype=torch.float32, device=q.device)
+    if part_ml is None:
+        part_ml = torch.empty((n, rows, 2), dtype=torch.float32, device=q.device)
+    _need(part_o, "part_o", torch.float32)
+    _need(part_ml, "part_ml", torch.float32)
+    if part_o.shape != (n, rows, head_dim) or part_ml.shape != (n, rows, 2):
+        raise ValueError(f"part_o / part_ml must be [{n}][{rows}][{head_dim}] / [{n}][{rows}][2]")
+    st = load_library().attn_verify_q8_partials(_ptr(q), n_rows, n_q_heads, ctypes.byref(cache.struct()), int(kv_len),
+                                                int(q_pos0), float(softmax_scale), _ptr(part_o), _ptr(part_ml),
+                                                int(n_split), _stream(stream))
+    _check("attn_verify_q8_partials", st)
+    return part_o, part_ml
 
 
 def attn_verify_append_q8_workspace_bytes(n_rows: int, n_q_heads: int, head_dim: int, q_pos0: int,

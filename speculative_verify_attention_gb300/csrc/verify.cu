@@ -736,13 +736,18 @@ namespace {
 
 // k_new / v_new (append-and-verify): the n_rows window tokens (kv_len must be q_pos0 + n_rows)
 // get a slice of their own, whose blocks quantise them into their tiles and into the cache.
+// part_o / part_ml (the partials entry point): the slices' partials go there, q_pos0 may be
+// negative, and no combine runs; out and the workspace are unused.
 int verify_impl(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv, int kv_len, int q_pos0,
                 const uint32_t* wmask, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
-                int n_split, kvq8_stream_t stream, const float* k_new = nullptr, const float* v_new = nullptr) {
+                int n_split, kvq8_stream_t stream, const float* k_new = nullptr, const float* v_new = nullptr,
+                float* part_o = nullptr, float* part_ml = nullptr) {
     const bool append = k_new != nullptr;
-    if (!kv || !q || !out) return KVQ8_ERR_INVALID_ARG;
+    const bool partials = part_o != nullptr;
+    if (!kv || !q || (!out && !partials) || (partials && !part_ml)) return KVQ8_ERR_INVALID_ARG;
     if (!kv->k_codes || !kv->k_scales || !kv->v_codes || !kv->v_scales) return KVQ8_ERR_INVALID_ARG;
-    if (kv->n_kv_heads < 1 || kv->capacity < 1 || q_pos0 < 0) return KVQ8_ERR_INVALID_ARG;
+    if (kv->n_kv_heads < 1 || kv->capacity < 1) return KVQ8_ERR_INVALID_ARG;
+    if (partials ? q_pos0 < -(1 << 30) : q_pos0 < 0) return KVQ8_ERR_INVALID_ARG;
     if (kv_len > kv->capacity) return KVQ8_ERR_INVALID_ARG;
     if (!(softmax_scale == softmax_scale) || softmax_scale == INFINITY || softmax_scale == -INFINITY)
         return KVQ8_ERR_INVALID_ARG;
@@ -751,12 +756,17 @@ int verify_impl(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv,
     const int rc = make_plan(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, n_split, &pl,
                              append ? n_rows : 0);
     if (rc != KVQ8_OK) return rc;
-    if (!aligned16(q) || !aligned16(out) || !aligned16(kv->k_codes) || !aligned16(kv->k_scales) ||
-        !aligned16(kv->v_codes) || !aligned16(kv->v_scales))
+    if (!aligned16(q) || !aligned16(kv->k_codes) || !aligned16(kv->k_scales) || !aligned16(kv->v_codes) ||
+        !aligned16(kv->v_scales))
         return KVQ8_ERR_MISALIGNED;
     if (append && (!aligned16(k_new) || !aligned16(v_new))) return KVQ8_ERR_MISALIGNED;
-    if (!workspace || workspace_bytes < pl.ws_bytes) return KVQ8_ERR_WORKSPACE;
-    if (!aligned16(workspace)) return KVQ8_ERR_MISALIGNED;
+    if (partials) {
+        if (!aligned16(part_o) || !aligned16(part_ml)) return KVQ8_ERR_MISALIGNED;
+    } else {
+        if (!aligned16(out)) return KVQ8_ERR_MISALIGNED;
+        if (!workspace || workspace_bytes < pl.ws_bytes) return KVQ8_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return KVQ8_ERR_MISALIGNED;
+    }
 
     VerifyParams vp;
     vp.q = q;
@@ -766,8 +776,9 @@ int verify_impl(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv,
     vp.v_scales = kv->v_scales;
     const size_t rows_total = (size_t)n_rows * n_q_heads;
     const size_t o_bytes = (size_t)pl.n_split * rows_total * kv->head_dim * sizeof(float);
-    vp.part_o = static_cast<float*>(workspace);
-    vp.part_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + ((o_bytes + 255) / 256) * 256);
+    vp.part_o = partials ? part_o : static_cast<float*>(workspace);
+    vp.part_ml = partials ? reinterpret_cast<float2*>(part_ml)
+                          : reinterpret_cast<float2*>(static_cast<char*>(workspace) + ((o_bytes + 255) / 256) * 256);
     vp.n_rows = n_rows;
     vp.n_q_heads = n_q_heads;
     vp.group = n_q_heads / kv->n_kv_heads;
@@ -795,7 +806,7 @@ int verify_impl(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv,
     else
         r1 = pl.hd == 128 ? dispatch_nt<128, false, false>(vp, pl, kv->n_kv_heads, s)
                           : dispatch_nt<256, false, false>(vp, pl, kv->n_kv_heads, s);
-    if (r1 != KVQ8_OK) return r1;
+    if (r1 != KVQ8_OK || partials) return r1;
     return launch_combine(vp.part_o, reinterpret_cast<const float*>(vp.part_ml), pl.n_split, (int)rows_total,
                           kv->head_dim, out, s);
 }
@@ -808,6 +819,21 @@ extern "C" int attn_verify_q8(const float* q, int n_rows, int n_q_heads, const k
                               int n_split, kvq8_stream_t stream) {
     return kvq8::verify_impl(q, n_rows, n_q_heads, kv, kv_len, q_pos0, nullptr, softmax_scale, out, workspace,
                              workspace_bytes, n_split, stream);
+}
+
+extern "C" int attn_verify_q8_partials_count(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_kv_heads,
+                                             int n_split) {
+    kvq8::Plan pl;
+    if (kvq8::make_plan(n_rows, n_q_heads, head_dim, kv_len, n_kv_heads, n_split, &pl) != KVQ8_OK) return 0;
+    return pl.n_split;
+}
+
+extern "C" int attn_verify_q8_partials(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv, int kv_len,
+                                       int q_pos0, float softmax_scale, float* part_o, float* part_ml, int n_split,
+                                       kvq8_stream_t stream) {
+    if (!part_o || !part_ml) return KVQ8_ERR_INVALID_ARG;
+    return kvq8::verify_impl(q, n_rows, n_q_heads, kv, kv_len, q_pos0, nullptr, softmax_scale, nullptr, nullptr, 0,
+                             n_split, stream, nullptr, nullptr, part_o, part_ml);
 }
 
 extern "C" size_t attn_verify_append_q8_workspace_bytes(int n_rows, int n_q_heads, int head_dim, int q_pos0,

@@ -11,7 +11,8 @@ Two ways to use N GPUs, both built from the single-GPU entry points:
   Summary: split-context partials and their reducer).
 
 Everything here is plain torch.distributed (NCCL between GPUs, gloo on CPU); the tests run
-the context-slice exchange with two gloo ranks.
+the context-slice exchange with two gloo ranks, and the per-rank kernel
+(attn_verify_q8_partials) as virtual ranks on one GPU.
 """
 from __future__ import annotations
 
@@ -67,3 +68,45 @@ def allgather_partials(part_o: torch.Tensor, part_ml: torch.Tensor) -> tuple[tor
     dist.all_gather(os_, part_o.contiguous())
     dist.all_gather(ms_, part_ml.contiguous())
     return torch.cat(os_, dim=0), torch.cat(ms_, dim=0)
+
+
+def empty_partials(n: int, rows: int, head_dim: int, device=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """n partials that hold no key (o = 0, m = -inf, l = 0): the merge skips them."""
+    po = torch.zeros((n, rows, head_dim), dtype=torch.float32, device=device)
+    pml = torch.zeros((n, rows, 2), dtype=torch.float32, device=device)
+    pml[..., 0] = -float("inf")
+    return po, pml
+
+
+def combine_sharded(part_o: torch.Tensor, part_ml: torch.Tensor, combine) -> torch.Tensor:
+    """The exchange step of a context-sharded verify: pad this rank's partials to the largest
+    count over the ranks with empty ones (all_gather wants equal shapes), gather them all and
+    merge with `combine(part_o, part_ml) -> out [rows][hd]` (attn_combine on GPUs)."""
+    n = part_o.shape[0]
+    dist_on = dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1
+    if dist_on:
+        t = torch.tensor([n], dtype=torch.int64, device=part_o.device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        n_max = int(t.item())
+        if n_max > n:
+            eo, eml = empty_partials(n_max - n, part_o.shape[1], part_o.shape[2], part_o.device)
+            part_o = torch.cat([part_o, eo], dim=0)
+            part_ml = torch.cat([part_ml, eml], dim=0)
+    go, gml = allgather_partials(part_o, part_ml)
+    return combine(go, gml)
+
+
+def verify_context_sharded(q: torch.Tensor, cache, kv_len: int, q_pos0: int, softmax_scale: float,
+                           n_split: int = 0) -> torch.Tensor:
+    """Verify attention with the context cut across ranks.  `cache` holds this rank's keys
+    (positions [0, kv_len) of it are global keys [first, first + kv_len)) and `q_pos0` is the
+    window's first position minus `first` (negative for a rank whose keys all come after it).
+    Every rank gets the full output fp32 [T][Hq][hd]."""
+    from .binding import attn_combine, attn_verify_q8_partials
+    T, n_q_heads, head_dim = q.shape
+    if kv_len > 0:
+        po, pml = attn_verify_q8_partials(q, cache, kv_len, q_pos0, softmax_scale, n_split)
+    else:
+        po, pml = empty_partials(1, T * n_q_heads, head_dim, q.device)
+    out = combine_sharded(po, pml, attn_combine)
+    return out.reshape(T, n_q_heads, head_dim)

@@ -2,8 +2,8 @@
 
 * max_over_ranks / barrier behave as the benchmark's timing reduction needs.
 * Context-slice sharding: each rank computes the partials of its key range (with the fp64
-  oracle standing in for the per-rank kernel), the partials are all-gathered, and the
-  log-sum-exp merge of the gathered partials equals unsharded attention."""
+  oracle standing in for the per-rank kernel), combine_sharded pads them to a common count,
+  all-gathers them, and the log-sum-exp merge equals unsharded attention."""
 import os
 import socket
 
@@ -33,18 +33,27 @@ def _worker(rank, world, port, results):
         # timing reduction
         m = multigpu.max_over_ranks(float(rank + 1))
         multigpu.barrier()
-        # context-slice sharding of one verify problem
+        # context-slice sharding of one verify problem: rank r's partials of its key range
+        # (the oracle standing in for the per-rank kernel; rank 0 cuts its range in two, so
+        # the counts differ and combine_sharded pads), then the exchange and the merge
         inp = workloads.random_small(77, 6, 2, 128, 700, 4)
         c = oracle.Cache(2, 128, 700)
         c.append(inp.k, inp.v, 0)
         b, e = multigpu.context_slices(700, world, align=128)[rank]
-        o, ml_m, ml_l = oracle.attention_partial(c, inp.q, 700, 696, 0.09, b, e)
-        part_o = torch.from_numpy(o.reshape(1, -1, 128))
-        part_ml = torch.from_numpy(np.stack([ml_m.reshape(1, -1), ml_l.reshape(1, -1)], axis=-1))
-        go, gml = multigpu.allgather_partials(part_o, part_ml)
-        out = oracle.combine(go.numpy(), gml[..., 0].numpy(), gml[..., 1].numpy())
+        cuts = [b, (b + e) // 2, e] if rank == 0 else [b, e]
+        parts = [oracle.attention_partial(c, inp.q, 700, 696, 0.09, x, y) for x, y in zip(cuts[:-1], cuts[1:])]
+        part_o = torch.from_numpy(np.stack([p[0].reshape(-1, 128) for p in parts]))
+        part_ml = torch.from_numpy(np.stack([np.stack([p[1].reshape(-1), p[2].reshape(-1)], axis=-1)
+                                             for p in parts]))
+        shapes = []
+
+        def merge(go, gml):
+            shapes.append(tuple(go.shape))
+            return oracle.combine(go.numpy(), gml[..., 0].numpy(), gml[..., 1].numpy())
+
+        out = multigpu.combine_sharded(part_o, part_ml, merge)
         ref = oracle.attention(c, inp.q, 700, 696, 0.09).reshape(-1, 128)
-        results[rank] = (m, float(np.max(np.abs(out - ref))), tuple(go.shape))
+        results[rank] = (m, float(np.max(np.abs(out - ref))), shapes[0])
     finally:
         dist.destroy_process_group()
 
@@ -65,7 +74,7 @@ def test_two_gloo_ranks_reduce_and_merge_context_slices():
             m, err, shape = results[r]
             assert m == 2.0
             assert err < 1e-12
-            assert shape == (2, 24, 128)
+            assert shape == (4, 24, 128)   # 2 ranks x 2 partials (rank 1 padded with an empty one)
 
 
 def test_context_slices_cover_the_context_in_whole_tiles():
