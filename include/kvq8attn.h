@@ -171,6 +171,26 @@ int attn_verify_append_q8(const float* q, const float* k_new, const float* v_new
                           float* out, void* workspace, size_t workspace_bytes, int n_split,
                           kvq8_stream_t stream);
 
+/* Device scratch attn_verify_append_q8_host needs (inputs, output and the verify workspace). */
+size_t attn_verify_append_q8_host_scratch_bytes(int n_rows, int n_q_heads, int head_dim, int q_pos0,
+                                                int n_kv_heads, int n_split);
+
+/*
+ * attn_verify_append_q8_host -- attn_verify_append_q8 from and to HOST buffers: the one entry
+ * point that touches host memory.
+ *   h_in   : host fp32, q [n_rows][n_q_heads][head_dim] followed by k_new and v_new
+ *            [n_rows][n_kv_heads][head_dim] each (pinned memory keeps the copy asynchronous)
+ *   h_out  : host fp32 [n_rows][n_q_heads][head_dim]
+ *   d_scratch : device, 16-byte aligned, attn_verify_append_q8_host_scratch_bytes(...) bytes
+ * One host-to-device copy of h_in, the two kernels of attn_verify_append_q8, one
+ * device-to-host copy into h_out, all queued on `stream`; h_out is valid once the stream has
+ * reached that point (the call itself does not synchronise).  Errors as for
+ * attn_verify_append_q8, WORKSPACE for a short scratch; nothing is queued on error.
+ */
+int attn_verify_append_q8_host(const float* h_in, int n_rows, int n_q_heads, const kvq8_cache* kv,
+                               int q_pos0, float softmax_scale, float* h_out, void* d_scratch,
+                               size_t scratch_bytes, int n_split, kvq8_stream_t stream);
+
 /*
  * attn_verify_tree_q8 -- attn_verify_q8 for a tree-shaped verify window.
  *   window_mask : device uint32 [n_rows], 4-byte aligned: row i sees every key n < q_pos0

@@ -29,7 +29,8 @@ KVQ8_ERR_CUDA = 5
 # Entry points declared in include/kvq8attn.h.
 EXPORTED = ("kvq8_quantize", "kvq8_append", "attn_verify_q8_workspace_bytes", "attn_verify_q8", "attn_verify_tree_q8",
             "attn_verify_append_q8_workspace_bytes", "attn_verify_append_q8", "attn_verify_q8_partials_count",
-            "attn_verify_q8_partials", "attn_combine",
+            "attn_verify_q8_partials", "attn_verify_append_q8_host_scratch_bytes", "attn_verify_append_q8_host",
+            "attn_combine",
             "attn_prompt_q8_workspace_bytes", "attn_prompt_q8", "attn_verify_q8_noalloc", "kvq8_device_error", "kvq8_status_str",
             "argmax_rows_top_prob_workspace_bytes", "argmax_rows_top_prob")
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
@@ -77,6 +78,10 @@ def load_library():
         lib.attn_verify_q8_partials_count.restype = i32
         lib.attn_verify_q8_partials.argtypes = [vp, i32, i32, cp, i32, i32, f32, vp, vp, i32, vp]
         lib.attn_verify_q8_partials.restype = i32
+        lib.attn_verify_append_q8_host_scratch_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.attn_verify_append_q8_host_scratch_bytes.restype = sz
+        lib.attn_verify_append_q8_host.argtypes = [vp, i32, i32, cp, i32, f32, vp, vp, sz, i32, vp]
+        lib.attn_verify_append_q8_host.restype = i32
         lib.attn_verify_append_q8_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.attn_verify_append_q8_workspace_bytes.restype = sz
         lib.attn_verify_append_q8.argtypes = [vp, vp, vp, i32, i32, cp, i32, f32, vp, vp, sz, i32, vp]
@@ -297,6 +302,63 @@ def attn_verify_append_q8(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Ten
                                               int(n_split), _stream(stream))
     _check("attn_verify_append_q8", st)
     return out
+
+
+def attn_verify_append_q8_host_scratch_bytes(n_rows: int, n_q_heads: int, head_dim: int, q_pos0: int,
+                                             n_kv_heads: int, n_split: int = 0) -> int:
+    return int(load_library().attn_verify_append_q8_host_scratch_bytes(n_rows, n_q_heads, head_dim, q_pos0,
+                                                                       n_kv_heads, n_split))
+
+
+def attn_verify_append_q8_host(h_in: torch.Tensor, n_rows: int, n_q_heads: int, cache: KVCacheQ8, q_pos0: int,
+                               softmax_scale: float, h_out: torch.Tensor, scratch: torch.Tensor, n_split: int = 0,
+                               stream=None) -> None:
+    """attn_verify_append_q8 from and to host tensors: h_in (CPU fp32, pinned for an async copy)
+    holds q [T][Hq][hd] then k_new and v_new [T][Hkv][hd]; h_out (CPU fp32 [T][Hq][hd]) is
+    written once the stream gets there.  scratch: device bytes from the scratch-size query."""
+    for t, name in ((h_in, "h_in"), (h_out, "h_out")):
+        if t.device.type != "cpu" or t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU float32 tensor")
+    hd, hkv = cache.head_dim, cache.n_kv_heads
+    if h_in.numel() != n_rows * (n_q_heads + 2 * hkv) * hd or h_out.numel() != n_rows * n_q_heads * hd:
+        raise ValueError("h_in / h_out sizes do not match the shape")
+    if scratch.device.type != "cuda" or not scratch.is_contiguous():
+        raise ValueError("scratch must be a contiguous device tensor")
+    st = load_library().attn_verify_append_q8_host(h_in.data_ptr(), n_rows, n_q_heads, ctypes.byref(cache.struct()),
+                                                   int(q_pos0), float(softmax_scale), h_out.data_ptr(),
+                                                   _ptr(scratch), scratch.numel() * scratch.element_size(),
+                                                   int(n_split), _stream(stream))
+    _check("attn_verify_append_q8_host", st)
+
+
+class PreparedAppendVerifyHost:
+    """attn_verify_append_q8_host with its arguments marshalled once, for a loop that repeats
+    one call (same buffers, cache and window position): calling it is one C-ABI call.  The
+    tensors must stay alive and in place while the object is used."""
+
+    def __init__(self, h_in: torch.Tensor, n_rows: int, n_q_heads: int, cache: KVCacheQ8, q_pos0: int,
+                 softmax_scale: float, h_out: torch.Tensor, scratch: torch.Tensor, n_split: int = 0, stream=None):
+        for t, name in ((h_in, "h_in"), (h_out, "h_out")):
+            if t.device.type != "cpu" or t.dtype != torch.float32 or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous CPU float32 tensor")
+        hd, hkv = cache.head_dim, cache.n_kv_heads
+        if h_in.numel() != n_rows * (n_q_heads + 2 * hkv) * hd or h_out.numel() != n_rows * n_q_heads * hd:
+            raise ValueError("h_in / h_out sizes do not match the shape")
+        if scratch.device.type != "cuda" or not scratch.is_contiguous():
+            raise ValueError("scratch must be a contiguous device tensor")
+        self._keep = (h_in, h_out, scratch, cache)
+        self._struct = cache.struct()
+        self._fn = load_library().attn_verify_append_q8_host
+        self._args = (ctypes.c_void_p(h_in.data_ptr()), ctypes.c_int(n_rows), ctypes.c_int(n_q_heads),
+                      ctypes.byref(self._struct), ctypes.c_int(int(q_pos0)), ctypes.c_float(float(softmax_scale)),
+                      ctypes.c_void_p(h_out.data_ptr()), _ptr(scratch),
+                      ctypes.c_size_t(scratch.numel() * scratch.element_size()), ctypes.c_int(int(n_split)),
+                      _stream(stream))
+
+    def __call__(self) -> None:
+        st = self._fn(*self._args)
+        if st != KVQ8_OK:
+            raise KVQ8Error("attn_verify_append_q8_host", st)
 
 
 def argmax_rows_top_prob(logits: torch.Tensor, workspace: torch.Tensor | None = None, argmax=None, top_prob=None,

@@ -645,10 +645,16 @@ struct Plan {
     size_t ws_bytes;
 };
 
+// SM count of the current device, looked up once per device (concurrent first lookups store
+// the same value).
 int sm_count() {
+    constexpr int kMaxDev = 64;
+    static int cached[kMaxDev] = {};
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDev && cached[dev] > 0) return cached[dev];
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDev) cached[dev] = n;
     return n;
 }
 
@@ -852,6 +858,68 @@ extern "C" int attn_verify_append_q8(const float* q, const float* k_new, const f
     if (!k_new || !v_new || q_pos0 < 0) return KVQ8_ERR_INVALID_ARG;
     return kvq8::verify_impl(q, n_rows, n_q_heads, kv, q_pos0 + n_rows, q_pos0, nullptr, softmax_scale, out,
                              workspace, workspace_bytes, n_split, stream, k_new, v_new);
+}
+
+namespace {
+// Scratch of the host-buffer entry: [q | k_new | v_new] fp32, out fp32, then the verify
+// workspace, each part starting on a 256-byte boundary.
+struct HostScratch {
+    size_t in_bytes, out_off, ws_off, ws_bytes, total;
+};
+inline size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+bool host_scratch(int n_rows, int n_q_heads, int head_dim, int q_pos0, int n_kv_heads, int n_split, HostScratch* h) {
+    kvq8::Plan pl;
+    if (q_pos0 < 0 || kvq8::make_plan(n_rows, n_q_heads, head_dim, q_pos0 + n_rows, n_kv_heads, n_split, &pl,
+                                      n_rows) != KVQ8_OK)
+        return false;
+    const size_t q_bytes = (size_t)n_rows * n_q_heads * head_dim * sizeof(float);
+    const size_t kv_bytes = (size_t)n_rows * n_kv_heads * head_dim * sizeof(float);
+    h->in_bytes = q_bytes + 2 * kv_bytes;
+    h->out_off = round256(h->in_bytes);
+    h->ws_off = h->out_off + round256(q_bytes);
+    h->ws_bytes = pl.ws_bytes;
+    h->total = h->ws_off + pl.ws_bytes;
+    return true;
+}
+}  // namespace
+
+extern "C" size_t attn_verify_append_q8_host_scratch_bytes(int n_rows, int n_q_heads, int head_dim, int q_pos0,
+                                                           int n_kv_heads, int n_split) {
+    HostScratch h;
+    return host_scratch(n_rows, n_q_heads, head_dim, q_pos0, n_kv_heads, n_split, &h) ? h.total : 0;
+}
+
+extern "C" int attn_verify_append_q8_host(const float* h_in, int n_rows, int n_q_heads, const kvq8_cache* kv,
+                                          int q_pos0, float softmax_scale, float* h_out, void* d_scratch,
+                                          size_t scratch_bytes, int n_split, kvq8_stream_t stream) {
+    if (!h_in || !h_out || !kv || q_pos0 < 0) return KVQ8_ERR_INVALID_ARG;
+    HostScratch h;
+    if (!host_scratch(n_rows, n_q_heads, kv->head_dim, q_pos0, kv->n_kv_heads, n_split, &h))
+        return n_rows < 1 || n_rows > 32 || n_q_heads < 1 || kv->n_kv_heads < 1 ? KVQ8_ERR_INVALID_ARG
+                                                                                  : KVQ8_ERR_UNSUPPORTED;
+    if (!d_scratch || scratch_bytes < h.total) return KVQ8_ERR_WORKSPACE;
+    if (!kvq8::aligned16(d_scratch)) return KVQ8_ERR_MISALIGNED;
+    if (q_pos0 + n_rows > kv->capacity) return KVQ8_ERR_INVALID_ARG;
+    // everything verify_impl checks past the shapes, before the input copy is queued
+    if (!kv->k_codes || !kv->k_scales || !kv->v_codes || !kv->v_scales) return KVQ8_ERR_INVALID_ARG;
+    if (!(softmax_scale == softmax_scale) || softmax_scale == INFINITY || softmax_scale == -INFINITY)
+        return KVQ8_ERR_INVALID_ARG;
+    if (!kvq8::aligned16(kv->k_codes) || !kvq8::aligned16(kv->k_scales) || !kvq8::aligned16(kv->v_codes) ||
+        !kvq8::aligned16(kv->v_scales))
+        return KVQ8_ERR_MISALIGNED;
+    char* base = static_cast<char*>(d_scratch);
+    const float* q = reinterpret_cast<const float*>(base);
+    const float* k_new = q + (size_t)n_rows * n_q_heads * kv->head_dim;
+    const float* v_new = k_new + (size_t)n_rows * kv->n_kv_heads * kv->head_dim;
+    float* out = reinterpret_cast<float*>(base + h.out_off);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(base, h_in, h.in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return KVQ8_ERR_CUDA;
+    const int rc = kvq8::verify_impl(q, n_rows, n_q_heads, kv, q_pos0 + n_rows, q_pos0, nullptr, softmax_scale, out,
+                                     base + h.ws_off, h.ws_bytes, n_split, stream, k_new, v_new);
+    if (rc != KVQ8_OK) return rc;
+    const size_t out_bytes = (size_t)n_rows * n_q_heads * kv->head_dim * sizeof(float);
+    return cudaMemcpyAsync(h_out, out, out_bytes, cudaMemcpyDeviceToHost, s) == cudaSuccess ? KVQ8_OK
+                                                                                              : KVQ8_ERR_CUDA;
 }
 
 extern "C" int attn_verify_tree_q8(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv, int kv_len,

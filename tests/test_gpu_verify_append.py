@@ -142,3 +142,58 @@ def test_append_verify_rejects_bad_arguments(lib):
     assert call(k=kn.data_ptr() + 4) == KVQ8_ERR_MISALIGNED
     assert call(wsb=nb - 1) == KVQ8_ERR_WORKSPACE
     torch.cuda.synchronize()
+
+
+def test_host_buffer_entry_matches_device_entry(lib):
+    """attn_verify_append_q8_host (pinned host in/out, one copy each way) gives the device
+    entry's output bit for bit and the same cache bytes."""
+    import torch
+
+    from speculative_verify_attention_gb300 import (attn_verify_append_q8, attn_verify_append_q8_host,
+                                                    attn_verify_append_q8_host_scratch_bytes)
+    w = workloads.verify_27b(4)
+    inp = workloads.make_inputs(w)
+    T, ctx = w.n_q, w.q_pos0
+    g1, _ = build_caches(_context_only(inp, ctx), capacity=w.kv_len)
+    g2, _ = build_caches(_context_only(inp, ctx), capacity=w.kv_len)
+    kn, vn = inp.k[ctx:ctx + T], inp.v[ctx:ctx + T]
+    h_in = torch.from_numpy(np.concatenate([inp.q.ravel(), kn.ravel(), vn.ravel()]).astype(np.float32)).pin_memory()
+    h_out = torch.empty(inp.q.size, dtype=torch.float32).pin_memory()
+    scratch = torch.empty(attn_verify_append_q8_host_scratch_bytes(T, 24, 256, ctx, 4), dtype=torch.uint8,
+                          device="cuda")
+    attn_verify_append_q8_host(h_in, T, 24, g1, ctx, w.softmax_scale, h_out, scratch)
+    ref = attn_verify_append_q8(torch.from_numpy(inp.q).cuda(), torch.from_numpy(np.ascontiguousarray(kn)).cuda(),
+                                torch.from_numpy(np.ascontiguousarray(vn)).cuda(), g2, ctx, w.softmax_scale)
+    torch.cuda.synchronize()
+    assert torch.equal(h_out.reshape(ref.shape), ref.cpu())
+    for a, b in ((g1.k_codes, g2.k_codes), (g1.v_codes, g2.v_codes), (g1.k_scales, g2.k_scales),
+                 (g1.v_scales, g2.v_scales)):
+        assert torch.equal(a, b)
+    from speculative_verify_attention_gb300.binding import KVQ8Error
+    with pytest.raises(KVQ8Error):
+        attn_verify_append_q8_host(h_in, T, 24, g1, ctx, w.softmax_scale, h_out, scratch[:-16])
+
+
+def test_prepared_host_call_repeats_the_call(lib):
+    """PreparedAppendVerifyHost: the same output as the one-off host call, over repeated use."""
+    import torch
+
+    from speculative_verify_attention_gb300 import (PreparedAppendVerifyHost, attn_verify_append_q8_host,
+                                                    attn_verify_append_q8_host_scratch_bytes)
+    inp = workloads.random_small(981, 8, 2, 128, 300, 6)
+    ctx, T = 294, 6
+    g1, _ = build_caches(_context_only(inp, ctx), capacity=300)
+    g2, _ = build_caches(_context_only(inp, ctx), capacity=300)
+    h_in = torch.from_numpy(np.concatenate([inp.q.ravel(), inp.k[ctx:].ravel(), inp.v[ctx:].ravel()])
+                            .astype(np.float32)).pin_memory()
+    o1 = torch.empty(inp.q.size, dtype=torch.float32).pin_memory()
+    o2 = torch.empty(inp.q.size, dtype=torch.float32).pin_memory()
+    nb = attn_verify_append_q8_host_scratch_bytes(T, 8, 128, ctx, 2)
+    s1 = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    s2 = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    call = PreparedAppendVerifyHost(h_in, T, 8, g1, ctx, 0.088, o1, s1)
+    for _ in range(3):
+        call()
+    attn_verify_append_q8_host(h_in, T, 8, g2, ctx, 0.088, o2, s2)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
