@@ -372,8 +372,12 @@ def run_native(args, world, rank, local):
             n_pairs = 24
             cpu_steps = 6
             g_, sec_, thr_, desc_ = oracle_verify_sample(n_pairs, cpu_steps, 1)
+            g1, _, _, _ = oracle_verify_sample(4, 2, 0, threads=1)   # the one-thread figure
+            import oracle
+            oracle.set_threads(thr_)
             cpu = {"value": g_, "unit": "GB/s", "cores": thr_, "kind": "oracle",
-                   "sample": desc_ + f"; {cpu_steps} steps timed"}
+                   "sample": desc_ + f"; {cpu_steps} steps timed", "value_1thread": g1,
+                   "sample_1thread": "4 pairs per step, 2 steps, one OpenMP thread"}
         bytes_per_launch = kv_bytes_step / len(VERIFY_T)
         achieved = bytes_per_launch / (us_per_call_verify * 1e-6) / 1e9
         result = {
@@ -521,9 +525,10 @@ def binary_tree_mask(T: int) -> np.ndarray:
 
 
 def time_verify_cell(w, ring, dev, reps=10, tree_mask=None):
-    """Median-free device time per attn_verify_q8 call (attn_verify_tree_q8 when a window mask
-    is given): a CUDA graph of calls walking the ring (total size > 4x L2) replayed `reps`
-    times; returns microseconds per call."""
+    """Device time per attn_verify_q8 call (attn_verify_tree_q8 when a window mask is given):
+    a CUDA graph of at least 32 calls walking the ring (total size > 4x L2, so K/V come from
+    HBM; a one-cache ring gives the warm-L2 time) is replayed `reps` times, each replay timed
+    with CUDA events; returns the median over the replays of microseconds per call."""
     import torch
 
     from speculative_verify_attention_gb300 import (attn_verify_q8, attn_verify_q8_workspace_bytes,
@@ -550,13 +555,14 @@ def time_verify_cell(w, ring, dev, reps=10, tree_mask=None):
             call(ring[i % len(ring)])
     g.replay()
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(reps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    ev[0].record()
+    for r in range(reps):
         g.replay()
-    b.record()
+        ev[r + 1].record()
     torch.cuda.synchronize()
-    return a.elapsed_time(b) * 1e3 / (reps * n_calls)
+    per = sorted(ev[r].elapsed_time(ev[r + 1]) * 1e3 / n_calls for r in range(reps))
+    return per[reps // 2]
 
 
 def sweep(args):
@@ -567,7 +573,7 @@ def sweep(args):
     import __graft_entry__
     __graft_entry__.build()
     from speculative_verify_attention_gb300 import workloads
-    hbm_peak, _, _ = _peaks()
+    hbm_peak, bf16_peak, _ = _peaks()
     dev = torch.device("cuda", 0)
     cells = [workloads.verify_27b(t) for t in workloads.VERIFY_27B_T]
     cells += [workloads.long_verify(c, t) for c in workloads.LONG_CTX for t in workloads.LONG_T]
@@ -584,11 +590,20 @@ def sweep(args):
             torch.cuda.empty_cache()
             ring = _ring_for(w, dev, args.ring_l2)
             key = (w.n_kv_heads, w.head_dim, w.kv_len)
-        us = time_verify_cell(w, ring, dev, tree_mask=binary_tree_mask(w.n_q) if kind else None)
+        mask = binary_tree_mask(w.n_q) if kind else None
+        us = time_verify_cell(w, ring, dev, tree_mask=mask)
+        us_warm = time_verify_cell(w, ring[:1], dev, tree_mask=mask)
         gbs = w.kv_bytes() / (us * 1e-6) / 1e9
+        # roofline of the cell: K/V bytes at the HBM peak, or the causal flops doubled by the
+        # fp16 hi + lo split at the dense tensor peak, whichever takes longer
+        t_hbm = w.kv_bytes() / (hbm_peak * 1e9)
+        t_tensor = 2 * w.causal_flops() / (bf16_peak * 1e12)
         print(json.dumps({"workload": f"{kind}-{w.name}" if kind else w.name, "us_per_call": us,
                           "kv_mb": w.kv_bytes() / 1e6, "kv_gbs": gbs, "hbm_frac": gbs / hbm_peak,
-                          "tflops_alg": w.causal_flops() / (us * 1e-6) / 1e12, "ring": len(ring)}), flush=True)
+                          "tflops_alg": w.causal_flops() / (us * 1e-6) / 1e12,
+                          "roofline_bound": "hbm" if t_hbm >= t_tensor else "tensor",
+                          "roofline_frac": max(t_hbm, t_tensor) / (us * 1e-6),
+                          "us_per_call_warm_l2": us_warm, "ring": len(ring)}), flush=True)
 
 
 def main():
