@@ -41,7 +41,11 @@ def build(force: bool = False) -> str:
 class _Cache(ctypes.Structure):
     _fields_ = [("k_codes", ctypes.c_void_p), ("k_scales", ctypes.c_void_p),
                 ("v_codes", ctypes.c_void_p), ("v_scales", ctypes.c_void_p),
-                ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("capacity", ctypes.c_int)]
+                ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("capacity", ctypes.c_int),
+                ("format", ctypes.c_int), ("k_f16", ctypes.c_void_p), ("v_f16", ctypes.c_void_p)]
+
+
+_Q8_0, _F16 = 0, 1
 
 
 def _load():
@@ -62,6 +66,8 @@ def _load():
             lib.oracle_quantize_q8_0.restype = None
             lib.oracle_kv_append_q8_0.argtypes = [vp, i32, i32, i32, vp, vp, i32, i32]
             lib.oracle_kv_append_q8_0.restype = i32
+            lib.oracle_kv_append_f16.argtypes = [vp, i32, i32, i32, vp, i32, i32]
+            lib.oracle_kv_append_f16.restype = i32
             lib.oracle_attention_partial.argtypes = [ctypes.POINTER(_Cache), vp, i32, i32, i32, i32, f64,
                                                      i64, i64, vp, vp, i64, vp, vp, vp]
             lib.oracle_attention_partial.restype = i32
@@ -147,7 +153,7 @@ class Cache:
 
     def _struct(self) -> _Cache:
         return _Cache(self.k_codes.ctypes.data, self.k_scales.ctypes.data, self.v_codes.ctypes.data,
-                      self.v_scales.ctypes.data, self.n_kv_heads, self.head_dim, self.capacity)
+                      self.v_scales.ctypes.data, self.n_kv_heads, self.head_dim, self.capacity, _Q8_0, None, None)
 
     def append(self, k, v, pos0: int) -> None:
         """Quantise and write K and V values [n_tok][n_kv_heads][head_dim] at positions pos0.."""
@@ -160,6 +166,42 @@ class Cache:
                                            _ptr(codes), _ptr(scales), self.capacity, int(pos0))
             if rc:
                 raise ValueError("oracle_kv_append_q8_0 rejected its arguments")
+
+
+class CacheF16:
+    """fp16 KV pool held as numpy arrays of fp16 bits (uint16), laid out like the library's
+    fp16 pool: k, v [n_kv_heads][capacity][head_dim].  Every attention function here takes
+    it in place of a Q8_0 Cache."""
+
+    def __init__(self, n_kv_heads: int, head_dim: int, capacity: int):
+        self.n_kv_heads, self.head_dim, self.capacity = n_kv_heads, head_dim, capacity
+        self.k = np.zeros((n_kv_heads, capacity, head_dim), dtype=np.uint16)
+        self.v = np.zeros((n_kv_heads, capacity, head_dim), dtype=np.uint16)
+
+    @classmethod
+    def from_planes(cls, k_bits, v_bits):
+        h, cap, hd = k_bits.shape
+        c = cls.__new__(cls)
+        c.n_kv_heads, c.head_dim, c.capacity = h, hd, cap
+        c.k = np.ascontiguousarray(k_bits, dtype=np.uint16)
+        c.v = np.ascontiguousarray(v_bits, dtype=np.uint16)
+        return c
+
+    def _struct(self) -> _Cache:
+        return _Cache(None, None, None, None, self.n_kv_heads, self.head_dim, self.capacity, _F16,
+                      self.k.ctypes.data, self.v.ctypes.data)
+
+    def append(self, k, v, pos0: int) -> None:
+        """Round K and V values [n_tok][n_kv_heads][head_dim] (fp32) to fp16 at positions pos0.."""
+        lib = _load()
+        for x, plane in ((k, self.k), (v, self.v)):
+            a = np.ascontiguousarray(x, dtype=np.float32)
+            if a.ndim != 3 or a.shape[1:] != (self.n_kv_heads, self.head_dim):
+                raise ValueError(f"bad K/V shape {a.shape}")
+            rc = lib.oracle_kv_append_f16(_ptr(a), a.shape[0], self.n_kv_heads, self.head_dim, _ptr(plane),
+                                          self.capacity, int(pos0))
+            if rc:
+                raise ValueError("oracle_kv_append_f16 rejected its arguments")
 
 
 def _sel(sel, n_q, n_q_heads):

@@ -34,6 +34,12 @@
  *    every key n < q_pos0 and the window key q_pos0 + j exactly when bit j of mask[i] is
  *    set (j < 32, n < kv_len).  The sequential window is mask[i] = 2^(i+1) - 1.
  *
+ *  - fp16 KV pools (the pages' other pool format, which their new kernels leave on the old
+ *    path: "gfx12 WMMA kernel for the int8-KV QSA prompt attention", Gating and Limits).
+ *    Reading: K and V are stored as IEEE binary16 values, [n_kv_heads][capacity][head_dim];
+ *    an append rounds the fp32 inputs to nearest even; attention is the same fp64 formula
+ *    with k[n][j] and v[n][j] the stored values (no codes, no block scales).
+ *
  *  - Split-context partials and their merge ("share Q8 KV scans across verifier
  *    rows", Summary: "The partials layout and reducer are unchanged"): a partial over
  *    keys [k0, k1) is (o, m, l) with m = max s over the visible keys of the range,
@@ -172,14 +178,40 @@ typedef struct {
     const int8_t* v_codes;
     const uint16_t* v_scales;
     int n_kv_heads, head_dim, capacity;
+    int format;              /* ORACLE_Q8_0 or ORACLE_F16 */
+    const uint16_t* k_f16;   /* ORACLE_F16: fp16 bits [n_kv_heads][capacity][head_dim] */
+    const uint16_t* v_f16;
 } oracle_cache;
 
-/* Dequantised value of element j of token n of kv head h in one plane. */
-static double deq(const int8_t* codes, const uint16_t* scales, const oracle_cache* c,
-                  int h, int64_t n, int j) {
+enum { ORACLE_Q8_0 = 0, ORACLE_F16 = 1 };
+
+/* Value of element j of token n of kv head h in one plane: code * block scale for Q8_0,
+ * the stored binary16 value for an fp16 pool. */
+static double deq_plane(const oracle_cache* c, int plane, int h, int64_t n, int j) {
     int64_t row = (int64_t)h * c->capacity + n;
+    if (c->format == ORACLE_F16)
+        return oracle_f16_bits_to_f64((plane ? c->v_f16 : c->k_f16)[row * c->head_dim + j]);
+    const int8_t* codes = plane ? c->v_codes : c->k_codes;
+    const uint16_t* scales = plane ? c->v_scales : c->k_scales;
     double d = oracle_f16_bits_to_f64(scales[row * (c->head_dim / QBLOCK) + j / QBLOCK]);
     return (double)codes[row * c->head_dim + j] * d;
+}
+#define deq_k(c, h, n, j) deq_plane((c), 0, (h), (n), (j))
+#define deq_v(c, h, n, j) deq_plane((c), 1, (h), (n), (j))
+
+/* Append n_tok fp32 tokens [n_tok][n_kv_heads][head_dim] to an fp16 plane at pos0 (round to
+ * nearest even).  Returns 0, or -1 for bad arguments. */
+int oracle_kv_append_f16(const float* x, int n_tok, int n_kv_heads, int head_dim, uint16_t* plane,
+                         int capacity, int pos0) {
+    if (!x || !plane || n_tok < 0 || n_kv_heads <= 0 || head_dim <= 0 || pos0 < 0 ||
+        (int64_t)pos0 + n_tok > capacity)
+        return -1;
+    for (int t = 0; t < n_tok; ++t)
+        for (int h = 0; h < n_kv_heads; ++h)
+            for (int j = 0; j < head_dim; ++j)
+                plane[((int64_t)h * capacity + pos0 + t) * head_dim + j] =
+                    oracle_f32_to_f16_bits(x[((int64_t)t * n_kv_heads + h) * head_dim + j]);
+    return 0;
 }
 
 /* One (query row, q head): softmax attention over keys [k0, min(k1, q_pos0+i+1)).
@@ -196,7 +228,7 @@ static void attend_one(const oracle_cache* c, const double* qrow, int kv_head, i
     double m = -INFINITY;
     for (int64_t n = k0; n < k1; ++n) {
         double s = 0.0;
-        for (int j = 0; j < hd; ++j) s += qrow[j] * deq(c->k_codes, c->k_scales, c, kv_head, n, j);
+        for (int j = 0; j < hd; ++j) s += qrow[j] * deq_k(c, kv_head, n, j);
         s *= scale;
         s_buf[n - k0] = s;
         if (s > m) m = s;
@@ -205,7 +237,7 @@ static void attend_one(const oracle_cache* c, const double* qrow, int kv_head, i
     for (int64_t n = k0; n < k1; ++n) {
         double p = exp(s_buf[n - k0] - m);
         l += p;
-        for (int j = 0; j < hd; ++j) o[j] += p * deq(c->v_codes, c->v_scales, c, kv_head, n, j);
+        for (int j = 0; j < hd; ++j) o[j] += p * deq_v(c, kv_head, n, j);
     }
     *m_out = m;
     *l_out = l;
@@ -213,6 +245,7 @@ static void attend_one(const oracle_cache* c, const double* qrow, int kv_head, i
 
 static int check_cache(const oracle_cache* c, int n_q_heads, int kv_len) {
     if (!c || c->n_kv_heads <= 0 || c->head_dim <= 0 || c->head_dim % QBLOCK) return -1;
+    if (c->format != ORACLE_Q8_0 && c->format != ORACLE_F16) return -1;
     if (n_q_heads <= 0 || n_q_heads % c->n_kv_heads) return -1;
     if (kv_len < 0 || kv_len > c->capacity) return -1;
     return 0;
@@ -284,7 +317,7 @@ static void attend_list(const oracle_cache* c, const double* qrow, int kv_head, 
     double m = -INFINITY;
     for (int64_t t = 0; t < n_keys; ++t) {
         double s = 0.0;
-        for (int j = 0; j < hd; ++j) s += qrow[j] * deq(c->k_codes, c->k_scales, c, kv_head, keys[t], j);
+        for (int j = 0; j < hd; ++j) s += qrow[j] * deq_k(c, kv_head, keys[t], j);
         s *= scale;
         s_buf[t] = s;
         if (s > m) m = s;
@@ -293,7 +326,7 @@ static void attend_list(const oracle_cache* c, const double* qrow, int kv_head, 
     for (int64_t t = 0; t < n_keys; ++t) {
         double p = exp(s_buf[t] - m);
         l += p;
-        for (int j = 0; j < hd; ++j) out[j] += p * deq(c->v_codes, c->v_scales, c, kv_head, keys[t], j);
+        for (int j = 0; j < hd; ++j) out[j] += p * deq_v(c, kv_head, keys[t], j);
     }
     for (int j = 0; j < hd; ++j) out[j] /= l;
 }
