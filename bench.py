@@ -511,6 +511,29 @@ def _ring_for(w, dev, ring_l2):
     return ring
 
 
+def _ring_f16(w, dev, ring_l2):
+    """A ring of fp16 pools holding the workload's K/V (total size above ring_l2 x L2)."""
+    import torch
+
+    from speculative_verify_attention_gb300 import KVCacheF16, workloads
+    inp = workloads.make_inputs(w)
+    base = KVCacheF16(w.n_kv_heads, w.head_dim, w.kv_len, device=dev)
+    base.append(torch.from_numpy(inp.k).to(dev), torch.from_numpy(inp.v).to(dev), 0)
+    nbytes = 2 * base.k.numel() * base.k.element_size()
+    ring = [base]
+    for _ in range(max(2, int(np.ceil(ring_l2 * L2_BYTES / nbytes))) - 1):
+        c = KVCacheF16(w.n_kv_heads, w.head_dim, w.kv_len, device=dev)
+        c.k.copy_(base.k)
+        c.v.copy_(base.v)
+        ring.append(c)
+    return ring
+
+
+def f16_kv_bytes(w) -> int:
+    """Bytes of the fp16 K and V planes read for kv_len tokens."""
+    return 2 * w.n_kv_heads * w.kv_len * w.head_dim * 2
+
+
 def binary_tree_mask(T: int) -> np.ndarray:
     """Window mask of a binary draft tree of T tokens (node i's parent is (i - 1) // 2): each row
     sees its ancestors and itself."""
@@ -531,13 +554,16 @@ def time_verify_cell(w, ring, dev, reps=10, tree_mask=None):
     with CUDA events; returns the median over the replays of microseconds per call."""
     import torch
 
-    from speculative_verify_attention_gb300 import (attn_verify_q8, attn_verify_q8_workspace_bytes,
-                                                    attn_verify_tree_q8, workloads)
+    from speculative_verify_attention_gb300 import (KVCacheF16, attn_verify_f16, attn_verify_q8,
+                                                    attn_verify_q8_workspace_bytes, attn_verify_tree_q8, workloads)
     q = torch.from_numpy(workloads.make_inputs(w, kv_len=1).q).to(dev)
     out = torch.empty_like(q)
     ws = torch.empty(attn_verify_q8_workspace_bytes(w.n_q, w.n_q_heads, w.head_dim, w.kv_len, w.n_kv_heads),
                      dtype=torch.uint8, device=dev)
-    if tree_mask is not None:
+    if isinstance(ring[0], KVCacheF16):   # fp16 pools (the same workspace size rule)
+        def call(c):
+            attn_verify_f16(q, c, w.kv_len, w.q_pos0, w.softmax_scale, out=out, workspace=ws)
+    elif tree_mask is not None:
         m = torch.from_numpy(np.ascontiguousarray(tree_mask, np.uint32).view(np.int32)).to(dev)
 
         def call(c):
@@ -580,26 +606,32 @@ def sweep(args):
     cells += [workloads.hd128_verify(t) for t in workloads.HD128_T]
     # tree-shaped windows (binary draft trees) on the 27B-class shape
     cells += [(workloads.verify_27b(t), "tree-binary") for t in (8, 16)]
+    # fp16 KV pools
+    cells += [(workloads.verify_27b(t), "f16") for t in (4, 8)]
+    cells += [(workloads.long_verify(c, t), "f16") for c in (20676, 32768) for t in (4, 8)]
+    cells += [(workloads.hd128_verify(t), "f16") for t in (4, 8)]
     cells = [c if isinstance(c, tuple) else (c, None) for c in cells]
     cells = [(w, kind) for w, kind in cells
              if not args.sweep_filter or args.sweep_filter in (f"{kind}-{w.name}" if kind else w.name)]
     key, ring = None, None
     for w, kind in cells:
-        if key != (w.n_kv_heads, w.head_dim, w.kv_len):
+        pool = "f16" if kind == "f16" else "q8"
+        if key != (pool, w.n_kv_heads, w.head_dim, w.kv_len):
             ring = None
             torch.cuda.empty_cache()
-            ring = _ring_for(w, dev, args.ring_l2)
-            key = (w.n_kv_heads, w.head_dim, w.kv_len)
-        mask = binary_tree_mask(w.n_q) if kind else None
+            ring = _ring_f16(w, dev, args.ring_l2) if pool == "f16" else _ring_for(w, dev, args.ring_l2)
+            key = (pool, w.n_kv_heads, w.head_dim, w.kv_len)
+        mask = binary_tree_mask(w.n_q) if kind == "tree-binary" else None
         us = time_verify_cell(w, ring, dev, tree_mask=mask)
         us_warm = time_verify_cell(w, ring[:1], dev, tree_mask=mask)
-        gbs = w.kv_bytes() / (us * 1e-6) / 1e9
+        kv_bytes = f16_kv_bytes(w) if pool == "f16" else w.kv_bytes()
+        gbs = kv_bytes / (us * 1e-6) / 1e9
         # roofline of the cell: K/V bytes at the HBM peak, or the causal flops doubled by the
         # fp16 hi + lo split at the dense tensor peak, whichever takes longer
-        t_hbm = w.kv_bytes() / (hbm_peak * 1e9)
+        t_hbm = kv_bytes / (hbm_peak * 1e9)
         t_tensor = 2 * w.causal_flops() / (bf16_peak * 1e12)
         print(json.dumps({"workload": f"{kind}-{w.name}" if kind else w.name, "us_per_call": us,
-                          "kv_mb": w.kv_bytes() / 1e6, "kv_gbs": gbs, "hbm_frac": gbs / hbm_peak,
+                          "kv_mb": kv_bytes / 1e6, "kv_gbs": gbs, "hbm_frac": gbs / hbm_peak,
                           "tflops_alg": w.causal_flops() / (us * 1e-6) / 1e12,
                           "roofline_bound": "hbm" if t_hbm >= t_tensor else "tensor",
                           "roofline_frac": max(t_hbm, t_tensor) / (us * 1e-6),

@@ -64,6 +64,17 @@ typedef struct {
     int32_t capacity;
 } kvq8_cache;
 
+/* An fp16 KV pool: K and V as IEEE binary16 bits, [n_kv_heads][capacity][head_dim] each,
+ * device memory owned by the caller.  The pool format the pages keep on their older kernel
+ * ("gfx12 WMMA kernel for the int8-KV QSA prompt attention", Gating and Limits). */
+typedef struct {
+    const uint16_t* k;
+    const uint16_t* v;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int32_t capacity;
+} kvf16_cache;
+
 /*
  * kvq8_quantize -- append n_tok tokens of K (or V) values to one plane pair.
  *   x      : fp32 [n_tok][n_kv_heads][head_dim]
@@ -190,6 +201,33 @@ size_t attn_verify_append_q8_host_scratch_bytes(int n_rows, int n_q_heads, int h
 int attn_verify_append_q8_host(const float* h_in, int n_rows, int n_q_heads, const kvq8_cache* kv,
                                int q_pos0, float softmax_scale, float* h_out, void* d_scratch,
                                size_t scratch_bytes, int n_split, kvq8_stream_t stream);
+
+/*
+ * kvf16_append -- round n_tok tokens of K and V (fp32 [n_tok][n_kv_heads][head_dim], device)
+ * to fp16 (nearest even) into both planes of an fp16 pool at positions [pos0, pos0 + n_tok).
+ * Errors: INVALID_ARG for null pointers, negative sizes or pos0 + n_tok > capacity;
+ * UNSUPPORTED when head_dim is not a multiple of 4; MISALIGNED unless every pointer is
+ * 16-byte aligned.  The pool's plane pointers are written through.
+ */
+int kvf16_append(const float* k, const float* v, int n_tok, const kvf16_cache* kv, int pos0,
+                 kvq8_stream_t stream);
+
+/* Bytes of workspace attn_verify_f16 needs for this shape (n_split 0 = the automatic choice). */
+size_t attn_verify_f16_workspace_bytes(int n_rows, int n_q_heads, int head_dim, int kv_len,
+                                       int n_kv_heads, int n_split);
+
+/*
+ * attn_verify_f16 -- attn_verify_q8 over an fp16 KV pool: the same window semantics, shapes
+ * (head_dim 128 or 256, 1 <= n_rows <= 32), split-context partials, merge, precision bound
+ * (q and p as fp16 hi + lo, fp32 accumulation; within 1e-4 of the fp64 oracle) and errors.
+ * The K and V values enter the tensor cores as they are stored; there are no block scales.
+ * Source: "perf(gfx1100): share Q8 KV scans across verifier rows", Summary, for the
+ * multi-row scan; the fp16 pool of "gfx12 WMMA kernel for the int8-KV QSA prompt
+ * attention", Gating and Limits.
+ */
+int attn_verify_f16(const float* q, int n_rows, int n_q_heads, const kvf16_cache* kv, int kv_len,
+                    int q_pos0, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                    int n_split, kvq8_stream_t stream);
 
 /*
  * attn_verify_tree_q8 -- attn_verify_q8 for a tree-shaped verify window.
