@@ -363,6 +363,10 @@ def run_native(args, world, rank, local):
 
     # prompt chunk (tensor-core kernel), L2 flushed between timed calls
     prompt = prompt_bench(args, dev, fp16_peak) if not args.no_prompt else None
+    if prompt is not None and "unavailable" not in prompt:   # the second prompt shape (hd128, 32q/8kv)
+        from speculative_verify_attention_gb300 import workloads as _wl
+        torch.cuda.empty_cache()
+        prompt["hd128"] = prompt_bench(args, dev, fp16_peak, _wl.PROMPT_HD128)
     head = head_bench(dev, hbm_peak, args.ring_l2) if not args.no_head else None
 
     result = None
@@ -456,12 +460,12 @@ def head_bench(dev, hbm_peak, ring_l2):
     return res
 
 
-def prompt_bench(args, dev, fp16_peak):
+def prompt_bench(args, dev, fp16_peak, w=None):
     import torch
 
     from speculative_verify_attention_gb300 import (KVCacheQ8, KVQ8Error, attn_prompt_q8,
                                                     attn_prompt_q8_workspace_bytes, workloads)
-    w = workloads.PROMPT
+    w = w or workloads.PROMPT
     inp = workloads.make_inputs(w)
     c = KVCacheQ8(w.n_kv_heads, w.head_dim, w.kv_len, device=dev)
     c.append(torch.from_numpy(inp.k).to(dev), torch.from_numpy(inp.v).to(dev), 0)
@@ -666,7 +670,9 @@ def main():
         import __graft_entry__
         __graft_entry__.build()
         hbm_peak, bf16_peak, _ = _peaks()
-        print(json.dumps(prompt_bench(args, torch.device("cuda", 0), bf16_peak * 0.951)), flush=True)
+        from speculative_verify_attention_gb300 import workloads as _wl
+        for w in (_wl.PROMPT, _wl.PROMPT_HD128):
+            print(json.dumps(prompt_bench(args, torch.device("cuda", 0), bf16_peak * 0.951, w)), flush=True)
         return 0
     if args.impl == "reference":
         return run_reference(args, world, rank)

@@ -38,35 +38,42 @@ int launch_combine(const float* part_o, const float* part_ml, int n_split, int r
 
 namespace {
 
-constexpr int HD = 256;
 constexpr int BM = 128;
 constexpr int BN = 64;
 constexpr int kSoftWarp0 = 2, kDeqWarp0 = 6, kDeqThreads = 320;
 constexpr int kThreads = (kDeqWarp0 + kDeqThreads / 32) * 32;   // 512: 128 registers per thread fill the SM
-constexpr int kChunks = BN * HD / 16;                            // 16-code chunks of one plane of a tile
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kMaxSegments = 8;
 
-// tensor memory columns
+// tensor memory columns (the same map at hd128, where Q and O use half of theirs)
 constexpr uint32_t TM_Q = 0, TM_O = 128, TM_S0 = 384, TM_NCOLS = 512;
 
-// shared memory layout (bytes, 1024-aligned tiles)
-constexpr int SM_KHAT = 0;                   // 2 x 32 KB, K-major 128B-swizzled [4 atoms][64 keys][128 B]
-constexpr int SM_VHAT = 65536;               // 2 x 32 KB, same physical layout, read as MN-major
-constexpr int HAT_BYTES = 32768;
-constexpr int SM_STAGE = 131072;             // 2 x 34 KB: K codes 16K | V codes 16K | K scales 1K | V scales 1K
-constexpr int STAGE_BYTES = 34816;
-constexpr int ST_KC = 0, ST_VC = 16384, ST_KS = 32768, ST_VS = 33792;
-constexpr int SM_BAR = SM_STAGE + 2 * STAGE_BYTES;
 enum { B_ST_FULL = 0, B_ST_EMPTY = 2, B_K_FULL = 4, B_V_FULL = 6, B_K_EMPTY = 8, B_V_EMPTY = 10, B_S_FULL = 12,
        B_P_FULL = 14, B_PV_DONE = 16, B_Q_READY = 18, B_COUNT = 19 };
-constexpr int SM_TMEM_SLOT = SM_BAR + B_COUNT * 8;
-constexpr int SM_SEG = SM_TMEM_SLOT + 16;    // this CTA's work segments (written by thread 0)
-constexpr int SMEM_BYTES = SM_SEG + 8 * 5 * 4 + 16;
 
-constexpr uint32_t IDESC_QK = tc::idesc_f16_f32(BM, BN, false);
-constexpr uint32_t IDESC_PV = tc::idesc_f16_f32(BM, HD, true);
+// Shared memory layout for head dim HD (bytes, 1024-aligned tiles):
+//   K^, V^ : 2 buffers each of [HD/64 atoms][64 keys][128 B], 128B-swizzled fp16 (K-major for
+//            K^, read as MN-major for V^)
+//   staging: 2 stages of K codes | V codes | K scales | V scales for one 64-key tile
+template <int HD>
+struct PL {
+    static constexpr int HAT_BYTES = (HD / 64) * BN * 128;
+    static constexpr int SM_KHAT = 0;
+    static constexpr int SM_VHAT = 2 * HAT_BYTES;
+    static constexpr int SM_STAGE = 4 * HAT_BYTES;
+    static constexpr int ST_KC = 0, ST_VC = BN * HD, ST_KS = 2 * BN * HD, ST_VS = 2 * BN * HD + BN * HD / 16;
+    static constexpr int STAGE_BYTES = 2 * BN * HD + 2 * (BN * HD / 16);
+    static constexpr int SM_BAR = SM_STAGE + 2 * STAGE_BYTES;
+    static constexpr int SM_TMEM_SLOT = SM_BAR + B_COUNT * 8;
+    static constexpr int SM_SEG = SM_TMEM_SLOT + 16;  // this CTA's work segments (written by thread 0)
+    static constexpr int SMEM_BYTES = SM_SEG + 8 * 5 * 4 + 16;
+    static constexpr int kChunks = BN * HD / 16;      // 16-code chunks of one plane of a tile
+    static constexpr uint32_t IDESC_QK = tc::idesc_f16_f32(BM, BN, false);
+    static constexpr uint32_t IDESC_PV = tc::idesc_f16_f32(BM, HD, true);
+    static_assert(STAGE_BYTES % 1024 == 0 && HAT_BYTES % 1024 == 0, "tiles stay 1024-byte aligned");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
 
 struct PromptParams {
     const uint16_t* q;
@@ -135,14 +142,17 @@ __device__ __forceinline__ void flag_timeout() { atomicOr(&g_kvq8_device_error, 
 
 // Convert one 64-key plane tile (codes + scales in staging) into the swizzled fp16 tile:
 // element (key n, dim j) -> atom j/64, row n, 16-byte chunk ((j%64)/8) ^ (n%8).
-// kDeqThreads threads share the tile's kChunks chunks of 16 codes.
+// kDeqThreads threads share the tile's kChunks chunks of 16 codes (HD/16 chunks per key).
+template <int HD>
 __device__ __forceinline__ void dequant_tile(const uint8_t* codes, const uint16_t* scales, uint8_t* hat, int nk,
                                              int d) {
+    constexpr int kChunks = PL<HD>::kChunks;
+    constexpr int CPK = HD / 16;
 #pragma unroll
     for (int k = 0; k < (kChunks + kDeqThreads - 1) / kDeqThreads; ++k) {
         const int c = d + kDeqThreads * k;
         if (c >= kChunks) break;
-        const int n = c >> 4, j16 = c & 15;
+        const int n = c / CPK, j16 = c % CPK;
         uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
         if (n < nk) {
             const uint4 raw = *reinterpret_cast<const uint4*>(codes + n * HD + j16 * 16);
@@ -169,7 +179,13 @@ __device__ __forceinline__ void dequant_tile(const uint8_t* codes, const uint16_
     }
 }
 
+template <int HD>
 __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptParams p) {
+    using L = PL<HD>;
+    constexpr int SM_KHAT = L::SM_KHAT, SM_VHAT = L::SM_VHAT, HAT_BYTES = L::HAT_BYTES, SM_STAGE = L::SM_STAGE;
+    constexpr int STAGE_BYTES = L::STAGE_BYTES, SM_BAR = L::SM_BAR, SM_TMEM_SLOT = L::SM_TMEM_SLOT, SM_SEG = L::SM_SEG;
+    constexpr int ST_KC = L::ST_KC, ST_VC = L::ST_VC, ST_KS = L::ST_KS, ST_VS = L::ST_VS;
+    constexpr uint32_t IDESC_QK = L::IDESC_QK, IDESC_PV = L::IDESC_PV;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t sbase = smem_u32(smem);
@@ -217,11 +233,17 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptPa
                     const int nk = min(BN, g.key_hi - key0);
                     const int64_t row0 = (int64_t)g.kvh * p.capacity + key0;
                     const uint32_t st = sbase + SM_STAGE + s * STAGE_BYTES;
-                    tc::mbar_arrive_expect_tx(B(B_ST_FULL + s), (uint32_t)(nk * (2 * HD + 2 * (HD / 16))));
+                    // codes rows are HD bytes (16-byte multiples); at hd256 a key's scales are 16
+                    // bytes too, at hd128 only 8, so there the dequantisers read them from global
+                    // memory instead (a bulk copy wants 16-byte aligned starts and sizes)
+                    constexpr int scale_bytes = HD == 256 ? 2 * (HD / 16) : 0;
+                    tc::mbar_arrive_expect_tx(B(B_ST_FULL + s), (uint32_t)(nk * (2 * HD + scale_bytes)));
                     tc::bulk_g2s(st + ST_KC, p.kc + row0 * HD, nk * HD, B(B_ST_FULL + s));
                     tc::bulk_g2s(st + ST_VC, p.vc + row0 * HD, nk * HD, B(B_ST_FULL + s));
-                    tc::bulk_g2s(st + ST_KS, p.ks + row0 * (HD / 32), nk * (HD / 16), B(B_ST_FULL + s));
-                    tc::bulk_g2s(st + ST_VS, p.vs + row0 * (HD / 32), nk * (HD / 16), B(B_ST_FULL + s));
+                    if constexpr (HD == 256) {
+                        tc::bulk_g2s(st + ST_KS, p.ks + row0 * (HD / 32), nk * (HD / 16), B(B_ST_FULL + s));
+                        tc::bulk_g2s(st + ST_VS, p.vs + row0 * (HD / 32), nk * (HD / 16), B(B_ST_FULL + s));
+                    }
                 }
             }
             if (!ok) flag_timeout();
@@ -299,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptPa
             {
                 const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)iq * p.n_q_heads + qh) * HD);
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < HD / 64; ++c) {   // 64 fp16 dims = 32 TMEM columns per store
                     uint32_t w[32];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
@@ -429,12 +451,14 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptPa
                 if (!__all_sync(0xffffffffu, tc::mbar_wait(B(B_ST_FULL + s), use & 1, kWaitLimit))) { ok = false; break; }
                 const int nk = min(BN, g.key_hi - t * BN);
                 const uint8_t* st = smem + SM_STAGE + s * STAGE_BYTES;
+                const int64_t srow0 = (int64_t)g.kvh * p.capacity + t * BN;
+                const uint16_t* k_sc = HD == 256 ? reinterpret_cast<const uint16_t*>(st + ST_KS) : p.ks + srow0 * (HD / 32);
+                const uint16_t* v_sc = HD == 256 ? reinterpret_cast<const uint16_t*>(st + ST_VS) : p.vs + srow0 * (HD / 32);
                 if (j >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait(B(B_K_EMPTY + s), (use - 1) & 1, kWaitLimit))) {
                     ok = false;
                     break;
                 }
-                dequant_tile(st + ST_KC, reinterpret_cast<const uint16_t*>(st + ST_KS), smem + SM_KHAT + s * HAT_BYTES,
-                             nk, d);
+                dequant_tile<HD>(st + ST_KC, k_sc, smem + SM_KHAT + s * HAT_BYTES, nk, d);
                 tc::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(B(B_K_FULL + s));
@@ -442,8 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptPa
                     ok = false;
                     break;
                 }
-                dequant_tile(st + ST_VC, reinterpret_cast<const uint16_t*>(st + ST_VS), smem + SM_VHAT + s * HAT_BYTES,
-                             nk, d);
+                dequant_tile<HD>(st + ST_VC, v_sc, smem + SM_VHAT + s * HAT_BYTES, nk, d);
                 tc::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
@@ -469,7 +492,7 @@ struct PromptPlan {
 
 int prompt_plan(int n_q, int n_q_heads, int head_dim, int kv_len, int q_pos0, int n_kv_heads, PromptPlan* pl) {
     if (n_q < 1 || n_q_heads < 1 || n_kv_heads < 1 || kv_len < 1 || q_pos0 < 0) return KVQ8_ERR_INVALID_ARG;
-    if (head_dim != HD || n_q_heads % n_kv_heads) return KVQ8_ERR_UNSUPPORTED;
+    if ((head_dim != 128 && head_dim != 256) || n_q_heads % n_kv_heads) return KVQ8_ERR_UNSUPPORTED;
     const int group = n_q_heads / n_kv_heads;
     const long long rows = (long long)n_q * group;
     if (rows > 0x7fffffffLL || (long long)n_q * n_q_heads > 0x7fffffffLL) return KVQ8_ERR_UNSUPPORTED;
@@ -504,9 +527,22 @@ int prompt_plan(int n_q, int n_q_heads, int head_dim, int kv_len, int q_pos0, in
     if (max_seg > kMaxSegments) return KVQ8_ERR_UNSUPPORTED;
     pl->n_parts = parts;
     const size_t rows_out = (size_t)n_q * n_q_heads;
-    const size_t o_bytes = (size_t)parts * rows_out * HD * sizeof(float);
+    const size_t o_bytes = (size_t)parts * rows_out * head_dim * sizeof(float);
     pl->ws_bytes = ((o_bytes + 255) / 256) * 256 + (size_t)parts * rows_out * 2 * sizeof(float);
     return KVQ8_OK;
+}
+
+template <int HD>
+int launch_prompt(const PromptParams& pp, int grid, cudaStream_t s) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(prompt_attn_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PL<HD>::SMEM_BYTES) != cudaSuccess)
+            return KVQ8_ERR_CUDA;
+        attr_set = true;
+    }
+    prompt_attn_kernel<HD><<<grid, kThreads, PL<HD>::SMEM_BYTES, s>>>(pp);
+    return launch_status();
 }
 
 }  // namespace
@@ -535,13 +571,7 @@ extern "C" int attn_prompt_q8(const uint16_t* q, int n_q, int n_q_heads, const k
         return KVQ8_ERR_MISALIGNED;
     if (!workspace || workspace_bytes < pl.ws_bytes) return KVQ8_ERR_WORKSPACE;
     if (!aligned16(workspace)) return KVQ8_ERR_MISALIGNED;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(prompt_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-            cudaSuccess)
-            return KVQ8_ERR_CUDA;
-        attr_set = true;
-    }
+    const int HD = kv->head_dim;
     const size_t rows_out = (size_t)n_q * n_q_heads;
     const size_t o_bytes = (size_t)pl.n_parts * rows_out * HD * sizeof(float);
     PromptParams pp;
@@ -565,8 +595,7 @@ extern "C" int attn_prompt_q8(const uint16_t* q, int n_q, int n_q_heads, const k
     pp.units = pl.units;
     pp.scale_log2 = softmax_scale * kLog2e;
     cudaStream_t s = (cudaStream_t)stream;
-    prompt_attn_kernel<<<pl.grid, kThreads, SMEM_BYTES, s>>>(pp);
-    const int r1 = launch_status();
+    const int r1 = HD == 128 ? launch_prompt<128>(pp, pl.grid, s) : launch_prompt<256>(pp, pl.grid, s);
     if (r1 != KVQ8_OK) return r1;
     return launch_combine(pp.part_o, reinterpret_cast<const float*>(pp.part_ml), pl.n_parts, (int)rows_out, HD, out, s);
 }

@@ -88,6 +88,8 @@ def hd128_verify(T: int) -> Workload:
 
 
 PROMPT = prompt_workload("prompt-12q1kv-hd256-kv32768-nq2048", 12, 1, 256, 32768, 2048, seed=4000)
+# the second prompt shape: the hd128 head layout of the 32q/8kv family, same chunk and context
+PROMPT_HD128 = prompt_workload("prompt-32q8kv-hd128-kv32768-nq2048", 32, 8, 128, 32768, 2048, seed=4001)
 
 VERIFY_27B_T = (4, 8)
 LONG_CTX = (2048, 20676, 32768)

@@ -21,10 +21,10 @@ def _run(gpu_cache, q16, kv_len, q_pos0, scale):
     return out.cpu().numpy()
 
 
-def _check(hq, hkv, L, nq, pos0, seed, capacity=None, sel_every=None):
-    inp = workloads.random_small(seed, hq, hkv, 256, L, nq, q_dtype="f16")
+def _check(hq, hkv, L, nq, pos0, seed, capacity=None, sel_every=None, hd=256):
+    inp = workloads.random_small(seed, hq, hkv, hd, L, nq, q_dtype="f16")
     gpu, orc = build_caches(inp, capacity=capacity)
-    scale = 1.0 / 16.0
+    scale = 1.0 / float(np.sqrt(hd))
     got = _run(gpu, inp.q, L, pos0, scale)
     if sel_every is None:
         ref = oracle.attention(orc, inp.q, L, pos0, scale)
@@ -51,6 +51,24 @@ def _check(hq, hkv, L, nq, pos0, seed, capacity=None, sel_every=None):
 ])
 def test_small_shapes(lib, hq, hkv, L, nq, pos0):
     _check(hq, hkv, L, nq, pos0, seed=hq * 100 + L)
+
+
+@pytest.mark.parametrize("hq,hkv,L,nq,pos0,capacity", [
+    (12, 1, 64, 11, 53, None),      # one tile
+    (12, 1, 200, 50, 150, 203),     # ragged last tile (odd key count), odd capacity
+    (4, 1, 1, 1, 0, 7),             # a single key, odd capacity
+    (32, 8, 333, 40, 290, 335),     # the 32q/8kv hd128 shape, rows crossing tiles, odd capacity
+    (8, 8, 130, 130, 0, None),      # MHA from position 0
+    (16, 4, 300, 60, 280, 301),     # rows past kv_len
+])
+def test_hd128_shapes(lib, hq, hkv, L, nq, pos0, capacity):
+    """hd128: a key's scales are 8 bytes, so odd capacities and odd key counts put tiles on
+    8-byte boundaries (the dequantisers read those scales from global memory)."""
+    _check(hq, hkv, L, nq, pos0, seed=hq * 100 + L + 7, capacity=capacity, hd=128)
+
+
+def test_hd128_medium_chunk(lib):
+    _check(32, 8, 2048, 256, 1792, seed=79, sel_every=5, hd=128)
 
 
 def test_capacity_larger_than_kv_len(lib):
@@ -85,8 +103,8 @@ def test_prompt_rejects_bad_arguments(lib):
 
     from speculative_verify_attention_gb300 import KVCacheQ8, KVQ8Error, attn_prompt_q8
     q = torch.zeros((4, 12, 256), dtype=torch.float16, device="cuda")
-    with pytest.raises(KVQ8Error) as e:       # head_dim 128 has no prompt kernel
-        attn_prompt_q8(torch.zeros((4, 4, 128), dtype=torch.float16, device="cuda"), KVCacheQ8(1, 128, 64), 64, 60,
+    with pytest.raises(KVQ8Error) as e:       # head_dim 64 has no prompt kernel
+        attn_prompt_q8(torch.zeros((4, 4, 64), dtype=torch.float16, device="cuda"), KVCacheQ8(1, 64, 64), 64, 60,
                        0.1)
     assert e.value.status == 2
     with pytest.raises(KVQ8Error) as e:       # kv_len beyond capacity
@@ -95,3 +113,19 @@ def test_prompt_rejects_bad_arguments(lib):
     with pytest.raises(KVQ8Error) as e:       # 12 q heads over 5 kv heads
         attn_prompt_q8(q, KVCacheQ8(5, 256, 64), 64, 60, 0.1)
     assert e.value.status == 2
+
+
+def test_full_hd128_prompt_workload_sampled(lib):
+    w = workloads.PROMPT_HD128
+    inp = workloads.make_inputs(w)
+    gpu, orc = build_caches(inp, garbage_tail=False)
+    got = _run(gpu, inp.q, w.kv_len, w.q_pos0, w.softmax_scale)
+    rng = np.random.default_rng(6)
+    sel = [(int(i), int(rng.integers(w.n_q_heads))) for i in rng.integers(0, w.n_q, 40)]
+    sel += [(0, h) for h in range(w.n_q_heads)] + [(w.n_q - 1, h) for h in range(w.n_q_heads)]
+    ref = oracle.attention(orc, inp.q, w.kv_len, w.q_pos0, w.softmax_scale, sel=sel)
+    err = rel_err(np.stack([got[i, h] for i, h in sel]), ref)
+    assert np.all(np.isfinite(got))
+    assert err <= PROMPT_TOL, f"rel err {err:.3e}"
+    from speculative_verify_attention_gb300 import kvq8_device_error
+    assert kvq8_device_error(reset=True) == 0
