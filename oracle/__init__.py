@@ -42,10 +42,11 @@ class _Cache(ctypes.Structure):
     _fields_ = [("k_codes", ctypes.c_void_p), ("k_scales", ctypes.c_void_p),
                 ("v_codes", ctypes.c_void_p), ("v_scales", ctypes.c_void_p),
                 ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("capacity", ctypes.c_int),
-                ("format", ctypes.c_int), ("k_f16", ctypes.c_void_p), ("v_f16", ctypes.c_void_p)]
+                ("format", ctypes.c_int), ("k_f16", ctypes.c_void_p), ("v_f16", ctypes.c_void_p),
+                ("v_q4", ctypes.c_void_p)]
 
 
-_Q8_0, _F16 = 0, 1
+_Q8_0, _F16, _K8V4 = 0, 1, 2
 
 
 def _load():
@@ -68,6 +69,10 @@ def _load():
             lib.oracle_kv_append_q8_0.restype = i32
             lib.oracle_kv_append_f16.argtypes = [vp, i32, i32, i32, vp, i32, i32]
             lib.oracle_kv_append_f16.restype = i32
+            lib.oracle_quantize_q4.argtypes = [vp, i64, vp, vp]
+            lib.oracle_quantize_q4.restype = None
+            lib.oracle_kv_append_q4.argtypes = [vp, i32, i32, i32, vp, vp, i32, i32]
+            lib.oracle_kv_append_q4.restype = i32
             lib.oracle_attention_partial.argtypes = [ctypes.POINTER(_Cache), vp, i32, i32, i32, i32, f64,
                                                      i64, i64, vp, vp, i64, vp, vp, vp]
             lib.oracle_attention_partial.restype = i32
@@ -153,7 +158,8 @@ class Cache:
 
     def _struct(self) -> _Cache:
         return _Cache(self.k_codes.ctypes.data, self.k_scales.ctypes.data, self.v_codes.ctypes.data,
-                      self.v_scales.ctypes.data, self.n_kv_heads, self.head_dim, self.capacity, _Q8_0, None, None)
+                      self.v_scales.ctypes.data, self.n_kv_heads, self.head_dim, self.capacity, _Q8_0, None, None,
+                      None)
 
     def append(self, k, v, pos0: int) -> None:
         """Quantise and write K and V values [n_tok][n_kv_heads][head_dim] at positions pos0.."""
@@ -166,6 +172,62 @@ class Cache:
                                            _ptr(codes), _ptr(scales), self.capacity, int(pos0))
             if rc:
                 raise ValueError("oracle_kv_append_q8_0 rejected its arguments")
+
+
+def quantize_q4(x) -> tuple[np.ndarray, np.ndarray]:
+    """4-bit V blocks of fp32 values [..., n*32] -> (nibbles uint8 [..., n*16], scales uint16 [..., n])."""
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    if a.shape[-1] % QBLOCK:
+        raise ValueError("last dimension must be a multiple of 32")
+    nb = a.size // QBLOCK
+    q = np.empty(a.shape[:-1] + (a.shape[-1] // 2,), dtype=np.uint8)
+    d = np.empty(a.shape[:-1] + (a.shape[-1] // QBLOCK,), dtype=np.uint16)
+    _load().oracle_quantize_q4(_ptr(a), nb, _ptr(q), _ptr(d))
+    return q, d
+
+
+class CacheK8V4:
+    """K8V4 pool held as numpy arrays: K as Q8_0 planes (k_codes int8 [Hkv][cap][hd], k_scales
+    uint16 [Hkv][cap][hd/32]) and V as 4-bit planes (v_q4 uint8 [Hkv][cap][hd/2] nibbles,
+    v_scales uint16 [Hkv][cap][hd/32]).  Every attention function here takes it."""
+
+    def __init__(self, n_kv_heads: int, head_dim: int, capacity: int):
+        self.n_kv_heads, self.head_dim, self.capacity = n_kv_heads, head_dim, capacity
+        nb = head_dim // QBLOCK
+        self.k_codes = np.zeros((n_kv_heads, capacity, head_dim), dtype=np.int8)
+        self.k_scales = np.zeros((n_kv_heads, capacity, nb), dtype=np.uint16)
+        self.v_q4 = np.full((n_kv_heads, capacity, head_dim // 2), 0x88, dtype=np.uint8)
+        self.v_scales = np.zeros((n_kv_heads, capacity, nb), dtype=np.uint16)
+
+    @classmethod
+    def from_planes(cls, k_codes, k_scales, v_q4, v_scales):
+        h, cap, hd = k_codes.shape
+        c = cls.__new__(cls)
+        c.n_kv_heads, c.head_dim, c.capacity = h, hd, cap
+        c.k_codes = np.ascontiguousarray(k_codes, dtype=np.int8)
+        c.k_scales = np.ascontiguousarray(k_scales, dtype=np.uint16)
+        c.v_q4 = np.ascontiguousarray(v_q4, dtype=np.uint8)
+        c.v_scales = np.ascontiguousarray(v_scales, dtype=np.uint16)
+        return c
+
+    def _struct(self) -> _Cache:
+        return _Cache(self.k_codes.ctypes.data, self.k_scales.ctypes.data, None, self.v_scales.ctypes.data,
+                      self.n_kv_heads, self.head_dim, self.capacity, _K8V4, None, None, self.v_q4.ctypes.data)
+
+    def append(self, k, v, pos0: int) -> None:
+        """Quantise K (Q8_0) and V (4-bit) values [n_tok][n_kv_heads][head_dim] at positions pos0.."""
+        lib = _load()
+        a_k = np.ascontiguousarray(k, dtype=np.float32)
+        a_v = np.ascontiguousarray(v, dtype=np.float32)
+        for a in (a_k, a_v):
+            if a.ndim != 3 or a.shape[1:] != (self.n_kv_heads, self.head_dim):
+                raise ValueError(f"bad K/V shape {a.shape}")
+        rc = lib.oracle_kv_append_q8_0(_ptr(a_k), a_k.shape[0], self.n_kv_heads, self.head_dim,
+                                       _ptr(self.k_codes), _ptr(self.k_scales), self.capacity, int(pos0))
+        rc |= lib.oracle_kv_append_q4(_ptr(a_v), a_v.shape[0], self.n_kv_heads, self.head_dim,
+                                      _ptr(self.v_q4), _ptr(self.v_scales), self.capacity, int(pos0))
+        if rc:
+            raise ValueError("oracle K8V4 append rejected its arguments")
 
 
 class CacheF16:
@@ -189,7 +251,7 @@ class CacheF16:
 
     def _struct(self) -> _Cache:
         return _Cache(None, None, None, None, self.n_kv_heads, self.head_dim, self.capacity, _F16,
-                      self.k.ctypes.data, self.v.ctypes.data)
+                      self.k.ctypes.data, self.v.ctypes.data, None)
 
     def append(self, k, v, pos0: int) -> None:
         """Round K and V values [n_tok][n_kv_heads][head_dim] (fp32) to fp16 at positions pos0.."""

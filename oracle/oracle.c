@@ -40,6 +40,15 @@
  *    an append rounds the fp32 inputs to nearest even; attention is the same fp64 formula
  *    with k[n][j] and v[n][j] the stored values (no codes, no block scales).
  *
+ *  - K8V4 pools (the pages run a `--kv k8v4` pool and keep it, like fp16, on the older
+ *    kernels: "gfx12 WMMA kernel for the int8-KV QSA prompt attention", Gating and Limits;
+ *    the 4-bit V format itself is not given).  Reading: K is Q8_0 as above; V is a
+ *    symmetric 4-bit block format mirroring the Q8_0 rule with 2^3 - 1 in place of 2^7 - 1:
+ *      d32 = amax / 7 (IEEE fp32 division), stored as fp16(d32) rounded to nearest even;
+ *      q = clamp(round_half_away_from_zero(x / d32), -7, 7), 0 for a block whose d32 is 0;
+ *      stored as the nibble q + 8, element 2m in the low and 2m + 1 in the high nibble of
+ *      byte m, [n_kv_heads][capacity][head_dim / 2] bytes; the value is (nibble - 8) * d.
+ *
  *  - Split-context partials and their merge ("share Q8 KV scans across verifier
  *    rows", Summary: "The partials layout and reducer are unchanged"): a partial over
  *    keys [k0, k1) is (o, m, l) with m = max s over the visible keys of the range,
@@ -170,6 +179,55 @@ int oracle_kv_append_q8_0(const float* x, int n_tok, int n_kv_heads, int head_di
     return 0;
 }
 
+/* ---------------------------------------------------------------- 4-bit V (K8V4) */
+
+/* Quantise one block of 32 fp32 values to 16 bytes of nibbles + an fp16 scale (rule in the
+ * header comment). */
+static void quantize_block_q4(const float* x, uint8_t* packed, uint16_t* d_bits) {
+    float amax = 0.0f;
+    for (int j = 0; j < QBLOCK; ++j) {
+        float a = fabsf(x[j]);
+        if (a > amax) amax = a;
+    }
+    float d32 = amax / 7.0f;
+    *d_bits = oracle_f32_to_f16_bits(d32);
+    for (int m = 0; m < QBLOCK / 2; ++m) packed[m] = 0;
+    for (int j = 0; j < QBLOCK; ++j) {
+        int q = 0;
+        if (d32 != 0.0f) {
+            float r = roundf(x[j] / d32);
+            if (r > 7.0f) r = 7.0f;
+            if (r < -7.0f) r = -7.0f;
+            q = (int)r;
+        }
+        packed[j / 2] |= (uint8_t)((q + 8) << (4 * (j & 1)));
+    }
+}
+
+void oracle_quantize_q4(const float* x, int64_t n_blocks, uint8_t* packed, uint16_t* d_bits) {
+    for (int64_t b = 0; b < n_blocks; ++b)
+        quantize_block_q4(x + b * QBLOCK, packed + b * (QBLOCK / 2), d_bits + b);
+}
+
+/* Append n_tok tokens of V values x[n_tok][n_kv_heads][head_dim] into the 4-bit plane
+ * codes[n_kv_heads][capacity][head_dim/2], scales[n_kv_heads][capacity][head_dim/32] at
+ * positions [pos0, pos0 + n_tok).  Returns 0, or -1 on a bad argument. */
+int oracle_kv_append_q4(const float* x, int n_tok, int n_kv_heads, int head_dim, uint8_t* codes,
+                        uint16_t* scales, int capacity, int pos0) {
+    if (n_tok < 0 || n_kv_heads <= 0 || head_dim <= 0 || head_dim % QBLOCK) return -1;
+    if (pos0 < 0 || (int64_t)pos0 + n_tok > capacity) return -1;
+    const int nb = head_dim / QBLOCK;
+    for (int t = 0; t < n_tok; ++t)
+        for (int h = 0; h < n_kv_heads; ++h) {
+            const float* src = x + ((int64_t)t * n_kv_heads + h) * head_dim;
+            int64_t row = (int64_t)h * capacity + pos0 + t;
+            for (int b = 0; b < nb; ++b)
+                quantize_block_q4(src + b * QBLOCK, codes + row * (head_dim / 2) + b * (QBLOCK / 2),
+                                  scales + row * nb + b);
+        }
+    return 0;
+}
+
 /* ---------------------------------------------------------------- attention */
 
 typedef struct {
@@ -178,12 +236,13 @@ typedef struct {
     const int8_t* v_codes;
     const uint16_t* v_scales;
     int n_kv_heads, head_dim, capacity;
-    int format;              /* ORACLE_Q8_0 or ORACLE_F16 */
+    int format;              /* ORACLE_Q8_0, ORACLE_F16 or ORACLE_K8V4 */
     const uint16_t* k_f16;   /* ORACLE_F16: fp16 bits [n_kv_heads][capacity][head_dim] */
     const uint16_t* v_f16;
+    const uint8_t* v_q4;     /* ORACLE_K8V4: V nibbles [n_kv_heads][capacity][head_dim/2] (scales in v_scales) */
 } oracle_cache;
 
-enum { ORACLE_Q8_0 = 0, ORACLE_F16 = 1 };
+enum { ORACLE_Q8_0 = 0, ORACLE_F16 = 1, ORACLE_K8V4 = 2 };
 
 /* Value of element j of token n of kv head h in one plane: code * block scale for Q8_0,
  * the stored binary16 value for an fp16 pool. */
@@ -191,6 +250,12 @@ static double deq_plane(const oracle_cache* c, int plane, int h, int64_t n, int 
     int64_t row = (int64_t)h * c->capacity + n;
     if (c->format == ORACLE_F16)
         return oracle_f16_bits_to_f64((plane ? c->v_f16 : c->k_f16)[row * c->head_dim + j]);
+    if (c->format == ORACLE_K8V4 && plane) {
+        uint8_t byte = c->v_q4[row * (c->head_dim / 2) + j / 2];
+        int nib = (j & 1) ? (byte >> 4) : (byte & 15);
+        double d = oracle_f16_bits_to_f64(c->v_scales[row * (c->head_dim / QBLOCK) + j / QBLOCK]);
+        return (double)(nib - 8) * d;
+    }
     const int8_t* codes = plane ? c->v_codes : c->k_codes;
     const uint16_t* scales = plane ? c->v_scales : c->k_scales;
     double d = oracle_f16_bits_to_f64(scales[row * (c->head_dim / QBLOCK) + j / QBLOCK]);
@@ -245,7 +310,7 @@ static void attend_one(const oracle_cache* c, const double* qrow, int kv_head, i
 
 static int check_cache(const oracle_cache* c, int n_q_heads, int kv_len) {
     if (!c || c->n_kv_heads <= 0 || c->head_dim <= 0 || c->head_dim % QBLOCK) return -1;
-    if (c->format != ORACLE_Q8_0 && c->format != ORACLE_F16) return -1;
+    if (c->format != ORACLE_Q8_0 && c->format != ORACLE_F16 && c->format != ORACLE_K8V4) return -1;
     if (n_q_heads <= 0 || n_q_heads % c->n_kv_heads) return -1;
     if (kv_len < 0 || kv_len > c->capacity) return -1;
     return 0;
