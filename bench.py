@@ -533,6 +533,31 @@ def _ring_f16(w, dev, ring_l2):
     return ring
 
 
+def _ring_k8v4(w, dev, ring_l2):
+    """A ring of K8V4 pools holding the workload's K/V (total size above ring_l2 x L2)."""
+    import torch
+
+    from speculative_verify_attention_gb300 import KVCacheK8V4, workloads
+    inp = workloads.make_inputs(w)
+    base = KVCacheK8V4(w.n_kv_heads, w.head_dim, w.kv_len, device=dev)
+    base.append(torch.from_numpy(inp.k).to(dev), torch.from_numpy(inp.v).to(dev), 0)
+    planes = ("k_codes", "k_scales", "v_codes", "v_scales")
+    nbytes = sum(getattr(base, n).numel() * getattr(base, n).element_size() for n in planes)
+    ring = [base]
+    for _ in range(max(2, int(np.ceil(ring_l2 * L2_BYTES / nbytes))) - 1):
+        c = KVCacheK8V4(w.n_kv_heads, w.head_dim, w.kv_len, device=dev)
+        for n in planes:
+            getattr(c, n).copy_(getattr(base, n))
+        ring.append(c)
+    return ring
+
+
+def k8v4_kv_bytes(w) -> int:
+    """Bytes of the K8V4 planes read for kv_len tokens: Q8_0 K, 4-bit V, fp16 scales for both."""
+    hd = w.head_dim
+    return w.n_kv_heads * w.kv_len * (hd + hd // 16 + hd // 2 + hd // 16)
+
+
 def f16_kv_bytes(w) -> int:
     """Bytes of the fp16 K and V planes read for kv_len tokens."""
     return 2 * w.n_kv_heads * w.kv_len * w.head_dim * 2
@@ -558,8 +583,9 @@ def time_verify_cell(w, ring, dev, reps=10, tree_mask=None):
     with CUDA events; returns the median over the replays of microseconds per call."""
     import torch
 
-    from speculative_verify_attention_gb300 import (KVCacheF16, attn_verify_f16, attn_verify_q8,
-                                                    attn_verify_q8_workspace_bytes, attn_verify_tree_q8, workloads)
+    from speculative_verify_attention_gb300 import (KVCacheF16, KVCacheK8V4, attn_verify_f16, attn_verify_k8v4,
+                                                    attn_verify_q8, attn_verify_q8_workspace_bytes,
+                                                    attn_verify_tree_q8, workloads)
     q = torch.from_numpy(workloads.make_inputs(w, kv_len=1).q).to(dev)
     out = torch.empty_like(q)
     ws = torch.empty(attn_verify_q8_workspace_bytes(w.n_q, w.n_q_heads, w.head_dim, w.kv_len, w.n_kv_heads),
@@ -567,6 +593,9 @@ def time_verify_cell(w, ring, dev, reps=10, tree_mask=None):
     if isinstance(ring[0], KVCacheF16):   # fp16 pools (the same workspace size rule)
         def call(c):
             attn_verify_f16(q, c, w.kv_len, w.q_pos0, w.softmax_scale, out=out, workspace=ws)
+    elif isinstance(ring[0], KVCacheK8V4):
+        def call(c):
+            attn_verify_k8v4(q, c, w.kv_len, w.q_pos0, w.softmax_scale, out=out, workspace=ws)
     elif tree_mask is not None:
         m = torch.from_numpy(np.ascontiguousarray(tree_mask, np.uint32).view(np.int32)).to(dev)
 
@@ -614,21 +643,25 @@ def sweep(args):
     cells += [(workloads.verify_27b(t), "f16") for t in (4, 8)]
     cells += [(workloads.long_verify(c, t), "f16") for c in (20676, 32768) for t in (4, 8)]
     cells += [(workloads.hd128_verify(t), "f16") for t in (4, 8)]
+    # K8V4 pools
+    cells += [(workloads.verify_27b(t), "k8v4") for t in (4, 8)]
+    cells += [(workloads.long_verify(c, t), "k8v4") for c in (20676, 32768) for t in (4, 8)]
+    cells += [(workloads.hd128_verify(t), "k8v4") for t in (4, 8)]
     cells = [c if isinstance(c, tuple) else (c, None) for c in cells]
     cells = [(w, kind) for w, kind in cells
              if not args.sweep_filter or args.sweep_filter in (f"{kind}-{w.name}" if kind else w.name)]
     key, ring = None, None
     for w, kind in cells:
-        pool = "f16" if kind == "f16" else "q8"
+        pool = kind if kind in ("f16", "k8v4") else "q8"
         if key != (pool, w.n_kv_heads, w.head_dim, w.kv_len):
             ring = None
             torch.cuda.empty_cache()
-            ring = _ring_f16(w, dev, args.ring_l2) if pool == "f16" else _ring_for(w, dev, args.ring_l2)
+            ring = {"f16": _ring_f16, "k8v4": _ring_k8v4, "q8": _ring_for}[pool](w, dev, args.ring_l2)
             key = (pool, w.n_kv_heads, w.head_dim, w.kv_len)
         mask = binary_tree_mask(w.n_q) if kind == "tree-binary" else None
         us = time_verify_cell(w, ring, dev, tree_mask=mask)
         us_warm = time_verify_cell(w, ring[:1], dev, tree_mask=mask)
-        kv_bytes = f16_kv_bytes(w) if pool == "f16" else w.kv_bytes()
+        kv_bytes = {"f16": f16_kv_bytes, "k8v4": k8v4_kv_bytes, "q8": lambda w_: w_.kv_bytes()}[pool](w)
         gbs = kv_bytes / (us * 1e-6) / 1e9
         # roofline of the cell: K/V bytes at the HBM peak, or the causal flops doubled by the
         # fp16 hi + lo split at the dense tensor peak, whichever takes longer

@@ -64,6 +64,21 @@ typedef struct {
     int32_t capacity;
 } kvq8_cache;
 
+/* A K8V4 KV pool: K as Q8_0 planes (as kvq8_cache), V as 4-bit blocks: v_codes holds
+ * [n_kv_heads][capacity][head_dim / 2] bytes, element 2m in the low nibble of byte m stored
+ * as code + 8 (code in [-7, 7]), v_scales one fp16 scale per 32 values as for Q8_0.
+ * The pages run such a pool without stating its V format; the reading is the Q8_0 rule with
+ * 7 in place of 127 ("gfx12 WMMA kernel for the int8-KV QSA prompt attention", Gating). */
+typedef struct {
+    const int8_t* k_codes;
+    const uint16_t* k_scales;
+    const uint8_t* v_codes;
+    const uint16_t* v_scales;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int32_t capacity;
+} kvk8v4_cache;
+
 /* An fp16 KV pool: K and V as IEEE binary16 bits, [n_kv_heads][capacity][head_dim] each,
  * device memory owned by the caller.  The pool format the pages keep on their older kernel
  * ("gfx12 WMMA kernel for the int8-KV QSA prompt attention", Gating and Limits). */
@@ -201,6 +216,23 @@ size_t attn_verify_append_q8_host_scratch_bytes(int n_rows, int n_q_heads, int h
 int attn_verify_append_q8_host(const float* h_in, int n_rows, int n_q_heads, const kvq8_cache* kv,
                                int q_pos0, float softmax_scale, float* h_out, void* d_scratch,
                                size_t scratch_bytes, int n_split, kvq8_stream_t stream);
+
+/*
+ * kvk8v4_append -- append n_tok tokens of K (to Q8_0) and V (to 4-bit blocks) into a K8V4
+ * pool at positions [pos0, pos0 + n_tok), one launch.  k, v: fp32 [n_tok][n_kv_heads][head_dim]
+ * on the device.  The K bytes equal kvq8_append's.  Errors as for kvq8_append.
+ */
+int kvk8v4_append(const float* k, const float* v, int n_tok, const kvk8v4_cache* kv, int pos0,
+                  kvq8_stream_t stream);
+
+/*
+ * attn_verify_k8v4 -- attn_verify_q8 over a K8V4 pool: the same window semantics, shapes,
+ * workspace (attn_verify_q8_workspace_bytes), precision bound and errors; the V codes are
+ * expanded from their nibbles in registers.
+ */
+int attn_verify_k8v4(const float* q, int n_rows, int n_q_heads, const kvk8v4_cache* kv, int kv_len,
+                     int q_pos0, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                     int n_split, kvq8_stream_t stream);
 
 /*
  * kvf16_append -- round n_tok tokens of K and V (fp32 [n_tok][n_kv_heads][head_dim], device)

@@ -30,7 +30,8 @@ KVQ8_ERR_CUDA = 5
 EXPORTED = ("kvq8_quantize", "kvq8_append", "attn_verify_q8_workspace_bytes", "attn_verify_q8", "attn_verify_tree_q8",
             "attn_verify_append_q8_workspace_bytes", "attn_verify_append_q8", "attn_verify_q8_partials_count",
             "attn_verify_q8_partials", "attn_verify_append_q8_host_scratch_bytes", "attn_verify_append_q8_host",
-            "kvf16_append", "attn_verify_f16_workspace_bytes", "attn_verify_f16", "attn_combine",
+            "kvf16_append", "attn_verify_f16_workspace_bytes", "attn_verify_f16", "kvk8v4_append", "attn_verify_k8v4",
+            "attn_combine",
             "attn_prompt_q8_workspace_bytes", "attn_prompt_q8", "attn_verify_q8_noalloc", "kvq8_device_error", "kvq8_status_str",
             "argmax_rows_top_prob_workspace_bytes", "argmax_rows_top_prob")
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
@@ -44,6 +45,12 @@ class KVQ8Error(RuntimeError):
 
 class kvf16_cache(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("capacity", ctypes.c_int32)]
+
+
+class kvk8v4_cache(ctypes.Structure):
+    _fields_ = [("k_codes", ctypes.c_void_p), ("k_scales", ctypes.c_void_p),
+                ("v_codes", ctypes.c_void_p), ("v_scales", ctypes.c_void_p),
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("capacity", ctypes.c_int32)]
 
 
@@ -87,6 +94,11 @@ def load_library():
         lib.attn_verify_append_q8_host_scratch_bytes.restype = sz
         lib.attn_verify_append_q8_host.argtypes = [vp, i32, i32, cp, i32, f32, vp, vp, sz, i32, vp]
         lib.attn_verify_append_q8_host.restype = i32
+        c44 = ctypes.POINTER(kvk8v4_cache)
+        lib.kvk8v4_append.argtypes = [vp, vp, i32, c44, i32, vp]
+        lib.kvk8v4_append.restype = i32
+        lib.attn_verify_k8v4.argtypes = [vp, i32, i32, c44, i32, i32, f32, vp, vp, sz, i32, vp]
+        lib.attn_verify_k8v4.restype = i32
         cf = ctypes.POINTER(kvf16_cache)
         lib.kvf16_append.argtypes = [vp, vp, i32, cf, i32, vp]
         lib.kvf16_append.restype = i32
@@ -175,6 +187,57 @@ class KVCacheQ8:
         """Quantise K and V values [n_tok][n_kv_heads][head_dim] (fp32) into positions pos0..
         (one kvq8_append launch for both planes)."""
         kvq8_append(k, v, self, pos0, stream)
+
+
+class KVCacheK8V4:
+    """Caller-owned K8V4 pool on one device (kvk8v4_cache of include/kvq8attn.h): K as Q8_0
+    planes, V as 4-bit nibbles v_codes uint8 [n_kv_heads][capacity][head_dim/2] with fp16
+    scales v_scales [n_kv_heads][capacity][head_dim/32]."""
+
+    def __init__(self, n_kv_heads: int, head_dim: int, capacity: int, device="cuda"):
+        self.n_kv_heads, self.head_dim, self.capacity = n_kv_heads, head_dim, capacity
+        nb = head_dim // 32
+        self.k_codes = torch.zeros((n_kv_heads, capacity, head_dim), dtype=torch.int8, device=device)
+        self.k_scales = torch.zeros((n_kv_heads, capacity, nb), dtype=torch.float16, device=device)
+        self.v_codes = torch.full((n_kv_heads, capacity, head_dim // 2), 0x88, dtype=torch.uint8, device=device)
+        self.v_scales = torch.zeros((n_kv_heads, capacity, nb), dtype=torch.float16, device=device)
+
+    def struct(self) -> kvk8v4_cache:
+        return kvk8v4_cache(self.k_codes.data_ptr(), self.k_scales.data_ptr(), self.v_codes.data_ptr(),
+                            self.v_scales.data_ptr(), self.n_kv_heads, self.head_dim, self.capacity)
+
+    def append(self, k: torch.Tensor, v: torch.Tensor, pos0: int, stream=None) -> None:
+        """Quantise K (Q8_0) and V (4-bit) values [n_tok][n_kv_heads][head_dim] (fp32) at pos0.."""
+        kvk8v4_append(k, v, self, pos0, stream)
+
+
+def kvk8v4_append(k: torch.Tensor, v: torch.Tensor, cache: KVCacheK8V4, pos0: int, stream=None) -> None:
+    _need(k, "k", torch.float32)
+    _need(v, "v", torch.float32)
+    if k.shape != v.shape or k.dim() != 3 or k.shape[1:] != (cache.n_kv_heads, cache.head_dim):
+        raise ValueError(f"k and v must both be [n_tok][{cache.n_kv_heads}][{cache.head_dim}]")
+    st = load_library().kvk8v4_append(_ptr(k), _ptr(v), k.shape[0], ctypes.byref(cache.struct()), int(pos0),
+                                      _stream(stream))
+    _check("kvk8v4_append", st)
+
+
+def attn_verify_k8v4(q: torch.Tensor, cache: KVCacheK8V4, kv_len: int, q_pos0: int, softmax_scale: float,
+                     out: torch.Tensor | None = None, workspace: torch.Tensor | None = None, n_split: int = 0,
+                     stream=None) -> torch.Tensor:
+    """Verify attention of fp32 q [T][Hq][hd] over a K8V4 pool; returns fp32 [T][Hq][hd]."""
+    _need(q, "q", torch.float32)
+    n_rows, n_q_heads, head_dim = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.float32)
+    if workspace is None:
+        nbytes = attn_verify_q8_workspace_bytes(n_rows, n_q_heads, head_dim, kv_len, cache.n_kv_heads, n_split)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    st = load_library().attn_verify_k8v4(_ptr(q), n_rows, n_q_heads, ctypes.byref(cache.struct()), int(kv_len),
+                                         int(q_pos0), float(softmax_scale), _ptr(out), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), int(n_split), _stream(stream))
+    _check("attn_verify_k8v4", st)
+    return out
 
 
 class KVCacheF16:

@@ -34,3 +34,29 @@ __device__ __forceinline__ uint32_t q8_0_block(float4 v, uint16_t* scale_bits) {
 }
 
 }  // namespace kvq8
+
+namespace kvq8 {
+
+// The 4-bit V blocks of a K8V4 pool: the same 8-lane block layout, scale max|x| / 7 (fp32
+// division, stored as fp16), codes round-half-away-from-zero of x / scale clamped to [-7, 7],
+// stored as nibbles code + 8 with element 2m in the low nibble of byte m.  Returns this
+// lane's 4 values as 2 bytes (little-endian in the low 16 bits).  The K8V4 pool is named,
+// without its format, in "gfx12 WMMA kernel for the int8-KV QSA prompt attention" (Gating).
+__device__ __forceinline__ uint32_t q4_block(float4 v, uint16_t* scale_bits) {
+    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float d32 = __fdiv_rn(amax, 7.0f);
+    const float xs[4] = {v.x, v.y, v.z, v.w};
+    uint32_t packed = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        float r = 0.0f;
+        if (d32 != 0.0f) r = fminf(fmaxf(roundf(__fdiv_rn(xs[e], d32)), -7.0f), 7.0f);
+        packed |= (uint32_t)((int)r + 8) << (4 * e);
+    }
+    *scale_bits = __half_as_ushort(__float2half_rn(d32));
+    return packed;
+}
+
+}  // namespace kvq8

@@ -73,8 +73,68 @@ int launch_quantize(const float* x0, const float* x1, int n_tok, int n_kv_heads,
     return launch_status();
 }
 
+// K8V4 append: blocks [0, n_blocks) are K (Q8_0), [n_blocks, 2 n_blocks) V (4-bit), one
+// 8-lane group per 32-value block as in the Q8_0 kernel.
+__global__ void __launch_bounds__(256) append_k8v4_kernel(const float4* __restrict__ k, const float4* __restrict__ v,
+                                                          int64_t n_blocks, int n_kv_heads, int nb_per_head_row,
+                                                          int8_t* __restrict__ k_codes, uint16_t* __restrict__ k_scales,
+                                                          uint8_t* __restrict__ v_codes,
+                                                          uint16_t* __restrict__ v_scales, int capacity, int pos0) {
+    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t blk_all = gid >> 3;
+    const bool is_v = blk_all >= n_blocks;
+    const int64_t blk = is_v ? blk_all - n_blocks : blk_all;
+    const int sub = threadIdx.x & 7;
+    const bool live = blk_all < 2 * n_blocks;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (live) x = __ldg((is_v ? v : k) + blk * 8 + sub);
+    // both quantisers run on every lane (their shuffles stay inside the lane's 8-lane group)
+    // and each lane keeps its own plane's result
+    uint16_t sq8, sq4;
+    const uint32_t p8 = q8_0_block(x, &sq8);
+    const uint32_t p4 = q4_block(x, &sq4);
+    if (!live) return;
+    const int64_t row_blocks = (int64_t)n_kv_heads * nb_per_head_row;
+    const int64_t tok = blk / row_blocks;
+    const int64_t rem = blk - tok * row_blocks;
+    const int h = (int)(rem / nb_per_head_row);
+    const int b = (int)(rem - (int64_t)h * nb_per_head_row);
+    const int64_t row = (int64_t)h * capacity + pos0 + tok;
+    if (!is_v) {
+        *reinterpret_cast<uint32_t*>(k_codes + row * (int64_t)nb_per_head_row * kQBlock + b * kQBlock + sub * 4) = p8;
+        if (sub == 0) k_scales[row * nb_per_head_row + b] = sq8;
+    } else {
+        *reinterpret_cast<uint16_t*>(v_codes + row * (int64_t)nb_per_head_row * (kQBlock / 2) + b * (kQBlock / 2) +
+                                     sub * 2) = (uint16_t)p4;
+        if (sub == 0) v_scales[row * nb_per_head_row + b] = sq4;
+    }
+}
+
 }  // namespace
 }  // namespace kvq8
+
+extern "C" int kvk8v4_append(const float* k, const float* v, int n_tok, const kvk8v4_cache* kv, int pos0,
+                             kvq8_stream_t stream) {
+    using namespace kvq8;
+    if (!kv || n_tok < 0 || pos0 < 0) return KVQ8_ERR_INVALID_ARG;
+    if (kv->n_kv_heads <= 0 || kv->head_dim <= 0 || kv->capacity <= 0) return KVQ8_ERR_INVALID_ARG;
+    if (kv->head_dim % kQBlock) return KVQ8_ERR_UNSUPPORTED;
+    if ((int64_t)pos0 + n_tok > kv->capacity) return KVQ8_ERR_INVALID_ARG;
+    if (n_tok == 0) return KVQ8_OK;
+    if (!k || !v || !kv->k_codes || !kv->k_scales || !kv->v_codes || !kv->v_scales) return KVQ8_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(kv->k_codes) || !aligned16(kv->k_scales) ||
+        !aligned16(kv->v_codes) || !aligned16(kv->v_scales))
+        return KVQ8_ERR_MISALIGNED;
+    const int nb = kv->head_dim / kQBlock;
+    const int64_t n_blocks = (int64_t)n_tok * kv->n_kv_heads * nb;
+    const int64_t grid = (n_blocks * 16 + 255) / 256;
+    if (grid > 0x7fffffffLL) return KVQ8_ERR_UNSUPPORTED;
+    append_k8v4_kernel<<<(unsigned)grid, 256, 0, (cudaStream_t)stream>>>(
+        reinterpret_cast<const float4*>(k), reinterpret_cast<const float4*>(v), n_blocks, kv->n_kv_heads, nb,
+        const_cast<int8_t*>(kv->k_codes), const_cast<uint16_t*>(kv->k_scales), const_cast<uint8_t*>(kv->v_codes),
+        const_cast<uint16_t*>(kv->v_scales), kv->capacity, pos0);
+    return launch_status();
+}
 
 extern "C" int kvq8_quantize(const float* x, int n_tok, int n_kv_heads, int head_dim, int8_t* codes,
                              uint16_t* scales, int capacity, int pos0, kvq8_stream_t stream) {

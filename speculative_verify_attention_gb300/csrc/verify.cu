@@ -142,6 +142,45 @@ __device__ __forceinline__ int div_group(int x, const VerifyParams& p) {
 __device__ __forceinline__ int frexp_exponent(float x) { return (int)((__float_as_uint(x) >> 23) & 0xFFu) - 126; }
 __device__ __forceinline__ float exp2_int(int n) { return __uint_as_float((uint32_t)(n + 127) << 23); }
 
+// 4-bit V codes of one tile (K8V4 pools): HD/2 bytes per key, 16-byte chunk c of row n stored
+// at chunk c ^ ((n >> 1) & (CPR - 1)), so the four key rows a PV load touches (2t, t = 0..3)
+// fall in four different chunks; rows at or past key_end are zero-filled.
+template <int HD>
+__device__ __forceinline__ void load_codes_v4(uint8_t* smem, const uint8_t* plane, int64_t head_row0, int tile_key0,
+                                              int key_end) {
+    constexpr int ROWB = HD / 2;
+    constexpr int CPR = ROWB / 16;                 // 8 (hd256) or 4 (hd128) chunks per row
+    constexpr int ROWS_PER_PASS = kThreads / CPR;  // 32 or 64
+    static_assert(ROWS_PER_PASS % (2 * CPR) == 0, "row step must keep the swizzle phase");
+    const int n0 = threadIdx.x / CPR, c16 = threadIdx.x % CPR;
+    const uint32_t dst0 = smem_u32(smem) + n0 * ROWB + ((c16 ^ ((n0 >> 1) & (CPR - 1))) << 4);
+    const uint8_t* src0 = plane + (head_row0 + tile_key0 + n0) * ROWB + c16 * 16;
+    const int valid = key_end - tile_key0 - n0;
+#pragma unroll
+    for (int k = 0; k < kKT / ROWS_PER_PASS; ++k) {
+        const bool ok = k * ROWS_PER_PASS < valid;
+        cp_async_16(dst0 + k * ROWS_PER_PASS * ROWB, ok ? src0 + (int64_t)k * ROWS_PER_PASS * ROWB : src0 - (int64_t)n0 * ROWB,
+                    ok ? 16 : 0);
+    }
+}
+
+// Nibble pairs -> fp16 pairs, exactly.  x holds two 16-bit halves (key a in the low half, key b
+// in the high half), each 4 nibbles of 4 consecutive dims.  lo: nibbles 0 and 4 (dim 0 of both
+// keys) placed in the fp16 pattern 0x640n is 1024 + n; subtracting 1032 gives n - 8.  hi:
+// nibbles 1 and 5 masked in place are 16 n in the mantissa, 1024 + 16 n; times 1/16 minus 72
+// gives n - 8.  (x >> 8 gives dims 2 and 3 the same way.)
+__device__ __forceinline__ uint32_t nib_lo_to_half2(uint32_t x) {
+    const uint32_t r = (x & 0x000F000Fu) | 0x64006400u;
+    const __half2 v = __hsub2(u32_as_h2(r), __half2half2(__ushort_as_half((unsigned short)0x6408u)));  // 1032
+    return h2_as_u32(v);
+}
+__device__ __forceinline__ uint32_t nib_hi_to_half2(uint32_t x) {
+    const uint32_t r = (x & 0x00F000F0u) | 0x64006400u;
+    const __half2 v = __hfma2(u32_as_h2(r), __half2half2(__ushort_as_half((unsigned short)0x2C00u)),   // 1/16
+                              __half2half2(__ushort_as_half((unsigned short)0xD480u)));                // -72
+    return h2_as_u32(v);
+}
+
 // Append-and-verify, window slice: quantises the nk (<= 32) window tokens' fp32 keys and
 // values to Q8_0 (bit-exact with the append kernel).  The keys go straight into this block's
 // K tile (the layout load_codes and load_scales produce, rows past nk zeroed as the
@@ -199,7 +238,7 @@ __device__ __forceinline__ void window_tile(const VerifyParams& p, uint8_t* smem
 // both the S^T and the O^T fragments, so the softmax factors never leave the thread.
 // TREE: the window's rows see the window keys their mask selects (p.wmask); otherwise the
 // window is sequential (row i sees keys < q_pos0 + i + 1) and the mask code is compiled out.
-template <int HD, int NT, bool TREE, bool APPEND>
+template <int HD, int NT, bool TREE, bool APPEND, bool V4 = false>
 __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kernel(const VerifyParams p) {
     using L = Smem<HD, NT>;
     constexpr int NB = L::NB, RP = L::RP, PS = L::PS;
@@ -347,13 +386,22 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
     const int v_cx = 2 * pvb + (g >> 2);
     const int v_off0 = (2 * t) * HD + ((v_cx ^ (2 * t)) << 4) + 4 * (g & 3);
     const int v_off1 = (2 * t + 1) * HD + ((v_cx ^ (2 * t + 1)) << 4) + 4 * (g & 3);
+    // 4-bit V (K8V4): rows of HD/2 bytes; the lane's 4 dims are the 2 bytes at 2g of chunk pvb,
+    // stored at chunk pvb ^ phase(row), phase(16 ks + 2t (+1)) = t and phase(16 ks + 2t + 8 (+9))
+    // = (t + 4) mod (HD/32)
+    constexpr int V4ROWB = HD / 2;
+    const int v4_off0 = (2 * t) * V4ROWB + ((pvb ^ t) << 4) + 2 * g;
+    const int v4_off8 = (2 * t + 8) * V4ROWB + ((pvb ^ ((t + 4) & (HD / 32 - 1))) << 4) + 2 * g;
     const uint2* const p_lane = sP + t * PS + g;
 
     for (int tile0 = key_begin; tile0 < key_end; tile0 += kKT) {
         const int nk = min(kKT, key_end - tile0);  // keys of this tile inside the slice
         cp_async_wait<0>();  // K of this tile landed (the only copy group in flight)
         __syncthreads();     // ... for every thread; and every warp is done with the previous sV
-        load_codes<HD>(sV, p.v_codes, head_row0, tile0, key_end);
+        if constexpr (V4)
+            load_codes_v4<HD>(sV, reinterpret_cast<const uint8_t*>(p.v_codes), head_row0, tile0, key_end);
+        else
+            load_codes<HD>(sV, p.v_codes, head_row0, tile0, key_end);
         load_scales<HD>(smem + L::kVs, p.v_scales, head_row0, tile0, key_end);
         cp_async_commit();
 
@@ -550,25 +598,46 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
             }
             const __half2 d01 = u32_as_h2(*reinterpret_cast<const uint32_t*>(sDv + kb + 2 * t));
             const __half2 d89 = u32_as_h2(*reinterpret_cast<const uint32_t*>(sDv + kb + 2 * t + 8));
-            const uint8_t* vp = sV + ks * 16 * HD;
-            const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vp + v_off0) ^ 0x80808080u;
-            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vp + v_off1) ^ 0x80808080u;
-            const uint32_t w8 = *reinterpret_cast<const uint32_t*>(vp + v_off0 + 8 * HD) ^ 0x80808080u;
-            const uint32_t w9 = *reinterpret_cast<const uint32_t*>(vp + v_off1 + 8 * HD) ^ 0x80808080u;
             uint32_t A[MTW][4];
-            if (HD == 256 || (warp & 1) == 0) {  // dims 4g, 4g+1 (and 4g+2, 4g+3 at hd256)
-                const uint32_t y01 = prmt2<0x5140>(w0, w1), y89 = prmt2<0x5140>(w8, w9);
-                A[0][0] = biased_bytes_to_half2<0x4140>(y01);
-                A[0][1] = biased_bytes_to_half2<0x4342>(y01);
-                A[0][2] = biased_bytes_to_half2<0x4140>(y89);
-                A[0][3] = biased_bytes_to_half2<0x4342>(y89);
-            }
-            if (HD == 256 || (warp & 1) == 1) {  // dims 4g+2, 4g+3
-                const uint32_t y01 = prmt2<0x7362>(w0, w1), y89 = prmt2<0x7362>(w8, w9);
-                A[MTW - 1][0] = biased_bytes_to_half2<0x4140>(y01);
-                A[MTW - 1][1] = biased_bytes_to_half2<0x4342>(y01);
-                A[MTW - 1][2] = biased_bytes_to_half2<0x4140>(y89);
-                A[MTW - 1][3] = biased_bytes_to_half2<0x4342>(y89);
+            if constexpr (V4) {
+                // keys (2t, 2t+1) and (2t+8, 2t+9) side by side: 4 nibbles of each key per half
+                const uint8_t* vp = sV + ks * 16 * V4ROWB;
+                const uint32_t x01 = (uint32_t)*reinterpret_cast<const uint16_t*>(vp + v4_off0) |
+                                     ((uint32_t)*reinterpret_cast<const uint16_t*>(vp + v4_off0 + V4ROWB) << 16);
+                const uint32_t x89 = (uint32_t)*reinterpret_cast<const uint16_t*>(vp + v4_off8) |
+                                     ((uint32_t)*reinterpret_cast<const uint16_t*>(vp + v4_off8 + V4ROWB) << 16);
+                if (HD == 256 || (warp & 1) == 0) {  // dims 4g, 4g+1
+                    A[0][0] = nib_lo_to_half2(x01);
+                    A[0][1] = nib_hi_to_half2(x01);
+                    A[0][2] = nib_lo_to_half2(x89);
+                    A[0][3] = nib_hi_to_half2(x89);
+                }
+                if (HD == 256 || (warp & 1) == 1) {  // dims 4g+2, 4g+3
+                    A[MTW - 1][0] = nib_lo_to_half2(x01 >> 8);
+                    A[MTW - 1][1] = nib_hi_to_half2(x01 >> 8);
+                    A[MTW - 1][2] = nib_lo_to_half2(x89 >> 8);
+                    A[MTW - 1][3] = nib_hi_to_half2(x89 >> 8);
+                }
+            } else {
+                const uint8_t* vp = sV + ks * 16 * HD;
+                const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vp + v_off0) ^ 0x80808080u;
+                const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vp + v_off1) ^ 0x80808080u;
+                const uint32_t w8 = *reinterpret_cast<const uint32_t*>(vp + v_off0 + 8 * HD) ^ 0x80808080u;
+                const uint32_t w9 = *reinterpret_cast<const uint32_t*>(vp + v_off1 + 8 * HD) ^ 0x80808080u;
+                if (HD == 256 || (warp & 1) == 0) {  // dims 4g, 4g+1 (and 4g+2, 4g+3 at hd256)
+                    const uint32_t y01 = prmt2<0x5140>(w0, w1), y89 = prmt2<0x5140>(w8, w9);
+                    A[0][0] = biased_bytes_to_half2<0x4140>(y01);
+                    A[0][1] = biased_bytes_to_half2<0x4342>(y01);
+                    A[0][2] = biased_bytes_to_half2<0x4140>(y89);
+                    A[0][3] = biased_bytes_to_half2<0x4342>(y89);
+                }
+                if (HD == 256 || (warp & 1) == 1) {  // dims 4g+2, 4g+3
+                    const uint32_t y01 = prmt2<0x7362>(w0, w1), y89 = prmt2<0x7362>(w8, w9);
+                    A[MTW - 1][0] = biased_bytes_to_half2<0x4140>(y01);
+                    A[MTW - 1][1] = biased_bytes_to_half2<0x4342>(y01);
+                    A[MTW - 1][2] = biased_bytes_to_half2<0x4140>(y89);
+                    A[MTW - 1][3] = biased_bytes_to_half2<0x4342>(y89);
+                }
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
@@ -638,28 +707,28 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
     }
 }
 
-template <int HD, int NT, bool TREE, bool APPEND>
+template <int HD, int NT, bool TREE, bool APPEND, bool V4>
 int launch_verify(const VerifyParams& vp, const Plan& pl, int n_kv_heads, cudaStream_t stream) {
     constexpr int bytes = Smem<HD, NT>::kBytes;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(verify_split_kernel<HD, NT, TREE, APPEND>,
+        if (cudaFuncSetAttribute(verify_split_kernel<HD, NT, TREE, APPEND, V4>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
             return KVQ8_ERR_CUDA;
         attr_set = true;
     }
     dim3 grid(pl.n_chunks, pl.n_split, n_kv_heads);
-    verify_split_kernel<HD, NT, TREE, APPEND><<<grid, kThreads, bytes, stream>>>(vp);
+    verify_split_kernel<HD, NT, TREE, APPEND, V4><<<grid, kThreads, bytes, stream>>>(vp);
     return launch_status();
 }
 
-template <int HD, bool TREE, bool APPEND>
+template <int HD, bool TREE, bool APPEND, bool V4 = false>
 int dispatch_nt(const VerifyParams& vp, const Plan& pl, int n_kv_heads, cudaStream_t s) {
     switch (pl.nt) {
-        case 1: return launch_verify<HD, 1, TREE, APPEND>(vp, pl, n_kv_heads, s);
-        case 2: return launch_verify<HD, 2, TREE, APPEND>(vp, pl, n_kv_heads, s);
-        case 3: return launch_verify<HD, 3, TREE, APPEND>(vp, pl, n_kv_heads, s);
-        case 4: return launch_verify<HD, 4, TREE, APPEND>(vp, pl, n_kv_heads, s);
+        case 1: return launch_verify<HD, 1, TREE, APPEND, V4>(vp, pl, n_kv_heads, s);
+        case 2: return launch_verify<HD, 2, TREE, APPEND, V4>(vp, pl, n_kv_heads, s);
+        case 3: return launch_verify<HD, 3, TREE, APPEND, V4>(vp, pl, n_kv_heads, s);
+        case 4: return launch_verify<HD, 4, TREE, APPEND, V4>(vp, pl, n_kv_heads, s);
         default: return KVQ8_ERR_UNSUPPORTED;
     }
 }
@@ -684,7 +753,7 @@ namespace {
 int verify_impl(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv, int kv_len, int q_pos0,
                 const uint32_t* wmask, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
                 int n_split, kvq8_stream_t stream, const float* k_new = nullptr, const float* v_new = nullptr,
-                float* part_o = nullptr, float* part_ml = nullptr) {
+                float* part_o = nullptr, float* part_ml = nullptr, bool v4 = false) {
     const bool append = k_new != nullptr;
     const bool partials = part_o != nullptr;
     if (!kv || !q || (!out && !partials) || (partials && !part_ml)) return KVQ8_ERR_INVALID_ARG;
@@ -740,7 +809,10 @@ int verify_impl(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv,
     vp.v_new = v_new;
     cudaStream_t s = (cudaStream_t)stream;
     int r1;
-    if (wmask)  // tree windows have no append variant
+    if (v4)  // K8V4 pools: causal windows, no append
+        r1 = pl.hd == 128 ? dispatch_nt<128, false, false, true>(vp, pl, kv->n_kv_heads, s)
+                          : dispatch_nt<256, false, false, true>(vp, pl, kv->n_kv_heads, s);
+    else if (wmask)  // tree windows have no append variant
         r1 = pl.hd == 128 ? dispatch_nt<128, true, false>(vp, pl, kv->n_kv_heads, s)
                           : dispatch_nt<256, true, false>(vp, pl, kv->n_kv_heads, s);
     else if (append)
@@ -762,6 +834,17 @@ extern "C" int attn_verify_q8(const float* q, int n_rows, int n_q_heads, const k
                               int n_split, kvq8_stream_t stream) {
     return kvq8::verify_impl(q, n_rows, n_q_heads, kv, kv_len, q_pos0, nullptr, softmax_scale, out, workspace,
                              workspace_bytes, n_split, stream);
+}
+
+extern "C" int attn_verify_k8v4(const float* q, int n_rows, int n_q_heads, const kvk8v4_cache* kv, int kv_len,
+                                int q_pos0, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                                int n_split, kvq8_stream_t stream) {
+    if (!kv) return KVQ8_ERR_INVALID_ARG;
+    // the Q8_0 view of the pool: the V plane pointer carries the nibbles
+    const kvq8_cache view = {kv->k_codes, kv->k_scales, reinterpret_cast<const int8_t*>(kv->v_codes), kv->v_scales,
+                             kv->n_kv_heads, kv->head_dim, kv->capacity};
+    return kvq8::verify_impl(q, n_rows, n_q_heads, &view, kv_len, q_pos0, nullptr, softmax_scale, out, workspace,
+                             workspace_bytes, n_split, stream, nullptr, nullptr, nullptr, nullptr, true);
 }
 
 extern "C" int attn_verify_q8_partials_count(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_kv_heads,

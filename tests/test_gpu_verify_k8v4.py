@@ -1,0 +1,142 @@
+"""kvk8v4_append / attn_verify_k8v4 on the GPU against the fp64 oracle's K8V4 pool: the
+append bit for bit (K as Q8_0, V as 4-bit nibbles + fp16 scales), attention within 1e-4."""
+import numpy as np
+import pytest
+
+import oracle
+from speculative_verify_attention_gb300 import workloads
+
+from ._util import VERIFY_TOL, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _pools(inp, capacity=None, pos0=0, junk=True):
+    """The same fp32 K/V appended to a library K8V4 pool and an oracle one; positions outside
+    the written range hold the same junk (finite scales) in both."""
+    import torch
+
+    from speculative_verify_attention_gb300 import KVCacheK8V4
+    L, hkv, hd = inp.k.shape
+    cap = capacity or (pos0 + L)
+    gpu = KVCacheK8V4(hkv, hd, cap, device="cuda")
+    orc = oracle.CacheK8V4(hkv, hd, cap)
+    if junk and cap > pos0 + L:
+        rng = np.random.default_rng(2468)
+        kc = rng.integers(-128, 128, (hkv, cap, hd), dtype=np.int8)
+        vc = rng.integers(0, 256, (hkv, cap, hd // 2), dtype=np.uint8)
+        sc = rng.integers(0, 1 << 16, (hkv, cap, hd // 32), dtype=np.uint16)
+        sc[(sc & 0x7C00) == 0x7C00] = 0x7BFF
+        orc.k_codes[:], orc.v_q4[:], orc.k_scales[:], orc.v_scales[:] = kc, vc, sc, sc
+        gpu.k_codes.copy_(torch.from_numpy(kc))
+        gpu.v_codes.copy_(torch.from_numpy(vc))
+        gpu.k_scales.copy_(torch.from_numpy(sc.view(np.float16)))
+        gpu.v_scales.copy_(torch.from_numpy(sc.view(np.float16)))
+    gpu.append(torch.from_numpy(inp.k).cuda(), torch.from_numpy(inp.v).cuda(), pos0)
+    orc.append(inp.k, inp.v, pos0)
+    torch.cuda.synchronize()
+    return gpu, orc
+
+
+def _run(gpu, q, kv_len, q_pos0, scale, n_split=0):
+    import torch
+
+    from speculative_verify_attention_gb300 import attn_verify_k8v4
+    out = attn_verify_k8v4(torch.from_numpy(np.ascontiguousarray(q, np.float32)).cuda(), gpu, kv_len, q_pos0, scale,
+                           n_split=n_split)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def test_append_matches_oracle_bitwise(lib):
+    inp = workloads.random_small(1300, 8, 2, 256, 45, 4)
+    gpu, orc = _pools(inp, capacity=60, pos0=9)
+    assert np.array_equal(gpu.k_codes.cpu().numpy(), orc.k_codes)
+    assert np.array_equal(gpu.k_scales.cpu().numpy().view(np.uint16), orc.k_scales)
+    assert np.array_equal(gpu.v_codes.cpu().numpy(), orc.v_q4)
+    assert np.array_equal(gpu.v_scales.cpu().numpy().view(np.uint16), orc.v_scales)
+
+
+def test_append_k_plane_equals_q8_append(lib):
+    import torch
+
+    from speculative_verify_attention_gb300 import KVCacheQ8
+    inp = workloads.random_small(1301, 8, 2, 128, 33, 4)
+    gpu, _ = _pools(inp, junk=False)
+    q8 = KVCacheQ8(2, 128, 33, device="cuda")
+    q8.append(torch.from_numpy(inp.k).cuda(), torch.from_numpy(inp.v).cuda(), 0)
+    torch.cuda.synchronize()
+    assert torch.equal(gpu.k_codes, q8.k_codes) and torch.equal(gpu.k_scales, q8.k_scales)
+
+
+@pytest.mark.parametrize("T,n_split", [(4, 0), (8, 0), (16, 0), (32, 0), (4, 3), (8, 1)])
+def test_27b_shape(lib, T, n_split):
+    w = workloads.verify_workload(f"k8v4-24q4kv-hd256-ctx1000-T{T}", 24, 4, 256, 1000, T, k_outliers=4,
+                                  seed=1310 + T)
+    inp = workloads.make_inputs(w)
+    gpu, orc = _pools(inp, capacity=w.kv_len + 30)
+    got = _run(gpu, inp.q, w.kv_len, w.q_pos0, w.softmax_scale, n_split)
+    ref = oracle.attention(orc, inp.q, w.kv_len, w.q_pos0, w.softmax_scale)
+    assert rel_err(got, ref) <= VERIFY_TOL
+
+
+@pytest.mark.parametrize("T", [4, 8, 12, 32])
+def test_hd128_shape(lib, T):
+    w = workloads.verify_workload(f"k8v4-32q8kv-hd128-ctx700-T{T}", 32, 8, 128, 700, T, seed=1350 + T)
+    inp = workloads.make_inputs(w)
+    gpu, orc = _pools(inp, capacity=w.kv_len + 9)
+    got = _run(gpu, inp.q, w.kv_len, w.q_pos0, w.softmax_scale)
+    ref = oracle.attention(orc, inp.q, w.kv_len, w.q_pos0, w.softmax_scale)
+    assert rel_err(got, ref) <= VERIFY_TOL
+
+
+@pytest.mark.parametrize("kv_len,q_pos0,T,hd", [(5, 1, 4, 128), (128, 120, 8, 256), (129, 125, 4, 128),
+                                                (300, 0, 6, 256), (1, 0, 1, 256)])
+def test_edges(lib, kv_len, q_pos0, T, hd):
+    inp = workloads.random_small(1370 + kv_len + hd, 6, 2, hd, kv_len, T)
+    gpu, orc = _pools(inp, capacity=kv_len + 16)
+    got = _run(gpu, inp.q, kv_len, q_pos0, 0.09)
+    ref = oracle.attention(orc, inp.q, kv_len, q_pos0, 0.09)
+    assert rel_err(got, ref) <= VERIFY_TOL
+
+
+def test_full_size_sampled(lib):
+    w = workloads.long_verify(20676, 4)
+    inp = workloads.make_inputs(w)
+    gpu, orc = _pools(inp, junk=False)
+    got = _run(gpu, inp.q, w.kv_len, w.q_pos0, w.softmax_scale)
+    rng = np.random.default_rng(4)
+    sel = [(i, int(rng.integers(w.n_q_heads))) for i in range(w.n_q)]
+    sel += [(int(rng.integers(w.n_q)), h) for h in range(w.n_q_heads)]
+    ref = oracle.attention(orc, inp.q, w.kv_len, w.q_pos0, w.softmax_scale, sel=sel)
+    assert rel_err(np.stack([got[i, h] for i, h in sel]), ref) <= VERIFY_TOL
+    assert np.all(np.isfinite(got))
+
+
+def test_k8v4_rejects_bad_arguments(lib):
+    import ctypes
+
+    import torch
+
+    from speculative_verify_attention_gb300 import KVCacheK8V4
+    from speculative_verify_attention_gb300.binding import (KVQ8_ERR_INVALID_ARG, KVQ8_ERR_MISALIGNED,
+                                                             KVQ8_ERR_WORKSPACE, load_library)
+    lib_ = load_library()
+    cache = KVCacheK8V4(2, 128, 64, device="cuda")
+    q = torch.zeros((4, 8, 128), device="cuda")
+    out = torch.empty_like(q)
+    nb = lib_.attn_verify_q8_workspace_bytes(4, 8, 128, 64, 2, 0)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+
+    def call(qp=q.data_ptr(), kv_len=64, wsb=nb):
+        return lib_.attn_verify_k8v4(qp, 4, 8, ctypes.byref(cache.struct()), kv_len, 60, 0.1, out.data_ptr(),
+                                     ws.data_ptr(), wsb, 0, None)
+
+    assert call() == 0
+    assert call(qp=None) == KVQ8_ERR_INVALID_ARG
+    assert call(kv_len=65) == KVQ8_ERR_INVALID_ARG
+    assert call(qp=q.data_ptr() + 4) == KVQ8_ERR_MISALIGNED
+    assert call(wsb=nb - 1) == KVQ8_ERR_WORKSPACE
+    k = torch.zeros((3, 2, 128), device="cuda")
+    assert lib_.kvk8v4_append(k.data_ptr(), k.data_ptr(), 3, ctypes.byref(cache.struct()), 62, None) == KVQ8_ERR_INVALID_ARG
+    torch.cuda.synchronize()
