@@ -367,6 +367,8 @@ def run_native(args, world, rank, local):
         from speculative_verify_attention_gb300 import workloads as _wl
         torch.cuda.empty_cache()
         prompt["hd128"] = prompt_bench(args, dev, fp16_peak, _wl.PROMPT_HD128)
+        torch.cuda.empty_cache()
+        prompt["k8v4"] = prompt_bench(args, dev, fp16_peak, _wl.PROMPT, pool="k8v4")
     head = head_bench(dev, hbm_peak, args.ring_l2) if not args.no_head else None
 
     result = None
@@ -460,15 +462,17 @@ def head_bench(dev, hbm_peak, ring_l2):
     return res
 
 
-def prompt_bench(args, dev, fp16_peak, w=None):
+def prompt_bench(args, dev, fp16_peak, w=None, pool="q8"):
     import torch
 
-    from speculative_verify_attention_gb300 import (KVCacheQ8, KVQ8Error, attn_prompt_q8,
-                                                    attn_prompt_q8_workspace_bytes, workloads)
+    from speculative_verify_attention_gb300 import (KVCacheK8V4, KVCacheQ8, KVQ8Error, attn_prompt_k8v4,
+                                                    attn_prompt_q8, attn_prompt_q8_workspace_bytes, workloads)
     w = w or workloads.PROMPT
     inp = workloads.make_inputs(w)
-    c = KVCacheQ8(w.n_kv_heads, w.head_dim, w.kv_len, device=dev)
+    c = (KVCacheK8V4 if pool == "k8v4" else KVCacheQ8)(w.n_kv_heads, w.head_dim, w.kv_len, device=dev)
     c.append(torch.from_numpy(inp.k).to(dev), torch.from_numpy(inp.v).to(dev), 0)
+    if pool == "k8v4":
+        attn_prompt_q8 = attn_prompt_k8v4  # noqa: F811  (the same call shape)
     q = torch.from_numpy(inp.q).to(dev)
     out = torch.empty(q.shape, dtype=torch.float32, device=dev)
     ws = torch.empty(attn_prompt_q8_workspace_bytes(w.n_q, w.n_q_heads, w.head_dim, w.kv_len, w.q_pos0,
@@ -491,7 +495,7 @@ def prompt_bench(args, dev, fp16_peak, w=None):
             times.append(a.elapsed_time(b))
     ms = statistics.median(times)
     tf = w.causal_flops() / (ms * 1e-3) / 1e12
-    return {"workload": w.name, "ms_per_call": ms, "tflops": tf, "peak_tflops": fp16_peak,
+    return {"workload": w.name, "pool": pool, "ms_per_call": ms, "tflops": tf, "peak_tflops": fp16_peak,
             "frac": tf / fp16_peak, "peak_source": "fp16 = measured bf16 x 0.951 (cuBLAS fp16/bf16 on GB300)",
             "flops": w.causal_flops(), "calls_timed": n, "l2": "flushed (256 MiB write) before every call"}
 
@@ -704,8 +708,8 @@ def main():
         __graft_entry__.build()
         hbm_peak, bf16_peak, _ = _peaks()
         from speculative_verify_attention_gb300 import workloads as _wl
-        for w in (_wl.PROMPT, _wl.PROMPT_HD128):
-            print(json.dumps(prompt_bench(args, torch.device("cuda", 0), bf16_peak * 0.951, w)), flush=True)
+        for w, pool in ((_wl.PROMPT, "q8"), (_wl.PROMPT_HD128, "q8"), (_wl.PROMPT, "k8v4")):
+            print(json.dumps(prompt_bench(args, torch.device("cuda", 0), bf16_peak * 0.951, w, pool)), flush=True)
         return 0
     if args.impl == "reference":
         return run_reference(args, world, rank)

@@ -235,6 +235,15 @@ int attn_verify_k8v4(const float* q, int n_rows, int n_q_heads, const kvk8v4_cac
                      int n_split, kvq8_stream_t stream);
 
 /*
+ * attn_prompt_k8v4 -- attn_prompt_q8 over a K8V4 pool (the same shapes, workspace from
+ * attn_prompt_q8_workspace_bytes, precision bound and errors); the dequantisers expand the
+ * 4-bit V blocks (value (nibble - 8) * scale, rounded once to fp16) into the V tiles.
+ */
+int attn_prompt_k8v4(const uint16_t* q, int n_q, int n_q_heads, const kvk8v4_cache* kv, int kv_len,
+                     int q_pos0, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                     kvq8_stream_t stream);
+
+/*
  * kvf16_append -- round n_tok tokens of K and V (fp32 [n_tok][n_kv_heads][head_dim], device)
  * to fp16 (nearest even) into both planes of an fp16 pool at positions [pos0, pos0 + n_tok).
  * Errors: INVALID_ARG for null pointers, negative sizes or pos0 + n_tok > capacity;

@@ -179,7 +179,48 @@ __device__ __forceinline__ void dequant_tile(const uint8_t* codes, const uint16_
     }
 }
 
+// The 4-bit V tile of a K8V4 pool (HD/2 bytes per key, element 2m in the low nibble of byte
+// m, value (nibble - 8) * scale) into the same swizzled fp16 tile.  A byte placed in bytes 0
+// and 2 of a word and masked with 0x00F0000F gives, after OR with 0x64006400, the fp16 pair
+// (1024 + lo, 1024 + 16 hi); one fma with (1, 1/16) and (-1032, -72) turns it into the two
+// codes exactly, and one multiply by the scale rounds once, as for Q8_0.
 template <int HD>
+__device__ __forceinline__ void dequant_tile_v4(const uint8_t* codes, const uint16_t* scales, uint8_t* hat, int nk,
+                                                int d) {
+    constexpr int kChunks = PL<HD>::kChunks;  // 16-dim items per tile
+    constexpr int CPK = HD / 16;
+    const __half2 mul = __halves2half2(__ushort_as_half((unsigned short)0x3C00u), __ushort_as_half((unsigned short)0x2C00u));
+    const __half2 add = __halves2half2(__ushort_as_half((unsigned short)0xE408u), __ushort_as_half((unsigned short)0xD480u));
+#pragma unroll
+    for (int k = 0; k < (kChunks + kDeqThreads - 1) / kDeqThreads; ++k) {
+        const int c = d + kDeqThreads * k;
+        if (c >= kChunks) break;
+        const int n = c / CPK, j16 = c % CPK;
+        uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
+        if (n < nk) {
+            const uint2 raw = *reinterpret_cast<const uint2*>(codes + n * (HD / 2) + j16 * 8);
+            const __half2 sc = __half2half2(__ushort_as_half(scales[n * (HD / 32) + (j16 >> 1)]));
+            uint32_t h[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const uint32_t w = m < 4 ? raw.x : raw.y;
+                uint32_t r;
+                asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(w), "r"(0u), "r"(0x4040u | ((m & 3) * 0x0101u)));
+                r = (r & 0x00F0000Fu) | 0x64006400u;
+                const __half2 v = __hmul2(__hfma2(u32_as_h2(r), mul, add), sc);
+                h[m] = h2_as_u32(v);
+            }
+            o0 = make_uint4(h[0], h[1], h[2], h[3]);
+            o1 = make_uint4(h[4], h[5], h[6], h[7]);
+        }
+        const int base = (j16 >> 2) * (BN * 128) + (n >> 3) * 1024 + (n & 7) * 128;
+        const int c0 = 2 * (j16 & 3);
+        *reinterpret_cast<uint4*>(hat + base + ((c0 ^ (n & 7)) << 4)) = o0;
+        *reinterpret_cast<uint4*>(hat + base + (((c0 + 1) ^ (n & 7)) << 4)) = o1;
+    }
+}
+
+template <int HD, bool V4 = false>
 __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptParams p) {
     using L = PL<HD>;
     constexpr int SM_KHAT = L::SM_KHAT, SM_VHAT = L::SM_VHAT, HAT_BYTES = L::HAT_BYTES, SM_STAGE = L::SM_STAGE;
@@ -237,9 +278,10 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptPa
                     // bytes too, at hd128 only 8, so there the dequantisers read them from global
                     // memory instead (a bulk copy wants 16-byte aligned starts and sizes)
                     constexpr int scale_bytes = HD == 256 ? 2 * (HD / 16) : 0;
-                    tc::mbar_arrive_expect_tx(B(B_ST_FULL + s), (uint32_t)(nk * (2 * HD + scale_bytes)));
+                    constexpr int v_row = V4 ? HD / 2 : HD;  // V code bytes per key
+                    tc::mbar_arrive_expect_tx(B(B_ST_FULL + s), (uint32_t)(nk * (HD + v_row + scale_bytes)));
                     tc::bulk_g2s(st + ST_KC, p.kc + row0 * HD, nk * HD, B(B_ST_FULL + s));
-                    tc::bulk_g2s(st + ST_VC, p.vc + row0 * HD, nk * HD, B(B_ST_FULL + s));
+                    tc::bulk_g2s(st + ST_VC, p.vc + row0 * v_row, nk * v_row, B(B_ST_FULL + s));
                     if constexpr (HD == 256) {
                         tc::bulk_g2s(st + ST_KS, p.ks + row0 * (HD / 32), nk * (HD / 16), B(B_ST_FULL + s));
                         tc::bulk_g2s(st + ST_VS, p.vs + row0 * (HD / 32), nk * (HD / 16), B(B_ST_FULL + s));
@@ -466,7 +508,10 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptPa
                     ok = false;
                     break;
                 }
-                dequant_tile<HD>(st + ST_VC, v_sc, smem + SM_VHAT + s * HAT_BYTES, nk, d);
+                if constexpr (V4)
+                    dequant_tile_v4<HD>(st + ST_VC, v_sc, smem + SM_VHAT + s * HAT_BYTES, nk, d);
+                else
+                    dequant_tile<HD>(st + ST_VC, v_sc, smem + SM_VHAT + s * HAT_BYTES, nk, d);
                 tc::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
@@ -532,16 +577,16 @@ int prompt_plan(int n_q, int n_q_heads, int head_dim, int kv_len, int q_pos0, in
     return KVQ8_OK;
 }
 
-template <int HD>
+template <int HD, bool V4>
 int launch_prompt(const PromptParams& pp, int grid, cudaStream_t s) {
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(prompt_attn_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(prompt_attn_kernel<HD, V4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PL<HD>::SMEM_BYTES) != cudaSuccess)
             return KVQ8_ERR_CUDA;
         attr_set = true;
     }
-    prompt_attn_kernel<HD><<<grid, kThreads, PL<HD>::SMEM_BYTES, s>>>(pp);
+    prompt_attn_kernel<HD, V4><<<grid, kThreads, PL<HD>::SMEM_BYTES, s>>>(pp);
     return launch_status();
 }
 
@@ -555,10 +600,12 @@ extern "C" size_t attn_prompt_q8_workspace_bytes(int n_q, int n_q_heads, int hea
     return pl.ws_bytes;
 }
 
-extern "C" int attn_prompt_q8(const uint16_t* q, int n_q, int n_q_heads, const kvq8_cache* kv, int kv_len, int q_pos0,
-                              float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
-                              kvq8_stream_t stream) {
-    using namespace kvq8;
+namespace kvq8 {
+namespace {
+
+int prompt_impl(const uint16_t* q, int n_q, int n_q_heads, const kvq8_cache* kv, int kv_len, int q_pos0,
+                float softmax_scale, float* out, void* workspace, size_t workspace_bytes, kvq8_stream_t stream,
+                bool v4) {
     if (!kv || !q || !out) return KVQ8_ERR_INVALID_ARG;
     if (!kv->k_codes || !kv->k_scales || !kv->v_codes || !kv->v_scales) return KVQ8_ERR_INVALID_ARG;
     if (kv->n_kv_heads < 1 || kv_len > kv->capacity) return KVQ8_ERR_INVALID_ARG;
@@ -595,9 +642,31 @@ extern "C" int attn_prompt_q8(const uint16_t* q, int n_q, int n_q_heads, const k
     pp.units = pl.units;
     pp.scale_log2 = softmax_scale * kLog2e;
     cudaStream_t s = (cudaStream_t)stream;
-    const int r1 = HD == 128 ? launch_prompt<128>(pp, pl.grid, s) : launch_prompt<256>(pp, pl.grid, s);
+    const int r1 = v4 ? (HD == 128 ? launch_prompt<128, true>(pp, pl.grid, s) : launch_prompt<256, true>(pp, pl.grid, s))
+                      : (HD == 128 ? launch_prompt<128, false>(pp, pl.grid, s) : launch_prompt<256, false>(pp, pl.grid, s));
     if (r1 != KVQ8_OK) return r1;
     return launch_combine(pp.part_o, reinterpret_cast<const float*>(pp.part_ml), pl.n_parts, (int)rows_out, HD, out, s);
+}
+
+}  // namespace
+}  // namespace kvq8
+
+extern "C" int attn_prompt_q8(const uint16_t* q, int n_q, int n_q_heads, const kvq8_cache* kv, int kv_len, int q_pos0,
+                              float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                              kvq8_stream_t stream) {
+    return kvq8::prompt_impl(q, n_q, n_q_heads, kv, kv_len, q_pos0, softmax_scale, out, workspace, workspace_bytes,
+                             stream, false);
+}
+
+extern "C" int attn_prompt_k8v4(const uint16_t* q, int n_q, int n_q_heads, const kvk8v4_cache* kv, int kv_len,
+                                int q_pos0, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                                kvq8_stream_t stream) {
+    if (!kv) return KVQ8_ERR_INVALID_ARG;
+    // the Q8_0 view of the pool: the V plane pointer carries the nibbles
+    const kvq8_cache view = {kv->k_codes, kv->k_scales, reinterpret_cast<const int8_t*>(kv->v_codes), kv->v_scales,
+                             kv->n_kv_heads, kv->head_dim, kv->capacity};
+    return kvq8::prompt_impl(q, n_q, n_q_heads, &view, kv_len, q_pos0, softmax_scale, out, workspace, workspace_bytes,
+                             stream, true);
 }
 
 extern "C" int kvq8_device_error(int reset) {

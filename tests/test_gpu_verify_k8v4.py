@@ -140,3 +140,48 @@ def test_k8v4_rejects_bad_arguments(lib):
     k = torch.zeros((3, 2, 128), device="cuda")
     assert lib_.kvk8v4_append(k.data_ptr(), k.data_ptr(), 3, ctypes.byref(cache.struct()), 62, None) == KVQ8_ERR_INVALID_ARG
     torch.cuda.synchronize()
+
+
+def _prompt(gpu, q16, kv_len, q_pos0, scale):
+    import torch
+
+    from speculative_verify_attention_gb300 import attn_prompt_k8v4
+    q = torch.from_numpy(np.ascontiguousarray(q16)).cuda()
+    out = torch.full(q.shape, float("nan"), dtype=torch.float32, device="cuda")
+    attn_prompt_k8v4(q, gpu, kv_len, q_pos0, scale, out=out)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+@pytest.mark.parametrize("hq,hkv,hd,L,nq,pos0,capacity", [
+    (12, 1, 256, 64, 11, 53, None),
+    (12, 1, 256, 200, 50, 150, 203),
+    (24, 2, 256, 512, 64, 448, None),
+    (32, 8, 128, 333, 40, 290, 335),
+    (16, 4, 128, 300, 60, 280, 301),
+])
+def test_prompt_k8v4_small_shapes(lib, hq, hkv, hd, L, nq, pos0, capacity):
+    from ._util import PROMPT_TOL
+    inp = workloads.random_small(1400 + hq + L, hq, hkv, hd, L, nq, q_dtype="f16")
+    gpu, orc = _pools(inp, capacity=capacity)
+    scale = 1.0 / float(np.sqrt(hd))
+    got = _prompt(gpu, inp.q, L, pos0, scale)
+    ref = oracle.attention(orc, inp.q, L, pos0, scale)
+    assert np.all(np.isfinite(got))
+    assert rel_err(got, ref) <= PROMPT_TOL
+
+
+def test_prompt_k8v4_full_workload_sampled(lib):
+    from ._util import PROMPT_TOL
+    from speculative_verify_attention_gb300 import kvq8_device_error
+    w = workloads.PROMPT
+    inp = workloads.make_inputs(w)
+    gpu, orc = _pools(inp, junk=False)
+    got = _prompt(gpu, inp.q, w.kv_len, w.q_pos0, w.softmax_scale)
+    rng = np.random.default_rng(8)
+    sel = [(int(i), int(rng.integers(w.n_q_heads))) for i in rng.integers(0, w.n_q, 30)]
+    sel += [(0, h) for h in range(w.n_q_heads)] + [(w.n_q - 1, h) for h in range(w.n_q_heads)]
+    ref = oracle.attention(orc, inp.q, w.kv_len, w.q_pos0, w.softmax_scale, sel=sel)
+    assert np.all(np.isfinite(got))
+    assert rel_err(np.stack([got[i, h] for i, h in sel]), ref) <= PROMPT_TOL
+    assert kvq8_device_error(reset=True) == 0
