@@ -369,6 +369,8 @@ def run_native(args, world, rank, local):
         prompt["hd128"] = prompt_bench(args, dev, fp16_peak, _wl.PROMPT_HD128)
         torch.cuda.empty_cache()
         prompt["k8v4"] = prompt_bench(args, dev, fp16_peak, _wl.PROMPT, pool="k8v4")
+        torch.cuda.empty_cache()
+        prompt["f16"] = prompt_bench(args, dev, fp16_peak, _wl.PROMPT, pool="f16")
     head = head_bench(dev, hbm_peak, args.ring_l2) if not args.no_head else None
 
     result = None
@@ -465,14 +467,15 @@ def head_bench(dev, hbm_peak, ring_l2):
 def prompt_bench(args, dev, fp16_peak, w=None, pool="q8"):
     import torch
 
-    from speculative_verify_attention_gb300 import (KVCacheK8V4, KVCacheQ8, KVQ8Error, attn_prompt_k8v4,
-                                                    attn_prompt_q8, attn_prompt_q8_workspace_bytes, workloads)
+    from speculative_verify_attention_gb300 import (KVCacheF16, KVCacheK8V4, KVCacheQ8, KVQ8Error, attn_prompt_f16,
+                                                    attn_prompt_k8v4, attn_prompt_q8, attn_prompt_q8_workspace_bytes,
+                                                    workloads)
     w = w or workloads.PROMPT
     inp = workloads.make_inputs(w)
-    c = (KVCacheK8V4 if pool == "k8v4" else KVCacheQ8)(w.n_kv_heads, w.head_dim, w.kv_len, device=dev)
+    pool_cls = {"q8": KVCacheQ8, "k8v4": KVCacheK8V4, "f16": KVCacheF16}[pool]
+    c = pool_cls(w.n_kv_heads, w.head_dim, w.kv_len, device=dev)
     c.append(torch.from_numpy(inp.k).to(dev), torch.from_numpy(inp.v).to(dev), 0)
-    if pool == "k8v4":
-        attn_prompt_q8 = attn_prompt_k8v4  # noqa: F811  (the same call shape)
+    attn_prompt_q8 = {"q8": attn_prompt_q8, "k8v4": attn_prompt_k8v4, "f16": attn_prompt_f16}[pool]  # same call shape
     q = torch.from_numpy(inp.q).to(dev)
     out = torch.empty(q.shape, dtype=torch.float32, device=dev)
     ws = torch.empty(attn_prompt_q8_workspace_bytes(w.n_q, w.n_q_heads, w.head_dim, w.kv_len, w.q_pos0,
@@ -708,7 +711,8 @@ def main():
         __graft_entry__.build()
         hbm_peak, bf16_peak, _ = _peaks()
         from speculative_verify_attention_gb300 import workloads as _wl
-        for w, pool in ((_wl.PROMPT, "q8"), (_wl.PROMPT_HD128, "q8"), (_wl.PROMPT, "k8v4")):
+        for w, pool in ((_wl.PROMPT, "q8"), (_wl.PROMPT_HD128, "q8"), (_wl.PROMPT, "k8v4"), (_wl.PROMPT, "f16"),
+                        (_wl.PROMPT_HD128, "f16")):
             print(json.dumps(prompt_bench(args, torch.device("cuda", 0), bf16_peak * 0.951, w, pool)), flush=True)
         return 0
     if args.impl == "reference":

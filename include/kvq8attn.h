@@ -244,6 +244,16 @@ int attn_prompt_k8v4(const uint16_t* q, int n_q, int n_q_heads, const kvk8v4_cac
                      kvq8_stream_t stream);
 
 /*
+ * attn_prompt_f16 -- attn_prompt_q8 over an fp16 pool (the same shapes, workspace from
+ * attn_prompt_q8_workspace_bytes, precision bound and errors).  The K and V tiles are loaded
+ * straight into the tensor-core operand layout by tensor copies over (head_dim, kv_len,
+ * n_kv_heads), so keys at or past kv_len read as zeros; the caller's pool needs no padding.
+ */
+int attn_prompt_f16(const uint16_t* q, int n_q, int n_q_heads, const kvf16_cache* kv, int kv_len,
+                    int q_pos0, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                    kvq8_stream_t stream);
+
+/*
  * kvf16_append -- round n_tok tokens of K and V (fp32 [n_tok][n_kv_heads][head_dim], device)
  * to fp16 (nearest even) into both planes of an fp16 pool at positions [pos0, pos0 + n_tok).
  * Errors: INVALID_ARG for null pointers, negative sizes or pos0 + n_tok > capacity;

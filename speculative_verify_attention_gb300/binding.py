@@ -31,7 +31,7 @@ EXPORTED = ("kvq8_quantize", "kvq8_append", "attn_verify_q8_workspace_bytes", "a
             "attn_verify_append_q8_workspace_bytes", "attn_verify_append_q8", "attn_verify_q8_partials_count",
             "attn_verify_q8_partials", "attn_verify_append_q8_host_scratch_bytes", "attn_verify_append_q8_host",
             "kvf16_append", "attn_verify_f16_workspace_bytes", "attn_verify_f16", "kvk8v4_append", "attn_verify_k8v4",
-            "attn_prompt_k8v4", "attn_combine",
+            "attn_prompt_k8v4", "attn_prompt_f16", "attn_combine",
             "attn_prompt_q8_workspace_bytes", "attn_prompt_q8", "attn_verify_q8_noalloc", "kvq8_device_error", "kvq8_status_str",
             "argmax_rows_top_prob_workspace_bytes", "argmax_rows_top_prob")
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
@@ -108,6 +108,8 @@ def load_library():
         lib.attn_verify_f16_workspace_bytes.restype = sz
         lib.attn_verify_f16.argtypes = [vp, i32, i32, cf, i32, i32, f32, vp, vp, sz, i32, vp]
         lib.attn_verify_f16.restype = i32
+        lib.attn_prompt_f16.argtypes = [vp, i32, i32, cf, i32, i32, f32, vp, vp, sz, vp]
+        lib.attn_prompt_f16.restype = i32
         lib.attn_verify_append_q8_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.attn_verify_append_q8_workspace_bytes.restype = sz
         lib.attn_verify_append_q8.argtypes = [vp, vp, vp, i32, i32, cp, i32, f32, vp, vp, sz, i32, vp]
@@ -310,6 +312,25 @@ def attn_verify_f16(q: torch.Tensor, cache: KVCacheF16, kv_len: int, q_pos0: int
                                         int(q_pos0), float(softmax_scale), _ptr(out), _ptr(workspace),
                                         workspace.numel() * workspace.element_size(), int(n_split), _stream(stream))
     _check("attn_verify_f16", st)
+    return out
+
+
+def attn_prompt_f16(q: torch.Tensor, cache: KVCacheF16, kv_len: int, q_pos0: int, softmax_scale: float,
+                    out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """Prompt-chunk attention of fp16 q [n_q][Hq][hd] over an fp16 pool; returns fp32 [n_q][Hq][hd]."""
+    _need(q, "q", torch.float16)
+    n_q, n_q_heads, head_dim = q.shape
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32)
+    if workspace is None:
+        nbytes = attn_prompt_q8_workspace_bytes(n_q, n_q_heads, head_dim, kv_len, q_pos0, cache.n_kv_heads)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    st = load_library().attn_prompt_f16(_ptr(q), n_q, n_q_heads, ctypes.byref(cache.struct()), int(kv_len),
+                                        int(q_pos0), float(softmax_scale), _ptr(out), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("attn_prompt_f16", st)
     return out
 
 

@@ -26,6 +26,10 @@
 // Barriers that many threads signal take one arrival per warp (after __syncwarp), not one
 // per thread.  Every mbarrier wait is bounded: on timeout the kernel records an error flag (read with
 // kvq8_device_error) and returns after releasing its tensor memory.
+#include <cuda.h>  // CUtensorMap and its encoding enums (the encoder itself is fetched at run time)
+
+#include <mutex>
+
 #include "common.cuh"
 #include "tc.cuh"
 
@@ -86,7 +90,13 @@ struct PromptParams {
     int n_q, n_q_heads, group, capacity, kv_len, q_pos0, rows, n_mtiles, n_items, n_parts;
     long long units;   // total 64-key tiles over all (KV head, row tile) items
     float scale_log2;
+    // fp16 pools: 3-D tensor maps (dims, keys < kv_len, KV heads) of the K and V planes with a
+    // 64-dim x 64-key box and the 128-byte swizzle of the K^/V^ tiles
+    CUtensorMap tmap_k, tmap_v;
 };
+
+// Pool formats of the prompt kernel.
+enum { kPoolQ8 = 0, kPoolK8V4 = 1, kPoolF16 = 2 };
 
 // Geometry of one work item: rows [r0, r0 + rows_here) of KV head kvh see keys < key_hi;
 // every row sees at least the keys < key_lo.
@@ -220,8 +230,21 @@ __device__ __forceinline__ void dequant_tile_v4(const uint8_t* codes, const uint
     }
 }
 
-template <int HD, bool V4 = false>
-__global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptParams p) {
+// One box of a 3-D tensor map into shared memory, completion counted on `mbar` in bytes.
+// x (the dim coordinate) is a multiple of 64 fp16 = 128 bytes, as a tiled copy requires.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(mbar)
+        : "memory");
+}
+
+// POOL: kPoolQ8, kPoolK8V4 (4-bit V codes) or kPoolF16 (the producer loads the fp16 tiles
+// straight into K^ and V^ with tensor copies; no staging and no dequantisation).
+template <int HD, int POOL = kPoolQ8>
+__global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_constant__ PromptParams p) {
+    constexpr bool V4 = POOL == kPoolK8V4, F16 = POOL == kPoolF16;
     using L = PL<HD>;
     constexpr int SM_KHAT = L::SM_KHAT, SM_VHAT = L::SM_VHAT, HAT_BYTES = L::HAT_BYTES, SM_STAGE = L::SM_STAGE;
     constexpr int STAGE_BYTES = L::STAGE_BYTES, SM_BAR = L::SM_BAR, SM_TMEM_SLOT = L::SM_TMEM_SLOT, SM_SEG = L::SM_SEG;
@@ -242,8 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptPa
         for (int s = 0; s < 2; ++s) {
             tc::mbar_init(B(B_ST_FULL + s), 1);
             tc::mbar_init(B(B_ST_EMPTY + s), kDeqThreads / 32);  // one arrival per warp
-            tc::mbar_init(B(B_K_FULL + s), kDeqThreads / 32);
-            tc::mbar_init(B(B_V_FULL + s), kDeqThreads / 32);
+            tc::mbar_init(B(B_K_FULL + s), F16 ? 1 : kDeqThreads / 32);  // F16: the producer's expect_tx
+            tc::mbar_init(B(B_V_FULL + s), F16 ? 1 : kDeqThreads / 32);
             tc::mbar_init(B(B_K_EMPTY + s), 1);
             tc::mbar_init(B(B_V_EMPTY + s), 1);
             tc::mbar_init(B(B_S_FULL + s), 1);
@@ -260,7 +283,38 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptPa
     const uint32_t tmem = *tmem_slot;
     const int n_seg = *n_seg_slot;
 
-    if (warp == 0) {
+    if (warp == 0 && F16) {
+        // ---------------------------------------------------------------- producer (fp16 pool)
+        if (lane == 0) {
+            constexpr uint32_t plane_bytes = (uint32_t)(HD / 64) * BN * 128;  // full boxes, past-the-end keys zero-filled
+            int j = 0;
+            bool ok = true;
+            for (int si = 0; ok && si < n_seg; ++si) {
+                const Item g = item_geometry(seg[si].item, p.n_mtiles, p.rows, p.group, p.kv_len, p.q_pos0);
+                for (int t = seg[si].t0; t < seg[si].t1; ++t, ++j) {
+                    const int b = j & 1, use = j >> 1;
+                    const int key0 = t * BN;
+                    // K^ of buffer b is free once the QK that read it two tiles ago has completed
+                    if (j >= 2 && !tc::mbar_wait(B(B_K_EMPTY + b), (use - 1) & 1, kWaitLimit)) { ok = false; break; }
+                    tc::mbar_arrive_expect_tx(B(B_K_FULL + b), plane_bytes);
+                    for (int a = 0; a < HD / 64; ++a)
+                        tma_load_3d(sbase + SM_KHAT + b * HAT_BYTES + a * (BN * 128), &p.tmap_k, 64 * a, key0, g.kvh,
+                                    B(B_K_FULL + b));
+                    if (j >= 2 && !tc::mbar_wait(B(B_V_EMPTY + b), (use - 1) & 1, kWaitLimit)) { ok = false; break; }
+                    tc::mbar_arrive_expect_tx(B(B_V_FULL + b), plane_bytes);
+                    for (int a = 0; a < HD / 64; ++a)
+                        tma_load_3d(sbase + SM_VHAT + b * HAT_BYTES + a * (BN * 128), &p.tmap_v, 64 * a, key0, g.kvh,
+                                    B(B_V_FULL + b));
+                }
+            }
+            if (!ok) flag_timeout();
+            // never leave the block while a copy into its shared memory is in flight
+            for (int i = max(0, j - 2); i < j; ++i) {
+                if (!tc::mbar_wait(B(B_K_FULL + (i & 1)), (i >> 1) & 1, kWaitLimit)) flag_timeout();
+                if (!tc::mbar_wait(B(B_V_FULL + (i & 1)), (i >> 1) & 1, kWaitLimit)) flag_timeout();
+            }
+        }
+    } else if (warp == 0) {
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
             int j = 0;
@@ -480,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptPa
             }
         }
         if (!ok) flag_timeout();
-    } else {
+    } else if (!F16) {
         // ---------------------------------------------------------------- dequantisers
         const int d = threadIdx.x - kDeqWarp0 * 32;
         int j = 0;
@@ -577,17 +631,49 @@ int prompt_plan(int n_q, int n_q_heads, int head_dim, int kv_len, int q_pos0, in
     return KVQ8_OK;
 }
 
-template <int HD, bool V4>
+template <int HD, int POOL>
 int launch_prompt(const PromptParams& pp, int grid, cudaStream_t s) {
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(prompt_attn_kernel<HD, V4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(prompt_attn_kernel<HD, POOL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PL<HD>::SMEM_BYTES) != cudaSuccess)
             return KVQ8_ERR_CUDA;
         attr_set = true;
     }
-    prompt_attn_kernel<HD, V4><<<grid, kThreads, PL<HD>::SMEM_BYTES, s>>>(pp);
+    prompt_attn_kernel<HD, POOL><<<grid, kThreads, PL<HD>::SMEM_BYTES, s>>>(pp);
     return launch_status();
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// Tensor map of one fp16 plane [n_kv_heads][capacity][hd]: dims (hd, kv_len, n_kv_heads), so
+// keys at or past kv_len read as zeros; box 64 dims x 64 keys x 1 head, 128-byte swizzle.
+bool encode_f16_plane(CUtensorMap* map, const uint16_t* plane, int hd, int kv_len, int n_kv_heads, int capacity) {
+    const EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)kv_len, (cuuint64_t)n_kv_heads};
+    const cuuint64_t strides[2] = {(cuuint64_t)hd * 2, (cuuint64_t)capacity * hd * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)BN, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t*>(plane), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -603,18 +689,21 @@ extern "C" size_t attn_prompt_q8_workspace_bytes(int n_q, int n_q_heads, int hea
 namespace kvq8 {
 namespace {
 
+// kv: the pool's planes seen as a kvq8_cache (for an fp16 pool k_codes / v_codes carry the fp16
+// planes and there are no scales).
 int prompt_impl(const uint16_t* q, int n_q, int n_q_heads, const kvq8_cache* kv, int kv_len, int q_pos0,
                 float softmax_scale, float* out, void* workspace, size_t workspace_bytes, kvq8_stream_t stream,
-                bool v4) {
+                int pool) {
     if (!kv || !q || !out) return KVQ8_ERR_INVALID_ARG;
-    if (!kv->k_codes || !kv->k_scales || !kv->v_codes || !kv->v_scales) return KVQ8_ERR_INVALID_ARG;
+    if (!kv->k_codes || !kv->v_codes) return KVQ8_ERR_INVALID_ARG;
+    if (pool != kPoolF16 && (!kv->k_scales || !kv->v_scales)) return KVQ8_ERR_INVALID_ARG;
     if (kv->n_kv_heads < 1 || kv_len > kv->capacity) return KVQ8_ERR_INVALID_ARG;
     if (!(softmax_scale > 0.0f) || softmax_scale == INFINITY) return KVQ8_ERR_INVALID_ARG;
     PromptPlan pl;
     const int rc = prompt_plan(n_q, n_q_heads, kv->head_dim, kv_len, q_pos0, kv->n_kv_heads, &pl);
     if (rc != KVQ8_OK) return rc;
-    if (!aligned16(q) || !aligned16(out) || !aligned16(kv->k_codes) || !aligned16(kv->k_scales) ||
-        !aligned16(kv->v_codes) || !aligned16(kv->v_scales))
+    if (!aligned16(q) || !aligned16(out) || !aligned16(kv->k_codes) || !aligned16(kv->v_codes) ||
+        (pool != kPoolF16 && (!aligned16(kv->k_scales) || !aligned16(kv->v_scales))))
         return KVQ8_ERR_MISALIGNED;
     if (!workspace || workspace_bytes < pl.ws_bytes) return KVQ8_ERR_WORKSPACE;
     if (!aligned16(workspace)) return KVQ8_ERR_MISALIGNED;
@@ -641,9 +730,21 @@ int prompt_impl(const uint16_t* q, int n_q, int n_q_heads, const kvq8_cache* kv,
     pp.n_parts = pl.n_parts;
     pp.units = pl.units;
     pp.scale_log2 = softmax_scale * kLog2e;
+    if (pool == kPoolF16) {
+        const uint16_t* kp = reinterpret_cast<const uint16_t*>(kv->k_codes);
+        const uint16_t* vp = reinterpret_cast<const uint16_t*>(kv->v_codes);
+        if (!encode_f16_plane(&pp.tmap_k, kp, HD, kv_len, kv->n_kv_heads, kv->capacity) ||
+            !encode_f16_plane(&pp.tmap_v, vp, HD, kv_len, kv->n_kv_heads, kv->capacity))
+            return KVQ8_ERR_CUDA;
+    }
     cudaStream_t s = (cudaStream_t)stream;
-    const int r1 = v4 ? (HD == 128 ? launch_prompt<128, true>(pp, pl.grid, s) : launch_prompt<256, true>(pp, pl.grid, s))
-                      : (HD == 128 ? launch_prompt<128, false>(pp, pl.grid, s) : launch_prompt<256, false>(pp, pl.grid, s));
+    int r1;
+    if (pool == kPoolF16)
+        r1 = HD == 128 ? launch_prompt<128, kPoolF16>(pp, pl.grid, s) : launch_prompt<256, kPoolF16>(pp, pl.grid, s);
+    else if (pool == kPoolK8V4)
+        r1 = HD == 128 ? launch_prompt<128, kPoolK8V4>(pp, pl.grid, s) : launch_prompt<256, kPoolK8V4>(pp, pl.grid, s);
+    else
+        r1 = HD == 128 ? launch_prompt<128, kPoolQ8>(pp, pl.grid, s) : launch_prompt<256, kPoolQ8>(pp, pl.grid, s);
     if (r1 != KVQ8_OK) return r1;
     return launch_combine(pp.part_o, reinterpret_cast<const float*>(pp.part_ml), pl.n_parts, (int)rows_out, HD, out, s);
 }
@@ -655,7 +756,7 @@ extern "C" int attn_prompt_q8(const uint16_t* q, int n_q, int n_q_heads, const k
                               float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
                               kvq8_stream_t stream) {
     return kvq8::prompt_impl(q, n_q, n_q_heads, kv, kv_len, q_pos0, softmax_scale, out, workspace, workspace_bytes,
-                             stream, false);
+                             stream, kvq8::kPoolQ8);
 }
 
 extern "C" int attn_prompt_k8v4(const uint16_t* q, int n_q, int n_q_heads, const kvk8v4_cache* kv, int kv_len,
@@ -666,7 +767,18 @@ extern "C" int attn_prompt_k8v4(const uint16_t* q, int n_q, int n_q_heads, const
     const kvq8_cache view = {kv->k_codes, kv->k_scales, reinterpret_cast<const int8_t*>(kv->v_codes), kv->v_scales,
                              kv->n_kv_heads, kv->head_dim, kv->capacity};
     return kvq8::prompt_impl(q, n_q, n_q_heads, &view, kv_len, q_pos0, softmax_scale, out, workspace, workspace_bytes,
-                             stream, true);
+                             stream, kvq8::kPoolK8V4);
+}
+
+extern "C" int attn_prompt_f16(const uint16_t* q, int n_q, int n_q_heads, const kvf16_cache* kv, int kv_len, int q_pos0,
+                               float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                               kvq8_stream_t stream) {
+    if (!kv) return KVQ8_ERR_INVALID_ARG;
+    // the fp16 planes ride in the code pointers of a scale-less view
+    const kvq8_cache view = {reinterpret_cast<const int8_t*>(kv->k), nullptr, reinterpret_cast<const int8_t*>(kv->v),
+                             nullptr, kv->n_kv_heads, kv->head_dim, kv->capacity};
+    return kvq8::prompt_impl(q, n_q, n_q_heads, &view, kv_len, q_pos0, softmax_scale, out, workspace, workspace_bytes,
+                             stream, kvq8::kPoolF16);
 }
 
 extern "C" int kvq8_device_error(int reset) {

@@ -125,3 +125,58 @@ def test_f16_rejects_bad_arguments(lib):
     assert lib_.kvf16_append(k.data_ptr(), k.data_ptr(), 3, ctypes.byref(cache.struct()), 62, None) == KVQ8_ERR_INVALID_ARG
     assert lib_.kvf16_append(k.data_ptr() + 4, k.data_ptr(), 3, ctypes.byref(cache.struct()), 0, None) == KVQ8_ERR_MISALIGNED
     torch.cuda.synchronize()
+
+
+def _prompt_f16(gpu, q16, kv_len, q_pos0, scale):
+    import torch
+
+    from speculative_verify_attention_gb300 import attn_prompt_f16
+    q = torch.from_numpy(np.ascontiguousarray(q16)).cuda()
+    out = torch.full(q.shape, float("nan"), dtype=torch.float32, device="cuda")
+    attn_prompt_f16(q, gpu, kv_len, q_pos0, scale, out=out)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+@pytest.mark.parametrize("hq,hkv,hd,L,nq,pos0,capacity", [
+    (12, 1, 256, 64, 11, 53, None),
+    (12, 1, 256, 200, 50, 150, 203),     # ragged last tile
+    (24, 2, 256, 512, 64, 448, None),
+    (32, 8, 128, 333, 40, 290, 335),
+    (16, 4, 128, 300, 60, 280, 301),     # rows past kv_len
+    (12, 1, 256, 1, 1, 0, 9),            # a single key
+])
+def test_prompt_f16_small_shapes(lib, hq, hkv, hd, L, nq, pos0, capacity):
+    """Positions past kv_len hold NaN: the tensor copies are bounded by kv_len, so those keys
+    arrive as zeros and never reach the output."""
+    import torch
+
+    from ._util import PROMPT_TOL
+    inp = workloads.random_small(1500 + hq + L, hq, hkv, hd, L, nq, q_dtype="f16")
+    gpu, orc = _pools(inp, capacity=capacity, junk=False)
+    if capacity and capacity > L:
+        gpu.k[:, L:] = float("nan")
+        gpu.v[:, L:] = float("nan")
+        torch.cuda.synchronize()
+    scale = 1.0 / float(np.sqrt(hd))
+    got = _prompt_f16(gpu, inp.q, L, pos0, scale)
+    ref = oracle.attention(orc, inp.q, L, pos0, scale)
+    assert np.all(np.isfinite(got))
+    assert rel_err(got, ref) <= PROMPT_TOL
+
+
+def test_prompt_f16_full_workload_sampled(lib):
+    from speculative_verify_attention_gb300 import kvq8_device_error
+
+    from ._util import PROMPT_TOL
+    w = workloads.PROMPT
+    inp = workloads.make_inputs(w)
+    gpu, orc = _pools(inp, junk=False)
+    got = _prompt_f16(gpu, inp.q, w.kv_len, w.q_pos0, w.softmax_scale)
+    rng = np.random.default_rng(9)
+    sel = [(int(i), int(rng.integers(w.n_q_heads))) for i in rng.integers(0, w.n_q, 30)]
+    sel += [(0, h) for h in range(w.n_q_heads)] + [(w.n_q - 1, h) for h in range(w.n_q_heads)]
+    ref = oracle.attention(orc, inp.q, w.kv_len, w.q_pos0, w.softmax_scale, sel=sel)
+    assert np.all(np.isfinite(got))
+    assert rel_err(np.stack([got[i, h] for i, h in sel]), ref) <= PROMPT_TOL
+    assert kvq8_device_error(reset=True) == 0
