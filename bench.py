@@ -697,6 +697,8 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="per-cell verify sweep instead of the headline line")
     ap.add_argument("--prompt-only", action="store_true", help="time only the prompt-chunk kernel")
     ap.add_argument("--sweep-filter", default="")
+    ap.add_argument("--prompt-filter", default="", help="with --prompt-only: time only the cells whose "
+                    "'<pool>-<workload>' name contains this")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -713,6 +715,8 @@ def main():
         from speculative_verify_attention_gb300 import workloads as _wl
         for w, pool in ((_wl.PROMPT, "q8"), (_wl.PROMPT_HD128, "q8"), (_wl.PROMPT, "k8v4"), (_wl.PROMPT, "f16"),
                         (_wl.PROMPT_HD128, "f16")):
+            if args.prompt_filter and args.prompt_filter not in f"{pool}-{w.name}":
+                continue
             print(json.dumps(prompt_bench(args, torch.device("cuda", 0), bf16_peak * 0.951, w, pool)), flush=True)
         return 0
     if args.impl == "reference":
