@@ -8,7 +8,8 @@
 // 16-byte load), a 3-step shuffle max, then per value an IEEE fp32 division and round
 // half away from zero (q8_0_block).  Bandwidth-bound: 4 bytes read, 1 + 1/16 bytes
 // written per value.
-// kvq8_append writes both planes (K and V) of a cache in one launch.
+// kvq8_append writes both planes (K and V) of a cache in one launch; kvk8v4_append does the
+// same for a K8V4 pool (K as Q8_0, V as 4-bit blocks, q4_block).
 #include "common.cuh"
 #include "q8_0.cuh"
 

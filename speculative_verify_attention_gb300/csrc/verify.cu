@@ -6,24 +6,30 @@
 // int8-KV QSA prompt attention", How: fp16 hi + lo split of q and p with fp32 accumulation,
 // online softmax, V scale folded into p.
 //
-// GB300 design (one thread block of 4 warps per (row chunk, context slice, KV head)):
+// GB300 design (one thread block of 8 warps per (row chunk, context slice, KV head); the
+// chunks and slices come from verify_plan.cuh):
 //   * K/V codes and scales of a 128-key tile are staged in shared memory with 16-byte
 //     cp.async copies into an XOR-swizzled layout (conflict-free fragment reads).  K of the
 //     next tile streams in while the softmax and PV of this tile run, and V while QK runs,
 //     so every K/V byte of the slice crosses HBM once for all T x group rows.
 //   * QK runs transposed on the tensor cores (m16n8k16, fp32 accumulate): keys are the M
-//     dimension (16 per fragment) and query rows the N dimension (8 per fragment), so a
-//     window of 4 rows x group 6 = 24 rows needs no padding.  int8 codes become fp16
-//     exactly in registers (byte permute + magic-bias subtract); q enters as fp16 hi + lo,
-//     both accumulated into the same fragment; the K scale, which varies along the
-//     contraction in 32-value blocks, is applied after each 32-deep step: s += dK * (q.k)_b.
-//   * Online softmax in base 2 (q pre-scaled by softmax_scale * log2 e), one cross-warp
-//     max per tile.
+//     dimension (16 per fragment, 16 keys per warp) and query rows the N dimension (8 per
+//     fragment), so a window of 4 rows x group 6 = 24 rows needs no padding.  int8 codes
+//     become fp16 exactly in registers (byte permute + magic-bias subtract); q enters as
+//     fp16 hi + lo, both accumulated into the same fragment; the K scale, which varies along
+//     the contraction in 32-value blocks, is applied after each 32-deep step:
+//     s += dK * (q.k)_b.
+//   * Online softmax in base 2 (q pre-scaled by softmax_scale * log2 e) with a lazy
+//     reference maximum per row: the exact cross-warp maxima and the O rescale run only on
+//     tiles where some score passes its row's reference by more than 2^kLazy.
 //   * PV runs transposed too (M = 16 output dims, N = 8 rows, K = 16 keys).  Each warp owns
-//     32-dim output blocks; its B fragments are w = p * dV[n][block] * 2^E split into fp16
-//     hi + lo, with E a per-warp power of two that keeps w inside the fp16 normal range
-//     (the accumulator is rescaled when E changes, and divided by 2^E at the end).
+//     a 32-dim output block (hd256) or half of one (hd128); its B fragments are
+//     w = p * dV[n][block] * 2^E split into fp16 hi + lo, with E a per-warp power of two that
+//     keeps w inside the fp16 normal range (the accumulator is rescaled when E changes).
 //   * Each slice writes an unnormalised partial (o, m, l); attn_combine merges them.
+// Instantiations: TREE (tree-shaped windows from per-row masks), APPEND (the window slice
+// quantises the T new tokens itself, attn_verify_append_q8), V4 (K8V4 pools: 4-bit V
+// codes expanded in registers).  attn_verify_q8_partials stops after the partials.
 #include <algorithm>
 
 #include "common.cuh"
