@@ -121,18 +121,29 @@ def _max_over_ranks(x: float, world: int) -> float:
     return multigpu.max_over_ranks(x, device="cuda" if world > 1 else None)
 
 
+def kernel_source_digest(kernel_files) -> str:
+    """sha256 of the kernel sources' code with comments and blank lines removed, so that an
+    edit of comments alone keeps a capture valid while any change of code invalidates it."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for name in kernel_files:
+        with open(os.path.join(ROOT, "speculative_verify_attention_gb300", "csrc", name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("\n".join(line.rstrip() for line in text.splitlines() if line.strip()).encode())
+    return h.hexdigest()
+
+
 def _kernel_traffic(kernel_files, workload: str):
     """DRAM bytes per launch from the committed ncu capture of `workload`, if the kernel
-    sources are still the ones that capture measured (else None: the counters are stale)."""
-    import hashlib
+    code is still the code that capture measured (else None: the counters are stale)."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             entry = json.load(f)[workload]
-        h = hashlib.sha256()
-        for name in kernel_files:
-            with open(os.path.join(ROOT, "speculative_verify_attention_gb300", "csrc", name), "rb") as f:
-                h.update(f.read())
-        return float(entry["dram_bytes_per_launch"]) if entry.get("source_sha256") == h.hexdigest() else None
+        ok = entry.get("code_sha256") == kernel_source_digest(kernel_files)
+        return float(entry["dram_bytes_per_launch"]) if ok else None
     except Exception:
         return None
 
