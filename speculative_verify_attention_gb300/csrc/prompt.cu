@@ -43,15 +43,18 @@ int launch_combine(const float* part_o, const float* part_ml, int n_split, int r
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 64;
+// keys per tile: 64 at hd256, 128 at hd128 (where a 64-key tile leaves the tensor core idle
+// behind the per-row softmax)
+__host__ __device__ constexpr int bn_for(int hd) { return hd == 128 ? 128 : 64; }
 constexpr int kSoftWarp0 = 2, kDeqWarp0 = 6, kDeqThreads = 320;
 constexpr int kThreads = (kDeqWarp0 + kDeqThreads / 32) * 32;   // 512: 128 registers per thread fill the SM
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kMaxSegments = 8;
 
-// tensor memory columns (the same map at hd128, where Q and O use half of theirs)
-constexpr uint32_t TM_Q = 0, TM_O = 128, TM_S0 = 384, TM_NCOLS = 512;
+// tensor memory columns: Q (hd/2 columns of fp16 pairs) at 0, O (hd fp32 columns) at 128, then
+// two S buffers of BN columns (384 + 2 x 64 at hd256, 256 + 2 x 128 at hd128)
+constexpr uint32_t TM_Q = 0, TM_O = 128, TM_NCOLS = 512;
 
 enum { B_ST_FULL = 0, B_ST_EMPTY = 2, B_K_FULL = 4, B_V_FULL = 6, B_K_EMPTY = 8, B_V_EMPTY = 10, B_S_FULL = 12,
        B_P_FULL = 14, B_PV_DONE = 16, B_Q_READY = 18, B_COUNT = 19 };
@@ -62,6 +65,9 @@ enum { B_ST_FULL = 0, B_ST_EMPTY = 2, B_K_FULL = 4, B_V_FULL = 6, B_K_EMPTY = 8,
 //   staging: 2 stages of K codes | V codes | K scales | V scales for one 64-key tile
 template <int HD>
 struct PL {
+    static constexpr int BN = bn_for(HD);
+    static constexpr uint32_t TM_S0 = HD == 128 ? 256 : 384;
+    static_assert(TM_S0 + 2 * BN <= TM_NCOLS && TM_O + HD <= TM_S0, "tensor memory map");
     static constexpr int HAT_BYTES = (HD / 64) * BN * 128;
     static constexpr int SM_KHAT = 0;
     static constexpr int SM_VHAT = 2 * HAT_BYTES;
@@ -88,7 +94,7 @@ struct PromptParams {
     float* part_o;     // [n_parts][n_q * n_q_heads][HD]
     float2* part_ml;   // [n_parts][n_q * n_q_heads]
     int n_q, n_q_heads, group, capacity, kv_len, q_pos0, rows, n_mtiles, n_items, n_parts;
-    long long units;   // total 64-key tiles over all (KV head, row tile) items
+    long long units;   // total tiles over all (KV head, row tile) items
     float scale_log2;
     // fp16 pools: 3-D tensor maps (dims, keys < kv_len, KV heads) of the K and V planes with a
     // 64-dim x 64-key box and the 128-byte swizzle of the K^/V^ tiles
@@ -104,7 +110,8 @@ struct Item {
     int kvh, r0, rows_here, key_lo, key_hi, n_tiles;
 };
 
-__host__ __device__ inline Item item_geometry(int it, int n_mtiles, int rows, int group, int kv_len, int q_pos0) {
+__host__ __device__ inline Item item_geometry(int it, int n_mtiles, int rows, int group, int kv_len, int q_pos0,
+                                              int bn) {
     Item g;
     g.kvh = it / n_mtiles;
     const int m = it - g.kvh * n_mtiles;
@@ -114,7 +121,7 @@ __host__ __device__ inline Item item_geometry(int it, int n_mtiles, int rows, in
     const long long lo = (long long)q_pos0 + g.r0 / group + 1;
     g.key_hi = (int)(hi < kv_len ? hi : kv_len);
     g.key_lo = (int)(lo < kv_len ? lo : kv_len);
-    g.n_tiles = (g.key_hi + BN - 1) / BN;
+    g.n_tiles = (g.key_hi + bn - 1) / bn;
     return g;
 }
 
@@ -127,12 +134,13 @@ struct Segment {
     int item, t0, t1, part, last;  // tiles [t0, t1) of item; part index; last = owns the item's final tile
 };
 
+template <int BN>
 __device__ int cta_segments(const PromptParams& p, int c, int G, Segment* seg) {
     const long long u0 = unit_begin(c, p.units, G), u1 = unit_begin(c + 1, p.units, G);
     int n = 0;
     long long s = 0;
     for (int it = 0; it < p.n_items && s < u1 && n < kMaxSegments; ++it) {
-        const Item g = item_geometry(it, p.n_mtiles, p.rows, p.group, p.kv_len, p.q_pos0);
+        const Item g = item_geometry(it, p.n_mtiles, p.rows, p.group, p.kv_len, p.q_pos0, BN);
         const long long e = s + g.n_tiles;
         if (e > u0) {
             const long long a = s > u0 ? s : u0, b = e < u1 ? e : u1;
@@ -182,7 +190,7 @@ __device__ __forceinline__ void dequant_tile(const uint8_t* codes, const uint16_
             o0 = make_uint4(h[0], h[1], h[2], h[3]);
             o1 = make_uint4(h[4], h[5], h[6], h[7]);
         }
-        const int base = (j16 >> 2) * (BN * 128) + (n >> 3) * 1024 + (n & 7) * 128;
+        const int base = (j16 >> 2) * (PL<HD>::BN * 128) + (n >> 3) * 1024 + (n & 7) * 128;
         const int c0 = 2 * (j16 & 3);
         *reinterpret_cast<uint4*>(hat + base + ((c0 ^ (n & 7)) << 4)) = o0;
         *reinterpret_cast<uint4*>(hat + base + (((c0 + 1) ^ (n & 7)) << 4)) = o1;
@@ -223,7 +231,7 @@ __device__ __forceinline__ void dequant_tile_v4(const uint8_t* codes, const uint
             o0 = make_uint4(h[0], h[1], h[2], h[3]);
             o1 = make_uint4(h[4], h[5], h[6], h[7]);
         }
-        const int base = (j16 >> 2) * (BN * 128) + (n >> 3) * 1024 + (n & 7) * 128;
+        const int base = (j16 >> 2) * (PL<HD>::BN * 128) + (n >> 3) * 1024 + (n & 7) * 128;
         const int c0 = 2 * (j16 & 3);
         *reinterpret_cast<uint4*>(hat + base + ((c0 ^ (n & 7)) << 4)) = o0;
         *reinterpret_cast<uint4*>(hat + base + (((c0 + 1) ^ (n & 7)) << 4)) = o1;
@@ -250,6 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
     constexpr int STAGE_BYTES = L::STAGE_BYTES, SM_BAR = L::SM_BAR, SM_TMEM_SLOT = L::SM_TMEM_SLOT, SM_SEG = L::SM_SEG;
     constexpr int ST_KC = L::ST_KC, ST_VC = L::ST_VC, ST_KS = L::ST_KS, ST_VS = L::ST_VS;
     constexpr uint32_t IDESC_QK = L::IDESC_QK, IDESC_PV = L::IDESC_PV;
+    constexpr int BN = L::BN;
+    constexpr uint32_t TM_S0 = L::TM_S0;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t sbase = smem_u32(smem);
@@ -261,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
     int* n_seg_slot = reinterpret_cast<int*>(smem + SM_SEG + kMaxSegments * (int)sizeof(Segment));
 
     if (threadIdx.x == 0) {
-        *n_seg_slot = cta_segments(p, blockIdx.x, gridDim.x, seg);
+        *n_seg_slot = cta_segments<BN>(p, blockIdx.x, gridDim.x, seg);
         for (int s = 0; s < 2; ++s) {
             tc::mbar_init(B(B_ST_FULL + s), 1);
             tc::mbar_init(B(B_ST_EMPTY + s), kDeqThreads / 32);  // one arrival per warp
@@ -290,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
             int j = 0;
             bool ok = true;
             for (int si = 0; ok && si < n_seg; ++si) {
-                const Item g = item_geometry(seg[si].item, p.n_mtiles, p.rows, p.group, p.kv_len, p.q_pos0);
+                const Item g = item_geometry(seg[si].item, p.n_mtiles, p.rows, p.group, p.kv_len, p.q_pos0, BN);
                 for (int t = seg[si].t0; t < seg[si].t1; ++t, ++j) {
                     const int b = j & 1, use = j >> 1;
                     const int key0 = t * BN;
@@ -320,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
             int j = 0;
             bool ok = true;
             for (int si = 0; ok && si < n_seg; ++si) {
-                const Item g = item_geometry(seg[si].item, p.n_mtiles, p.rows, p.group, p.kv_len, p.q_pos0);
+                const Item g = item_geometry(seg[si].item, p.n_mtiles, p.rows, p.group, p.kv_len, p.q_pos0, BN);
                 for (int t = seg[si].t0; t < seg[si].t1; ++t, ++j) {
                     const int s = j & 1, use = j >> 1;
                     if (j >= 2 && !tc::mbar_wait(B(B_ST_EMPTY + s), (use - 1) & 1, kWaitLimit)) { ok = false; break; }
@@ -406,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
         bool ok = true;
         int j = 0;
         for (int si = 0; ok && si < n_seg; ++si) {
-            const Item g = item_geometry(seg[si].item, p.n_mtiles, p.rows, p.group, p.kv_len, p.q_pos0);
+            const Item g = item_geometry(seg[si].item, p.n_mtiles, p.rows, p.group, p.kv_len, p.q_pos0, BN);
             const bool valid = r < g.rows_here;
             const int rr = g.r0 + r;
             const int iq = valid ? rr / p.group : 0;
@@ -441,65 +451,141 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
                 const bool ready = tc::mbar_wait(B(B_S_FULL + b), use & 1, kWaitLimit);
                 if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }
                 tc::fence_after_sync();
-                uint32_t s0[32], s1[32];
-                const uint32_t scol = tmem + lane_base + TM_S0 + b * BN;
-                tc::tmem_ld32(scol, s0);
-                tc::tmem_ld32(scol + 32, s1);
-                tc::tmem_wait_ld();
-                float x[64];
+                if constexpr (BN == 64) {  // one 64-key tile per S buffer, held in registers throughout
+                    uint32_t s0[32], s1[32];
+                    const uint32_t scol = tmem + lane_base + TM_S0 + b * BN;
+                    tc::tmem_ld32(scol, s0);
+                    tc::tmem_ld32(scol + 32, s1);
+                    tc::tmem_wait_ld();
+                    float x[64];
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    x[c] = __uint_as_float(s0[c]);
-                    x[32 + c] = __uint_as_float(s1[c]);
-                }
-                const int key0 = t * BN;
-                if (key0 + BN > g.key_lo) {  // the causal diagonal (or rows past kv_len) crosses this tile
-#pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        if (key0 + c >= vis_end) x[c] = -INFINITY;
-                }
-                float mt = x[0];
-#pragma unroll
-                for (int c = 1; c < 64; ++c) mt = fmaxf(mt, x[c]);
-                const float m_new = fmaxf(m_ref, mt * cs);
-                const bool need = m_new > m_ref + kRescaleThreshold || (m_ref == -INFINITY && m_new != -INFINITY);
-                if (__any_sync(0xffffffffu, need)) {
-                    float alpha = 1.0f;
-                    if (need) {
-                        alpha = (m_ref == -INFINITY) ? 0.0f : ex2_approx(m_ref - m_new);
-                        m_ref = m_new;
-                        l *= alpha;
+                    for (int c = 0; c < 32; ++c) {
+                        x[c] = __uint_as_float(s0[c]);
+                        x[32 + c] = __uint_as_float(s1[c]);
                     }
-                    if (t > seg[si].t0) {  // rescale the O row once every earlier PV has landed
-                        const int pj = j - 1;
-                        const bool done = tc::mbar_wait(B(B_PV_DONE + (pj & 1)), (pj >> 1) & 1, kWaitLimit);
-                        if (!__all_sync(0xffffffffu, done)) { ok = false; break; }
-                        tc::fence_after_sync();
-#pragma unroll 1
-                        for (int c = 0; c < HD / 32; ++c) {
-                            uint32_t o[32];
-                            tc::tmem_ld32(tmem + lane_base + TM_O + 32 * c, o);
-                            tc::tmem_wait_ld();
+                    const int key0 = t * BN;
+                    if (key0 + BN > g.key_lo) {  // the causal diagonal (or rows past kv_len) crosses this tile
 #pragma unroll
-                            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                            tc::tmem_st32(tmem + lane_base + TM_O + 32 * c, o);
+                        for (int c = 0; c < 64; ++c)
+                            if (key0 + c >= vis_end) x[c] = -INFINITY;
+                    }
+                    float mt = x[0];
+#pragma unroll
+                    for (int c = 1; c < 64; ++c) mt = fmaxf(mt, x[c]);
+                    const float m_new = fmaxf(m_ref, mt * cs);
+                    const bool need = m_new > m_ref + kRescaleThreshold || (m_ref == -INFINITY && m_new != -INFINITY);
+                    if (__any_sync(0xffffffffu, need)) {
+                        float alpha = 1.0f;
+                        if (need) {
+                            alpha = (m_ref == -INFINITY) ? 0.0f : ex2_approx(m_ref - m_new);
+                            m_ref = m_new;
+                            l *= alpha;
+                        }
+                        if (t > seg[si].t0) {  // rescale the O row once every earlier PV has landed
+                            const int pj = j - 1;
+                            const bool done = tc::mbar_wait(B(B_PV_DONE + (pj & 1)), (pj >> 1) & 1, kWaitLimit);
+                            if (!__all_sync(0xffffffffu, done)) { ok = false; break; }
+                            tc::fence_after_sync();
+#pragma unroll 1
+                            for (int c = 0; c < HD / 32; ++c) {
+                                uint32_t o[32];
+                                tc::tmem_ld32(tmem + lane_base + TM_O + 32 * c, o);
+                                tc::tmem_wait_ld();
+#pragma unroll
+                                for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                                tc::tmem_st32(tmem + lane_base + TM_O + 32 * c, o);
+                            }
                         }
                     }
-                }
-                uint32_t pk[32];
-                float sum = 0.0f;
-                const bool live = m_ref != -INFINITY;
-                const float neg = live ? -m_ref : 0.0f;
+                    uint32_t pk[32];
+                    float sum = 0.0f;
+                    const bool live = m_ref != -INFINITY;
+                    const float neg = live ? -m_ref : 0.0f;
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const float a = live ? ex2_approx(fmaf(x[2 * c], cs, neg)) : 0.0f;
-                    const float bq = live ? ex2_approx(fmaf(x[2 * c + 1], cs, neg)) : 0.0f;
-                    sum += a + bq;
-                    const __half2 h = __floats2half2_rn(a, bq);
-                    pk[c] = *reinterpret_cast<const uint32_t*>(&h);
+                    for (int c = 0; c < 32; ++c) {
+                        const float a = live ? ex2_approx(fmaf(x[2 * c], cs, neg)) : 0.0f;
+                        const float bq = live ? ex2_approx(fmaf(x[2 * c + 1], cs, neg)) : 0.0f;
+                        sum += a + bq;
+                        const __half2 h = __floats2half2_rn(a, bq);
+                        pk[c] = *reinterpret_cast<const uint32_t*>(&h);
+                    }
+                    l += sum;
+                    tc::tmem_st32(scol, pk);  // P overwrites the first 32 columns of this S buffer
+                } else {  // 128-key tiles: the S row in two 64-column halves, read twice
+                    const uint32_t scol = tmem + lane_base + TM_S0 + b * BN;
+                    const int key0 = t * BN;
+                    const bool diag = key0 + BN > g.key_lo;  // the causal diagonal (or rows past kv_len) crosses this tile
+                    // S row of this thread, 64 columns at a time (the tile's BN/64 halves), masked
+                    auto load_half = [&](int h, float (&x)[64]) {
+                        uint32_t s0[32], s1[32];
+                        tc::tmem_ld32(scol + 64 * h, s0);
+                        tc::tmem_ld32(scol + 64 * h + 32, s1);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            x[c] = __uint_as_float(s0[c]);
+                            x[32 + c] = __uint_as_float(s1[c]);
+                        }
+                        if (diag) {
+#pragma unroll
+                            for (int c = 0; c < 64; ++c)
+                                if (key0 + 64 * h + c >= vis_end) x[c] = -INFINITY;
+                        }
+                    };
+                    float x[64];
+                    float mt = -INFINITY;
+#pragma unroll 1
+                    for (int h = 0; h < BN / 64; ++h) {
+                        load_half(h, x);
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) mt = fmaxf(mt, x[c]);
+                    }
+                    const float m_new = fmaxf(m_ref, mt * cs);
+                    const bool need = m_new > m_ref + kRescaleThreshold || (m_ref == -INFINITY && m_new != -INFINITY);
+                    if (__any_sync(0xffffffffu, need)) {
+                        float alpha = 1.0f;
+                        if (need) {
+                            alpha = (m_ref == -INFINITY) ? 0.0f : ex2_approx(m_ref - m_new);
+                            m_ref = m_new;
+                            l *= alpha;
+                        }
+                        if (t > seg[si].t0) {  // rescale the O row once every earlier PV has landed
+                            const int pj = j - 1;
+                            const bool done = tc::mbar_wait(B(B_PV_DONE + (pj & 1)), (pj >> 1) & 1, kWaitLimit);
+                            if (!__all_sync(0xffffffffu, done)) { ok = false; break; }
+                            tc::fence_after_sync();
+#pragma unroll 1
+                            for (int c = 0; c < HD / 32; ++c) {
+                                uint32_t o[32];
+                                tc::tmem_ld32(tmem + lane_base + TM_O + 32 * c, o);
+                                tc::tmem_wait_ld();
+#pragma unroll
+                                for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                                tc::tmem_st32(tmem + lane_base + TM_O + 32 * c, o);
+                            }
+                        }
+                    }
+                    const bool live = m_ref != -INFINITY;
+                    const float neg = live ? -m_ref : 0.0f;
+                    // P of keys 64h .. 64h+63 goes to columns 32h .. 32h+31 of this S buffer: those
+                    // hold S of keys 32h .. 32h+63, already read (half 0 by now, half 1 below)
+#pragma unroll 1
+                    for (int h = 0; h < BN / 64; ++h) {
+                        if (BN > 64) load_half(h, x);  // at BN = 64 the half is still in registers
+                        uint32_t pk[32];
+                        float sum = 0.0f;
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            const float a = live ? ex2_approx(fmaf(x[2 * c], cs, neg)) : 0.0f;
+                            const float bq = live ? ex2_approx(fmaf(x[2 * c + 1], cs, neg)) : 0.0f;
+                            sum += a + bq;
+                            const __half2 hh = __floats2half2_rn(a, bq);
+                            pk[c] = *reinterpret_cast<const uint32_t*>(&hh);
+                        }
+                        l += sum;
+                        tc::tmem_st32(scol + 32 * h, pk);
+                    }
                 }
-                l += sum;
-                tc::tmem_st32(scol, pk);  // P overwrites the first 32 columns of this S buffer
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
@@ -540,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
         int j = 0;
         bool ok = true;
         for (int si = 0; ok && si < n_seg; ++si) {
-            const Item g = item_geometry(seg[si].item, p.n_mtiles, p.rows, p.group, p.kv_len, p.q_pos0);
+            const Item g = item_geometry(seg[si].item, p.n_mtiles, p.rows, p.group, p.kv_len, p.q_pos0, BN);
             for (int t = seg[si].t0; t < seg[si].t1; ++t, ++j) {
                 const int s = j & 1, use = j >> 1;
                 // waits are decided per warp, so that a warp arrives (lane 0) only as a whole
@@ -601,7 +687,7 @@ int prompt_plan(int n_q, int n_q_heads, int head_dim, int kv_len, int q_pos0, in
     pl->n_items = (int)items;
     long long U = 0;
     for (int it = 0; it < pl->n_items; ++it)
-        U += item_geometry(it, pl->n_mtiles, (int)rows, group, kv_len, q_pos0).n_tiles;
+        U += item_geometry(it, pl->n_mtiles, (int)rows, group, kv_len, q_pos0, bn_for(head_dim)).n_tiles;
     pl->units = U;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
@@ -613,7 +699,7 @@ int prompt_plan(int n_q, int n_q_heads, int head_dim, int kv_len, int q_pos0, in
     long long s = 0;
     int max_seg = 0, cur_cta = -1, cur_seg = 0;
     for (int it = 0; it < pl->n_items; ++it) {
-        const int nt = item_geometry(it, pl->n_mtiles, (int)rows, group, kv_len, q_pos0).n_tiles;
+        const int nt = item_geometry(it, pl->n_mtiles, (int)rows, group, kv_len, q_pos0, bn_for(head_dim)).n_tiles;
         const long long c0 = cta_of_unit(s, U, pl->grid), c1 = cta_of_unit(s + nt - 1, U, pl->grid);
         parts = (int)(c1 - c0 + 1) > parts ? (int)(c1 - c0 + 1) : parts;
         for (long long c = c0; c <= c1; ++c) {
@@ -665,6 +751,7 @@ EncodeTiledFn encode_tiled_fn() {
 // Tensor map of one fp16 plane [n_kv_heads][capacity][hd]: dims (hd, kv_len, n_kv_heads), so
 // keys at or past kv_len read as zeros; box 64 dims x 64 keys x 1 head, 128-byte swizzle.
 bool encode_f16_plane(CUtensorMap* map, const uint16_t* plane, int hd, int kv_len, int n_kv_heads, int capacity) {
+    const int BN = bn_for(hd);
     const EncodeTiledFn fn = encode_tiled_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)kv_len, (cuuint64_t)n_kv_heads};
