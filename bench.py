@@ -725,7 +725,7 @@ def main():
         hbm_peak, bf16_peak, _ = _peaks()
         from speculative_verify_attention_gb300 import workloads as _wl
         for w, pool in ((_wl.PROMPT, "q8"), (_wl.PROMPT_HD128, "q8"), (_wl.PROMPT, "k8v4"), (_wl.PROMPT, "f16"),
-                        (_wl.PROMPT_HD128, "f16")):
+                        (_wl.PROMPT_HD128, "f16"), (_wl.PROMPT_HD128, "k8v4")):
             if args.prompt_filter and args.prompt_filter not in f"{pool}-{w.name}":
                 continue
             print(json.dumps(prompt_bench(args, torch.device("cuda", 0), bf16_peak * 0.951, w, pool)), flush=True)

@@ -62,7 +62,9 @@ enum { B_ST_FULL = 0, B_ST_EMPTY = 2, B_K_FULL = 4, B_V_FULL = 6, B_K_EMPTY = 8,
 // Shared memory layout for head dim HD (bytes, 1024-aligned tiles):
 //   K^, V^ : 2 buffers each of [HD/64 atoms][64 keys][128 B], 128B-swizzled fp16 (K-major for
 //            K^, read as MN-major for V^)
-//   staging: 2 stages of K codes | V codes | K scales | V scales for one 64-key tile
+//   staging: 2 stages of K codes | V codes | K scales | V scales for one tile; at hd128 each
+//            scale area has 16 spare bytes so that a tile's scales sit at the same offset mod 16
+//            as in global memory
 template <int HD>
 struct PL {
     static constexpr int BN = bn_for(HD);
@@ -72,8 +74,9 @@ struct PL {
     static constexpr int SM_KHAT = 0;
     static constexpr int SM_VHAT = 2 * HAT_BYTES;
     static constexpr int SM_STAGE = 4 * HAT_BYTES;
-    static constexpr int ST_KC = 0, ST_VC = BN * HD, ST_KS = 2 * BN * HD, ST_VS = 2 * BN * HD + BN * HD / 16;
-    static constexpr int STAGE_BYTES = 2 * BN * HD + 2 * (BN * HD / 16);
+    static constexpr int SC_PAD = HD == 128 ? 16 : 0;
+    static constexpr int ST_KC = 0, ST_VC = BN * HD, ST_KS = 2 * BN * HD, ST_VS = ST_KS + BN * HD / 16 + SC_PAD;
+    static constexpr int STAGE_BYTES = (2 * BN * HD + 2 * (BN * HD / 16 + SC_PAD) + 1023) / 1024 * 1024;
     static constexpr int SM_BAR = SM_STAGE + 2 * STAGE_BYTES;
     static constexpr int SM_TMEM_SLOT = SM_BAR + B_COUNT * 8;
     static constexpr int SM_SEG = SM_TMEM_SLOT + 16;  // this CTA's work segments (written by thread 0)
@@ -338,17 +341,42 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
                     const int nk = min(BN, g.key_hi - key0);
                     const int64_t row0 = (int64_t)g.kvh * p.capacity + key0;
                     const uint32_t st = sbase + SM_STAGE + s * STAGE_BYTES;
-                    // codes rows are HD bytes (16-byte multiples); at hd256 a key's scales are 16
-                    // bytes too, at hd128 only 8, so there the dequantisers read them from global
-                    // memory instead (a bulk copy wants 16-byte aligned starts and sizes)
-                    constexpr int scale_bytes = HD == 256 ? 2 * (HD / 16) : 0;
                     constexpr int v_row = V4 ? HD / 2 : HD;  // V code bytes per key
-                    tc::mbar_arrive_expect_tx(B(B_ST_FULL + s), (uint32_t)(nk * (HD + v_row + scale_bytes)));
-                    tc::bulk_g2s(st + ST_KC, p.kc + row0 * HD, nk * HD, B(B_ST_FULL + s));
-                    tc::bulk_g2s(st + ST_VC, p.vc + row0 * v_row, nk * v_row, B(B_ST_FULL + s));
-                    if constexpr (HD == 256) {
+                    if constexpr (HD == 256) {  // code rows and a key's 16 bytes of scales: 16-byte multiples
+                        tc::mbar_arrive_expect_tx(B(B_ST_FULL + s), (uint32_t)(nk * (HD + v_row + 2 * (HD / 16))));
+                        tc::bulk_g2s(st + ST_KC, p.kc + row0 * HD, nk * HD, B(B_ST_FULL + s));
+                        tc::bulk_g2s(st + ST_VC, p.vc + row0 * v_row, nk * v_row, B(B_ST_FULL + s));
                         tc::bulk_g2s(st + ST_KS, p.ks + row0 * (HD / 32), nk * (HD / 16), B(B_ST_FULL + s));
                         tc::bulk_g2s(st + ST_VS, p.vs + row0 * (HD / 32), nk * (HD / 16), B(B_ST_FULL + s));
+                    } else {
+                        // a key's scales are 8 bytes: the tile's scales start 0 or 8 bytes past a
+                        // 16-byte boundary (off) and land at the same offset in the stage.  The
+                        // 16-byte aligned interior goes by bulk copy, an 8-byte head or tail by a
+                        // plain load; the arrival comes after the plain stores (release).
+                        const int off = (int)(row0 & 1) * 8, end = off + nk * 8;
+                        const int a = off == 0 ? 0 : 16, bnd = end & ~15;
+                        const int inner = bnd > a ? bnd - a : 0;
+                        tc::mbar_expect_tx(B(B_ST_FULL + s), (uint32_t)(nk * (HD + v_row) + 2 * inner));
+                        tc::bulk_g2s(st + ST_KC, p.kc + row0 * HD, nk * HD, B(B_ST_FULL + s));
+                        tc::bulk_g2s(st + ST_VC, p.vc + row0 * v_row, nk * v_row, B(B_ST_FULL + s));
+                        const uint8_t* gk = reinterpret_cast<const uint8_t*>(p.ks + row0 * (HD / 32)) - off;
+                        const uint8_t* gv = reinterpret_cast<const uint8_t*>(p.vs + row0 * (HD / 32)) - off;
+                        if (inner > 0) {
+                            tc::bulk_g2s(st + ST_KS + a, gk + a, inner, B(B_ST_FULL + s));
+                            tc::bulk_g2s(st + ST_VS + a, gv + a, inner, B(B_ST_FULL + s));
+                        }
+                        uint8_t* sst = smem + SM_STAGE + s * STAGE_BYTES;
+                        if (off == 8) {
+                            *reinterpret_cast<uint2*>(sst + ST_KS + 8) = __ldg(reinterpret_cast<const uint2*>(gk + 8));
+                            *reinterpret_cast<uint2*>(sst + ST_VS + 8) = __ldg(reinterpret_cast<const uint2*>(gv + 8));
+                        }
+                        if ((end & 15) == 8) {
+                            *reinterpret_cast<uint2*>(sst + ST_KS + end - 8) =
+                                __ldg(reinterpret_cast<const uint2*>(gk + end - 8));
+                            *reinterpret_cast<uint2*>(sst + ST_VS + end - 8) =
+                                __ldg(reinterpret_cast<const uint2*>(gv + end - 8));
+                        }
+                        tc::mbar_arrive(B(B_ST_FULL + s));
                     }
                 }
             }
@@ -633,9 +661,10 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
                 if (!__all_sync(0xffffffffu, tc::mbar_wait(B(B_ST_FULL + s), use & 1, kWaitLimit))) { ok = false; break; }
                 const int nk = min(BN, g.key_hi - t * BN);
                 const uint8_t* st = smem + SM_STAGE + s * STAGE_BYTES;
-                const int64_t srow0 = (int64_t)g.kvh * p.capacity + t * BN;
-                const uint16_t* k_sc = HD == 256 ? reinterpret_cast<const uint16_t*>(st + ST_KS) : p.ks + srow0 * (HD / 32);
-                const uint16_t* v_sc = HD == 256 ? reinterpret_cast<const uint16_t*>(st + ST_VS) : p.vs + srow0 * (HD / 32);
+                // at hd128 the scales sit at the tile's 0- or 8-byte offset from a 16-byte boundary
+                const int soff = HD == 256 ? 0 : (int)(((int64_t)g.kvh * p.capacity + t * BN) & 1) * 8;
+                const uint16_t* k_sc = reinterpret_cast<const uint16_t*>(st + ST_KS + soff);
+                const uint16_t* v_sc = reinterpret_cast<const uint16_t*>(st + ST_VS + soff);
                 if (j >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait(B(B_K_EMPTY + s), (use - 1) & 1, kWaitLimit))) {
                     ok = false;
                     break;

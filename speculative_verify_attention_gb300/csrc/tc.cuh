@@ -95,6 +95,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar, uint32_t by
                  "r"(bytes)
                  : "memory");
 }
+// Raises the transaction count of the current phase without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t mbar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
