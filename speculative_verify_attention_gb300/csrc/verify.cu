@@ -591,9 +591,7 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
             for (int k = 0; k < kKT / 32; ++k) sDv[lane + 32 * k] = __half_as_ushort(__float2half_rn(dv[k] * esc));
             __syncwarp();
         }
-        const int n_ks = (nk + 15) >> 4;
-#pragma unroll 2
-        for (int ks = 0; ks < n_ks; ++ks) {
+        auto pv_step = [&](const int ks) {
             const int kb = ks * 16;
             uint2 pp01[NT], pp89[NT];  // (hi, lo) pairs of keys (2t, 2t+1) and (2t+8, 2t+9), row g of n-tile
             const uint2* pp = p_lane + ks * 8 * PS;
@@ -661,6 +659,19 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
                     mma_f16_16816(O[mt][nt], A[mt][0], A[mt][1], A[mt][2], A[mt][3], bl0, bl1);
                 }
             }
+        };
+        if constexpr (NT <= 3) {
+            // 32-key steps (offsets fixed at compile time): key rows past nk hold p = 0 and
+            // zero V codes and scales, so a ragged tile may round up
+            const int n_u = (nk + 31) >> 5;
+            for (int u4 = 0; u4 < n_u; ++u4) {
+                pv_step(2 * u4);
+                pv_step(2 * u4 + 1);
+            }
+        } else {
+            const int n_ks = (nk + 15) >> 4;
+#pragma unroll 2
+            for (int ks = 0; ks < n_ks; ++ks) pv_step(ks);
         }
         __syncthreads();  // all warps done with sV, sP and the scale tables
     }

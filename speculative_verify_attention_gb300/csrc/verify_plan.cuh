@@ -1,5 +1,5 @@
 // verify_plan.cuh -- how a multi-row verify call is cut into thread blocks: row chunks of at
-// most 8 * kMaxNT (row, q-head) pairs per KV head, times context slices of whole 64-key units.
+// most 8 * kMaxNT (row, q-head) pairs per KV head, times context slices of whole 16-key units.
 // Shared by the Q8_0 and the fp16-pool verify kernels.
 #pragma once
 
@@ -10,7 +10,7 @@
 namespace kvq8 {
 
 constexpr int kKT = 128;        // keys per tile
-constexpr int kSplitUnit = 64;  // context slices are whole multiples of this many keys
+constexpr int kSplitUnit = 16;  // context slices are whole multiples of this many keys
 constexpr int kMaxNT = 4;       // n8 row tiles per chunk (<= 32 rows per thread block)
 
 // resident thread blocks per SM of the Q8_0 verify kernel: two up to 24 rows per chunk
@@ -49,8 +49,9 @@ inline int make_plan(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_
     pl->n_chunks = (R + 8 * kMaxNT - 1) / (8 * kMaxNT);
     pl->rows_per_chunk = (R + pl->n_chunks - 1) / pl->n_chunks;
     pl->nt = (pl->rows_per_chunk + 7) / 8;
-    // slices are whole 64-key units; the automatic count fills every SM with as many thread
-    // blocks as fit at once (blocks_per_sm of the kernel that will run)
+    // slices are whole 16-key units, fine enough that the blocks of one wave get nearly equal
+    // work; the automatic count fills every SM with as many thread blocks as fit at once
+    // (blocks_per_sm of the kernel that will run)
     const int ctx_end = kv_len - window_keys;
     if (ctx_end < 0) return KVQ8_ERR_INVALID_ARG;
     const int n_units = (ctx_end + kSplitUnit - 1) / kSplitUnit;
@@ -62,12 +63,14 @@ inline int make_plan(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_
         ns = std::max(1, (per_sm * sms) / (n_kv_heads * pl->n_chunks));
     }
     ns = std::max(1, std::min(ns, n_units));
-    // an automatic slice holds at least one whole 128-key tile
-    const int min_units = n_split_req > 0 ? 1 : kKT / kSplitUnit;
+    // an automatic slice holds at least one whole 128-key tile; every slice is at least as
+    // long as the window, whose slice spans keys_per_split keys from ctx_end
+    const int min_units = std::max(n_split_req > 0 ? 1 : kKT / kSplitUnit,
+                                   (window_keys + kSplitUnit - 1) / kSplitUnit);
     const int units_per_split = std::max(min_units, (n_units + ns - 1) / ns);
     pl->keys_per_split = units_per_split * kSplitUnit;
     pl->n_ctx_splits = (ctx_end + pl->keys_per_split - 1) / pl->keys_per_split;
-    // with a window slice (window_keys <= 32 < keys_per_split) the context slices are aligned
+    // with a window slice (window_keys <= keys_per_split) the context slices are aligned
     // to end at ctx_end, so the first one is the short one
     pl->key_shift = window_keys > 0 ? pl->n_ctx_splits * pl->keys_per_split - ctx_end : 0;
     pl->n_split = pl->n_ctx_splits + (window_keys > 0 ? 1 : 0);

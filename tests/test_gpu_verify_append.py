@@ -45,7 +45,7 @@ def _written_equal(gpu, orc, end):
     return bool(ok)
 
 
-@pytest.mark.parametrize("T,n_split", [(4, 0), (8, 0), (16, 0), (32, 0), (4, 5), (8, 1)])
+@pytest.mark.parametrize("T,n_split", [(4, 0), (8, 0), (16, 0), (32, 0), (4, 5), (8, 1), (32, 100)])
 def test_27b_shape_matches_oracle(lib, T, n_split):
     w = workloads.verify_workload(f"append-24q4kv-hd256-ctx1000-T{T}", 24, 4, 256, 1000, T, k_outliers=4,
                                   seed=950 + T)
@@ -58,8 +58,8 @@ def test_27b_shape_matches_oracle(lib, T, n_split):
 
 @pytest.mark.parametrize("q_pos0", [0, 1, 63, 64, 127, 128, 129, 511])
 def test_hd128_window_slice_boundaries(lib, q_pos0):
-    """Context ends on and off the 64-key unit and the 128-key tile; q_pos0 = 0 leaves the
-    window slice alone."""
+    """Context ends on and off 64-key and 128-key boundaries; q_pos0 = 0 leaves the window
+    slice alone."""
     T = 12
     inp = workloads.random_small(960 + q_pos0, 8, 2, 128, q_pos0 + T, T)
     gpu, orc, got = _append_verify(inp, q_pos0, 0.088, q_pos0 + T + 7)

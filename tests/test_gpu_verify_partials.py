@@ -64,8 +64,8 @@ def test_rows_before_the_cache_get_empty_partials(lib):
     inp = workloads.random_small(992, 6, 2, 128, 200, 4)
     gpu, _ = build_caches(inp, capacity=208)
     n = attn_verify_q8_partials_count(4, 6, 128, 200, 2, 4)
-    assert n == 4                                  # 4 slices of 64 keys (whole 64-key units)
-    assert attn_verify_q8_partials_count(4, 6, 128, 200, 2, 3) == 2   # 3 asked: 128-key slices
+    assert n == 4                                  # 4 slices of 64 keys (whole 16-key units)
+    assert attn_verify_q8_partials_count(4, 6, 128, 200, 2, 3) == 3   # 3 asked: 80-key slices
     o, ml = attn_verify_q8_partials(torch.from_numpy(inp.q).cuda(), gpu, 200, -4, 0.1, n_split=4)
     torch.cuda.synchronize()
     assert o.shape == (4, 24, 128) and ml.shape == (4, 24, 2)
