@@ -183,6 +183,63 @@ def oracle_verify_sample(n_pairs_per_step: int, steps: int, warmup: int, threads
     return gbs, dt / steps, n_thr, desc
 
 
+def oracle_sweep() -> None:
+    """The fp64 oracle timed per configuration on the host cores (a baseline only): full calls
+    of the verify configurations, all OpenMP threads, median of up to three runs, plus a
+    one-thread figure scaled from a sample of (row, q-head) pairs; the prompt chunk from a
+    sample of pairs at random rows, scaled to the whole chunk.  One JSON line per cell."""
+    import oracle
+    from speculative_verify_attention_gb300 import workloads
+
+    n_thr = oracle.get_threads()
+
+    def cache_for(w, inp):
+        c = oracle.Cache(w.n_kv_heads, w.head_dim, w.kv_len)
+        c.append(inp.k, inp.v, 0)
+        return c
+
+    def timed(fn, runs):
+        ts = []
+        for _ in range(runs):
+            t0 = time.perf_counter()
+            fn()
+            ts.append(time.perf_counter() - t0)
+        return float(np.median(ts))
+
+    cells = [(workloads.TINY, 3), (workloads.verify_27b(4), 3), (workloads.verify_27b(8), 3),
+             (workloads.long_verify(20676, 4), 3), (workloads.long_verify(20676, 8), 1),
+             (workloads.long_verify(20676, 32), 1), (workloads.long_verify(32768, 4), 3),
+             (workloads.hd128_verify(4), 3)]
+    for w, runs in cells:
+        inp = workloads.make_inputs(w)
+        c = cache_for(w, inp)
+        oracle.set_threads(n_thr)
+        sec = timed(lambda: oracle.attention(c, inp.q, w.kv_len, w.q_pos0, w.softmax_scale), runs)
+        pairs = [(i, h) for i in range(w.n_q) for h in range(w.n_q_heads)]
+        sel = [pairs[k] for k in np.random.default_rng(1).integers(0, len(pairs), 4)]
+        oracle.set_threads(1)
+        sec1 = timed(lambda: oracle.attention(c, inp.q, w.kv_len, w.q_pos0, w.softmax_scale, sel=sel), 1)
+        oracle.set_threads(n_thr)
+        print(json.dumps({"oracle_cell": w.name, "ms_per_call": sec * 1e3, "runs": runs, "cores": n_thr,
+                          "kv_gbs": w.kv_bytes() / sec / 1e9,
+                          "ms_per_call_1thread": sec1 * len(pairs) / len(sel) * 1e3,
+                          "sample_1thread": f"{len(sel)} of {len(pairs)} pairs, scaled"}), flush=True)
+        del c, inp
+    for w in (workloads.PROMPT, workloads.PROMPT_HD128):
+        inp = workloads.make_inputs(w)
+        c = cache_for(w, inp)
+        n_pairs = 4 * n_thr
+        rng = np.random.default_rng(2)
+        sel = [(int(i), int(h)) for i, h in zip(rng.integers(0, w.n_q, n_pairs), rng.integers(0, w.n_q_heads, n_pairs))]
+        sec = timed(lambda: oracle.attention(c, inp.q, w.kv_len, w.q_pos0, w.softmax_scale, sel=sel), 1)
+        total = w.n_q * w.n_q_heads
+        print(json.dumps({"oracle_cell": w.name, "ms_per_call": sec * total / n_pairs * 1e3, "runs": 1,
+                          "cores": n_thr, "tflops": w.causal_flops() / (sec * total / n_pairs) / 1e12,
+                          "sample": f"{n_pairs} of {total} (query, q-head) pairs at random rows, scaled "
+                                    f"to the chunk ({sec:.2f} s timed)"}), flush=True)
+        del c, inp
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return 0
@@ -707,6 +764,8 @@ def main():
     ap.add_argument("--no-long-context", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="per-cell verify sweep instead of the headline line")
     ap.add_argument("--prompt-only", action="store_true", help="time only the prompt-chunk kernel")
+    ap.add_argument("--oracle-sweep", action="store_true",
+                    help="time the fp64 CPU oracle per configuration (host cores only, no GPU)")
     ap.add_argument("--sweep-filter", default="")
     ap.add_argument("--prompt-filter", default="", help="with --prompt-only: time only the cells whose "
                     "'<pool>-<workload>' name contains this")
@@ -714,6 +773,9 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     world, rank, local = _dist()
+    if args.oracle_sweep:
+        oracle_sweep()
+        return 0
     if args.sweep:
         sweep(args)
         return 0
