@@ -335,16 +335,17 @@ size_t attn_prompt_q8_workspace_bytes(int n_q, int n_q_heads, int head_dim, int 
 
 /*
  * attn_prompt_q8 -- prompt-chunk attention: many query rows over a long Q8_0 context.
- *   q        : fp16 bits [n_q][n_q_heads][head_dim], head_dim 256
- *   kv       : the cache (head_dim 256, any n_kv_heads dividing n_q_heads)
+ *   q        : fp16 bits [n_q][n_q_heads][head_dim], head_dim 128 or 256
+ *   kv       : the cache (the same head_dim, any n_kv_heads dividing n_q_heads)
  *   out      : fp32 [n_q][n_q_heads][head_dim]
  *   workspace: device scratch of at least attn_prompt_q8_workspace_bytes(...) bytes,
  *              caller-owned; holds the per-slice partials merged by the second kernel
  *   softmax_scale must be > 0.
  * Row i sees keys n <= q_pos0 + i, n < kv_len.  K and V are dequantised on chip to fp16
  * (code * scale, one rounding) and contracted on the tcgen05 tensor cores with fp32
- * accumulation in tensor memory; p enters the PV product as fp16.  The work -- 64-key
- * tiles of 128-row tiles of (query, head) pairs of every KV head -- is cut into one equal
+ * accumulation in tensor memory; p enters the PV product as fp16.  The work -- key tiles
+ * (64 keys at head_dim 256, 128 at 128) of 128-row tiles of (query, head) pairs of every
+ * KV head -- is cut into one equal
  * contiguous share per SM (a persistent grid); each share writes partials that the
  * log-sum-exp combine merges into `out`.  Tiles past a row tile's causal bound are
  * skipped.  Within 2e-3 of the fp64 oracle (max |err| / max |out|) for values inside the

@@ -8,11 +8,11 @@
 // NaN); +inf entries share the row's probability mass; a row of -inf only is the uniform
 // limit (argmax 0, probability 1/V).
 //
-// One pass computes both results.  Every thread keeps an online accumulator over its elements
-// -- the running maximum m, the first index of m, s = sum exp(x - m) (rescaled when m grows)
-// and the first NaN index -- and accumulators merge with the same rule, first across the
-// warp, then across the block, then across the blocks of a row (second kernel, launched as a
-// programmatic dependent).  HBM-bound: 4 bytes read per logit.
+// One read of the logits computes both results.  Every thread reduces the logits it holds in
+// registers to an accumulator -- the maximum m, the first index of m, s = sum exp(x - m) and
+// the first NaN index -- and accumulators merge (s rescaled to the larger m), first across
+// the warp, then across the block, then across the blocks of a row (second kernel, launched
+// as a programmatic dependent).  HBM-bound: 4 bytes read per logit.
 #include <climits>
 
 #include "common.cuh"
@@ -31,23 +31,6 @@ struct HeadAcc {
 };
 
 __device__ __forceinline__ HeadAcc acc_empty() { return HeadAcc{-INFINITY, 0.0f, INT_MAX, INT_MAX}; }
-
-__device__ __forceinline__ void acc_add(HeadAcc& a, float x, int j) {
-    if (x != x) {
-        a.nan = min(a.nan, j);
-    } else if (x > a.m) {
-        a.s = (a.m == -INFINITY) ? 1.0f : fmaf(a.s, __expf(a.m - x), 1.0f);
-        a.m = x;
-        a.idx = j;
-    } else if (x == a.m) {
-        if (a.m != -INFINITY) {
-            a.s += 1.0f;
-            a.idx = min(a.idx, j);
-        }
-    } else if (a.m != -INFINITY) {
-        a.s += __expf(x - a.m);
-    }
-}
 
 __device__ __forceinline__ HeadAcc acc_merge(const HeadAcc& a, const HeadAcc& b) {
     HeadAcc r;
@@ -75,6 +58,40 @@ __device__ __forceinline__ HeadAcc acc_shfl_xor(const HeadAcc& a, int o) {
     b.idx = __shfl_xor_sync(0xffffffffu, a.idx, o);
     b.nan = __shfl_xor_sync(0xffffffffu, a.nan, o);
     return b;
+}
+
+// Accumulator of one thread's N register-resident logits, x[i] at index jx(i) (increasing in
+// i): a pass for the maximum and its first index (predicated, no branches), a pass for
+// s = sum 2^((x - m) log2 e), and a NaN scan only where the sum says there is one or the
+// maximum is infinite (the rare cases).
+template <int N, typename JF>
+__device__ __forceinline__ HeadAcc acc_of(const float (&x)[N], JF jx) {
+    float m = -INFINITY;
+    int idx = INT_MAX;
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        if (x[i] > m) {
+            m = x[i];
+            idx = jx(i);
+        }
+    HeadAcc a{m, 0.0f, idx, INT_MAX};
+    bool scan = true;
+    if (m == INFINITY) {  // the +inf entries share the mass
+#pragma unroll
+        for (int i = 0; i < N; ++i) a.s += x[i] == INFINITY ? 1.0f : 0.0f;
+    } else if (m != -INFINITY) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int i = 0; i < N; ++i) sum += ex2_approx((x[i] - m) * kLog2e);
+        a.s = sum;
+        scan = sum != sum;  // a NaN among the values makes the sum NaN
+    }
+    if (scan) {
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if (x[i] != x[i]) a.nan = min(a.nan, jx(i));
+    }
+    return a;
 }
 
 template <int THREADS>
@@ -110,20 +127,17 @@ __global__ void __launch_bounds__(kHeadThreads) head_partial_kernel(const float*
         const float4* x4 = reinterpret_cast<const float4*>(x);
         const int e4 = vocab >> 2;
         const int k0 = b * (kChunkVec / 4) + threadIdx.x;
-        float4 v[kPer];
+        float v[4 * kPer];
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
             const int k = k0 + u * kHeadThreads;
-            v[u] = k < e4 ? __ldg(x4 + k) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            const float4 f = k < e4 ? __ldg(x4 + k) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            v[4 * u] = f.x;
+            v[4 * u + 1] = f.y;
+            v[4 * u + 2] = f.z;
+            v[4 * u + 3] = f.w;
         }
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const int j = 4 * (k0 + u * kHeadThreads);
-            acc_add(a, v[u].x, j);
-            acc_add(a, v[u].y, j + 1);
-            acc_add(a, v[u].z, j + 2);
-            acc_add(a, v[u].w, j + 3);
-        }
+        a = acc_of(v, [&](int i) { return 4 * (k0 + (i >> 2) * kHeadThreads) + (i & 3); });
     } else {
         const int j0 = b * kChunkScalar + threadIdx.x;
         float v[kPer];
@@ -132,11 +146,23 @@ __global__ void __launch_bounds__(kHeadThreads) head_partial_kernel(const float*
             const int j = j0 + u * kHeadThreads;
             v[u] = j < vocab ? __ldg(x + j) : -INFINITY;
         }
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) acc_add(a, v[u], j0 + u * kHeadThreads);
+        a = acc_of(v, [&](int i) { return j0 + i * kHeadThreads; });
     }
     a = block_merge<kHeadThreads>(a, s_acc);
     if (threadIdx.x == 0) part[(int64_t)row * gridDim.x + b] = a;
+}
+
+__device__ __forceinline__ void head_write(const HeadAcc& a, int vocab, int row, int32_t* argmax, float* top_prob) {
+    if (a.nan != INT_MAX) {
+        argmax[row] = a.nan;
+        top_prob[row] = __int_as_float(0x7fc00000);  // quiet NaN
+    } else if (a.m == -INFINITY) {
+        argmax[row] = 0;
+        top_prob[row] = 1.0f / (float)vocab;
+    } else {
+        argmax[row] = a.idx;
+        top_prob[row] = 1.0f / a.s;
+    }
 }
 
 __global__ void __launch_bounds__(kMergeThreads) head_merge_kernel(const HeadAcc* __restrict__ part, int n_blocks,
@@ -148,18 +174,7 @@ __global__ void __launch_bounds__(kMergeThreads) head_merge_kernel(const HeadAcc
     HeadAcc a = acc_empty();
     for (int b = threadIdx.x; b < n_blocks; b += kMergeThreads) a = acc_merge(a, part[(int64_t)row * n_blocks + b]);
     a = block_merge<kMergeThreads>(a, s_acc);
-    if (threadIdx.x == 0) {
-        if (a.nan != INT_MAX) {
-            argmax[row] = a.nan;
-            top_prob[row] = __int_as_float(0x7fc00000);  // quiet NaN
-        } else if (a.m == -INFINITY) {
-            argmax[row] = 0;
-            top_prob[row] = 1.0f / (float)vocab;
-        } else {
-            argmax[row] = a.idx;
-            top_prob[row] = 1.0f / a.s;
-        }
-    }
+    if (threadIdx.x == 0) head_write(a, vocab, row, argmax, top_prob);
 }
 
 bool head_vec(const float* logits, int vocab) { return vocab % 4 == 0 && aligned16(logits); }
@@ -191,8 +206,8 @@ extern "C" int argmax_rows_top_prob(const float* logits, int n_rows, int vocab, 
     if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(argmax) |
          reinterpret_cast<uintptr_t>(top_prob)) & 3u)
         return KVQ8_ERR_MISALIGNED;
-    HeadAcc* part = static_cast<HeadAcc*>(workspace);
     cudaStream_t s = (cudaStream_t)stream;
+    HeadAcc* part = static_cast<HeadAcc*>(workspace);
     dim3 grid(B, n_rows);
     if (vec)
         head_partial_kernel<true><<<grid, kHeadThreads, 0, s>>>(logits, vocab, part);

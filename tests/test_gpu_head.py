@@ -59,6 +59,33 @@ def test_vocab_not_a_multiple_of_four(lib, vocab):
     _check(x)
 
 
+@pytest.mark.parametrize("vocab", [4, 8, 12, 4096])
+def test_small_vocab_multiple_of_four(lib, vocab):
+    rng = np.random.default_rng(vocab + 5)
+    x = (rng.standard_normal((5, vocab)) * 4.0).astype(np.float32)
+    x[2, :] = x[2, 0]                             # uniform: the first index wins the tie
+    _check(x)
+
+
+def test_ties_and_nan_on_block_boundaries(lib):
+    """A block reduces 8192 logits (16-byte loads): ties straddling a block boundary go to the
+    smaller index, and a NaN in a late block still wins."""
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal((3, V)) * 2.0).astype(np.float32)
+    x[0, [8191, 8192]] = 40.0
+    x[1, [29 * 8192 - 1, 29 * 8192]] = 40.0
+    x[2, 30 * 8192 + 5] = np.nan
+    _check(x)
+
+
+@pytest.mark.parametrize("n_rows", [64, 65, 130])
+def test_many_rows(lib, n_rows):
+    rng = np.random.default_rng(n_rows)
+    x = (rng.standard_normal((n_rows, 20000)) * 3.0).astype(np.float32)
+    x[n_rows - 1, 19999] = 99.0
+    _check(x)
+
+
 def test_rejects_bad_arguments(lib):
     import torch
 
