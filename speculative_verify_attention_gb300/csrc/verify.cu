@@ -109,6 +109,11 @@ __device__ __forceinline__ void load_codes(uint8_t* smem, const int8_t* plane, i
     const int n0 = threadIdx.x / CPR, c16 = threadIdx.x % CPR;
     const uint32_t dst0 = smem_u32(smem) + n0 * HD + ((c16 ^ (n0 & 7)) << 4);
     const int8_t* src0 = plane + (head_row0 + tile_key0 + n0) * HD + c16 * 16;
+    if (key_end - tile_key0 >= kKT) {  // a whole tile: every copy is live, offsets are immediates
+#pragma unroll
+        for (int k = 0; k < kKT / ROWS_PER_PASS; ++k) cp_async_16(dst0 + k * ROWS_PER_PASS * HD, src0 + k * ROWS_PER_PASS * HD, 16);
+        return;
+    }
     const int valid = key_end - tile_key0 - n0;  // rows of this thread's column still inside the slice
 #pragma unroll
     for (int k = 0; k < kKT / ROWS_PER_PASS; ++k) {
@@ -126,6 +131,16 @@ __device__ __forceinline__ void load_scales(uint8_t* smem, const uint16_t* plane
     constexpr int SB = HD / 16;
     const uint32_t base = smem_u32(smem);
     const uint16_t* src0 = plane + (head_row0 + tile_key0) * (HD / 32);
+    static_assert(kThreads >= kKT, "one scale row per thread");
+    if (key_end - tile_key0 >= kKT) {  // a whole tile
+        if (threadIdx.x < kKT) {
+            if constexpr (SB == 16)
+                cp_async_16(base + threadIdx.x * SB, src0 + threadIdx.x * (HD / 32), 16);
+            else
+                cp_async_8(base + threadIdx.x * SB, src0 + threadIdx.x * (HD / 32), 8);
+        }
+        return;
+    }
     for (int n = threadIdx.x; n < kKT; n += kThreads) {
         const bool ok = tile_key0 + n < key_end;
         const uint16_t* src = ok ? src0 + n * (HD / 32) : src0;
@@ -161,6 +176,12 @@ __device__ __forceinline__ void load_codes_v4(uint8_t* smem, const uint8_t* plan
     const int n0 = threadIdx.x / CPR, c16 = threadIdx.x % CPR;
     const uint32_t dst0 = smem_u32(smem) + n0 * ROWB + ((c16 ^ ((n0 >> 1) & (CPR - 1))) << 4);
     const uint8_t* src0 = plane + (head_row0 + tile_key0 + n0) * ROWB + c16 * 16;
+    if (key_end - tile_key0 >= kKT) {
+#pragma unroll
+        for (int k = 0; k < kKT / ROWS_PER_PASS; ++k)
+            cp_async_16(dst0 + k * ROWS_PER_PASS * ROWB, src0 + k * ROWS_PER_PASS * ROWB, 16);
+        return;
+    }
     const int valid = key_end - tile_key0 - n0;
 #pragma unroll
     for (int k = 0; k < kKT / ROWS_PER_PASS; ++k) {
