@@ -83,6 +83,11 @@ __device__ __forceinline__ void load_tile(uint8_t* smem, const uint16_t* plane, 
     const int n0 = threadIdx.x / CPR, c16 = threadIdx.x % CPR;
     const uint32_t dst0 = smem_u32(smem) + n0 * ROWB + ((c16 ^ phi(n0)) << 4);
     const uint16_t* src0 = plane + (head_row0 + tile_key0 + n0) * HD + c16 * 8;
+    if (key_end - tile_key0 >= kKT) {  // a whole tile: every copy is live, offsets are immediates
+#pragma unroll
+        for (int k = 0; k < kKT / ROWS_PER_PASS; ++k) cp_async_16(dst0 + k * ROWS_PER_PASS * ROWB, src0 + k * ROWS_PER_PASS * HD, 16);
+        return;
+    }
     const int valid = key_end - tile_key0 - n0;
 #pragma unroll
     for (int k = 0; k < kKT / ROWS_PER_PASS; ++k) {
