@@ -497,9 +497,10 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
                         for (int c = 0; c < 64; ++c)
                             if (key0 + c >= vis_end) x[c] = -INFINITY;
                     }
-                    float mt = x[0];
+                    float mq[4] = {x[0], x[1], x[2], x[3]};  // four chains
 #pragma unroll
-                    for (int c = 1; c < 64; ++c) mt = fmaxf(mt, x[c]);
+                    for (int c = 4; c < 64; ++c) mq[c & 3] = fmaxf(mq[c & 3], x[c]);
+                    const float mt = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
                     const float m_new = fmaxf(m_ref, mt * cs);
                     const bool need = m_new > m_ref + kRescaleThreshold || (m_ref == -INFINITY && m_new != -INFINITY);
                     if (__any_sync(0xffffffffu, need)) {
@@ -526,18 +527,18 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
                         }
                     }
                     uint32_t pk[32];
-                    float sum = 0.0f;
+                    float sq[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // four chains
                     const bool live = m_ref != -INFINITY;
                     const float neg = live ? -m_ref : 0.0f;
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
                         const float a = live ? ex2_approx(fmaf(x[2 * c], cs, neg)) : 0.0f;
                         const float bq = live ? ex2_approx(fmaf(x[2 * c + 1], cs, neg)) : 0.0f;
-                        sum += a + bq;
+                        sq[c & 3] += a + bq;
                         const __half2 h = __floats2half2_rn(a, bq);
                         pk[c] = *reinterpret_cast<const uint32_t*>(&h);
                     }
-                    l += sum;
+                    l += (sq[0] + sq[1]) + (sq[2] + sq[3]);
                     tc::tmem_st32(scol, pk);  // P overwrites the first 32 columns of this S buffer
                 } else {  // 128-key tiles: the S row in two 64-column halves, read twice
                     const uint32_t scol = tmem + lane_base + TM_S0 + b * BN;
@@ -561,13 +562,14 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
                         }
                     };
                     float x[64];
-                    float mt = -INFINITY;
+                    float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four chains
 #pragma unroll 1
                     for (int h = 0; h < BN / 64; ++h) {
                         load_half(h, x);
 #pragma unroll
-                        for (int c = 0; c < 64; ++c) mt = fmaxf(mt, x[c]);
+                        for (int c = 0; c < 64; ++c) mq[c & 3] = fmaxf(mq[c & 3], x[c]);
                     }
+                    const float mt = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
                     const float m_new = fmaxf(m_ref, mt * cs);
                     const bool need = m_new > m_ref + kRescaleThreshold || (m_ref == -INFINITY && m_new != -INFINITY);
                     if (__any_sync(0xffffffffu, need)) {
@@ -601,16 +603,16 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
                     for (int h = 0; h < BN / 64; ++h) {
                         if (BN > 64) load_half(h, x);  // at BN = 64 the half is still in registers
                         uint32_t pk[32];
-                        float sum = 0.0f;
+                        float sq[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // four chains
 #pragma unroll
                         for (int c = 0; c < 32; ++c) {
                             const float a = live ? ex2_approx(fmaf(x[2 * c], cs, neg)) : 0.0f;
                             const float bq = live ? ex2_approx(fmaf(x[2 * c + 1], cs, neg)) : 0.0f;
-                            sum += a + bq;
+                            sq[c & 3] += a + bq;
                             const __half2 hh = __floats2half2_rn(a, bq);
                             pk[c] = *reinterpret_cast<const uint32_t*>(&hh);
                         }
-                        l += sum;
+                        l += (sq[0] + sq[1]) + (sq[2] + sq[3]);
                         tc::tmem_st32(scol + 32 * h, pk);
                     }
                 }
