@@ -208,10 +208,13 @@ size_t attn_verify_append_q8_host_scratch_bytes(int n_rows, int n_q_heads, int h
  *            [n_rows][n_kv_heads][head_dim] each (pinned memory keeps the copy asynchronous)
  *   h_out  : host fp32 [n_rows][n_q_heads][head_dim]
  *   d_scratch : device, 16-byte aligned, attn_verify_append_q8_host_scratch_bytes(...) bytes
- * One host-to-device copy of h_in, the two kernels of attn_verify_append_q8, one
- * device-to-host copy into h_out, all queued on `stream`; h_out is valid once the stream has
- * reached that point (the call itself does not synchronise).  Errors as for
- * attn_verify_append_q8, WORKSPACE for a short scratch; nothing is queued on error.
+ * Pinned host buffers (mapped into the device address space, as every pinned allocation is
+ * on unified-addressing systems): a copy kernel reads h_in once over the host link into the
+ * scratch, the two kernels of attn_verify_append_q8 run, and the merge writes h_out in place.
+ * Pageable buffers: a host-to-device copy-engine transfer, the two kernels, a device-to-host
+ * transfer.  All queued on `stream`; h_out is valid once the stream has reached the end (the
+ * call itself does not synchronise).  Errors as for attn_verify_append_q8, WORKSPACE for a
+ * short scratch; nothing is queued on error.
  */
 int attn_verify_append_q8_host(const float* h_in, int n_rows, int n_q_heads, const kvq8_cache* kv,
                                int q_pos0, float softmax_scale, float* h_out, void* d_scratch,

@@ -947,6 +947,38 @@ extern "C" size_t attn_verify_append_q8_host_scratch_bytes(int n_rows, int n_q_h
     return host_scratch(n_rows, n_q_heads, head_dim, q_pos0, n_kv_heads, n_split, &h) ? h.total : 0;
 }
 
+namespace {
+// Device address of pinned host memory mapped into the device address space (null if `p` is
+// not such memory: pageable memory goes through the copy engine instead).
+const void* mapped_device_ptr(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+// n16 16-byte words from mapped host memory to device memory: every word read once over the
+// host link (lower latency than a copy-engine transfer for the few hundred KB of a window).
+constexpr int kCopyThreads = 256, kCopyPer = 4;
+__global__ void __launch_bounds__(kCopyThreads) host_copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                                 int n16) {
+    const int i0 = blockIdx.x * (kCopyThreads * kCopyPer) + threadIdx.x;
+    uint4 v[kCopyPer];
+#pragma unroll
+    for (int k = 0; k < kCopyPer; ++k) {
+        const int i = i0 + k * kCopyThreads;
+        if (i < n16) v[k] = src[i];
+    }
+#pragma unroll
+    for (int k = 0; k < kCopyPer; ++k) {
+        const int i = i0 + k * kCopyThreads;
+        if (i < n16) dst[i] = v[k];
+    }
+}
+}  // namespace
+
 extern "C" int attn_verify_append_q8_host(const float* h_in, int n_rows, int n_q_heads, const kvq8_cache* kv,
                                           int q_pos0, float softmax_scale, float* h_out, void* d_scratch,
                                           size_t scratch_bytes, int n_split, kvq8_stream_t stream) {
@@ -971,10 +1003,23 @@ extern "C" int attn_verify_append_q8_host(const float* h_in, int n_rows, int n_q
     const float* v_new = k_new + (size_t)n_rows * kv->n_kv_heads * kv->head_dim;
     float* out = reinterpret_cast<float*>(base + h.out_off);
     cudaStream_t s = (cudaStream_t)stream;
-    if (cudaMemcpyAsync(base, h_in, h.in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return KVQ8_ERR_CUDA;
-    const int rc = kvq8::verify_impl(q, n_rows, n_q_heads, kv, q_pos0 + n_rows, q_pos0, nullptr, softmax_scale, out,
-                                     base + h.ws_off, h.ws_bytes, n_split, stream, k_new, v_new);
-    if (rc != KVQ8_OK) return rc;
+    // Pinned (mapped) host buffers: the inputs come in through a copy kernel and the merge
+    // writes the output into h_out itself; pageable ones go through the copy engine.
+    const void* m_in = mapped_device_ptr(h_in);
+    float* m_out = static_cast<float*>(const_cast<void*>(mapped_device_ptr(h_out)));
+    if (m_in && kvq8::aligned16(m_in) && h.in_bytes % 16 == 0) {
+        const int n16 = (int)(h.in_bytes / 16);
+        host_copy_kernel<<<(n16 + kCopyThreads * kCopyPer - 1) / (kCopyThreads * kCopyPer), kCopyThreads, 0, s>>>(
+            static_cast<const uint4*>(m_in), reinterpret_cast<uint4*>(base), n16);
+        if (kvq8::launch_status() != KVQ8_OK) return KVQ8_ERR_CUDA;
+    } else if (cudaMemcpyAsync(base, h_in, h.in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+        return KVQ8_ERR_CUDA;
+    }
+    const bool direct_out = m_out && kvq8::aligned16(m_out);
+    const int rc = kvq8::verify_impl(q, n_rows, n_q_heads, kv, q_pos0 + n_rows, q_pos0, nullptr, softmax_scale,
+                                     direct_out ? m_out : out, base + h.ws_off, h.ws_bytes, n_split, stream, k_new,
+                                     v_new);
+    if (rc != KVQ8_OK || direct_out) return rc;
     const size_t out_bytes = (size_t)n_rows * n_q_heads * kv->head_dim * sizeof(float);
     return cudaMemcpyAsync(h_out, out, out_bytes, cudaMemcpyDeviceToHost, s) == cudaSuccess ? KVQ8_OK
                                                                                               : KVQ8_ERR_CUDA;

@@ -144,9 +144,11 @@ def test_append_verify_rejects_bad_arguments(lib):
     torch.cuda.synchronize()
 
 
-def test_host_buffer_entry_matches_device_entry(lib):
-    """attn_verify_append_q8_host (pinned host in/out, one copy each way) gives the device
-    entry's output bit for bit and the same cache bytes."""
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_buffer_entry_matches_device_entry(lib, pinned):
+    """attn_verify_append_q8_host gives the device entry's output bit for bit and the same
+    cache bytes: with pinned buffers (inputs through a copy kernel, the output written in
+    place by the merge) and with pageable ones (copy-engine transfers)."""
     import torch
 
     from speculative_verify_attention_gb300 import (attn_verify_append_q8, attn_verify_append_q8_host,
@@ -157,8 +159,10 @@ def test_host_buffer_entry_matches_device_entry(lib):
     g1, _ = build_caches(_context_only(inp, ctx), capacity=w.kv_len)
     g2, _ = build_caches(_context_only(inp, ctx), capacity=w.kv_len)
     kn, vn = inp.k[ctx:ctx + T], inp.v[ctx:ctx + T]
-    h_in = torch.from_numpy(np.concatenate([inp.q.ravel(), kn.ravel(), vn.ravel()]).astype(np.float32)).pin_memory()
-    h_out = torch.empty(inp.q.size, dtype=torch.float32).pin_memory()
+    h_in = torch.from_numpy(np.concatenate([inp.q.ravel(), kn.ravel(), vn.ravel()]).astype(np.float32))
+    h_out = torch.full((inp.q.size,), float("nan"), dtype=torch.float32)
+    if pinned:
+        h_in, h_out = h_in.pin_memory(), h_out.pin_memory()
     scratch = torch.empty(attn_verify_append_q8_host_scratch_bytes(T, 24, 256, ctx, 4), dtype=torch.uint8,
                           device="cuda")
     attn_verify_append_q8_host(h_in, T, 24, g1, ctx, w.softmax_scale, h_out, scratch)
