@@ -440,6 +440,7 @@ def run_native(args, world, rank, local):
         torch.cuda.empty_cache()
         prompt["f16"] = prompt_bench(args, dev, fp16_peak, _wl.PROMPT, pool="f16")
     head = head_bench(dev, hbm_peak, args.ring_l2) if not args.no_head else None
+    quant = quantize_bench(dev, hbm_peak) if not args.no_head else None
 
     result = None
     if rank == 0:
@@ -478,6 +479,7 @@ def run_native(args, world, rank, local):
             "long_context": long_ctx,
             "prompt": prompt,
             "verify_head": head,
+            "quantize": quant,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "us_per_step": e2e_sec / e2e_steps * 1e6,
@@ -530,6 +532,40 @@ def head_bench(dev, hbm_peak, ring_l2):
         del ring
         torch.cuda.empty_cache()
     return res
+
+
+def quantize_bench(dev, hbm_peak):
+    """kvq8_append (Q8_0 quantiser, both planes in one launch) of a 32,768-token prefill chunk
+    of a 4-KV-head hd256 cache: 67 M values, 268 MB fp32 read and 71 MB written per call, so the
+    inputs exceed the L2 and every call streams them from HBM.  Device time per call from CUDA
+    events around 20 calls."""
+    import torch
+
+    from speculative_verify_attention_gb300 import KVCacheQ8
+    n_tok, hkv, hd = 32768, 4, 256
+    gen = torch.Generator(device=dev).manual_seed(91)
+    k = torch.randn((n_tok, hkv, hd), device=dev, generator=gen)
+    v = torch.randn((n_tok, hkv, hd), device=dev, generator=gen)
+    cache = KVCacheQ8(hkv, hd, n_tok, device=dev)
+    for _ in range(3):
+        cache.append(k, v, 0)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = 20
+    a.record()
+    for _ in range(n):
+        cache.append(k, v, 0)
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / n
+    values = 2 * n_tok * hkv * hd
+    nbytes = values * 4 + values + values // 32 * 2
+    gbs = nbytes / (us * 1e-6) / 1e9
+    del k, v, cache
+    torch.cuda.empty_cache()
+    return {"workload": f"kvq8_append-{n_tok}tok-{hkv}kv-hd{hd}", "us_per_call": us, "values": values,
+            "bytes_per_call": nbytes, "gbs": gbs, "hbm_frac": gbs / hbm_peak,
+            "l2": "inputs (268 MB) larger than the L2"}
 
 
 def prompt_bench(args, dev, fp16_peak, w=None, pool="q8"):

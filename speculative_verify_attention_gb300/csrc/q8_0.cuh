@@ -13,6 +13,39 @@
 
 namespace kvq8 {
 
+// Codes of one lane's 4 values x / d, rounded half away from zero and clamped to [-qmax, qmax],
+// equal to rounding the IEEE quotient fl(x / d).  The fast form rounds y = x * r, r =
+// rcp.approx(d) (relative error about 2^-23), to the nearest integer: y differs from fl(x / d)
+// by at most |x / d| (2^-23 + 2^-24 + 2^-24) < 2^-14 (|x / d| < 128 here), and rounding to an
+// integer only changes at the half-integers, so when y is farther than 2^-12 from one the
+// nearest integer of y is the code (and no tie arises).  A lane with a value that near a
+// half-integer, or with a y that is not finite (d subnormal, flushed by the approximation),
+// recomputes its codes with the IEEE division; the warp takes that branch only if some lane
+// needs it.  d == 0 gives codes 0.  Every lane of the warp must call it.
+template <int QMAX>
+__device__ __forceinline__ void codes_of(const float (&x)[4], float d, int (&c)[4]) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
+    bool slow = false;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float y = x[e] * r;
+        const float n = rintf(y);
+        c[e] = (int)n;
+        slow |= !(fabsf(y) < 1024.0f) || fabsf(y - n) > 0.5f - 0x1p-12f;
+    }
+    if (d == 0.0f) {
+        slow = false;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c[e] = 0;
+    }
+    if (__any_sync(0xffffffffu, slow) && slow) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            c[e] = (int)fminf(fmaxf(roundf(__fdiv_rn(x[e], d)), -(float)QMAX), (float)QMAX);
+    }
+}
+
 // One 32-value block held by 8 consecutive lanes (lanes 8i .. 8i+7 of the warp), 4 values per
 // lane in block order.  Every lane of the warp must call it (the max is a warp shuffle).
 // Returns this lane's 4 codes packed little-endian; *scale_bits gets the block's fp16 scale.
@@ -22,13 +55,11 @@ __device__ __forceinline__ uint32_t q8_0_block(float4 v, uint16_t* scale_bits) {
     for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float d32 = __fdiv_rn(amax, 127.0f);
     const float xs[4] = {v.x, v.y, v.z, v.w};
+    int c[4];
+    codes_of<127>(xs, d32, c);
     uint32_t packed = 0;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        float r = 0.0f;
-        if (d32 != 0.0f) r = fminf(fmaxf(roundf(__fdiv_rn(xs[e], d32)), -127.0f), 127.0f);
-        packed |= (uint32_t)(uint8_t)(int8_t)(int)r << (8 * e);
-    }
+    for (int e = 0; e < 4; ++e) packed |= (uint32_t)(c[e] & 0xff) << (8 * e);
     *scale_bits = __half_as_ushort(__float2half_rn(d32));
     return packed;
 }
@@ -48,13 +79,11 @@ __device__ __forceinline__ uint32_t q4_block(float4 v, uint16_t* scale_bits) {
     for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float d32 = __fdiv_rn(amax, 7.0f);
     const float xs[4] = {v.x, v.y, v.z, v.w};
+    int c[4];
+    codes_of<7>(xs, d32, c);
     uint32_t packed = 0;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        float r = 0.0f;
-        if (d32 != 0.0f) r = fminf(fmaxf(roundf(__fdiv_rn(xs[e], d32)), -7.0f), 7.0f);
-        packed |= (uint32_t)((int)r + 8) << (4 * e);
-    }
+    for (int e = 0; e < 4; ++e) packed |= (uint32_t)(c[e] + 8) << (4 * e);
     *scale_bits = __half_as_ushort(__float2half_rn(d32));
     return packed;
 }

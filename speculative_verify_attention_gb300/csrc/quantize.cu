@@ -4,10 +4,11 @@
 // a warp-per-block quantiser that reduces max|x| over the 32-value block with shuffles
 // and writes the fp16 scale and 32 int8 codes, bitwise equal to its CPU reference.
 //
-// Here a warp covers four blocks: eight lanes per block, four values per lane (one
-// 16-byte load), a 3-step shuffle max, then per value an IEEE fp32 division and round
-// half away from zero (q8_0_block).  Bandwidth-bound: 4 bytes read, 1 + 1/16 bytes
-// written per value.
+// Here a warp covers four blocks of a token row: eight lanes per block, four values per lane
+// (one 16-byte load), a 3-step shuffle max, then per value an IEEE fp32 division and round
+// half away from zero (q8_0_block).  A thread keeps one column for four tokens, so the
+// (head, block) position is worked out once per thread.  Bandwidth-bound: 4 bytes read,
+// 1 + 1/16 bytes written per value.
 // kvq8_append writes both planes (K and V) of a cache in one launch; kvk8v4_append does the
 // same for a K8V4 pool (K as Q8_0, V as 4-bit blocks, q4_block).
 #include "common.cuh"
@@ -16,41 +17,51 @@
 namespace kvq8 {
 namespace {
 
-// Plane 0 (x0 -> codes0/scales0) holds blocks [0, n_blocks); when x1 is given, plane 1
-// (x1 -> codes1/scales1) holds blocks [n_blocks, 2 n_blocks) of the same launch.
-__global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4* __restrict__ x0,
-                                                            const float4* __restrict__ x1, int64_t n_blocks,
-                                                            int n_kv_heads, int nb_per_head_row,
-                                                            int8_t* __restrict__ codes0,
-                                                            uint16_t* __restrict__ scales0,
-                                                            int8_t* __restrict__ codes1,
-                                                            uint16_t* __restrict__ scales1, int capacity,
-                                                            int pos0) {
-    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t blk_all = gid >> 3;  // Q8_0 block handled by this lane's group of 8
-    const bool second = blk_all >= n_blocks;
-    const int64_t blk = second ? blk_all - n_blocks : blk_all;
+// Grid (token groups, column chunks, planes): a block quantises columns
+// [256 y, 256 y + 256) of kTokPerBlock consecutive token rows of one plane (plane z: x0 ->
+// codes0/scales0, or x1 -> codes1/scales1).  A row holds n_kv_heads * head_dim values, read as
+// float4 column j: head j / (head_dim/4), block (j mod head_dim/4) / 8 of that head.  A thread
+// keeps one column for all its tokens, so the (head, block) split is done once per thread; its
+// kTokPerBlock loads are issued before any is used.  Lanes past the row or past the last
+// token quantise zeros (every lane takes part in the block's shuffle max) and store nothing.
+constexpr int kQuantThreads = 256;
+constexpr int kTokPerBlock = 4;
+
+__global__ void __launch_bounds__(kQuantThreads) quantize_q8_0_kernel(const float4* __restrict__ x0,
+                                                                      const float4* __restrict__ x1, int n_tok,
+                                                                      int n_kv_heads, int head_dim,
+                                                                      int8_t* __restrict__ codes0,
+                                                                      uint16_t* __restrict__ scales0,
+                                                                      int8_t* __restrict__ codes1,
+                                                                      uint16_t* __restrict__ scales1, int capacity,
+                                                                      int pos0) {
+    const bool second = blockIdx.z != 0;
     const float4* x = second ? x1 : x0;
     int8_t* codes = second ? codes1 : codes0;
     uint16_t* scales = second ? scales1 : scales0;
-    const int sub = threadIdx.x & 7;
-    const bool live = blk_all < (x1 ? 2 * n_blocks : n_blocks);
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (live) v = __ldg(x + blk * 8 + sub);
-    uint16_t scale_bits;
-    const uint32_t packed = q8_0_block(v, &scale_bits);
-    if (!live) return;
-
-    // block index -> (token, kv head, block within the head row)
-    const int64_t row_blocks = (int64_t)n_kv_heads * nb_per_head_row;
-    const int64_t tok = blk / row_blocks;
-    const int64_t rem = blk - tok * row_blocks;
-    const int h = (int)(rem / nb_per_head_row);
-    const int b = (int)(rem - (int64_t)h * nb_per_head_row);
-    const int64_t row = (int64_t)h * capacity + pos0 + tok;
-    int8_t* dst = codes + row * (int64_t)nb_per_head_row * kQBlock + b * kQBlock + sub * 4;
-    *reinterpret_cast<uint32_t*>(dst) = packed;
-    if (sub == 0) scales[row * nb_per_head_row + b] = scale_bits;
+    const int f4_head = head_dim / 4;
+    const int row_f4 = n_kv_heads * f4_head;
+    const int j = blockIdx.y * kQuantThreads + threadIdx.x;
+    const bool col_ok = j < row_f4;
+    const int h = j / f4_head, i = j - h * f4_head;  // head and float4 within the head row
+    const int tok0 = blockIdx.x * kTokPerBlock;
+    float4 v[kTokPerBlock];
+#pragma unroll
+    for (int t = 0; t < kTokPerBlock; ++t) {
+        v[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (col_ok && tok0 + t < n_tok) v[t] = __ldg(x + (int64_t)(tok0 + t) * row_f4 + j);
+    }
+    const int nb = head_dim / kQBlock;
+    const int64_t row0 = (int64_t)h * capacity + pos0 + tok0;  // cache row of the first token
+#pragma unroll
+    for (int t = 0; t < kTokPerBlock; ++t) {
+        uint16_t scale_bits;
+        const uint32_t packed = q8_0_block(v[t], &scale_bits);
+        if (col_ok && tok0 + t < n_tok) {
+            *reinterpret_cast<uint32_t*>(codes + (row0 + t) * head_dim + i * 4) = packed;
+            if ((i & 7) == 0) scales[(row0 + t) * nb + (i >> 3)] = scale_bits;
+        }
+    }
 }
 
 }  // namespace
@@ -62,52 +73,60 @@ namespace {
 int launch_quantize(const float* x0, const float* x1, int n_tok, int n_kv_heads, int head_dim, int8_t* codes0,
                     uint16_t* scales0, int8_t* codes1, uint16_t* scales1, int capacity, int pos0,
                     cudaStream_t stream) {
-    const int nb = head_dim / kQBlock;
-    const int64_t n_blocks = (int64_t)n_tok * n_kv_heads * nb;
-    const int64_t threads = n_blocks * 8 * (x1 ? 2 : 1);
-    const int64_t grid = (threads + 255) / 256;
-    if (grid > 0x7fffffffLL) return KVQ8_ERR_UNSUPPORTED;
-    quantize_q8_0_kernel<<<(unsigned)grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(x0),
-                                                           reinterpret_cast<const float4*>(x1), n_blocks,
-                                                           n_kv_heads, nb, codes0, scales0, codes1, scales1,
-                                                           capacity, pos0);
+    const int64_t row_f4 = (int64_t)n_kv_heads * head_dim / 4;
+    const int64_t gy = (row_f4 + kQuantThreads - 1) / kQuantThreads;
+    const int64_t gx = ((int64_t)n_tok + kTokPerBlock - 1) / kTokPerBlock;
+    if (row_f4 > 0x7fffffffLL - kQuantThreads || gy > 65535) return KVQ8_ERR_UNSUPPORTED;
+    const dim3 grid((unsigned)gx, (unsigned)gy, x1 ? 2u : 1u);
+    quantize_q8_0_kernel<<<grid, kQuantThreads, 0, stream>>>(reinterpret_cast<const float4*>(x0),
+                                                             reinterpret_cast<const float4*>(x1), n_tok, n_kv_heads,
+                                                             head_dim, codes0, scales0, codes1, scales1, capacity,
+                                                             pos0);
     return launch_status();
 }
 
-// K8V4 append: blocks [0, n_blocks) are K (Q8_0), [n_blocks, 2 n_blocks) V (4-bit), one
-// 8-lane group per 32-value block as in the Q8_0 kernel.
-__global__ void __launch_bounds__(256) append_k8v4_kernel(const float4* __restrict__ k, const float4* __restrict__ v,
-                                                          int64_t n_blocks, int n_kv_heads, int nb_per_head_row,
-                                                          int8_t* __restrict__ k_codes, uint16_t* __restrict__ k_scales,
-                                                          uint8_t* __restrict__ v_codes,
-                                                          uint16_t* __restrict__ v_scales, int capacity, int pos0) {
-    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t blk_all = gid >> 3;
-    const bool is_v = blk_all >= n_blocks;
-    const int64_t blk = is_v ? blk_all - n_blocks : blk_all;
-    const int sub = threadIdx.x & 7;
-    const bool live = blk_all < 2 * n_blocks;
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (live) x = __ldg((is_v ? v : k) + blk * 8 + sub);
-    // both quantisers run on every lane (their shuffles stay inside the lane's 8-lane group)
-    // and each lane keeps its own plane's result
-    uint16_t sq8, sq4;
-    const uint32_t p8 = q8_0_block(x, &sq8);
-    const uint32_t p4 = q4_block(x, &sq4);
-    if (!live) return;
-    const int64_t row_blocks = (int64_t)n_kv_heads * nb_per_head_row;
-    const int64_t tok = blk / row_blocks;
-    const int64_t rem = blk - tok * row_blocks;
-    const int h = (int)(rem / nb_per_head_row);
-    const int b = (int)(rem - (int64_t)h * nb_per_head_row);
-    const int64_t row = (int64_t)h * capacity + pos0 + tok;
-    if (!is_v) {
-        *reinterpret_cast<uint32_t*>(k_codes + row * (int64_t)nb_per_head_row * kQBlock + b * kQBlock + sub * 4) = p8;
-        if (sub == 0) k_scales[row * nb_per_head_row + b] = sq8;
-    } else {
-        *reinterpret_cast<uint16_t*>(v_codes + row * (int64_t)nb_per_head_row * (kQBlock / 2) + b * (kQBlock / 2) +
-                                     sub * 2) = (uint16_t)p4;
-        if (sub == 0) v_scales[row * nb_per_head_row + b] = sq4;
+// K8V4 append, the same grid: plane 0 quantises K to Q8_0, plane 1 V to 4-bit blocks.
+__global__ void __launch_bounds__(kQuantThreads) append_k8v4_kernel(const float4* __restrict__ k,
+                                                                    const float4* __restrict__ v, int n_tok,
+                                                                    int n_kv_heads, int head_dim,
+                                                                    int8_t* __restrict__ k_codes,
+                                                                    uint16_t* __restrict__ k_scales,
+                                                                    uint8_t* __restrict__ v_codes,
+                                                                    uint16_t* __restrict__ v_scales, int capacity,
+                                                                    int pos0) {
+    const bool is_v = blockIdx.z != 0;
+    const float4* x = is_v ? v : k;
+    const int f4_head = head_dim / 4;
+    const int row_f4 = n_kv_heads * f4_head;
+    const int j = blockIdx.y * kQuantThreads + threadIdx.x;
+    const bool col_ok = j < row_f4;
+    const int h = j / f4_head, i = j - h * f4_head;
+    const int tok0 = blockIdx.x * kTokPerBlock;
+    float4 xv[kTokPerBlock];
+#pragma unroll
+    for (int t = 0; t < kTokPerBlock; ++t) {
+        xv[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (col_ok && tok0 + t < n_tok) xv[t] = __ldg(x + (int64_t)(tok0 + t) * row_f4 + j);
+    }
+    const int nb = head_dim / kQBlock;
+    const int64_t row0 = (int64_t)h * capacity + pos0 + tok0;
+#pragma unroll
+    for (int t = 0; t < kTokPerBlock; ++t) {
+        const bool st = col_ok && tok0 + t < n_tok;
+        uint16_t sc;
+        if (!is_v) {  // uniform per block: every lane of a warp runs the same quantiser
+            const uint32_t p8 = q8_0_block(xv[t], &sc);
+            if (st) {
+                *reinterpret_cast<uint32_t*>(k_codes + (row0 + t) * head_dim + i * 4) = p8;
+                if ((i & 7) == 0) k_scales[(row0 + t) * nb + (i >> 3)] = sc;
+            }
+        } else {
+            const uint32_t p4 = q4_block(xv[t], &sc);
+            if (st) {
+                *reinterpret_cast<uint16_t*>(v_codes + (row0 + t) * (head_dim / 2) + i * 2) = (uint16_t)p4;
+                if ((i & 7) == 0) v_scales[(row0 + t) * nb + (i >> 3)] = sc;
+            }
+        }
     }
 }
 
@@ -126,12 +145,12 @@ extern "C" int kvk8v4_append(const float* k, const float* v, int n_tok, const kv
     if (!aligned16(k) || !aligned16(v) || !aligned16(kv->k_codes) || !aligned16(kv->k_scales) ||
         !aligned16(kv->v_codes) || !aligned16(kv->v_scales))
         return KVQ8_ERR_MISALIGNED;
-    const int nb = kv->head_dim / kQBlock;
-    const int64_t n_blocks = (int64_t)n_tok * kv->n_kv_heads * nb;
-    const int64_t grid = (n_blocks * 16 + 255) / 256;
-    if (grid > 0x7fffffffLL) return KVQ8_ERR_UNSUPPORTED;
-    append_k8v4_kernel<<<(unsigned)grid, 256, 0, (cudaStream_t)stream>>>(
-        reinterpret_cast<const float4*>(k), reinterpret_cast<const float4*>(v), n_blocks, kv->n_kv_heads, nb,
+    const int64_t row_f4 = (int64_t)kv->n_kv_heads * kv->head_dim / 4;
+    const int64_t gy = (row_f4 + kQuantThreads - 1) / kQuantThreads;
+    const int64_t gx = ((int64_t)n_tok + kTokPerBlock - 1) / kTokPerBlock;
+    if (row_f4 > 0x7fffffffLL - kQuantThreads || gy > 65535) return KVQ8_ERR_UNSUPPORTED;
+    append_k8v4_kernel<<<dim3((unsigned)gx, (unsigned)gy, 2u), kQuantThreads, 0, (cudaStream_t)stream>>>(
+        reinterpret_cast<const float4*>(k), reinterpret_cast<const float4*>(v), n_tok, kv->n_kv_heads, kv->head_dim,
         const_cast<int8_t*>(kv->k_codes), const_cast<uint16_t*>(kv->k_scales), const_cast<uint8_t*>(kv->v_codes),
         const_cast<uint16_t*>(kv->v_scales), kv->capacity, pos0);
     return launch_status();

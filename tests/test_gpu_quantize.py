@@ -142,3 +142,23 @@ def test_append_rejects_bad_arguments(lib):
     assert e.value.status == 1
     with pytest.raises(ValueError):           # shape does not match the cache
         kvq8_append(torch.zeros((4, 2, 128), device="cuda"), k, c, 0)
+
+
+def test_quotients_near_half_integers_bit_exact(lib):
+    """Values one to four ulps either side of (k + 1/2) d for many block scales d: the
+    quotients x / d sit right at the rounding boundaries, where a quotient computed as x times
+    an approximate reciprocal could round the other way than the IEEE division does."""
+    rng = np.random.default_rng(23)
+    n_blk = 4096
+    amax = (rng.uniform(0.5, 2.0, n_blk) * np.exp2(rng.integers(-20, 20, n_blk))).astype(np.float32)
+    d = (amax / np.float32(127.0)).astype(np.float32)            # the IEEE fp32 scale the quantiser uses
+    k = rng.integers(-127, 127, (n_blk, 31)).astype(np.float32)
+    base = ((k + np.float32(0.5)) * d[:, None]).astype(np.float32)
+    steps = rng.integers(-4, 5, (n_blk, 31)).astype(np.int32)
+    vals = base.view(np.int32) + np.where(base >= 0, steps, -steps)
+    vals = vals.view(np.float32)
+    vals = np.clip(vals, -amax[:, None], amax[:, None])          # keep amax the block maximum
+    x = np.concatenate([amax[:, None], vals], axis=1).reshape(n_blk // 8, 1, 256)
+    codes, scales = _gpu_quant(x)
+    q, dd = oracle.quantize_q8_0(x)
+    assert np.array_equal(codes, q.transpose(1, 0, 2)) and np.array_equal(scales, dd.transpose(1, 0, 2))

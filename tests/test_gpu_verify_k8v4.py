@@ -185,3 +185,30 @@ def test_prompt_k8v4_full_workload_sampled(lib):
     assert np.all(np.isfinite(got))
     assert rel_err(np.stack([got[i, h] for i, h in sel]), ref) <= PROMPT_TOL
     assert kvq8_device_error(reset=True) == 0
+
+
+def test_q4_quotients_near_half_integers_bit_exact(lib):
+    """4-bit V blocks with values a few ulps around (k + 1/2) d: the append kernel's codes
+    equal the oracle's IEEE-division codes."""
+    import torch
+
+    from speculative_verify_attention_gb300 import KVCacheK8V4, kvk8v4_append
+    rng = np.random.default_rng(31)
+    n_blk = 2048
+    amax = (rng.uniform(0.5, 2.0, n_blk) * np.exp2(rng.integers(-16, 16, n_blk))).astype(np.float32)
+    d = (amax / np.float32(7.0)).astype(np.float32)
+    kk = rng.integers(-7, 7, (n_blk, 31)).astype(np.float32)
+    base = ((kk + np.float32(0.5)) * d[:, None]).astype(np.float32)
+    steps = rng.integers(-4, 5, (n_blk, 31)).astype(np.int32)
+    vals = (base.view(np.int32) + np.where(base >= 0, steps, -steps)).view(np.float32)
+    vals = np.clip(vals, -amax[:, None], amax[:, None])
+    v = np.concatenate([amax[:, None], vals], axis=1).reshape(n_blk // 8, 1, 256)
+    n_tok = v.shape[0]
+    cache = KVCacheK8V4(1, 256, n_tok, device="cuda")
+    kvk8v4_append(torch.from_numpy(v).cuda(), torch.from_numpy(v).cuda(), cache, 0)
+    torch.cuda.synchronize()
+    q4, d4 = oracle.quantize_q4(v)
+    got_codes = cache.v_codes.cpu().numpy()[0]
+    got_scales = cache.v_scales.cpu().numpy().view(np.uint16)[0]
+    assert np.array_equal(got_scales, d4[:, 0, :])
+    assert np.array_equal(got_codes, q4[:, 0, :])
