@@ -32,7 +32,7 @@ __device__ __forceinline__ void codes_of(const float (&x)[4], float d, int (&c)[
         const float y = x[e] * r;
         const float n = rintf(y);
         c[e] = (int)n;
-        slow |= !(fabsf(y) < 1024.0f) || fabsf(y - n) > 0.5f - 0x1p-12f;
+        slow |= !(fabsf(y - n) <= 0.5f - 0x1p-12f);  // also true for a y that is not finite
     }
     if (d == 0.0f) {
         slow = false;
@@ -57,9 +57,11 @@ __device__ __forceinline__ uint32_t q8_0_block(float4 v, uint16_t* scale_bits) {
     const float xs[4] = {v.x, v.y, v.z, v.w};
     int c[4];
     codes_of<127>(xs, d32, c);
-    uint32_t packed = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) packed |= (uint32_t)(c[e] & 0xff) << (8 * e);
+    // low bytes of the four codes, in order: two byte permutes pair them, a third joins the pairs
+    uint32_t t01, t23, packed;
+    asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(t01) : "r"(c[0]), "r"(c[1]));
+    asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(t23) : "r"(c[2]), "r"(c[3]));
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(packed) : "r"(t01), "r"(t23));
     *scale_bits = __half_as_ushort(__float2half_rn(d32));
     return packed;
 }
