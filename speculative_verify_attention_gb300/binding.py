@@ -482,9 +482,11 @@ def attn_verify_append_q8_host_scratch_bytes(n_rows: int, n_q_heads: int, head_d
 def attn_verify_append_q8_host(h_in: torch.Tensor, n_rows: int, n_q_heads: int, cache: KVCacheQ8, q_pos0: int,
                                softmax_scale: float, h_out: torch.Tensor, scratch: torch.Tensor, n_split: int = 0,
                                stream=None) -> None:
-    """attn_verify_append_q8 from and to host tensors: h_in (CPU fp32, pinned for an async copy)
-    holds q [T][Hq][hd] then k_new and v_new [T][Hkv][hd]; h_out (CPU fp32 [T][Hq][hd]) is
-    written once the stream gets there.  scratch: device bytes from the scratch-size query."""
+    """attn_verify_append_q8 from and to host tensors: h_in (CPU fp32) holds q [T][Hq][hd] then
+    k_new and v_new [T][Hkv][hd]; h_out (CPU fp32 [T][Hq][hd]) is written once the stream gets
+    there.  Pinned tensors are read by a copy kernel and written in place by the merge;
+    pageable ones go through copy-engine transfers.  scratch: device bytes from the
+    scratch-size query."""
     for t, name in ((h_in, "h_in"), (h_out, "h_out")):
         if t.device.type != "cpu" or t.dtype != torch.float32 or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CPU float32 tensor")
