@@ -298,14 +298,25 @@ def run_native(args, world, rank, local):
                           dtype=torch.uint8, device=dev) for T in VERIFY_T}
     kv_bytes_step = sum(ws_[T].kv_bytes() for T in VERIFY_T)
 
-    def step(s, do_append=True):
-        c = ring[s % n_ring]
-        for T in VERIFY_T:
-            if do_append:   # append of the window's K/V fused with the verify scan
-                attn_verify_append_q8(q[T], knew[T], vnew[T], c, ctx, w0.softmax_scale, out=out[T],
-                                      workspace=wsb[T])
-            else:
-                attn_verify_q8(q[T], c, ctx + T, ctx, w0.softmax_scale, out=out[T], workspace=wsb[T])
+    side = [torch.cuda.Stream(device=dev) for _ in VERIFY_T]
+
+    def step(s, do_append=True, concurrent=True):
+        # the step's windows are independent problems (their own caches of the ring); with
+        # concurrent=True each runs on a stream of its own, as two sequences' verify calls would
+        cur = torch.cuda.current_stream()
+        for j, T in enumerate(VERIFY_T):
+            c = ring[(s + j * (n_ring // len(VERIFY_T))) % n_ring]
+            st = side[j] if concurrent else cur
+            st.wait_stream(cur)
+            with torch.cuda.stream(st):
+                if do_append:   # append of the window's K/V fused with the verify scan
+                    attn_verify_append_q8(q[T], knew[T], vnew[T], c, ctx, w0.softmax_scale, out=out[T],
+                                          workspace=wsb[T])
+                else:
+                    attn_verify_q8(q[T], c, ctx + T, ctx, w0.softmax_scale, out=out[T], workspace=wsb[T])
+        if concurrent:
+            for st in side:
+                cur.wait_stream(st)
 
     launches_per_step = len(VERIFY_T) * 2   # verify split (with the append) + combine per T
 
@@ -324,7 +335,7 @@ def run_native(args, world, rank, local):
         return g
 
     g_step = capture()
-    g_verify = capture(do_append=False)
+    g_verify = capture(do_append=False, concurrent=False)   # one call at a time: the per-call time
     reps = max(1, int(np.ceil(args.steps / GRAPH_STEPS)))
     steps = reps * GRAPH_STEPS
     wreps = max(1, int(np.ceil(args.warmup / GRAPH_STEPS)))
@@ -466,7 +477,9 @@ def run_native(args, world, rank, local):
                        "parallelism": f"replicas x{world}", "l2": f"ring of {n_ring} caches, "
                        f"{n_ring * cache_bytes / 2**20:.0f} MiB > 4x L2 (every step reads a different cache)",
                        "step": "per T in {4,8}: attn_verify_append_q8 (K/V of T new tokens quantised into the "
-                               "cache by the verify kernel's window slice; scan over ctx+T)",
+                               "cache by the verify kernel's window slice; scan over ctx+T); the two windows are "
+                               "independent (each on its own cache of the ring) and run concurrently on two "
+                               "streams, joined at the end of the step",
                        "graph": f"{GRAPH_STEPS} steps per CUDA graph replay"},
             "us_per_call": us_per_call_verify, "verify_only_gbs": verify_gbs,
             "hbm_frac": verify_gbs / hbm_peak, "per_T": per_t,
