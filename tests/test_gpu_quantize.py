@@ -162,3 +162,17 @@ def test_quotients_near_half_integers_bit_exact(lib):
     codes, scales = _gpu_quant(x)
     q, dd = oracle.quantize_q8_0(x)
     assert np.array_equal(codes, q.transpose(1, 0, 2)) and np.array_equal(scales, dd.transpose(1, 0, 2))
+
+
+def test_subnormal_scales_bit_exact(lib):
+    """Blocks whose scale max|x| / 127 is an fp32 subnormal (the reciprocal approximation flushes
+    it, so every code comes from the IEEE division), next to blocks with normal scales."""
+    rng = np.random.default_rng(24)
+    x = rng.standard_normal((64, 1, 256)).astype(np.float32)
+    tiny = np.array([1e-36, 3e-37, 1e-38, 1e-39, 1e-41, 1.4e-45], np.float32)
+    for i, t in enumerate(tiny):
+        x[i, 0, :32] = (rng.uniform(-1.0, 1.0, 32) * t).astype(np.float32)
+        x[i, 0, 7] = t
+    codes, scales = _gpu_quant(x)
+    q, d = oracle.quantize_q8_0(x)
+    assert np.array_equal(codes, q.transpose(1, 0, 2)) and np.array_equal(scales, d.transpose(1, 0, 2))
