@@ -30,6 +30,8 @@
 // Instantiations: TREE (tree-shaped windows from per-row masks), APPEND (the window slice
 // quantises the T new tokens itself, attn_verify_append_q8), V4 (K8V4 pools: 4-bit V
 // codes expanded in registers).  attn_verify_q8_partials stops after the partials.
+// attn_verify_append_q8_host works from host buffers: pinned ones are read by a copy kernel
+// and written in place by the merge, pageable ones go through copy-engine transfers.
 #include <algorithm>
 
 #include "common.cuh"
