@@ -4,6 +4,9 @@ Two ways to use N GPUs, both built from the single-GPU entry points:
 
 * replicas -- every rank runs its own independent verify / prompt problems (different
   sequences); no data crosses ranks, only the benchmark's timing reduction does.
+* KV heads -- each rank owns a contiguous range of KV heads (and the q heads of their
+  groups) in a cache of its own and computes their outputs with no exchange at all; only a
+  caller that wants every head on every rank gathers the outputs afterwards.
 * context slices -- one long context is cut into N contiguous key ranges, each rank
   computes the unnormalised partials (o, m, l) of its range, the partials are all-gathered,
   and the log-sum-exp merge (attn_combine) produces the output.  This is the one real
@@ -40,6 +43,42 @@ def max_over_ranks(x: float, device=None) -> float:
     t = torch.tensor([float(x)], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def kv_head_range(n_kv_heads: int, world: int, rank: int) -> tuple[int, int]:
+    """KV heads [h0, h1) of `rank`: contiguous ranges as equal as possible (the first
+    n_kv_heads % world ranks hold one more; ranks past n_kv_heads hold none)."""
+    if n_kv_heads < 0 or world < 1 or not 0 <= rank < world:
+        raise ValueError("bad head-range arguments")
+    base, extra = divmod(n_kv_heads, world)
+    h0 = rank * base + min(rank, extra)
+    return h0, h0 + base + (1 if rank < extra else 0)
+
+
+def verify_kv_head_sharded(q: torch.Tensor, cache, kv_len: int, q_pos0: int, softmax_scale: float,
+                           h0: int, h1: int, group: int, n_split: int = 0) -> torch.Tensor:
+    """Verify attention for KV heads [h0, h1): `cache` holds exactly those heads, `q` is the
+    full window [T][Hq][hd] (q head h belongs to KV head h // group).  Returns this rank's
+    output [T][(h1 - h0) * group][hd]; nothing crosses ranks."""
+    from .binding import attn_verify_q8
+    q_local = q[:, h0 * group:h1 * group].contiguous()
+    return attn_verify_q8(q_local, cache, kv_len, q_pos0, softmax_scale, n_split=n_split)
+
+
+def gather_head_outputs(out_local: torch.Tensor, n_kv_heads: int, group: int) -> torch.Tensor:
+    """Every rank's [T][heads_r * group][hd] output gathered into [T][n_kv_heads * group][hd] in
+    head order (ranks with fewer heads are padded for the all_gather, then trimmed)."""
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return out_local
+    w = dist.get_world_size()
+    ranges = [kv_head_range(n_kv_heads, w, r) for r in range(w)]
+    width = max(h1 - h0 for h0, h1 in ranges) * group
+    T, n_loc, hd = out_local.shape
+    padded = torch.zeros((T, width, hd), dtype=out_local.dtype, device=out_local.device)
+    padded[:, :n_loc] = out_local
+    parts = [torch.empty_like(padded) for _ in range(w)]
+    dist.all_gather(parts, padded)
+    return torch.cat([parts[r][:, :(h1 - h0) * group] for r, (h0, h1) in enumerate(ranges)], dim=1)
 
 
 def context_slices(kv_len: int, world: int, align: int = 128) -> list[tuple[int, int]]:

@@ -127,3 +127,30 @@ def test_partials_reject_bad_arguments(lib):
     assert call(o=po.data_ptr() + 4) == KVQ8_ERR_MISALIGNED
     assert lib_.attn_verify_q8_partials_count(4, 8, 128, 0, 2, 0) == 0
     torch.cuda.synchronize()
+
+
+def test_kv_head_sharding_as_virtual_ranks(lib):
+    """verify_kv_head_sharded over 1-3 head ranges, each with a cache of its own heads: the
+    concatenated outputs match the oracle (no exchange is involved)."""
+    import torch
+
+    from speculative_verify_attention_gb300 import KVCacheQ8, multigpu
+    w = workloads.verify_27b(4)
+    inp = workloads.make_inputs(w)
+    g = w.group
+    orc = oracle.Cache(w.n_kv_heads, w.head_dim, w.kv_len)
+    orc.append(inp.k, inp.v, 0)
+    ref = oracle.attention(orc, inp.q, w.kv_len, w.q_pos0, w.softmax_scale)
+    q = torch.from_numpy(inp.q).cuda()
+    for world in (1, 2, 3):
+        outs = []
+        for r in range(world):
+            h0, h1 = multigpu.kv_head_range(w.n_kv_heads, world, r)
+            c = KVCacheQ8(h1 - h0, w.head_dim, w.kv_len, device="cuda")
+            c.append(torch.from_numpy(np.ascontiguousarray(inp.k[:, h0:h1])).cuda(),
+                     torch.from_numpy(np.ascontiguousarray(inp.v[:, h0:h1])).cuda(), 0)
+            outs.append(multigpu.verify_kv_head_sharded(q, c, w.kv_len, w.q_pos0, w.softmax_scale, h0, h1, g))
+        torch.cuda.synchronize()
+        got = torch.cat(outs, dim=1).cpu().numpy()
+        assert got.shape == ref.shape
+        assert rel_err(got, ref) <= VERIFY_TOL

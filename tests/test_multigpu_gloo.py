@@ -77,6 +77,62 @@ def test_two_gloo_ranks_reduce_and_merge_context_slices():
             assert shape == (4, 24, 128)   # 2 ranks x 2 partials (rank 1 padded with an empty one)
 
 
+def _head_worker(rank, world, port, results):
+    import torch.distributed as dist
+
+    import oracle
+    from speculative_verify_attention_gb300 import workloads
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # KV-head sharding of one verify problem with 3 KV heads over 2 ranks (2 + 1 heads):
+        # each rank attends with its own heads' cache (the oracle standing in for the kernel),
+        # nothing is exchanged until the outputs are gathered for the comparison
+        group, hkv, hd, L, T = 2, 3, 128, 300, 4
+        inp = workloads.random_small(81, hkv * group, hkv, hd, L, T)
+        h0, h1 = multigpu.kv_head_range(hkv, world, rank)
+        c = oracle.Cache(h1 - h0, hd, L)
+        c.append(np.ascontiguousarray(inp.k[:, h0:h1]), np.ascontiguousarray(inp.v[:, h0:h1]), 0)
+        out_local = oracle.attention(c, np.ascontiguousarray(inp.q[:, h0 * group:h1 * group]), L, L - T, 0.09)
+        full = multigpu.gather_head_outputs(torch.from_numpy(out_local), hkv, group)
+        cf = oracle.Cache(hkv, hd, L)
+        cf.append(inp.k, inp.v, 0)
+        ref = oracle.attention(cf, inp.q, L, L - T, 0.09)
+        results[rank] = (h1 - h0, tuple(full.shape), float(np.max(np.abs(full.numpy() - ref))))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_shard_kv_heads_without_exchange():
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        results = mgr.dict()
+        procs = [ctx.Process(target=_head_worker, args=(r, world, port, results)) for r in range(world)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(timeout=240)
+        assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+        assert results[0][0] == 2 and results[1][0] == 1
+        for r in range(world):
+            assert results[r][1] == (4, 6, 128)
+            assert results[r][2] == 0.0   # per-head attention is independent: bit-identical
+
+
+def test_kv_head_ranges_partition_the_heads():
+    for n, world in ((4, 2), (3, 2), (8, 8), (2, 4), (5, 3), (0, 2)):
+        rs = [multigpu.kv_head_range(n, world, r) for r in range(world)]
+        assert rs[0][0] == 0 and rs[-1][1] == n
+        for (a0, a1), (b0, _) in zip(rs[:-1], rs[1:]):
+            assert a1 == b0 and a0 <= a1
+        assert max(h1 - h0 for h0, h1 in rs) - min(h1 - h0 for h0, h1 in rs) <= 1
+    with pytest.raises(ValueError):
+        multigpu.kv_head_range(4, 2, 2)
+
+
 def test_context_slices_cover_the_context_in_whole_tiles():
     for kv_len, world in ((700, 2), (4100, 8), (100, 4), (0, 3), (129, 2)):
         sl = multigpu.context_slices(kv_len, world)
