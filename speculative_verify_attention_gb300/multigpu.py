@@ -7,6 +7,9 @@ Two ways to use N GPUs, both built from the single-GPU entry points:
 * KV heads -- each rank owns a contiguous range of KV heads (and the q heads of their
   groups) in a cache of its own and computes their outputs with no exchange at all; only a
   caller that wants every head on every rank gathers the outputs afterwards.
+* prompt rows -- a prompt chunk's query rows are cut into N contiguous ranges; a rank runs
+  the prompt kernel on its rows (their positions shift with the range) against the whole
+  context, with no exchange.
 * context slices -- one long context is cut into N contiguous key ranges, each rank
   computes the unnormalised partials (o, m, l) of its range, the partials are all-gathered,
   and the log-sum-exp merge (attn_combine) produces the output.  This is the one real
@@ -79,6 +82,20 @@ def gather_head_outputs(out_local: torch.Tensor, n_kv_heads: int, group: int) ->
     parts = [torch.empty_like(padded) for _ in range(w)]
     dist.all_gather(parts, padded)
     return torch.cat([parts[r][:, :(h1 - h0) * group] for r, (h0, h1) in enumerate(ranges)], dim=1)
+
+
+def prompt_row_range(n_q: int, world: int, rank: int) -> tuple[int, int]:
+    """Query rows [r0, r1) of `rank` for a prompt chunk: contiguous and as equal as possible."""
+    return kv_head_range(n_q, world, rank)
+
+
+def prompt_rows_sharded(q: torch.Tensor, cache, kv_len: int, q_pos0: int, softmax_scale: float, r0: int,
+                        r1: int) -> torch.Tensor:
+    """Prompt attention for rows [r0, r1) of the chunk q [n_q][Hq][hd] (row i at position
+    q_pos0 + i): the rank's rows sit at q_pos0 + r0 onwards and see keys up to their own
+    positions, so the result equals rows r0..r1-1 of the unsharded call."""
+    from .binding import attn_prompt_q8
+    return attn_prompt_q8(q[r0:r1].contiguous(), cache, kv_len, q_pos0 + r0, softmax_scale)
 
 
 def context_slices(kv_len: int, world: int, align: int = 128) -> list[tuple[int, int]]:

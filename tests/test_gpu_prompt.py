@@ -129,3 +129,26 @@ def test_full_hd128_prompt_workload_sampled(lib):
     assert err <= PROMPT_TOL, f"rel err {err:.3e}"
     from speculative_verify_attention_gb300 import kvq8_device_error
     assert kvq8_device_error(reset=True) == 0
+
+
+def test_prompt_rows_sharded_as_virtual_ranks(lib):
+    """prompt_rows_sharded over 3 row ranges of a 512-row chunk: the concatenated rows match the
+    oracle (sampled) and the unsharded call."""
+    import torch
+
+    from speculative_verify_attention_gb300 import attn_prompt_q8, multigpu
+    hq, hkv, L, nq = 12, 1, 2048, 512
+    inp = workloads.random_small(90, hq, hkv, 256, L, nq, q_dtype="f16")
+    gpu, orc = build_caches(inp)
+    scale = 1.0 / 16.0
+    q = torch.from_numpy(np.ascontiguousarray(inp.q)).cuda()
+    parts = [multigpu.prompt_rows_sharded(q, gpu, L, L - nq, scale, *multigpu.prompt_row_range(nq, 3, r))
+             for r in range(3)]
+    full = attn_prompt_q8(q, gpu, L, L - nq, scale)
+    torch.cuda.synchronize()
+    got = torch.cat(parts, dim=0).cpu().numpy()
+    assert rel_err(got, full.cpu().numpy()) <= PROMPT_TOL
+    rng = np.random.default_rng(91)
+    sel = [(int(i), int(rng.integers(hq))) for i in rng.integers(0, nq, 40)] + [(nq - 1, h) for h in range(hq)]
+    ref = oracle.attention(orc, inp.q, L, L - nq, scale, sel=sel)
+    assert rel_err(np.stack([got[i, h] for i, h in sel]), ref) <= PROMPT_TOL

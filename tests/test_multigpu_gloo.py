@@ -122,6 +122,23 @@ def test_two_gloo_ranks_shard_kv_heads_without_exchange():
             assert results[r][2] == 0.0   # per-head attention is independent: bit-identical
 
 
+def test_prompt_row_ranges_match_the_unsharded_rows():
+    """Prompt rows cut across 3 ranks: each range, placed at q_pos0 + r0, gives the same rows as
+    the unsharded chunk (the oracle standing in for the per-rank kernel)."""
+    import oracle
+    from speculative_verify_attention_gb300 import workloads
+    hq, hkv, hd, L, nq = 4, 1, 128, 260, 37
+    inp = workloads.random_small(83, hq, hkv, hd, L, nq, q_dtype="f16")
+    c = oracle.Cache(hkv, hd, L)
+    c.append(inp.k, inp.v, 0)
+    ref = oracle.attention(c, inp.q, L, L - nq, 0.09)
+    parts = []
+    for r in range(3):
+        r0, r1 = multigpu.prompt_row_range(nq, 3, r)
+        parts.append(oracle.attention(c, np.ascontiguousarray(inp.q[r0:r1]), L, L - nq + r0, 0.09))
+    assert np.array_equal(np.concatenate(parts, axis=0), ref)
+
+
 def test_kv_head_ranges_partition_the_heads():
     for n, world in ((4, 2), (3, 2), (8, 8), (2, 4), (5, 3), (0, 2)):
         rs = [multigpu.kv_head_range(n, world, r) for r in range(world)]
