@@ -176,3 +176,26 @@ def test_subnormal_scales_bit_exact(lib):
     codes, scales = _gpu_quant(x)
     q, d = oracle.quantize_q8_0(x)
     assert np.array_equal(codes, q.transpose(1, 0, 2)) and np.array_equal(scales, d.transpose(1, 0, 2))
+
+
+def test_block_maxima_over_every_exponent_bit_exact(lib):
+    """Block maxima at every fp32 exponent (subnormal to near the fp16-scale limit) with edge and
+    random mantissas, the other values at (k + 1/2) d one ulp either side: the scale
+    fl(max / 127) and every code match the IEEE-division oracle."""
+    rng = np.random.default_rng(25)
+    exps = np.arange(-149, 20)
+    mants = np.concatenate([[1.0, 1.0 + 2.0 ** -23, 2.0 - 2.0 ** -23], rng.uniform(1.0, 2.0, 13)])
+    amax = np.array([np.ldexp(m, e) for e in exps for m in mants], dtype=np.float64).astype(np.float32)
+    amax = amax[amax > 0]
+    n_blk = amax.size - amax.size % 8
+    amax = amax[:n_blk]
+    d = (amax / np.float32(127.0)).astype(np.float32)
+    k = rng.integers(-127, 127, (n_blk, 31)).astype(np.float32)
+    base = ((k + np.float32(0.5)) * d[:, None]).astype(np.float32)
+    steps = rng.choice(np.array([-1, 1], np.int32), (n_blk, 31))
+    vals = (base.view(np.int32) + np.where(base >= 0, steps, -steps)).view(np.float32)
+    vals = np.clip(np.nan_to_num(vals), -amax[:, None], amax[:, None])
+    x = np.concatenate([amax[:, None], vals], axis=1).reshape(n_blk // 8, 1, 256)
+    codes, scales = _gpu_quant(x)
+    q, dd = oracle.quantize_q8_0(x)
+    assert np.array_equal(codes, q.transpose(1, 0, 2)) and np.array_equal(scales, dd.transpose(1, 0, 2))
