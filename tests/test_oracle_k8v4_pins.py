@@ -117,3 +117,42 @@ def test_equals_q8_attention_on_small_codes():
     b = oracle.Cache.from_planes(kc, ks, vq.astype(np.int8), vs)
     q = rng.standard_normal((5, 8, hd))
     assert np.array_equal(oracle.attention(a, q, 38, 33, 0.09), oracle.attention(b, q, 38, 33, 0.09))
+
+
+@pytest.mark.parametrize("hkv,hd,cap,pos0,n_tok", [(2, 64, 23, 7, 5), (3, 128, 40, 31, 9)])
+def test_append_places_each_token_at_its_row(hkv, hd, cap, pos0, n_tok):
+    """The 4-bit append at pos0 > 0 with several KV heads: the nibbles of token t of head h
+    decode (here, not with the oracle's code) to values within the round-trip bound of that
+    token's own inputs, so a wrong row stride, head/token order or pos0 offset in the append
+    fails; every row outside [pos0, pos0 + n_tok) keeps its zero-code filler and zero scale."""
+    rng = np.random.default_rng(hkv * 100 + pos0)
+    k = rng.standard_normal((n_tok, hkv, hd)).astype(np.float32)
+    v = (rng.standard_normal((n_tok, hkv, hd)) * rng.uniform(0.1, 10.0, (n_tok, hkv, 1))).astype(np.float32)
+    c = oracle.CacheK8V4(hkv, hd, cap)
+    c.append(k, v, pos0)
+    q = _decode(c.v_q4).astype(np.float64)                                    # [hkv][cap][hd]
+    d16 = np.repeat(c.v_scales.view(np.float16).astype(np.float64), 32, axis=-1)
+    for h in range(hkv):
+        for t in range(n_tok):
+            x = v[t, h].astype(np.float64)
+            d32 = np.repeat(np.abs(x).reshape(-1, 32).max(axis=1) / 7, 32)
+            row = pos0 + t
+            err = np.abs(q[h, row] * d16[h, row] - x)
+            assert np.all(err <= d32 / 2 + 7 * np.abs(d16[h, row] - d32) + 1e-6 * d32), (h, t)
+            # each block's largest magnitude lands on +-7 with the input's sign
+            blk = np.abs(x).reshape(-1, 32).argmax(axis=1) + 32 * np.arange(hd // 32)
+            assert np.all(q[h, row, blk] == 7 * np.sign(x[blk]))
+    untouched = np.ones(cap, bool)
+    untouched[pos0:pos0 + n_tok] = False
+    assert np.all(c.v_q4[:, untouched] == 0x88)
+    assert np.all(c.v_scales[:, untouched] == 0)
+    # the K plane of the same append lands at the same rows (Q8_0 round-trip bound)
+    kq = c.k_codes.astype(np.float64)
+    ks = np.repeat(c.k_scales.view(np.float16).astype(np.float64), 32, axis=-1)
+    for h in range(hkv):
+        for t in range(n_tok):
+            x = k[t, h].astype(np.float64)
+            d32 = np.repeat(np.abs(x).reshape(-1, 32).max(axis=1) / 127, 32)
+            err = np.abs(kq[h, pos0 + t] * ks[h, pos0 + t] - x)
+            assert np.all(err <= d32 / 2 + 127 * np.abs(ks[h, pos0 + t] - d32) + 1e-6 * d32), (h, t)
+    assert np.all(c.k_codes[:, untouched] == 0) and np.all(c.k_scales[:, untouched] == 0)
