@@ -386,6 +386,26 @@ int attn_verify_q8_noalloc(const float* q, int n_rows, int n_q_heads, const kvq8
                            int q_pos0, float softmax_scale, float* out, int n_split, kvq8_stream_t stream);
 
 /*
+ * kvq8_selftest_convert -- a self-test hook: runs the code -> fp16 conversions that the verify
+ * and prompt kernels use, unchanged, on caller data, so that a test can check them exhaustively.
+ *   kind 0: in[i] = 4 int8 codes; out[2i], out[2i+1] = fp16 pairs of codes (0, 1) and (2, 3)
+ *           (the K operand of the verify scans, the prompt dequantisers).  out: 2n words.
+ *   kind 1: in[2i], in[2i+1] = words w0, w1 of 4 codes each (two key rows); out[4i + m] = the fp16
+ *           pair (w0 byte m, w1 byte m) through the byte interleave of the PV operands.  n even;
+ *           out: 2n words.
+ *   kind 2: in[i] = two 16-bit halves of 4 nibbles each (stored code + 8); out[4i .. 4i+3] = the
+ *           pairs of nibbles (0, 4), (1, 5), (2, 6), (3, 7), one from each half (the 4-bit PV
+ *           operands).  out: 4n words.
+ *   kind 3: in[i] = 4 bytes of nibble pairs; out[4i + m] = the pair (low, high) of byte m as
+ *           codes (the 4-bit prompt dequantiser).  out: 4n words.
+ * Each fp16 value must equal the code exactly.  in, out: device, 4-byte aligned.  Errors:
+ * INVALID_ARG (kind, n, null pointers), MISALIGNED.  One launch on `stream`.
+ * Source: "gfx12 WMMA kernel for the int8-KV QSA prompt attention", How: the exact int8 -> fp16
+ * conversion, checked over all byte pairs.
+ */
+int kvq8_selftest_convert(int kind, const uint32_t* in, uint32_t* out, int n, kvq8_stream_t stream);
+
+/*
  * kvq8_device_error -- read (and with reset != 0, clear) the library's device error flag.
  * Nonzero means a kernel gave up on an internal wait after its bounded poll count and
  * returned early.  Returns the flag, or -1 if it could not be read.  Unlike every other

@@ -33,7 +33,7 @@ EXPORTED = ("kvq8_quantize", "kvq8_append", "attn_verify_q8_workspace_bytes", "a
             "kvf16_append", "attn_verify_f16_workspace_bytes", "attn_verify_f16", "kvk8v4_append", "attn_verify_k8v4",
             "attn_prompt_k8v4", "attn_prompt_f16", "attn_combine",
             "attn_prompt_q8_workspace_bytes", "attn_prompt_q8", "attn_verify_q8_noalloc", "kvq8_device_error", "kvq8_status_str",
-            "argmax_rows_top_prob_workspace_bytes", "argmax_rows_top_prob")
+            "argmax_rows_top_prob_workspace_bytes", "argmax_rows_top_prob", "kvq8_selftest_convert")
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 
@@ -118,6 +118,8 @@ def load_library():
         lib.argmax_rows_top_prob_workspace_bytes.restype = sz
         lib.argmax_rows_top_prob.argtypes = [vp, i32, i32, vp, vp, vp, sz, vp]
         lib.argmax_rows_top_prob.restype = i32
+        lib.kvq8_selftest_convert.argtypes = [i32, vp, vp, i32, vp]
+        lib.kvq8_selftest_convert.restype = i32
         lib.attn_combine.argtypes = [vp, vp, i32, i32, i32, vp, vp]
         lib.attn_combine.restype = i32
         lib.attn_prompt_q8_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
@@ -554,6 +556,17 @@ def argmax_rows_top_prob(logits: torch.Tensor, workspace: torch.Tensor | None = 
                                   workspace.numel() * workspace.element_size(), _stream(stream))
     _check("argmax_rows_top_prob", st)
     return argmax, top_prob
+
+
+def kvq8_selftest_convert(kind: int, words: torch.Tensor, stream=None) -> torch.Tensor:
+    """Run the kernels' code -> fp16 conversion `kind` (0-3, see the header) over int32 words on the
+    device; returns the fp16 pairs as int32 words (2 per input word for kinds 0 and 1, 4 for 2 and 3)."""
+    _need(words, "words", torch.int32)
+    n = words.numel()
+    out = torch.empty(n * (2 if kind in (0, 1) else 4), dtype=torch.int32, device=words.device)
+    st = load_library().kvq8_selftest_convert(int(kind), _ptr(words), _ptr(out), n, _stream(stream))
+    _check("kvq8_selftest_convert", st)
+    return out
 
 
 def attn_combine(part_o: torch.Tensor, part_ml: torch.Tensor, out: torch.Tensor | None = None,

@@ -13,6 +13,9 @@ constexpr int kQBlock = 32;          // values per Q8_0 block
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<const __half2*>(&u); }
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline int launch_status() {
@@ -31,6 +34,38 @@ __device__ __forceinline__ uint32_t biased_bytes_to_half2(uint32_t x) {
     const __half2 h = *reinterpret_cast<const __half2*>(&r);
     const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480u));  // 1152.0
     const __half2 v = __hsub2(h, bias);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Nibble pairs -> fp16 pairs, exactly.  x holds two 16-bit halves (key a in the low half, key b
+// in the high half), each 4 nibbles of 4 consecutive dims.  lo: nibbles 0 and 4 (dim 0 of both
+// keys) placed in the fp16 pattern 0x640n is 1024 + n; subtracting 1032 gives n - 8.  hi:
+// nibbles 1 and 5 masked in place are 16 n in the mantissa, 1024 + 16 n; times 1/16 minus 72
+// gives n - 8.  (x >> 8 gives dims 2 and 3 the same way.)
+__device__ __forceinline__ uint32_t nib_lo_to_half2(uint32_t x) {
+    const uint32_t r = (x & 0x000F000Fu) | 0x64006400u;
+    const __half2 v = __hsub2(u32_as_h2(r), __half2half2(__ushort_as_half((unsigned short)0x6408u)));  // 1032
+    return h2_as_u32(v);
+}
+__device__ __forceinline__ uint32_t nib_hi_to_half2(uint32_t x) {
+    const uint32_t r = (x & 0x00F000F0u) | 0x64006400u;
+    const __half2 v = __hfma2(u32_as_h2(r), __half2half2(__ushort_as_half((unsigned short)0x2C00u)),   // 1/16
+                              __half2half2(__ushort_as_half((unsigned short)0xD480u)));                // -72
+    return h2_as_u32(v);
+}
+
+// Byte m of w (two 4-bit codes stored as nibble + 8, element 2k in the low nibble) -> the fp16
+// pair (low - 8, high - 8), exactly: the byte placed in bytes 0 and 2 of a word and masked with
+// 0x00F0000F gives, after OR with 0x64006400, the pair (1024 + lo, 1024 + 16 hi); one fma with
+// (1, 1/16) and (-1032, -72) turns it into the two codes.
+template <int M>
+__device__ __forceinline__ uint32_t nib_byte_to_half2(uint32_t w) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(w), "r"(0u), "n"(0x4040u | (M * 0x0101u)));
+    r = (r & 0x00F0000Fu) | 0x64006400u;
+    const __half2 mul = __halves2half2(__ushort_as_half((unsigned short)0x3C00u), __ushort_as_half((unsigned short)0x2C00u));
+    const __half2 add = __halves2half2(__ushort_as_half((unsigned short)0xE408u), __ushort_as_half((unsigned short)0xD480u));
+    const __half2 v = __hfma2(*reinterpret_cast<const __half2*>(&r), mul, add);
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
@@ -69,8 +104,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
-__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<const __half2*>(&u); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -26,12 +26,11 @@
 // Barriers that many threads signal take one arrival per warp (after __syncwarp), not one
 // per thread.  Every mbarrier wait is bounded: on timeout the kernel records an error flag (read with
 // kvq8_device_error) and returns after releasing its tensor memory.
-#include <cuda.h>  // CUtensorMap and its encoding enums (the encoder itself is fetched at run time)
-
 #include <mutex>
 
 #include "common.cuh"
 #include "tc.cuh"
+#include "tmap.cuh"
 
 __device__ unsigned int g_kvq8_device_error = 0;
 
@@ -201,17 +200,13 @@ __device__ __forceinline__ void dequant_tile(const uint8_t* codes, const uint16_
 }
 
 // The 4-bit V tile of a K8V4 pool (HD/2 bytes per key, element 2m in the low nibble of byte
-// m, value (nibble - 8) * scale) into the same swizzled fp16 tile.  A byte placed in bytes 0
-// and 2 of a word and masked with 0x00F0000F gives, after OR with 0x64006400, the fp16 pair
-// (1024 + lo, 1024 + 16 hi); one fma with (1, 1/16) and (-1032, -72) turns it into the two
-// codes exactly, and one multiply by the scale rounds once, as for Q8_0.
+// m, value (nibble - 8) * scale) into the same swizzled fp16 tile: each byte becomes its two
+// codes exactly (nib_byte_to_half2), and one multiply by the scale rounds once, as for Q8_0.
 template <int HD>
 __device__ __forceinline__ void dequant_tile_v4(const uint8_t* codes, const uint16_t* scales, uint8_t* hat, int nk,
                                                 int d) {
     constexpr int kChunks = PL<HD>::kChunks;  // 16-dim items per tile
     constexpr int CPK = HD / 16;
-    const __half2 mul = __halves2half2(__ushort_as_half((unsigned short)0x3C00u), __ushort_as_half((unsigned short)0x2C00u));
-    const __half2 add = __halves2half2(__ushort_as_half((unsigned short)0xE408u), __ushort_as_half((unsigned short)0xD480u));
 #pragma unroll
     for (int k = 0; k < (kChunks + kDeqThreads - 1) / kDeqThreads; ++k) {
         const int c = d + kDeqThreads * k;
@@ -221,16 +216,12 @@ __device__ __forceinline__ void dequant_tile_v4(const uint8_t* codes, const uint
         if (n < nk) {
             const uint2 raw = *reinterpret_cast<const uint2*>(codes + n * (HD / 2) + j16 * 8);
             const __half2 sc = __half2half2(__ushort_as_half(scales[n * (HD / 32) + (j16 >> 1)]));
+            const uint32_t e[8] = {nib_byte_to_half2<0>(raw.x), nib_byte_to_half2<1>(raw.x), nib_byte_to_half2<2>(raw.x),
+                                   nib_byte_to_half2<3>(raw.x), nib_byte_to_half2<0>(raw.y), nib_byte_to_half2<1>(raw.y),
+                                   nib_byte_to_half2<2>(raw.y), nib_byte_to_half2<3>(raw.y)};
             uint32_t h[8];
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                const uint32_t w = m < 4 ? raw.x : raw.y;
-                uint32_t r;
-                asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(w), "r"(0u), "r"(0x4040u | ((m & 3) * 0x0101u)));
-                r = (r & 0x00F0000Fu) | 0x64006400u;
-                const __half2 v = __hmul2(__hfma2(u32_as_h2(r), mul, add), sc);
-                h[m] = h2_as_u32(v);
-            }
+            for (int m = 0; m < 8; ++m) h[m] = h2_as_u32(__hmul2(u32_as_h2(e[m]), sc));
             o0 = make_uint4(h[0], h[1], h[2], h[3]);
             o1 = make_uint4(h[4], h[5], h[6], h[7]);
         }
@@ -761,24 +752,6 @@ int launch_prompt(const PromptParams& pp, int grid, cudaStream_t s) {
     return launch_status();
 }
 
-// cuTensorMapEncodeTiled from the driver, looked up once.
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-EncodeTiledFn encode_tiled_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-    });
-    return fn;
-}
-
 // Tensor map of one fp16 plane [n_kv_heads][capacity][hd]: dims (hd, kv_len, n_kv_heads), so
 // keys at or past kv_len read as zeros; box 64 dims x 64 keys x 1 head, 128-byte swizzle.
 bool encode_f16_plane(CUtensorMap* map, const uint16_t* plane, int hd, int kv_len, int n_kv_heads, int capacity) {
@@ -898,6 +871,23 @@ extern "C" int attn_prompt_f16(const uint16_t* q, int n_q, int n_q_heads, const 
     return kvq8::prompt_impl(q, n_q, n_q_heads, &view, kv_len, q_pos0, softmax_scale, out, workspace, workspace_bytes,
                              stream, kvq8::kPoolF16);
 }
+
+namespace kvq8 {
+// The flag's device address per device, looked up with that device current (concurrent first
+// lookups store the same value).
+unsigned int* device_error_flag() {
+    constexpr int kMaxDev = 64;
+    static unsigned int* cached[kMaxDev] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+    if (!cached[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_kvq8_device_error) != cudaSuccess) return nullptr;
+        cached[dev] = static_cast<unsigned int*>(ptr);
+    }
+    return cached[dev];
+}
+}  // namespace kvq8
 
 extern "C" int kvq8_device_error(int reset) {
     unsigned int v = 0;

@@ -1,4 +1,5 @@
-// verify.cu -- split-context multi-row verify attention over a Q8_0 GQA cache (attn_verify_q8).
+// verify.cu -- the verify entry points (attn_verify_q8 and its variants) and the all-mma.sync
+// split-context scan used for tree-shaped windows and K8V4 pools.
 //
 // Source: "perf(gfx1100): share Q8 KV scans across verifier rows", Summary: one worker owns
 // all the query rows of a verify window and shares each K/V scan across them; the context
@@ -6,7 +7,11 @@
 // int8-KV QSA prompt attention", How: fp16 hi + lo split of q and p with fp32 accumulation,
 // online softmax, V scale folded into p.
 //
-// GB300 design (one thread block of 8 warps per (row chunk, context slice, KV head); the
+// Routing: causal windows over a Q8_0 cache (attn_verify_q8, attn_verify_q8_partials,
+// attn_verify_append_q8 and the host-buffer and no-allocation entries built on them) run the
+// tcgen05 scan of verify_tc.cu; tree-shaped windows and K8V4 pools run the kernel below.
+//
+// The kernel below (one thread block of 8 warps per (row chunk, context slice, KV head); the
 // chunks and slices come from verify_plan.cuh):
 //   * K/V codes and scales of a 128-key tile are staged in shared memory with 16-byte
 //     cp.async copies into an XOR-swizzled layout (conflict-free fragment reads).  K of the
@@ -27,16 +32,16 @@
 //     w = p * dV[n][block] * 2^E split into fp16 hi + lo, with E a per-warp power of two that
 //     keeps w inside the fp16 normal range (the accumulator is rescaled when E changes).
 //   * Each slice writes an unnormalised partial (o, m, l); attn_combine merges them.
-// Instantiations: TREE (tree-shaped windows from per-row masks), APPEND (the window slice
-// quantises the T new tokens itself, attn_verify_append_q8), V4 (K8V4 pools: 4-bit V
-// codes expanded in registers).  attn_verify_q8_partials stops after the partials.
+// Instantiations: TREE (tree-shaped windows from per-row masks), V4 (K8V4 pools: 4-bit V
+// codes expanded in registers).
 // attn_verify_append_q8_host works from host buffers: pinned ones are read by a copy kernel
 // and written in place by the merge, pageable ones go through copy-engine transfers.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
-#include "q8_0.cuh"
 #include "verify_plan.cuh"
+#include "verify_tc.cuh"
 
 namespace kvq8 {
 
@@ -66,11 +71,7 @@ struct VerifyParams {
     int kv_len;
     int q_pos0;
     int keys_per_split;
-    int key_shift;       // slice s starts at key s * keys_per_split - key_shift (0 without a window slice)
-    int n_ctx_splits;    // slices >= n_ctx_splits: the window slice (append-and-verify path)
     int n_kv_heads;
-    const float* k_new;  // append-and-verify: fp32 [n_rows][n_kv_heads][HD] window keys and values,
-    const float* v_new;  // quantised by the window slice (into its tile and into the cache)
     int rows_per_chunk;  // real rows per chunk (<= 8 * NT)
     float qscale;        // softmax_scale * log2(e)
     const uint32_t* wmask;  // tree windows: bit j of wmask[i] = row i sees key q_pos0 + j; null = causal
@@ -193,72 +194,6 @@ __device__ __forceinline__ void load_codes_v4(uint8_t* smem, const uint8_t* plan
     }
 }
 
-// Nibble pairs -> fp16 pairs, exactly.  x holds two 16-bit halves (key a in the low half, key b
-// in the high half), each 4 nibbles of 4 consecutive dims.  lo: nibbles 0 and 4 (dim 0 of both
-// keys) placed in the fp16 pattern 0x640n is 1024 + n; subtracting 1032 gives n - 8.  hi:
-// nibbles 1 and 5 masked in place are 16 n in the mantissa, 1024 + 16 n; times 1/16 minus 72
-// gives n - 8.  (x >> 8 gives dims 2 and 3 the same way.)
-__device__ __forceinline__ uint32_t nib_lo_to_half2(uint32_t x) {
-    const uint32_t r = (x & 0x000F000Fu) | 0x64006400u;
-    const __half2 v = __hsub2(u32_as_h2(r), __half2half2(__ushort_as_half((unsigned short)0x6408u)));  // 1032
-    return h2_as_u32(v);
-}
-__device__ __forceinline__ uint32_t nib_hi_to_half2(uint32_t x) {
-    const uint32_t r = (x & 0x00F000F0u) | 0x64006400u;
-    const __half2 v = __hfma2(u32_as_h2(r), __half2half2(__ushort_as_half((unsigned short)0x2C00u)),   // 1/16
-                              __half2half2(__ushort_as_half((unsigned short)0xD480u)));                // -72
-    return h2_as_u32(v);
-}
-
-// Append-and-verify, window slice: quantises the nk (<= 32) window tokens' fp32 keys and
-// values to Q8_0 (bit-exact with the append kernel).  The keys go straight into this block's
-// K tile (the layout load_codes and load_scales produce, rows past nk zeroed as the
-// zero-filling copies would leave them) and, from the chunk-0 block, into the cache.  The
-// values go to the cache only: the tile loop then loads them like any V tile, after the
-// barrier at its top has made this block's stores visible.  With several row chunks every
-// chunk's window block stores the same value bytes.  8 lanes per 32-value block, both planes
-// in one pass over 2 nk HD/32 blocks.
-template <int HD>
-__device__ __forceinline__ void window_tile(const VerifyParams& p, uint8_t* smem, int kvh, bool chunk0, int pos0,
-                                            int nk) {
-    using L = Smem<HD, 1>;  // the tile offsets do not depend on NT
-    constexpr int NB = HD / 32;
-    uint8_t* sK = smem + L::kK;
-    uint16_t* sKs = reinterpret_cast<uint16_t*>(smem + L::kKs);
-    // zero code rows [nk, 32) (read by the 16-key steps) and scale rows [nk, kKT)
-    for (int i = nk * HD / 16 + threadIdx.x; i < 32 * HD / 16; i += kThreads)
-        reinterpret_cast<uint4*>(sK)[i] = make_uint4(0u, 0u, 0u, 0u);
-    for (int i = nk * NB / 2 + threadIdx.x; i < kKT * NB / 2; i += kThreads)
-        reinterpret_cast<uint32_t*>(sKs)[i] = 0u;
-    const int nblk = nk * NB;  // blocks per plane
-    const int sub = threadIdx.x & 7;
-    for (int base = 0; base < 2 * nblk; base += kThreads / 8) {  // uniform trip count
-        const int blk = base + (threadIdx.x >> 3);
-        const bool live = blk < 2 * nblk;
-        const bool vplane = blk >= nblk;
-        const int bb = vplane ? blk - nblk : blk;
-        const int j = bb / NB, b = bb - j * NB;
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (live)
-            x = __ldg(reinterpret_cast<const float4*>((vplane ? p.v_new : p.k_new) +
-                                                      ((int64_t)j * p.n_kv_heads + kvh) * HD + 32 * b) + sub);
-        uint16_t scale_bits;
-        const uint32_t packed = q8_0_block(x, &scale_bits);
-        if (!live) continue;
-        const int64_t row = (int64_t)kvh * p.capacity + pos0 + j;
-        if (!vplane) {
-            *reinterpret_cast<uint32_t*>(sK + swz<HD>(j, 32 * b + 4 * sub)) = packed;
-            if (sub == 0) sKs[j * NB + b] = scale_bits;
-        }
-        if (vplane || chunk0) {
-            int8_t* codes = const_cast<int8_t*>(vplane ? p.v_codes : p.k_codes);
-            uint16_t* scales = const_cast<uint16_t*>(vplane ? p.v_scales : p.k_scales);
-            *reinterpret_cast<uint32_t*>(codes + row * HD + 32 * b + 4 * sub) = packed;
-            if (sub == 0) scales[row * NB + b] = scale_bits;
-        }
-    }
-}
-
 // Work split inside a thread block (8 warps):
 //   QK  : warp w owns keys 16w .. 16w+15 of the tile (one m16 fragment), all row tiles;
 //   PV  : at hd256 warp w owns the 32-dim output block w (two m16 fragments); at hd128 warps
@@ -267,7 +202,7 @@ __device__ __forceinline__ void window_tile(const VerifyParams& p, uint8_t* smem
 // both the S^T and the O^T fragments, so the softmax factors never leave the thread.
 // TREE: the window's rows see the window keys their mask selects (p.wmask); otherwise the
 // window is sequential (row i sees keys < q_pos0 + i + 1) and the mask code is compiled out.
-template <int HD, int NT, bool TREE, bool APPEND, bool V4 = false>
+template <int HD, int NT, bool TREE, bool V4 = false>
 __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kernel(const VerifyParams p) {
     using L = Smem<HD, NT>;
     constexpr int NB = L::NB, RP = L::RP, PS = L::PS;
@@ -289,13 +224,9 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
     const int rows_total = p.n_rows * p.n_q_heads;
     const int row0 = chunk * p.rows_per_chunk;
     const int rows_here = min(p.rows_per_chunk, R - row0);
-    // Slice s covers keys [s * keys_per_split - key_shift, (s + 1) * keys_per_split - key_shift)
-    // clipped to [0, kv_len). key_shift is 0 unless a window slice follows the context slices
-    // (the append-and-verify path): then it puts the end of slice n_ctx_splits - 1 at the first
-    // window key, and slice n_ctx_splits holds the window keys alone.
-    const int key_base = split * p.keys_per_split - p.key_shift;
-    const int key_begin = split == 0 ? 0 : key_base;  // key_shift < keys_per_split
-    const int key_end = min(key_base + p.keys_per_split, p.kv_len);
+    // Slice s covers keys [s * keys_per_split, (s + 1) * keys_per_split) clipped to kv_len.
+    const int key_begin = split * p.keys_per_split;
+    const int key_end = min(key_begin + p.keys_per_split, p.kv_len);
     const int64_t head_row0 = (int64_t)kvh * p.capacity;
     const int pvb = HD == 256 ? warp : (warp >> 1);  // PV output block of this warp
     uint16_t* sDv = reinterpret_cast<uint16_t*>(smem + L::kDv) + warp * kKT;
@@ -326,8 +257,7 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
         // The first K tile is requested after the q loads, so those are not queued behind
         // every block's first tile; K alone lands in about half the time of K + V.  The V
         // tile of each iteration is requested once its K has landed (top of the loop).
-        // (on the append-and-verify path the window slice quantises its tile itself, below)
-        if (key_begin < key_end && !(APPEND && split >= p.n_ctx_splits)) {
+        if (key_begin < key_end) {
             load_codes<HD>(sK, p.k_codes, head_row0, key_begin, key_end);
             load_scales<HD>(smem + L::kKs, p.k_scales, head_row0, key_begin, key_end);
         }
@@ -353,10 +283,6 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
             dst[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             dst[32] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
-    }
-
-    if constexpr (APPEND) {
-        if (split >= p.n_ctx_splits) window_tile<HD>(p, smem, kvh, chunk == 0, key_begin, key_end - key_begin);
     }
 
     // Visibility bound per owned row (row rr sees keys < vis_end; for a tree window, keys at
@@ -747,40 +673,63 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
     }
 }
 
-template <int HD, int NT, bool TREE, bool APPEND, bool V4>
+template <int HD, int NT, bool TREE, bool V4>
 int launch_verify(const VerifyParams& vp, const Plan& pl, int n_kv_heads, cudaStream_t stream) {
     constexpr int bytes = Smem<HD, NT>::kBytes;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(verify_split_kernel<HD, NT, TREE, APPEND, V4>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
-            return KVQ8_ERR_CUDA;
-        attr_set = true;
+    // the shared-memory opt-in is a property of the kernel on one device: set once per device
+    constexpr int kMaxDev = 64;
+    static bool attr_set[kMaxDev] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return KVQ8_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!attr_set[dev]) {
+            if (cudaFuncSetAttribute(verify_split_kernel<HD, NT, TREE, V4>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+                return KVQ8_ERR_CUDA;
+            attr_set[dev] = true;
+        }
     }
     dim3 grid(pl.n_chunks, pl.n_split, n_kv_heads);
-    verify_split_kernel<HD, NT, TREE, APPEND, V4><<<grid, kThreads, bytes, stream>>>(vp);
+    verify_split_kernel<HD, NT, TREE, V4><<<grid, kThreads, bytes, stream>>>(vp);
     return launch_status();
 }
 
-template <int HD, bool TREE, bool APPEND, bool V4 = false>
+template <int HD, bool TREE, bool V4 = false>
 int dispatch_nt(const VerifyParams& vp, const Plan& pl, int n_kv_heads, cudaStream_t s) {
     switch (pl.nt) {
-        case 1: return launch_verify<HD, 1, TREE, APPEND, V4>(vp, pl, n_kv_heads, s);
-        case 2: return launch_verify<HD, 2, TREE, APPEND, V4>(vp, pl, n_kv_heads, s);
-        case 3: return launch_verify<HD, 3, TREE, APPEND, V4>(vp, pl, n_kv_heads, s);
-        case 4: return launch_verify<HD, 4, TREE, APPEND, V4>(vp, pl, n_kv_heads, s);
+        case 1: return launch_verify<HD, 1, TREE, V4>(vp, pl, n_kv_heads, s);
+        case 2: return launch_verify<HD, 2, TREE, V4>(vp, pl, n_kv_heads, s);
+        case 3: return launch_verify<HD, 3, TREE, V4>(vp, pl, n_kv_heads, s);
+        case 4: return launch_verify<HD, 4, TREE, V4>(vp, pl, n_kv_heads, s);
         default: return KVQ8_ERR_UNSUPPORTED;
     }
 }
 
 }  // namespace
+
+// Plans of the two scan kernels: causal windows over a Q8_0 cache run the tcgen05 kernel
+// (row chunks of <= 24 rows, one block per SM); tree windows and K8V4 pools the all-mma.sync one.
+inline int plan_tc(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_kv_heads, int n_split, Plan* pl,
+                   int window_keys = 0) {
+    return make_plan(n_rows, n_q_heads, head_dim, kv_len, n_kv_heads, n_split, pl, window_keys, tc_blocks_per_sm,
+                     kTcMaxRows);
+}
+inline int plan_mma(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_kv_heads, int n_split, Plan* pl) {
+    return make_plan(n_rows, n_q_heads, head_dim, kv_len, n_kv_heads, n_split, pl);
+}
+
 }  // namespace kvq8
 
+// The one workspace size that serves attn_verify_q8, attn_verify_tree_q8 and attn_verify_k8v4.
 extern "C" size_t attn_verify_q8_workspace_bytes(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_kv_heads,
                                                  int n_split) {
-    kvq8::Plan pl;
-    if (kvq8::make_plan(n_rows, n_q_heads, head_dim, kv_len, n_kv_heads, n_split, &pl) != KVQ8_OK) return 0;
-    return pl.ws_bytes;
+    kvq8::Plan a, b;
+    if (kvq8::plan_tc(n_rows, n_q_heads, head_dim, kv_len, n_kv_heads, n_split, &a) != KVQ8_OK ||
+        kvq8::plan_mma(n_rows, n_q_heads, head_dim, kv_len, n_kv_heads, n_split, &b) != KVQ8_OK)
+        return 0;
+    return std::max(a.ws_bytes, b.ws_bytes);
 }
 
 namespace kvq8 {
@@ -804,9 +753,11 @@ int verify_impl(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv,
     if (!(softmax_scale == softmax_scale) || softmax_scale == INFINITY || softmax_scale == -INFINITY)
         return KVQ8_ERR_INVALID_ARG;
     if (append && (!v_new || kv_len != q_pos0 + n_rows)) return KVQ8_ERR_INVALID_ARG;
+    const bool tc = !v4 && !wmask;  // causal windows over a Q8_0 cache: the tcgen05 kernel
     Plan pl;
-    const int rc = make_plan(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, n_split, &pl,
-                             append ? n_rows : 0);
+    const int rc = tc ? plan_tc(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, n_split, &pl,
+                                append ? n_rows : 0)
+                      : plan_mma(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, n_split, &pl);
     if (rc != KVQ8_OK) return rc;
     if (!aligned16(q) || !aligned16(kv->k_codes) || !aligned16(kv->k_scales) || !aligned16(kv->v_codes) ||
         !aligned16(kv->v_scales))
@@ -839,28 +790,46 @@ int verify_impl(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv,
     vp.kv_len = kv_len;
     vp.q_pos0 = q_pos0;
     vp.keys_per_split = pl.keys_per_split;
-    vp.key_shift = pl.key_shift;
-    vp.n_ctx_splits = pl.n_ctx_splits;
     vp.rows_per_chunk = pl.rows_per_chunk;
     vp.qscale = softmax_scale * kLog2e;
     vp.wmask = wmask;
     vp.n_kv_heads = kv->n_kv_heads;
-    vp.k_new = k_new;
-    vp.v_new = v_new;
     cudaStream_t s = (cudaStream_t)stream;
     int r1;
-    if (v4)  // K8V4 pools: causal windows, no append
-        r1 = pl.hd == 128 ? dispatch_nt<128, false, false, true>(vp, pl, kv->n_kv_heads, s)
-                          : dispatch_nt<256, false, false, true>(vp, pl, kv->n_kv_heads, s);
-    else if (wmask)  // tree windows have no append variant
-        r1 = pl.hd == 128 ? dispatch_nt<128, true, false>(vp, pl, kv->n_kv_heads, s)
-                          : dispatch_nt<256, true, false>(vp, pl, kv->n_kv_heads, s);
-    else if (append)
+    if (tc) {
+        VerifyTcParams tp;
+        tp.q = q;
+        tp.k_codes = const_cast<int8_t*>(kv->k_codes);
+        tp.k_scales = const_cast<uint16_t*>(kv->k_scales);
+        tp.v_codes = const_cast<int8_t*>(kv->v_codes);
+        tp.v_scales = const_cast<uint16_t*>(kv->v_scales);
+        tp.part_o = vp.part_o;
+        tp.part_ml = vp.part_ml;
+        tp.k_new = k_new;
+        tp.v_new = v_new;
+        tp.err = nullptr;
+        tp.n_rows = n_rows;
+        tp.n_q_heads = n_q_heads;
+        tp.group = vp.group;
+        tp.group_magic = vp.group_magic;
+        tp.capacity = kv->capacity;
+        tp.kv_len = kv_len;
+        tp.q_pos0 = q_pos0;
+        tp.keys_per_split = pl.keys_per_split;
+        tp.key_shift = pl.key_shift;
+        tp.n_ctx_splits = pl.n_ctx_splits;
+        tp.n_kv_heads = kv->n_kv_heads;
+        tp.rows_per_chunk = pl.rows_per_chunk;
+        tp.qscale = vp.qscale;
+        r1 = launch_verify_tc(tp, pl, kv->n_kv_heads, append, s);
+    } else if (v4)  // K8V4 pools: causal windows, no append
         r1 = pl.hd == 128 ? dispatch_nt<128, false, true>(vp, pl, kv->n_kv_heads, s)
                           : dispatch_nt<256, false, true>(vp, pl, kv->n_kv_heads, s);
+    else if (wmask)  // tree windows have no append variant
+        r1 = pl.hd == 128 ? dispatch_nt<128, true>(vp, pl, kv->n_kv_heads, s)
+                          : dispatch_nt<256, true>(vp, pl, kv->n_kv_heads, s);
     else
-        r1 = pl.hd == 128 ? dispatch_nt<128, false, false>(vp, pl, kv->n_kv_heads, s)
-                          : dispatch_nt<256, false, false>(vp, pl, kv->n_kv_heads, s);
+        return KVQ8_ERR_UNSUPPORTED;
     if (r1 != KVQ8_OK || partials) return r1;
     return launch_combine(vp.part_o, reinterpret_cast<const float*>(vp.part_ml), pl.n_split, (int)rows_total,
                           kv->head_dim, out, s);
@@ -890,7 +859,7 @@ extern "C" int attn_verify_k8v4(const float* q, int n_rows, int n_q_heads, const
 extern "C" int attn_verify_q8_partials_count(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_kv_heads,
                                              int n_split) {
     kvq8::Plan pl;
-    if (kvq8::make_plan(n_rows, n_q_heads, head_dim, kv_len, n_kv_heads, n_split, &pl) != KVQ8_OK) return 0;
+    if (kvq8::plan_tc(n_rows, n_q_heads, head_dim, kv_len, n_kv_heads, n_split, &pl) != KVQ8_OK) return 0;
     return pl.n_split;
 }
 
@@ -905,7 +874,7 @@ extern "C" int attn_verify_q8_partials(const float* q, int n_rows, int n_q_heads
 extern "C" size_t attn_verify_append_q8_workspace_bytes(int n_rows, int n_q_heads, int head_dim, int q_pos0,
                                                         int n_kv_heads, int n_split) {
     kvq8::Plan pl;
-    if (q_pos0 < 0 || kvq8::make_plan(n_rows, n_q_heads, head_dim, q_pos0 + n_rows, n_kv_heads, n_split, &pl,
+    if (q_pos0 < 0 || kvq8::plan_tc(n_rows, n_q_heads, head_dim, q_pos0 + n_rows, n_kv_heads, n_split, &pl,
                                       n_rows) != KVQ8_OK)
         return 0;
     return pl.ws_bytes;
@@ -929,7 +898,7 @@ struct HostScratch {
 inline size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 bool host_scratch(int n_rows, int n_q_heads, int head_dim, int q_pos0, int n_kv_heads, int n_split, HostScratch* h) {
     kvq8::Plan pl;
-    if (q_pos0 < 0 || kvq8::make_plan(n_rows, n_q_heads, head_dim, q_pos0 + n_rows, n_kv_heads, n_split, &pl,
+    if (q_pos0 < 0 || kvq8::plan_tc(n_rows, n_q_heads, head_dim, q_pos0 + n_rows, n_kv_heads, n_split, &pl,
                                       n_rows) != KVQ8_OK)
         return false;
     const size_t q_bytes = (size_t)n_rows * n_q_heads * head_dim * sizeof(float);
@@ -1075,25 +1044,13 @@ extern "C" int attn_verify_q8_noalloc(const float* q, int n_rows, int n_q_heads,
     using namespace kvq8;
     if (!kv) return KVQ8_ERR_INVALID_ARG;
     Plan pl;
-    int rc = make_plan(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, n_split, &pl);
+    const int rc = plan_tc(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, n_split, &pl);
     if (rc != KVQ8_OK) return rc;
-    if (pl.ws_bytes > (size_t)KVQ8_NOALLOC_SCRATCH_BYTES) {
-        if (n_split != 0) return KVQ8_ERR_WORKSPACE;  // the caller's split count does not fit
-        // automatic split count: take the largest one whose partials fit the array
-        const size_t rows_total = (size_t)n_rows * n_q_heads;
-        const size_t per_split = rows_total * (size_t)kv->head_dim * sizeof(float) + rows_total * 2 * sizeof(float);
-        int ns = (int)((KVQ8_NOALLOC_SCRATCH_BYTES - 256) / per_split);
-        for (; ns >= 1; --ns) {
-            rc = make_plan(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, ns, &pl);
-            if (rc != KVQ8_OK) return rc;
-            if (pl.ws_bytes <= (size_t)KVQ8_NOALLOC_SCRATCH_BYTES) break;
-        }
-        if (ns < 1) return KVQ8_ERR_WORKSPACE;  // even one slice exceeds the array
-        n_split = ns;
-    }
+    // the partials of this plan must fit the array; nothing is launched otherwise
+    if (pl.ws_bytes > (size_t)KVQ8_NOALLOC_SCRATCH_BYTES) return KVQ8_ERR_WORKSPACE;
     void* scratch = nullptr;
-    rc = noalloc_scratch(&scratch);
-    if (rc != KVQ8_OK) return rc;
+    const int rs = noalloc_scratch(&scratch);
+    if (rs != KVQ8_OK) return rs;
     return attn_verify_q8(q, n_rows, n_q_heads, kv, kv_len, q_pos0, softmax_scale, out, scratch,
                           (size_t)KVQ8_NOALLOC_SCRATCH_BYTES, n_split, stream);
 }

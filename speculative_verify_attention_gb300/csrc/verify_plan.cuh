@@ -15,6 +15,9 @@ constexpr int kMaxNT = 4;       // n8 row tiles per chunk (<= 32 rows per thread
 
 // resident thread blocks per SM of the Q8_0 verify kernel: two up to 24 rows per chunk
 inline int q8_blocks_per_sm(int /*hd*/, int nt) { return nt <= 3 ? 2 : 1; }
+// ... and of the tcgen05 verify kernel (all of tensor memory, about 196 KB of shared memory)
+inline int tc_blocks_per_sm(int /*hd*/, int /*nt*/) { return 1; }
+constexpr int kTcMaxRows = 24;  // rows per chunk of the tcgen05 verify kernel
 
 struct Plan {
     int hd, nt, n_chunks, rows_per_chunk, n_split, keys_per_split, key_shift, n_ctx_splits;
@@ -36,8 +39,11 @@ inline int sm_count() {
 
 // window_keys > 0: the last window_keys keys get a slice of their own (the append-and-verify
 // path), the context slices cover the keys before them.
+// max_rows: rows (row x q-head pairs) per chunk at most, a multiple of 8 (32 for the all-mma.sync
+// kernels, 24 for the tcgen05 one).  sms: SM count to plan for (0 = the current device's).
 inline int make_plan(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_kv_heads, int n_split_req, Plan* pl,
-                     int window_keys = 0, int (*blocks_per_sm)(int hd, int nt) = q8_blocks_per_sm) {
+                     int window_keys = 0, int (*blocks_per_sm)(int hd, int nt) = q8_blocks_per_sm,
+                     int max_rows = 8 * kMaxNT, int sms = 0) {
     if (n_rows < 1 || n_rows > 32 || n_q_heads < 1 || n_kv_heads < 1 || kv_len < 1) return KVQ8_ERR_INVALID_ARG;
     if (n_q_heads % n_kv_heads) return KVQ8_ERR_UNSUPPORTED;
     const int group = n_q_heads / n_kv_heads;
@@ -46,7 +52,7 @@ inline int make_plan(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_
     if (n_split_req < 0 || n_split_req > 1024) return KVQ8_ERR_INVALID_ARG;
     const int R = n_rows * group;
     pl->hd = head_dim;
-    pl->n_chunks = (R + 8 * kMaxNT - 1) / (8 * kMaxNT);
+    pl->n_chunks = (R + max_rows - 1) / max_rows;
     pl->rows_per_chunk = (R + pl->n_chunks - 1) / pl->n_chunks;
     pl->nt = (pl->rows_per_chunk + 7) / 8;
     // slices are whole 16-key units, fine enough that the blocks of one wave get nearly equal
@@ -57,7 +63,7 @@ inline int make_plan(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_
     const int n_units = (ctx_end + kSplitUnit - 1) / kSplitUnit;
     int ns = n_split_req;
     if (ns == 0) {
-        int sms = sm_count();
+        if (sms <= 0) sms = sm_count();
         if (sms <= 0) sms = 152;
         const int per_sm = blocks_per_sm(head_dim, pl->nt);
         ns = std::max(1, (per_sm * sms) / (n_kv_heads * pl->n_chunks));

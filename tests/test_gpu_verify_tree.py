@@ -62,17 +62,20 @@ def test_random_masks_hd128_and_context_free_rows(lib):
             assert not got[0].any()              # row 0 sees nothing
 
 
-def test_chain_mask_matches_causal_kernel_bitwise(lib):
+def test_chain_mask_matches_causal_call(lib):
+    """A chain mask is the sequential window: the tree kernel and the causal call (a different
+    kernel, with its own rounding order) agree far inside the oracle tolerance."""
     import torch
 
     from speculative_verify_attention_gb300 import attn_verify_q8
     w = workloads.verify_27b(8)
     inp = workloads.make_inputs(w)
-    gpu, _ = build_caches(inp, garbage_tail=False)
+    gpu, orc = build_caches(inp, garbage_tail=False)
     got = _run(gpu, inp.q, w.kv_len, w.q_pos0, w.softmax_scale, oracle.chain_mask(8))
     ref = attn_verify_q8(torch.from_numpy(inp.q).cuda(), gpu, w.kv_len, w.q_pos0, w.softmax_scale)
     torch.cuda.synchronize()
-    assert np.array_equal(got, ref.cpu().numpy())
+    assert rel_err(got, ref.cpu().numpy()) <= 1e-5
+    assert rel_err(got, oracle.attention(orc, inp.q, w.kv_len, w.q_pos0, w.softmax_scale)) <= VERIFY_TOL
 
 
 def test_tree_rejects_bad_arguments(lib):
