@@ -376,10 +376,13 @@ int attn_prompt_q8(const uint16_t* q, int n_q, int n_q_heads, const kvq8_cache* 
  *     current); make that first call before any stream capture.
  *   - All calls share the one array: calls that overlap on the GPU (different streams, or
  *     several host threads) race on it and must be serialised by the caller.
- *   - With n_split = 0 the split count is lowered, if needed, until the partials fit; a
- *     shape whose partials do not fit even with one slice (n_rows * n_q_heads * (head_dim
- *     + 2) * 4 bytes above the array), or an explicit n_split that does not fit, returns
- *     KVQ8_ERR_WORKSPACE and launches nothing.
+ *   - With n_split = 0 the automatic plan is used: each KV head and row chunk (up to 24
+ *     row x q-head pairs) gets at most SM count / (KV heads x chunks) context slices, so the
+ *     partials take at most about SM count x 24 x (head_dim + 2) x 4 bytes (3.8 MB at
+ *     head_dim 256 on 152 SMs).  When there are more KV heads x chunks than SMs every chunk
+ *     gets one slice, n_rows * n_q_heads * (head_dim + 2) * 4 bytes in all.  A plan, automatic
+ *     or from an explicit n_split, whose partials exceed the array returns KVQ8_ERR_WORKSPACE
+ *     and launches nothing.
  */
 #define KVQ8_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
 int attn_verify_q8_noalloc(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv, int kv_len,

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "kvq8attn.h"
 
 namespace kvq8 {
@@ -17,6 +19,26 @@ __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_c
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<const __half2*>(&u); }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The dynamic shared-memory opt-in of one kernel, set once per device (the attribute belongs to
+// the kernel on the current device); one static object per kernel instantiation.
+struct SmemOptIn {
+    static constexpr int kMaxDev = 64;
+    std::mutex mu;
+    bool done[kMaxDev] = {};
+    template <typename Kernel>
+    int ensure(Kernel* kernel, int bytes) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return KVQ8_ERR_CUDA;
+        std::lock_guard<std::mutex> lock(mu);
+        if (!done[dev]) {
+            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+                return KVQ8_ERR_CUDA;
+            done[dev] = true;
+        }
+        return KVQ8_OK;
+    }
+};
 
 inline int launch_status() {
     cudaError_t e = cudaGetLastError();

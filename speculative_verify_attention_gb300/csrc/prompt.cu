@@ -741,13 +741,8 @@ int prompt_plan(int n_q, int n_q_heads, int head_dim, int kv_len, int q_pos0, in
 
 template <int HD, int POOL>
 int launch_prompt(const PromptParams& pp, int grid, cudaStream_t s) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(prompt_attn_kernel<HD, POOL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 PL<HD>::SMEM_BYTES) != cudaSuccess)
-            return KVQ8_ERR_CUDA;
-        attr_set = true;
-    }
+    static SmemOptIn opt;
+    if (opt.ensure(prompt_attn_kernel<HD, POOL>, PL<HD>::SMEM_BYTES) != KVQ8_OK) return KVQ8_ERR_CUDA;
     prompt_attn_kernel<HD, POOL><<<grid, kThreads, PL<HD>::SMEM_BYTES, s>>>(pp);
     return launch_status();
 }

@@ -37,7 +37,6 @@
 // attn_verify_append_q8_host works from host buffers: pinned ones are read by a copy kernel
 // and written in place by the merge, pageable ones go through copy-engine transfers.
 #include <algorithm>
-#include <mutex>
 
 #include "common.cuh"
 #include "verify_plan.cuh"
@@ -676,21 +675,8 @@ __global__ void __launch_bounds__(kThreads, (NT <= 3 ? 2 : 1)) verify_split_kern
 template <int HD, int NT, bool TREE, bool V4>
 int launch_verify(const VerifyParams& vp, const Plan& pl, int n_kv_heads, cudaStream_t stream) {
     constexpr int bytes = Smem<HD, NT>::kBytes;
-    // the shared-memory opt-in is a property of the kernel on one device: set once per device
-    constexpr int kMaxDev = 64;
-    static bool attr_set[kMaxDev] = {};
-    static std::mutex mu;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return KVQ8_ERR_CUDA;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (!attr_set[dev]) {
-            if (cudaFuncSetAttribute(verify_split_kernel<HD, NT, TREE, V4>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
-                return KVQ8_ERR_CUDA;
-            attr_set[dev] = true;
-        }
-    }
+    static SmemOptIn opt;
+    if (opt.ensure(verify_split_kernel<HD, NT, TREE, V4>, bytes) != KVQ8_OK) return KVQ8_ERR_CUDA;
     dim3 grid(pl.n_chunks, pl.n_split, n_kv_heads);
     verify_split_kernel<HD, NT, TREE, V4><<<grid, kThreads, bytes, stream>>>(vp);
     return launch_status();

@@ -434,13 +434,8 @@ __global__ void __launch_bounds__(kThreads, f16_min_blocks<HD, NT>()) verify_f16
 template <int HD, int NT>
 int launch_f16(const F16Params& fp, const Plan& pl, int n_kv_heads, cudaStream_t stream) {
     constexpr int bytes = SmemF16<HD, NT>::kBytes;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(verify_f16_kernel<HD, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
-            cudaSuccess)
-            return KVQ8_ERR_CUDA;
-        attr_set = true;
-    }
+    static SmemOptIn opt;
+    if (opt.ensure(verify_f16_kernel<HD, NT>, bytes) != KVQ8_OK) return KVQ8_ERR_CUDA;
     dim3 grid(pl.n_chunks, pl.n_split, n_kv_heads);
     verify_f16_kernel<HD, NT><<<grid, kThreads, bytes, stream>>>(fp);
     return launch_status();

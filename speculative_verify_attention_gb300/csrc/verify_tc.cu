@@ -748,20 +748,8 @@ bool encode_code_plane(CUtensorMap* map, const int8_t* plane, int hd, int kv_len
 template <int HD, int RP, bool APPEND>
 int launch_tc(const VerifyTcParams& vp, dim3 grid, cudaStream_t s) {
     using L = TcLayout<HD, RP>;
-    constexpr int kMaxDev = 64;
-    static bool attr_set[kMaxDev] = {};
-    static std::mutex mu;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return KVQ8_ERR_CUDA;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (!attr_set[dev]) {
-            if (cudaFuncSetAttribute(verify_tc_kernel<HD, RP, APPEND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     L::BYTES) != cudaSuccess)
-                return KVQ8_ERR_CUDA;
-            attr_set[dev] = true;
-        }
-    }
+    static SmemOptIn opt;
+    if (opt.ensure(verify_tc_kernel<HD, RP, APPEND>, L::BYTES) != KVQ8_OK) return KVQ8_ERR_CUDA;
     verify_tc_kernel<HD, RP, APPEND><<<grid, kTcThreads, L::BYTES, s>>>(vp);
     return launch_status();
 }

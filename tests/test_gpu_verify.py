@@ -69,7 +69,10 @@ def test_hd128_workload(lib, T):
 @pytest.mark.parametrize("ctx", workloads.LONG_CTX)
 @pytest.mark.parametrize("T", workloads.LONG_T)
 def test_long_context_workload(lib, ctx, T):
+    from speculative_verify_attention_gb300 import kvq8_device_error
+    kvq8_device_error(reset=True)
     _check_sampled(workloads.long_verify(ctx, T))
+    assert kvq8_device_error(reset=True) == 0, "a kernel gave up on an internal wait"
 
 
 @pytest.mark.parametrize("hq,hkv,hd,L,T,pos0", [
@@ -161,3 +164,30 @@ def test_verify_rejects_bad_arguments(lib):
     with pytest.raises(KVQ8Error) as e:       # workspace too small
         attn_verify_q8(q, c, 40, 0, 0.1, workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
     assert e.value.status == 4
+
+
+def test_second_device_after_the_first(lib):
+    """The kernels' shared-memory opt-in is per device: a process that drives a second GPU runs
+    the verify and prompt kernels there after running them on the first."""
+    import torch
+
+    from speculative_verify_attention_gb300 import KVCacheQ8, attn_prompt_q8, attn_verify_q8
+    if torch.cuda.device_count() < 2:
+        pytest.skip("one GPU visible")
+    w = workloads.TINY
+    inp = workloads.make_inputs(w)
+    pw = workloads.prompt_workload("two-device-prompt", 12, 1, 256, 512, 128, seed=4011)
+    pin = workloads.make_inputs(pw)
+    outs = []
+    for dev in (0, 1):
+        with torch.cuda.device(dev):
+            c = KVCacheQ8(w.n_kv_heads, w.head_dim, w.kv_len, device=f"cuda:{dev}")
+            c.append(torch.from_numpy(inp.k).to(f"cuda:{dev}"), torch.from_numpy(inp.v).to(f"cuda:{dev}"), 0)
+            o = attn_verify_q8(torch.from_numpy(inp.q).to(f"cuda:{dev}"), c, w.kv_len, w.q_pos0, w.softmax_scale)
+            pc = KVCacheQ8(1, 256, pw.kv_len, device=f"cuda:{dev}")
+            pc.append(torch.from_numpy(pin.k).to(f"cuda:{dev}"), torch.from_numpy(pin.v).to(f"cuda:{dev}"), 0)
+            po = attn_prompt_q8(torch.from_numpy(pin.q).to(f"cuda:{dev}"), pc, pw.kv_len, pw.q_pos0, pw.softmax_scale)
+            torch.cuda.synchronize(dev)
+            outs.append((o.cpu().numpy(), po.cpu().numpy()))
+    assert np.array_equal(outs[0][0], outs[1][0])
+    assert np.array_equal(outs[0][1], outs[1][1])
