@@ -3,28 +3,32 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
 
-One JSON line on rank 0.  A step is one speculative-verify step on the 27B-class
-workload (24 q heads / 4 kv heads, head_dim 256, context 4096): for each window length
+One JSON line on rank 0.  A step is one speculative-verify step on the long-context
+workload (24 q heads / 4 kv heads, head_dim 256, context 20,676): for each window length
 T in {4, 8}, one attn_verify_append_q8 call appends the T new K/V tokens to the Q8_0 cache
 and runs the verify scan over ctx + T keys: the split-context kernel, whose window slice
-quantises the new tokens itself, and the log-sum-exp combine.
+quantises the new tokens itself, and the log-sum-exp combine.  The two windows are
+independent problems (each on its own cache) and run on two streams.
 `value` is the KV-scan bandwidth of the whole job (Q8_0 K/V bytes read by the verify
-calls / time), in GB/s; `us_per_call` gives the per-call latency.  The prompt-chunk
-kernel (12 q heads / 1 kv head, hd256, 2048 queries over a 32768-token int8 context) is
-timed in the same run and reported under "prompt" in TFLOP/s.
+calls / time), in GB/s; `per_T` gives the per-call latency of each window length, `cells`
+the same figures at contexts 32,768 and 4,096.  The prompt-chunk kernel (12 q heads /
+1 kv head, hd256, 2048 queries over a 32768-token int8 context) is timed in the same run
+and reported under "prompt" in TFLOP/s.
 
-Timing: steps are captured once in a CUDA graph and replayed, so the device time is not
-hidden behind Python launch overhead; every step reads a different cache of a ring whose
-total size is above 4x the L2, so K/V bytes come from HBM.  The `e2e` figure instead goes
-through the C ABI's host-buffer entry (attn_verify_append_q8_host) with pinned host
-buffers: each call copies q and the new K/V tokens host->device in one copy, runs the
-kernels and reads the output back, eagerly, with no graph.
+Timing: steps are captured in CUDA graphs and replayed, so the device time is not hidden
+behind Python launch overhead; exactly --warmup untimed and --steps timed steps run (a graph
+of up to 64 steps, replayed, plus one graph of the remainder).  Every step reads a different
+cache of a ring whose total size is above 4x the L2, so K/V bytes come from HBM.  The `e2e`
+figure instead goes through the C ABI's host-buffer entry (attn_verify_append_q8_host) with
+pinned host buffers: each call copies q and the new K/V tokens host->device in one copy,
+runs the kernels and reads the output back, eagerly, with no graph.
 """
 from __future__ import annotations
 
 import argparse
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -39,7 +43,22 @@ sys.path.insert(0, ROOT)
 METRIC = "verify-attn us/call and KV-scan GB/s (% HBM peak); prompt-attn TFLOP/s"
 L2_BYTES = 129 * 1024 * 1024
 VERIFY_T = (4, 8)
-GRAPH_STEPS = 64
+HEADLINE_CTX = 20676            # the context the pages' verify speedups are quoted at
+EXTRA_CTX = (32768, 4096)       # the largest context, and the 27B-class context with outliers
+GRAPH_MAX = 64                  # steps per CUDA graph at most
+HEADLINE_WORKLOAD = f"verify-24q4kv-hd256-ctx{HEADLINE_CTX}-T4+T8"
+
+
+def graph_chunks(n: int, g_max: int = GRAPH_MAX) -> list[tuple[int, int]]:
+    """(steps per graph, replays) pairs whose steps add up to exactly n: a graph of
+    min(n, g_max) steps replayed n // that many times, plus one graph of the remainder."""
+    if n <= 0:
+        return []
+    g = min(n, g_max)
+    out = [(g, n // g)]
+    if n % g:
+        out.append((n % g, 1))
+    return out
 
 
 def _peaks():
@@ -131,7 +150,6 @@ def kernel_source_digest(kernel_files) -> str:
     """sha256 of the kernel sources' code with comments and blank lines removed, so that an
     edit of comments alone keeps a capture valid while any change of code invalidates it."""
     import hashlib
-    import re
     h = hashlib.sha256()
     for name in kernel_files:
         with open(os.path.join(ROOT, "speculative_verify_attention_gb300", "csrc", name)) as f:
@@ -156,13 +174,16 @@ def _kernel_traffic(kernel_files, workload: str):
 
 # ----------------------------------------------------------------------------- oracle arm
 
-def oracle_verify_sample(n_pairs_per_step: int, steps: int, warmup: int, threads: int | None = None):
-    """Time the fp64 oracle on (row, head) pairs of the 27B-class T=4 verify call.
+def oracle_verify_sample(steps: int, warmup: int, budget_s: float, threads: int | None = None,
+                         max_pairs: int = 96):
+    """Time the fp64 oracle on (row, q-head) pairs of the headline T=4 verify call (context
+    20,676), a bounded sample: one untimed probe batch sets the pairs per step so that `steps`
+    steps take about `budget_s` seconds (at least one pair, at most max_pairs).
     Returns (GB/s-equivalent, seconds per step, threads, description)."""
     import oracle
     from speculative_verify_attention_gb300 import workloads
 
-    w = workloads.verify_27b(4)
+    w = workloads.long_verify(HEADLINE_CTX, 4)
     inp = workloads.make_inputs(w)
     c = oracle.Cache(w.n_kv_heads, w.head_dim, w.kv_len)
     c.append(inp.k, inp.v, 0)
@@ -172,20 +193,25 @@ def oracle_verify_sample(n_pairs_per_step: int, steps: int, warmup: int, threads
     pairs = [(i, h) for i in range(w.n_q) for h in range(w.n_q_heads)]
     rng = np.random.default_rng(0)
 
-    def one():
-        sel = [pairs[k] for k in rng.integers(0, len(pairs), n_pairs_per_step)]
+    def run(n):
+        sel = [pairs[k] for k in rng.integers(0, len(pairs), n)]
         oracle.attention(c, inp.q, w.kv_len, w.q_pos0, w.softmax_scale, sel=sel)
 
+    t0 = time.perf_counter()
+    run(n_thr)                                           # probe: one pair per thread
+    per_pair = (time.perf_counter() - t0) / n_thr
+    n_pairs = int(max(1, min(max_pairs, budget_s / max(steps, 1) / max(per_pair, 1e-9))))
     for _ in range(warmup):
-        one()
+        run(n_pairs)
     t0 = time.perf_counter()
     for _ in range(steps):
-        one()
+        run(n_pairs)
     dt = time.perf_counter() - t0
-    calls = steps * n_pairs_per_step / len(pairs)
+    calls = steps * n_pairs / len(pairs)
     gbs = calls * w.kv_bytes() / dt / 1e9
-    desc = (f"{n_pairs_per_step} (row, q-head) pairs per step of the T=4 call (kv_len {w.kv_len}); "
-            f"GB/s counts each pair as 1/{len(pairs)} of the call's {w.kv_bytes() / 1e6:.2f} MB of K/V")
+    desc = (f"{n_pairs} random (row, q-head) pairs per step of the {len(pairs)} of the T=4 call at context "
+            f"{HEADLINE_CTX} (kv_len {w.kv_len}), {steps} steps; GB/s counts each pair as 1/{len(pairs)} of the "
+            f"call's {w.kv_bytes() / 1e6:.2f} MB of K/V")
     return gbs, dt / steps, n_thr, desc
 
 
@@ -249,13 +275,11 @@ def oracle_sweep() -> None:
 def run_reference(args, world, rank):
     if rank != 0:
         return 0
-    n_pairs = 8 if args.steps > 200 else 96
-    gbs, sec, thr, desc = oracle_verify_sample(n_pairs, args.steps, min(args.warmup, 3))
-    from speculative_verify_attention_gb300 import workloads
+    gbs, sec, thr, desc = oracle_verify_sample(args.steps, min(args.warmup, 3), budget_s=90.0)
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workloads.verify_27b(4).name + " (CPU oracle sample)"},
+            "config": {"workload": HEADLINE_WORKLOAD + " (CPU oracle sample)"},
             "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": thr, "kind": "oracle", "sample": desc},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -269,34 +293,27 @@ def run_native(args, world, rank, local):
 
     import __graft_entry__
     __graft_entry__.build()
-    from speculative_verify_attention_gb300 import (KVCacheQ8, KVQ8Error, attn_prompt_q8, attn_verify_append_q8,
-                                                    attn_verify_append_q8_workspace_bytes, attn_verify_q8,
-                                                    attn_verify_q8_workspace_bytes, workloads)
+    from speculative_verify_attention_gb300 import (PreparedAppendVerifyHost, attn_verify_append_q8,
+                                                    attn_verify_append_q8_host_scratch_bytes,
+                                                    attn_verify_append_q8_workspace_bytes,
+                                                    attn_verify_q8_workspace_bytes, kvq8_device_error, workloads)
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     hbm_peak, bf16_peak, peak_src = _peaks()
-    fp16_peak = bf16_peak * 0.951   # cuBLAS fp16 / bf16 measured on this part: 1815.6 / 1908.7
+    fp16_peak = bf16_peak   # fp16 and bf16 operands share one dense tensor-core rate
 
-    ws_ = {T: workloads.verify_27b(T) for T in VERIFY_T}
+    ctx = HEADLINE_CTX
+    ws_ = {T: workloads.long_verify(ctx, T) for T in VERIFY_T}
     w0 = ws_[VERIFY_T[0]]
-    ctx = w0.ctx
-    cap = ctx + max(VERIFY_T)
-    inp = workloads.make_inputs(workloads.verify_27b(max(VERIFY_T)))   # K/V for ctx + 8 tokens, seeded
-    base = KVCacheQ8(w0.n_kv_heads, w0.head_dim, cap, device=dev)
-    base.append(torch.from_numpy(inp.k).to(dev), torch.from_numpy(inp.v).to(dev), 0)
-    cache_bytes = sum(t.numel() * t.element_size() for t in (base.k_codes, base.v_codes, base.k_scales, base.v_scales))
-    n_ring = max(2, int(np.ceil(args.ring_l2 * L2_BYTES / cache_bytes)))
-    ring = [base]
-    for _ in range(n_ring - 1):
-        c = KVCacheQ8(w0.n_kv_heads, w0.head_dim, cap, device=dev)
-        for a, b in ((c.k_codes, base.k_codes), (c.v_codes, base.v_codes), (c.k_scales, base.k_scales),
-                     (c.v_scales, base.v_scales)):
-            a.copy_(b)
-        ring.append(c)
+    inp = workloads.make_inputs(ws_[max(VERIFY_T)])     # K/V for ctx + 8 tokens, seeded
+    ring = _ring_for(ws_[max(VERIFY_T)], dev, args.ring_l2, inp=inp)
+    n_ring = len(ring)
+    cache_bytes = _cache_bytes(ring[0])
     q = {T: torch.from_numpy(workloads.make_inputs(ws_[T], kv_len=1).q).to(dev) for T in VERIFY_T}
     knew = {T: torch.from_numpy(inp.k[ctx:ctx + T].copy()).to(dev) for T in VERIFY_T}
     vnew = {T: torch.from_numpy(inp.v[ctx:ctx + T].copy()).to(dev) for T in VERIFY_T}
+    del inp
     out = {T: torch.empty_like(q[T]) for T in VERIFY_T}
     wsb = {T: torch.empty(max(attn_verify_q8_workspace_bytes(T, w0.n_q_heads, w0.head_dim, ctx + T, w0.n_kv_heads),
                               attn_verify_append_q8_workspace_bytes(T, w0.n_q_heads, w0.head_dim, ctx,
@@ -306,48 +323,46 @@ def run_native(args, world, rank, local):
 
     side = [torch.cuda.Stream(device=dev) for _ in VERIFY_T]
 
-    def step(s, do_append=True, concurrent=True):
-        # the step's windows are independent problems (their own caches of the ring); with
-        # concurrent=True each runs on a stream of its own, as two sequences' verify calls would
+    def step(s):
+        # the step's windows are independent problems (their own caches of the ring), each on a
+        # stream of its own, as two sequences' verify calls would be; each call appends its
+        # window's K/V to the cache (fused into the verify kernel) and scans ctx + T keys
         cur = torch.cuda.current_stream()
         for j, T in enumerate(VERIFY_T):
             c = ring[(s + j * (n_ring // len(VERIFY_T))) % n_ring]
-            st = side[j] if concurrent else cur
-            st.wait_stream(cur)
-            with torch.cuda.stream(st):
-                if do_append:   # append of the window's K/V fused with the verify scan
-                    attn_verify_append_q8(q[T], knew[T], vnew[T], c, ctx, w0.softmax_scale, out=out[T],
-                                          workspace=wsb[T])
-                else:
-                    attn_verify_q8(q[T], c, ctx + T, ctx, w0.softmax_scale, out=out[T], workspace=wsb[T])
-        if concurrent:
-            for st in side:
-                cur.wait_stream(st)
+            side[j].wait_stream(cur)
+            with torch.cuda.stream(side[j]):
+                attn_verify_append_q8(q[T], knew[T], vnew[T], c, ctx, w0.softmax_scale, out=out[T],
+                                      workspace=wsb[T])
+        for st in side:
+            cur.wait_stream(st)
 
     launches_per_step = len(VERIFY_T) * 2   # verify split (with the append) + combine per T
 
-    def capture(**kw):
-        s = torch.cuda.Stream(device=dev)
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            for i in range(3):
-                step(i, **kw)
-        torch.cuda.current_stream().wait_stream(s)
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for i in range(GRAPH_STEPS):
-                step(i, **kw)
-        return g
+    timed_chunks = graph_chunks(args.steps)
+    warm_chunks = graph_chunks(args.warmup)
+    s_ = torch.cuda.Stream(device=dev)
+    s_.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s_):
+        for i in range(3):
+            step(i)
+    torch.cuda.current_stream().wait_stream(s_)
+    torch.cuda.synchronize()
+    graphs = {}
+    for g_len, _ in timed_chunks + warm_chunks:
+        if g_len not in graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(g_len):
+                    step(i)
+            graphs[g_len] = g
 
-    g_step = capture()
-    g_verify = capture(do_append=False, concurrent=False)   # one call at a time: the per-call time
-    reps = max(1, int(np.ceil(args.steps / GRAPH_STEPS)))
-    steps = reps * GRAPH_STEPS
-    wreps = max(1, int(np.ceil(args.warmup / GRAPH_STEPS)))
+    def replay(chunks):
+        for g_len, reps in chunks:
+            for _ in range(reps):
+                graphs[g_len].replay()
 
-    for _ in range(wreps):
-        g_step.replay()
+    replay(warm_chunks)
     torch.cuda.synchronize()
     _barrier(world)
     torch.cuda.synchronize()
@@ -355,64 +370,25 @@ def run_native(args, world, rank, local):
     clk.start()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(reps):
-        g_step.replay()
+    replay(timed_chunks)
     e1.record()
     torch.cuda.synchronize()
     _barrier(world)
     ms = e0.elapsed_time(e1)
-    # the verify calls alone (same ring walk), for the roofline of the dominant kernel
-    v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    v0.record()
-    for _ in range(reps):
-        g_verify.replay()
-    v1.record()
-    torch.cuda.synchronize()
-    clocks = clk.stop()
-    ms_verify = v0.elapsed_time(v1)
-    ms = _max_over_ranks(ms, world)
 
+    # per-T cells (one call at a time): the whole call (split + combine) and the split kernel
+    # alone, whose time is the roofline's denominator
+    per_t = {T: _verify_cell(ws_[T], ring, dev, hbm_peak) for T in VERIFY_T}
+    clocks = clk.stop()
+    ms = _max_over_ranks(ms, world)
+    steps = args.steps
     ms_per_step = ms / steps
     gbs = world * kv_bytes_step * steps / (ms * 1e-3) / 1e9
-    us_per_call_verify = ms_verify * 1e3 / (steps * len(VERIFY_T))
-    verify_gbs = kv_bytes_step * steps / (ms_verify * 1e-3) / 1e9
-
-    # per-T latency (graph of a single T)
-    per_t = {}
-    for T in VERIFY_T:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for i in range(GRAPH_STEPS):
-                attn_verify_q8(q[T], ring[i % n_ring], ctx + T, ctx, w0.softmax_scale, out=out[T], workspace=wsb[T])
-        g.replay()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(max(1, reps // 2)):
-            g.replay()
-        b.record()
-        torch.cuda.synchronize()
-        us = a.elapsed_time(b) * 1e3 / (max(1, reps // 2) * GRAPH_STEPS)
-        per_t[f"T{T}"] = {"us_per_call": us, "kv_gbs": ws_[T].kv_bytes() / (us * 1e-6) / 1e9,
-                          "hbm_frac": ws_[T].kv_bytes() / (us * 1e-6) / 1e9 / hbm_peak}
-
-    # the long-context cells the pages' headline speedups are quoted at (ctx 20,676)
-    long_ctx = {}
-    if not args.no_long_context:
-        torch.cuda.empty_cache()
-        lw = {T: workloads.long_verify(20676, T) for T in VERIFY_T}
-        lring = _ring_for(lw[max(VERIFY_T)], dev, args.ring_l2)   # capacity covers every T
-        for T in VERIFY_T:
-            us = time_verify_cell(lw[T], lring, dev)
-            gbs_ = lw[T].kv_bytes() / (us * 1e-6) / 1e9
-            long_ctx[f"T{T}"] = {"workload": lw[T].name, "us_per_call": us, "kv_gbs": gbs_, "hbm_frac": gbs_ / hbm_peak}
-        del lring
-        torch.cuda.empty_cache()
+    del graphs
 
     # e2e through the C ABI with pinned host buffers, eager: per T one attn_verify_append_q8_host
     # call (q, k_new, v_new copied in with one host-to-device copy, the two kernels, the output
     # copied back)
-    from speculative_verify_attention_gb300 import PreparedAppendVerifyHost, attn_verify_append_q8_host_scratch_bytes
     h_in = {T: torch.cat([q[T].cpu().reshape(-1), knew[T].cpu().reshape(-1), vnew[T].cpu().reshape(-1)]).pin_memory()
             for T in VERIFY_T}
     h_out = {T: torch.empty(out[T].numel(), dtype=torch.float32).pin_memory() for T in VERIFY_T}
@@ -445,6 +421,19 @@ def run_native(args, world, rank, local):
     torch.cuda.synchronize()
     e2e_sec = _max_over_ranks(time.perf_counter() - t0, world)
     e2e_gbs = world * kv_bytes_step * e2e_steps / e2e_sec / 1e9
+    del prepared, ring
+    torch.cuda.empty_cache()
+
+    # the other contexts of the family: the largest (32,768) and the 27B-class 4,096 with outliers
+    cells = {}
+    if not args.no_long_context:
+        for c_ in EXTRA_CTX:
+            cw = {T: (workloads.long_verify(c_, T) if c_ != 4096 else workloads.verify_27b(T)) for T in VERIFY_T}
+            cring = _ring_for(cw[max(VERIFY_T)], dev, args.ring_l2)   # capacity covers every T
+            for T in VERIFY_T:
+                cells[cw[T].name] = _verify_cell(cw[T], cring, dev, hbm_peak)
+            del cring
+            torch.cuda.empty_cache()
 
     # prompt chunk (tensor-core kernel), L2 flushed between timed calls
     prompt = prompt_bench(args, dev, fp16_peak) if not args.no_prompt else None
@@ -458,27 +447,30 @@ def run_native(args, world, rank, local):
         prompt["f16"] = prompt_bench(args, dev, fp16_peak, _wl.PROMPT, pool="f16")
     head = head_bench(dev, hbm_peak, args.ring_l2) if not args.no_head else None
     quant = quantize_bench(dev, hbm_peak) if not args.no_head else None
+    device_error = kvq8_device_error(reset=True)
 
     result = None
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
-            n_pairs = 24
             cpu_steps = 6
-            g_, sec_, thr_, desc_ = oracle_verify_sample(n_pairs, cpu_steps, 1)
-            g1, _, _, _ = oracle_verify_sample(4, 2, 0, threads=1)   # the one-thread figure
+            g_, sec_, thr_, desc_ = oracle_verify_sample(cpu_steps, 1, budget_s=15.0)
+            g1, _, _, desc1 = oracle_verify_sample(2, 0, budget_s=4.0, threads=1)   # the one-thread figure
             import oracle
             oracle.set_threads(thr_)
-            cpu = {"value": g_, "unit": "GB/s", "cores": thr_, "kind": "oracle",
-                   "sample": desc_ + f"; {cpu_steps} steps timed", "value_1thread": g1,
-                   "sample_1thread": "4 pairs per step, 2 steps, one OpenMP thread"}
+            cpu = {"value": g_, "unit": "GB/s", "cores": thr_, "kind": "oracle", "sample": desc_,
+                   "value_1thread": g1, "sample_1thread": desc1 + ", one OpenMP thread"}
+        # roofline of the dominant kernel (the split-context verify kernel): the step's K/V bytes
+        # over the split kernel's per-launch device time, both T together
+        split_us = {T: per_t[T]["split_us_per_launch"] for T in VERIFY_T}
         bytes_per_launch = kv_bytes_step / len(VERIFY_T)
-        achieved = bytes_per_launch / (us_per_call_verify * 1e-6) / 1e9
+        achieved = kv_bytes_step / (sum(split_us.values()) * 1e-6) / 1e9
         result = {
             "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "int8-kv, f16 hi+lo tensor-core, f32 accumulate", "data": "synthetic",
-            "config": {"workload": "verify-24q4kv-hd256-ctx4096-T4+T8-outliers", "model": None,
+            "dtype": "int8 K/V codes (Q8_0); QK fp16 hi+lo on tcgen05, PV fp16 hi+lo on mma.sync, f32 accumulate",
+            "data": "synthetic",
+            "config": {"workload": HEADLINE_WORKLOAD, "model": None,
                        "global_batch": world, "seq_len": ctx, "verify_rows": list(VERIFY_T),
                        "parallelism": f"replicas x{world}", "l2": f"ring of {n_ring} caches, "
                        f"{n_ring * cache_bytes / 2**20:.0f} MiB > 4x L2 (every step reads a different cache)",
@@ -486,28 +478,49 @@ def run_native(args, world, rank, local):
                                "cache by the verify kernel's window slice; scan over ctx+T); the two windows are "
                                "independent (each on its own cache of the ring) and run concurrently on two "
                                "streams, joined at the end of the step",
-                       "graph": f"{GRAPH_STEPS} steps per CUDA graph replay"},
-            "us_per_call": us_per_call_verify, "verify_only_gbs": verify_gbs,
-            "hbm_frac": verify_gbs / hbm_peak, "per_T": per_t,
+                       "graph": " + ".join(f"{r} x {g}-step graph" for g, r in timed_chunks) + " timed; "
+                                + " + ".join(f"{r} x {g}-step graph" for g, r in warm_chunks) + " warm-up"},
+            "us_per_call": sum(per_t[T]["us_per_call"] for T in VERIFY_T) / len(VERIFY_T),
+            "per_T": {f"T{T}": per_t[T] for T in VERIFY_T},
+            "cells": cells,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak,
-                         "traffic": _kernel_traffic(["verify.cu", "combine.cu"], "verify-24q4kv-hd256-ctx4096-T4+T8"),
-                         "peak_source": peak_src,
-                         "kernel": "attn_verify_q8 (verify_split_kernel + combine_kernel)",
-                         "algorithmic_bytes_per_launch": bytes_per_launch},
-            "long_context": long_ctx,
+                         "traffic": _kernel_traffic(["verify_tc.cu"], f"verify-24q4kv-hd256-ctx{ctx}-T4+T8"),
+                         "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, burst)",
+                         "kernel": "verify_tc_kernel (the split-context verify kernel, timed alone through "
+                                   "attn_verify_q8_partials over the same ring)",
+                         "algorithmic_bytes_per_launch": bytes_per_launch,
+                         "us_per_launch": {f"T{T}": split_us[T] for T in VERIFY_T}},
             "prompt": prompt,
             "verify_head": head,
             "quantize": quant,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "us_per_step": e2e_sec / e2e_steps * 1e6,
+                    "us_per_step": e2e_sec / e2e_steps * 1e6, "steps": e2e_steps,
                     "path": "attn_verify_append_q8_host (C ABI, pinned host buffers, arguments marshalled "
                             "once), eager, one call per T, the two T on two streams"},
             "clocks": clocks,
             "gpu_launches": launches_per_step * steps,
+            "device_error_flag": device_error,
         }
     return result
+
+
+def _cache_bytes(c) -> int:
+    return sum(t.numel() * t.element_size() for t in (c.k_codes, c.v_codes, c.k_scales, c.v_scales))
+
+
+def _verify_cell(w, ring, dev, hbm_peak) -> dict:
+    """Per-call device time of attn_verify_q8 on workload w over the ring, and of its split
+    kernel alone (attn_verify_q8_partials), each from a CUDA graph of at least 32 calls
+    replayed 10 times (median replay)."""
+    us = time_verify_cell(w, ring, dev)
+    split = time_verify_cell(w, ring, dev, partials=True)
+    n_calls = max(len(ring), 32)
+    gbs = w.kv_bytes() / (us * 1e-6) / 1e9
+    return {"workload": w.name, "us_per_call": us, "kv_gbs": gbs, "hbm_frac": gbs / hbm_peak,
+            "split_us_per_launch": split, "split_hbm_frac": w.kv_bytes() / (split * 1e-6) / 1e9 / hbm_peak,
+            "kv_bytes": w.kv_bytes(), "calls_timed": 10 * n_calls, "ring": len(ring)}
 
 
 def head_bench(dev, hbm_peak, ring_l2):
@@ -622,15 +635,17 @@ def prompt_bench(args, dev, fp16_peak, w=None, pool="q8"):
     ms = statistics.median(times)
     tf = w.causal_flops() / (ms * 1e-3) / 1e12
     return {"workload": w.name, "pool": pool, "ms_per_call": ms, "tflops": tf, "peak_tflops": fp16_peak,
-            "frac": tf / fp16_peak, "peak_source": "fp16 = measured bf16 x 0.951 (cuBLAS fp16/bf16 on GB300)",
+            "frac": tf / fp16_peak, "peak_source": "MEASURED_PEAKS.json bf16_tflops (cuBLAS bf16, burst); fp16 "
+            "and bf16 share one dense tensor-core rate", "dtype": "fp16 operands, single pass (q, K, P, V "
+            "each one fp16 value, not split hi+lo), f32 accumulate",
             "flops": w.causal_flops(), "calls_timed": n, "l2": "flushed (256 MiB write) before every call"}
 
 
-def _ring_for(w, dev, ring_l2):
+def _ring_for(w, dev, ring_l2, inp=None):
     import torch
 
     from speculative_verify_attention_gb300 import KVCacheQ8, workloads
-    inp = workloads.make_inputs(w)
+    inp = inp if inp is not None else workloads.make_inputs(w)
     base = KVCacheQ8(w.n_kv_heads, w.head_dim, w.kv_len, device=dev)
     base.append(torch.from_numpy(inp.k).to(dev), torch.from_numpy(inp.v).to(dev), 0)
     nbytes = sum(t.numel() * t.element_size() for t in (base.k_codes, base.v_codes, base.k_scales, base.v_scales))
@@ -706,15 +721,17 @@ def binary_tree_mask(T: int) -> np.ndarray:
     return np.array(masks, dtype=np.uint32)
 
 
-def time_verify_cell(w, ring, dev, reps=10, tree_mask=None):
-    """Device time per attn_verify_q8 call (attn_verify_tree_q8 when a window mask is given):
+def time_verify_cell(w, ring, dev, reps=10, tree_mask=None, partials=False):
+    """Device time per attn_verify_q8 call (attn_verify_tree_q8 when a window mask is given;
+    attn_verify_q8_partials, the split kernel alone, with partials=True):
     a CUDA graph of at least 32 calls walking the ring (total size > 4x L2, so K/V come from
     HBM; a one-cache ring gives the warm-L2 time) is replayed `reps` times, each replay timed
     with CUDA events; returns the median over the replays of microseconds per call."""
     import torch
 
     from speculative_verify_attention_gb300 import (KVCacheF16, KVCacheK8V4, attn_verify_f16, attn_verify_k8v4,
-                                                    attn_verify_q8, attn_verify_q8_workspace_bytes,
+                                                    attn_verify_q8, attn_verify_q8_partials,
+                                                    attn_verify_q8_partials_count, attn_verify_q8_workspace_bytes,
                                                     attn_verify_tree_q8, workloads)
     q = torch.from_numpy(workloads.make_inputs(w, kv_len=1).q).to(dev)
     out = torch.empty_like(q)
@@ -726,6 +743,13 @@ def time_verify_cell(w, ring, dev, reps=10, tree_mask=None):
     elif isinstance(ring[0], KVCacheK8V4):
         def call(c):
             attn_verify_k8v4(q, c, w.kv_len, w.q_pos0, w.softmax_scale, out=out, workspace=ws)
+    elif partials:
+        n = attn_verify_q8_partials_count(w.n_q, w.n_q_heads, w.head_dim, w.kv_len, w.n_kv_heads)
+        po = torch.empty((n, w.n_q * w.n_q_heads, w.head_dim), dtype=torch.float32, device=dev)
+        pml = torch.empty((n, w.n_q * w.n_q_heads, 2), dtype=torch.float32, device=dev)
+
+        def call(c):
+            attn_verify_q8_partials(q, c, w.kv_len, w.q_pos0, w.softmax_scale, part_o=po, part_ml=pml)
     elif tree_mask is not None:
         m = torch.from_numpy(np.ascontiguousarray(tree_mask, np.uint32).view(np.int32)).to(dev)
 
@@ -779,7 +803,7 @@ def sweep(args):
     cells += [(workloads.hd128_verify(t), "k8v4") for t in (4, 8)]
     cells = [c if isinstance(c, tuple) else (c, None) for c in cells]
     cells = [(w, kind) for w, kind in cells
-             if not args.sweep_filter or args.sweep_filter in (f"{kind}-{w.name}" if kind else w.name)]
+             if not args.sweep_filter or re.search(args.sweep_filter, f"{kind}-{w.name}" if kind else w.name)]
     key, ring = None, None
     for w, kind in cells:
         pool = kind if kind in ("f16", "k8v4") else "q8"
@@ -821,7 +845,8 @@ def main():
     ap.add_argument("--prompt-only", action="store_true", help="time only the prompt-chunk kernel")
     ap.add_argument("--oracle-sweep", action="store_true",
                     help="time the fp64 CPU oracle per configuration (host cores only, no GPU)")
-    ap.add_argument("--sweep-filter", default="")
+    ap.add_argument("--sweep-filter", default="", help="with --sweep: time only the cells whose name matches "
+                    "this regular expression")
     ap.add_argument("--prompt-filter", default="", help="with --prompt-only: time only the cells whose "
                     "'<pool>-<workload>' name contains this")
     args = ap.parse_args()
@@ -845,7 +870,7 @@ def main():
                         (_wl.PROMPT_HD128, "f16"), (_wl.PROMPT_HD128, "k8v4")):
             if args.prompt_filter and args.prompt_filter not in f"{pool}-{w.name}":
                 continue
-            print(json.dumps(prompt_bench(args, torch.device("cuda", 0), bf16_peak * 0.951, w, pool)), flush=True)
+            print(json.dumps(prompt_bench(args, torch.device("cuda", 0), bf16_peak, w, pool)), flush=True)
         return 0
     if args.impl == "reference":
         return run_reference(args, world, rank)

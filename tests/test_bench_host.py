@@ -53,3 +53,12 @@ def test_committed_traffic_capture_names_its_command_and_digest():
         assert entry["command"].startswith("python bench.py")
         assert len(entry["code_sha256"]) == 64
         assert entry["dram_bytes_per_launch"] == sum(k["dram_read"] + k["dram_write"] for k in entry["kernels"].values())
+
+
+def test_graph_chunks_cover_exactly_the_requested_steps():
+    for n in [1, 2, 3, 5, 20, 63, 64, 65, 100, 127, 128, 129, 2048, 2049]:
+        chunks = bench.graph_chunks(n)
+        assert sum(g * r for g, r in chunks) == n
+        assert all(1 <= g <= bench.GRAPH_MAX and r >= 1 for g, r in chunks)
+        assert len(chunks) <= 2
+    assert bench.graph_chunks(0) == []
