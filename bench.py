@@ -8,7 +8,7 @@ workload (24 q heads / 4 kv heads, head_dim 256, context 20,676): for each windo
 T in {4, 8}, one attn_verify_append_q8 call appends the T new K/V tokens to the Q8_0 cache
 and runs the verify scan over ctx + T keys: the split-context kernel, whose window slice
 quantises the new tokens itself, and the log-sum-exp combine.  The two windows are
-independent problems (each on its own cache) and run on two streams.
+independent problems (each on its own cache), run back to back on one stream.
 `value` is the KV-scan bandwidth of the whole job (Q8_0 K/V bytes read by the verify
 calls / time), in GB/s; `per_T` gives the per-call latency of each window length, `cells`
 the same figures at contexts 32,768 and 4,096.  The prompt-chunk kernel (12 q heads /
@@ -321,21 +321,15 @@ def run_native(args, world, rank, local):
                           dtype=torch.uint8, device=dev) for T in VERIFY_T}
     kv_bytes_step = sum(ws_[T].kv_bytes() for T in VERIFY_T)
 
-    side = [torch.cuda.Stream(device=dev) for _ in VERIFY_T]
-
     def step(s):
-        # the step's windows are independent problems (their own caches of the ring), each on a
-        # stream of its own, as two sequences' verify calls would be; each call appends its
-        # window's K/V to the cache (fused into the verify kernel) and scans ctx + T keys
-        cur = torch.cuda.current_stream()
+        # the step's windows are independent problems (their own caches of the ring), run back to
+        # back on one stream (measured a little faster than two streams: each call's split kernel
+        # fills every SM, and the next call's prologue overlaps the merge kernel before it); each
+        # call appends its window's K/V to the cache (fused into the verify kernel) and scans
+        # ctx + T keys
         for j, T in enumerate(VERIFY_T):
             c = ring[(s + j * (n_ring // len(VERIFY_T))) % n_ring]
-            side[j].wait_stream(cur)
-            with torch.cuda.stream(side[j]):
-                attn_verify_append_q8(q[T], knew[T], vnew[T], c, ctx, w0.softmax_scale, out=out[T],
-                                      workspace=wsb[T])
-        for st in side:
-            cur.wait_stream(st)
+            attn_verify_append_q8(q[T], knew[T], vnew[T], c, ctx, w0.softmax_scale, out=out[T], workspace=wsb[T])
 
     launches_per_step = len(VERIFY_T) * 2   # verify split (with the append) + combine per T
 
@@ -476,8 +470,7 @@ def run_native(args, world, rank, local):
                        f"{n_ring * cache_bytes / 2**20:.0f} MiB > 4x L2 (every step reads a different cache)",
                        "step": "per T in {4,8}: attn_verify_append_q8 (K/V of T new tokens quantised into the "
                                "cache by the verify kernel's window slice; scan over ctx+T); the two windows are "
-                               "independent (each on its own cache of the ring) and run concurrently on two "
-                               "streams, joined at the end of the step",
+                               "independent (each on its own cache of the ring), back to back on one stream",
                        "graph": " + ".join(f"{r} x {g}-step graph" for g, r in timed_chunks) + " timed; "
                                 + " + ".join(f"{r} x {g}-step graph" for g, r in warm_chunks) + " warm-up"},
             "us_per_call": sum(per_t[T]["us_per_call"] for T in VERIFY_T) / len(VERIFY_T),

@@ -53,6 +53,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float4* 
     const float4* src = part_o + (int64_t)row * hd4 + c;
     // launched as a programmatic dependent of the split kernel: wait until its partials are complete
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the next call's split kernel may start its prologue now: every kernel before this one has
+    // completed, and it writes no partials before its own wait for this grid
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     float4 o[kPrefetch];
 #pragma unroll
@@ -136,6 +139,7 @@ __global__ void __launch_bounds__(kWideThreads) combine_wide_kernel(const float4
                                                                     int n_split, int rows, int hd4,
                                                                     float* __restrict__ out) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int per_row = hd4 / kWideVec;
     const int64_t item = (int64_t)blockIdx.x * kWideThreads + threadIdx.x;
     if (item >= (int64_t)rows * per_row) return;

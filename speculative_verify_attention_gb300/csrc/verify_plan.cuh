@@ -67,6 +67,8 @@ inline int make_plan(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_
         if (sms <= 0) sms = 152;
         const int per_sm = blocks_per_sm(head_dim, pl->nt);
         ns = std::max(1, (per_sm * sms) / (n_kv_heads * pl->n_chunks));
+        // the window slice takes one of the blocks' places, so that the grid stays one wave
+        if (window_keys > 0) ns = std::max(1, ns - 1);
     }
     ns = std::max(1, std::min(ns, n_units));
     // an automatic slice holds at least one whole 128-key tile; every slice is at least as

@@ -85,7 +85,7 @@ struct TcLayout {
     static constexpr int VIS = LRED + 4 * RP * 4;
     static constexpr int BARS = (VIS + RP * 4 + 7) / 8 * 8;
     enum { KF = 0, KE = 2, VF = 4, VE = VF + kVSlots, PF = VE + kVSlots, PE = PF + 2, GO = PE + 2, QKD = GO + 1,
-           NBARS = QKD + 1 };
+           VGO = QKD + 1, NBARS = VGO + 1 };
     static constexpr int KH = GO;               // K^ of the tile written (the fold warps)
     static constexpr int SLOT = BARS + NBARS * 8;
     static constexpr int BYTES = SLOT + 16;
@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
         }
         tc::mbar_init(bar(L::KH), 8);   // K^ of the tile written (and the previous accumulators read)
         tc::mbar_init(bar(L::QKD), 1);
+        tc::mbar_init(bar(L::VGO), 1);  // K tile 0 has landed: the other stages may go out
         tc::mbar_init_fence();
     }
     if (warp == kMmaWarp) tc::tmem_alloc(smem_u32(tmem_slot), L::TM_COLS);
@@ -235,13 +236,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
         cp_async_arrive(full);
     };
     const int n_halves = (kKT / kVKeys) * n_tiles;  // V units
-    // the first two tiles of each plane go out before the q rows are staged (the window slice of
-    // the append path first writes its tokens into the cache, below)
-    if (producer && !window) {
-        const bool vplane = warp == kVProdWarp;
-        const int first = vplane ? min(n_halves, kVSlots) : min(n_tiles, 2);
-        for (int t = 0; t < first; ++t) load_stage(vplane, t);
-    }
+    // K tile 0 goes out first and alone, before the q rows are staged, so that it reaches every
+    // block ahead of the other stages' bytes (all blocks start at once); the other first stages
+    // follow once it has landed.  The window slice of the append path first writes its tokens
+    // into the cache, below.
+    if (warp == kKProdWarp && !window && n_tiles > 0) load_stage(false, 0);
+    // Launched as a programmatic dependent: the kernel before this one in the stream may still be
+    // running (the previous call's merge kernel).  Reading K tile 0 before this wait is safe: no
+    // kernel of the library that lets a dependent start early writes the cache.  Everything else
+    // (q, the window tokens' cache writes, the partials) comes after it.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (!producer) {
         const int wtid = threadIdx.x - (warp > kVProdWarp ? 64 : 0);  // 0 .. kWorkThreads - 1
@@ -324,11 +328,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
         const bool vplane = warp == kVProdWarp;
         const int slots = vplane ? kVSlots : 2;        // ring depth
         const int total = vplane ? n_halves : n_tiles;  // loads of this plane
-        int issued = min(total, slots);
-        if (window)
-            for (int t = 0; t < issued; ++t) load_stage(vplane, t);
-        const uint32_t empty0 = bar(vplane ? L::VE : L::KE);
+        const int issued0 = min(total, slots);
+        int issued = issued0;
         bool ok = true;
+        if (!vplane) {
+            if (window && n_tiles > 0) load_stage(false, 0);
+            // this warp alone refills slot 0, so the slot cannot run a phase ahead of this wait
+            if (n_tiles > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(L::KF), 0, kTcWait));
+            for (int t = 1; t < issued0; ++t) load_stage(false, t);
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bar(L::VGO));
+        } else {
+            ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(L::VGO), 0, kTcWait));
+            for (int t = 0; t < issued0; ++t) load_stage(true, t);
+        }
+        if (!ok && lane == 0) flag_timeout(p.err);
+        ok = true;
+        const uint32_t empty0 = bar(vplane ? L::VE : L::KE);
         for (int t = 0; t + slots < total; ++t) {  // load t + slots into the slot load t leaves
             ok = __all_sync(0xffffffffu, tc::mbar_wait(empty0 + 8u * (uint32_t)(t % slots), (t / slots) & 1, kTcWait));
             if (!ok) break;
@@ -750,8 +766,17 @@ int launch_tc(const VerifyTcParams& vp, dim3 grid, cudaStream_t s) {
     using L = TcLayout<HD, RP>;
     static SmemOptIn opt;
     if (opt.ensure(verify_tc_kernel<HD, RP, APPEND>, L::BYTES) != KVQ8_OK) return KVQ8_ERR_CUDA;
-    verify_tc_kernel<HD, RP, APPEND><<<grid, kTcThreads, L::BYTES, s>>>(vp);
-    return launch_status();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = L::BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, verify_tc_kernel<HD, RP, APPEND>, vp) == cudaSuccess ? KVQ8_OK : KVQ8_ERR_CUDA;
 }
 
 template <int HD, bool APPEND>

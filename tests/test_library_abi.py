@@ -27,3 +27,24 @@ def test_library_exports_every_declared_symbol():
     lib.kvq8_status_str.restype = ctypes.c_char_p
     assert lib.kvq8_status_str(0) == b"ok"
     assert lib.kvq8_status_str(4) == b"workspace missing or too small"
+
+
+def test_automatic_plans_fill_one_wave_of_a_152_sm_part():
+    """The automatic split count keeps the verify grid (slices x row chunks x KV heads) within one
+    block per SM, the append path's window slice included; derived from the workspace size
+    (n_split x rows x (head_dim + 2) x 4 bytes), with no GPU present (the planner assumes 152
+    SMs then)."""
+    lib = ctypes.CDLL(build.build())
+    for fn in (lib.attn_verify_append_q8_workspace_bytes, lib.attn_verify_q8_workspace_bytes):
+        fn.restype = ctypes.c_size_t
+    hq, hkv, hd = 24, 4, 256
+    for ctx in (512, 4096, 20676, 32768):
+        for T in (1, 2, 4, 8, 16, 24, 32):
+            rows = T * hq
+            chunks = -(-T * (hq // hkv) // 24)
+            ws = lib.attn_verify_append_q8_workspace_bytes(T, hq, hd, ctx, hkv, 0)
+            assert ws % (rows * (hd + 2) * 4) == 0
+            n_split = ws // (rows * (hd + 2) * 4)
+            assert 2 <= n_split and n_split * chunks * hkv <= 152, (ctx, T, n_split)
+            if ctx >= 20676:   # long enough for every slice to hold whole 128-key tiles and fill the SMs
+                assert (n_split + 1) * chunks * hkv > 152 - chunks * hkv, (ctx, T, n_split)
