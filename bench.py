@@ -47,6 +47,7 @@ HEADLINE_CTX = 20676            # the context the pages' verify speedups are quo
 EXTRA_CTX = (32768, 4096)       # the largest context, and the 27B-class context with outliers
 GRAPH_MAX = 64                  # steps per CUDA graph at most
 HEADLINE_WORKLOAD = f"verify-24q4kv-hd256-ctx{HEADLINE_CTX}-T4+T8"
+TC_KERNEL_FILES = ["verify_tc.cu", "verify_plan.cuh", "tc.cuh"]   # the code a traffic capture covers
 
 
 def graph_chunks(n: int, g_max: int = GRAPH_MAX) -> list[tuple[int, int]]:
@@ -478,7 +479,7 @@ def run_native(args, world, rank, local):
             "cells": cells,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak,
-                         "traffic": _kernel_traffic(["verify_tc.cu"], f"verify-24q4kv-hd256-ctx{ctx}-T4+T8"),
+                         "traffic": _kernel_traffic(TC_KERNEL_FILES, f"verify-24q4kv-hd256-ctx{ctx}-T4+T8"),
                          "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, burst)",
                          "kernel": "verify_tc_kernel (the split-context verify kernel, timed alone through "
                                    "attn_verify_q8_partials over the same ring)",

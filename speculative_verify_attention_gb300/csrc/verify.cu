@@ -1,5 +1,5 @@
 // verify.cu -- the verify entry points (attn_verify_q8 and its variants) and the all-mma.sync
-// split-context scan used for tree-shaped windows and K8V4 pools.
+// split-context scan used for tree-shaped windows, K8V4 pools and short causal scans.
 //
 // Source: "perf(gfx1100): share Q8 KV scans across verifier rows", Summary: one worker owns
 // all the query rows of a verify window and shares each K/V scan across them; the context
@@ -9,7 +9,9 @@
 //
 // Routing: causal windows over a Q8_0 cache (attn_verify_q8, attn_verify_q8_partials,
 // attn_verify_append_q8 and the host-buffer and no-allocation entries built on them) run the
-// tcgen05 scan of verify_tc.cu; tree-shaped windows and K8V4 pools run the kernel below.
+// tcgen05 scan of verify_tc.cu, except short scans (fewer than two 128-key tiles per block, or
+// hd128 chunks of <= 32 rows; see plan_causal) outside the append path, which run the kernel
+// below; tree-shaped windows and K8V4 pools always run the kernel below.
 //
 // The kernel below (one thread block of 8 warps per (row chunk, context slice, KV head); the
 // chunks and slices come from verify_plan.cuh):
@@ -706,6 +708,23 @@ inline int plan_mma(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_k
     return make_plan(n_rows, n_q_heads, head_dim, kv_len, n_kv_heads, n_split, pl);
 }
 
+// Plan of a causal window over a Q8_0 cache, and which kernel runs it.  The tcgen05 kernel has
+// the longer pipeline fill: it runs a window when each of its blocks gets at least two 128-key
+// tiles and the chunk is large enough to keep its roles busy (hd256, or more than 32 rows per
+// KV head at hd128); otherwise the all-mma.sync kernel does (measured on GB300, 24q/4kv/hd256:
+// ctx 4096 T = 4 9.9 vs 10.3 us; 32q/8kv/hd128 ctx 8192 T = 4 12.5 vs 13.2 us).  The append
+// path always takes the tcgen05 kernel (its window slice lives there).  Every entry point that
+// sizes or launches a causal scan goes through here, so counts and launches agree.
+inline int plan_causal(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_kv_heads, int n_split, Plan* pl,
+                       bool* use_tc, int window_keys = 0) {
+    const int rc = plan_tc(n_rows, n_q_heads, head_dim, kv_len, n_kv_heads, n_split, pl, window_keys);
+    if (rc != KVQ8_OK) return rc;
+    const int rows_per_kv_head = n_rows * (n_q_heads / n_kv_heads);
+    const int tiles = (std::min(pl->keys_per_split, kv_len) + kKT - 1) / kKT;
+    *use_tc = window_keys > 0 || (tiles >= 2 && (head_dim == 256 || rows_per_kv_head > 32));
+    return *use_tc ? KVQ8_OK : plan_mma(n_rows, n_q_heads, head_dim, kv_len, n_kv_heads, n_split, pl);
+}
+
 }  // namespace kvq8
 
 // The one workspace size that serves attn_verify_q8, attn_verify_tree_q8 and attn_verify_k8v4.
@@ -739,11 +758,14 @@ int verify_impl(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv,
     if (!(softmax_scale == softmax_scale) || softmax_scale == INFINITY || softmax_scale == -INFINITY)
         return KVQ8_ERR_INVALID_ARG;
     if (append && (!v_new || kv_len != q_pos0 + n_rows)) return KVQ8_ERR_INVALID_ARG;
-    const bool tc = !v4 && !wmask;  // causal windows over a Q8_0 cache: the tcgen05 kernel
+    // causal windows over a Q8_0 cache: the kernel plan_causal picks; tree windows and K8V4
+    // pools: the all-mma.sync kernel
+    bool tc = false;
     Plan pl;
-    const int rc = tc ? plan_tc(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, n_split, &pl,
-                                append ? n_rows : 0)
-                      : plan_mma(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, n_split, &pl);
+    const int rc = (!v4 && !wmask)
+                       ? plan_causal(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, n_split, &pl, &tc,
+                                     append ? n_rows : 0)
+                       : plan_mma(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, n_split, &pl);
     if (rc != KVQ8_OK) return rc;
     if (!aligned16(q) || !aligned16(kv->k_codes) || !aligned16(kv->k_scales) || !aligned16(kv->v_codes) ||
         !aligned16(kv->v_scales))
@@ -814,6 +836,9 @@ int verify_impl(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv,
     else if (wmask)  // tree windows have no append variant
         r1 = pl.hd == 128 ? dispatch_nt<128, true>(vp, pl, kv->n_kv_heads, s)
                           : dispatch_nt<256, true>(vp, pl, kv->n_kv_heads, s);
+    else if (!append)  // short causal scans (plan_causal)
+        r1 = pl.hd == 128 ? dispatch_nt<128, false>(vp, pl, kv->n_kv_heads, s)
+                          : dispatch_nt<256, false>(vp, pl, kv->n_kv_heads, s);
     else
         return KVQ8_ERR_UNSUPPORTED;
     if (r1 != KVQ8_OK || partials) return r1;
@@ -845,7 +870,8 @@ extern "C" int attn_verify_k8v4(const float* q, int n_rows, int n_q_heads, const
 extern "C" int attn_verify_q8_partials_count(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_kv_heads,
                                              int n_split) {
     kvq8::Plan pl;
-    if (kvq8::plan_tc(n_rows, n_q_heads, head_dim, kv_len, n_kv_heads, n_split, &pl) != KVQ8_OK) return 0;
+    bool tc = false;
+    if (kvq8::plan_causal(n_rows, n_q_heads, head_dim, kv_len, n_kv_heads, n_split, &pl, &tc) != KVQ8_OK) return 0;
     return pl.n_split;
 }
 
@@ -1030,7 +1056,8 @@ extern "C" int attn_verify_q8_noalloc(const float* q, int n_rows, int n_q_heads,
     using namespace kvq8;
     if (!kv) return KVQ8_ERR_INVALID_ARG;
     Plan pl;
-    const int rc = plan_tc(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, n_split, &pl);
+    bool tc = false;
+    const int rc = plan_causal(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, n_split, &pl, &tc);
     if (rc != KVQ8_OK) return rc;
     // the partials of this plan must fit the array; nothing is launched otherwise
     if (pl.ws_bytes > (size_t)KVQ8_NOALLOC_SCRATCH_BYTES) return KVQ8_ERR_WORKSPACE;

@@ -18,6 +18,16 @@ def rel_err(got, ref) -> float:
     return float(np.max(np.abs(got - ref)) / (den if den > 0 else 1.0))
 
 
+def report_err(name: str, got, ref) -> float:
+    """rel_err, printed with the output scale it is relative to (max |oracle|) and the largest
+    absolute difference, so that a run with -s records the error each workload reaches."""
+    err = rel_err(got, ref)
+    scale = float(np.max(np.abs(np.asarray(ref, dtype=np.float64))))
+    print(f"\nACHIEVED {name}: max|gpu - oracle| / max|oracle| = {err:.3e}, max|oracle| = {scale:.4g}, "
+          f"max|gpu - oracle| = {err * scale:.3e}")
+    return err
+
+
 def build_caches(inp: workloads.Inputs, capacity: int | None = None, pos0: int = 0, garbage_tail: bool = True):
     """Quantise inp.k / inp.v at positions pos0.. into a library cache (on the GPU) and an
     oracle cache (on the CPU).  Positions outside the written range hold junk bytes in both,

@@ -52,7 +52,20 @@ def test_committed_traffic_capture_names_its_command_and_digest():
     for entry in t.values():
         assert entry["command"].startswith("python bench.py")
         assert len(entry["code_sha256"]) == 64
-        assert entry["dram_bytes_per_launch"] == sum(k["dram_read"] + k["dram_write"] for k in entry["kernels"].values())
+        total = sum(k["dram_read"] + k["dram_write"] for k in entry["kernels"].values())
+        assert entry["dram_bytes_per_launch"] == total / entry.get("launches_averaged", 1)
+
+
+def test_committed_traffic_capture_is_used_only_for_the_code_it_measured():
+    """The bench's roofline reports the committed capture while the kernel's code is the code the
+    capture measured, and null (stale counters) once it has changed."""
+    import json
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        t = json.load(f)
+    entry = t[bench.HEADLINE_WORKLOAD]
+    fresh = entry["code_sha256"] == bench.kernel_source_digest(bench.TC_KERNEL_FILES)
+    got = bench._kernel_traffic(bench.TC_KERNEL_FILES, bench.HEADLINE_WORKLOAD)
+    assert got == (entry["dram_bytes_per_launch"] if fresh else None)
 
 
 def test_graph_chunks_cover_exactly_the_requested_steps():

@@ -5,7 +5,7 @@ import pytest
 import oracle
 from speculative_verify_attention_gb300 import workloads
 
-from ._util import PROMPT_TOL, build_caches, rel_err
+from ._util import PROMPT_TOL, build_caches, rel_err, report_err
 
 pytestmark = pytest.mark.gpu
 
@@ -90,7 +90,7 @@ def test_full_prompt_workload_sampled(lib):
     sel = [(int(i), int(rng.integers(w.n_q_heads))) for i in rng.integers(0, w.n_q, 40)]
     sel += [(0, h) for h in range(w.n_q_heads)] + [(w.n_q - 1, h) for h in range(w.n_q_heads)]
     ref = oracle.attention(orc, inp.q, w.kv_len, w.q_pos0, w.softmax_scale, sel=sel)
-    err = rel_err(np.stack([got[i, h] for i, h in sel]), ref)
+    err = report_err(w.name, np.stack([got[i, h] for i, h in sel]), ref)
     assert np.all(np.isfinite(got))
     assert err <= PROMPT_TOL, f"rel err {err:.3e}"
     from speculative_verify_attention_gb300 import kvq8_device_error
@@ -124,7 +124,7 @@ def test_full_hd128_prompt_workload_sampled(lib):
     sel = [(int(i), int(rng.integers(w.n_q_heads))) for i in rng.integers(0, w.n_q, 40)]
     sel += [(0, h) for h in range(w.n_q_heads)] + [(w.n_q - 1, h) for h in range(w.n_q_heads)]
     ref = oracle.attention(orc, inp.q, w.kv_len, w.q_pos0, w.softmax_scale, sel=sel)
-    err = rel_err(np.stack([got[i, h] for i, h in sel]), ref)
+    err = report_err(w.name, np.stack([got[i, h] for i, h in sel]), ref)
     assert np.all(np.isfinite(got))
     assert err <= PROMPT_TOL, f"rel err {err:.3e}"
     from speculative_verify_attention_gb300 import kvq8_device_error

@@ -5,7 +5,7 @@ import pytest
 import oracle
 from speculative_verify_attention_gb300 import workloads
 
-from ._util import VERIFY_TOL, build_caches, planes_equal, rel_err
+from ._util import VERIFY_TOL, build_caches, planes_equal, rel_err, report_err
 
 pytestmark = pytest.mark.gpu
 
@@ -26,7 +26,7 @@ def _check_full(w: workloads.Workload, n_split=0):
     assert planes_equal(gpu, orc)
     got = _run(gpu, inp.q, w.kv_len, w.q_pos0, w.softmax_scale, n_split)
     ref = oracle.attention(orc, inp.q, w.kv_len, w.q_pos0, w.softmax_scale)
-    err = rel_err(got, ref)
+    err = report_err(w.name, got, ref)
     assert err <= VERIFY_TOL, f"{w.name}: rel err {err:.3e}"
     return err
 
@@ -42,7 +42,7 @@ def _check_sampled(w: workloads.Workload, n_pairs=24, seed=0):
     sel = sel[: max(n_pairs, w.n_q)]
     ref = oracle.attention(orc, inp.q, w.kv_len, w.q_pos0, w.softmax_scale, sel=sel)
     g = np.stack([got[i, h] for i, h in sel])
-    err = rel_err(g, ref)
+    err = report_err(w.name, g, ref)
     assert err <= VERIFY_TOL, f"{w.name}: rel err {err:.3e}"
     assert np.all(np.isfinite(got))
     return err
