@@ -830,7 +830,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=64)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--ring-l2", type=float, default=4.2, help="ring size in multiples of the L2")
-    ap.add_argument("--prompt-steps", type=int, default=10)
+    ap.add_argument("--prompt-steps", type=int, default=20)
     ap.add_argument("--no-prompt", action="store_true")
     ap.add_argument("--no-head", action="store_true", help="skip the verify-head (argmax / top probability) timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -160,19 +160,27 @@ __device__ int cta_segments(const PromptParams& p, int c, int G, Segment* seg) {
 
 __device__ __forceinline__ void flag_timeout() { atomicOr(&g_kvq8_device_error, 1u); }
 
-// Convert one 64-key plane tile (codes + scales in staging) into the swizzled fp16 tile:
+// Convert one plane tile (codes + scales in staging) into the swizzled fp16 tile:
 // element (key n, dim j) -> atom j/64, row n, 16-byte chunk ((j%64)/8) ^ (n%8).
 // kDeqThreads threads share the tile's kChunks chunks of 16 codes (HD/16 chunks per key).
+// Chunk order: every 8 consecutive chunks (a quarter warp's 16-byte accesses) are the 4 chunks
+// of one 64-dim atom of key 2m and the 4 chunks of the neighbouring atom of key 2m + 1.  Their
+// code loads then fill the 32 banks once (the two keys' 64-byte runs sit 128 bytes apart modulo
+// the 128-byte bank line), and so do their swizzled stores (key 2m's chunks land on even chunk
+// slots, key 2m + 1's on odd ones): neither side has a bank conflict.
 template <int HD>
 __device__ __forceinline__ void dequant_tile(const uint8_t* codes, const uint16_t* scales, uint8_t* hat, int nk,
                                              int d) {
     constexpr int kChunks = PL<HD>::kChunks;
-    constexpr int CPK = HD / 16;
+    constexpr int NAP = HD / 128;  // atom pairs per key
 #pragma unroll
     for (int k = 0; k < (kChunks + kDeqThreads - 1) / kDeqThreads; ++k) {
         const int c = d + kDeqThreads * k;
         if (c >= kChunks) break;
-        const int n = c / CPK, j16 = c % CPK;
+        // c = ((m * NAP + ap) * 2 + sw) * 8 + kp * 4 + jj: key 2m + kp, atom 2 ap + (sw ^ kp), chunk jj
+        const int jj = c & 3, kp = (c >> 2) & 1, sw = (c >> 3) & 1;
+        const int rest = c >> 4, ap = rest % NAP, m = rest / NAP;
+        const int n = 2 * m + kp, j16 = 4 * (2 * ap + (sw ^ kp)) + jj;
         uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
         if (n < nk) {
             const uint4 raw = *reinterpret_cast<const uint4*>(codes + n * HD + j16 * 16);
