@@ -160,27 +160,38 @@ __device__ int cta_segments(const PromptParams& p, int c, int G, Segment* seg) {
 
 __device__ __forceinline__ void flag_timeout() { atomicOr(&g_kvq8_device_error, 1u); }
 
+// The order in which the dequantisers take a tile's 16-dim chunks (one chunk: 16 codes of one
+// key, written as two 16-byte swizzled pieces):
+//   c = ((m * 2 + sw) * NAP + ap) * 8 + kp * 4 + jj  ->  key 2m + kp, atom 2 ap + (sw ^ kp), chunk jj
+// (NAP = HD / 128 atom pairs).  A quarter warp (8 consecutive chunks) thus holds the 4 chunks of
+// one 64-dim atom of key 2m and the 4 chunks of the neighbouring atom of key 2m + 1: its swizzled
+// stores cover the 32 banks once (key 2m lands on even chunk slots, key 2m + 1 on odd ones), and
+// so do its 16-byte code loads (the two keys' 64-byte runs sit 128 bytes apart modulo the bank
+// line).  A half warp holds key 2m's atoms {sw, sw + 2} and key 2m + 1's other two, so the 8-byte
+// loads of 4-bit codes (two pieces of 32 bytes per key) fill distinct banks as well.
+template <int HD>
+__device__ __forceinline__ void chunk_of(int c, int& n, int& j16) {
+    constexpr int NAP = HD / 128;
+    const int jj = c & 3, kp = (c >> 2) & 1, ap = (c >> 3) % NAP;
+    const int rest = (c >> 3) / NAP, sw = rest & 1, m = rest >> 1;
+    n = 2 * m + kp;
+    j16 = 4 * (2 * ap + (sw ^ kp)) + jj;
+}
+
 // Convert one plane tile (codes + scales in staging) into the swizzled fp16 tile:
 // element (key n, dim j) -> atom j/64, row n, 16-byte chunk ((j%64)/8) ^ (n%8).
-// kDeqThreads threads share the tile's kChunks chunks of 16 codes (HD/16 chunks per key).
-// Chunk order: every 8 consecutive chunks (a quarter warp's 16-byte accesses) are the 4 chunks
-// of one 64-dim atom of key 2m and the 4 chunks of the neighbouring atom of key 2m + 1.  Their
-// code loads then fill the 32 banks once (the two keys' 64-byte runs sit 128 bytes apart modulo
-// the 128-byte bank line), and so do their swizzled stores (key 2m's chunks land on even chunk
-// slots, key 2m + 1's on odd ones): neither side has a bank conflict.
+// kDeqThreads threads share the tile's kChunks chunks of 16 codes (HD/16 chunks per key), in
+// the chunk_of order.
 template <int HD>
 __device__ __forceinline__ void dequant_tile(const uint8_t* codes, const uint16_t* scales, uint8_t* hat, int nk,
                                              int d) {
     constexpr int kChunks = PL<HD>::kChunks;
-    constexpr int NAP = HD / 128;  // atom pairs per key
 #pragma unroll
     for (int k = 0; k < (kChunks + kDeqThreads - 1) / kDeqThreads; ++k) {
         const int c = d + kDeqThreads * k;
         if (c >= kChunks) break;
-        // c = ((m * NAP + ap) * 2 + sw) * 8 + kp * 4 + jj: key 2m + kp, atom 2 ap + (sw ^ kp), chunk jj
-        const int jj = c & 3, kp = (c >> 2) & 1, sw = (c >> 3) & 1;
-        const int rest = c >> 4, ap = rest % NAP, m = rest / NAP;
-        const int n = 2 * m + kp, j16 = 4 * (2 * ap + (sw ^ kp)) + jj;
+        int n, j16;
+        chunk_of<HD>(c, n, j16);
         uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
         if (n < nk) {
             const uint4 raw = *reinterpret_cast<const uint4*>(codes + n * HD + j16 * 16);
@@ -210,16 +221,17 @@ __device__ __forceinline__ void dequant_tile(const uint8_t* codes, const uint16_
 // The 4-bit V tile of a K8V4 pool (HD/2 bytes per key, element 2m in the low nibble of byte
 // m, value (nibble - 8) * scale) into the same swizzled fp16 tile: each byte becomes its two
 // codes exactly (nib_byte_to_half2), and one multiply by the scale rounds once, as for Q8_0.
+// Chunks in the chunk_of order.
 template <int HD>
 __device__ __forceinline__ void dequant_tile_v4(const uint8_t* codes, const uint16_t* scales, uint8_t* hat, int nk,
                                                 int d) {
     constexpr int kChunks = PL<HD>::kChunks;  // 16-dim items per tile
-    constexpr int CPK = HD / 16;
 #pragma unroll
     for (int k = 0; k < (kChunks + kDeqThreads - 1) / kDeqThreads; ++k) {
         const int c = d + kDeqThreads * k;
         if (c >= kChunks) break;
-        const int n = c / CPK, j16 = c % CPK;
+        int n, j16;
+        chunk_of<HD>(c, n, j16);
         uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
         if (n < nk) {
             const uint2 raw = *reinterpret_cast<const uint2*>(codes + n * (HD / 2) + j16 * 8);
