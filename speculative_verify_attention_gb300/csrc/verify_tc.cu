@@ -195,7 +195,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
         }
         for (int s = 0; s < kVSlots; ++s) {
             tc::mbar_init(bar(L::VF + s), 33);
-            tc::mbar_init(bar(L::VE + s), 8);   // the PV warps
         }
         tc::mbar_init(bar(L::KH), 8);   // K^ of the tile written (and the previous accumulators read)
         tc::mbar_init(bar(L::QKD), 1);
@@ -344,7 +343,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
         }
         if (!ok && lane == 0) flag_timeout(p.err);
         ok = true;
-        const uint32_t empty0 = bar(vplane ? L::VE : L::KE);
+        // a V slot (one tile) is free when the PV warps release that tile's P buffer
+        static_assert(kVKeys == kKT && kVSlots == 2, "one V slot per tile, paired with the P buffers");
+        const uint32_t empty0 = bar(vplane ? L::PE : L::KE);
         for (int t = 0; t + slots < total; ++t) {  // load t + slots into the slot load t leaves
             ok = __all_sync(0xffffffffu, tc::mbar_wait(empty0 + 8u * (uint32_t)(t % slots), (t / slots) & 1, kTcWait));
             if (!ok) break;
@@ -534,6 +535,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
                     hdr[4 + h * RPH + lane] = av;
                 }
                 if (fw == 0 && lane == 0) *reinterpret_cast<int*>(hdr) = need ? 1 : 0;
+                // fold warp 0 publishes P(t-1) only once V(t-1) has landed, so that the PV warps
+                // wait on one barrier per tile; the V slot cannot run a phase ahead of this wait
+                // (it is refilled only after the PV warps have released tile t-1).  Lane 0, the
+                // one that arrives, waits itself.
+                if (fw == 0 && lane == 0 && ok)
+                    ok = tc::mbar_wait(bar(L::VF + (t - 1) % kVSlots), ((t - 1) / kVSlots) & 1, kTcWait);
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(bar(L::PF + pb));
             }
@@ -610,10 +617,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
             for (int hh = 0; hh < kKT / kVKeys; ++hh) {
                 const int hv = (kKT / kVKeys) * t + hh;  // V unit
                 const int slot = hv % kVSlots;
-                if (!__all_sync(0xffffffffu, tc::mbar_wait(bar(L::VF + slot), (hv / kVSlots) & 1, kTcWait))) {
-                    ok = false;
-                    break;
-                }
+                // the tile's V codes have landed: fold warp 0 saw VF before it published P
                 const uint8_t* vst = smem + L::VST + slot * L::HSTAGE;
                 const uint16_t* sVs = reinterpret_cast<const uint16_t*>(vst + L::HCODES);
                 const int nkh = min(max(nk - L::HKEYS * hh, 0), L::HKEYS);  // the slice's keys in this half
@@ -709,11 +713,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
                     pv_step(2 * u4);
                     pv_step(2 * u4 + 1);
                 }
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(bar(L::VE + slot));
             }
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(bar(L::PE + b));
+            if (lane == 0) tc::mbar_arrive(bar(L::PE + b));  // P buffer and V slot of tile t free
         }
         if (!ok && lane == 0) flag_timeout(p.err);
         // ---- the slice partial: O is (p 2^4)(v 2^E) summed; lane owns dims 32 pvb + 4g .. +3
