@@ -9,17 +9,22 @@
 // folded into p.
 //
 // GB300 design.  One thread block (one per SM) per (row chunk of <= 24 (row, q-head) pairs,
-// context slice, KV head); 18 warps with fixed roles, coupled by mbarriers:
-//   warp 16      producer: 128-key tiles of int8 codes by tensor copies (128-byte swizzle, keys
-//                past kv_len read as zeros) into 2-stage K and V rings, the fp16 block scales by
-//                16/8-byte async copies that arrive on the same barrier;
-//   warp 17      tensor-memory owner and MMA issuer (one thread);
+// context slice, KV head); 19 warps with fixed roles, coupled by mbarriers:
+//   warp 16      K producer: 128-key tiles of int8 codes by tensor copies (128-byte swizzle, keys
+//                past kv_len read as zeros) into a 2-stage ring, the fp16 block scales by 16/8-byte
+//                async copies that arrive on the same barrier.  Tile 0 goes out first and alone;
+//   warp 17      V producer: the same for V, starting once K tile 0 has landed; a V slot is
+//                refilled when the PV warps release that tile's P buffer;
+//   warp 18      tensor-memory owner and MMA issuer (one thread);
 //   warps 0-7    "fold" warps, one key per thread (TMEM lane quadrant warp % 4, half warp / 4):
 //                convert the K codes of tile t to fp16 (exact) straight into tensor memory,
 //                then take the QK accumulators of tile t-1 out of tensor memory and fold the
-//                K scales in, mask, keep the lazy row maxima and write p as fp16 hi + lo;
+//                K scales in, mask, keep the lazy row maxima and write p as fp16 hi + lo
+//                (published once V of that tile has landed, so the PV warps wait once a tile);
 //   warps 8-15   PV warps: O^T += V^T (p dV) on mma.sync, each warp one 32-dim output block
 //                (hd256) or half of one (hd128), as in the all-mma.sync kernel.
+// The kernel is launched as a programmatic dependent: its prologue and K tile 0 overlap the
+// kernel before it in the stream; q, the window's cache writes and the partials wait for it.
 // QK on tcgen05, transposed (keys are M = 128): A = the tile's K codes as fp16 in tensor memory
 // (lane = key, column c = dims 2c, 2c + 1), B = the chunk's q rows as fp16 hi and lo stacked
 // along N (N = 2 RP, K-major, 128-byte swizzle), one accumulator D_b [128 keys x N] per 32-dim
@@ -84,6 +89,7 @@ struct TcLayout {
     static constexpr int LRED = RED + 4 * RP * 4;
     static constexpr int VIS = LRED + 4 * RP * 4;
     static constexpr int BARS = (VIS + RP * 4 + 7) / 8 * 8;
+    // (VE: unused; a V slot is released with its tile's P buffer, PE)
     enum { KF = 0, KE = 2, VF = 4, VE = VF + kVSlots, PF = VE + kVSlots, PE = PF + 2, GO = PE + 2, QKD = GO + 1,
            VGO = QKD + 1, NBARS = VGO + 1 };
     static constexpr int KH = GO;               // K^ of the tile written (the fold warps)
