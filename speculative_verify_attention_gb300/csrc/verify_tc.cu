@@ -57,6 +57,7 @@ constexpr int kVSlots = 2;       // V ring slots
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kWorkThreads = kTcThreads - 64;  // every warp but the two producers
 constexpr uint32_t kTcWait = 1u << 24;   // polls per mbarrier wait
+constexpr uint32_t kProdSleepNs = 200, kMmaSleepNs = 32;  // sleeps between polls
 constexpr float kLazyTc = 8.0f;          // log2 units: a row's reference maximum moves only past this
 constexpr float kPShiftTc = 4.0f;        // p is stored as p 2^4 (<= 2^12)
 
@@ -104,6 +105,19 @@ struct TcLayout {
     static_assert(QATOM % 1024 == 0 && STAGE % 1024 == 0 && HSTAGE % 1024 == 0, "swizzled tiles stay 1024-byte aligned");
     static_assert(BYTES <= 227 * 1024, "shared memory");
 };
+
+// A bounded wait for the roles that wait long (the producers for a stage to be released, the
+// MMA issuer for the next K^): between polls the warp sleeps, so that its polling takes fewer
+// issue slots from the fold and PV warps that share its sub-partition.  The producers have
+// slack and sleep longer; the MMA issuer's wake-up is on the tile's critical path.
+template <uint32_t kSleepNs>
+__device__ __forceinline__ bool mbar_wait_idle(uint32_t mbar, uint32_t parity, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i) {
+        if (tc::mbar_try_wait(mbar, parity)) return true;
+        __nanosleep(kSleepNs);
+    }
+    return false;
+}
 
 __device__ __forceinline__ void flag_timeout(unsigned int* err) {
     if (err) atomicOr(err, 1u);
@@ -339,12 +353,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
         if (!vplane) {
             if (window && n_tiles > 0) load_stage(false, 0);
             // this warp alone refills slot 0, so the slot cannot run a phase ahead of this wait
-            if (n_tiles > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(L::KF), 0, kTcWait));
+            if (n_tiles > 0) ok = __all_sync(0xffffffffu, mbar_wait_idle<kProdSleepNs>(bar(L::KF), 0, kTcWait));
             for (int t = 1; t < issued0; ++t) load_stage(false, t);
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(bar(L::VGO));
         } else {
-            ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(L::VGO), 0, kTcWait));
+            ok = __all_sync(0xffffffffu, mbar_wait_idle<kProdSleepNs>(bar(L::VGO), 0, kTcWait));
             for (int t = 0; t < issued0; ++t) load_stage(true, t);
         }
         if (!ok && lane == 0) flag_timeout(p.err);
@@ -353,7 +367,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
         static_assert(kVKeys == kKT && kVSlots == 2, "one V slot per tile, paired with the P buffers");
         const uint32_t empty0 = bar(vplane ? L::PE : L::KE);
         for (int t = 0; t + slots < total; ++t) {  // load t + slots into the slot load t leaves
-            ok = __all_sync(0xffffffffu, tc::mbar_wait(empty0 + 8u * (uint32_t)(t % slots), (t / slots) & 1, kTcWait));
+            ok = __all_sync(0xffffffffu, mbar_wait_idle<kProdSleepNs>(empty0 + 8u * (uint32_t)(t % slots), (t / slots) & 1, kTcWait));
             if (!ok) break;
             load_stage(vplane, t + slots);
             issued = t + slots + 1;
@@ -370,7 +384,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
             bool ok = true;
             int issued = 0;
             for (int t = 0; t < n_tiles; ++t) {
-                if (!tc::mbar_wait(bar(L::KH), t & 1, kTcWait)) { ok = false; break; }
+                if (!mbar_wait_idle<kMmaSleepNs>(bar(L::KH), t & 1, kTcWait)) { ok = false; break; }
                 tc::fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < HD / 16; ++ks)
