@@ -409,6 +409,16 @@ int attn_verify_q8_noalloc(const float* q, int n_rows, int n_q_heads, const kvq8
 int kvq8_selftest_convert(int kind, const uint32_t* in, uint32_t* out, int n, kvq8_stream_t stream);
 
 /*
+ * kvq8_selftest_wait_timeout -- a self-test hook for the kernels' failure path: one launch whose
+ * thread waits on an mbarrier that nothing arrives on, with the bounded wait every pipeline
+ * kernel of the library uses, limited to `polls` polls.  The wait gives up, the kernel sets the
+ * library's device error flag (read with kvq8_device_error) and returns; the context stays
+ * usable.  polls: 1 .. 1 << 20.  Errors: INVALID_ARG (polls out of range), CUDA (no device
+ * flag).  One launch on `stream`.
+ */
+int kvq8_selftest_wait_timeout(int polls, kvq8_stream_t stream);
+
+/*
  * kvq8_device_error -- read (and with reset != 0, clear) the library's device error flag.
  * Nonzero means a kernel gave up on an internal wait after its bounded poll count and
  * returned early.  Returns the flag, or -1 if it could not be read.  Unlike every other

@@ -10,7 +10,7 @@ from .binding import (EXPORTED, KVCacheF16, KVCacheK8V4, KVCacheQ8, attn_prompt_
                       attn_verify_append_q8, attn_verify_append_q8_workspace_bytes, attn_verify_q8_partials,
                       attn_verify_q8_partials_count, attn_verify_append_q8_host,
                       attn_verify_append_q8_host_scratch_bytes,
-                      attn_verify_q8_noalloc, attn_verify_q8_workspace_bytes, attn_verify_tree_q8, kvq8_append, kvq8_cache, kvq8_device_error, kvq8_quantize, kvq8_selftest_convert, kvq8_status_str, library_path,
+                      attn_verify_q8_noalloc, attn_verify_q8_workspace_bytes, attn_verify_tree_q8, kvq8_append, kvq8_cache, kvq8_device_error, kvq8_quantize, kvq8_selftest_convert, kvq8_selftest_wait_timeout, kvq8_status_str, library_path,
                       load_library)
 
 __all__ = ["EXPORTED", "KVCacheF16", "KVCacheK8V4", "KVCacheQ8", "attn_prompt_k8v4", "attn_verify_k8v4", "kvk8v4_append",
@@ -19,5 +19,5 @@ __all__ = ["EXPORTED", "KVCacheF16", "KVCacheK8V4", "KVCacheQ8", "attn_prompt_k8
            "attn_verify_append_q8", "attn_verify_append_q8_workspace_bytes", "attn_verify_q8_partials",
            "attn_verify_q8_partials_count", "attn_verify_append_q8_host",
            "attn_verify_append_q8_host_scratch_bytes",
-           "attn_verify_q8_noalloc", "attn_verify_q8_workspace_bytes", "attn_verify_tree_q8", "kvq8_append", "kvq8_cache", "kvq8_device_error", "kvq8_quantize", "kvq8_selftest_convert", "kvq8_status_str", "library_path",
+           "attn_verify_q8_noalloc", "attn_verify_q8_workspace_bytes", "attn_verify_tree_q8", "kvq8_append", "kvq8_cache", "kvq8_device_error", "kvq8_quantize", "kvq8_selftest_convert", "kvq8_selftest_wait_timeout", "kvq8_status_str", "library_path",
            "load_library"]

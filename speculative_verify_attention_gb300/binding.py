@@ -33,7 +33,8 @@ EXPORTED = ("kvq8_quantize", "kvq8_append", "attn_verify_q8_workspace_bytes", "a
             "kvf16_append", "attn_verify_f16_workspace_bytes", "attn_verify_f16", "kvk8v4_append", "attn_verify_k8v4",
             "attn_prompt_k8v4", "attn_prompt_f16", "attn_combine",
             "attn_prompt_q8_workspace_bytes", "attn_prompt_q8", "attn_verify_q8_noalloc", "kvq8_device_error", "kvq8_status_str",
-            "argmax_rows_top_prob_workspace_bytes", "argmax_rows_top_prob", "kvq8_selftest_convert")
+            "argmax_rows_top_prob_workspace_bytes", "argmax_rows_top_prob", "kvq8_selftest_convert",
+            "kvq8_selftest_wait_timeout")
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 
@@ -120,6 +121,8 @@ def load_library():
         lib.argmax_rows_top_prob.restype = i32
         lib.kvq8_selftest_convert.argtypes = [i32, vp, vp, i32, vp]
         lib.kvq8_selftest_convert.restype = i32
+        lib.kvq8_selftest_wait_timeout.argtypes = [i32, vp]
+        lib.kvq8_selftest_wait_timeout.restype = i32
         lib.attn_combine.argtypes = [vp, vp, i32, i32, i32, vp, vp]
         lib.attn_combine.restype = i32
         lib.attn_prompt_q8_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
@@ -567,6 +570,13 @@ def kvq8_selftest_convert(kind: int, words: torch.Tensor, stream=None) -> torch.
     st = load_library().kvq8_selftest_convert(int(kind), _ptr(words), _ptr(out), n, _stream(stream))
     _check("kvq8_selftest_convert", st)
     return out
+
+
+def kvq8_selftest_wait_timeout(polls: int = 4096, stream=None) -> None:
+    """One launch whose bounded wait on a barrier that nothing arrives on gives up after `polls`
+    polls and sets the device error flag (read it with kvq8_device_error)."""
+    st = load_library().kvq8_selftest_wait_timeout(int(polls), _stream(stream))
+    _check("kvq8_selftest_wait_timeout", st)
 
 
 def attn_combine(part_o: torch.Tensor, part_ml: torch.Tensor, out: torch.Tensor | None = None,

@@ -5,6 +5,8 @@
 // conversion of the codes is exact and was checked over all byte pairs; the same device
 // functions that the verify and prompt kernels call (common.cuh) run here unchanged.
 #include "common.cuh"
+#include "tc.cuh"
+#include "tmap.cuh"
 
 namespace kvq8 {
 namespace {
@@ -47,6 +49,20 @@ __global__ void __launch_bounds__(kSelfThreads) selftest_convert_kernel(int kind
     }
 }
 
+// One thread waits on a barrier that nothing arrives on (phase 0 never completes), with the
+// library's bounded wait; when the wait gives up it sets the device error flag, as the pipeline
+// kernels do on a timeout, and the kernel returns.
+__global__ void selftest_wait_kernel(unsigned int* err, uint32_t polls) {
+    __shared__ __align__(8) uint64_t mbar;
+    const uint32_t a = smem_u32(&mbar);
+    if (threadIdx.x == 0) {
+        tc::mbar_init(a, 1);
+        tc::mbar_init_fence();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !tc::mbar_wait(a, 0, polls)) atomicOr(err, 1u);
+}
+
 }  // namespace
 }  // namespace kvq8
 
@@ -58,5 +74,13 @@ extern "C" int kvq8_selftest_convert(int kind, const uint32_t* in, uint32_t* out
     if (kind == 1 && (n & 1)) return KVQ8_ERR_INVALID_ARG;
     kvq8::selftest_convert_kernel<<<(items + kvq8::kSelfThreads - 1) / kvq8::kSelfThreads, kvq8::kSelfThreads, 0,
                                     (cudaStream_t)stream>>>(kind, in, out, items);
+    return kvq8::launch_status();
+}
+
+extern "C" int kvq8_selftest_wait_timeout(int polls, kvq8_stream_t stream) {
+    if (polls < 1 || polls > (1 << 20)) return KVQ8_ERR_INVALID_ARG;
+    unsigned int* err = kvq8::device_error_flag();
+    if (!err) return KVQ8_ERR_CUDA;
+    kvq8::selftest_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(err, (uint32_t)polls);
     return kvq8::launch_status();
 }
