@@ -1,5 +1,5 @@
 // verify.cu -- the verify entry points (attn_verify_q8 and its variants) and the all-mma.sync
-// split-context scan used for tree-shaped windows, K8V4 pools and short causal scans.
+// split-context scan used for K8V4 pools and short causal or tree-window scans.
 //
 // Source: "perf(gfx1100): share Q8 KV scans across verifier rows", Summary: one worker owns
 // all the query rows of a verify window and shares each K/V scan across them; the context
@@ -7,11 +7,11 @@
 // int8-KV QSA prompt attention", How: fp16 hi + lo split of q and p with fp32 accumulation,
 // online softmax, V scale folded into p.
 //
-// Routing: causal windows over a Q8_0 cache (attn_verify_q8, attn_verify_q8_partials,
-// attn_verify_append_q8 and the host-buffer and no-allocation entries built on them) run the
-// tcgen05 scan of verify_tc.cu, except short scans (fewer than two 128-key tiles per block, or
-// hd128 chunks of <= 32 rows; see plan_causal) outside the append path, which run the kernel
-// below; tree-shaped windows and K8V4 pools always run the kernel below.
+// Routing: causal and tree-shaped windows over a Q8_0 cache (attn_verify_q8,
+// attn_verify_tree_q8, attn_verify_q8_partials, attn_verify_append_q8 and the host-buffer and
+// no-allocation entries built on them) run the tcgen05 scan of verify_tc.cu, except short scans
+// (fewer than two 128-key tiles per block, or hd128 chunks of <= 32 rows; see plan_causal)
+// outside the append path, which run the kernel below; K8V4 pools always run the kernel below.
 //
 // The kernel below (one thread block of 8 warps per (row chunk, context slice, KV head); the
 // chunks and slices come from verify_plan.cuh):
@@ -758,11 +758,11 @@ int verify_impl(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv,
     if (!(softmax_scale == softmax_scale) || softmax_scale == INFINITY || softmax_scale == -INFINITY)
         return KVQ8_ERR_INVALID_ARG;
     if (append && (!v_new || kv_len != q_pos0 + n_rows)) return KVQ8_ERR_INVALID_ARG;
-    // causal windows over a Q8_0 cache: the kernel plan_causal picks; tree windows and K8V4
-    // pools: the all-mma.sync kernel
+    // causal and tree windows over a Q8_0 cache: the kernel plan_causal picks; K8V4 pools: the
+    // all-mma.sync kernel
     bool tc = false;
     Plan pl;
-    const int rc = (!v4 && !wmask)
+    const int rc = !v4
                        ? plan_causal(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, n_split, &pl, &tc,
                                      append ? n_rows : 0)
                        : plan_mma(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, n_split, &pl);
@@ -816,6 +816,7 @@ int verify_impl(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv,
         tp.k_new = k_new;
         tp.v_new = v_new;
         tp.err = nullptr;
+        tp.wmask = wmask;
         tp.n_rows = n_rows;
         tp.n_q_heads = n_q_heads;
         tp.group = vp.group;

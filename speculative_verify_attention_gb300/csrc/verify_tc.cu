@@ -89,7 +89,8 @@ struct TcLayout {
     static constexpr int RED = DV + 8 * kKT * 2;
     static constexpr int LRED = RED + 4 * RP * 4;
     static constexpr int VIS = LRED + 4 * RP * 4;
-    static constexpr int BARS = (VIS + RP * 4 + 7) / 8 * 8;
+    static constexpr int WM = VIS + RP * 4;    // tree windows: each row's window mask
+    static constexpr int BARS = (WM + RP * 4 + 7) / 8 * 8;
     // (VE: unused; a V slot is released with its tile's P buffer, PE)
     enum { KF = 0, KE = 2, VF = 4, VE = VF + kVSlots, PF = VE + kVSlots, PE = PF + 2, GO = PE + 2, QKD = GO + 1,
            VGO = QKD + 1, NBARS = VGO + 1 };
@@ -178,7 +179,7 @@ __device__ __forceinline__ void ld_rows(uint32_t taddr, uint32_t (&d)[RP]) {
     }
 }
 
-template <int HD, int RP, bool APPEND>
+template <int HD, int RP, bool APPEND, bool TREE>
 __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_constant__ VerifyTcParams p) {
     using L = TcLayout<HD, RP>;
     constexpr int NB = L::NB, RPH = L::RPH, N = L::N, PS = L::PS, NT = RP / 8, MTW = HD / 128;
@@ -202,6 +203,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
     const bool producer = warp == kKProdWarp || warp == kVProdWarp;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::SLOT);
     int* sVis = reinterpret_cast<int*>(smem + L::VIS);
+    uint32_t* sWm = reinterpret_cast<uint32_t*>(smem + L::WM);
+    constexpr bool tree = TREE;  // rows see the window keys their masks select (p.wmask)
 
     // The merge kernel may be launched now; it waits for this grid before reading.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -297,15 +300,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
             *reinterpret_cast<uint4*>(atom + nh * 128 + ((c ^ (nh & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             *reinterpret_cast<uint4*>(atom + nl * 128 + ((c ^ (nl & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
-        // visibility bound of each row of the chunk (padding rows: 0)
+        // visibility bound of each row of the chunk (padding rows: 0); a tree window's row sees
+        // every key below q_pos0 and the window keys q_pos0 + j its mask selects (bit j)
         if (wtid < RP) {
             const int r = wtid;
             int v = 0;
+            uint32_t wm = 0u;
             if (r < rows_here) {
                 const int i = div_group_tc(row0 + r, p.group_magic);
-                v = min(min(p.q_pos0 + i + 1, p.kv_len), key_end);
+                v = min(min(tree ? p.q_pos0 + 32 : p.q_pos0 + i + 1, p.kv_len), key_end);
+                if (tree) wm = __ldg(p.wmask + i);
             }
             sVis[r] = v;
+            sWm[r] = wm;
         }
         if (APPEND && window) {
             // the window tokens' keys and values -> Q8_0 in the cache (bit-exact with the append
@@ -409,7 +416,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
         const int qd = fw & 3, h = fw >> 2;
         const int key_lane = 32 * qd + lane;
         const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
-        const int vis_min = min(min(p.q_pos0 + div_group_tc(row0, p.group_magic) + 1, p.kv_len), key_end);
+        const int vis_min =
+            min(min(tree ? p.q_pos0 : p.q_pos0 + div_group_tc(row0, p.group_magic) + 1, p.kv_len), key_end);
         float m_ref[RPH], l_acc[RPH], s[RPH];
 #pragma unroll
         for (int rr = 0; rr < RPH; ++rr) {
@@ -489,7 +497,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
                 if (tile0 + kKT > vis_min) {
 #pragma unroll
                     for (int rr = 0; rr < RPH; ++rr)
-                        if (key >= sVis[h * RPH + rr]) s[rr] = -INFINITY;
+                        if (key >= sVis[h * RPH + rr] ||
+                            (tree && key >= p.q_pos0 && !((sWm[h * RPH + rr] >> (key - p.q_pos0)) & 1u)))
+                            s[rr] = -INFINITY;
                 }
                 bool need = false;
 #pragma unroll
@@ -783,11 +793,11 @@ bool encode_code_plane(CUtensorMap* map, const int8_t* plane, int hd, int kv_len
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int HD, int RP, bool APPEND>
+template <int HD, int RP, bool APPEND, bool TREE>
 int launch_tc(const VerifyTcParams& vp, dim3 grid, cudaStream_t s) {
     using L = TcLayout<HD, RP>;
     static SmemOptIn opt;
-    if (opt.ensure(verify_tc_kernel<HD, RP, APPEND>, L::BYTES) != KVQ8_OK) return KVQ8_ERR_CUDA;
+    if (opt.ensure(verify_tc_kernel<HD, RP, APPEND, TREE>, L::BYTES) != KVQ8_OK) return KVQ8_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kTcThreads);
@@ -798,15 +808,15 @@ int launch_tc(const VerifyTcParams& vp, dim3 grid, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, verify_tc_kernel<HD, RP, APPEND>, vp) == cudaSuccess ? KVQ8_OK : KVQ8_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, verify_tc_kernel<HD, RP, APPEND, TREE>, vp) == cudaSuccess ? KVQ8_OK : KVQ8_ERR_CUDA;
 }
 
-template <int HD, bool APPEND>
+template <int HD, bool APPEND, bool TREE>
 int dispatch_rp(const VerifyTcParams& vp, int rp, dim3 grid, cudaStream_t s) {
     switch (rp) {
-        case 8: return launch_tc<HD, 8, APPEND>(vp, grid, s);
-        case 16: return launch_tc<HD, 16, APPEND>(vp, grid, s);
-        case 24: return launch_tc<HD, 24, APPEND>(vp, grid, s);
+        case 8: return launch_tc<HD, 8, APPEND, TREE>(vp, grid, s);
+        case 16: return launch_tc<HD, 16, APPEND, TREE>(vp, grid, s);
+        case 24: return launch_tc<HD, 24, APPEND, TREE>(vp, grid, s);
         default: return KVQ8_ERR_UNSUPPORTED;
     }
 }
@@ -821,9 +831,15 @@ int launch_verify_tc(VerifyTcParams& vp, const Plan& pl, int n_kv_heads, bool ap
     if (!vp.err) return KVQ8_ERR_CUDA;
     const int rp = 8 * pl.nt;
     const dim3 grid(pl.n_chunks, pl.n_split, n_kv_heads);
+    // tree windows have no append variant (the append path is causal)
+    if (append && vp.wmask) return KVQ8_ERR_UNSUPPORTED;
     if (pl.hd == 128)
-        return append ? dispatch_rp<128, true>(vp, rp, grid, s) : dispatch_rp<128, false>(vp, rp, grid, s);
-    return append ? dispatch_rp<256, true>(vp, rp, grid, s) : dispatch_rp<256, false>(vp, rp, grid, s);
+        return append ? dispatch_rp<128, true, false>(vp, rp, grid, s)
+                      : (vp.wmask ? dispatch_rp<128, false, true>(vp, rp, grid, s)
+                                  : dispatch_rp<128, false, false>(vp, rp, grid, s));
+    return append ? dispatch_rp<256, true, false>(vp, rp, grid, s)
+                  : (vp.wmask ? dispatch_rp<256, false, true>(vp, rp, grid, s)
+                              : dispatch_rp<256, false, false>(vp, rp, grid, s));
 }
 
 }  // namespace kvq8

@@ -18,6 +18,7 @@ struct VerifyTcParams {
     const float* k_new;  // append path: fp32 [n_rows][n_kv_heads][HD] window keys and values
     const float* v_new;
     unsigned int* err;   // the library's timeout flag (set by launch_verify_tc)
+    const uint32_t* wmask;  // tree windows: bit j of wmask[i] = row i sees key q_pos0 + j; null = causal
     int n_rows, n_q_heads, group, group_magic, capacity, kv_len, q_pos0, keys_per_split, key_shift, n_ctx_splits,
         n_kv_heads, rows_per_chunk;
     float qscale;        // softmax_scale * log2(e)
