@@ -698,7 +698,7 @@ int dispatch_nt(const VerifyParams& vp, const Plan& pl, int n_kv_heads, cudaStre
 }  // namespace
 
 // Plans of the two scan kernels: causal windows over a Q8_0 cache run the tcgen05 kernel
-// (row chunks of <= 24 rows, one block per SM); tree windows and K8V4 pools the all-mma.sync one.
+// (row chunks of <= 24 rows, one block per SM); short scans (plan_causal) and K8V4 pools the all-mma.sync one.
 inline int plan_tc(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_kv_heads, int n_split, Plan* pl,
                    int window_keys = 0) {
     return make_plan(n_rows, n_q_heads, head_dim, kv_len, n_kv_heads, n_split, pl, window_keys, tc_blocks_per_sm,
