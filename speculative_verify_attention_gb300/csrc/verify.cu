@@ -9,9 +9,10 @@
 //
 // Routing: causal and tree-shaped windows over a Q8_0 cache (attn_verify_q8,
 // attn_verify_tree_q8, attn_verify_q8_partials, attn_verify_append_q8 and the host-buffer and
-// no-allocation entries built on them) run the tcgen05 scan of verify_tc.cu, except short scans
-// (fewer than two 128-key tiles per block, or hd128 chunks of <= 32 rows; see plan_causal)
-// outside the append path, which run the kernel below; K8V4 pools always run the kernel below.
+// no-allocation entries built on them) and causal windows over a K8V4 pool at hd256
+// (attn_verify_k8v4) run the tcgen05 scan of verify_tc.cu, except short scans (fewer than two
+// 128-key tiles per block, or hd128 chunks of <= 32 rows; see plan_causal) outside the append
+// path, which run the kernel below; K8V4 pools at hd128 always run the kernel below.
 //
 // The kernel below (one thread block of 8 warps per (row chunk, context slice, KV head); the
 // chunks and slices come from verify_plan.cuh):
@@ -698,7 +699,8 @@ int dispatch_nt(const VerifyParams& vp, const Plan& pl, int n_kv_heads, cudaStre
 }  // namespace
 
 // Plans of the two scan kernels: causal windows over a Q8_0 cache run the tcgen05 kernel
-// (row chunks of <= 24 rows, one block per SM); short scans (plan_causal) and K8V4 pools the all-mma.sync one.
+// (row chunks of <= 24 rows, one block per SM); short scans (plan_causal) and K8V4 pools at hd128
+// the all-mma.sync one.
 inline int plan_tc(int n_rows, int n_q_heads, int head_dim, int kv_len, int n_kv_heads, int n_split, Plan* pl,
                    int window_keys = 0) {
     return make_plan(n_rows, n_q_heads, head_dim, kv_len, n_kv_heads, n_split, pl, window_keys, tc_blocks_per_sm,
@@ -758,11 +760,11 @@ int verify_impl(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv,
     if (!(softmax_scale == softmax_scale) || softmax_scale == INFINITY || softmax_scale == -INFINITY)
         return KVQ8_ERR_INVALID_ARG;
     if (append && (!v_new || kv_len != q_pos0 + n_rows)) return KVQ8_ERR_INVALID_ARG;
-    // causal and tree windows over a Q8_0 cache: the kernel plan_causal picks; K8V4 pools: the
-    // all-mma.sync kernel
+    // causal and tree windows over a Q8_0 cache and causal windows over a K8V4 pool at hd256: the
+    // kernel plan_causal picks; K8V4 pools at hd128: the all-mma.sync kernel
     bool tc = false;
     Plan pl;
-    const int rc = !v4
+    const int rc = !v4 || kv->head_dim == 256
                        ? plan_causal(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, n_split, &pl, &tc,
                                      append ? n_rows : 0)
                        : plan_mma(n_rows, n_q_heads, kv->head_dim, kv_len, kv->n_kv_heads, n_split, &pl);
@@ -830,7 +832,7 @@ int verify_impl(const float* q, int n_rows, int n_q_heads, const kvq8_cache* kv,
         tp.n_kv_heads = kv->n_kv_heads;
         tp.rows_per_chunk = pl.rows_per_chunk;
         tp.qscale = vp.qscale;
-        r1 = launch_verify_tc(tp, pl, kv->n_kv_heads, append, s);
+        r1 = launch_verify_tc(tp, pl, kv->n_kv_heads, append, v4, s);
     } else if (v4)  // K8V4 pools: causal windows, no append
         r1 = pl.hd == 128 ? dispatch_nt<128, false, true>(vp, pl, kv->n_kv_heads, s)
                           : dispatch_nt<256, false, true>(vp, pl, kv->n_kv_heads, s);

@@ -1,6 +1,7 @@
 // verify_tc.cu -- the split-context verify scan over a Q8_0 cache with QK on the tcgen05 tensor
 // cores (the causal windows of attn_verify_q8, attn_verify_q8_partials and
-// attn_verify_append_q8).
+// attn_verify_append_q8, the tree windows of attn_verify_tree_q8, and the causal windows of
+// attn_verify_k8v4 at hd256, whose V plane holds 4-bit codes expanded in the PV warps).
 //
 // Source: "perf(gfx1100): share Q8 KV scans across verifier rows", Summary: one worker owns all
 // query rows of a verify window and shares each K/V scan across them; context slices write
@@ -61,7 +62,7 @@ constexpr uint32_t kProdSleepNs = 200, kMmaSleepNs = 32;  // sleeps between poll
 constexpr float kLazyTc = 8.0f;          // log2 units: a row's reference maximum moves only past this
 constexpr float kPShiftTc = 4.0f;        // p is stored as p 2^4 (<= 2^12)
 
-template <int HD, int RP>
+template <int HD, int RP, bool V4 = false>
 struct TcLayout {
     static constexpr int NB = HD / 32;          // scale blocks per key
     static constexpr int RPH = RP / 2;          // rows per fold-warp half
@@ -78,7 +79,9 @@ struct TcLayout {
     // V: a ring of kVSlots units of kVKeys keys (a whole tile or a fraction of one)
     static constexpr int HKEYS = kVKeys;
     static constexpr int HBOX = HKEYS * 128;
-    static constexpr int HCODES = NBOX * HBOX;
+    // V codes per key: HD bytes, or HD/2 bytes of 4-bit codes (K8V4 pools, hd256 only: one box)
+    static constexpr int NBOXV = V4 ? 1 : NBOX;
+    static constexpr int HCODES = NBOXV * HBOX;
     static constexpr int HSTAGE = (HCODES + HKEYS * NB * 2 + 1023) / 1024 * 1024;
     static constexpr int VST = KST + 2 * STAGE;
     static constexpr int P = VST + kVSlots * HSTAGE;
@@ -102,6 +105,7 @@ struct TcLayout {
     static constexpr uint32_t TM_COLS = TM_USED <= 128 ? 128 : TM_USED <= 256 ? 256 : 512;
     static constexpr uint32_t IDESC = tc::idesc_f16_f32(128, N, false);
     static_assert(RP % 8 == 0 && RP <= 24, "rows per chunk");
+    static_assert(!V4 || HD == 256, "4-bit V tiles of one 128-byte box per key");
     static_assert(TM_USED <= 512, "tensor memory");
     static_assert(QATOM % 1024 == 0 && STAGE % 1024 == 0 && HSTAGE % 1024 == 0, "swizzled tiles stay 1024-byte aligned");
     static_assert(BYTES <= 227 * 1024, "shared memory");
@@ -179,9 +183,9 @@ __device__ __forceinline__ void ld_rows(uint32_t taddr, uint32_t (&d)[RP]) {
     }
 }
 
-template <int HD, int RP, bool APPEND, bool TREE>
+template <int HD, int RP, bool APPEND, bool TREE, bool V4>
 __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_constant__ VerifyTcParams p) {
-    using L = TcLayout<HD, RP>;
+    using L = TcLayout<HD, RP, V4>;
     constexpr int NB = L::NB, RPH = L::RPH, N = L::N, PS = L::PS, NT = RP / 8, MTW = HD / 128;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -240,7 +244,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
         if (lane == 0) {
             tc::mbar_arrive_expect_tx(full, (uint32_t)codes);
 #pragma unroll
-            for (int bx = 0; bx < L::NBOX; ++bx)
+            for (int bx = 0; bx < (vplane ? L::NBOXV : L::NBOX); ++bx)
                 tma_box(st + (uint32_t)(bx * (vplane ? L::HBOX : L::BOX)), vplane ? &p.tmap_v : &p.tmap_k, 128 * bx,
                         key0, kvh, full);
         }
@@ -623,6 +627,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
         const int cq = 2 * (pvb & 3) + (g >> 2);
         const int v_off0 = hb * L::HBOX + (2 * tq) * 128 + ((cq ^ (2 * tq)) << 4) + 4 * (g & 3);
         const int v_off1 = hb * L::HBOX + (2 * tq + 1) * 128 + ((cq ^ (2 * tq + 1)) << 4) + 4 * (g & 3);
+        // 4-bit V (hd256): the lane's dims 32 pvb + 4g .. +3 are the 2 bytes at 2g of chunk pvb
+        // (4 nibbles, element 2m in the low nibble of byte m), stored at chunk pvb ^ (row % 8)
+        const int v4_off0 = (2 * tq) * 128 + ((pvb ^ (2 * tq)) << 4) + 2 * g;
+        const int v4_off1 = (2 * tq + 1) * 128 + ((pvb ^ (2 * tq + 1)) << 4) + 2 * g;
         bool ok = true;
         for (int t = 0; t < n_tiles && ok; ++t) {
             const int b = t & 1, u = t >> 1;
@@ -701,6 +709,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
                     const __half2 d89 = u32_as_h2(*reinterpret_cast<const uint32_t*>(sDv + kb + 2 * tq + 8));
                     uint32_t A[MTW][4];
                     const uint8_t* vp = vst + ks * 16 * 128;
+                    if constexpr (V4) {
+                        // keys (2tq, 2tq+1) and (2tq+8, 2tq+9) side by side, 4 nibbles of each per
+                        // half: dims 4g, 4g+1 (mt 0) and 4g+2, 4g+3 (mt 1), exactly as fp16
+                        const uint32_t x01 = (uint32_t)*reinterpret_cast<const uint16_t*>(vp + v4_off0) |
+                                             ((uint32_t)*reinterpret_cast<const uint16_t*>(vp + v4_off1) << 16);
+                        const uint32_t x89 = (uint32_t)*reinterpret_cast<const uint16_t*>(vp + v4_off0 + 8 * 128) |
+                                             ((uint32_t)*reinterpret_cast<const uint16_t*>(vp + v4_off1 + 8 * 128) << 16);
+                        A[0][0] = nib_lo_to_half2(x01);
+                        A[0][1] = nib_hi_to_half2(x01);
+                        A[0][2] = nib_lo_to_half2(x89);
+                        A[0][3] = nib_hi_to_half2(x89);
+                        A[MTW - 1][0] = nib_lo_to_half2(x01 >> 8);
+                        A[MTW - 1][1] = nib_hi_to_half2(x01 >> 8);
+                        A[MTW - 1][2] = nib_lo_to_half2(x89 >> 8);
+                        A[MTW - 1][3] = nib_hi_to_half2(x89 >> 8);
+                    } else {
                     const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vp + v_off0) ^ 0x80808080u;
                     const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vp + v_off1) ^ 0x80808080u;
                     const uint32_t w8 = *reinterpret_cast<const uint32_t*>(vp + v_off0 + 8 * 128) ^ 0x80808080u;
@@ -718,6 +742,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
                         A[MTW - 1][1] = biased_bytes_to_half2<0x4342>(y01);
                         A[MTW - 1][2] = biased_bytes_to_half2<0x4140>(y89);
                         A[MTW - 1][3] = biased_bytes_to_half2<0x4342>(y89);
+                    }
                     }
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
@@ -793,11 +818,11 @@ bool encode_code_plane(CUtensorMap* map, const int8_t* plane, int hd, int kv_len
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int HD, int RP, bool APPEND, bool TREE>
+template <int HD, int RP, bool APPEND, bool TREE, bool V4>
 int launch_tc(const VerifyTcParams& vp, dim3 grid, cudaStream_t s) {
-    using L = TcLayout<HD, RP>;
+    using L = TcLayout<HD, RP, V4>;
     static SmemOptIn opt;
-    if (opt.ensure(verify_tc_kernel<HD, RP, APPEND, TREE>, L::BYTES) != KVQ8_OK) return KVQ8_ERR_CUDA;
+    if (opt.ensure(verify_tc_kernel<HD, RP, APPEND, TREE, V4>, L::BYTES) != KVQ8_OK) return KVQ8_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kTcThreads);
@@ -808,24 +833,28 @@ int launch_tc(const VerifyTcParams& vp, dim3 grid, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, verify_tc_kernel<HD, RP, APPEND, TREE>, vp) == cudaSuccess ? KVQ8_OK : KVQ8_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, verify_tc_kernel<HD, RP, APPEND, TREE, V4>, vp) == cudaSuccess ? KVQ8_OK
+                                                                                                 : KVQ8_ERR_CUDA;
 }
 
-template <int HD, bool APPEND, bool TREE>
+template <int HD, bool APPEND, bool TREE, bool V4 = false>
 int dispatch_rp(const VerifyTcParams& vp, int rp, dim3 grid, cudaStream_t s) {
     switch (rp) {
-        case 8: return launch_tc<HD, 8, APPEND, TREE>(vp, grid, s);
-        case 16: return launch_tc<HD, 16, APPEND, TREE>(vp, grid, s);
-        case 24: return launch_tc<HD, 24, APPEND, TREE>(vp, grid, s);
+        case 8: return launch_tc<HD, 8, APPEND, TREE, V4>(vp, grid, s);
+        case 16: return launch_tc<HD, 16, APPEND, TREE, V4>(vp, grid, s);
+        case 24: return launch_tc<HD, 24, APPEND, TREE, V4>(vp, grid, s);
         default: return KVQ8_ERR_UNSUPPORTED;
     }
 }
 
 }  // namespace
 
-int launch_verify_tc(VerifyTcParams& vp, const Plan& pl, int n_kv_heads, bool append, cudaStream_t s) {
+int launch_verify_tc(VerifyTcParams& vp, const Plan& pl, int n_kv_heads, bool append, bool v4, cudaStream_t s) {
+    // 4-bit V (K8V4 pools): causal windows at hd256 only, the V plane rows hd/2 bytes long
+    if (v4 && (append || vp.wmask || pl.hd != 256)) return KVQ8_ERR_UNSUPPORTED;
     if (!encode_code_plane(&vp.tmap_k, vp.k_codes, pl.hd, vp.kv_len, n_kv_heads, vp.capacity, kKT) ||
-        !encode_code_plane(&vp.tmap_v, vp.v_codes, pl.hd, vp.kv_len, n_kv_heads, vp.capacity, kVKeys))
+        !encode_code_plane(&vp.tmap_v, vp.v_codes, v4 ? pl.hd / 2 : pl.hd, vp.kv_len, n_kv_heads, vp.capacity,
+                           kVKeys))
         return KVQ8_ERR_CUDA;
     vp.err = device_error_flag();
     if (!vp.err) return KVQ8_ERR_CUDA;
@@ -833,6 +862,7 @@ int launch_verify_tc(VerifyTcParams& vp, const Plan& pl, int n_kv_heads, bool ap
     const dim3 grid(pl.n_chunks, pl.n_split, n_kv_heads);
     // tree windows have no append variant (the append path is causal)
     if (append && vp.wmask) return KVQ8_ERR_UNSUPPORTED;
+    if (v4) return dispatch_rp<256, false, false, true>(vp, rp, grid, s);
     if (pl.hd == 128)
         return append ? dispatch_rp<128, true, false>(vp, rp, grid, s)
                       : (vp.wmask ? dispatch_rp<128, false, true>(vp, rp, grid, s)

@@ -27,7 +27,8 @@ struct VerifyTcParams {
 };
 
 // The tcgen05 verify scan of one call planned with make_plan(..., tc_blocks_per_sm, kTcMaxRows):
-// one launch writing the slices' partials; `append` selects the window-slice variant.
-int launch_verify_tc(VerifyTcParams& vp, const Plan& pl, int n_kv_heads, bool append, cudaStream_t s);
+// one launch writing the slices' partials; `append` selects the window-slice variant, `v4` the
+// 4-bit V plane of a K8V4 pool (v_codes then holds hd/2 bytes per key; causal, hd256 only).
+int launch_verify_tc(VerifyTcParams& vp, const Plan& pl, int n_kv_heads, bool append, bool v4, cudaStream_t s);
 
 }  // namespace kvq8

@@ -80,6 +80,39 @@ def test_27b_shape(lib, T, n_split):
     assert rel_err(got, ref) <= VERIFY_TOL
 
 
+@pytest.mark.parametrize("hq,hkv,L,T,pos0,n_split", [
+    (6, 1, 3001, 1, 3000, 3),      # one 8-row chunk of 6 rows, ragged last tile
+    (6, 1, 2500, 3, 2497, 4),      # 18 rows: one 24-row chunk
+    (16, 1, 3333, 2, 3331, 2),     # group 16: 32 rows in two 16-row chunks
+    (8, 8, 2000, 4, 1996, 2),      # MHA, eight KV heads
+    (24, 4, 2600, 32, 2568, 2),    # T = 32: eight 24-row chunks per KV head
+    (4, 1, 1500, 6, 1600, 2),      # rows past kv_len see kv_len keys
+    (4, 1, 3000, 4, 2000, 3),      # kv_len beyond the window
+    (24, 4, 2055, 8, 2047, 5),     # slices end mid-tile
+])
+def test_hd256_on_the_tcgen05_scan(lib, hq, hkv, L, T, pos0, n_split):
+    """hd256 K8V4 windows whose blocks get several 128-key tiles run the tcgen05 scan with the
+    4-bit V plane; junk codes and scales past kv_len stay unseen."""
+    inp = workloads.random_small(1500 + hq + L + T, hq, hkv, 256, L, T, k_gain=1.5)
+    gpu, orc = _pools(inp, capacity=L + 40)
+    got = _run(gpu, inp.q, L, pos0, 0.0625, n_split)
+    ref = oracle.attention(orc, inp.q, L, pos0, 0.0625)
+    assert np.all(np.isfinite(got))
+    assert rel_err(got, ref) <= VERIFY_TOL
+
+
+def test_hd256_routes_agree(lib):
+    """One window through the all-mma.sync kernel (the automatic plan of a short scan) and the
+    tcgen05 scan (two slices): both within the tolerance of the oracle and of each other."""
+    inp = workloads.random_small(1520, 24, 4, 256, 1024, 4)
+    gpu, orc = _pools(inp, capacity=1100)
+    a = _run(gpu, inp.q, 1024, 1020, 0.0625, 0)
+    b = _run(gpu, inp.q, 1024, 1020, 0.0625, 2)
+    ref = oracle.attention(orc, inp.q, 1024, 1020, 0.0625)
+    assert rel_err(a, ref) <= VERIFY_TOL and rel_err(b, ref) <= VERIFY_TOL
+    assert rel_err(a, b) <= VERIFY_TOL
+
+
 @pytest.mark.parametrize("T", [4, 8, 12, 32])
 def test_hd128_shape(lib, T):
     w = workloads.verify_workload(f"k8v4-32q8kv-hd128-ctx700-T{T}", 32, 8, 128, 700, T, seed=1350 + T)
