@@ -764,6 +764,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
                 // 32-key steps: key rows past nkh hold p = 0 (masked) and finite codes and scales
                 // (zeros past kv_len), so a ragged half may round up
                 const int n_u = (nkh + 31) >> 5;
+#pragma unroll 2
                 for (int u4 = 0; u4 < n_u; ++u4) {
                     pv_step(2 * u4);
                     pv_step(2 * u4 + 1);
