@@ -133,8 +133,9 @@ def test_edges(lib, kv_len, q_pos0, T, hd):
     assert rel_err(got, ref) <= VERIFY_TOL
 
 
-def test_full_size_sampled(lib):
-    w = workloads.long_verify(20676, 4)
+@pytest.mark.parametrize("ctx,T", [(20676, 4), (32768, 8)])
+def test_full_size_sampled(lib, ctx, T):
+    w = workloads.long_verify(ctx, T)
     inp = workloads.make_inputs(w)
     gpu, orc = _pools(inp, junk=False)
     got = _run(gpu, inp.q, w.kv_len, w.q_pos0, w.softmax_scale)

@@ -93,3 +93,20 @@ def test_tree_rejects_bad_arguments(lib):
                                   ctypes.c_float(0.1), ctypes.c_void_p(out.data_ptr()),
                                   ctypes.c_void_p(ws.data_ptr()), ws.numel(), 0, None)
     assert st == 1                                # null window mask
+
+
+@pytest.mark.parametrize("T", [8, 32])
+def test_binary_tree_full_context_sampled(lib, T):
+    """A binary-tree window at the long-context shape (24q/4kv/hd256, ctx 20676; the tcgen05 scan
+    with the automatic plan): every row and every q head sampled against the oracle."""
+    w = workloads.long_verify(20676, T)
+    inp = workloads.make_inputs(w)
+    gpu, orc = build_caches(inp, garbage_tail=False)
+    mask = _binary_tree(T)
+    got = _run(gpu, inp.q, w.kv_len, w.q_pos0, w.softmax_scale, mask)
+    rng = np.random.default_rng(40 + T)
+    sel = [(i, int(rng.integers(w.n_q_heads))) for i in range(w.n_q)]
+    sel += [(int(rng.integers(w.n_q)), h) for h in range(w.n_q_heads)]
+    ref = oracle.attention_tree(orc, inp.q, w.kv_len, w.q_pos0, w.softmax_scale, mask, sel=sel)
+    assert np.all(np.isfinite(got))
+    assert rel_err(np.stack([got[i, h] for i, h in sel]), ref) <= VERIFY_TOL
