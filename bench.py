@@ -148,8 +148,9 @@ def _max_over_ranks(x: float, world: int) -> float:
 
 
 def kernel_source_digest(kernel_files) -> str:
-    """sha256 of the kernel sources' code with comments and blank lines removed, so that an
-    edit of comments alone keeps a capture valid while any change of code invalidates it."""
+    """sha256 of the kernel sources' code with comments, blank lines and spacing removed, so that
+    an edit of comments or layout alone keeps a capture valid while any change of code
+    invalidates it."""
     import hashlib
     h = hashlib.sha256()
     for name in kernel_files:
@@ -157,7 +158,7 @@ def kernel_source_digest(kernel_files) -> str:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
-        h.update("\n".join(line.rstrip() for line in text.splitlines() if line.strip()).encode())
+        h.update("\n".join(" ".join(line.split()) for line in text.splitlines() if line.strip()).encode())
     return h.hexdigest()
 
 

@@ -725,24 +725,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
                         A[MTW - 1][2] = nib_lo_to_half2(x89 >> 8);
                         A[MTW - 1][3] = nib_hi_to_half2(x89 >> 8);
                     } else {
-                    const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vp + v_off0) ^ 0x80808080u;
-                    const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vp + v_off1) ^ 0x80808080u;
-                    const uint32_t w8 = *reinterpret_cast<const uint32_t*>(vp + v_off0 + 8 * 128) ^ 0x80808080u;
-                    const uint32_t w9 = *reinterpret_cast<const uint32_t*>(vp + v_off1 + 8 * 128) ^ 0x80808080u;
-                    if (HD == 256 || (pw & 1) == 0) {  // dims 4g, 4g+1 (and 4g+2, 4g+3 at hd256)
-                        const uint32_t y01 = prmt2<0x5140>(w0, w1), y89 = prmt2<0x5140>(w8, w9);
-                        A[0][0] = biased_bytes_to_half2<0x4140>(y01);
-                        A[0][1] = biased_bytes_to_half2<0x4342>(y01);
-                        A[0][2] = biased_bytes_to_half2<0x4140>(y89);
-                        A[0][3] = biased_bytes_to_half2<0x4342>(y89);
-                    }
-                    if (HD == 256 || (pw & 1) == 1) {  // dims 4g+2, 4g+3
-                        const uint32_t y01 = prmt2<0x7362>(w0, w1), y89 = prmt2<0x7362>(w8, w9);
-                        A[MTW - 1][0] = biased_bytes_to_half2<0x4140>(y01);
-                        A[MTW - 1][1] = biased_bytes_to_half2<0x4342>(y01);
-                        A[MTW - 1][2] = biased_bytes_to_half2<0x4140>(y89);
-                        A[MTW - 1][3] = biased_bytes_to_half2<0x4342>(y89);
-                    }
+                        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vp + v_off0) ^ 0x80808080u;
+                        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vp + v_off1) ^ 0x80808080u;
+                        const uint32_t w8 = *reinterpret_cast<const uint32_t*>(vp + v_off0 + 8 * 128) ^ 0x80808080u;
+                        const uint32_t w9 = *reinterpret_cast<const uint32_t*>(vp + v_off1 + 8 * 128) ^ 0x80808080u;
+                        if (HD == 256 || (pw & 1) == 0) {  // dims 4g, 4g+1 (and 4g+2, 4g+3 at hd256)
+                            const uint32_t y01 = prmt2<0x5140>(w0, w1), y89 = prmt2<0x5140>(w8, w9);
+                            A[0][0] = biased_bytes_to_half2<0x4140>(y01);
+                            A[0][1] = biased_bytes_to_half2<0x4342>(y01);
+                            A[0][2] = biased_bytes_to_half2<0x4140>(y89);
+                            A[0][3] = biased_bytes_to_half2<0x4342>(y89);
+                        }
+                        if (HD == 256 || (pw & 1) == 1) {  // dims 4g+2, 4g+3
+                            const uint32_t y01 = prmt2<0x7362>(w0, w1), y89 = prmt2<0x7362>(w8, w9);
+                            A[MTW - 1][0] = biased_bytes_to_half2<0x4140>(y01);
+                            A[MTW - 1][1] = biased_bytes_to_half2<0x4342>(y01);
+                            A[MTW - 1][2] = biased_bytes_to_half2<0x4140>(y89);
+                            A[MTW - 1][3] = biased_bytes_to_half2<0x4342>(y89);
+                        }
                     }
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
@@ -804,14 +804,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
     if (warp == kMmaWarp) tc::tmem_dealloc(tmem, L::TM_COLS);
 }
 
-// Tensor map of one code plane [n_kv_heads][capacity][hd] (bytes): dims (hd, kv_len, n_kv_heads),
-// so keys at or past kv_len read as zeros; box 128 bytes x 128 keys x 1 head, 128-byte swizzle.
-bool encode_code_plane(CUtensorMap* map, const int8_t* plane, int hd, int kv_len, int n_kv_heads, int capacity,
+// Tensor map of one code plane [n_kv_heads][capacity][row_bytes] (bytes; row_bytes = hd, or hd/2
+// for 4-bit codes): dims (row_bytes, kv_len, n_kv_heads), so keys at or past kv_len read as zeros;
+// box 128 bytes x box_keys keys x 1 head, 128-byte swizzle.
+bool encode_code_plane(CUtensorMap* map, const int8_t* plane, int row_bytes, int kv_len, int n_kv_heads, int capacity,
                        int box_keys) {
     const EncodeTiledFn fn = encode_tiled_fn();
     if (!fn) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)kv_len, (cuuint64_t)n_kv_heads};
-    const cuuint64_t strides[2] = {(cuuint64_t)hd, (cuuint64_t)capacity * hd};
+    const cuuint64_t dims[3] = {(cuuint64_t)row_bytes, (cuuint64_t)kv_len, (cuuint64_t)n_kv_heads};
+    const cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)capacity * row_bytes};
     const cuuint32_t box[3] = {128, (cuuint32_t)box_keys, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<int8_t*>(plane), dims, strides, box, estr,
