@@ -170,6 +170,21 @@ __device__ __forceinline__ void fma2(float& s0, float& s1, float a, float b0, fl
         : "f"(a), "f"(b0), "f"(b1));
 }
 
+// (s0, s1) -= (a, b) and (s0, s1) += (a, b): one packed fp32 instruction, each half rounded as
+// the scalar operation would.
+__device__ __forceinline__ void sub2(float& s0, float& s1, float a, float b) {
+    asm("{\n .reg .b64 x, z;\n mov.b64 x, {%2, %3};\n mov.b64 z, {%0, %1};\n sub.rn.f32x2 z, z, x;\n"
+        " mov.b64 {%0, %1}, z;\n}\n"
+        : "+f"(s0), "+f"(s1)
+        : "f"(a), "f"(b));
+}
+__device__ __forceinline__ void add2(float& s0, float& s1, float a, float b) {
+    asm("{\n .reg .b64 x, z;\n mov.b64 x, {%2, %3};\n mov.b64 z, {%0, %1};\n add.rn.f32x2 z, z, x;\n"
+        " mov.b64 {%0, %1}, z;\n}\n"
+        : "+f"(s0), "+f"(s1)
+        : "f"(a), "f"(b));
+}
+
 // RP columns of one accumulator block (this warp's rows: RP/2 hi then RP/2 lo columns).
 template <int RP>
 __device__ __forceinline__ void ld_rows(uint32_t taddr, uint32_t (&d)[RP]) {
@@ -535,10 +550,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
                     }
                 }
 #pragma unroll
-                for (int rr = 0; rr < RPH; ++rr) {
-                    const float mb = m_ref[rr] == -INFINITY ? 0.0f : m_ref[rr] - kPShiftTc;
-                    s[rr] = ex2_approx(s[rr] - mb);
-                    l_acc[rr] += s[rr];
+                for (int rr = 0; rr < RPH; rr += 2) {  // row pairs: packed subtract and sum
+                    const float mb0 = m_ref[rr] == -INFINITY ? 0.0f : m_ref[rr] - kPShiftTc;
+                    const float mb1 = m_ref[rr + 1] == -INFINITY ? 0.0f : m_ref[rr + 1] - kPShiftTc;
+                    sub2(s[rr], s[rr + 1], mb0, mb1);
+                    s[rr] = ex2_approx(s[rr]);
+                    s[rr + 1] = ex2_approx(s[rr + 1]);
+                    add2(l_acc[rr], l_acc[rr + 1], s[rr], s[rr + 1]);
                 }
                 // P(t-1) into buffer (t-1) & 1 once the PV warps are done with tile t-3
                 const int pb = (t - 1) & 1, pu = (t - 1) >> 1;
@@ -556,7 +574,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
                     const float pe = ev ? s[k] : recv;
                     const float po = ev ? recv : s[RPH / 2 + k];
                     const __half2 ph = __floats2half2_rn(pe, po);
-                    const __half2 pl = __floats2half2_rn(pe - __low2float(ph), po - __high2float(ph));
+                    float re = pe, ro = po;  // the residuals p - hi, one packed subtract
+                    sub2(re, ro, __low2float(ph), __high2float(ph));
+                    const __half2 pl = __floats2half2_rn(re, ro);
                     const int row = h * RPH + (ev ? k : RPH / 2 + k);
                     sP[kp * PS + row] = make_uint2(h2_as_u32(ph), h2_as_u32(pl));
                 }
