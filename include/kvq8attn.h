@@ -238,9 +238,10 @@ int attn_verify_k8v4(const float* q, int n_rows, int n_q_heads, const kvk8v4_cac
                      int n_split, kvq8_stream_t stream);
 
 /*
- * attn_prompt_k8v4 -- attn_prompt_q8 over a K8V4 pool (the same shapes, workspace from
- * attn_prompt_q8_workspace_bytes, precision bound and errors); the dequantisers expand the
- * 4-bit V blocks (value (nibble - 8) * scale, rounded once to fp16) into the V tiles.
+ * attn_prompt_k8v4 -- attn_prompt_q8 over a K8V4 pool (the same shapes, routes, workspace
+ * from attn_prompt_q8_workspace_bytes, precision bound and errors); the dequantisers expand
+ * the 4-bit V blocks (value (nibble - 8) * scale, rounded once to fp16) into the V tiles or,
+ * on the two-pass route, into the fp16 copy.
  */
 int attn_prompt_k8v4(const uint16_t* q, int n_q, int n_q_heads, const kvk8v4_cache* kv, int kv_len,
                      int q_pos0, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
@@ -332,7 +333,12 @@ int argmax_rows_top_prob(const float* logits, int n_rows, int vocab, int32_t* ar
 int attn_combine(const float* part_o, const float* part_ml, int n_split, int rows, int head_dim,
                  float* out, kvq8_stream_t stream);
 
-/* Bytes of workspace attn_prompt_q8 needs for this shape (on the current device). */
+/*
+ * Bytes of workspace attn_prompt_q8 (and attn_prompt_k8v4 / attn_prompt_f16) needs for this
+ * shape (on the current device): the partials, plus, for chunks of 32 or more 128-row tiles
+ * per KV head, room for the fp16 copy of both planes (2 * n_kv_heads * min(kv_len, q_pos0 +
+ * n_q) * head_dim * 2 bytes) that the two-pass route writes.  fp16 pools never use that room.
+ */
 size_t attn_prompt_q8_workspace_bytes(int n_q, int n_q_heads, int head_dim, int kv_len, int q_pos0,
                                       int n_kv_heads);
 
@@ -342,11 +348,16 @@ size_t attn_prompt_q8_workspace_bytes(int n_q, int n_q_heads, int head_dim, int 
  *   kv       : the cache (the same head_dim, any n_kv_heads dividing n_q_heads)
  *   out      : fp32 [n_q][n_q_heads][head_dim]
  *   workspace: device scratch of at least attn_prompt_q8_workspace_bytes(...) bytes,
- *              caller-owned; holds the per-slice partials merged by the second kernel
+ *              caller-owned; holds the per-slice partials merged by the last kernel and,
+ *              on the two-pass route, the fp16 copy of the planes
  *   softmax_scale must be > 0.
- * Row i sees keys n <= q_pos0 + i, n < kv_len.  K and V are dequantised on chip to fp16
- * (code * scale, one rounding) and contracted on the tcgen05 tensor cores with fp32
- * accumulation in tensor memory; p enters the PV product as fp16.  The work -- key tiles
+ * Row i sees keys n <= q_pos0 + i, n < kv_len.  K and V are dequantised to fp16 (code *
+ * scale, one rounding) and contracted on the tcgen05 tensor cores with fp32 accumulation in
+ * tensor memory; p enters the PV product as fp16.  Short chunks (fewer than 32 row tiles per
+ * KV head) dequantise each tile on chip, once per row tile that sees it.  Longer chunks take
+ * the two-pass route: one pass writes the fp16 planes of keys < min(kv_len, q_pos0 + n_q)
+ * into the workspace, and the kernel of attn_prompt_f16 runs over that copy; the operands, and
+ * so the results, are the same on both routes.  The work -- key tiles
  * (64 keys at head_dim 256, 128 at 128) of 128-row tiles of (query, head) pairs of every
  * KV head -- is cut into one equal
  * contiguous share per SM (a persistent grid); each share writes partials that the

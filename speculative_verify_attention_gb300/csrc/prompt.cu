@@ -269,6 +269,64 @@ __device__ __forceinline__ void dequant_tile_v4(const uint8_t* codes, const uint
     }
 }
 
+// The dequantising pass of the two-pass route: keys < n_keys of the pool's K and V planes
+// ([n_kv_heads][capacity] rows of codes and scales) as fp16 planes [n_kv_heads][n_keys][hd] in
+// the workspace.  Each value is code x scale rounded once to fp16, exactly as the
+// dequantisers of the one-pass kernel compute it, so both routes feed the tensor cores the
+// same operands.  One thread per 32-value block: 32 code bytes (16 for a 4-bit V plane) and one
+// scale in, 64 bytes out; a warp covers consecutive blocks, so loads and stores coalesce.
+// blockIdx.y = plane * n_kv_heads + KV head (plane 0 = K, 1 = V); blocks stride along x.
+struct DequantParams {
+    const int8_t* kc;
+    const uint16_t* ks;
+    const int8_t* vc;
+    const uint16_t* vs;
+    uint16_t* k16;
+    uint16_t* v16;
+    int hd, n_keys, capacity, n_kv_heads;
+};
+
+template <bool V4>
+__global__ void __launch_bounds__(256) dequant_planes_kernel(const DequantParams p) {
+    const int plane = blockIdx.y / p.n_kv_heads, h = blockIdx.y - plane * p.n_kv_heads;
+    const bool vplane = plane == 1;
+    const int nb_shift = p.hd == 256 ? 3 : 2;  // 32-value blocks per key: 8 or 4
+    const int n_blocks = p.n_keys << nb_shift;
+    const int8_t* codes = vplane ? p.vc : p.kc;
+    const uint16_t* scales = (vplane ? p.vs : p.ks) + (size_t)h * p.capacity * (p.hd / 32);
+    uint16_t* dst_plane = (vplane ? p.v16 : p.k16) + (size_t)h * p.n_keys * p.hd;
+    for (int b = blockIdx.x * 256 + threadIdx.x; b < n_blocks; b += gridDim.x * 256) {
+        const int n = b >> nb_shift, j = b & ((1 << nb_shift) - 1);
+        const __half2 sc = __half2half2(__ushort_as_half(scales[(size_t)n * (p.hd / 32) + j]));
+        uint32_t o[16];
+        if (V4 && vplane) {
+            const uint4 raw =
+                *reinterpret_cast<const uint4*>(codes + ((size_t)h * p.capacity + n) * (p.hd / 2) + 16 * j);
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                o[4 * e + 0] = h2_as_u32(__hmul2(u32_as_h2(nib_byte_to_half2<0>(w[e])), sc));
+                o[4 * e + 1] = h2_as_u32(__hmul2(u32_as_h2(nib_byte_to_half2<1>(w[e])), sc));
+                o[4 * e + 2] = h2_as_u32(__hmul2(u32_as_h2(nib_byte_to_half2<2>(w[e])), sc));
+                o[4 * e + 3] = h2_as_u32(__hmul2(u32_as_h2(nib_byte_to_half2<3>(w[e])), sc));
+            }
+        } else {
+            const uint4* src = reinterpret_cast<const uint4*>(codes + ((size_t)h * p.capacity + n) * p.hd + 32 * j);
+            const uint4 r0 = src[0], r1 = src[1];
+            const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t x = w[e] ^ 0x80808080u;
+                o[2 * e] = h2_as_u32(__hmul2(u32_as_h2(biased_bytes_to_half2<0x4140>(x)), sc));
+                o[2 * e + 1] = h2_as_u32(__hmul2(u32_as_h2(biased_bytes_to_half2<0x4342>(x)), sc));
+            }
+        }
+        uint4* dst = reinterpret_cast<uint4*>(dst_plane + (size_t)n * p.hd + 32 * j);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+    }
+}
+
 // One box of a 3-D tensor map into shared memory, completion counted on `mbar` in bytes.
 // x (the dim coordinate) is a multiple of 64 fp16 = 128 bytes, as a tiled copy requires.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t mbar) {
@@ -749,8 +807,18 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
 struct PromptPlan {
     int n_mtiles, n_items, n_parts, grid;
     long long units;
-    size_t ws_bytes;
+    // two-pass route: the fp16 copy of keys < copy_keys of both planes at byte copy_off of the
+    // workspace (copy_keys = 0: the one-pass kernel dequantises in shared memory)
+    int copy_keys;
+    size_t copy_off, ws_bytes;
 };
+
+// Row tiles per KV head from which a Q8_0 or K8V4 chunk takes the two-pass route.  The one-pass
+// kernel dequantises every K/V tile once per row tile that sees it; the two-pass route pays one
+// pass over the planes (6.1 bytes of traffic per value) and then runs without staging.  Measured
+// on GB300 over a 32K context: the routes tie at 24 row tiles at hd256 (12q/1kv), the two-pass
+// route is 8 % slower at 16 row tiles at hd128 (32q/8kv) and 9-12 % faster at 64 and more.
+constexpr int kTwoPassMinMtiles = 32;
 
 int prompt_plan(int n_q, int n_q_heads, int head_dim, int kv_len, int q_pos0, int n_kv_heads, PromptPlan* pl) {
     if (n_q < 1 || n_q_heads < 1 || n_kv_heads < 1 || kv_len < 1 || q_pos0 < 0) return KVQ8_ERR_INVALID_ARG;
@@ -790,8 +858,33 @@ int prompt_plan(int n_q, int n_q_heads, int head_dim, int kv_len, int q_pos0, in
     pl->n_parts = parts;
     const size_t rows_out = (size_t)n_q * n_q_heads;
     const size_t o_bytes = (size_t)parts * rows_out * head_dim * sizeof(float);
-    pl->ws_bytes = ((o_bytes + 255) / 256) * 256 + (size_t)parts * rows_out * 2 * sizeof(float);
+    const size_t part_bytes = ((o_bytes + 255) / 256) * 256 + (size_t)parts * rows_out * 2 * sizeof(float);
+    // the highest key any row sees is q_pos0 + n_q - 1 (or the context's end)
+    const long long last = (long long)q_pos0 + n_q;
+    pl->copy_keys = pl->n_mtiles >= kTwoPassMinMtiles ? (int)(last < kv_len ? last : kv_len) : 0;
+    pl->copy_off = ((part_bytes + 255) / 256) * 256;
+    pl->ws_bytes = pl->copy_keys ? pl->copy_off + 2 * (size_t)n_kv_heads * pl->copy_keys * head_dim * sizeof(uint16_t)
+                                 : part_bytes;
     return KVQ8_OK;
+}
+
+int launch_dequant_planes(const DequantParams& dp, bool v4, cudaStream_t s) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess || sms <= 0)
+        sms = 152;
+    const int planes = 2 * dp.n_kv_heads;
+    if (planes > 65535) return KVQ8_ERR_UNSUPPORTED;
+    const long long blocks = (long long)dp.n_keys * (dp.hd / 32);
+    // about eight 256-thread blocks per SM over all planes and heads, each looping over its share
+    long long gx = (blocks + 255) / 256, cap = (8LL * sms + planes - 1) / planes;
+    gx = gx < cap ? gx : cap;
+    const dim3 grid((unsigned)(gx > 0 ? gx : 1), (unsigned)planes);
+    if (v4)
+        dequant_planes_kernel<true><<<grid, 256, 0, s>>>(dp);
+    else
+        dequant_planes_kernel<false><<<grid, 256, 0, s>>>(dp);
+    return launch_status();
 }
 
 template <int HD, int POOL>
@@ -871,16 +964,29 @@ int prompt_impl(const uint16_t* q, int n_q, int n_q_heads, const kvq8_cache* kv,
     pp.n_parts = pl.n_parts;
     pp.units = pl.units;
     pp.scale_log2 = softmax_scale * kLog2e;
-    if (pool == kPoolF16) {
+    cudaStream_t s = (cudaStream_t)stream;
+    // two-pass route (long chunks over Q8_0 / K8V4 pools): dequantise the planes once into the
+    // workspace, then run the tensor-copy kernel of fp16 pools over that copy
+    const bool two_pass = pool != kPoolF16 && pl.copy_keys > 0;
+    if (two_pass) {
+        uint16_t* k16 = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + pl.copy_off);
+        uint16_t* v16 = k16 + (size_t)kv->n_kv_heads * pl.copy_keys * HD;
+        const DequantParams dp = {kv->k_codes, kv->k_scales, kv->v_codes, kv->v_scales, k16, v16,
+                                  HD, pl.copy_keys, kv->capacity, kv->n_kv_heads};
+        const int r0 = launch_dequant_planes(dp, pool == kPoolK8V4, s);
+        if (r0 != KVQ8_OK) return r0;
+        if (!encode_f16_plane(&pp.tmap_k, k16, HD, pl.copy_keys, kv->n_kv_heads, pl.copy_keys) ||
+            !encode_f16_plane(&pp.tmap_v, v16, HD, pl.copy_keys, kv->n_kv_heads, pl.copy_keys))
+            return KVQ8_ERR_CUDA;
+    } else if (pool == kPoolF16) {
         const uint16_t* kp = reinterpret_cast<const uint16_t*>(kv->k_codes);
         const uint16_t* vp = reinterpret_cast<const uint16_t*>(kv->v_codes);
         if (!encode_f16_plane(&pp.tmap_k, kp, HD, kv_len, kv->n_kv_heads, kv->capacity) ||
             !encode_f16_plane(&pp.tmap_v, vp, HD, kv_len, kv->n_kv_heads, kv->capacity))
             return KVQ8_ERR_CUDA;
     }
-    cudaStream_t s = (cudaStream_t)stream;
     int r1;
-    if (pool == kPoolF16)
+    if (pool == kPoolF16 || two_pass)
         r1 = HD == 128 ? launch_prompt<128, kPoolF16>(pp, pl.grid, s) : launch_prompt<256, kPoolF16>(pp, pl.grid, s);
     else if (pool == kPoolK8V4)
         r1 = HD == 128 ? launch_prompt<128, kPoolK8V4>(pp, pl.grid, s) : launch_prompt<256, kPoolK8V4>(pp, pl.grid, s);

@@ -152,3 +152,43 @@ def test_prompt_rows_sharded_as_virtual_ranks(lib):
     sel = [(int(i), int(rng.integers(hq))) for i in rng.integers(0, nq, 40)] + [(nq - 1, h) for h in range(hq)]
     ref = oracle.attention(orc, inp.q, L, L - nq, scale, sel=sel)
     assert rel_err(np.stack([got[i, h] for i, h in sel]), ref) <= PROMPT_TOL
+
+
+@pytest.mark.parametrize("hq,hkv,L,nq,pos0,capacity,hd", [
+    (12, 1, 900, 342, 558, 933, 256),   # 33 row tiles per KV head (the last one 8 rows), odd capacity
+    (12, 1, 1100, 342, 500, 1200, 256), # the copy stops at q_pos0 + n_q = 842, short of kv_len
+    (12, 1, 500, 360, 300, None, 256),  # rows past kv_len see all 500 keys
+    (24, 2, 900, 360, 540, None, 256),  # two KV heads, each its own plane in the copy
+    (32, 8, 1100, 1030, 70, 1103, 128), # hd128, 33 row tiles per KV head, odd capacity
+])
+def test_two_pass_route(lib, hq, hkv, L, nq, pos0, capacity, hd):
+    """Chunks of 32 or more 128-row tiles per KV head take the two-pass route (the planes
+    dequantised into the workspace, then the tensor-copy kernel over that fp16 copy)."""
+    _check(hq, hkv, L, nq, pos0, seed=hq * 100 + L + 11, capacity=capacity, hd=hd,
+           sel_every=None if hd == 256 else 3)
+
+
+@pytest.mark.parametrize("hq,hkv,L,nq,pos0,hd", [
+    (12, 1, 900, 342, 558, 256),
+    (32, 8, 1100, 1030, 70, 128),
+])
+def test_two_pass_equals_the_f16_pool_of_the_dequantised_values(lib, hq, hkv, L, nq, pos0, hd):
+    """The two-pass route's operands are fp16(code x scale), rounded once: attn_prompt_f16 over
+    a pool holding exactly those values (computed here with numpy from the cache's codes and
+    scales) gives the same output bit for bit."""
+    import torch
+
+    from speculative_verify_attention_gb300 import KVCacheF16, attn_prompt_f16, attn_prompt_q8
+    inp = workloads.random_small(hq * 10 + L, hq, hkv, hd, L, nq, q_dtype="f16")
+    gpu, _ = build_caches(inp)
+    f16 = KVCacheF16(hkv, hd, gpu.capacity)
+    for codes, scales, dst in ((gpu.k_codes, gpu.k_scales, f16.k), (gpu.v_codes, gpu.v_scales, f16.v)):
+        c = codes.cpu().numpy()[:, :L].astype(np.float16)
+        s = np.repeat(scales.cpu().numpy()[:, :L], 32, axis=2)
+        dst[:, :L].copy_(torch.from_numpy(c * s))   # numpy rounds the exact product once to fp16
+    q = torch.from_numpy(np.ascontiguousarray(inp.q)).cuda()
+    scale = 1.0 / float(np.sqrt(hd))
+    a = attn_prompt_q8(q, gpu, L, pos0, scale)
+    b = attn_prompt_f16(q, f16, L, pos0, scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)

@@ -193,6 +193,8 @@ def _prompt(gpu, q16, kv_len, q_pos0, scale):
     (24, 2, 256, 512, 64, 448, None),
     (32, 8, 128, 333, 40, 290, 335),
     (16, 4, 128, 300, 60, 280, 301),
+    (12, 1, 256, 900, 342, 558, 933),   # 33 row tiles per KV head: the two-pass route
+    (32, 8, 128, 1100, 1030, 70, 1103),
 ])
 def test_prompt_k8v4_small_shapes(lib, hq, hkv, hd, L, nq, pos0, capacity):
     from ._util import PROMPT_TOL

@@ -48,3 +48,37 @@ def test_automatic_plans_fill_one_wave_of_a_152_sm_part():
             assert 2 <= n_split and n_split * chunks * hkv <= 152, (ctx, T, n_split)
             if ctx >= 20676:   # long enough for every slice to hold whole 128-key tiles and fill the SMs
                 assert (n_split + 1) * chunks * hkv > 152 - chunks * hkv, (ctx, T, n_split)
+
+
+def _partials_bytes_match(ws, rows_out, hd):
+    """ws is the partials layout (o aligned to 256 bytes, then (m, l)) for some part count."""
+    for parts in range(1, 257):
+        o = parts * rows_out * hd * 4
+        if ws == -(-o // 256) * 256 + parts * rows_out * 8:
+            return True
+    return False
+
+
+def test_prompt_workspace_adds_the_fp16_copy_from_32_row_tiles():
+    """attn_prompt_q8_workspace_bytes: the partials alone below 32 128-row tiles per KV head;
+    from 32 on, the partials rounded up to 256 bytes plus the fp16 copy of both planes, keys
+    < min(kv_len, q_pos0 + n_q) (computed without a GPU: the planner assumes 152 SMs)."""
+    lib = ctypes.CDLL(build.build())
+    fn = lib.attn_prompt_q8_workspace_bytes
+    fn.restype = ctypes.c_size_t
+    for hq, hkv, hd, kv_len, nq, pos0 in ((12, 1, 256, 32768, 330, 32438),   # 31 row tiles
+                                          (12, 1, 256, 32768, 342, 32426),   # 33
+                                          (12, 1, 256, 4096, 342, 1000),     # copy stops at 1342
+                                          (32, 8, 128, 32768, 2048, 30720),  # 64
+                                          (32, 8, 128, 8192, 1000, 7192),    # 32 (4000 rows)
+                                          (32, 8, 128, 8192, 992, 7200)):    # 31
+        ws = fn(nq, hq, hd, kv_len, pos0, hkv)
+        rows_out = nq * hq
+        mtiles = -(-nq * (hq // hkv) // 128)
+        if mtiles < 32:
+            assert _partials_bytes_match(ws, rows_out, hd), (hq, nq)
+            continue
+        copy = 2 * hkv * min(kv_len, pos0 + nq) * hd * 2
+        part = ws - copy
+        assert part % 256 == 0 and part > 0, (hq, nq)
+        assert any(_partials_bytes_match(part - pad, rows_out, hd) for pad in range(0, 256, 8)), (hq, nq)
