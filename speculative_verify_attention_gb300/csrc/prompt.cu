@@ -498,8 +498,11 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
                 const int jfirst = j;
                 for (int t = seg[si].t0; t < seg[si].t1; ++t, ++j) {
                     const int b = j & 1, use = j >> 1;
+                    // S(j) overwrites the columns from which PV(j-2) reads P(j-2); both MMAs come
+                    // from this thread and tcgen05 MMAs run in issue order, so QK(j) is issued
+                    // without waiting for PV(j-2) to complete (waiting cost 5-7 % on the 32K x 2048
+                    // chunks: the tensor pipe drained once per tile)
                     if (!tc::mbar_wait(B(B_K_FULL + b), use & 1, kWaitLimit)) { ok = false; break; }
-                    if (j >= 2 && !tc::mbar_wait(B(B_PV_DONE + b), (use - 1) & 1, kWaitLimit)) { ok = false; break; }
                     tc::fence_after_sync();
                     const uint32_t khat = sbase + SM_KHAT + b * HAT_BYTES;
 #pragma unroll
