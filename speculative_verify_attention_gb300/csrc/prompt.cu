@@ -273,8 +273,10 @@ __device__ __forceinline__ void dequant_tile_v4(const uint8_t* codes, const uint
 // ([n_kv_heads][capacity] rows of codes and scales) as fp16 planes [n_kv_heads][n_keys][hd] in
 // the workspace.  Each value is code x scale rounded once to fp16, exactly as the
 // dequantisers of the one-pass kernel compute it, so both routes feed the tensor cores the
-// same operands.  One thread per 32-value block: 32 code bytes (16 for a 4-bit V plane) and one
-// scale in, 64 bytes out; a warp covers consecutive blocks, so loads and stores coalesce.
+// same operands.  One thread per 8 consecutive values: 8 code bytes (4 for a 4-bit V plane) and
+// their scale in, 16 bytes out, so that each warp instruction loads 256 (128) and stores 512
+// contiguous bytes (one thread per 32-value block, with its four 16-byte stores 64 bytes apart
+// across the warp, half-filled every sector and measured 1-2 % slower on the prompt call).
 // blockIdx.y = plane * n_kv_heads + KV head (plane 0 = K, 1 = V); blocks stride along x.
 struct DequantParams {
     const int8_t* kc;
@@ -290,40 +292,31 @@ template <bool V4>
 __global__ void __launch_bounds__(256) dequant_planes_kernel(const DequantParams p) {
     const int plane = blockIdx.y / p.n_kv_heads, h = blockIdx.y - plane * p.n_kv_heads;
     const bool vplane = plane == 1;
-    const int nb_shift = p.hd == 256 ? 3 : 2;  // 32-value blocks per key: 8 or 4
-    const int n_blocks = p.n_keys << nb_shift;
+    const int g_shift = p.hd == 256 ? 5 : 4;  // 8-value groups per key: 32 or 16
     const int8_t* codes = vplane ? p.vc : p.kc;
     const uint16_t* scales = (vplane ? p.vs : p.ks) + (size_t)h * p.capacity * (p.hd / 32);
     uint16_t* dst_plane = (vplane ? p.v16 : p.k16) + (size_t)h * p.n_keys * p.hd;
-    for (int b = blockIdx.x * 256 + threadIdx.x; b < n_blocks; b += gridDim.x * 256) {
-        const int n = b >> nb_shift, j = b & ((1 << nb_shift) - 1);
-        const __half2 sc = __half2half2(__ushort_as_half(scales[(size_t)n * (p.hd / 32) + j]));
-        uint32_t o[16];
+    const int n_groups = p.n_keys << g_shift;
+    for (int b = blockIdx.x * 256 + threadIdx.x; b < n_groups; b += gridDim.x * 256) {
+        const int n = b >> g_shift, g8 = b & ((1 << g_shift) - 1);
+        const __half2 sc = __half2half2(__ushort_as_half(scales[(size_t)n * (p.hd / 32) + (g8 >> 2)]));
+        uint32_t o[4];
         if (V4 && vplane) {
-            const uint4 raw =
-                *reinterpret_cast<const uint4*>(codes + ((size_t)h * p.capacity + n) * (p.hd / 2) + 16 * j);
-            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                o[4 * e + 0] = h2_as_u32(__hmul2(u32_as_h2(nib_byte_to_half2<0>(w[e])), sc));
-                o[4 * e + 1] = h2_as_u32(__hmul2(u32_as_h2(nib_byte_to_half2<1>(w[e])), sc));
-                o[4 * e + 2] = h2_as_u32(__hmul2(u32_as_h2(nib_byte_to_half2<2>(w[e])), sc));
-                o[4 * e + 3] = h2_as_u32(__hmul2(u32_as_h2(nib_byte_to_half2<3>(w[e])), sc));
-            }
+            const uint32_t w =
+                *reinterpret_cast<const uint32_t*>(codes + ((size_t)h * p.capacity + n) * (p.hd / 2) + 4 * g8);
+            o[0] = h2_as_u32(__hmul2(u32_as_h2(nib_byte_to_half2<0>(w)), sc));
+            o[1] = h2_as_u32(__hmul2(u32_as_h2(nib_byte_to_half2<1>(w)), sc));
+            o[2] = h2_as_u32(__hmul2(u32_as_h2(nib_byte_to_half2<2>(w)), sc));
+            o[3] = h2_as_u32(__hmul2(u32_as_h2(nib_byte_to_half2<3>(w)), sc));
         } else {
-            const uint4* src = reinterpret_cast<const uint4*>(codes + ((size_t)h * p.capacity + n) * p.hd + 32 * j);
-            const uint4 r0 = src[0], r1 = src[1];
-            const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const uint32_t x = w[e] ^ 0x80808080u;
-                o[2 * e] = h2_as_u32(__hmul2(u32_as_h2(biased_bytes_to_half2<0x4140>(x)), sc));
-                o[2 * e + 1] = h2_as_u32(__hmul2(u32_as_h2(biased_bytes_to_half2<0x4342>(x)), sc));
-            }
+            const uint2 r = *reinterpret_cast<const uint2*>(codes + ((size_t)h * p.capacity + n) * p.hd + 8 * g8);
+            const uint32_t x0 = r.x ^ 0x80808080u, x1 = r.y ^ 0x80808080u;
+            o[0] = h2_as_u32(__hmul2(u32_as_h2(biased_bytes_to_half2<0x4140>(x0)), sc));
+            o[1] = h2_as_u32(__hmul2(u32_as_h2(biased_bytes_to_half2<0x4342>(x0)), sc));
+            o[2] = h2_as_u32(__hmul2(u32_as_h2(biased_bytes_to_half2<0x4140>(x1)), sc));
+            o[3] = h2_as_u32(__hmul2(u32_as_h2(biased_bytes_to_half2<0x4342>(x1)), sc));
         }
-        uint4* dst = reinterpret_cast<uint4*>(dst_plane + (size_t)n * p.hd + 32 * j);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+        *reinterpret_cast<uint4*>(dst_plane + (size_t)n * p.hd + 8 * g8) = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
@@ -877,9 +870,10 @@ int launch_dequant_planes(const DequantParams& dp, bool v4, cudaStream_t s) {
                                                   cudaSuccess || sms <= 0)
         sms = 152;
     const int planes = 2 * dp.n_kv_heads;
-    if (planes > 65535) return KVQ8_ERR_UNSUPPORTED;
-    const long long blocks = (long long)dp.n_keys * (dp.hd / 32);
+    const long long blocks = (long long)dp.n_keys * (dp.hd / 8);   // 8-value groups per plane
+    if (planes > 65535 || blocks > 0x7fffffffLL) return KVQ8_ERR_UNSUPPORTED;
     // about eight 256-thread blocks per SM over all planes and heads, each looping over its share
+    // of the 8-value groups
     long long gx = (blocks + 255) / 256, cap = (8LL * sms + planes - 1) / planes;
     gx = gx < cap ? gx : cap;
     const dim3 grid((unsigned)(gx > 0 ? gx : 1), (unsigned)planes);
