@@ -335,7 +335,7 @@ int attn_combine(const float* part_o, const float* part_ml, int n_split, int row
 
 /*
  * Bytes of workspace attn_prompt_q8 (and attn_prompt_k8v4 / attn_prompt_f16) needs for this
- * shape (on the current device): the partials, plus, for chunks of 32 or more 128-row tiles
+ * shape (on the current device): the partials, plus, for chunks of 24 or more 128-row tiles
  * per KV head, room for the fp16 copy of both planes (2 * n_kv_heads * min(kv_len, q_pos0 +
  * n_q) * head_dim * 2 bytes) that the two-pass route writes.  fp16 pools never use that room.
  */
@@ -353,7 +353,7 @@ size_t attn_prompt_q8_workspace_bytes(int n_q, int n_q_heads, int head_dim, int 
  *   softmax_scale must be > 0.
  * Row i sees keys n <= q_pos0 + i, n < kv_len.  K and V are dequantised to fp16 (code *
  * scale, one rounding) and contracted on the tcgen05 tensor cores with fp32 accumulation in
- * tensor memory; p enters the PV product as fp16.  Short chunks (fewer than 32 row tiles per
+ * tensor memory; p enters the PV product as fp16.  Short chunks (fewer than 24 row tiles per
  * KV head) dequantise each tile on chip, once per row tile that sees it.  Longer chunks take
  * the two-pass route: one pass writes the fp16 planes of keys < min(kv_len, q_pos0 + n_q)
  * into the workspace, and the kernel of attn_prompt_f16 runs over that copy; the operands, and

@@ -812,9 +812,10 @@ struct PromptPlan {
 // Row tiles per KV head from which a Q8_0 or K8V4 chunk takes the two-pass route.  The one-pass
 // kernel dequantises every K/V tile once per row tile that sees it; the two-pass route pays one
 // pass over the planes (6.1 bytes of traffic per value) and then runs without staging.  Measured
-// on GB300 over a 32K context: the routes tie at 24 row tiles at hd256 (12q/1kv), the two-pass
-// route is 8 % slower at 16 row tiles at hd128 (32q/8kv) and 9-12 % faster at 64 and more.
-constexpr int kTwoPassMinMtiles = 32;
+// on GB300 over a 32K context: at hd256 (12q/1kv) the routes tie at 17 row tiles and the
+// two-pass route is 3 % faster at 24, 7 % at 48; at hd128 (32q/8kv) it is 2 % slower at 16 row
+// tiles and 15 % faster at 64.
+constexpr int kTwoPassMinMtiles = 24;
 
 int prompt_plan(int n_q, int n_q_heads, int head_dim, int kv_len, int q_pos0, int n_kv_heads, PromptPlan* pl) {
     if (n_q < 1 || n_q_heads < 1 || n_kv_heads < 1 || kv_len < 1 || q_pos0 < 0) return KVQ8_ERR_INVALID_ARG;

@@ -162,7 +162,7 @@ def test_prompt_rows_sharded_as_virtual_ranks(lib):
     (32, 8, 1100, 1030, 70, 1103, 128), # hd128, 33 row tiles per KV head, odd capacity
 ])
 def test_two_pass_route(lib, hq, hkv, L, nq, pos0, capacity, hd):
-    """Chunks of 32 or more 128-row tiles per KV head take the two-pass route (the planes
+    """Chunks of 24 or more 128-row tiles per KV head take the two-pass route (the planes
     dequantised into the workspace, then the tensor-copy kernel over that fp16 copy)."""
     _check(hq, hkv, L, nq, pos0, seed=hq * 100 + L + 11, capacity=capacity, hd=hd,
            sel_every=None if hd == 256 else 3)

@@ -59,23 +59,23 @@ def _partials_bytes_match(ws, rows_out, hd):
     return False
 
 
-def test_prompt_workspace_adds_the_fp16_copy_from_32_row_tiles():
-    """attn_prompt_q8_workspace_bytes: the partials alone below 32 128-row tiles per KV head;
-    from 32 on, the partials rounded up to 256 bytes plus the fp16 copy of both planes, keys
+def test_prompt_workspace_adds_the_fp16_copy_from_24_row_tiles():
+    """attn_prompt_q8_workspace_bytes: the partials alone below 24 128-row tiles per KV head;
+    from 24 on, the partials rounded up to 256 bytes plus the fp16 copy of both planes, keys
     < min(kv_len, q_pos0 + n_q) (computed without a GPU: the planner assumes 152 SMs)."""
     lib = ctypes.CDLL(build.build())
     fn = lib.attn_prompt_q8_workspace_bytes
     fn.restype = ctypes.c_size_t
-    for hq, hkv, hd, kv_len, nq, pos0 in ((12, 1, 256, 32768, 330, 32438),   # 31 row tiles
-                                          (12, 1, 256, 32768, 342, 32426),   # 33
-                                          (12, 1, 256, 4096, 342, 1000),     # copy stops at 1342
+    for hq, hkv, hd, kv_len, nq, pos0 in ((12, 1, 256, 32768, 245, 32523),   # 23 row tiles
+                                          (12, 1, 256, 32768, 246, 32522),   # 24 (2952 rows)
+                                          (12, 1, 256, 4096, 342, 1000),     # 33; copy stops at 1342
                                           (32, 8, 128, 32768, 2048, 30720),  # 64
-                                          (32, 8, 128, 8192, 1000, 7192),    # 32 (4000 rows)
-                                          (32, 8, 128, 8192, 992, 7200)):    # 31
+                                          (32, 8, 128, 8192, 768, 7424),     # 24 (3072 rows)
+                                          (32, 8, 128, 8192, 736, 7456)):    # 23
         ws = fn(nq, hq, hd, kv_len, pos0, hkv)
         rows_out = nq * hq
         mtiles = -(-nq * (hq // hkv) // 128)
-        if mtiles < 32:
+        if mtiles < 24:
             assert _partials_bytes_match(ws, rows_out, hd), (hq, nq)
             continue
         copy = 2 * hkv * min(kv_len, pos0 + nq) * hd * 2
