@@ -469,16 +469,23 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
         if (lane == 0) {
             bool ok = true;
             int j = 0, pv_issued = 0;
+            // One thread issues every MMA, and its issue rate sets the tile period, so the shared-
+            // memory descriptors are built once: a descriptor's address field is (address >> 4)
+            // in 14 bits, and every operand lies below 228 KB on a 16-byte boundary, so the
+            // descriptor of base + off is the base descriptor + (off >> 4), a constant per MMA
+            // (building each from its address measured 4-5 % slower on the 32K x 2048 chunks).
+            const uint64_t kdesc0 = tc::smem_desc_sw128(sbase + SM_KHAT, 16, 1024);
+            const uint64_t vdesc0 = tc::smem_desc_sw128(sbase + SM_VHAT, BN * 128, 1024);
             auto issue_pv = [&](int jj, bool first) -> bool {
                 const int bb = jj & 1, u = jj >> 1;
                 if (!tc::mbar_wait(B(B_P_FULL + bb), u & 1, kWaitLimit)) return false;
                 if (!tc::mbar_wait(B(B_V_FULL + bb), u & 1, kWaitLimit)) return false;
                 tc::fence_after_sync();
-                const uint32_t vhat = sbase + SM_VHAT + bb * HAT_BYTES;
+                const uint64_t vdesc = vdesc0 + (uint64_t)((bb * HAT_BYTES) >> 4);
                 const uint32_t pcol = tmem + TM_S0 + bb * BN;
 #pragma unroll
                 for (int ks = 0; ks < BN / 16; ++ks)
-                    tc::mma_ts(tmem + TM_O, pcol + ks * 8, tc::smem_desc_sw128(vhat + ks * 2048, BN * 128, 1024),
+                    tc::mma_ts(tmem + TM_O, pcol + ks * 8, vdesc + (uint64_t)((ks * 2048) >> 4),
                                IDESC_PV, (!first || ks > 0) ? 1u : 0u);
                 tc::mma_commit(B(B_PV_DONE + bb));
                 tc::mma_commit(B(B_V_EMPTY + bb));
@@ -497,11 +504,11 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
                     // chunks: the tensor pipe drained once per tile)
                     if (!tc::mbar_wait(B(B_K_FULL + b), use & 1, kWaitLimit)) { ok = false; break; }
                     tc::fence_after_sync();
-                    const uint32_t khat = sbase + SM_KHAT + b * HAT_BYTES;
+                    const uint64_t kdesc = kdesc0 + (uint64_t)((b * HAT_BYTES) >> 4);
 #pragma unroll
                     for (int ks = 0; ks < HD / 16; ++ks)
                         tc::mma_ts(tmem + TM_S0 + b * BN, tmem + TM_Q + ks * 8,
-                                   tc::smem_desc_sw128(khat + (ks >> 2) * (BN * 128) + (ks & 3) * 32, 16, 1024),
+                                   kdesc + (uint64_t)((((ks >> 2) * (BN * 128)) + (ks & 3) * 32) >> 4),
                                    IDESC_QK, ks > 0 ? 1u : 0u);
                     tc::mma_commit(B(B_S_FULL + b));
                     tc::mma_commit(B(B_K_EMPTY + b));
