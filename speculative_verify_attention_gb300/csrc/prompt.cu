@@ -16,6 +16,9 @@
 //   warps 6-15  dequantisers: int8 -> fp16 exactly (byte permute + magic-bias subtract), then
 //               times the block scale (one fp16 rounding), written to double-buffered
 //               128-byte-swizzled K^ and V^ tiles in shared memory.
+// With an fp16 pool (or the fp16 copy of the two-pass route) there is nothing to dequantise:
+// warp 0 loads the K tiles and warp 6 the V tiles straight into K^ / V^ by tensor copies, and
+// warps 7-15 idle.
 // Tensor memory (512 columns): Q as fp16 pairs (128), O fp32 (256), two S buffers (64 each)
 // whose first 32 columns take P as fp16 pairs after the softmax has read S.
 //   S = Q K^T : tcgen05.mma kind::f16, A = Q from TMEM, B = K^ (K-major), M=128 N=64 K=256
@@ -375,8 +378,12 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
     const uint32_t tmem = *tmem_slot;
     const int n_seg = *n_seg_slot;
 
-    if (warp == 0 && F16) {
-        // ---------------------------------------------------------------- producer (fp16 pool)
+    if ((warp == 0 || warp == kDeqWarp0) && F16) {
+        // ---------------------------------------------------------------- producers (fp16 pool)
+        // K copies from warp 0, V copies from the first (idle) dequantiser warp: a K slot frees
+        // when its QK completes, a V slot only when its PV does, and one thread issuing both
+        // held each K copy behind the previous tile's V slot (1-2 % at hd256)
+        const bool vprod = warp == kDeqWarp0;
         if (lane == 0) {
             constexpr uint32_t plane_bytes = (uint32_t)(HD / 64) * BN * 128;  // full boxes, past-the-end keys zero-filled
             int j = 0;
@@ -386,25 +393,20 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
                 for (int t = seg[si].t0; t < seg[si].t1; ++t, ++j) {
                     const int b = j & 1, use = j >> 1;
                     const int key0 = t * BN;
-                    // K^ of buffer b is free once the QK that read it two tiles ago has completed
-                    if (j >= 2 && !tc::mbar_wait(B(B_K_EMPTY + b), (use - 1) & 1, kWaitLimit)) { ok = false; break; }
-                    tc::mbar_arrive_expect_tx(B(B_K_FULL + b), plane_bytes);
+                    const int e_bar = vprod ? B_V_EMPTY : B_K_EMPTY, f_bar = vprod ? B_V_FULL : B_K_FULL;
+                    if (j >= 2 && !tc::mbar_wait(B(e_bar + b), (use - 1) & 1, kWaitLimit)) { ok = false; break; }
+                    tc::mbar_arrive_expect_tx(B(f_bar + b), plane_bytes);
+                    const uint32_t dst = sbase + (vprod ? SM_VHAT : SM_KHAT) + b * HAT_BYTES;
+                    const CUtensorMap* map = vprod ? &p.tmap_v : &p.tmap_k;
                     for (int a = 0; a < HD / 64; ++a)
-                        tma_load_3d(sbase + SM_KHAT + b * HAT_BYTES + a * (BN * 128), &p.tmap_k, 64 * a, key0, g.kvh,
-                                    B(B_K_FULL + b));
-                    if (j >= 2 && !tc::mbar_wait(B(B_V_EMPTY + b), (use - 1) & 1, kWaitLimit)) { ok = false; break; }
-                    tc::mbar_arrive_expect_tx(B(B_V_FULL + b), plane_bytes);
-                    for (int a = 0; a < HD / 64; ++a)
-                        tma_load_3d(sbase + SM_VHAT + b * HAT_BYTES + a * (BN * 128), &p.tmap_v, 64 * a, key0, g.kvh,
-                                    B(B_V_FULL + b));
+                        tma_load_3d(dst + a * (BN * 128), map, 64 * a, key0, g.kvh, B(f_bar + b));
                 }
             }
             if (!ok) flag_timeout();
             // never leave the block while a copy into its shared memory is in flight
-            for (int i = max(0, j - 2); i < j; ++i) {
-                if (!tc::mbar_wait(B(B_K_FULL + (i & 1)), (i >> 1) & 1, kWaitLimit)) flag_timeout();
-                if (!tc::mbar_wait(B(B_V_FULL + (i & 1)), (i >> 1) & 1, kWaitLimit)) flag_timeout();
-            }
+            const int f_bar = vprod ? B_V_FULL : B_K_FULL;
+            for (int i = max(0, j - 2); i < j; ++i)
+                if (!tc::mbar_wait(B(f_bar + (i & 1)), (i >> 1) & 1, kWaitLimit)) flag_timeout();
         }
     } else if (warp == 0) {
         // ---------------------------------------------------------------- producer
