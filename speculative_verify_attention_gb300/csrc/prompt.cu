@@ -58,8 +58,11 @@ constexpr int kMaxSegments = 8;
 // two S buffers of BN columns (384 + 2 x 64 at hd256, 256 + 2 x 128 at hd128)
 constexpr uint32_t TM_Q = 0, TM_O = 128, TM_NCOLS = 512;
 
-enum { B_ST_FULL = 0, B_ST_EMPTY = 2, B_K_FULL = 4, B_V_FULL = 6, B_K_EMPTY = 8, B_V_EMPTY = 10, B_S_FULL = 12,
-       B_P_FULL = 14, B_PV_DONE = 16, B_Q_READY = 18, B_COUNT = 19 };
+// A K^ buffer is free again when its QK has completed (B_S_FULL) and a V^ buffer when its PV has
+// (B_PV_DONE): those commits already mark the events, and every commit costs the one issuing
+// thread (two extra commits per tile measured 4-5 % slower at hd256).
+enum { B_ST_FULL = 0, B_ST_EMPTY = 2, B_K_FULL = 4, B_V_FULL = 6, B_S_FULL = 8, B_P_FULL = 10, B_PV_DONE = 12,
+       B_Q_READY = 14, B_COUNT = 15 };
 
 // Shared memory layout for head dim HD (bytes, 1024-aligned tiles):
 //   K^, V^ : 2 buffers each of [HD/64 atoms][64 keys][128 B], 128B-swizzled fp16 (K-major for
@@ -362,8 +365,6 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
             tc::mbar_init(B(B_ST_EMPTY + s), kDeqThreads / 32);  // one arrival per warp
             tc::mbar_init(B(B_K_FULL + s), F16 ? 1 : kDeqThreads / 32);  // F16: the producer's expect_tx
             tc::mbar_init(B(B_V_FULL + s), F16 ? 1 : kDeqThreads / 32);
-            tc::mbar_init(B(B_K_EMPTY + s), 1);
-            tc::mbar_init(B(B_V_EMPTY + s), 1);
             tc::mbar_init(B(B_S_FULL + s), 1);
             tc::mbar_init(B(B_P_FULL + s), 4);
             tc::mbar_init(B(B_PV_DONE + s), 1);
@@ -393,7 +394,9 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
                 for (int t = seg[si].t0; t < seg[si].t1; ++t, ++j) {
                     const int b = j & 1, use = j >> 1;
                     const int key0 = t * BN;
-                    const int e_bar = vprod ? B_V_EMPTY : B_K_EMPTY, f_bar = vprod ? B_V_FULL : B_K_FULL;
+                    // slot b frees when QK (K) or PV (V) of tile j - 2 completes; that commit cannot
+                    // have moved on a further phase, since tile j's MMAs need this very copy
+                    const int e_bar = vprod ? B_PV_DONE : B_S_FULL, f_bar = vprod ? B_V_FULL : B_K_FULL;
                     if (j >= 2 && !tc::mbar_wait(B(e_bar + b), (use - 1) & 1, kWaitLimit)) { ok = false; break; }
                     tc::mbar_arrive_expect_tx(B(f_bar + b), plane_bytes);
                     const uint32_t dst = sbase + (vprod ? SM_VHAT : SM_KHAT) + b * HAT_BYTES;
@@ -490,7 +493,6 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
                     tc::mma_ts(tmem + TM_O, pcol + ks * 8, vdesc + (uint64_t)((ks * 2048) >> 4),
                                IDESC_PV, (!first || ks > 0) ? 1u : 0u);
                 tc::mma_commit(B(B_PV_DONE + bb));
-                tc::mma_commit(B(B_V_EMPTY + bb));
                 pv_issued = jj + 1;
                 return true;
             };
@@ -513,7 +515,6 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
                                    kdesc + (uint64_t)((((ks >> 2) * (BN * 128)) + (ks & 3) * 32) >> 4),
                                    IDESC_QK, ks > 0 ? 1u : 0u);
                     tc::mma_commit(B(B_S_FULL + b));
-                    tc::mma_commit(B(B_K_EMPTY + b));
                     if (j > jfirst && !issue_pv(j - 1, j - 1 == jfirst)) { ok = false; break; }
                 }
                 if (ok && j > jfirst && !issue_pv(j - 1, j - 1 == jfirst)) ok = false;
@@ -776,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
                 const int soff = HD == 256 ? 0 : (int)(((int64_t)g.kvh * p.capacity + t * BN) & 1) * 8;
                 const uint16_t* k_sc = reinterpret_cast<const uint16_t*>(st + ST_KS + soff);
                 const uint16_t* v_sc = reinterpret_cast<const uint16_t*>(st + ST_VS + soff);
-                if (j >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait(B(B_K_EMPTY + s), (use - 1) & 1, kWaitLimit))) {
+                if (j >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait(B(B_S_FULL + s), (use - 1) & 1, kWaitLimit))) {
                     ok = false;
                     break;
                 }
@@ -784,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const __grid_c
                 tc::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(B(B_K_FULL + s));
-                if (j >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait(B(B_V_EMPTY + s), (use - 1) & 1, kWaitLimit))) {
+                if (j >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait(B(B_PV_DONE + s), (use - 1) & 1, kWaitLimit))) {
                     ok = false;
                     break;
                 }
