@@ -207,6 +207,36 @@ def test_prompt_k8v4_small_shapes(lib, hq, hkv, hd, L, nq, pos0, capacity):
     assert rel_err(got, ref) <= PROMPT_TOL
 
 
+@pytest.mark.parametrize("hq,hkv,L,nq,pos0,hd", [
+    (12, 1, 900, 342, 558, 256),
+    (32, 8, 1100, 1030, 70, 128),
+])
+def test_prompt_k8v4_two_pass_equals_the_f16_pool_of_the_dequantised_values(lib, hq, hkv, L, nq, pos0, hd):
+    """On the two-pass route the operands are fp16(code x scale) for K and fp16((nibble - 8) x
+    scale) for V, each rounded once: attn_prompt_f16 over a pool holding exactly those values
+    (computed here with numpy; element 2m of a V row is the low nibble of byte m) gives the same
+    output bit for bit."""
+    import torch
+
+    from speculative_verify_attention_gb300 import KVCacheF16, attn_prompt_f16, attn_prompt_k8v4
+    inp = workloads.random_small(1700 + hq + L, hq, hkv, hd, L, nq, q_dtype="f16")
+    gpu, _ = _pools(inp, junk=False)
+    f16 = KVCacheF16(hkv, hd, gpu.capacity)
+    kc = gpu.k_codes.cpu().numpy()[:, :L].astype(np.float16)
+    ks = np.repeat(gpu.k_scales.cpu().numpy()[:, :L], 32, axis=2)
+    f16.k[:, :L].copy_(torch.from_numpy(kc * ks))
+    vb = gpu.v_codes.cpu().numpy()[:, :L]
+    vq = np.stack([(vb & 15).astype(np.int16) - 8, (vb >> 4).astype(np.int16) - 8], axis=-1)
+    vs = np.repeat(gpu.v_scales.cpu().numpy()[:, :L], 32, axis=2)
+    f16.v[:, :L].copy_(torch.from_numpy(vq.reshape(hkv, L, hd).astype(np.float16) * vs))
+    q = torch.from_numpy(np.ascontiguousarray(inp.q)).cuda()
+    scale = 1.0 / float(np.sqrt(hd))
+    a = attn_prompt_k8v4(q, gpu, L, pos0, scale)
+    b = attn_prompt_f16(q, f16, L, pos0, scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
 def test_prompt_k8v4_full_workload_sampled(lib):
     from ._util import PROMPT_TOL
     from speculative_verify_attention_gb300 import kvq8_device_error
