@@ -979,13 +979,14 @@ int prompt_impl(const uint16_t* q, int n_q, int n_q_heads, const kvq8_cache* kv,
     if (two_pass) {
         uint16_t* k16 = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + pl.copy_off);
         uint16_t* v16 = k16 + (size_t)kv->n_kv_heads * pl.copy_keys * HD;
+        // the maps need only the addresses: encode them before launching anything
+        if (!encode_f16_plane(&pp.tmap_k, k16, HD, pl.copy_keys, kv->n_kv_heads, pl.copy_keys) ||
+            !encode_f16_plane(&pp.tmap_v, v16, HD, pl.copy_keys, kv->n_kv_heads, pl.copy_keys))
+            return KVQ8_ERR_CUDA;
         const DequantParams dp = {kv->k_codes, kv->k_scales, kv->v_codes, kv->v_scales, k16, v16,
                                   HD, pl.copy_keys, kv->capacity, kv->n_kv_heads};
         const int r0 = launch_dequant_planes(dp, pool == kPoolK8V4, s);
         if (r0 != KVQ8_OK) return r0;
-        if (!encode_f16_plane(&pp.tmap_k, k16, HD, pl.copy_keys, kv->n_kv_heads, pl.copy_keys) ||
-            !encode_f16_plane(&pp.tmap_v, v16, HD, pl.copy_keys, kv->n_kv_heads, pl.copy_keys))
-            return KVQ8_ERR_CUDA;
     } else if (pool == kPoolF16) {
         const uint16_t* kp = reinterpret_cast<const uint16_t*>(kv->k_codes);
         const uint16_t* vp = reinterpret_cast<const uint16_t*>(kv->v_codes);
