@@ -248,8 +248,15 @@ int attn_prompt_k8v4(const uint16_t* q, int n_q, int n_q_heads, const kvk8v4_cac
                      kvq8_stream_t stream);
 
 /*
- * attn_prompt_f16 -- attn_prompt_q8 over an fp16 pool (the same shapes, workspace from
- * attn_prompt_q8_workspace_bytes, precision bound and errors).  The K and V tiles are loaded
+ * Bytes of workspace attn_prompt_f16 needs for this shape: the partials only (an fp16 pool has
+ * no copy to make).  Never more than attn_prompt_q8_workspace_bytes for the same shape.
+ */
+size_t attn_prompt_f16_workspace_bytes(int n_q, int n_q_heads, int head_dim, int kv_len, int q_pos0,
+                                       int n_kv_heads);
+
+/*
+ * attn_prompt_f16 -- attn_prompt_q8 over an fp16 pool (the same shapes, precision bound and
+ * errors; workspace from attn_prompt_f16_workspace_bytes).  The K and V tiles are loaded
  * straight into the tensor-core operand layout by tensor copies over (head_dim, kv_len,
  * n_kv_heads), so keys at or past kv_len read as zeros; the caller's pool needs no padding.
  */
@@ -337,7 +344,8 @@ int attn_combine(const float* part_o, const float* part_ml, int n_split, int row
  * Bytes of workspace attn_prompt_q8 (and attn_prompt_k8v4 / attn_prompt_f16) needs for this
  * shape (on the current device): the partials, plus, for chunks of 24 or more 128-row tiles
  * per KV head, room for the fp16 copy of both planes (2 * n_kv_heads * min(kv_len, q_pos0 +
- * n_q) * head_dim * 2 bytes) that the two-pass route writes.  fp16 pools never use that room.
+ * n_q) * head_dim * 2 bytes) that the two-pass route writes.  fp16 pools never use that room
+ * (attn_prompt_f16_workspace_bytes gives their smaller size).
  */
 size_t attn_prompt_q8_workspace_bytes(int n_q, int n_q_heads, int head_dim, int kv_len, int q_pos0,
                                       int n_kv_heads);

@@ -6,7 +6,8 @@ generators used by the tests and the benchmark.
 """
 from .binding import (EXPORTED, KVCacheF16, KVCacheK8V4, KVCacheQ8, attn_prompt_k8v4, attn_verify_k8v4, kvk8v4_append,
                       kvk8v4_cache, KVQ8Error, PreparedAppendVerifyHost, attn_prompt_f16, attn_verify_f16,
-                      attn_verify_f16_workspace_bytes, kvf16_append, kvf16_cache, argmax_rows_top_prob, attn_combine, attn_prompt_q8, attn_prompt_q8_workspace_bytes, attn_verify_q8,
+                      attn_verify_f16_workspace_bytes, kvf16_append, kvf16_cache, argmax_rows_top_prob, attn_combine, attn_prompt_q8, attn_prompt_q8_workspace_bytes,
+                      attn_prompt_f16_workspace_bytes, attn_verify_q8,
                       attn_verify_append_q8, attn_verify_append_q8_workspace_bytes, attn_verify_q8_partials,
                       attn_verify_q8_partials_count, attn_verify_append_q8_host,
                       attn_verify_append_q8_host_scratch_bytes,
@@ -15,7 +16,8 @@ from .binding import (EXPORTED, KVCacheF16, KVCacheK8V4, KVCacheQ8, attn_prompt_
 
 __all__ = ["EXPORTED", "KVCacheF16", "KVCacheK8V4", "KVCacheQ8", "attn_prompt_k8v4", "attn_verify_k8v4", "kvk8v4_append",
            "kvk8v4_cache", "KVQ8Error", "PreparedAppendVerifyHost", "attn_prompt_f16", "attn_verify_f16",
-           "attn_verify_f16_workspace_bytes", "kvf16_append", "kvf16_cache", "argmax_rows_top_prob", "attn_combine", "attn_prompt_q8", "attn_prompt_q8_workspace_bytes", "attn_verify_q8",
+           "attn_verify_f16_workspace_bytes", "kvf16_append", "kvf16_cache", "argmax_rows_top_prob", "attn_combine", "attn_prompt_q8", "attn_prompt_q8_workspace_bytes",
+           "attn_prompt_f16_workspace_bytes", "attn_verify_q8",
            "attn_verify_append_q8", "attn_verify_append_q8_workspace_bytes", "attn_verify_q8_partials",
            "attn_verify_q8_partials_count", "attn_verify_append_q8_host",
            "attn_verify_append_q8_host_scratch_bytes",

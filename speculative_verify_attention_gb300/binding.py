@@ -31,7 +31,7 @@ EXPORTED = ("kvq8_quantize", "kvq8_append", "attn_verify_q8_workspace_bytes", "a
             "attn_verify_append_q8_workspace_bytes", "attn_verify_append_q8", "attn_verify_q8_partials_count",
             "attn_verify_q8_partials", "attn_verify_append_q8_host_scratch_bytes", "attn_verify_append_q8_host",
             "kvf16_append", "attn_verify_f16_workspace_bytes", "attn_verify_f16", "kvk8v4_append", "attn_verify_k8v4",
-            "attn_prompt_k8v4", "attn_prompt_f16", "attn_combine",
+            "attn_prompt_k8v4", "attn_prompt_f16_workspace_bytes", "attn_prompt_f16", "attn_combine",
             "attn_prompt_q8_workspace_bytes", "attn_prompt_q8", "attn_verify_q8_noalloc", "kvq8_device_error", "kvq8_status_str",
             "argmax_rows_top_prob_workspace_bytes", "argmax_rows_top_prob", "kvq8_selftest_convert",
             "kvq8_selftest_wait_timeout")
@@ -127,6 +127,8 @@ def load_library():
         lib.attn_combine.restype = i32
         lib.attn_prompt_q8_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.attn_prompt_q8_workspace_bytes.restype = sz
+        lib.attn_prompt_f16_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.attn_prompt_f16_workspace_bytes.restype = sz
         lib.attn_prompt_q8.argtypes = [vp, i32, i32, cp, i32, i32, f32, vp, vp, sz, vp]
         lib.attn_prompt_q8.restype = i32
         lib.attn_verify_q8_noalloc.argtypes = [vp, i32, i32, cp, i32, i32, f32, vp, i32, vp]
@@ -330,7 +332,7 @@ def attn_prompt_f16(q: torch.Tensor, cache: KVCacheF16, kv_len: int, q_pos0: int
         out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
     _need(out, "out", torch.float32)
     if workspace is None:
-        nbytes = attn_prompt_q8_workspace_bytes(n_q, n_q_heads, head_dim, kv_len, q_pos0, cache.n_kv_heads)
+        nbytes = attn_prompt_f16_workspace_bytes(n_q, n_q_heads, head_dim, kv_len, q_pos0, cache.n_kv_heads)
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
     st = load_library().attn_prompt_f16(_ptr(q), n_q, n_q_heads, ctypes.byref(cache.struct()), int(kv_len),
                                         int(q_pos0), float(softmax_scale), _ptr(out), _ptr(workspace),
@@ -597,6 +599,11 @@ def attn_combine(part_o: torch.Tensor, part_ml: torch.Tensor, out: torch.Tensor 
 def attn_prompt_q8_workspace_bytes(n_q: int, n_q_heads: int, head_dim: int, kv_len: int, q_pos0: int,
                                    n_kv_heads: int) -> int:
     return int(load_library().attn_prompt_q8_workspace_bytes(n_q, n_q_heads, head_dim, kv_len, q_pos0, n_kv_heads))
+
+
+def attn_prompt_f16_workspace_bytes(n_q: int, n_q_heads: int, head_dim: int, kv_len: int, q_pos0: int,
+                                    n_kv_heads: int) -> int:
+    return int(load_library().attn_prompt_f16_workspace_bytes(n_q, n_q_heads, head_dim, kv_len, q_pos0, n_kv_heads))
 
 
 def attn_prompt_q8(q: torch.Tensor, cache: KVCacheQ8, kv_len: int, q_pos0: int, softmax_scale: float,

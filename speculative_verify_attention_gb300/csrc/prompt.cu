@@ -816,7 +816,7 @@ struct PromptPlan {
     // two-pass route: the fp16 copy of keys < copy_keys of both planes at byte copy_off of the
     // workspace (copy_keys = 0: the one-pass kernel dequantises in shared memory)
     int copy_keys;
-    size_t copy_off, ws_bytes;
+    size_t part_bytes, copy_off, ws_bytes;  // partials alone; the copy's offset; the whole workspace
 };
 
 // Row tiles per KV head from which a Q8_0 or K8V4 chunk takes the two-pass route.  The one-pass
@@ -866,6 +866,7 @@ int prompt_plan(int n_q, int n_q_heads, int head_dim, int kv_len, int q_pos0, in
     const size_t rows_out = (size_t)n_q * n_q_heads;
     const size_t o_bytes = (size_t)parts * rows_out * head_dim * sizeof(float);
     const size_t part_bytes = ((o_bytes + 255) / 256) * 256 + (size_t)parts * rows_out * 2 * sizeof(float);
+    pl->part_bytes = part_bytes;
     // the highest key any row sees is q_pos0 + n_q - 1 (or the context's end)
     const long long last = (long long)q_pos0 + n_q;
     pl->copy_keys = pl->n_mtiles >= kTwoPassMinMtiles ? (int)(last < kv_len ? last : kv_len) : 0;
@@ -928,6 +929,13 @@ extern "C" size_t attn_prompt_q8_workspace_bytes(int n_q, int n_q_heads, int hea
     return pl.ws_bytes;
 }
 
+extern "C" size_t attn_prompt_f16_workspace_bytes(int n_q, int n_q_heads, int head_dim, int kv_len, int q_pos0,
+                                                  int n_kv_heads) {
+    kvq8::PromptPlan pl;
+    if (kvq8::prompt_plan(n_q, n_q_heads, head_dim, kv_len, q_pos0, n_kv_heads, &pl) != KVQ8_OK) return 0;
+    return pl.part_bytes;
+}
+
 namespace kvq8 {
 namespace {
 
@@ -947,7 +955,8 @@ int prompt_impl(const uint16_t* q, int n_q, int n_q_heads, const kvq8_cache* kv,
     if (!aligned16(q) || !aligned16(out) || !aligned16(kv->k_codes) || !aligned16(kv->v_codes) ||
         (pool != kPoolF16 && (!aligned16(kv->k_scales) || !aligned16(kv->v_scales))))
         return KVQ8_ERR_MISALIGNED;
-    if (!workspace || workspace_bytes < pl.ws_bytes) return KVQ8_ERR_WORKSPACE;
+    // an fp16 pool needs the partials only; the fp16 copy is for the dequantising pools
+    if (!workspace || workspace_bytes < (pool == kPoolF16 ? pl.part_bytes : pl.ws_bytes)) return KVQ8_ERR_WORKSPACE;
     if (!aligned16(workspace)) return KVQ8_ERR_MISALIGNED;
     const int HD = kv->head_dim;
     const size_t rows_out = (size_t)n_q * n_q_heads;

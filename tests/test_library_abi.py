@@ -82,3 +82,23 @@ def test_prompt_workspace_adds_the_fp16_copy_from_24_row_tiles():
         part = ws - copy
         assert part % 256 == 0 and part > 0, (hq, nq)
         assert any(_partials_bytes_match(part - pad, rows_out, hd) for pad in range(0, 256, 8)), (hq, nq)
+
+
+def test_prompt_f16_workspace_is_the_partials_alone():
+    """attn_prompt_f16_workspace_bytes: an fp16 pool makes no copy, so its workspace is the
+    partials part of attn_prompt_q8_workspace_bytes: equal to it below 24 row tiles per KV head,
+    that part rounded to 256 bytes (the copy's offset) plus the copy from 24 on."""
+    lib = ctypes.CDLL(build.build())
+    for fn in (lib.attn_prompt_q8_workspace_bytes, lib.attn_prompt_f16_workspace_bytes):
+        fn.restype = ctypes.c_size_t
+    for hq, hkv, hd, kv_len, nq, pos0 in ((12, 1, 256, 32768, 245, 32523), (12, 1, 256, 32768, 2048, 30720),
+                                          (32, 8, 128, 32768, 2048, 30720), (32, 8, 128, 8192, 736, 7456)):
+        q8 = lib.attn_prompt_q8_workspace_bytes(nq, hq, hd, kv_len, pos0, hkv)
+        f16 = lib.attn_prompt_f16_workspace_bytes(nq, hq, hd, kv_len, pos0, hkv)
+        mtiles = -(-nq * (hq // hkv) // 128)
+        if mtiles < 24:
+            assert f16 == q8, (hq, nq)
+        else:
+            copy = 2 * hkv * min(kv_len, pos0 + nq) * hd * 2
+            assert q8 == -(-f16 // 256) * 256 + copy, (hq, nq)
+            assert _partials_bytes_match(f16, nq * hq, hd), (hq, nq)
