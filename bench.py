@@ -599,8 +599,8 @@ def prompt_bench(args, dev, fp16_peak, w=None, pool="q8"):
     import torch
 
     from speculative_verify_attention_gb300 import (KVCacheF16, KVCacheK8V4, KVCacheQ8, KVQ8Error, attn_prompt_f16,
-                                                    attn_prompt_k8v4, attn_prompt_q8, attn_prompt_q8_workspace_bytes,
-                                                    workloads)
+                                                    attn_prompt_f16_workspace_bytes, attn_prompt_k8v4, attn_prompt_q8,
+                                                    attn_prompt_q8_workspace_bytes, workloads)
     w = w or workloads.PROMPT
     inp = workloads.make_inputs(w)
     pool_cls = {"q8": KVCacheQ8, "k8v4": KVCacheK8V4, "f16": KVCacheF16}[pool]
@@ -609,8 +609,14 @@ def prompt_bench(args, dev, fp16_peak, w=None, pool="q8"):
     attn_prompt_q8 = {"q8": attn_prompt_q8, "k8v4": attn_prompt_k8v4, "f16": attn_prompt_f16}[pool]  # same call shape
     q = torch.from_numpy(inp.q).to(dev)
     out = torch.empty(q.shape, dtype=torch.float32, device=dev)
-    ws = torch.empty(attn_prompt_q8_workspace_bytes(w.n_q, w.n_q_heads, w.head_dim, w.kv_len, w.q_pos0,
-                                                    w.n_kv_heads), dtype=torch.uint8, device=dev)
+    ws_bytes = attn_prompt_q8_workspace_bytes(w.n_q, w.n_q_heads, w.head_dim, w.kv_len, w.q_pos0, w.n_kv_heads)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    # the library's own sizes tell the route: only the two-pass route needs room for an fp16 copy
+    two_pass = pool != "f16" and ws_bytes > attn_prompt_f16_workspace_bytes(
+        w.n_q, w.n_q_heads, w.head_dim, w.kv_len, w.q_pos0, w.n_kv_heads)
+    route = ("fp16 tiles by tensor copy" if pool == "f16" else
+             "two-pass: one dequantising pass into an fp16 copy in the workspace, then the tensor-copy kernel"
+             if two_pass else "one-pass: tiles dequantised in shared memory")
     try:
         attn_prompt_q8(q, c, w.kv_len, w.q_pos0, w.softmax_scale, out=out, workspace=ws)
     except KVQ8Error as e:
@@ -633,7 +639,8 @@ def prompt_bench(args, dev, fp16_peak, w=None, pool="q8"):
             "frac": tf / fp16_peak, "peak_source": "MEASURED_PEAKS.json bf16_tflops (cuBLAS bf16, burst); fp16 "
             "and bf16 share one dense tensor-core rate", "dtype": "fp16 operands, single pass (q, K, P, V "
             "each one fp16 value, not split hi+lo), f32 accumulate",
-            "flops": w.causal_flops(), "calls_timed": n, "l2": "flushed (256 MiB write) before every call"}
+            "flops": w.causal_flops(), "calls_timed": n, "l2": "flushed (256 MiB write) before every call",
+            "route": route, "workspace_bytes": ws_bytes}
 
 
 def _ring_for(w, dev, ring_l2, inp=None):
